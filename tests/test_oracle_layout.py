@@ -1,0 +1,157 @@
+"""Pins for the oracle's bit packing, tile layouts and byte counts."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import cache, layout
+from conftest import golden
+
+
+def _pack_bigint(codes, bits):
+    """Brute force: the stream as one little-endian integer sum(code_i << bits*i)."""
+    v = 0
+    for i, c in enumerate(codes):
+        v |= int(c) << (bits * i)
+    n = (len(codes) * bits + 7) // 8
+    return np.frombuffer(v.to_bytes(n, "little"), dtype=np.uint8)
+
+
+def test_hand_worked_examples():
+    for case in golden("pack_examples.json")["cases"]:
+        got = layout.pack_bits(np.array(case["codes"], np.uint8), case["bits"])
+        assert got.tobytes().hex() == case["bytes_hex"], case
+        back = layout.unpack_bits(got, len(case["codes"]), case["bits"])
+        assert back.tolist() == case["codes"]
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("n", [1, 7, 32, 100, 129])
+def test_round_trip_and_bigint(bits, n):
+    codes = synth.random_codes(n * 10 + bits, n, bits)
+    packed = layout.pack_bits(codes, bits)
+    assert packed.size == layout.packed_size(n, bits)
+    assert np.array_equal(packed, _pack_bigint(codes, bits))
+    assert np.array_equal(layout.unpack_bits(packed, n, bits), codes)
+    rows = np.stack([codes] * 3)
+    if (n * bits) % 8 == 0:
+        pr = layout.pack_rows(rows, bits)
+        assert np.array_equal(pr[1], packed)
+        assert np.array_equal(layout.unpack_rows(pr, n, bits), rows)
+
+
+def test_three_bit_32_values_fill_12_bytes():
+    assert layout.packed_size(32, 3) == 12
+    assert layout.pack_bits(np.full(32, 7, np.uint8), 3).tolist() == [255] * 12
+
+
+def test_plane_words_brute_force():
+    bits = synth.random_codes(1, 3 * 128, 1).reshape(3, 128)
+    words = layout.bits_to_plane_words(bits)
+    for r in range(3):
+        for w in range(4):
+            want = 0
+            for j in range(16):
+                for e in range(2):
+                    want |= int(bits[r, 32 * w + 2 * j + e]) << (16 * e + j)
+            assert int(words[r, w]) == want
+    assert np.array_equal(layout.plane_words_to_bits(words), bits)
+
+
+def test_vq_words_brute_force():
+    codes = synth.random_codes(2, 16 * 64, 2).reshape(16, 64)
+    words = layout.codes_to_vq_words(codes)
+    for i in range(64):
+        want = 0
+        for t in range(16):
+            j, e = divmod(t, 2)
+            want |= int(codes[t, i]) << (16 * e + 2 * j)
+        assert int(words[i]) == want
+    assert np.array_equal(layout.vq_words_to_codes(words), codes)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_main_tile_round_trip(d):
+    g = np.random.default_rng(d)
+    f = {
+        "idx": g.integers(0, 4, (3, 16, d), dtype=np.uint8),
+        "sigma": g.integers(0, 2, (3, 16, d), dtype=np.uint8),
+        "vq": g.integers(0, 4, (3, 16, d), dtype=np.uint8),
+        "vs": g.standard_normal((3, 16, d // 32)).astype(np.float16),
+        "vmn": g.standard_normal((3, 16, d // 32)).astype(np.float16),
+        "n_k": g.standard_normal((3, 16)).astype(np.float16),
+        "n_r": g.standard_normal((3, 16)).astype(np.float16),
+    }
+    t = layout.pack_main_tiles(f["idx"], f["sigma"], f["vq"], f["vs"], f["vmn"], f["n_k"], f["n_r"])
+    assert t.shape == (3, layout.main_tile_bytes(d))
+    back = layout.unpack_main_tiles(t, d)
+    for k, v in f.items():
+        assert np.array_equal(back[k].view(np.uint8), v.view(np.uint8)), k
+    # field placement: norms at the documented offsets
+    assert np.array_equal(t[1, 12 * d:12 * d + 32].view("<f2"), f["n_k"][1])
+    assert np.array_equal(t[2, 12 * d + 32:].view("<f2"), f["n_r"][2])
+    # KH word 0 of token 0 built from idx >> 1 in even/odd split order
+    w0 = int(t[0, 0:4].view("<u4")[0])
+    want = 0
+    for j in range(16):
+        for e in range(2):
+            want |= int(f["idx"][0, 0, 2 * j + e] >> 1) << (16 * e + j)
+    assert w0 == want
+
+
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+def test_alt_tile_round_trip(d):
+    g = np.random.default_rng(d + 1)
+    f = {
+        "kq": g.integers(0, 256, (2, 16, d), dtype=np.uint8),
+        "ks": g.standard_normal((2, 16, d // 32)).astype(np.float16),
+        "kmn": g.standard_normal((2, 16, d // 32)).astype(np.float16),
+        "vidx": g.integers(0, 8, (2, 16, d), dtype=np.uint8),
+        "n_v": g.standard_normal((2, 16)).astype(np.float16),
+    }
+    t = layout.pack_alt_tiles(f["kq"], f["ks"], f["kmn"], f["vidx"], f["n_v"])
+    assert t.shape == (2, layout.alt_tile_bytes(d))
+    back = layout.unpack_alt_tiles(t, d)
+    for k, v in f.items():
+        assert np.array_equal(back[k].view(np.uint8), v.view(np.uint8)), k
+    row = t[1, 18 * d + 5 * (3 * d // 8):18 * d + 6 * (3 * d // 8)]
+    assert np.array_equal(row, _pack_bigint(f["vidx"][1, 5], 3))
+
+
+def test_bytes_per_token_closed_form():
+    assert layout.main_bytes_per_token_head(128) == 100
+    # 32 + 16 bytes of key bits, 32 bytes of value codes, 4 groups x 4 bytes, 2 norms
+    assert 128 * 3 // 8 + 128 * 2 // 8 + 4 * 4 + 2 + 2 == 100
+    for d in (64, 128, 256, 512):
+        assert layout.alt_bytes_per_token_head(d) == 1.5 * d + 2
+        assert layout.main_tile_bytes(d) % 16 == 0 and layout.alt_tile_bytes(d) % 16 == 0
+
+
+def test_memory_table_of_the_benchmark_page():
+    """100 B per token-head plus a 128-token fp16 ring reproduces the printed table."""
+    for row in golden("kv_memory_table.json")["rows"]:
+        n = row["tokens"]
+        n_c, n_buf = cache.ring_split(n)
+        assert (n_c, n_buf) == (n - 128, 128)
+        fp16 = n * 512
+        tq = n_c * layout.main_bytes_per_token_head(128) + n_buf * 512
+        assert round(fp16 / tq, 1) == row["ratio_printed"]
+        assert round(row["fp16_mb"] * tq / fp16) == row["tq_mb"]
+
+
+def test_vllm_metal_compression_table_reading():
+    """K = b*d/8 + 16 B, V = v*d/8 + 8 B per vector reproduces every printed ratio."""
+    d = 128
+    for row in golden("vllm_metal_compression.json")["rows"]:
+        per = row["k_bits"] * d / 8 + 16 + row["v_bits"] * d / 8 + 8
+        assert round(2 * d * 2 / per, 2) == row["ratio_printed"]
+    # this project's alternate layout (int8 K + 3-bit V) is tighter by 6 B
+    assert layout.alt_bytes_per_token_head(128) == 194
+
+
+def test_ring_split():
+    assert cache.ring_split(0) == (0, 0)
+    assert cache.ring_split(1) == (0, 1)
+    assert cache.ring_split(128) == (0, 128)
+    assert cache.ring_split(129) == (128, 1)
+    assert cache.ring_split(1024) == (896, 128)
+    assert cache.ring_split(32768) == (32640, 128)
