@@ -1,0 +1,515 @@
+#!/usr/bin/env python3
+"""Benchmark: compressed-KV decode attention GB/s and encode tokens/s on GB300.
+
+One *step* is one decode step of every layer of the workload: per layer the
+new token's k, v are appended to the exact ring (flushing 128 tokens into
+the compressed pages when the ring is full) and decode attention runs for
+all query heads over the compressed history plus the ring.  ``value`` is the
+decode-attention throughput in GB/s of algorithmic bytes: compressed records
+read (100 B per token-head in the main layout, 1.5 d + 2 B in the alternate
+one) + fp16 ring tokens (4 d B per token-head) + fp16 queries + fp32 outputs.
+
+Workloads (synthetic inputs from ``synth``; no weights or datasets):
+  qwen3-0.6b-32k   28 layers, 16 q / 4 KV heads, d 128, batch 1, 32768-token prefix
+                   compressed in 128-token flushes, then decode steps (default)
+  tiny-1k          1 layer, 16 / 4, d 128, batch 1, 1024 tokens
+  qwen2.5-7b-b8    28 layers, 28 / 4, d 128, batch 8, 32768 tokens each, shuffled pages
+  alt-d{64,128,256,512}  alternate layout, 8 / 8, batch 4, 65536 tokens, no ring
+  qwen2.5-32b-ragged     1 of 64 layers, 40 / 8, d 128, batch 16, lengths U[1024, 131072]
+
+Launch: ``python bench.py [--gpus N --steps K --warmup W --workload NAME]``;
+for N > 1 under torchrun, each rank runs the same per-GPU workload (weak
+scaling, no data-path collective) and rank 0 prints one JSON line.
+``--impl reference`` times the CPU oracle instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "decode-attn compressed-KV GB/s (% of GB300 HBM peak); encode tokens/s"
+
+WORKLOADS = {
+    "tiny-1k": dict(layout="main", layers=1, batch=1, hq=16, hkv=4, d=128, ctx=1024, shuffled=False, seed=0),
+    "qwen3-0.6b-32k": dict(layout="main", layers=28, batch=1, hq=16, hkv=4, d=128, ctx=32768, shuffled=False, seed=0),
+    "qwen2.5-7b-b8": dict(layout="main", layers=28, batch=8, hq=28, hkv=4, d=128, ctx=32768, shuffled=True, seed=0),
+    "alt-d64": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=64, ctx=65536, shuffled=False, seed=0),
+    "alt-d128": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=128, ctx=65536, shuffled=False, seed=0),
+    "alt-d256": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=256, ctx=65536, shuffled=False, seed=0),
+    "alt-d512": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=512, ctx=65536, shuffled=False, seed=0),
+    "qwen2.5-32b-ragged": dict(layout="main", layers=1, batch=16, hq=40, hkv=8, d=128, ctx=None, lo=1024, hi=131072,
+                               shuffled=True, seed=7),
+}
+DEFAULT_WORKLOAD = "qwen3-0.6b-32k"
+
+
+# ---------------------------------------------------------------------- helpers
+def ring_split(length: int):
+    if length <= 0:
+        return 0, 0
+    n_c = 128 * ((length - 1) // 128)
+    return n_c, length - n_c
+
+
+def record_bytes(w) -> int:
+    d = w["d"]
+    return (3 * d) // 4 + 4 if w["layout"] == "main" else (3 * d) // 2 + 2
+
+
+def step_bytes(w, lengths_after_append):
+    """Algorithmic bytes one layer's decode attention moves at the given lengths."""
+    rb, d = record_bytes(w), w["d"]
+    tot = 0
+    for L in lengths_after_append:
+        if w["layout"] == "main":
+            nc, nb = ring_split(L)
+        else:
+            nc, nb = L, 0
+        tot += w["hkv"] * (nc * rb + nb * 4 * d)
+    tot += w["batch"] * w["hq"] * d * (2 + 4)
+    return tot
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_index: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x for x in vis.split(",") if x.strip()]
+        self.gpu = ids[local_index].strip() if local_index < len(ids) else str(local_index)
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- GPU arm
+class Layer:
+    """One layer's context, pool, ring and block table on the device."""
+
+    def __init__(self, tq, torch, w, layer_idx, lengths, max_len, bt_np):
+        lay = tq.TQ_LAYOUT_MAIN if w["layout"] == "main" else tq.TQ_LAYOUT_ALT
+        self.ctx = tq.Context(lay, w["d"], w["hq"], w["hkv"], w["seed"] + layer_idx)
+        self.max_blocks = bt_np.shape[1]
+        self.bt = torch.from_numpy(bt_np).cuda()
+        nblk = bt_np.shape[0] * bt_np.shape[1]
+        self.pool = torch.empty((nblk, w["hkv"], self.ctx.page_bytes), dtype=torch.uint8, device="cuda")
+        self.ring_k = torch.zeros((w["batch"], w["hkv"], 128, w["d"]), dtype=torch.float16, device="cuda")
+        self.ring_v = torch.zeros_like(self.ring_k)
+        self.out = torch.empty((w["batch"], w["hq"], w["d"]), dtype=torch.float32, device="cuda")
+
+
+def build_gpu_state(tq, torch, w, steps_total):
+    bsz, hkv, d = w["batch"], w["hkv"], w["d"]
+    if w["ctx"] is None:
+        lengths = [int(x) for x in synth.ragged_lengths(w["seed"], bsz, w["lo"], w["hi"])]
+    else:
+        lengths = [w["ctx"]] * bsz
+    max_len = max(lengths) + steps_total + 128 + 64  # room for the end-to-end steps
+    max_blocks = (max_len + 15) // 16
+    bt_np = synth.block_table(w["seed"], bsz, max_blocks, w["shuffled"])
+    # one shared synthetic K/V prefix (layer 0 recipe), reused by every layer with its own tables
+    kv_len = ((max(lengths) + 15) // 16) * 16
+    if w["layout"] == "main":
+        k_np, v_np = synth.kv_main(w["seed"], 1, hkv, kv_len, d)
+    else:
+        k_np, v_np = synth.kv_alt(w["seed"], 1, hkv, kv_len, d)
+    k1 = torch.from_numpy(k_np).cuda()
+    v1 = torch.from_numpy(v_np).cuda()
+    layers = [Layer(tq, torch, w, li, lengths, max_len, bt_np) for li in range(w["layers"])]
+    return lengths, k1, v1, layers
+
+
+def encode_prefix(tq, torch, w, lengths, k1, v1, layers, timed=True):
+    """Compress every sequence's prefix (page-aligned part) and fill the rings; returns (ms, tokens)."""
+    bsz = w["batch"]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_tok_total = 0
+    torch.cuda.synchronize()
+    ev0.record()
+    start = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for lay in layers:
+        for b in range(bsz):
+            L = lengths[b]
+            nc, nb = ring_split(L) if w["layout"] == "main" else (L, 0)
+            if nc:
+                lay.ctx.encode_flush(k1, v1, start, lay.bt[b:b + 1], lay.pool, n_tokens=nc)
+                n_tok_total += nc
+            if nb:
+                lay.ring_k[b, :, :nb] = k1[0, :, nc:nc + nb]
+                lay.ring_v[b, :, :nb] = v1[0, :, nc:nc + nb]
+    ev1.record()
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1), n_tok_total
+
+
+def encode_throughput(tq, torch, w, layers, k1, v1, reps=3):
+    """Time tq_encode_flush alone on a 32768-token (or shorter) page-aligned prefix per layer."""
+    n = min(k1.shape[2], 32768) // 128 * 128
+    kb, vb = k1[:, :, :n].contiguous(), v1[:, :, :n].contiguous()
+    start = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scratch = torch.empty((n // 16 + 1, w["hkv"], layers[0].ctx.page_bytes), dtype=torch.uint8, device="cuda")
+    bt = torch.arange(n // 16 + 1, dtype=torch.int32, device="cuda")[None, :]
+    ctx = layers[0].ctx
+    for _ in range(2):
+        ctx.encode_flush(kb, vb, start, bt, scratch)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ctx.encode_flush(kb, vb, start, bt, scratch)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    toks = n
+    return {"tokens_per_s": toks / (ms * 1e-3), "token_heads_per_s": toks * w["hkv"] / (ms * 1e-3),
+            "ms_per_call": ms, "tokens_per_call": toks}
+
+
+def run_gpu(args, w, rank, world):
+    import torch
+
+    from kv_cache_quantization_tq_gb300.build import build
+
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        torch.distributed.barrier()
+    import kv_cache_quantization_tq_gb300 as tq
+
+    steps_total = args.warmup + args.steps
+    lengths, k1, v1, layers = build_gpu_state(tq, torch, w, steps_total)
+    encode_prefix(tq, torch, w, lengths, k1, v1, layers)
+    enc = encode_throughput(tq, torch, w, layers, k1, v1)
+    bsz, hq, hkv, d = w["batch"], w["hq"], w["hkv"], w["d"]
+    main = w["layout"] == "main"
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234 + rank)
+    # per-step device inputs, prepared before timing
+    q_all = torch.randn((steps_total, w["layers"], bsz, hq, d), generator=g, device="cuda").half()
+    kn_all = torch.randn((steps_total, w["layers"], bsz, hkv, d), generator=g, device="cuda").half()
+    vn_all = torch.randn((steps_total, w["layers"], bsz, hkv, d), generator=g, device="cuda").half()
+    pos_np = np.array([[L + s for L in lengths] for s in range(steps_total)], np.int32)
+    after = pos_np + 1
+    if main:
+        nc_np = (128 * ((after - 1) // 128)).astype(np.int32)
+        nb_np = (after - nc_np).astype(np.int32)
+    else:
+        nc_np = np.array([[L for L in lengths] for _ in range(steps_total)], np.int32)
+        nb_np = np.zeros_like(nc_np)
+    pos_d = torch.from_numpy(pos_np).cuda()
+    nc_d = torch.from_numpy(nc_np).cuda()
+    nb_d = torch.from_numpy(nb_np).cuda()
+    max_ctx = int(((nc_np.max() + 15) // 16) * 16)
+    ws = torch.empty(layers[0].ctx.workspace_size(bsz, max_ctx), dtype=torch.uint8, device="cuda")
+    bytes_per_step = [w["layers"] * step_bytes(w, after[s] if main else nc_np[s]) for s in range(steps_total)]
+
+    def step(s):
+        for li, lay in enumerate(layers):
+            if main:
+                lay.ctx.append_token(kn_all[s, li], vn_all[s, li], pos_d[s], lay.ring_k, lay.ring_v, lay.bt, lay.pool)
+            lay.ctx.decode_attention(q_all[s, li], lay.pool, lay.bt, nc_d[s], lay.ring_k if main else None,
+                                     lay.ring_v if main else None, nb_d[s] if main else None, max_ctx, lay.out, ws)
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    launches0 = sum(l.ctx.launch_count for l in layers)
+    for lay in layers:
+        lay.ctx.profile_begin()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        e0.record()
+        for s in range(args.warmup, steps_total):
+            step(s)
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    prof = [lay.ctx.profile_end() for lay in layers]
+    launches = sum(l.ctx.launch_count for l in layers) - launches0
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    timed_bytes = sum(bytes_per_step[args.warmup:])
+    value = timed_bytes * world / (ms * 1e-3) / 1e9
+
+    # dominant kernel: the fused decode kernel, timed by the library's CUDA events
+    dec_ms = sum(p["decode_ms"] for p in prof)
+    dec_n = sum(p["decode_launches"] for p in prof)
+    peak, peak_kind = measured_peaks()
+    per_launch_bytes = timed_bytes / max(dec_n, 1)
+    achieved = per_launch_bytes / (dec_ms / max(dec_n, 1) * 1e-3) / 1e9 if dec_n else None
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak if achieved else None, "traffic": None,
+                "kernel": "decode_main_kernel" if main else "decode_alt_kernel", "peak_source": peak_kind,
+                "launches": dec_n, "avg_launch_us": dec_ms / max(dec_n, 1) * 1e3,
+                "merge_us_per_launch": sum(p["merge_ms"] for p in prof) / max(dec_n, 1) * 1e3}
+
+    # end to end through the same C ABI with host buffers (pinned), copies inside the timed region
+    e2e = run_e2e(torch, w, layers, lengths, args, main, max_ctx, ws)
+    return {
+        "value": value, "ms_per_step": ms / args.steps, "roofline": roofline, "encode": enc, "e2e": e2e,
+        "gpu_launches": int(launches), "clocks": clk.summary(), "lengths": lengths,
+    }
+
+
+def run_e2e(torch, w, layers, lengths, args, main, max_ctx, ws):
+    """Same decode step, inputs copied from pinned host memory and outputs read back every step."""
+    bsz, hq, hkv, d, nl = w["batch"], w["hq"], w["hkv"], w["d"], w["layers"]
+    steps = max(3, min(args.steps, 16))
+    base = [L + args.warmup + args.steps for L in lengths]
+    rng = np.random.default_rng(5)
+    q_h = torch.from_numpy(rng.standard_normal((steps, nl, bsz, hq, d)).astype(np.float16)).pin_memory()
+    k_h = torch.from_numpy(rng.standard_normal((steps, nl, bsz, hkv, d)).astype(np.float16)).pin_memory()
+    v_h = torch.from_numpy(rng.standard_normal((steps, nl, bsz, hkv, d)).astype(np.float16)).pin_memory()
+    out_h = torch.empty((steps, nl, bsz, hq, d), dtype=torch.float32).pin_memory()
+    meta = []
+    for s in range(steps):
+        pos = np.array([b + s for b in base], np.int32)
+        after = pos + 1
+        nc = (128 * ((after - 1) // 128)).astype(np.int32) if main else np.array(lengths, np.int32)
+        nb = (after - nc).astype(np.int32) if main else np.zeros(bsz, np.int32)
+        meta.append((torch.from_numpy(pos).pin_memory(), torch.from_numpy(nc).pin_memory(),
+                     torch.from_numpy(nb).pin_memory(), after if main else nc))
+    q_d = torch.empty((nl, bsz, hq, d), dtype=torch.float16, device="cuda")
+    k_d = torch.empty((nl, bsz, hkv, d), dtype=torch.float16, device="cuda")
+    v_d = torch.empty_like(k_d)
+    pnb = torch.empty((3, bsz), dtype=torch.int32, device="cuda")
+    max_ctx2 = max_ctx + ((steps + 127) // 128 + 1) * 128
+    ws2 = torch.empty(layers[0].ctx.workspace_size(bsz, max_ctx2), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tot_bytes = 0
+    e0.record()
+    for s in range(steps):
+        q_d.copy_(q_h[s], non_blocking=True)
+        k_d.copy_(k_h[s], non_blocking=True)
+        v_d.copy_(v_h[s], non_blocking=True)
+        pnb[0].copy_(meta[s][0], non_blocking=True)
+        pnb[1].copy_(meta[s][1], non_blocking=True)
+        pnb[2].copy_(meta[s][2], non_blocking=True)
+        for li, lay in enumerate(layers):
+            if main:
+                lay.ctx.append_token(k_d[li], v_d[li], pnb[0], lay.ring_k, lay.ring_v, lay.bt, lay.pool)
+            lay.ctx.decode_attention(q_d[li], lay.pool, lay.bt, pnb[1], lay.ring_k if main else None,
+                                     lay.ring_v if main else None, pnb[2] if main else None, max_ctx2, lay.out, ws2)
+            out_h[s, li].copy_(lay.out, non_blocking=True)
+        tot_bytes += nl * step_bytes(w, meta[s][3])
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    h2d = (q_h[0].numel() + k_h[0].numel() + v_h[0].numel()) * 2 + 3 * bsz * 4
+    d2h = out_h[0].numel() * 4
+    return {"value": tot_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+# ---------------------------------------------------------------------- CPU oracle arm
+def oracle_layer_step(w, seed, sample_len):
+    """Build one oracle-encoded (sequence, all KV heads) sample and return a closure timing its decode."""
+    from oracle import attention, cache, codebook, layout, rng
+
+    d, hkv, hq = w["d"], w["hkv"], w["hq"]
+    L = sample_len
+    if w["layout"] == "main":
+        nc, nb = ring_split(L)
+        c, _ = codebook.lloyd_max(d, 2)
+        sg, sk = rng.signs(seed, d), rng.gaussian_matrix(seed, d, d)
+        k, v = synth.kv_main(seed, 1, hkv, L, d)
+        bt = np.arange((L + 15) // 16, dtype=np.int32)[None, :]
+        pool = np.zeros((bt.shape[1], hkv, layout.main_tile_bytes(d)), np.uint8)
+        cache.encode_main_range(pool, bt, 0, k[:, :, :nc], v[:, :, :nc], sg, c, sk)
+        ring_k = np.zeros((1, hkv, 128, d), np.float16)
+        ring_v = np.zeros_like(ring_k)
+        ring_k[0, :, :nb] = k[0, :, nc:nc + nb]
+        ring_v[0, :, :nb] = v[0, :, nc:nc + nb]
+        q = synth.queries(seed, 1, hq, d)
+
+        def run():
+            attention.decode_main(q, pool, bt, np.array([nc]), ring_k, ring_v, np.array([nb]), sg, c, sk, hkv)
+        nbytes = hkv * (nc * record_bytes(w) + nb * 4 * d) + hq * d * 6
+    else:
+        c3, _ = codebook.lloyd_max(d, 3)
+        sg = rng.signs(seed, d)
+        k, v = synth.kv_alt(seed, 1, hkv, L, d)
+        bt = np.arange(L // 16, dtype=np.int32)[None, :]
+        pool = np.zeros((bt.shape[1], hkv, layout.alt_tile_bytes(d)), np.uint8)
+        cache.encode_alt_range(pool, bt, 0, k, v, sg, c3)
+        q = synth.queries(seed, 1, hq, d)
+
+        def run():
+            attention.decode_alt(q, pool, bt, np.array([L]), None, None, None, sg, c3, hkv)
+        nbytes = hkv * L * record_bytes(w) + hq * d * 6
+    return run, nbytes
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        info = threadpool_info()
+        if info:
+            return max(int(i.get("num_threads", 1)) for i in info)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_oracle(w, reps, sample_len, budget_s=10.0):
+    """Time the oracle decode of one sample; at most ``reps`` runs or ``budget_s`` seconds."""
+    run, nbytes = oracle_layer_step(w, w["seed"], sample_len)
+    run()  # warm
+    t0 = time.perf_counter()
+    n = 0
+    while n < reps and (n == 0 or time.perf_counter() - t0 < budget_s):
+        run()
+        n += 1
+    dt = (time.perf_counter() - t0) / n
+    return nbytes / dt / 1e9, dt, nbytes, n
+
+
+def oracle_sample_len(w):
+    base = w["ctx"] if w["ctx"] is not None else 32768
+    return int(min(base, 32768 if w["layout"] == "main" else 16384))
+
+
+# ---------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    config = {"workload": args.workload, "layout": w["layout"], "layers": w["layers"], "batch": w["batch"],
+              "q_heads": w["hq"], "kv_heads": w["hkv"], "head_dim": w["d"],
+              "context": w["ctx"] if w["ctx"] is not None else f"U[{w['lo']},{w['hi']}]",
+              "l2": "inputs larger than L2 (every step reads all layers' pools)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        sample_len = oracle_sample_len(w)
+        for _ in range(args.warmup):
+            run_oracle(w, 1, sample_len, budget_s=0)
+        val, dt, nbytes, reps = run_oracle(w, max(1, args.steps), sample_len, budget_s=60.0)
+        sample = f"oracle decode of one sequence x {w['hkv']} KV heads at {sample_len} tokens per step"
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+                "steps": reps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    res = run_gpu(args, w, rank, world)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        sample_len = oracle_sample_len(w)
+        val, dt, nbytes, reps = run_oracle(w, 20, sample_len, budget_s=10.0)
+        cpu = {"value": val, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"{reps} oracle decodes of one sequence x {w['hkv']} KV heads at {sample_len} tokens "
+                         f"({nbytes / 1e6:.1f} MB of records each), {dt:.2f} s each"}
+    peak, _ = measured_peaks()
+    line = {
+        "metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
+        "frac_of_hbm_peak": res["value"] / world / peak,
+        "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"], "gpu_launches": res["gpu_launches"],
+        "clocks": res["clocks"], "encode": res["encode"],
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

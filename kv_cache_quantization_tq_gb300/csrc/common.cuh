@@ -1,0 +1,105 @@
+// Device helpers shared by the libtq kernels.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "tq_internal.h"
+
+namespace tq {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------------------
+// Warp-level coordinate mapping used by every warp-per-vector routine.
+//
+// A vector of D = 32*E coordinates is spread over the 32 lanes of a warp;
+// lane l holds E values, element e being coordinate
+//     coord(e, l) = 32 e + 2 (l & 15) + (l >> 4).
+// Within each aligned 32-coordinate word this is the "even/odd split" order
+// of the bit planes (coordinate 32w + 2j + s sits at bit 16 s + j), so one
+// __ballot_sync over element e yields plane word e directly.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int coord_of(int e, int lane) { return 32 * e + 2 * (lane & 15) + (lane >> 4); }
+
+// Sylvester Walsh-Hadamard transform (unnormalised) of a warp-distributed
+// vector, y_i = sum_j (-1)^popcount(i & j) x_j.  Index bit 0 is lane bit 4,
+// index bits 1..4 are lane bits 0..3, index bits >= 5 are the element index.
+// Each butterfly maps (lo, hi) -> (lo + hi, lo - hi).
+template <int E>
+__device__ __forceinline__ void wht_warp(float (&x)[E], int lane) {
+#pragma unroll
+  for (int lb = 0; lb < 5; ++lb) {
+    const int mask = lb == 0 ? 16 : (1 << (lb - 1));
+    const bool upper = lane & mask;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      float p = __shfl_xor_sync(kFull, x[e], mask);
+      x[e] = upper ? (p - x[e]) : (x[e] + p);
+    }
+  }
+#pragma unroll
+  for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if (!(e & h)) {
+        float a = x[e], b = x[e | h];
+        x[e] = a + b;
+        x[e | h] = a - b;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int m = 16; m; m >>= 1) v += __shfl_xor_sync(kFull, v, m);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int m = 16; m; m >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, m));
+  return v;
+}
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+  for (int m = 16; m; m >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, m));
+  return v;
+}
+
+// Asymmetric min/max quantiser of one group held as one value per lane
+// (IEEE float32 arithmetic, no contraction): s = fp16((mx - mn) / levels),
+// q = clamp(rint((v - mn) / s), 0, levels), q = 0 when s == 0.
+struct GroupCode {
+  __half s, mn;
+  int q;
+};
+__device__ __forceinline__ GroupCode group_quant_lane(float v, float levels) {
+  const float mn = warp_min(v);
+  const float mx = warp_max(v);
+  GroupCode g;
+  g.s = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), levels));
+  g.mn = __float2half_rn(mn);
+  const float s = __half2float(g.s);
+  int q = 0;
+  if (s > 0.f) {
+    float t = rintf(__fdiv_rn(__fsub_rn(v, mn), s));
+    t = fminf(fmaxf(t, 0.f), levels);
+    q = (int)t;
+  }
+  g.q = q;
+  return g;
+}
+
+// c[i] for a 4-entry table held in kernel parameters, without dynamic indexing.
+__device__ __forceinline__ float sel4(const CodeTables& t, int i) {
+  float r = t.c[0];
+  r = i == 1 ? t.c[1] : r;
+  r = i == 2 ? t.c[2] : r;
+  r = i == 3 ? t.c[3] : r;
+  return r;
+}
+
+__device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }
+
+}  // namespace tq

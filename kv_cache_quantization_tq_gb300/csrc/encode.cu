@@ -1,0 +1,429 @@
+// Write path of the compressed KV cache: the encode/flush kernels and the
+// ring-buffer append with flush-on-overflow.
+//
+// Main layout, per (token, KV head) (turboquant vLLM guide, section 2 steps
+// 1-5; turboquant-bench, compression algorithm details):
+//   n_k = ||k||; y = H (D k) / (sqrt(d) n_k); idx_i = #{boundaries <= y_i};
+//   r = y - c[idx]; n_r = ||r||; sigma_j = [(S r)_j >= 0];
+//   values: asymmetric 2-bit min/max quantisation in groups of 32.
+// Alternate layout (vllm-metal TurboQuant guide, quantisation table):
+//   keys: 8-bit affine per block of 32; values: n_v = ||v||,
+//   3-bit Lloyd-Max index of H (D v) / (sqrt(d) n_v).
+//
+// One CTA encodes up to TB tokens of one (sequence, KV head): a warp per
+// token computes norms, the rotation (registers + shuffles), the Lloyd-Max
+// indices (bit planes straight from __ballot_sync) and the value codes; the
+// QJL projection S r of all TB tokens is then a CTA-wide FP32 product with
+// the residuals staged in shared memory; finished tiles leave through
+// 16-byte stores to the pages named by the block table.
+#include "common.cuh"
+
+namespace tq {
+namespace {
+
+struct EncArgs {
+  const __half* k;
+  const __half* v;
+  int src_tokens;
+  int n_tokens;
+  const int32_t* start_pos;
+  const int32_t* block_table;
+  int max_blocks;
+  uint8_t* pool;
+  int num_blocks;
+  int hkv;
+  const float* signs;
+  const float* sketch_t;  // [d][m]
+  CodeTables tab;
+  uint32_t* err;
+};
+
+// ------------------------------------------------------------------ main layout
+template <int D>
+struct MainEnc {
+  static constexpr int E = D / 32;
+  static constexpr int TB = D <= 128 ? 128 : (D == 256 ? 64 : 32);
+  static constexpr int TILE = 12 * D + 64;
+  static constexpr int THREADS = 256;
+  static constexpr int JT = D <= 128 ? 1 : D / 128;    // sketch rows (words) per thread
+  static constexpr int SLICE = D / JT;                 // threads sharing a token slice
+  static constexpr int NSLICE = THREADS / SLICE;
+  static constexpr int TT = TB / NSLICE;               // tokens per thread in S r
+  static constexpr size_t SMEM_R = sizeof(float) * TB * D;
+  static constexpr size_t SMEM_TILES = (size_t)(TB / 16) * TILE;
+  static constexpr size_t SMEM_CODES = (size_t)TB * D;
+  static constexpr size_t SMEM = SMEM_R + SMEM_TILES + SMEM_CODES;
+  static_assert(TT * JT <= 64, "accumulator budget");
+};
+
+// Copy `npages` staged tiles to the pool pages of (b, h) starting at token `start`.
+template <int TILE>
+__device__ void store_tiles(const EncArgs& a, const uint8_t* tiles, int npages, int b, int h, int first_page) {
+  for (int p = 0; p < npages; ++p) {
+    const int page = first_page + p;
+    int blk = -1;
+    if (page < a.max_blocks) blk = a.block_table[(size_t)b * a.max_blocks + page];
+    if (page >= a.max_blocks || blk < 0 || blk >= a.num_blocks) {
+      if (threadIdx.x == 0) flag_error(a.err, page >= a.max_blocks ? TQ_DEVERR_POSITION : TQ_DEVERR_BLOCK_ID);
+      continue;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(a.pool + ((size_t)blk * a.hkv + h) * TILE);
+    const uint4* src = reinterpret_cast<const uint4*>(tiles + (size_t)p * TILE);
+    for (int i = threadIdx.x; i < TILE / 16; i += blockDim.x) dst[i] = src[i];
+  }
+}
+
+template <int D>
+__device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int ntok, int start, uint8_t* smem) {
+  using C = MainEnc<D>;
+  constexpr int E = C::E;
+  constexpr int TB = C::TB;
+  float* rbuf = reinterpret_cast<float*>(smem);                 // [TB][D]
+  uint8_t* tiles = smem + C::SMEM_R;                            // [TB/16][TILE]
+  uint8_t* vcodes = tiles + C::SMEM_TILES;                      // [TB][D]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const size_t base = ((size_t)b * a.hkv + h) * a.src_tokens;
+
+  float sg[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) sg[e] = a.signs[coord_of(e, lane)];
+  const float sqrt_d = sqrtf((float)D);
+
+  // ---- phase 1: one warp per token
+  for (int tt = warp; tt < ntok; tt += C::THREADS / 32) {
+    const __half* kp = a.k + (base + tok0 + tt) * D;
+    const __half* vp = a.v + (base + tok0 + tt) * D;
+    float x[E], vv[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      x[e] = __half2float(kp[coord_of(e, lane)]);
+      vv[e] = __half2float(vp[coord_of(e, lane)]);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss = fmaf(x[e], x[e], ss);
+    const float nk = sqrtf(warp_sum(ss));
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] *= sg[e];
+    wht_warp<E>(x, lane);
+    const float inv = nk > 0.f ? __fdiv_rn(1.f, sqrt_d * nk) : 0.f;
+    uint8_t* tile = tiles + (size_t)(tt >> 4) * C::TILE;
+    const int slot = tt & 15;
+    float rr = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float y = x[e] * inv;
+      const int idx = (y >= a.tab.b[0]) + (y >= a.tab.b[1]) + (y >= a.tab.b[2]);
+      const float r = y - sel4(a.tab, idx);
+      rr = fmaf(r, r, rr);
+      rbuf[tt * D + coord_of(e, lane)] = r;
+      const unsigned hi = __ballot_sync(kFull, idx >> 1);
+      const unsigned lo = __ballot_sync(kFull, idx & 1);
+      if (lane == 0) {
+        reinterpret_cast<uint32_t*>(tile + slot * (D / 8))[e] = hi;
+        reinterpret_cast<uint32_t*>(tile + 2 * D + slot * (D / 8))[e] = lo;
+      }
+    }
+    const float nr = sqrtf(warp_sum(rr));
+    if (lane == 0) {
+      reinterpret_cast<__half*>(tile + 12 * D)[slot] = __float2half_rn(nk);
+      reinterpret_cast<__half*>(tile + 12 * D + 32)[slot] = __float2half_rn(nr);
+    }
+    // values: group e = coordinates 32e..32e+31, one per lane
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      GroupCode g = group_quant_lane(vv[e], 3.f);
+      vcodes[tt * D + coord_of(e, lane)] = (uint8_t)g.q;
+      if (lane == 0) {
+        __half* sm = reinterpret_cast<__half*>(tile + 10 * D + (slot * (D / 32) + e) * 4);
+        sm[0] = g.s;
+        sm[1] = g.mn;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 2: QJL sketch z = S r for all tokens, sign bits by ballot
+  {
+    const int slice = threadIdx.x / C::SLICE;
+    const int ts = threadIdx.x % C::SLICE;
+    const int wsl = ts >> 5;  // warp within slice
+    int jrow[C::JT];
+#pragma unroll
+    for (int u = 0; u < C::JT; ++u) jrow[u] = 32 * (wsl * C::JT + u) + 2 * (lane & 15) + (lane >> 4);
+    float acc[C::JT][C::TT];
+#pragma unroll
+    for (int u = 0; u < C::JT; ++u)
+#pragma unroll
+      for (int t = 0; t < C::TT; ++t) acc[u][t] = 0.f;
+    const int t0 = slice * C::TT;
+    for (int i = 0; i < D; i += 4) {
+      float s4[C::JT][4];
+#pragma unroll
+      for (int u = 0; u < C::JT; ++u)
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) s4[u][ii] = __ldg(a.sketch_t + (size_t)(i + ii) * D + jrow[u]);
+#pragma unroll
+      for (int t = 0; t < C::TT; ++t) {
+        const float4 r4 = *reinterpret_cast<const float4*>(rbuf + (t0 + t) * D + i);
+#pragma unroll
+        for (int u = 0; u < C::JT; ++u) {
+          acc[u][t] = fmaf(s4[u][0], r4.x, acc[u][t]);
+          acc[u][t] = fmaf(s4[u][1], r4.y, acc[u][t]);
+          acc[u][t] = fmaf(s4[u][2], r4.z, acc[u][t]);
+          acc[u][t] = fmaf(s4[u][3], r4.w, acc[u][t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < C::TT; ++t) {
+      const int tt = t0 + t;
+#pragma unroll
+      for (int u = 0; u < C::JT; ++u) {
+        const unsigned bits = __ballot_sync(kFull, acc[u][t] >= 0.f);
+        if (lane == 0 && tt < ntok) {
+          uint8_t* tile = tiles + (size_t)(tt >> 4) * C::TILE;
+          reinterpret_cast<uint32_t*>(tile + 4 * D + (tt & 15) * (D / 8))[wsl * C::JT + u] = bits;
+        }
+      }
+    }
+  }
+  // ---- phase 3: dimension-major value-code words (token 2j+e at bits 16e+2j)
+  for (int w = threadIdx.x; w < (ntok >> 4) * D; w += C::THREADS) {
+    const int p = w / D, i = w % D;
+    uint32_t word = 0;
+#pragma unroll
+    for (int s = 0; s < 16; ++s) word |= (uint32_t)vcodes[(p * 16 + s) * D + i] << (16 * (s & 1) + 2 * (s >> 1));
+    reinterpret_cast<uint32_t*>(tiles + (size_t)p * C::TILE + 6 * D)[i] = word;
+  }
+  __syncthreads();
+  store_tiles<C::TILE>(a, tiles, ntok >> 4, b, h, (start + tok0) >> 4);
+}
+
+// ------------------------------------------------------------------ alternate layout
+template <int D>
+struct AltEnc {
+  static constexpr int E = D / 32;
+  static constexpr int TB = 32;
+  static constexpr int TILE = 24 * D + 32;
+  static constexpr int THREADS = 256;
+  static constexpr size_t SMEM_TILES = (size_t)(TB / 16) * TILE;
+  static constexpr size_t SMEM = SMEM_TILES + (size_t)TB * D;
+};
+
+template <int D>
+__device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int ntok, int start, uint8_t* smem) {
+  using C = AltEnc<D>;
+  constexpr int E = C::E;
+  uint8_t* tiles = smem;
+  uint8_t* vcodes = smem + C::SMEM_TILES;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const size_t base = ((size_t)b * a.hkv + h) * a.src_tokens;
+  float sg[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) sg[e] = a.signs[coord_of(e, lane)];
+  const float sqrt_d = sqrtf((float)D);
+
+  for (int tt = warp; tt < ntok; tt += C::THREADS / 32) {
+    const __half* kp = a.k + (base + tok0 + tt) * D;
+    const __half* vp = a.v + (base + tok0 + tt) * D;
+    uint8_t* tile = tiles + (size_t)(tt >> 4) * C::TILE;
+    const int slot = tt & 15;
+    float vv[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int c = coord_of(e, lane);
+      const float kx = __half2float(kp[c]);
+      vv[e] = __half2float(vp[c]);
+      GroupCode g = group_quant_lane(kx, 255.f);
+      tile[slot * D + c] = (uint8_t)g.q;
+      if (lane == 0) {
+        __half* sm = reinterpret_cast<__half*>(tile + 16 * D + (slot * (D / 32) + e) * 4);
+        sm[0] = g.s;
+        sm[1] = g.mn;
+      }
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss = fmaf(vv[e], vv[e], ss);
+    const float nv = sqrtf(warp_sum(ss));
+#pragma unroll
+    for (int e = 0; e < E; ++e) vv[e] *= sg[e];
+    wht_warp<E>(vv, lane);
+    const float inv = nv > 0.f ? __fdiv_rn(1.f, sqrt_d * nv) : 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float y = vv[e] * inv;
+      int idx = 0;
+#pragma unroll
+      for (int j = 0; j < 7; ++j) idx += (y >= a.tab.b[j]);
+      vcodes[tt * D + coord_of(e, lane)] = (uint8_t)idx;
+    }
+    if (lane == 0) reinterpret_cast<__half*>(tile + 24 * D)[slot] = __float2half_rn(nv);
+  }
+  __syncthreads();
+  // dense 3-bit stream per token: 32 indices -> 3 words
+  for (int w = threadIdx.x; w < ntok * (D / 32); w += C::THREADS) {
+    const int tt = w / (D / 32), chunk = w % (D / 32);
+    uint32_t o[3] = {0u, 0u, 0u};
+#pragma unroll
+    for (int kk = 0; kk < 32; ++kk) {
+      const uint32_t code = vcodes[tt * D + chunk * 32 + kk];
+      const int bit = 3 * kk;
+      o[bit >> 5] |= code << (bit & 31);
+      if ((bit & 31) > 29) o[(bit >> 5) + 1] |= code >> (32 - (bit & 31));
+    }
+    uint32_t* dst = reinterpret_cast<uint32_t*>(tiles + (size_t)(tt >> 4) * C::TILE + 18 * D +
+                                                (tt & 15) * (3 * D / 8) + chunk * 12);
+    dst[0] = o[0];
+    dst[1] = o[1];
+    dst[2] = o[2];
+  }
+  __syncthreads();
+  store_tiles<C::TILE>(a, tiles, ntok >> 4, b, h, (start + tok0) >> 4);
+}
+
+// ------------------------------------------------------------------ kernels
+template <int D, bool MAIN>
+__global__ void __launch_bounds__(256) encode_kernel(EncArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int b = blockIdx.z, h = blockIdx.y;
+  constexpr int TB = MAIN ? MainEnc<D>::TB : AltEnc<D>::TB;
+  const int tok0 = blockIdx.x * TB;
+  const int ntok = min(TB, a.n_tokens - tok0);
+  const int start = a.start_pos[b];
+  if (start < 0 || (start & 15)) {
+    if (threadIdx.x == 0) flag_error(a.err, TQ_DEVERR_POSITION);
+    return;
+  }
+  if (MAIN)
+    encode_main_block<D>(a, b, h, tok0, ntok, start, smem);
+  else
+    encode_alt_block<D>(a, b, h, tok0, ntok, start, smem);
+}
+
+struct AppendArgs {
+  EncArgs enc;          // k/v point at the rings, src_tokens = 128
+  const __half* k_new;
+  const __half* v_new;
+  const int32_t* pos;
+  __half* ring_k;
+  __half* ring_v;
+};
+
+template <int D, bool MAIN>
+__global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int b = blockIdx.y, h = blockIdx.x;
+  const int pos = a.pos[b];
+  if (pos < 0) {
+    if (threadIdx.x == 0) flag_error(a.enc.err, TQ_DEVERR_POSITION);
+    return;
+  }
+  if (pos > 0 && (pos % kRing) == 0) {
+    const int start = pos - kRing;
+    constexpr int TB = MAIN ? MainEnc<D>::TB : AltEnc<D>::TB;
+    static_assert(kRing % TB == 0, "ring flush is a whole number of encode batches");
+    for (int t0 = 0; t0 < kRing; t0 += TB) {
+      if (MAIN)
+        encode_main_block<D>(a.enc, b, h, t0, TB, start, smem);
+      else
+        encode_alt_block<D>(a.enc, b, h, t0, TB, start, smem);
+      __syncthreads();
+    }
+  }
+  const int slot = pos % kRing;
+  const size_t src = ((size_t)b * a.enc.hkv + h) * D;
+  const size_t dst = (((size_t)b * a.enc.hkv + h) * kRing + slot) * D;
+  for (int i = threadIdx.x; i < D / 8; i += blockDim.x) {
+    reinterpret_cast<uint4*>(a.ring_k + dst)[i] = reinterpret_cast<const uint4*>(a.k_new + src)[i];
+    reinterpret_cast<uint4*>(a.ring_v + dst)[i] = reinterpret_cast<const uint4*>(a.v_new + src)[i];
+  }
+}
+
+template <int D, bool MAIN>
+cudaError_t launch_encode_t(const EncArgs& a, int batch, cudaStream_t s) {
+  constexpr int TB = MAIN ? MainEnc<D>::TB : AltEnc<D>::TB;
+  constexpr size_t SMEM = MAIN ? MainEnc<D>::SMEM : AltEnc<D>::SMEM;
+  auto kern = encode_kernel<D, MAIN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.n_tokens + TB - 1) / TB, a.hkv, batch);
+  kern<<<grid, 256, SMEM, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D, bool MAIN>
+cudaError_t launch_append_t(const AppendArgs& a, int batch, cudaStream_t s) {
+  constexpr size_t SMEM = MAIN ? MainEnc<D>::SMEM : AltEnc<D>::SMEM;
+  auto kern = append_kernel<D, MAIN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.enc.hkv, batch);
+  kern<<<grid, 256, SMEM, s>>>(a);
+  return cudaGetLastError();
+}
+
+EncArgs make_args(tq_ctx* ctx, const void* k, const void* v, int src_tokens, int n_tokens, const int32_t* start_pos,
+                  const int32_t* block_table, int max_blocks, void* pool, int num_blocks) {
+  EncArgs a;
+  a.k = static_cast<const __half*>(k);
+  a.v = static_cast<const __half*>(v);
+  a.src_tokens = src_tokens;
+  a.n_tokens = n_tokens;
+  a.start_pos = start_pos;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.pool = static_cast<uint8_t*>(pool);
+  a.num_blocks = num_blocks;
+  a.hkv = ctx->cfg.num_kv_heads;
+  a.signs = ctx->d_signs;
+  a.sketch_t = ctx->d_sketch_t;
+  a.tab = ctx->tab;
+  a.err = ctx->d_err;
+  return a;
+}
+
+}  // namespace
+
+cudaError_t launch_encode(tq_ctx* ctx, const void* k, const void* v, int batch, int src_tokens, int n_tokens,
+                          const int32_t* start_pos, const int32_t* block_table, int max_blocks, void* pool,
+                          int num_blocks, cudaStream_t s) {
+  EncArgs a = make_args(ctx, k, v, src_tokens, n_tokens, start_pos, block_table, max_blocks, pool, num_blocks);
+  const bool main = ctx->cfg.layout == TQ_LAYOUT_MAIN;
+  cudaError_t e = cudaErrorInvalidValue;
+  prof_start(ctx, kProfEncode, s);
+  switch (ctx->cfg.head_dim) {
+    case 64: e = main ? launch_encode_t<64, true>(a, batch, s) : launch_encode_t<64, false>(a, batch, s); break;
+    case 128: e = main ? launch_encode_t<128, true>(a, batch, s) : launch_encode_t<128, false>(a, batch, s); break;
+    case 256: e = main ? launch_encode_t<256, true>(a, batch, s) : launch_encode_t<256, false>(a, batch, s); break;
+    case 512: e = main ? launch_encode_t<512, true>(a, batch, s) : launch_encode_t<512, false>(a, batch, s); break;
+  }
+  prof_stop(ctx, kProfEncode, s);
+  if (e == cudaSuccess) ctx->launches++;
+  return e;
+}
+
+cudaError_t launch_append(tq_ctx* ctx, const void* k_new, const void* v_new, const int32_t* pos, int batch,
+                          void* ring_k, void* ring_v, const int32_t* block_table, int max_blocks, void* pool,
+                          int num_blocks, cudaStream_t s) {
+  AppendArgs a;
+  a.enc = make_args(ctx, ring_k, ring_v, kRing, kRing, nullptr, block_table, max_blocks, pool, num_blocks);
+  a.k_new = static_cast<const __half*>(k_new);
+  a.v_new = static_cast<const __half*>(v_new);
+  a.pos = pos;
+  a.ring_k = static_cast<__half*>(ring_k);
+  a.ring_v = static_cast<__half*>(ring_v);
+  const bool main = ctx->cfg.layout == TQ_LAYOUT_MAIN;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (ctx->cfg.head_dim) {
+    case 64: e = main ? launch_append_t<64, true>(a, batch, s) : launch_append_t<64, false>(a, batch, s); break;
+    case 128: e = main ? launch_append_t<128, true>(a, batch, s) : launch_append_t<128, false>(a, batch, s); break;
+    case 256: e = main ? launch_append_t<256, true>(a, batch, s) : launch_append_t<256, false>(a, batch, s); break;
+    case 512: e = main ? launch_append_t<512, true>(a, batch, s) : launch_append_t<512, false>(a, batch, s); break;
+  }
+  if (e == cudaSuccess) ctx->launches++;
+  return e;
+}
+
+}  // namespace tq

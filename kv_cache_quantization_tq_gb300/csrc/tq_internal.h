@@ -1,0 +1,82 @@
+// Internal declarations shared by the host glue (host.cpp) and the CUDA
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+#include <vector>
+
+#include "../../include/tq.h"
+
+namespace tq {
+
+constexpr int kPage = 16;        // tokens per page
+constexpr int kRing = 128;       // exact recent-token buffer
+constexpr int kGroup = 32;       // value group / key block
+constexpr int kMaxRep = 8;       // query heads handled by one decode CTA
+
+// Small per-context tables passed by value as kernel parameters.
+struct CodeTables {
+  float c[8];   // centroids, ascending (4 used by main keys, 8 by alt values)
+  float b[8];   // decision boundaries (midpoints), K-1 used
+};
+
+struct ProfileKind {
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev;  // recorded pairs
+  size_t used = 0;
+};
+
+}  // namespace tq
+
+struct tq_ctx {
+  tq_config cfg;
+  int device = 0;
+  int n_rep = 1;
+  int ncent = 4;
+  tq::CodeTables tab{};
+  std::vector<float> h_centroids, h_boundaries, h_signs, h_sketch;
+  float* d_signs = nullptr;     // [d]
+  float* d_sketch = nullptr;    // [m][d]
+  float* d_sketch_t = nullptr;  // [d][m]
+  uint32_t* d_err = nullptr;    // device error word
+  int64_t launches = 0;
+  bool profiling = false;
+  tq::ProfileKind prof[3];      // 0 decode, 1 encode, 2 merge
+};
+
+namespace tq {
+
+enum ProfKind { kProfDecode = 0, kProfEncode = 1, kProfMerge = 2 };
+
+// Event bracketing for the profiler (no-ops unless profiling is on).
+void prof_start(tq_ctx* ctx, int kind, cudaStream_t s);
+void prof_stop(tq_ctx* ctx, int kind, cudaStream_t s);
+
+// Decode chunking policy shared by tq_workspace_size and tq_decode_attention.
+struct DecodePlan {
+  int chunk_tokens;   // compressed tokens per split-K chunk (multiple of 16)
+  int n_chunks;       // chunks for max_ctx compressed tokens
+  int n_parts;        // n_chunks + 1 (ring part)
+  size_t q_bytes;     // pre-rotated queries
+  size_t part_bytes;  // split-K partials
+  size_t total;
+};
+DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx);
+
+// ---- launchers implemented in the .cu files (return a cudaError_t) ----
+cudaError_t launch_encode(tq_ctx* ctx, const void* k, const void* v, int batch, int src_tokens, int n_tokens,
+                          const int32_t* start_pos, const int32_t* block_table, int max_blocks, void* pool,
+                          int num_blocks, cudaStream_t s);
+cudaError_t launch_append(tq_ctx* ctx, const void* k_new, const void* v_new, const int32_t* pos, int batch,
+                          void* ring_k, void* ring_v, const int32_t* block_table, int max_blocks, void* pool,
+                          int num_blocks, cudaStream_t s);
+cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, int batch, const void* pool,
+                          int num_blocks, const int32_t* block_table, int max_blocks, const int32_t* n_compressed,
+                          const void* ring_k, const void* ring_v, const int32_t* n_buf, int max_ctx, float* out,
+                          void* workspace, cudaStream_t s);
+cudaError_t launch_pack(const uint8_t* codes, int64_t n, int bits, void* dst, cudaStream_t s);
+cudaError_t launch_unpack(const void* src, int64_t n, int bits, uint8_t* codes, cudaStream_t s);
+
+}  // namespace tq

@@ -1,0 +1,129 @@
+"""Scenario builders and comparison helpers for the GPU parity tests.
+
+Inputs come from ``synth``; expected values from ``oracle``; nothing here
+computes the method.  Bit extraction for comparisons is written out here so
+that CUDA output is never fed through oracle code.
+"""
+import numpy as np
+import torch
+
+import synth
+from oracle import cache, codebook, layout, quant, rng
+
+MARGIN = 1e-5  # oracle values this close to a decision boundary may legitimately differ
+
+
+def oracle_tables(seed, d, layout_main=True):
+    bits = 2 if layout_main else 3
+    c, _ = codebook.lloyd_max(d, bits)
+    c32 = c.astype(np.float32)
+    signs = rng.signs(seed, d).astype(np.float32)
+    sketch = rng.gaussian_matrix(seed, d, d) if layout_main else None
+    return c32, signs, sketch
+
+
+def make_ctx(tq, layout_main, d, hq, hkv, seed):
+    c32, signs, sketch = oracle_tables(seed, d, layout_main)
+    lay = tq.TQ_LAYOUT_MAIN if layout_main else tq.TQ_LAYOUT_ALT
+    ctx = tq.Context(lay, d, hq, hkv, seed, centroids=c32, signs=signs, sketch=sketch)
+    return ctx, c32.astype(np.float64), signs.astype(np.float64), sketch
+
+
+def to_dev(x, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+# ---------------------------------------------------------------- bit helpers (test-local)
+def plane_bits(words_u32):
+    """uint32 [..., n/32] -> bits [..., n] with coordinate 32w+2j+e at bit 16e+j."""
+    w = words_u32.astype(np.uint64)[..., None, None]
+    sh = (16 * np.arange(2)[None, :] + np.arange(16)[:, None]).astype(np.uint64)
+    b = (w >> sh) & np.uint64(1)
+    return b.reshape(words_u32.shape[:-1] + (words_u32.shape[-1] * 32,)).astype(np.uint8)
+
+
+def main_fields(tiles, d):
+    t = np.ascontiguousarray(tiles)
+    lead = t.shape[:-1]
+    w = lambda off, n: np.ascontiguousarray(t[..., off:off + n]).view("<u4")
+    kh = plane_bits(w(0, 2 * d).reshape(lead + (16, d // 32)))
+    kl = plane_bits(w(2 * d, 2 * d).reshape(lead + (16, d // 32)))
+    ks = plane_bits(w(4 * d, 2 * d).reshape(lead + (16, d // 32)))
+    return {
+        "idx": 2 * kh + kl,
+        "sigma": ks,
+        "v_bytes": t[..., 6 * d:12 * d],
+        "kn": np.ascontiguousarray(t[..., 12 * d:12 * d + 32]).view("<i2"),
+        "rn": np.ascontiguousarray(t[..., 12 * d + 32:12 * d + 64]).view("<i2"),
+    }
+
+
+def alt_fields(tiles, d):
+    t = np.ascontiguousarray(tiles)
+    lead = t.shape[:-1]
+    vi = t[..., 18 * d:24 * d].reshape(lead + (16, 3 * d // 8))
+    bits = np.unpackbits(vi, axis=-1, bitorder="little").reshape(lead + (16, d, 3)).astype(np.uint8)
+    idx = bits[..., 0] + 2 * bits[..., 1] + 4 * bits[..., 2]
+    return {
+        "k_bytes": t[..., :18 * d],
+        "vidx": idx,
+        "vn": np.ascontiguousarray(t[..., 24 * d:24 * d + 32]).view("<i2"),
+    }
+
+
+def near_boundary(y, centroids):
+    b = 0.5 * (centroids[:-1] + centroids[1:])
+    return np.min(np.abs(y[..., None] - b), axis=-1) < MARGIN
+
+
+def tile_index(bt, starts, n_tok):
+    """(block ids [B, pages]) of the pages holding tokens start..start+n_tok-1 of each sequence."""
+    pages = np.arange(n_tok // 16)
+    return np.stack([bt[b, starts[b] // 16 + pages] for b in range(len(starts))])
+
+
+def allclose_report(got, ref, atol=2e-3, rtol=1e-3):
+    err = np.abs(got - ref)
+    bad = err > atol + rtol * np.abs(ref)
+    return (not bad.any()), float(err.max()) if err.size else 0.0, int(bad.sum())
+
+
+# ---------------------------------------------------------------- decode scenarios
+def build_main_cache(seed, d, hkv, lengths, centroids, signs, sketch, shuffled=True, extra_blocks=0):
+    """Oracle-encoded pool + ring for sequences of the given total lengths."""
+    bsz = len(lengths)
+    lmax = max(max(lengths), 1)
+    t_all = ((lmax + 15) // 16) * 16
+    k, v = synth.kv_main(seed, bsz, hkv, t_all, d)
+    max_blocks = max(t_all // 16, 1)
+    bt = synth.block_table(seed, bsz, max_blocks, shuffled)
+    nblk = bsz * max_blocks + extra_blocks
+    pool = np.zeros((nblk, hkv, layout.main_tile_bytes(d)), np.uint8)
+    n_c = np.zeros(bsz, np.int32)
+    n_b = np.zeros(bsz, np.int32)
+    ring_k = np.zeros((bsz, hkv, 128, d), np.float16)
+    ring_v = np.zeros_like(ring_k)
+    for b, L in enumerate(lengths):
+        nc, nb = cache.ring_split(L)
+        n_c[b], n_b[b] = nc, nb
+        if nc:
+            cache.encode_main_range(pool, bt[b:b + 1], 0, k[b:b + 1, :, :nc], v[b:b + 1, :, :nc], signs, centroids, sketch)
+        ring_k[b, :, :nb] = k[b, :, nc:nc + nb]
+        ring_v[b, :, :nb] = v[b, :, nc:nc + nb]
+    return dict(k=k, v=v, bt=bt, pool=pool, n_c=n_c, n_b=n_b, ring_k=ring_k, ring_v=ring_v, max_ctx=int(n_c.max()) if bsz else 0)
+
+
+def build_alt_cache(seed, d, hkv, lengths, centroids3, signs, shuffled=True):
+    bsz = len(lengths)
+    t_all = ((max(lengths) + 15) // 16) * 16
+    k, v = synth.kv_alt(seed, bsz, hkv, t_all, d)
+    max_blocks = t_all // 16
+    bt = synth.block_table(seed, bsz, max_blocks, shuffled)
+    pool = np.zeros((bsz * max_blocks, hkv, layout.alt_tile_bytes(d)), np.uint8)
+    n_c = np.array(lengths, np.int32)
+    for b, L in enumerate(lengths):
+        cache.encode_alt_range(pool, bt[b:b + 1], 0, k[b:b + 1, :, :L], v[b:b + 1, :, :L], signs, centroids3)
+    return dict(k=k, v=v, bt=bt, pool=pool, n_c=n_c, max_ctx=int(n_c.max()))

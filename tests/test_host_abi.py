@@ -1,0 +1,108 @@
+"""Host-side checks of libtq (no GPU): exports, setup tables, host packing, argument validation."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from conftest import ROOT, golden
+from oracle import codebook, layout, rng
+
+from kv_cache_quantization_tq_gb300.build import build
+
+build()
+from kv_cache_quantization_tq_gb300 import binding as B  # noqa: E402
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "tq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tq_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_function_is_exported_and_bound():
+    names = _header_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(B.lib, n), n
+    assert sorted(B.EXPORTED) == names
+
+
+def test_product_code_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "kv_cache_quantization_tq_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cpp", ".h", ".cuh")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle", text, re.M), f
+                assert "oracle/" not in text, f
+
+
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_host_codebook_matches_oracle(d, bits):
+    c, b = B.tq_lloyd_max(d, bits)
+    co, bo = codebook.lloyd_max(d, bits)
+    assert np.max(np.abs(c - co)) < 1e-9
+    assert np.max(np.abs(b - bo)) < 1e-9
+    assert np.array_equal(c, -c[::-1])
+
+
+@pytest.mark.parametrize("seed", [0, 1, 12345, 2**63 + 7])
+def test_host_tables_match_oracle_generator(seed):
+    d = 128
+    s, sk = B.tq_generate_tables(seed, d, d)
+    assert np.array_equal(s, rng.signs(seed, d).astype(np.float32))
+    ref = rng.gaussian_matrix(seed, d, d)
+    ulp = np.spacing(np.abs(ref).astype(np.float32))
+    assert np.all(np.abs(sk - ref) <= ulp)
+
+
+@pytest.mark.parametrize("bits", list(range(1, 9)))
+def test_host_pack_matches_oracle(bits):
+    for n in (1, 5, 64, 333):
+        codes = synth.random_codes(n + bits, n, bits)
+        got = B.tq_pack_host(codes, bits)
+        assert np.array_equal(got, layout.pack_bits(codes, bits))
+        assert np.array_equal(B.tq_unpack_host(got, n, bits), codes)
+
+
+def test_host_pack_golden_examples():
+    for case in golden("pack_examples.json")["cases"]:
+        got = B.tq_pack_host(np.array(case["codes"], np.uint8), case["bits"])
+        assert got.tobytes().hex() == case["bytes_hex"]
+
+
+def test_host_pack_rejects_out_of_range_codes():
+    with pytest.raises(B.TQError):
+        B.tq_pack_host(np.array([4], np.uint8), 2)
+
+
+def test_config_validation():
+    B.tq_config_init(B.TQ_LAYOUT_MAIN, 128, 28, 4)
+    B.tq_config_init(B.TQ_LAYOUT_ALT, 512, 8, 8)
+    B.tq_config_init(B.TQ_LAYOUT_MAIN, 128, 64, 4)  # n_rep 16 = 2 groups of 8
+    with pytest.raises(B.TQError) as e:
+        B.tq_config_init(B.TQ_LAYOUT_MAIN, 96, 16, 4)
+    assert e.value.status == B.TQ_ERR_UNSUPPORTED
+    with pytest.raises(B.TQError) as e:
+        B.tq_config_init(B.TQ_LAYOUT_MAIN, 128, 10, 4)
+    assert e.value.status == B.TQ_ERR_INVALID_ARG
+    with pytest.raises(B.TQError) as e:
+        B.tq_config_init(B.TQ_LAYOUT_MAIN, 128, 36, 4)  # n_rep 9 cannot split evenly
+    assert e.value.status == B.TQ_ERR_UNSUPPORTED
+
+
+def test_null_context_calls_are_rejected_without_cuda():
+    lib = B.lib
+    assert lib.tq_encode_flush(None, None, None, 1, 16, 16, None, None, 1, None, 1, None) == B.TQ_ERR_INVALID_ARG
+    assert lib.tq_decode_attention(None, None, 1, None, 0, None, 0, None, None, None, None, 0, None, None, 0,
+                                   None) == B.TQ_ERR_INVALID_ARG
+    assert lib.tq_append_token(None, None, None, None, 1, None, None, None, 0, None, 0, None) == B.TQ_ERR_INVALID_ARG
+    assert lib.tq_pack(None, 10, 9, None, None) == B.TQ_ERR_INVALID_ARG
+    assert lib.tq_bytes_per_token_head(None) == 0
+    assert lib.tq_launch_count(None) == 0
+    assert lib.tq_status_string(B.TQ_ERR_WORKSPACE).startswith(b"TQ_ERR_WORKSPACE")
+    assert lib.tq_workspace_size(None, 1, 16, C.byref(C.c_size_t())) == B.TQ_ERR_INVALID_ARG
