@@ -74,13 +74,14 @@ def step_bytes(w, lengths_after_append):
     rb, d = record_bytes(w), w["d"]
     tot = 0
     for L in lengths_after_append:
+        L = int(L)
         if w["layout"] == "main":
             nc, nb = ring_split(L)
         else:
             nc, nb = L, 0
         tot += w["hkv"] * (nc * rb + nb * 4 * d)
     tot += w["batch"] * w["hq"] * d * (2 + 4)
-    return tot
+    return int(tot)
 
 
 def measured_peaks():
@@ -109,7 +110,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -231,6 +232,58 @@ def encode_throughput(tq, torch, w, layers, k1, v1, reps=3):
             "ms_per_call": ms, "tokens_per_call": toks}
 
 
+class StepGraph:
+    """One decode step of every layer, captured once as a CUDA graph and replayed.
+
+    Per-step state lives in fixed device buffers: ``pos`` (index of the token
+    being appended), and the compressed / ring counts derived from it.  The
+    graph appends the token in every layer (flushing a full ring), derives the
+    counts, runs decode attention in every layer and advances ``pos``.
+    """
+
+    def __init__(self, torch, w, layers, lengths, max_ctx, ws, q, kn, vn, out_host=None, in_host=None):
+        self.torch = torch
+        self.w, self.layers, self.max_ctx, self.ws = w, layers, max_ctx, ws
+        self.main = w["layout"] == "main"
+        self.pos = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+        self.nc = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+        self.nb = torch.zeros_like(self.nc)
+        self.q, self.kn, self.vn = q, kn, vn
+        self.out_host, self.in_host = out_host, in_host
+        self.graph = None
+
+    def body(self):
+        torch = self.torch
+        if self.in_host is not None:
+            qh, kh, vh = self.in_host
+            self.q.copy_(qh, non_blocking=True)
+            self.kn.copy_(kh, non_blocking=True)
+            self.vn.copy_(vh, non_blocking=True)
+        if self.main:
+            for li, lay in enumerate(self.layers):
+                lay.ctx.append_token(self.kn[li], self.vn[li], self.pos, lay.ring_k, lay.ring_v, lay.bt, lay.pool)
+            t = self.pos + 1
+            self.nc.copy_(torch.div(t - 1, 128, rounding_mode="floor") * 128)
+            self.nb.copy_(t - self.nc)
+        for li, lay in enumerate(self.layers):
+            lay.ctx.decode_attention(self.q[li], lay.pool, lay.bt, self.nc, lay.ring_k if self.main else None,
+                                     lay.ring_v if self.main else None, self.nb if self.main else None,
+                                     self.max_ctx, lay.out, self.ws)
+            if self.out_host is not None:
+                self.out_host[li].copy_(lay.out, non_blocking=True)
+        if self.main:
+            self.pos.add_(1)
+
+    def capture(self):
+        torch = self.torch
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, capture_error_mode="thread_local"):
+            self.body()
+
+    def replay(self):
+        self.graph.replay()
+
+
 def run_gpu(args, w, rank, world):
     import torch
 
@@ -242,135 +295,114 @@ def run_gpu(args, w, rank, world):
         torch.distributed.barrier()
     import kv_cache_quantization_tq_gb300 as tq
 
-    steps_total = args.warmup + args.steps
+    steps_total = args.warmup + args.steps + 64  # + end-to-end steps
     lengths, k1, v1, layers = build_gpu_state(tq, torch, w, steps_total)
     encode_prefix(tq, torch, w, lengths, k1, v1, layers)
     enc = encode_throughput(tq, torch, w, layers, k1, v1)
-    bsz, hq, hkv, d = w["batch"], w["hq"], w["hkv"], w["d"]
+    bsz, hq, hkv, d, nl = w["batch"], w["hq"], w["hkv"], w["d"], w["layers"]
     main = w["layout"] == "main"
     g = torch.Generator(device="cuda")
     g.manual_seed(1234 + rank)
-    # per-step device inputs, prepared before timing
-    q_all = torch.randn((steps_total, w["layers"], bsz, hq, d), generator=g, device="cuda").half()
-    kn_all = torch.randn((steps_total, w["layers"], bsz, hkv, d), generator=g, device="cuda").half()
-    vn_all = torch.randn((steps_total, w["layers"], bsz, hkv, d), generator=g, device="cuda").half()
-    pos_np = np.array([[L + s for L in lengths] for s in range(steps_total)], np.int32)
-    after = pos_np + 1
-    if main:
-        nc_np = (128 * ((after - 1) // 128)).astype(np.int32)
-        nb_np = (after - nc_np).astype(np.int32)
-    else:
-        nc_np = np.array([[L for L in lengths] for _ in range(steps_total)], np.int32)
-        nb_np = np.zeros_like(nc_np)
-    pos_d = torch.from_numpy(pos_np).cuda()
-    nc_d = torch.from_numpy(nc_np).cuda()
-    nb_d = torch.from_numpy(nb_np).cuda()
-    max_ctx = int(((nc_np.max() + 15) // 16) * 16)
+    q = torch.randn((nl, bsz, hq, d), generator=g, device="cuda").half()
+    kn = torch.randn((nl, bsz, hkv, d), generator=g, device="cuda").half()
+    vn = torch.randn((nl, bsz, hkv, d), generator=g, device="cuda").half()
+    max_ctx = int(((max(lengths) + steps_total + 15) // 16) * 16)
     ws = torch.empty(layers[0].ctx.workspace_size(bsz, max_ctx), dtype=torch.uint8, device="cuda")
-    bytes_per_step = [w["layers"] * step_bytes(w, after[s] if main else nc_np[s]) for s in range(steps_total)]
 
-    def step(s):
-        for li, lay in enumerate(layers):
-            if main:
-                lay.ctx.append_token(kn_all[s, li], vn_all[s, li], pos_d[s], lay.ring_k, lay.ring_v, lay.bt, lay.pool)
-            lay.ctx.decode_attention(q_all[s, li], lay.pool, lay.bt, nc_d[s], lay.ring_k if main else None,
-                                     lay.ring_v if main else None, nb_d[s] if main else None, max_ctx, lay.out, ws)
+    def bytes_at(pos_list):
+        after = [p + 1 for p in pos_list] if main else list(pos_list)
+        return nl * step_bytes(w, after)
 
-    for s in range(args.warmup):
-        step(s)
+    sg = StepGraph(torch, w, layers, lengths, max_ctx, ws, q, kn, vn)
+    pos = list(lengths)
+    for _ in range(args.warmup):  # eager warm-up steps (same calls as the graph)
+        sg.body()
+        if main:
+            pos = [p + 1 for p in pos]
+    torch.cuda.synchronize()
+    for lay in layers:
+        lay.ctx.profile_begin()
+    launches0 = sum(l.ctx.launch_count for l in layers)
+    sg.capture()
+    launches_per_step = sum(l.ctx.launch_count for l in layers) - launches0
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    launches0 = sum(l.ctx.launch_count for l in layers)
-    for lay in layers:
-        lay.ctx.profile_begin()
+    timed_bytes = 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
         torch.cuda.synchronize()
         e0.record()
-        for s in range(args.warmup, steps_total):
-            step(s)
+        for _ in range(args.steps):
+            sg.replay()
         e1.record()
         torch.cuda.synchronize()
+    for _ in range(args.steps):
+        timed_bytes += bytes_at(pos)
+        if main:
+            pos = [p + 1 for p in pos]
     ms = e0.elapsed_time(e1)
-    prof = [lay.ctx.profile_end() for lay in layers]
-    launches = sum(l.ctx.launch_count for l in layers) - launches0
+    prof = [lay.ctx.profile_end() for lay in layers]  # events of the last replay
     if world > 1:
         t = torch.tensor([ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
         torch.distributed.barrier()
-    timed_bytes = sum(bytes_per_step[args.warmup:])
     value = timed_bytes * world / (ms * 1e-3) / 1e9
 
-    # dominant kernel: the fused decode kernel, timed by the library's CUDA events
+    # dominant kernel: the fused decode kernel, timed by the library's CUDA
+    # events captured into the step graph (last replayed step)
     dec_ms = sum(p["decode_ms"] for p in prof)
     dec_n = sum(p["decode_launches"] for p in prof)
     peak, peak_kind = measured_peaks()
-    per_launch_bytes = timed_bytes / max(dec_n, 1)
+    last_pos = [p - 1 for p in pos] if main else pos
+    per_launch_bytes = bytes_at(last_pos) / nl
     achieved = per_launch_bytes / (dec_ms / max(dec_n, 1) * 1e-3) / 1e9 if dec_n else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak if achieved else None, "traffic": None,
-                "kernel": "decode_main_kernel" if main else "decode_alt_kernel", "peak_source": peak_kind,
-                "launches": dec_n, "avg_launch_us": dec_ms / max(dec_n, 1) * 1e3,
-                "merge_us_per_launch": sum(p["merge_ms"] for p in prof) / max(dec_n, 1) * 1e3}
+                "kernel": "tc_decode_kernel" if (main and d == 128) else ("decode_main_kernel" if main else
+                                                                          "decode_alt_kernel"),
+                "peak_source": peak_kind, "launches": dec_n, "avg_launch_us": dec_ms / max(dec_n, 1) * 1e3,
+                "merge_us_per_launch": sum(p["merge_ms"] for p in prof) / max(dec_n, 1) * 1e3,
+                "bytes_per_launch": per_launch_bytes}
 
-    # end to end through the same C ABI with host buffers (pinned), copies inside the timed region
-    e2e = run_e2e(torch, w, layers, lengths, args, main, max_ctx, ws)
+    e2e = run_e2e(torch, w, layers, pos, max_ctx, ws, q, kn, vn, bytes_at)
     return {
         "value": value, "ms_per_step": ms / args.steps, "roofline": roofline, "encode": enc, "e2e": e2e,
-        "gpu_launches": int(launches), "clocks": clk.summary(), "lengths": lengths,
+        "gpu_launches": int(launches_per_step * args.steps), "clocks": clk.summary(), "lengths": lengths,
     }
 
 
-def run_e2e(torch, w, layers, lengths, args, main, max_ctx, ws):
-    """Same decode step, inputs copied from pinned host memory and outputs read back every step."""
-    bsz, hq, hkv, d, nl = w["batch"], w["hq"], w["hkv"], w["d"], w["layers"]
-    steps = max(3, min(args.steps, 16))
-    base = [L + args.warmup + args.steps for L in lengths]
+def run_e2e(torch, w, layers, pos, max_ctx, ws, q, kn, vn, bytes_at, steps=16):
+    """Same decode step through the same C ABI, with the step's q, k, v copied in from pinned host
+    memory and every layer's output copied back to pinned host memory inside the timed region
+    (captured in the step graph)."""
+    nl = w["layers"]
     rng = np.random.default_rng(5)
-    q_h = torch.from_numpy(rng.standard_normal((steps, nl, bsz, hq, d)).astype(np.float16)).pin_memory()
-    k_h = torch.from_numpy(rng.standard_normal((steps, nl, bsz, hkv, d)).astype(np.float16)).pin_memory()
-    v_h = torch.from_numpy(rng.standard_normal((steps, nl, bsz, hkv, d)).astype(np.float16)).pin_memory()
-    out_h = torch.empty((steps, nl, bsz, hq, d), dtype=torch.float32).pin_memory()
-    meta = []
-    for s in range(steps):
-        pos = np.array([b + s for b in base], np.int32)
-        after = pos + 1
-        nc = (128 * ((after - 1) // 128)).astype(np.int32) if main else np.array(lengths, np.int32)
-        nb = (after - nc).astype(np.int32) if main else np.zeros(bsz, np.int32)
-        meta.append((torch.from_numpy(pos).pin_memory(), torch.from_numpy(nc).pin_memory(),
-                     torch.from_numpy(nb).pin_memory(), after if main else nc))
-    q_d = torch.empty((nl, bsz, hq, d), dtype=torch.float16, device="cuda")
-    k_d = torch.empty((nl, bsz, hkv, d), dtype=torch.float16, device="cuda")
-    v_d = torch.empty_like(k_d)
-    pnb = torch.empty((3, bsz), dtype=torch.int32, device="cuda")
-    max_ctx2 = max_ctx + ((steps + 127) // 128 + 1) * 128
-    ws2 = torch.empty(layers[0].ctx.workspace_size(bsz, max_ctx2), dtype=torch.uint8, device="cuda")
+    qh = torch.from_numpy(rng.standard_normal(tuple(q.shape)).astype(np.float16)).pin_memory()
+    kh = torch.from_numpy(rng.standard_normal(tuple(kn.shape)).astype(np.float16)).pin_memory()
+    vh = torch.from_numpy(rng.standard_normal(tuple(vn.shape)).astype(np.float16)).pin_memory()
+    out_h = torch.empty((nl,) + tuple(layers[0].out.shape), dtype=torch.float32).pin_memory()
+    sg = StepGraph(torch, w, layers, pos, max_ctx, ws, q, kn, vn, out_host=out_h, in_host=(qh, kh, vh))
+    sg.capture()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    tot_bytes = 0
     e0.record()
-    for s in range(steps):
-        q_d.copy_(q_h[s], non_blocking=True)
-        k_d.copy_(k_h[s], non_blocking=True)
-        v_d.copy_(v_h[s], non_blocking=True)
-        pnb[0].copy_(meta[s][0], non_blocking=True)
-        pnb[1].copy_(meta[s][1], non_blocking=True)
-        pnb[2].copy_(meta[s][2], non_blocking=True)
-        for li, lay in enumerate(layers):
-            if main:
-                lay.ctx.append_token(k_d[li], v_d[li], pnb[0], lay.ring_k, lay.ring_v, lay.bt, lay.pool)
-            lay.ctx.decode_attention(q_d[li], lay.pool, lay.bt, pnb[1], lay.ring_k if main else None,
-                                     lay.ring_v if main else None, pnb[2] if main else None, max_ctx2, lay.out, ws2)
-            out_h[s, li].copy_(lay.out, non_blocking=True)
-        tot_bytes += nl * step_bytes(w, meta[s][3])
+    for _ in range(steps):
+        sg.replay()
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    h2d = (q_h[0].numel() + k_h[0].numel() + v_h[0].numel()) * 2 + 3 * bsz * 4
-    d2h = out_h[0].numel() * 4
-    return {"value": tot_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+    tot = 0
+    main = w["layout"] == "main"
+    p = list(pos)
+    for _ in range(steps):
+        tot += bytes_at(p)
+        if main:
+            p = [x + 1 for x in p]
+    h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
+    d2h = out_h.numel() * 4
+    return {"value": tot / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps}
 
 
@@ -452,8 +484,11 @@ def main():
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling runs)")
     args = ap.parse_args()
-    w = WORKLOADS[args.workload]
+    w = dict(WORKLOADS[args.workload])
+    if args.layers:
+        w["layers"] = args.layers
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -19,6 +19,7 @@
 //                   ("TurboQuant-MLX overview": butterfly pulled out of the V sum)
 //  3. merge  o = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i per query head.
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace tq {
 namespace {
@@ -623,6 +624,35 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
                           int num_blocks, const int32_t* block_table, int max_blocks, const int32_t* n_compressed,
                           const void* ring_k, const void* ring_v, const int32_t* n_buf, int max_ctx, float* out,
                           void* workspace, cudaStream_t s) {
+  if (plan.tensor_core) {
+    TcArgs t{};
+    t.q = static_cast<const __half*>(q);
+    t.pool = static_cast<const uint8_t*>(pool);
+    t.num_blocks = num_blocks;
+    t.block_table = block_table;
+    t.max_blocks = max_blocks;
+    t.n_compressed = n_compressed;
+    t.ring_k = static_cast<const __half*>(ring_k);
+    t.ring_v = static_cast<const __half*>(ring_v);
+    t.n_buf = n_buf;
+    t.max_ctx = max_ctx;
+    t.out = out;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    t.afrag = reinterpret_cast<uint4*>(ws);
+    t.parts = reinterpret_cast<float*>(ws + plan.q_bytes);
+    t.chunk_pages = plan.chunk_tokens / kPage;
+    t.n_chunks = plan.n_chunks;
+    t.n_parts = plan.n_parts;
+    t.hq = ctx->cfg.num_q_heads;
+    t.hkv = ctx->cfg.num_kv_heads;
+    t.n_rep = ctx->n_rep;
+    t.groups = (ctx->n_rep + kMaxRep - 1) / kMaxRep;
+    t.nrg = ctx->n_rep / t.groups;
+    t.signs = ctx->d_signs;
+    t.sketch_t = ctx->d_sketch_t;
+    t.err = ctx->d_err;
+    return launch_decode_tc(ctx, t, batch, s);
+  }
   DecArgs a;
   a.q = static_cast<const __half*>(q);
   a.batch = batch;

@@ -1,0 +1,572 @@
+// Main-layout decode attention on the tensor cores (head_dim 128, <= 8 query
+// heads per KV head and CTA).
+//
+// The n_rep query heads that share a KV head turn one decode step into a
+// small dense product per page of 16 tokens (the GQA grouping of the
+// "TurboQuant-MLX overview", GPU kernel section: n_rep), so both halves run
+// as mma.sync m16n8k16 (fp16 inputs, fp32 accumulation):
+//
+//   scores  S[16 x 16 tok] = Q'[16 x 384] . P[384 x 16 tok]
+//     rows 0..7 = heads (fp16 high part), rows 8..15 = the same heads (fp16
+//     low part, (value - high) * 2^11), so each product is good to ~22 bits;
+//     K = three bit planes of 128 coordinates: the high and the low bit of
+//     the 2-bit Lloyd-Max index and the QJL sign bit.  Each bit enters as an
+//     exact +-1.  With a symmetric 2-bit codebook, c[idx] = x a + y b for
+//     a, b = +-1 taken from the two index bits (x = (c3+c2)/2, y = (c3-c2)/2),
+//     so the Lloyd-Max dot <q_r, c[idx]> and the QJL dot <S q_r, 2 sigma - 1>
+//     are plain +-1 contractions, with -x q_r, -y q_r and -S q_r as the rows.
+//     logit = n_k (lm + sqrt(pi/2)/m n_r qjl) / sqrt(d)   (turboquant vLLM
+//     guide, section 2 step 3, unbiased inner-product estimator).
+//   values  O[16 x 128] += P'_g[16 x 16 tok] . C[16 tok x 128]
+//     P'_g = p * s_g (fp16 high / low rows), C = the 2-bit codes taken from
+//     the packed word as the exact fp16 values 1 + q/4 (one shift and one
+//     bit-select per register); O = 4 (P'_g . C) + sum_t p_t (mn_g(t) - 4 s_g(t)),
+//     i.e. the group minimum and the removal of the encoding offset enter once
+//     per group and token through an fp32 accumulator (turboquant-bench:
+//     asymmetric group quantisation).
+//
+// Work split: one CTA per (chunk of pages, KV-head group, sequence), four
+// warps per CTA, each warp walking its own pages through a 4-deep cp.async
+// pipeline with its own online-softmax state; warps combine at the end of the
+// chunk, CTAs through a split-K partial that a small merge kernel combines
+// (a sequence whose work fits one CTA is written directly).  The exact
+// recent buffer is one more work item of the same kernel, scored from the raw
+// fp16 keys and values with the same tensor-core path.
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int D = 128;
+constexpr int TILE = 12 * D + 64;  // 1600 bytes
+constexpr int NWARP = 4;
+constexpr int STAGES = 4;
+constexpr int KSTEPS = 24;         // 3 planes x 8 k-steps of 16 coordinates
+constexpr int AFRAG_U4 = KSTEPS * 32;
+constexpr size_t SMEM_A = AFRAG_U4 * sizeof(uint4);
+constexpr size_t SMEM_STAGE = (size_t)NWARP * STAGES * TILE;
+constexpr size_t SMEM_TOTAL = SMEM_A + SMEM_STAGE;
+static_assert((size_t)NWARP * kMaxRep * D * sizeof(float) <= SMEM_STAGE, "combine buffer fits the stages");
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kPartStride = D + 4;  // floats per split-K partial: o[D], m, l, pad (16-byte rows)
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+
+// Bits j and j+16 of w as an fp16 pair: +1 where the bit is clear, -1 where set.
+__device__ __forceinline__ uint32_t sgn_pair(uint32_t w, int j) {
+  return ((w << (15 - j)) & 0x80008000u) | 0x3C003C00u;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// fp16 high/low split of a pair: high = fp16(v), low = fp16((v - high) * 2^11).
+// The low part is stored scaled so that it has the magnitude of the high part
+// (|v - high| <= 2^-11 |v|): it never becomes subnormal before the high part
+// does, and the scale cannot overflow.  Rows of low parts accumulate into
+// their own accumulator rows, which are multiplied by 2^-11 in the epilogue.
+constexpr float kLoScale = 2048.f;
+constexpr float kLoUnscale = 1.f / 2048.f;
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  hi = h2_bits(h);
+  lo = h2_bits(__floats2half2_rn((a - hf.x) * kLoScale, (b - hf.y) * kLoScale));
+}
+
+__device__ __forceinline__ void cp16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ int tc_nc(const TcArgs& a, int b) {
+  const int nc = a.n_compressed[b];
+  if (nc < 0 || (nc & 15) || nc > a.max_blocks * kPage) {
+    if (threadIdx.x == 0) flag_error(a.err, TQ_DEVERR_POSITION);
+    return 0;
+  }
+  if (nc > a.max_ctx) {
+    if (threadIdx.x == 0) flag_error(a.err, TQ_DEVERR_CHUNKS);
+    return 0;
+  }
+  return nc;
+}
+
+__device__ __forceinline__ int tc_nb(const TcArgs& a, int b) {
+  if (!a.n_buf) return 0;
+  const int nb = a.n_buf[b];
+  if (nb < 0 || nb > kRing) {
+    if (threadIdx.x == 0) flag_error(a.err, TQ_DEVERR_RING);
+    return 0;
+  }
+  return nb;
+}
+
+// ------------------------------------------------------------------ prep
+// Per (KV-head group, sequence): q_r = H (D q) / sqrt(d), t = S q_r and the
+// score-side A fragments (-x q_r, -y q_r, -t as fp16 high/low rows) in the
+// exact register order of mma.sync m16n8k16: fragment (k-step, lane) holds
+//   reg0 = row g,   cols 2t..2t+1     reg1 = row g+8, cols 2t..2t+1
+//   reg2 = row g,   cols 2t+8..2t+9   reg3 = row g+8, cols 2t+8..2t+9
+// with g = lane / 4, t = lane % 4; row g is head g (high part), row g+8 the
+// same head's low part.
+__global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
+  __shared__ float qr[kMaxRep][D];
+  __shared__ float qt[kMaxRep][D];
+  const int hg = blockIdx.x, b = blockIdx.y;
+  const int kvh = hg / a.groups;
+  const int h0 = kvh * a.n_rep + (hg % a.groups) * a.nrg;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float rs = rsqrtf((float)D);
+  for (int h = warp; h < kMaxRep; h += NWARP) {
+    float x[D / 32];
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) {
+      const int c = coord_of(e, lane);
+      x[e] = h < a.nrg ? __half2float(a.q[((size_t)b * a.hq + h0 + h) * D + c]) * a.signs[c] : 0.f;
+    }
+    wht_warp<D / 32>(x, lane);
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) qr[h][coord_of(e, lane)] = x[e] * rs;
+  }
+  __syncthreads();
+  {
+    float acc[kMaxRep];
+#pragma unroll
+    for (int h = 0; h < kMaxRep; ++h) acc[h] = 0.f;
+    for (int i = 0; i < D; ++i) {
+      const float s = __ldg(a.sketch_t + (size_t)i * D + tid);
+#pragma unroll
+      for (int h = 0; h < kMaxRep; ++h) acc[h] = fmaf(s, qr[h][i], acc[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < kMaxRep; ++h) qt[h][tid] = acc[h];
+  }
+  __syncthreads();
+  uint32_t* dst = reinterpret_cast<uint32_t*>(a.afrag + ((size_t)b * a.hkv * a.groups + hg) * AFRAG_U4);
+  for (int idx = tid; idx < AFRAG_U4 * 4; idx += 128) {
+    const int r = idx & 3, L = (idx >> 2) & 31, ks = idx >> 7;
+    const int plane = ks >> 3, kb = ks & 7;
+    const int g = L >> 2, t = L & 3;
+    const int dim = kb * 16 + 2 * t + ((r >> 1) ? 8 : 0);
+    float v0, v1;
+    if (plane == 0) {
+      v0 = a.neg_x * qr[g][dim];
+      v1 = a.neg_x * qr[g][dim + 1];
+    } else if (plane == 1) {
+      v0 = a.neg_y * qr[g][dim];
+      v1 = a.neg_y * qr[g][dim + 1];
+    } else {
+      v0 = -qt[g][dim];
+      v1 = -qt[g][dim + 1];
+    }
+    uint32_t hi, lo;
+    split2(v0, v1, hi, lo);
+    dst[idx] = (r & 1) ? lo : hi;
+  }
+}
+
+// ------------------------------------------------------------------ decode
+struct WarpState {
+  float m, l;
+  float o[16][4];
+  float mn[4];
+};
+
+__device__ __forceinline__ void softmax_update(WarpState& st, float (&s)[4], float (&p)[4]) {
+  float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+  const float m_new = fmaxf(st.m, mx);
+  const float alpha = exp2f(st.m - m_new);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) p[k] = exp2f(s[k] - m_new);
+  st.l = st.l * alpha + (p[0] + p[1]) + (p[2] + p[3]);
+  st.m = m_new;
+  if (__any_sync(kFull, alpha != 1.f)) {
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) st.o[nt][r] *= alpha;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) st.mn[g] *= alpha;
+  }
+}
+
+// One compressed page (16 tokens) of the warp's KV head.
+__device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA, const uint8_t* T, WarpState& st,
+                                                int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  uint4 rw[3][2];
+#pragma unroll
+  for (int p = 0; p < 3; ++p) {
+    rw[p][0] = *reinterpret_cast<const uint4*>(T + 256 * p + g * 16);
+    rw[p][1] = *reinterpret_cast<const uint4*>(T + 256 * p + (g + 8) * 16);
+  }
+  float acc[2][2][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[i][n][r] = 0.f;
+#pragma unroll
+  for (int p = 0; p < 3; ++p) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t w0 = word_of(rw[p][0], w), w1 = word_of(rw[p][1], w);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint4 A = sA[(p * 8 + w * 2 + half) * 32 + lane];
+        const int j = 8 * half + t;
+        mma_f16(acc[p == 2][0], A, sgn_pair(w0, j), sgn_pair(w0, j + 4));
+        mma_f16(acc[p == 2][1], A, sgn_pair(w1, j), sgn_pair(w1, j + 4));
+      }
+    }
+  }
+  // logits of tokens 2t, 2t+1 (n-tile 0) and 8+2t, 9+2t (n-tile 1), log2 domain
+  const float coef = a.qjl_coef, scale = a.logit_scale;
+  float s[4];
+#pragma unroll
+  for (int n = 0; n < 2; ++n) {
+    const float2 nk = __half22float2(*reinterpret_cast<const __half2*>(T + 12 * D + (8 * n + 2 * t) * 2));
+    const float2 nr = __half22float2(*reinterpret_cast<const __half2*>(T + 12 * D + 32 + (8 * n + 2 * t) * 2));
+    const float lm0 = fmaf(acc[0][n][2], kLoUnscale, acc[0][n][0]);
+    const float lm1 = fmaf(acc[0][n][3], kLoUnscale, acc[0][n][1]);
+    const float qj0 = fmaf(acc[1][n][2], kLoUnscale, acc[1][n][0]);
+    const float qj1 = fmaf(acc[1][n][3], kLoUnscale, acc[1][n][1]);
+    s[2 * n] = nk.x * fmaf(coef * nr.x, qj0, lm0) * scale;
+    s[2 * n + 1] = nk.y * fmaf(coef * nr.y, qj1, lm1) * scale;
+  }
+  float p[4];
+  softmax_update(st, s, p);
+  // value weights p * s_g as fp16 high/low rows, minimum term per group
+  uint4 sm[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int tok = (k >> 1) * 8 + 2 * t + (k & 1);
+    sm[k] = *reinterpret_cast<const uint4*>(T + 10 * D + tok * 16);
+  }
+  uint4 Ap[4];
+#pragma unroll
+  for (int gg = 0; gg < 4; ++gg) {
+    float sc[4], mn[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t wv = word_of(sm[k], gg);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv));
+      sc[k] = f.x;
+      mn[k] = f.y;
+    }
+    float w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = p[k] * sc[k];
+    split2(w[0], w[1], Ap[gg].x, Ap[gg].y);
+    split2(w[2], w[3], Ap[gg].z, Ap[gg].w);
+    // group minimum, minus the 1 of the code encoding below (4 w, as the codes are scaled by 4)
+    float acc_mn = st.mn[gg];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc_mn = fmaf(p[k], mn[k], fmaf(-4.f, w[k], acc_mn));
+    st.mn[gg] = acc_mn;
+  }
+  // 2-bit code q of tokens 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1) as the normal fp16 value 1 + q/4
+  // (bit pattern 0x3C00 | q << 8): exact, and free of the reduced accumulation precision
+  // that subnormal operands get when products are chained.
+  const uint32_t* vq = reinterpret_cast<const uint32_t*>(T + 6 * D);
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) {
+    const uint32_t wv = vq[nt * 8 + g];
+    const uint32_t b0 = ((wv << (8 - 2 * t)) & 0x03000300u) | 0x3C003C00u;
+    const uint32_t b1 = ((wv >> (2 * t)) & 0x03000300u) | 0x3C003C00u;
+    mma_f16(st.o[nt], Ap[nt >> 2], b0, b1);
+  }
+}
+
+// One ring page: tokens t0 .. t0+cnt-1 of the exact fp16 buffer.
+__device__ __forceinline__ void page_ring(const TcArgs& a, const uint4 (&Aq)[8], const __half* rk, const __half* rv,
+                                          int t0, int cnt, WarpState& st, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  float acc[2][4];
+#pragma unroll
+  for (int n = 0; n < 2; ++n)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[n][r] = 0.f;
+  const uint32_t* k0 = reinterpret_cast<const uint32_t*>(rk + (size_t)(t0 + g) * D);
+  const uint32_t* k1 = reinterpret_cast<const uint32_t*>(rk + (size_t)(t0 + g + 8) * D);
+#pragma unroll
+  for (int kb = 0; kb < 8; ++kb) {
+    const int c = kb * 8 + t;  // uint32 index of dims kb*16 + 2t, +1
+    mma_f16(acc[0], Aq[kb], k0[c], k0[c + 4]);
+    mma_f16(acc[1], Aq[kb], k1[c], k1[c + 4]);
+  }
+  float s[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int tok = (k >> 1) * 8 + 2 * t + (k & 1);
+    s[k] = tok < cnt ? acc[k >> 1][k & 1] * a.logit_scale : -INFINITY;
+  }
+  float p[4];
+  softmax_update(st, s, p);
+  uint4 Ap;
+  split2(p[0], p[1], Ap.x, Ap.y);
+  split2(p[2], p[3], Ap.z, Ap.w);
+  const unsigned short* v16 = reinterpret_cast<const unsigned short*>(rv);
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) {
+    const int dim = nt * 8 + g;
+    uint32_t e[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int tok = (k >> 1) * 8 + 2 * t + (k & 1);
+      e[k] = tok < cnt ? (uint32_t)v16[(size_t)(t0 + tok) * D + dim] : 0u;
+    }
+    mma_f16(st.o[nt], Ap, e[0] | (e[1] << 16), e[2] | (e[3] << 16));
+  }
+}
+
+__global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint4* sA = reinterpret_cast<uint4*>(smem);
+  uint8_t* stage = smem + SMEM_A;
+  __shared__ float wm[NWARP][kMaxRep], wl[NWARP][kMaxRep];
+
+  const int part = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
+  const int kvh = hg / a.groups;
+  const int h0 = kvh * a.n_rep + (hg % a.groups) * a.nrg;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int nc = tc_nc(a, b), nb = tc_nb(a, b);
+  const int npages = nc >> 4;
+  const int nch = (npages + a.chunk_pages - 1) / a.chunk_pages;
+  const int nparts = nch + (nb > 0 ? 1 : 0);
+  if (nparts == 0) {
+    if (part == 0)
+      for (int i = tid; i < a.nrg * D; i += blockDim.x) a.out[((size_t)b * a.hq + h0) * D + i] = 0.f;
+    return;
+  }
+  const bool ring = part == a.n_chunks;
+  if (ring ? nb == 0 : part >= nch) return;
+
+  WarpState st;
+  st.m = -INFINITY;
+  st.l = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) st.o[nt][r] = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) st.mn[k] = 0.f;
+  float vscale = 4.f;  // value codes entered as 1 + q/4; the offset is removed through st.mn
+
+  if (!ring) {
+    const uint4* af = a.afrag + ((size_t)b * a.hkv * a.groups + hg) * AFRAG_U4;
+    for (int i = tid; i < AFRAG_U4; i += blockDim.x) cp16(&sA[i], &af[i]);
+    cp_commit();
+    const int pbeg = part * a.chunk_pages;
+    const int npg = min(npages, pbeg + a.chunk_pages) - pbeg;
+    const int nw = npg > warp ? (npg - warp + NWARP - 1) / NWARP : 0;
+    uint8_t* wst = stage + (size_t)warp * STAGES * TILE;
+    const int32_t* btb = a.block_table + (size_t)b * a.max_blocks;
+    auto issue = [&](int k) {
+      if (k < nw) {
+        const int blk = btb[pbeg + warp + NWARP * k];
+        if (blk >= 0 && blk < a.num_blocks) {
+          const uint8_t* gsrc = a.pool + ((size_t)blk * a.hkv + kvh) * TILE;
+          uint8_t* sdst = wst + (k % STAGES) * TILE;
+          for (int c = lane; c < TILE / 16; c += 32) cp16(sdst + c * 16, gsrc + c * 16);
+        }
+      }
+      cp_commit();
+    };
+#pragma unroll
+    for (int k = 0; k < STAGES - 1; ++k) issue(k);
+    cp_wait<STAGES - 1>();
+    __syncthreads();  // every thread's share of the A fragments has landed
+    for (int k = 0; k < nw; ++k) {
+      issue(k + STAGES - 1);
+      cp_wait<STAGES - 1>();
+      __syncwarp();
+      const int blk = btb[pbeg + warp + NWARP * k];
+      if (blk < 0 || blk >= a.num_blocks) {
+        if (lane == 0) flag_error(a.err, TQ_DEVERR_BLOCK_ID);
+        continue;
+      }
+      page_compressed(a, sA, wst + (k % STAGES) * TILE, st, lane);
+      __syncwarp();
+    }
+    cp_wait<0>();
+  } else {
+    vscale = 1.f;
+    uint4 Aq[8];
+    const __half* qh = a.q + ((size_t)b * a.hq + h0 + g) * D;
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+      const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qh);
+      Aq[kb].x = g < a.nrg ? q32[kb * 8 + t] : 0u;
+      Aq[kb].y = 0u;
+      Aq[kb].z = g < a.nrg ? q32[kb * 8 + t + 4] : 0u;
+      Aq[kb].w = 0u;
+    }
+    const __half* rk = a.ring_k + ((size_t)b * a.hkv + kvh) * kRing * D;
+    const __half* rv = a.ring_v + ((size_t)b * a.hkv + kvh) * kRing * D;
+    for (int t0 = warp * 16; t0 < nb; t0 += NWARP * 16) page_ring(a, Aq, rk, rv, t0, min(16, nb - t0), st, lane);
+  }
+
+  // ---- per-warp results: head g, dims nt*8 + 2t + {0,1}
+  float l = st.l;
+  l += __shfl_xor_sync(kFull, l, 1);
+  l += __shfl_xor_sync(kFull, l, 2);
+  float mn[4];
+#pragma unroll
+  for (int gg = 0; gg < 4; ++gg) {
+    mn[gg] = st.mn[gg];
+    mn[gg] += __shfl_xor_sync(kFull, mn[gg], 1);
+    mn[gg] += __shfl_xor_sync(kFull, mn[gg], 2);
+  }
+  __syncthreads();  // stage buffers are free: reuse them for the combine
+  float* wo = reinterpret_cast<float*>(stage);  // [NWARP][kMaxRep][D]
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int dim = nt * 8 + 2 * t + e;
+      wo[((size_t)warp * kMaxRep + g) * D + dim] = fmaf(st.o[nt][2 + e], kLoUnscale, st.o[nt][e]) * vscale + mn[nt >> 2];
+    }
+  }
+  if (t == 0) {
+    wm[warp][g] = st.m;
+    wl[warp][g] = l;
+  }
+  __syncthreads();
+  const bool direct = nparts == 1;  // sole contributor: write the output itself
+  for (int i = tid; i < a.nrg * D; i += blockDim.x) {
+    const int h = i / D, dim = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) M = fmaxf(M, wm[w][h]);
+    float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NWARP; ++w) {
+        const float f = exp2f(wm[w][h] - M);
+        num = fmaf(f, wo[((size_t)w * kMaxRep + h) * D + dim], num);
+        den = fmaf(f, wl[w][h], den);
+      }
+    }
+    if (direct) {
+      a.out[((size_t)b * a.hq + h0 + h) * D + dim] = den > 0.f ? num / den : 0.f;
+    } else {
+      float* dst = a.parts + (((size_t)b * a.hq + h0 + h) * a.n_parts + part) * kPartStride;
+      dst[dim] = num;
+      if (dim == 0) {
+        dst[D] = M;
+        dst[D + 1] = den;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ merge
+// o = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i over the split-K partials
+// of one query head (sequences with a single partial were written directly).
+// Step 1 reduces the maxima and the weighted sums over all partials with the
+// whole CTA; step 2 gives each warp a quarter of the partials and each lane
+// four consecutive dimensions (16-byte loads).
+__global__ void __launch_bounds__(128) tc_merge_kernel(TcArgs a) {
+  extern __shared__ float sw[];  // [n_parts] weights
+  __shared__ float red[NWARP][D];
+  __shared__ float s_m[NWARP], s_l[NWARP];
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nc = tc_nc(a, b), nb = tc_nb(a, b);
+  const int nch = ((nc >> 4) + a.chunk_pages - 1) / a.chunk_pages;
+  const int nparts = nch + (nb > 0 ? 1 : 0);
+  if (nparts <= 1) return;
+  const float* base = a.parts + ((size_t)b * a.hq + h) * a.n_parts * kPartStride;
+  auto part = [&](int i) { return base + (size_t)(i < nch ? i : a.n_chunks) * kPartStride; };
+  float M = -INFINITY;
+  for (int i = tid; i < nparts; i += 128) {
+    const float m = __ldcg(part(i) + D);
+    sw[i] = m;
+    M = fmaxf(M, m);
+  }
+  M = warp_max(M);
+  if (lane == 0) s_m[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
+  float den = 0.f;
+  for (int i = tid; i < nparts; i += 128) {
+    const float w = M == -INFINITY ? 0.f : exp2f(sw[i] - M);
+    sw[i] = w;
+    den = fmaf(w, __ldcg(part(i) + D + 1), den);
+  }
+  den = warp_sum(den);
+  if (lane == 0) s_l[warp] = den;
+  __syncthreads();
+  den = (s_l[0] + s_l[1]) + (s_l[2] + s_l[3]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int i = warp; i < nparts; i += NWARP) {
+    const float w = sw[i];
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(part(i)) + lane);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  }
+  reinterpret_cast<float4*>(red[warp])[lane] = acc;
+  __syncthreads();
+  const float o = (red[0][tid] + red[1][tid]) + (red[2][tid] + red[3][tid]);
+  a.out[((size_t)b * a.hq + h) * D + tid] = den > 0.f ? o / den : 0.f;
+}
+
+}  // namespace
+
+bool tc_supported(const tq_ctx* ctx) {
+  return ctx->cfg.layout == TQ_LAYOUT_MAIN && ctx->cfg.head_dim == D;
+}
+
+cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) {
+  const int hgroups = a.hkv * a.groups;
+  const float c2 = ctx->tab.c[2], c3 = ctx->tab.c[3];
+  a.neg_x = -0.5f * (c3 + c2);
+  a.neg_y = -0.5f * (c3 - c2);
+  a.qjl_coef = 1.2533141373155003f / (float)ctx->cfg.qjl_m;
+  a.logit_scale = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
+  tc_prep_kernel<<<dim3(hgroups, batch), 128, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ctx->launches++;
+  e = cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TOTAL);
+  if (e != cudaSuccess) return e;
+  prof_start(ctx, kProfDecode, s);
+  tc_decode_kernel<<<dim3(a.n_parts, hgroups, batch), 128, SMEM_TOTAL, s>>>(a);
+  prof_stop(ctx, kProfDecode, s);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ctx->launches++;
+  prof_start(ctx, kProfMerge, s);
+  tc_merge_kernel<<<dim3(a.hq, batch), 128, sizeof(float) * a.n_parts, s>>>(a);
+  prof_stop(ctx, kProfMerge, s);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) ctx->launches++;
+  return e;
+}
+
+}  // namespace tq

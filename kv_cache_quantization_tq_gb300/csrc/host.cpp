@@ -182,6 +182,17 @@ tq_status finish_create(const tq_config* cfg, std::vector<float> cent, std::vect
 
 namespace tq {
 
+// Inside stream capture an ordinary record only orders the captured work;
+// the "external" flavour makes the event a node that records a timestamp
+// each time the graph runs.
+static void record_event(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
 void prof_start(tq_ctx* ctx, int kind, cudaStream_t s) {
   if (!ctx->profiling) return;
   ProfileKind& p = ctx->prof[kind];
@@ -195,14 +206,14 @@ void prof_start(tq_ctx* ctx, int kind, cudaStream_t s) {
     }
     p.ev.push_back({a, b});
   }
-  cudaEventRecord(p.ev[p.used].first, s);
+  record_event(p.ev[p.used].first, s);
 }
 
 void prof_stop(tq_ctx* ctx, int kind, cudaStream_t s) {
   if (!ctx->profiling) return;
   ProfileKind& p = ctx->prof[kind];
   if (p.used >= 65536 || p.used >= p.ev.size()) return;
-  cudaEventRecord(p.ev[p.used].second, s);
+  record_event(p.ev[p.used].second, s);
   p.used++;
 }
 
@@ -211,17 +222,30 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
   const int d = ctx->cfg.head_dim;
   const int hkv = ctx->cfg.num_kv_heads;
   const int hq = ctx->cfg.num_q_heads;
+  const int groups = (ctx->n_rep + kMaxRep - 1) / kMaxRep;
   const int64_t pages = ((int64_t)max_ctx + kPage - 1) / kPage;
-  const int64_t total_pages = pages * batch * hkv;
-  // about 8 CTAs per SM worth of split-K chunks, each between 4 and 64 pages
-  int64_t per = (total_pages + 1215) / 1216;
-  per = std::max<int64_t>(4, std::min<int64_t>(64, per));
+  const int64_t total_pages = pages * batch * hkv * groups;
+  auto align = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  pl.tensor_core = ctx->cfg.layout == TQ_LAYOUT_MAIN && d == 128;
+  int64_t per;
+  if (pl.tensor_core) {
+    // ~6 chunks per SM (3 resident CTAs, two waves), 8..256 pages, a multiple of the 4 warps
+    per = (total_pages + 911) / 912;
+    per = std::max<int64_t>(8, std::min<int64_t>(256, per));
+    per = (per + 3) / 4 * 4;
+  } else {
+    // about 8 CTAs per SM worth of split-K chunks, each between 4 and 64 pages
+    per = (total_pages + 1215) / 1216;
+    per = std::max<int64_t>(4, std::min<int64_t>(64, per));
+  }
   pl.chunk_tokens = (int)(per * kPage);
   pl.n_chunks = (int)((pages + per - 1) / per);
   pl.n_parts = pl.n_chunks + 1;
-  auto align = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  pl.q_bytes = ctx->cfg.layout == TQ_LAYOUT_MAIN ? align(sizeof(float) * batch * hq * 2 * d) : 0;
-  pl.part_bytes = align(sizeof(float) * (size_t)batch * hq * pl.n_parts * (d + 2));
+  if (pl.tensor_core)
+    pl.q_bytes = align((size_t)batch * hkv * groups * 24 * 32 * 16);
+  else
+    pl.q_bytes = ctx->cfg.layout == TQ_LAYOUT_MAIN ? align(sizeof(float) * batch * hq * 2 * d) : 0;
+  pl.part_bytes = align(sizeof(float) * (size_t)batch * hq * pl.n_parts * (d + (pl.tensor_core ? 4 : 2)));
   pl.total = pl.q_bytes + pl.part_bytes;
   return pl;
 }

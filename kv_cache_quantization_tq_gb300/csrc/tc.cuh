@@ -1,0 +1,36 @@
+// Arguments and entry points of the tensor-core main-layout decode (decode_tc.cu).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "tq_internal.h"
+
+namespace tq {
+
+struct TcArgs {
+  const __half* q;
+  const uint8_t* pool;
+  int num_blocks;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* n_compressed;
+  const __half* ring_k;
+  const __half* ring_v;
+  const int32_t* n_buf;
+  int max_ctx;
+  float* out;
+  uint4* afrag;    // [B][Hkv * groups][24 k-steps][32 lanes] score-side A fragments
+  float* parts;    // [B][Hq][n_parts][d + 4] split-K partials (o, m, l, pad)
+  int chunk_pages, n_chunks, n_parts;
+  int hq, hkv, n_rep, nrg, groups;
+  const float* signs;
+  const float* sketch_t;
+  uint32_t* err;
+  float neg_x, neg_y, qjl_coef, logit_scale;
+};
+
+bool tc_supported(const tq_ctx* ctx);
+cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s);
+
+}  // namespace tq

@@ -56,10 +56,11 @@ void prof_stop(tq_ctx* ctx, int kind, cudaStream_t s);
 
 // Decode chunking policy shared by tq_workspace_size and tq_decode_attention.
 struct DecodePlan {
+  bool tensor_core;   // main layout, head_dim 128: decode_tc.cu
   int chunk_tokens;   // compressed tokens per split-K chunk (multiple of 16)
   int n_chunks;       // chunks for max_ctx compressed tokens
   int n_parts;        // n_chunks + 1 (ring part)
-  size_t q_bytes;     // pre-rotated queries
+  size_t q_bytes;     // pre-rotated queries / score fragments
   size_t part_bytes;  // split-K partials
   size_t total;
 };
