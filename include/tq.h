@@ -219,6 +219,27 @@ tq_status tq_decode_attention(tq_ctx* ctx, const void* q, int batch, const void*
                               const void* ring_k, const void* ring_v, const int32_t* n_buf, int max_ctx,
                               float* out, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* Decode attention without a caller-provided workspace.  This call has no
+ * counterpart in the source pages; it exists for callers that cannot allocate
+ * device memory when they decode, such as an engine that fixes its memory
+ * budget before it starts serving, a caller recording its work into a CUDA
+ * graph, or a host whose device allocator belongs to another runtime.
+ * Arguments and results are those of tq_decode_attention minus the workspace.
+ * The scratch is one file-scope device array of 16 MiB (16 << 20 bytes) that
+ * every GPU which loads libtq holds until the process exits; a call whose
+ * tq_workspace_size(batch, max_ctx) exceeds 16 MiB returns TQ_ERR_WORKSPACE
+ * and launches nothing.  The first call on a device looks up that device's
+ * address of the array (cudaGetSymbolAddress, with the device current); make
+ * that first call before any stream capture.  The call itself allocates no
+ * device memory.  All calls share the one array and it keeps the last call's
+ * contents (nothing in it needs to start at zero): calls that can overlap on
+ * the GPU (different streams, or different host threads without ordering)
+ * race on it, so keep them ordered on one stream. */
+tq_status tq_decode_attention_static(tq_ctx* ctx, const void* q, int batch, const void* pool, int num_blocks,
+                                     const int32_t* block_table, int max_blocks, const int32_t* n_compressed,
+                                     const void* ring_k, const void* ring_v, const int32_t* n_buf, int max_ctx,
+                                     float* out, cudaStream_t stream);
+
 /* ------------------------------------------------------------------ bit packing */
 
 /* Pack n codes (each < 2^bits, 1 <= bits <= 8) into a little-endian,

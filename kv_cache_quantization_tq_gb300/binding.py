@@ -78,6 +78,7 @@ _SIGS = {
     "tq_encode_flush": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _i, _vp, _i, _vp]),
     "tq_append_token": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _vp, _i, _vp]),
     "tq_decode_attention": (_i, [_vp, _vp, _i, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
+    "tq_decode_attention_static": (_i, [_vp, _vp, _i, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp]),
     "tq_pack": (_i, [_vp, _i64, _i, _vp, _vp]),
     "tq_unpack": (_i, [_vp, _i64, _i, _vp, _vp]),
     "tq_pack_host": (_i, [_vp, _i64, _i, _vp]),
@@ -306,6 +307,26 @@ class Context:
                                        _dev(n_buf, torch.int32, "n_buf"), max_ctx, _dev(out, torch.float32, "out"),
                                        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)),
                "tq_decode_attention")
+
+    def decode_attention_static(self, q, pool, block_table, n_compressed, ring_k, ring_v, n_buf, max_ctx, out,
+                                stream=None):
+        """tq_decode_attention_static: as decode_attention, scratch in the library's fixed device array."""
+        import torch
+
+        bsz = q.shape[0]
+        if tuple(q.shape) != (bsz, self.num_q_heads, self.head_dim) or tuple(out.shape) != tuple(q.shape):
+            raise ValueError("q must be [batch, Hq, d] fp16 and out [batch, Hq, d] fp32")
+        self._check_pool(pool)
+        self._check_bt(block_table, bsz)
+        _check(lib.tq_decode_attention_static(self.ptr, _dev(q, torch.float16, "q"), bsz,
+                                              _dev(pool, torch.uint8, "pool") if pool is not None else None,
+                                              pool.shape[0] if pool is not None else 0,
+                                              _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                              _dev(n_compressed, torch.int32, "n_compressed"),
+                                              _dev(ring_k, torch.float16, "ring_k"), _dev(ring_v, torch.float16, "ring_v"),
+                                              _dev(n_buf, torch.int32, "n_buf"), max_ctx,
+                                              _dev(out, torch.float32, "out"), _stream(stream)),
+               "tq_decode_attention_static")
 
     # -- diagnostics
     def device_errors(self, stream=None) -> int:
