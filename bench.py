@@ -84,6 +84,23 @@ def step_bytes(w, lengths_after_append):
     return int(tot)
 
 
+def max_over_ranks(value: float, device="cpu") -> float:
+    """The largest ``value`` over all ranks (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_rank: int, ms_max: float, world: int) -> float:
+    """Whole-job throughput: every rank moves ``bytes_per_rank`` (weak scaling) in ``ms_max``."""
+    return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -344,11 +361,9 @@ def run_gpu(args, w, rank, world):
     ms = e0.elapsed_time(e1)
     prof = [lay.ctx.profile_end() for lay in layers]  # events of the last replay
     if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, device="cuda")
         torch.distributed.barrier()
-    value = timed_bytes * world / (ms * 1e-3) / 1e9
+    value = aggregate_gbs(timed_bytes, ms, world)
 
     # dominant kernel: the fused decode kernel, timed by the library's CUDA
     # events captured into the step graph (last replayed step)
