@@ -61,8 +61,19 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint4& a, uint32_t 
 }
 
 // Bits j and j+16 of w as an fp16 pair: +1 where the bit is clear, -1 where set.
-__device__ __forceinline__ uint32_t sgn_pair(uint32_t w, int j) {
-  return ((w << (15 - j)) & 0x80008000u) | 0x3C003C00u;
+// The shift is a multiplication by mul = 2^(15 - j) (an integer multiply-add
+// runs on the FMA pipe and leaves the ALU pipe to the bit select).
+__device__ __forceinline__ uint32_t sgn_pair(uint32_t w, uint32_t mul) {
+  uint32_t x;
+  asm("mul.lo.u32 %0, %1, %2;" : "=r"(x) : "r"(w), "r"(mul));
+  return (x & 0x80008000u) | 0x3C003C00u;
+}
+
+// 2^x for x <= 0 (log2-domain softmax weights); -inf gives +0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
@@ -126,10 +137,11 @@ __device__ __forceinline__ int tc_nb(const TcArgs& a, int b) {
 //   reg2 = row g,   cols 2t+8..2t+9   reg3 = row g+8, cols 2t+8..2t+9
 // with g = lane / 4, t = lane % 4; row g is head g (high part), row g+8 the
 // same head's low part.
+constexpr int kPrepSlices = 8;
 __global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
-  __shared__ float qr[kMaxRep][D];
-  __shared__ float qt[kMaxRep][D];
-  const int hg = blockIdx.x, b = blockIdx.y;
+  __shared__ __align__(16) float qr[kMaxRep][D];
+  __shared__ float qt[kMaxRep][16];
+  const int hg = blockIdx.x, b = blockIdx.y, slice = blockIdx.z;
   const int kvh = hg / a.groups;
   const int h0 = kvh * a.n_rep + (hg % a.groups) * a.nrg;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -147,24 +159,28 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
   }
   __syncthreads();
   {
-    float acc[kMaxRep];
-#pragma unroll
-    for (int h = 0; h < kMaxRep; ++h) acc[h] = 0.f;
-    for (int i = 0; i < D; ++i) {
-      const float s = __ldg(a.sketch_t + (size_t)i * D + tid);
-#pragma unroll
-      for (int h = 0; h < kMaxRep; ++h) acc[h] = fmaf(s, qr[h][i], acc[h]);
+    // t_j for the 16 sketch rows j of this slice: thread (j, head) streams row j of S
+    const int jl = tid >> 3, h = tid & 7, j = slice * 16 + jl;
+    const float4* row = reinterpret_cast<const float4*>(a.sketch + (size_t)j * D);
+    const float4* qv = reinterpret_cast<const float4*>(qr[h]);
+    float acc = 0.f;
+#pragma unroll 8
+    for (int i4 = 0; i4 < D / 4; ++i4) {
+      const float4 sv = __ldg(row + i4);
+      const float4 q4 = qv[i4];
+      acc = fmaf(sv.x, q4.x, fmaf(sv.y, q4.y, fmaf(sv.z, q4.z, fmaf(sv.w, q4.w, acc))));
     }
-#pragma unroll
-    for (int h = 0; h < kMaxRep; ++h) qt[h][tid] = acc[h];
+    qt[h][jl] = acc;
   }
   __syncthreads();
   uint32_t* dst = reinterpret_cast<uint32_t*>(a.afrag + ((size_t)b * a.hkv * a.groups + hg) * AFRAG_U4);
-  for (int idx = tid; idx < AFRAG_U4 * 4; idx += 128) {
-    const int r = idx & 3, L = (idx >> 2) & 31, ks = idx >> 7;
+  for (int idx = tid; idx < 3 * 32 * 4; idx += 128) {
+    const int r = idx & 3, L = (idx >> 2) & 31, which = idx >> 7;  // which: 0, 1 = Lloyd-Max planes, 2 = QJL
+    const int ks = which == 0 ? slice : which == 1 ? slice + 8 : 16 + slice;
     const int plane = ks >> 3, kb = ks & 7;
     const int g = L >> 2, t = L & 3;
-    const int dim = kb * 16 + 2 * t + ((r >> 1) ? 8 : 0);
+    const int col = 2 * t + ((r >> 1) ? 8 : 0);
+    const int dim = kb * 16 + col;
     float v0, v1;
     if (plane == 0) {
       v0 = a.neg_x * qr[g][dim];
@@ -173,12 +189,12 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
       v0 = a.neg_y * qr[g][dim];
       v1 = a.neg_y * qr[g][dim + 1];
     } else {
-      v0 = -qt[g][dim];
-      v1 = -qt[g][dim + 1];
+      v0 = -qt[g][col];
+      v1 = -qt[g][col + 1];
     }
     uint32_t hi, lo;
     split2(v0, v1, hi, lo);
-    dst[idx] = (r & 1) ? lo : hi;
+    dst[(ks * 32 + L) * 4 + r] = (r & 1) ? lo : hi;
   }
 }
 
@@ -194,9 +210,9 @@ __device__ __forceinline__ void softmax_update(WarpState& st, float (&s)[4], flo
   mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
   const float m_new = fmaxf(st.m, mx);
-  const float alpha = exp2f(st.m - m_new);
+  const float alpha = fast_exp2(st.m - m_new);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) p[k] = exp2f(s[k] - m_new);
+  for (int k = 0; k < 4; ++k) p[k] = fast_exp2(s[k] - m_new);
   st.l = st.l * alpha + (p[0] + p[1]) + (p[2] + p[3]);
   st.m = m_new;
   if (__any_sync(kFull, alpha != 1.f)) {
@@ -226,6 +242,8 @@ __device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA
     for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[i][n][r] = 0.f;
+  // bit j = 8 half + t (b0) and j + 4 (b1) of each plane word, moved to bit 15
+  const uint32_t mul[4] = {1u << (15 - t), 1u << (11 - t), 1u << (7 - t), 1u << (3 - t)};
 #pragma unroll
   for (int p = 0; p < 3; ++p) {
 #pragma unroll
@@ -234,9 +252,9 @@ __device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const uint4 A = sA[(p * 8 + w * 2 + half) * 32 + lane];
-        const int j = 8 * half + t;
-        mma_f16(acc[p == 2][0], A, sgn_pair(w0, j), sgn_pair(w0, j + 4));
-        mma_f16(acc[p == 2][1], A, sgn_pair(w1, j), sgn_pair(w1, j + 4));
+        const uint32_t m0 = mul[2 * half], m1 = mul[2 * half + 1];
+        mma_f16(acc[p == 2][0], A, sgn_pair(w0, m0), sgn_pair(w0, m1));
+        mma_f16(acc[p == 2][1], A, sgn_pair(w1, m0), sgn_pair(w1, m1));
       }
     }
   }
@@ -485,14 +503,15 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
 // ------------------------------------------------------------------ merge
 // o = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i over the split-K partials
 // of one query head (sequences with a single partial were written directly).
-// Step 1 reduces the maxima and the weighted sums over all partials with the
-// whole CTA; step 2 gives each warp a quarter of the partials and each lane
-// four consecutive dimensions (16-byte loads).
+// One CTA per (query head, sequence, quarter of the dimensions): the maxima
+// and weighted sums are reduced over all partials by the whole CTA, then 16
+// slices of partials x 8 lanes of 16-byte loads cover the 32 dimensions.
+constexpr int kMergeSplit = 4;  // dimension quarters per head
 __global__ void __launch_bounds__(128) tc_merge_kernel(TcArgs a) {
   extern __shared__ float sw[];  // [n_parts] weights
-  __shared__ float red[NWARP][D];
+  __shared__ float4 red[16][8];
   __shared__ float s_m[NWARP], s_l[NWARP];
-  const int h = blockIdx.x, b = blockIdx.y;
+  const int h = blockIdx.x, b = blockIdx.y, quarter = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nc = tc_nc(a, b), nb = tc_nb(a, b);
   const int nch = ((nc >> 4) + a.chunk_pages - 1) / a.chunk_pages;
@@ -517,23 +536,34 @@ __global__ void __launch_bounds__(128) tc_merge_kernel(TcArgs a) {
     den = fmaf(w, __ldcg(part(i) + D + 1), den);
   }
   den = warp_sum(den);
+  __syncthreads();  // all weights written; s_m reads done
   if (lane == 0) s_l[warp] = den;
   __syncthreads();
   den = (s_l[0] + s_l[1]) + (s_l[2] + s_l[3]);
+  const int slice = tid >> 3, q4 = tid & 7;  // 16 partial slices, 8 float4 of this quarter
+  const int col4 = quarter * 8 + q4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-  for (int i = warp; i < nparts; i += NWARP) {
+  for (int i = slice; i < nparts; i += 16) {
     const float w = sw[i];
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(part(i)) + lane);
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(part(i)) + col4);
     acc.x = fmaf(w, v.x, acc.x);
     acc.y = fmaf(w, v.y, acc.y);
     acc.z = fmaf(w, v.z, acc.z);
     acc.w = fmaf(w, v.w, acc.w);
   }
-  reinterpret_cast<float4*>(red[warp])[lane] = acc;
+  red[slice][q4] = acc;
   __syncthreads();
-  const float o = (red[0][tid] + red[1][tid]) + (red[2][tid] + red[3][tid]);
-  a.out[((size_t)b * a.hq + h) * D + tid] = den > 0.f ? o / den : 0.f;
+  if (tid < 32) {
+    const int c = tid >> 2, comp = tid & 3;  // 8 float4 x 4 components = 32 dimensions
+    float o = 0.f;
+#pragma unroll
+    for (int sl = 0; sl < 16; ++sl) {
+      const float4 v = red[sl][c];
+      o += comp == 0 ? v.x : comp == 1 ? v.y : comp == 2 ? v.z : v.w;
+    }
+    a.out[((size_t)b * a.hq + h) * D + quarter * 32 + tid] = den > 0.f ? o / den : 0.f;
+  }
 }
 
 }  // namespace
@@ -549,7 +579,7 @@ cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) 
   a.neg_y = -0.5f * (c3 - c2);
   a.qjl_coef = 1.2533141373155003f / (float)ctx->cfg.qjl_m;
   a.logit_scale = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
-  tc_prep_kernel<<<dim3(hgroups, batch), 128, 0, s>>>(a);
+  tc_prep_kernel<<<dim3(hgroups, batch, kPrepSlices), 128, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ctx->launches++;
@@ -562,7 +592,7 @@ cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) 
   if (e != cudaSuccess) return e;
   ctx->launches++;
   prof_start(ctx, kProfMerge, s);
-  tc_merge_kernel<<<dim3(a.hq, batch), 128, sizeof(float) * a.n_parts, s>>>(a);
+  tc_merge_kernel<<<dim3(a.hq, batch, kMergeSplit), 128, sizeof(float) * a.n_parts, s>>>(a);
   prof_stop(ctx, kProfMerge, s);
   e = cudaGetLastError();
   if (e == cudaSuccess) ctx->launches++;

@@ -25,7 +25,8 @@ struct TcArgs {
   int chunk_pages, n_chunks, n_parts;
   int hq, hkv, n_rep, nrg, groups;
   const float* signs;
-  const float* sketch_t;
+  const float* sketch;    // [m][d]
+  const float* sketch_t;  // [d][m]
   uint32_t* err;
   float neg_x, neg_y, qjl_coef, logit_scale;
 };

@@ -8,7 +8,7 @@
 #include <utility>
 #include <vector>
 
-#include "../../include/tq.h"
+#include "tq.h"
 
 namespace tq {
 
@@ -16,6 +16,7 @@ constexpr int kPage = 16;        // tokens per page
 constexpr int kRing = 128;       // exact recent-token buffer
 constexpr int kGroup = 32;       // value group / key block
 constexpr int kMaxRep = 8;       // query heads handled by one decode CTA
+constexpr int kMaxChunks = 8192;  // split-K chunks per sequence (merge weights in shared memory)
 
 // Small per-context tables passed by value as kernel parameters.
 struct CodeTables {
