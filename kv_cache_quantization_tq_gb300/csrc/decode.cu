@@ -22,6 +22,11 @@
 #include "tc.cuh"
 
 namespace tq {
+
+cudaError_t launch_decode_alt_v2(tq_ctx* ctx, const void* q, const void* pool, int num_blocks,
+                                 const int32_t* block_table, int max_blocks, const int32_t* n_compressed, int max_ctx,
+                                 float* parts, int chunk_tokens, int n_chunks, int n_parts, int batch, cudaStream_t s);
+
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -42,6 +47,7 @@ struct DecArgs {
   float* qprep;  // [B][Hq][2d] (main)
   float* parts;  // [B][Hq][n_parts][d + 2]
   int chunk_tokens, n_chunks, n_parts;
+  int first_part;  // blockIdx.x + first_part = part index
   int hq, hkv, n_rep, nrg, groups;
   const float* signs;
   const float* sketch_t;
@@ -236,7 +242,7 @@ __global__ void __launch_bounds__(128) decode_main_kernel(DecArgs a) {
   __shared__ float msum[NR][G];
   __shared__ SoftState<NR> st;
 
-  const int part = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
+  const int part = blockIdx.x + a.first_part, hg = blockIdx.y, b = blockIdx.z;
   const int kvh = hg / a.groups;
   const int h0 = kvh * a.n_rep + (hg % a.groups) * a.nrg;
   const int tid = threadIdx.x;
@@ -399,7 +405,7 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
   __shared__ float ob[NR][D];
   __shared__ SoftState<NR> st;
 
-  const int part = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
+  const int part = blockIdx.x + a.first_part, hg = blockIdx.y, b = blockIdx.z;
   const int kvh = hg / a.groups;
   const int h0 = kvh * a.n_rep + (hg % a.groups) * a.nrg;
   const int tid = threadIdx.x;
@@ -566,38 +572,50 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
 }
 
 // ------------------------------------------------------------------ merge
+// grid (hq, batch, d / 32): one block per query head and 32 output dimensions.
+// The part weights 2^(m_i - M) are computed once into shared memory; each warp
+// then sums every fourth part over the block's 32 dimensions (one coalesced
+// 128-byte row per part) and the four warp sums are added at the end.
 __global__ void __launch_bounds__(128) merge_kernel(DecArgs a, int d) {
-  const int h = blockIdx.x, b = blockIdx.y;
+  extern __shared__ float sw[];  // [n_parts]
+  __shared__ float red[4][32];
+  __shared__ float s_m[4], s_l[4];
+  const int h = blockIdx.x, b = blockIdx.y, col = blockIdx.z * 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nc = seq_nc(a, b);
   const int nb = seq_nb(a, b);
-  const int nchunks = (nc + a.chunk_tokens - 1) / a.chunk_tokens;
+  const int nch = (nc + a.chunk_tokens - 1) / a.chunk_tokens;
+  const int nparts = nch + (nb > 0 ? 1 : 0);
   const float* base = a.parts + ((size_t)b * a.hq + h) * a.n_parts * (d + 2);
+  auto part = [&](int i) { return base + (size_t)(i < nch ? i : a.n_chunks) * (d + 2); };
   float M = -INFINITY;
-  for (int c = 0; c < nchunks; ++c) M = fmaxf(M, base[(size_t)c * (d + 2) + d]);
-  if (nb > 0) M = fmaxf(M, base[(size_t)a.n_chunks * (d + 2) + d]);
+  for (int i = tid; i < nparts; i += 128) {
+    const float m = part(i)[d];
+    sw[i] = m;
+    M = fmaxf(M, m);
+  }
+  M = warp_max(M);
+  if (lane == 0) s_m[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
   float den = 0.f;
-  for (int c = 0; c < nchunks; ++c) {
-    const float* p = base + (size_t)c * (d + 2);
-    if (M != -INFINITY) den += exp2f(p[d] - M) * p[d + 1];
+  for (int i = tid; i < nparts; i += 128) {
+    const float w = M == -INFINITY ? 0.f : exp2f(sw[i] - M);
+    sw[i] = w;
+    den = fmaf(w, part(i)[d + 1], den);
   }
-  if (nb > 0 && M != -INFINITY) {
-    const float* p = base + (size_t)a.n_chunks * (d + 2);
-    den += exp2f(p[d] - M) * p[d + 1];
-  }
-  float* out = a.out + ((size_t)b * a.hq + h) * d;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    float num = 0.f;
-    if (M != -INFINITY) {
-      for (int c = 0; c < nchunks; ++c) {
-        const float* p = base + (size_t)c * (d + 2);
-        num += exp2f(p[d] - M) * p[i];
-      }
-      if (nb > 0) {
-        const float* p = base + (size_t)a.n_chunks * (d + 2);
-        num += exp2f(p[d] - M) * p[i];
-      }
-    }
-    out[i] = den > 0.f ? num / den : 0.f;
+  den = warp_sum(den);
+  if (lane == 0) s_l[warp] = den;
+  __syncthreads();  // weights and s_l
+  den = (s_l[0] + s_l[1]) + (s_l[2] + s_l[3]);
+  float acc = 0.f;
+#pragma unroll 4
+  for (int i = warp; i < nparts; i += 4) acc = fmaf(sw[i], part(i)[col + lane], acc);
+  red[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    const float o = (red[0][lane] + red[1][lane]) + (red[2][lane] + red[3][lane]);
+    a.out[((size_t)b * a.hq + h) * d + col + lane] = den > 0.f ? o / den : 0.f;
   }
 }
 
@@ -649,6 +667,7 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
     t.groups = (ctx->n_rep + kMaxRep - 1) / kMaxRep;
     t.nrg = ctx->n_rep / t.groups;
     t.signs = ctx->d_signs;
+    t.sketch = ctx->d_sketch;
     t.sketch_t = ctx->d_sketch_t;
     t.err = ctx->d_err;
     return launch_decode_tc(ctx, t, batch, s);
@@ -695,19 +714,40 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
     if (e != cudaSuccess) return e;
     ctx->launches++;
   }
+  a.first_part = 0;
   dim3 grid(plan.n_parts, a.hkv * a.groups, batch);
-  prof_start(ctx, kProfDecode, s);
-  switch (d) {
-    case 64: e = launch_d<64>(a, main, grid, s); break;
-    case 128: e = launch_d<128>(a, main, grid, s); break;
-    case 256: e = launch_d<256>(a, main, grid, s); break;
-    case 512: e = launch_d<512>(a, main, grid, s); break;
+  bool done = false;
+  if (!main) {
+    // compressed chunks: warp-per-page kernel; the exact buffer (if any): the part kernel below
+    prof_start(ctx, kProfDecode, s);
+    e = launch_decode_alt_v2(ctx, q, pool, num_blocks, block_table, max_blocks, n_compressed, max_ctx, a.parts,
+                             plan.chunk_tokens, plan.n_chunks, plan.n_parts, batch, s);
+    prof_stop(ctx, kProfDecode, s);
+    if (e == cudaSuccess) {
+      ctx->launches++;
+      done = true;
+      a.first_part = plan.n_chunks;
+      grid.x = 1;
+    } else if (e != cudaErrorNotSupported) {
+      return e;
+    } else {
+      cudaGetLastError();
+    }
   }
-  prof_stop(ctx, kProfDecode, s);
-  if (e != cudaSuccess) return e;
-  ctx->launches++;
+  if (!done || n_buf) {
+    if (!done) prof_start(ctx, kProfDecode, s);
+    switch (d) {
+      case 64: e = launch_d<64>(a, main, grid, s); break;
+      case 128: e = launch_d<128>(a, main, grid, s); break;
+      case 256: e = launch_d<256>(a, main, grid, s); break;
+      case 512: e = launch_d<512>(a, main, grid, s); break;
+    }
+    if (!done) prof_stop(ctx, kProfDecode, s);
+    if (e != cudaSuccess) return e;
+    ctx->launches++;
+  }
   prof_start(ctx, kProfMerge, s);
-  merge_kernel<<<dim3(a.hq, batch), 128, 0, s>>>(a, d);
+  merge_kernel<<<dim3(a.hq, batch, d / 32), 128, sizeof(float) * plan.n_parts, s>>>(a, d);
   prof_stop(ctx, kProfMerge, s);
   e = cudaGetLastError();
   if (e == cudaSuccess) ctx->launches++;

@@ -1,0 +1,361 @@
+// Alternate-layout decode attention, one warp per page (CUDA cores).
+//
+// Keys are 8-bit affine codes per block of 32 (no rotation), values are
+// 3-bit Lloyd-Max indices of the rotated unit value with an fp16 norm
+// (vllm-metal TurboQuant guide, quantisation table).  With one query head per
+// KV head the work per byte is small, so the kernel is written to stream the
+// pages: each warp walks its own pages through a cp.async pipeline, lane l
+// owns the E = d/32 consecutive dimensions [l E, l E + E):
+//
+//   logit_t = sum_b s_b <q_b, code_b> + mn_b sum(q_b)       (per lane: its block)
+//   the 16 per-lane partials of a page are summed over the warp with a
+//   transposed butterfly (16 shuffles per page), so lane l ends with token l/2;
+//   online softmax per head; v_rot += p_t n_v,t c[idx_t] in the rotated domain;
+//   one inverse rotation per chunk ("TurboQuant-MLX overview", GPU kernel
+//   section: butterfly pulled out of the value sum).
+//
+// Split-K partials use the same layout as the main-layout kernels
+// ([d] values, max, sum; stride d + 2) and the same merge kernel.
+#include "common.cuh"
+
+namespace tq {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kWarps = 4;
+
+struct AltArgs {
+  const __half* q;
+  const uint8_t* pool;
+  int num_blocks;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* n_compressed;
+  const __half* ring_k;
+  const __half* ring_v;
+  const int32_t* n_buf;
+  int max_ctx;
+  float* parts;
+  int chunk_tokens, n_chunks, n_parts;
+  int hq, hkv, n_rep, nrg, groups;
+  const float* signs;
+  CodeTables tab;
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void cp16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// byte k of w as a float (exact): the byte becomes the low mantissa of 2^23 + byte
+__device__ __forceinline__ float byte_f(uint32_t w, int k) {
+  return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | (uint32_t)k)) - 8388608.f;
+}
+
+template <int D>
+struct AltCfg {
+  static constexpr int E = D / 32;      // dimensions per lane
+  static constexpr int TILE = 24 * D + 32;
+  static constexpr int STAGES = TILE <= 3200 ? 4 : (TILE <= 6400 ? 3 : 2);
+  static constexpr size_t SMEM = (size_t)kWarps * STAGES * TILE;
+};
+
+// Sum of 16 per-lane values over the warp; lane l returns the total of value l/2.
+__device__ __forceinline__ float transpose_sum16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool up = lane & 16;
+    const float send = up ? v[i] : v[i + 8];
+    const float keep = up ? v[i + 8] : v[i];
+    v[i] = keep + __shfl_xor_sync(kFull, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool up = lane & 8;
+    const float send = up ? v[i] : v[i + 4];
+    const float keep = up ? v[i + 4] : v[i];
+    v[i] = keep + __shfl_xor_sync(kFull, send, 8);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool up = lane & 4;
+    const float send = up ? v[i] : v[i + 2];
+    const float keep = up ? v[i + 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(kFull, send, 4);
+  }
+  {
+    const bool up = lane & 2;
+    const float send = up ? v[0] : v[1];
+    const float keep = up ? v[1] : v[0];
+    v[0] = keep + __shfl_xor_sync(kFull, send, 2);
+  }
+  return v[0] + __shfl_xor_sync(kFull, v[0], 1);
+}
+
+template <int D, int NR>
+__global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
+  using C = AltCfg<D>;
+  constexpr int E = C::E;
+  constexpr int G = D / 32;
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ float lut[8];
+  __shared__ float wm[kWarps][NR], wl[kWarps][NR];
+  __shared__ float wo[kWarps][NR][D];
+
+  const int part = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
+  const int kvh = hg / a.groups;
+  const int h0 = kvh * a.n_rep + (hg % a.groups) * a.nrg;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int nc = a.n_compressed[b];
+  if (nc < 0 || (nc & 15) || nc > a.max_blocks * kPage || nc > a.max_ctx) {
+    if (tid == 0) flag_error(a.err, nc > a.max_ctx ? TQ_DEVERR_CHUNKS : TQ_DEVERR_POSITION);
+    nc = 0;
+  }
+  const int tbeg = part * a.chunk_tokens;
+  const int tend = min(nc, tbeg + a.chunk_tokens);
+  if (tbeg >= tend) return;
+  if (tid < 8) {
+    float c = a.tab.c[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) c = tid == j ? a.tab.c[j] : c;
+    lut[tid] = c;
+  }
+
+  // queries: lane's E dimensions of every head, and their sums (per lane)
+  float qv[NR][E], qs[NR];
+#pragma unroll
+  for (int h = 0; h < NR; ++h) {
+    qs[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      qv[h][e] = h < a.nrg ? __half2float(a.q[((size_t)b * a.hq + h0 + h) * D + lane * E + e]) : 0.f;
+      qs[h] += qv[h][e];
+    }
+  }
+  float m_run[NR], l_run[NR], acc[NR][E];
+#pragma unroll
+  for (int h = 0; h < NR; ++h) {
+    m_run[h] = -INFINITY;
+    l_run[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[h][e] = 0.f;
+  }
+  __syncthreads();  // lut
+
+  const float scale = kLog2e / sqrtf((float)D);
+  const int pbeg = tbeg >> 4;
+  const int npg = (tend >> 4) - pbeg;
+  const int nw = npg > warp ? (npg - warp + kWarps - 1) / kWarps : 0;
+  uint8_t* wst = smem + (size_t)warp * C::STAGES * C::TILE;
+  const int32_t* btb = a.block_table + (size_t)b * a.max_blocks;
+  auto issue = [&](int k) {
+    if (k < nw) {
+      const int blk = btb[pbeg + warp + kWarps * k];
+      if (blk >= 0 && blk < a.num_blocks) {
+        const uint8_t* src = a.pool + ((size_t)blk * a.hkv + kvh) * C::TILE;
+        uint8_t* dst = wst + (k % C::STAGES) * C::TILE;
+        for (int c = lane; c < C::TILE / 16; c += 32) cp16(dst + c * 16, src + c * 16);
+      }
+    }
+    cp_commit();
+  };
+#pragma unroll
+  for (int k = 0; k < C::STAGES - 1; ++k) issue(k);
+  const int blk_lane = lane * E;  // first dimension of this lane
+  const int my_block = blk_lane >> 5;
+  for (int k = 0; k < nw; ++k) {
+    issue(k + C::STAGES - 1);
+    cp_wait<C::STAGES - 1>();
+    __syncwarp();
+    const int blk = btb[pbeg + warp + kWarps * k];
+    if (blk < 0 || blk >= a.num_blocks) {
+      if (lane == 0) flag_error(a.err, TQ_DEVERR_BLOCK_ID);
+      continue;
+    }
+    const uint8_t* T = wst + (k % C::STAGES) * C::TILE;
+    const __half* ksm = reinterpret_cast<const __half*>(T + 16 * D);
+    const uint32_t* vi = reinterpret_cast<const uint32_t*>(T + 18 * D);
+    const __half* vn = reinterpret_cast<const __half*>(T + 24 * D);
+#pragma unroll
+    for (int h = 0; h < NR; ++h) {
+      if (h >= a.nrg) break;
+      float sc[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const uint8_t* row = T + t * D + blk_lane;
+        float dot = 0.f;
+        if (E == 2) {
+          const uint32_t w = *reinterpret_cast<const uint16_t*>(row);
+          dot = fmaf(qv[h][0], byte_f(w, 0), qv[h][1] * byte_f(w, 1));
+        } else {
+#pragma unroll
+          for (int c = 0; c < E / 4; ++c) {
+            const uint32_t w = reinterpret_cast<const uint32_t*>(row)[c];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) dot = fmaf(qv[h][4 * c + kk], byte_f(w, kk), dot);
+          }
+        }
+        const float2 sm = __half22float2(*reinterpret_cast<const __half2*>(ksm + (t * G + my_block) * 2));
+        sc[t] = fmaf(sm.x, dot, sm.y * qs[h]);
+      }
+      const float s_tok = transpose_sum16(sc, lane) * scale;  // token lane/2
+      float mx = s_tok;
+#pragma unroll
+      for (int o = 16; o >= 2; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      const float m_new = fmaxf(m_run[h], mx);
+      const float alpha = fast_exp2(m_run[h] - m_new);
+      const float p = fast_exp2(s_tok - m_new);
+      float ps = (lane & 1) ? 0.f : p;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) ps += __shfl_xor_sync(kFull, ps, o);
+      l_run[h] = l_run[h] * alpha + ps;
+      m_run[h] = m_new;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[h][e] *= alpha;
+      const float w = p * __half2float(vn[lane >> 1]);
+      // v_rot += w_t c[idx_t] for the lane's E dimensions (3E bits at bit 3 E lane of the row)
+      const int bit0 = 3 * E * lane;
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const float wt = __shfl_sync(kFull, w, 2 * t);
+        const uint32_t* row = vi + t * (3 * D / 32);
+        const uint32_t lo = row[bit0 >> 5];
+        const uint32_t hi = ((bit0 & 31) + 3 * E > 32) ? row[(bit0 >> 5) + 1] : 0u;
+        const uint32_t bits = __funnelshift_r(lo, hi, bit0 & 31);
+        if (E <= 8) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[h][e] = fmaf(wt, lut[(bits >> (3 * e)) & 7u], acc[h][e]);
+        } else {
+          // 48 bits: second part from the following word pair
+          const int bit1 = bit0 + 24;
+          const uint32_t lo2 = row[bit1 >> 5];
+          const uint32_t hi2 = ((bit1 & 31) + 24 > 32) ? row[(bit1 >> 5) + 1] : 0u;
+          const uint32_t bits2 = __funnelshift_r(lo2, hi2, bit1 & 31);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(wt, lut[(bits >> (3 * e)) & 7u], acc[h][e]);
+#pragma unroll
+          for (int e = 8; e < E; ++e) acc[h][e] = fmaf(wt, lut[(bits2 >> (3 * (e - 8))) & 7u], acc[h][e]);
+        }
+      }
+    }
+    __syncwarp();
+  }
+  cp_wait<0>();
+
+  // per-warp results (rotated domain) -> shared memory, combine, inverse rotation, partial
+#pragma unroll
+  for (int h = 0; h < NR; ++h) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) wo[warp][h][lane * E + e] = acc[h][e];
+    if (lane == 0) {
+      wm[warp][h] = m_run[h];
+      wl[warp][h] = l_run[h];
+    }
+  }
+  __syncthreads();
+  for (int h = warp; h < a.nrg; h += kWarps) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w][h]);
+    float f[kWarps], den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      f[w] = M == -INFINITY ? 0.f : fast_exp2(wm[w][h] - M);
+      den = fmaf(f[w], wl[w][h], den);
+    }
+    float x[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int c = coord_of(e, lane);
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) s = fmaf(f[w], wo[w][h][c], s);
+      x[e] = s;
+    }
+    wht_warp<E>(x, lane);
+    float* dst = a.parts + (((size_t)b * a.hq + h0 + h) * a.n_parts + part) * (D + 2);
+    const float rs = rsqrtf((float)D);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int c = coord_of(e, lane);
+      dst[c] = x[e] * rs * a.signs[c];
+    }
+    if (lane == 0) {
+      dst[D] = M;
+      dst[D + 1] = den;
+    }
+  }
+}
+
+template <int D, int NR>
+cudaError_t launch_alt(const AltArgs& a, dim3 grid, cudaStream_t s) {
+  auto kern = decode_alt_v2_kernel<D, NR>;
+  constexpr size_t SMEM = AltCfg<D>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 128, SMEM, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Compressed parts of the alternate layout with the warp-per-page kernel, when it
+// supports (d, heads per group); returns cudaErrorNotSupported otherwise.
+cudaError_t launch_decode_alt_v2(tq_ctx* ctx, const void* q, const void* pool, int num_blocks,
+                                 const int32_t* block_table, int max_blocks, const int32_t* n_compressed, int max_ctx,
+                                 float* parts, int chunk_tokens, int n_chunks, int n_parts, int batch, cudaStream_t s) {
+  AltArgs a{};
+  a.q = static_cast<const __half*>(q);
+  a.pool = static_cast<const uint8_t*>(pool);
+  a.num_blocks = num_blocks;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.n_compressed = n_compressed;
+  a.max_ctx = max_ctx;
+  a.parts = parts;
+  a.chunk_tokens = chunk_tokens;
+  a.n_chunks = n_chunks;
+  a.n_parts = n_parts;
+  a.hq = ctx->cfg.num_q_heads;
+  a.hkv = ctx->cfg.num_kv_heads;
+  a.n_rep = ctx->n_rep;
+  a.groups = (ctx->n_rep + kMaxRep - 1) / kMaxRep;
+  a.nrg = ctx->n_rep / a.groups;
+  a.signs = ctx->d_signs;
+  a.tab = ctx->tab;
+  a.err = ctx->d_err;
+  dim3 grid(n_chunks, a.hkv * a.groups, batch);
+  const int d = ctx->cfg.head_dim, nr = a.nrg;
+  if (nr == 1) {
+    switch (d) {
+      case 64: return launch_alt<64, 1>(a, grid, s);
+      case 128: return launch_alt<128, 1>(a, grid, s);
+      case 256: return launch_alt<256, 1>(a, grid, s);
+      case 512: return launch_alt<512, 1>(a, grid, s);
+    }
+  } else if (nr == 2) {
+    switch (d) {
+      case 64: return launch_alt<64, 2>(a, grid, s);
+      case 128: return launch_alt<128, 2>(a, grid, s);
+      case 256: return launch_alt<256, 2>(a, grid, s);
+    }
+  } else if (nr <= 4) {
+    if (d == 64) return launch_alt<64, 4>(a, grid, s);
+    if (d == 128) return launch_alt<128, 4>(a, grid, s);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace tq

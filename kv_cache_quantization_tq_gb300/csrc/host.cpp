@@ -238,6 +238,9 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
     per = (total_pages + 1215) / 1216;
     per = std::max<int64_t>(4, std::min<int64_t>(64, per));
   }
+  // at most kMaxChunks chunks per sequence: the merge keeps one weight per part in shared memory
+  per = std::max<int64_t>(per, (pages + kMaxChunks - 1) / kMaxChunks);
+  if (pl.tensor_core) per = (per + 3) / 4 * 4;
   pl.chunk_tokens = (int)(per * kPage);
   pl.n_chunks = (int)((pages + per - 1) / per);
   pl.n_parts = pl.n_chunks + 1;
