@@ -156,6 +156,7 @@ tq_status finish_create(const tq_config* cfg, std::vector<float> cent, std::vect
   ctx->h_signs = signs;
   ctx->h_sketch = sketch;
   bool ok = cudaGetDevice(&ctx->device) == cudaSuccess;
+  ok = ok && cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device) == cudaSuccess;
   ok = ok && cudaMalloc(&ctx->d_signs, sizeof(float) * d) == cudaSuccess;
   ok = ok && cudaMalloc(&ctx->d_err, sizeof(uint32_t)) == cudaSuccess;
   ok = ok && cudaMemcpy(ctx->d_signs, signs.data(), sizeof(float) * d, cudaMemcpyHostToDevice) == cudaSuccess;
@@ -229,9 +230,13 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
   pl.tensor_core = ctx->cfg.layout == TQ_LAYOUT_MAIN && d == 128;
   int64_t per;
   if (pl.tensor_core) {
-    // ~6 chunks per SM (3 resident CTAs, two waves), 8..256 pages, a multiple of the 4 warps
-    per = (total_pages + 911) / 912;
-    per = std::max<int64_t>(8, std::min<int64_t>(256, per));
+    // About 1.75 CTAs per SM, i.e. one wave at the occupancy the kernel gets, with 16..64 pages
+    // per chunk (4..16 per warp).  Measured on GB300 over 8K..65K-page decode steps: fewer,
+    // longer chunks leave SMs idle; shorter ones pay the per-CTA fragment load and combine
+    // more often than they gain parallelism.
+    const int64_t target = std::max<int64_t>(1, (int64_t)ctx->sm_count * 7 / 4);
+    per = (total_pages + target - 1) / target;
+    per = std::max<int64_t>(16, std::min<int64_t>(64, per));
     per = (per + 3) / 4 * 4;
   } else {
     // about 8 CTAs per SM worth of split-K chunks, each between 4 and 64 pages

@@ -34,6 +34,7 @@ struct ProfileKind {
 struct tq_ctx {
   tq_config cfg;
   int device = 0;
+  int sm_count = 152;  // multiprocessors of the context's device (split-K sizing)
   int n_rep = 1;
   int ncent = 4;
   tq::CodeTables tab{};
