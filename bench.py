@@ -101,6 +101,16 @@ def aggregate_gbs(bytes_per_rank: int, ms_max: float, world: int) -> float:
     return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
 
 
+# DRAM bytes (read + write) of one decode-kernel launch, from the ncu captures summarised in
+# profiles/ (dram__bytes_read.sum + dram__bytes_write.sum).  An entry is valid only for the
+# kernel source it was captured on; a workload without one reports null.
+NCU_TRAFFIC = {
+    ("qwen3-0.6b-32k", "tc_decode_kernel"): 13.229824e6,   # profiles/tc_decode_kernel__qwen3-0.6b-32k.md
+    ("qwen2.5-7b-b8", "tc_decode_kernel"): 108.803584e6,   # profiles/tc_decode_kernel__qwen2.5-7b-b8.md
+    ("alt-d128", "decode_alt_v2_kernel"): 411.482112e6,    # profiles/decode_alt_v2_kernel__alt-d128.md
+}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -399,7 +409,8 @@ def run_gpu(args, w, rank, world):
     per_launch_bytes = bytes_at(last_pos) / nl
     achieved = per_launch_bytes / (dec_ms / max(dec_n, 1) * 1e-3) / 1e9 if dec_n else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak if achieved else None, "traffic": None,
+                "frac": achieved / peak if achieved else None,
+                "traffic": NCU_TRAFFIC.get((args.workload, decode_kernel_name(w))),
                 "kernel": decode_kernel_name(w),
                 "peak_source": peak_kind, "launches": dec_n, "avg_launch_us": dec_ms / max(dec_n, 1) * 1e3,
                 "merge_us_per_launch": sum(p["merge_ms"] for p in prof) / max(dec_n, 1) * 1e3,
