@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
   __shared__ float lut[8];
   __shared__ float wm[kWarps][NR], wl[kWarps][NR];
   __shared__ float wo[kWarps][NR][D];
+  __shared__ int sblk[kWarps][C::STAGES];
 
   const int part = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int kvh = hg / a.groups;
@@ -160,9 +161,11 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
   const int nw = npg > warp ? (npg - warp + kWarps - 1) / kWarps : 0;
   uint8_t* wst = smem + (size_t)warp * C::STAGES * C::TILE;
   const int32_t* btb = a.block_table + (size_t)b * a.max_blocks;
-  auto issue = [&](int k) {
+  // block id of the next page to copy read one page ahead; ids of pages in flight per warp
+  auto blk_of = [&](int k) { return k < nw ? __ldg(btb + pbeg + warp + kWarps * k) : -1; };
+  auto issue = [&](int k, int blk) {
     if (k < nw) {
-      const int blk = btb[pbeg + warp + kWarps * k];
+      if (lane == 0) sblk[warp][k % C::STAGES] = blk;
       if (blk >= 0 && blk < a.num_blocks) {
         const uint8_t* src = a.pool + ((size_t)blk * a.hkv + kvh) * C::TILE;
         uint8_t* dst = wst + (k % C::STAGES) * C::TILE;
@@ -172,14 +175,18 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
     cp_commit();
   };
 #pragma unroll
-  for (int k = 0; k < C::STAGES - 1; ++k) issue(k);
+  for (int k = 0; k < C::STAGES - 1; ++k) issue(k, blk_of(k));
+  int nxt = blk_of(C::STAGES - 1);
   const int blk_lane = lane * E;  // first dimension of this lane
   const int my_block = blk_lane >> 5;
   for (int k = 0; k < nw; ++k) {
-    issue(k + C::STAGES - 1);
+    __syncwarp();  // every lane is done with the slot and stage that are refilled next
+    const int cur = nxt;
+    nxt = blk_of(k + C::STAGES);
+    issue(k + C::STAGES - 1, cur);
     cp_wait<C::STAGES - 1>();
     __syncwarp();
-    const int blk = btb[pbeg + warp + kWarps * k];
+    const int blk = sblk[warp][k % C::STAGES];
     if (blk < 0 || blk >= a.num_blocks) {
       if (lane == 0) flag_error(a.err, TQ_DEVERR_BLOCK_ID);
       continue;

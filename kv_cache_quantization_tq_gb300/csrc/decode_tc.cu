@@ -363,6 +363,7 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
   uint4* sA = reinterpret_cast<uint4*>(smem);
   uint8_t* stage = smem + SMEM_A;
   __shared__ float wm[NWARP][kMaxRep], wl[NWARP][kMaxRep];
+  __shared__ int sblk[NWARP][STAGES];
 
   const int part = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int kvh = hg / a.groups;
@@ -401,9 +402,13 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
     const int nw = npg > warp ? (npg - warp + NWARP - 1) / NWARP : 0;
     uint8_t* wst = stage + (size_t)warp * STAGES * TILE;
     const int32_t* btb = a.block_table + (size_t)b * a.max_blocks;
-    auto issue = [&](int k) {
+    // Block ids: the id of the next page to copy is read one page ahead, so the table read
+    // never holds up a copy (or the compute queued behind it); the ids of the pages in flight
+    // are kept per warp in shared memory.
+    auto blk_of = [&](int k) { return k < nw ? __ldg(btb + pbeg + warp + NWARP * k) : -1; };
+    auto issue = [&](int k, int blk) {
       if (k < nw) {
-        const int blk = btb[pbeg + warp + NWARP * k];
+        if (lane == 0) sblk[warp][k % STAGES] = blk;
         if (blk >= 0 && blk < a.num_blocks) {
           const uint8_t* gsrc = a.pool + ((size_t)blk * a.hkv + kvh) * TILE;
           uint8_t* sdst = wst + (k % STAGES) * TILE;
@@ -413,14 +418,18 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
       cp_commit();
     };
 #pragma unroll
-    for (int k = 0; k < STAGES - 1; ++k) issue(k);
+    for (int k = 0; k < STAGES - 1; ++k) issue(k, blk_of(k));
+    int nxt = blk_of(STAGES - 1);
     cp_wait<STAGES - 1>();
     __syncthreads();  // every thread's share of the A fragments has landed
     for (int k = 0; k < nw; ++k) {
-      issue(k + STAGES - 1);
+      __syncwarp();  // every lane is done with the slot and stage that are refilled next
+      const int cur = nxt;
+      nxt = blk_of(k + STAGES);
+      issue(k + STAGES - 1, cur);
       cp_wait<STAGES - 1>();
       __syncwarp();
-      const int blk = btb[pbeg + warp + NWARP * k];
+      const int blk = sblk[warp][k % STAGES];
       if (blk < 0 || blk >= a.num_blocks) {
         if (lane == 0) flag_error(a.err, TQ_DEVERR_BLOCK_ID);
         continue;
