@@ -240,6 +240,28 @@ tq_status tq_decode_attention_static(tq_ctx* ctx, const void* q, int batch, cons
                                      const void* ring_k, const void* ring_v, const int32_t* n_buf, int max_ctx,
                                      float* out, cudaStream_t stream);
 
+/* Prefill materialisation: the compressed history read back as dense fp16
+ * keys and values (vllm-metal TurboQuant guide, advanced settings: history
+ * pages dequantised to fp16/bf16 before a long prefill).  Keys are the
+ * reconstruction the decode estimator stands for, k^ = n_k D H x / sqrt(d)
+ * with x = c[idx] + sqrt(pi/2)/m n_r S^T (2 sigma - 1) (turboquant vLLM
+ * guide, section 2 steps 2-3); values are mn + s q (main layout); in the
+ * alternate layout keys are mn + s q and values n_v D H c[idx] / sqrt(d)
+ * (vllm-metal TurboQuant guide, quantisation table).
+ *   pool, block_table, max_blocks, num_blocks   as for tq_decode_attention
+ *   n_compressed  device int32 [batch]: tokens 0..n-1 read from the pool; a
+ *                 multiple of 16, at most min(max_tokens, 16 max_blocks)
+ *   ring_k/v      device fp16 [batch][Hkv][ring_capacity][d] and
+ *   n_buf         device int32 [batch], or all NULL: ring slots
+ *                 0..n_buf-1 are copied to rows n .. n+n_buf-1
+ *   k_out, v_out  device fp16 [batch][Hkv][max_tokens][d], 16-byte aligned;
+ *                 rows past n + n_buf are not written
+ * Bad device values (lengths, block ids, ring counts) skip the affected rows
+ * and set bits of the device error word. */
+tq_status tq_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, const int32_t* block_table, int max_blocks,
+                        const int32_t* n_compressed, const void* ring_k, const void* ring_v, const int32_t* n_buf,
+                        int batch, int max_tokens, void* k_out, void* v_out, cudaStream_t stream);
+
 /* ------------------------------------------------------------------ bit packing */
 
 /* Pack n codes (each < 2^bits, 1 <= bits <= 8) into a little-endian,

@@ -79,6 +79,7 @@ _SIGS = {
     "tq_append_token": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _vp, _i, _vp]),
     "tq_decode_attention": (_i, [_vp, _vp, _i, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "tq_decode_attention_static": (_i, [_vp, _vp, _i, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp]),
+    "tq_dequantize": (_i, [_vp, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp]),
     "tq_pack": (_i, [_vp, _i64, _i, _vp, _vp]),
     "tq_unpack": (_i, [_vp, _i64, _i, _vp, _vp]),
     "tq_pack_host": (_i, [_vp, _i64, _i, _vp]),
@@ -327,6 +328,26 @@ class Context:
                                               _dev(n_buf, torch.int32, "n_buf"), max_ctx,
                                               _dev(out, torch.float32, "out"), _stream(stream)),
                "tq_decode_attention_static")
+
+    def dequantize(self, pool, block_table, n_compressed, k_out, v_out, ring_k=None, ring_v=None, n_buf=None,
+                   stream=None):
+        """tq_dequantize: rows 0..n_compressed[b]-1 of k_out / v_out [batch, Hkv, max_tokens, d] (fp16) from
+        the pool, followed by the n_buf[b] ring tokens when a ring is given."""
+        import torch
+
+        bsz = k_out.shape[0]
+        shape = (bsz, self.num_kv_heads, k_out.shape[2], self.head_dim)
+        if tuple(k_out.shape) != shape or tuple(v_out.shape) != shape:
+            raise ValueError("k_out and v_out must be [batch, Hkv, max_tokens, d] fp16")
+        self._check_pool(pool)
+        self._check_bt(block_table, bsz)
+        _check(lib.tq_dequantize(self.ptr, _dev(pool, torch.uint8, "pool"), pool.shape[0],
+                                 _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                 _dev(n_compressed, torch.int32, "n_compressed"),
+                                 _dev(ring_k, torch.float16, "ring_k"), _dev(ring_v, torch.float16, "ring_v"),
+                                 _dev(n_buf, torch.int32, "n_buf"), bsz, k_out.shape[2],
+                                 _dev(k_out, torch.float16, "k_out"), _dev(v_out, torch.float16, "v_out"),
+                                 _stream(stream)), "tq_dequantize")
 
     # -- diagnostics
     def device_errors(self, stream=None) -> int:

@@ -421,6 +421,19 @@ tq_status tq_decode_attention(tq_ctx* ctx, const void* q, int batch, const void*
                                        ring_k, ring_v, n_buf, max_ctx, out, workspace, stream));
 }
 
+tq_status tq_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, const int32_t* block_table, int max_blocks,
+                        const int32_t* n_compressed, const void* ring_k, const void* ring_v, const int32_t* n_buf,
+                        int batch, int max_tokens, void* k_out, void* v_out, cudaStream_t stream) {
+  if (!ctx || batch < 0 || max_blocks < 0 || num_blocks < 0 || max_tokens < 0) return TQ_ERR_INVALID_ARG;
+  if (batch == 0 || max_tokens == 0) return TQ_OK;
+  if (!k_out || !v_out || !n_compressed || !block_table || !pool) return TQ_ERR_INVALID_ARG;
+  if (n_buf && (!ring_k || !ring_v)) return TQ_ERR_INVALID_ARG;
+  if ((((uintptr_t)k_out) | ((uintptr_t)v_out)) & 15) return TQ_ERR_INVALID_ARG;
+  if (n_buf && ((((uintptr_t)ring_k) | ((uintptr_t)ring_v)) & 15)) return TQ_ERR_INVALID_ARG;
+  return cuda_status(tq::launch_dequantize(ctx, pool, num_blocks, block_table, max_blocks, n_compressed, ring_k,
+                                           ring_v, n_buf, batch, max_tokens, k_out, v_out, stream));
+}
+
 tq_status tq_pack(const uint8_t* codes, int64_t n, int bits, void* dst, cudaStream_t stream) {
   if (n < 0 || bits < 1 || bits > 8) return TQ_ERR_INVALID_ARG;
   if (n == 0) return TQ_OK;

@@ -79,6 +79,10 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
                           int num_blocks, const int32_t* block_table, int max_blocks, const int32_t* n_compressed,
                           const void* ring_k, const void* ring_v, const int32_t* n_buf, int max_ctx, float* out,
                           void* workspace, cudaStream_t s);
+cudaError_t launch_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, const int32_t* block_table,
+                              int max_blocks, const int32_t* n_tokens, const void* ring_k, const void* ring_v,
+                              const int32_t* n_buf, int batch, int max_tokens, void* k_out, void* v_out,
+                              cudaStream_t s);
 cudaError_t launch_pack(const uint8_t* codes, int64_t n, int bits, void* dst, cudaStream_t s);
 cudaError_t launch_unpack(const void* src, int64_t n, int bits, uint8_t* codes, cudaStream_t s);
 

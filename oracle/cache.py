@@ -97,3 +97,45 @@ def read_alt(pool, block_table, b, n_c, d):
         val = np.moveaxis(val, 1, 0)
         out[key] = val.reshape((val.shape[0], npg * layout.P) + val.shape[3:])
     return out
+
+
+def materialize_main(pool, block_table, b, n_c, ring_k, ring_v, n_buf, signs, centroids, s_mat, d):
+    """Dense history of sequence b as float64 (k, v) [Hkv, n_c + n_buf, d] (main layout).
+
+    Prefill materialisation (vllm-metal TurboQuant guide, advanced settings): the
+    compressed tokens become the explicit reconstruction k^ (quant.dequant_keys) and
+    mn + s q (quant.group_dequant); the ring tokens follow unchanged.
+    """
+    f = read_main(pool, block_table, b, n_c, d) if n_c else None
+    hkv = pool.shape[1]
+    ks, vs = [], []
+    for g in range(hkv):
+        kk, vv = [], []
+        if n_c:
+            enc = {"idx": f["idx"][g], "sigma": f["sigma"][g], "n_k": f["n_k"][g], "n_r": f["n_r"][g]}
+            kk.append(quant.dequant_keys(enc, signs, centroids, s_mat))
+            vv.append(quant.group_dequant(f["vq"][g], f["vs"][g], f["vmn"][g], 32))
+        if n_buf:
+            kk.append(np.asarray(ring_k[b, g, :n_buf], np.float64))
+            vv.append(np.asarray(ring_v[b, g, :n_buf], np.float64))
+        ks.append(np.concatenate(kk, axis=0) if kk else np.zeros((0, d)))
+        vs.append(np.concatenate(vv, axis=0) if vv else np.zeros((0, d)))
+    return np.stack(ks), np.stack(vs)
+
+
+def materialize_alt(pool, block_table, b, n_c, ring_k, ring_v, n_buf, signs, centroids3, d):
+    """Dense history of sequence b as float64 (k, v) [Hkv, n_c + n_buf, d] (alternate layout)."""
+    f = read_alt(pool, block_table, b, n_c, d) if n_c else None
+    hkv = pool.shape[1]
+    ks, vs = [], []
+    for g in range(hkv):
+        kk, vv = [], []
+        if n_c:
+            kk.append(quant.group_dequant(f["kq"][g], f["ks"][g], f["kmn"][g], 32))
+            vv.append(quant.dequant_alt_values(f["vidx"][g], f["n_v"][g], signs, centroids3))
+        if n_buf:
+            kk.append(np.asarray(ring_k[b, g, :n_buf], np.float64))
+            vv.append(np.asarray(ring_v[b, g, :n_buf], np.float64))
+        ks.append(np.concatenate(kk, axis=0) if kk else np.zeros((0, d)))
+        vs.append(np.concatenate(vv, axis=0) if vv else np.zeros((0, d)))
+    return np.stack(ks), np.stack(vs)

@@ -1,0 +1,73 @@
+"""Pins for the oracle's prefill materialisation (dense history from the compressed pool)."""
+import numpy as np
+
+import synth
+from oracle import attention, cache, codebook, layout, rng
+
+from test_oracle_attention import _setup_main
+
+
+def _attend(q16, k, v, n_kv):
+    """Plain float64 softmax attention of q [Hq, d] over k, v [Hkv, T, d]."""
+    q = np.asarray(q16, np.float64)
+    hq, d = q.shape
+    n_rep = hq // n_kv
+    out = np.zeros((hq, d))
+    for h in range(hq):
+        g = h // n_rep
+        z = k[g] @ q[h] / np.sqrt(d)
+        w = np.exp(z - z.max())
+        out[h] = w @ v[g] / w.sum()
+    return out
+
+
+def test_main_materialised_history_reproduces_the_decode_estimator():
+    # attention over (k^, v^) is the decode step computed from the packed bits (estimator form)
+    e = _setup_main(3, 2, 2, 3, 64, [300, 160])
+    args = (e["q"], e["pool"], e["bt"], e["n_c"], e["ring_k"], e["ring_v"], e["n_b"], e["sg"], e["c"], e["s"], e["hkv"])
+    ref = attention.decode_main(*args)
+    for b in range(2):
+        k, v = cache.materialize_main(e["pool"], e["bt"], b, int(e["n_c"][b]), e["ring_k"], e["ring_v"],
+                                      int(e["n_b"][b]), e["sg"], e["c"], e["s"], 64)
+        assert k.shape == (2, 300 if b == 0 else 160, 64)
+        assert np.allclose(_attend(e["q"][b], k, v, e["hkv"]), ref[b], rtol=0, atol=1e-12)
+
+
+def test_main_materialised_rows_keep_ring_exact_and_values_within_half_a_step():
+    e = _setup_main(4, 1, 2, 1, 128, [1000])
+    nc, nb = int(e["n_c"][0]), int(e["n_b"][0])
+    k, v = cache.materialize_main(e["pool"], e["bt"], 0, nc, e["ring_k"], e["ring_v"], nb, e["sg"], e["c"], e["s"], 128)
+    # ring rows are the exact fp16 tokens
+    assert np.array_equal(k[:, nc:], e["k"][0, :, nc:nc + nb].astype(np.float64))
+    assert np.array_equal(v[:, nc:], e["v"][0, :, nc:nc + nb].astype(np.float64))
+    # the asymmetric quantiser: |v^ - v| <= s/2 (plus rounding), s = (max - min)/3 per group of 32
+    v0 = e["v"][0, :, :nc].astype(np.float64).reshape(2, nc, 4, 32)
+    step = (v0.max(-1) - v0.min(-1)) / 3.0
+    err = np.abs(v[:, :nc].reshape(2, nc, 4, 32) - v0)
+    assert np.all(err <= step[..., None] * (0.5 + 2e-3) + 1e-6)
+    # keys: the reconstruction is unbiased in the sketch, so on average it points along k
+    k0 = e["k"][0, :, :nc].astype(np.float64)
+    cos = np.sum(k[:, :nc] * k0, -1) / (np.linalg.norm(k[:, :nc], axis=-1) * np.linalg.norm(k0, axis=-1))
+    assert cos.mean() > 0.8
+
+
+def test_alt_materialised_history_reproduces_the_decode():
+    seed, d, hkv, bsz = 5, 64, 2, 2
+    sg = rng.signs(seed, d)
+    c3, _ = codebook.lloyd_max(d, 3)
+    lengths = [160, 96]
+    k, v = synth.kv_alt(seed, bsz, hkv, 160, d)
+    bt = synth.block_table(seed, bsz, 10, True)
+    pool = np.zeros((bsz * 10, hkv, layout.alt_tile_bytes(d)), np.uint8)
+    for b, L in enumerate(lengths):
+        cache.encode_alt_range(pool, bt[b:b + 1], 0, k[b:b + 1, :, :L], v[b:b + 1, :, :L], sg, c3)
+    q = synth.queries(seed, bsz, hkv, d)
+    n_c = np.array(lengths)
+    ref = attention.decode_alt(q, pool, bt, n_c, None, None, None, sg, c3, hkv)
+    for b, L in enumerate(lengths):
+        kk, vv = cache.materialize_alt(pool, bt, b, L, None, None, 0, sg, c3, d)
+        assert np.allclose(_attend(q[b], kk, vv, hkv), ref[b], rtol=0, atol=1e-12)
+        # keys: 255-level affine codes per block of 32, error at most half a step
+        k0 = k[b, :, :L].astype(np.float64).reshape(hkv, L, d // 32, 32)
+        step = (k0.max(-1) - k0.min(-1)) / 255.0
+        assert np.all(np.abs(kk.reshape(hkv, L, d // 32, 32) - k0) <= step[..., None] * (0.5 + 2e-3) + 1e-6)
