@@ -12,9 +12,12 @@
 //   k^  = mn_b + s_b q ;  v^ = n_v * D (H c[idx]) / sqrt(d).
 //
 // One CTA handles TB tokens (whole pages) of one (sequence, KV head).  The
-// QJL back-projection S^T (2 sigma - 1) of all TB tokens is a CTA-wide FP32
-// product (S streamed row by row, the +-1 vectors from shared memory); the
-// rest is warp-per-token work: codes from the bit planes, the butterfly in
+// QJL back-projection Z = (2 sigma - 1) S of a page (16 tokens x m sketch
+// rows -> 16 x d) is a dense product and runs as mma.sync m16n8k16: the sign
+// bits enter as exact fp16 +-1 (A), S as an fp16 high part plus a low part
+// scaled by 2^11 (B, precomputed per context in fragment order), the low pass
+// with A = +-2^-11 so both passes share one fp32 accumulator (~22-bit S).
+// The rest is warp-per-token work: codes from the bit planes, the butterfly in
 // registers and shuffles, coalesced fp16 stores.  The exact recent buffer is
 // appended after the compressed tokens by a copy kernel.
 #include "common.cuh"
@@ -36,11 +39,43 @@ struct DqArgs {
   __half* v_out;
   int hkv;
   const float* signs;
-  const float* sketch;  // [m][d]
+  const uint4* sfrag;   // S as mma.sync B fragments (back-projection order), fp16 high / low
   CodeTables tab;
   float qjl_coef;       // sqrt(pi/2) / m
   uint32_t* err;
 };
+
+__device__ __forceinline__ void mma_f16_acc(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+
+// S (m = d rows) as B fragments of mma.sync m16n8k16 for Z = A S with k = sketch row j and
+// n = coordinate i: entry (ks, nt, lane) holds, for j0 = 16 ks + 2 (lane % 4) and
+// i = 8 nt + lane / 4, the fp16 pairs (S[j0][i], S[j0+1][i]), (S[j0+8][i], S[j0+9][i]) — high
+// parts, then the low parts (S - high) * 2^11.
+__global__ void sketch_frag_kernel(const float* __restrict__ s, int d, uint4* __restrict__ frag) {
+  const int total = (d / 16) * (d / 8) * 32;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= total) return;
+  const int lane = idx & 31, unit = idx >> 5;
+  const int nt = unit % (d / 8), ks = unit / (d / 8);
+  const int j0 = 16 * ks + 2 * (lane & 3), i = 8 * nt + (lane >> 2);
+  const int rows[4] = {j0, j0 + 1, j0 + 8, j0 + 9};
+  unsigned short hi[4], lo[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const float v = s[(size_t)rows[r] * d + i];
+    const __half h = __float2half_rn(v);
+    hi[r] = __half_as_ushort(h);
+    lo[r] = __half_as_ushort(__float2half_rn((v - __half2float(h)) * 2048.f));
+  }
+  frag[idx] = make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16, lo[0] | (uint32_t)lo[1] << 16,
+                         lo[2] | (uint32_t)lo[3] << 16);
+}
 
 // Compressed tokens of sequence b, validated against the block table and the output rows.
 __device__ __forceinline__ int dq_ntok(const DqArgs& a, int b) {
@@ -81,13 +116,13 @@ struct MainDq {
   static constexpr int TB = D >= 512 ? 16 : 32;          // tokens per CTA
   static constexpr int TILE = 12 * D + 64;
   static constexpr int THREADS = 256;
-  static constexpr int IPT = D > THREADS ? D / THREADS : 1;  // outputs i per thread
-  static constexpr int NSL = D >= THREADS ? 1 : THREADS / D;  // token slices
-  static constexpr int TPS = TB / NSL;                     // tokens per slice
-  static constexpr size_t SMEM_TILES = (size_t)(TB / 16) * TILE;
-  static constexpr size_t SMEM_PM = sizeof(float) * D * TB;   // (2 sigma - 1) as [j][token]
+  static constexpr int PAGES = TB / 16;
+  static constexpr int WPP = (THREADS / 32) / PAGES;       // warps per page
+  static constexpr int NT = (D / 8) / WPP;                 // n-tiles (8 outputs) per warp
+  static constexpr int KS = D / 16;                        // k-steps (16 sketch rows; m = d)
+  static constexpr size_t SMEM_TILES = (size_t)PAGES * TILE;
   static constexpr size_t SMEM_CORR = sizeof(float) * TB * D; // S^T (2 sigma - 1) as [token][i]
-  static constexpr size_t SMEM = SMEM_TILES + SMEM_PM + SMEM_CORR;
+  static constexpr size_t SMEM = SMEM_TILES + SMEM_CORR;
 };
 
 template <int D>
@@ -96,8 +131,7 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
   constexpr int E = C::E;
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* tiles = smem;
-  float* pmT = reinterpret_cast<float*>(smem + C::SMEM_TILES);
-  float* corr = reinterpret_cast<float*>(smem + C::SMEM_TILES + C::SMEM_PM);
+  float* corr = reinterpret_cast<float*>(smem + C::SMEM_TILES);
   __shared__ bool ok[C::TB / 16];
   const int b = blockIdx.z, h = blockIdx.y;
   const int tok0 = blockIdx.x * C::TB;
@@ -107,50 +141,50 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
   load_tiles<C::TILE>(a, tiles, b, h, tok0 >> 4, ntok >> 4, ok);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  // (2 sigma - 1) of every token, transposed: pmT[j][t]; tokens past ntok are 0
-  for (int tt = warp; tt < C::TB; tt += C::THREADS / 32) {
-    const uint32_t* ks = reinterpret_cast<const uint32_t*>(tiles + (size_t)(tt >> 4) * C::TILE + 4 * D +
-                                                           (tt & 15) * (D / 8));
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      float pm = 0.f;
-      if (tt < ntok) pm = (ks[e] >> (16 * (lane >> 4) + (lane & 15))) & 1u ? 1.f : -1.f;
-      pmT[coord_of(e, lane) * C::TB + tt] = pm;
-    }
-  }
-  __syncthreads();
-
-  // corr[t][i] = sum_j S[j][i] pm[t][j]
+  // corr[t][i] = sum_j (2 sigma_tj - 1) S[j][i]: warp -> (page, NT n-tiles); A = -(2 sigma - 1)
   {
-    const int slice = threadIdx.x / (C::THREADS / C::NSL);
-    const int i0 = threadIdx.x % (C::THREADS / C::NSL);
-    const int t0 = slice * C::TPS;
-    float acc[C::IPT][C::TPS];
+    const int page = warp / C::WPP, nt0 = (warp % C::WPP) * C::NT;
+    const int g = lane >> 2, t = lane & 3;
+    if (page * 16 < ntok) {
+      const uint32_t* ks0 = reinterpret_cast<const uint32_t*>(tiles + (size_t)page * C::TILE + 4 * D + g * (D / 8));
+      const uint32_t* ks1 = ks0 + 8 * (D / 32);  // token g + 8
+      float acc[C::NT][4];
 #pragma unroll
-    for (int u = 0; u < C::IPT; ++u)
+      for (int j = 0; j < C::NT; ++j)
 #pragma unroll
-      for (int t = 0; t < C::TPS; ++t) acc[u][t] = 0.f;
-    for (int j = 0; j < D; ++j) {
-      float sv[C::IPT];
+        for (int r = 0; r < 4; ++r) acc[j][r] = 0.f;
+#pragma unroll 2
+      for (int ks = 0; ks < C::KS; ++ks) {
+        const uint32_t w0 = ks0[ks >> 1], w1 = ks1[ks >> 1];
+        const int jj = 8 * (ks & 1) + t;
+        const uint32_t m0 = 1u << (15 - jj), m1 = 1u << (11 - jj);
+        const uint32_t x00 = w0 * m0, x10 = w1 * m0, x01 = w0 * m1, x11 = w1 * m1;
+        uint4 ah, al;  // bit set -> -1 (-2^-11), clear -> +1 (+2^-11)
+        ah.x = (x00 & 0x80008000u) | 0x3C003C00u;
+        ah.y = (x10 & 0x80008000u) | 0x3C003C00u;
+        ah.z = (x01 & 0x80008000u) | 0x3C003C00u;
+        ah.w = (x11 & 0x80008000u) | 0x3C003C00u;
+        al.x = (x00 & 0x80008000u) | 0x10001000u;
+        al.y = (x10 & 0x80008000u) | 0x10001000u;
+        al.z = (x01 & 0x80008000u) | 0x10001000u;
+        al.w = (x11 & 0x80008000u) | 0x10001000u;
+        const uint4* bf = a.sfrag + ((size_t)ks * (D / 8) + nt0) * 32 + lane;
 #pragma unroll
-      for (int u = 0; u < C::IPT; ++u) sv[u] = __ldg(a.sketch + (size_t)j * D + i0 + u * (D / C::IPT));
-      const float* pj = pmT + j * C::TB + t0;
-#pragma unroll
-      for (int t4 = 0; t4 < C::TPS; t4 += 4) {
-        const float4 p4 = *reinterpret_cast<const float4*>(pj + t4);
-#pragma unroll
-        for (int u = 0; u < C::IPT; ++u) {
-          acc[u][t4] = fmaf(sv[u], p4.x, acc[u][t4]);
-          acc[u][t4 + 1] = fmaf(sv[u], p4.y, acc[u][t4 + 1]);
-          acc[u][t4 + 2] = fmaf(sv[u], p4.z, acc[u][t4 + 2]);
-          acc[u][t4 + 3] = fmaf(sv[u], p4.w, acc[u][t4 + 3]);
+        for (int j = 0; j < C::NT; ++j) {
+          const uint4 bv = __ldg(bf + j * 32);
+          mma_f16_acc(acc[j], ah, bv.x, bv.y);
+          mma_f16_acc(acc[j], al, bv.z, bv.w);
         }
       }
+      float* c0 = corr + (page * 16 + g) * D;
+      float* c1 = c0 + 8 * D;
+#pragma unroll
+      for (int j = 0; j < C::NT; ++j) {
+        const int i = 8 * (nt0 + j) + 2 * t;
+        *reinterpret_cast<float2*>(c0 + i) = make_float2(-acc[j][0], -acc[j][1]);
+        *reinterpret_cast<float2*>(c1 + i) = make_float2(-acc[j][2], -acc[j][3]);
+      }
     }
-#pragma unroll
-    for (int u = 0; u < C::IPT; ++u)
-#pragma unroll
-      for (int t = 0; t < C::TPS; ++t) corr[(t0 + t) * D + i0 + u * (D / C::IPT)] = acc[u][t];
   }
   __syncthreads();
 
@@ -295,7 +329,7 @@ cudaError_t launch_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, con
   a.v_out = static_cast<__half*>(v_out);
   a.hkv = ctx->cfg.num_kv_heads;
   a.signs = ctx->d_signs;
-  a.sketch = ctx->d_sketch;
+  a.sfrag = ctx->d_sfrag;
   a.tab = ctx->tab;
   a.qjl_coef = (float)(1.2533141373155003 / (double)ctx->cfg.qjl_m);
   a.err = ctx->d_err;
@@ -323,6 +357,15 @@ cudaError_t launch_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, con
     ctx->launches++;
   }
   return cudaSuccess;
+}
+
+size_t sketch_frag_bytes(int d) { return (size_t)(d / 16) * (d / 8) * 32 * sizeof(uint4); }
+
+cudaError_t build_sketch_frags(const float* sketch, int d, void* frag) {
+  const int total = (d / 16) * (d / 8) * 32;
+  sketch_frag_kernel<<<(total + 255) / 256, 256>>>(sketch, d, static_cast<uint4*>(frag));
+  cudaError_t e = cudaGetLastError();
+  return e != cudaSuccess ? e : cudaDeviceSynchronize();
 }
 
 }  // namespace tq

@@ -42,6 +42,7 @@ struct tq_ctx {
   float* d_signs = nullptr;     // [d]
   float* d_sketch = nullptr;    // [m][d]
   float* d_sketch_t = nullptr;  // [d][m]
+  uint4* d_sfrag = nullptr;     // S as fp16 high/low mma.sync B fragments (back-projection)
   uint32_t* d_err = nullptr;    // device error word
   int64_t launches = 0;
   bool profiling = false;
@@ -83,6 +84,8 @@ cudaError_t launch_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, con
                               int max_blocks, const int32_t* n_tokens, const void* ring_k, const void* ring_v,
                               const int32_t* n_buf, int batch, int max_tokens, void* k_out, void* v_out,
                               cudaStream_t s);
+size_t sketch_frag_bytes(int d);
+cudaError_t build_sketch_frags(const float* sketch, int d, void* frag);
 cudaError_t launch_pack(const uint8_t* codes, int64_t n, int bits, void* dst, cudaStream_t s);
 cudaError_t launch_unpack(const void* src, int64_t n, int bits, uint8_t* codes, cudaStream_t s);
 
