@@ -13,9 +13,13 @@
 // One CTA encodes up to TB tokens of one (sequence, KV head): a warp per
 // token computes norms, the rotation (registers + shuffles), the Lloyd-Max
 // indices (bit planes straight from __ballot_sync) and the value codes; the
-// QJL projection S r of all TB tokens is then a CTA-wide FP32 product with
-// the residuals staged in shared memory; finished tiles leave through
-// 16-byte stores to the pages named by the block table.
+// QJL projection z = S r of all TB tokens is then a dense product on the
+// tensor cores (mma.sync m16n8k16): the residuals are staged in shared memory
+// as fp16 high parts and low parts scaled by 2^11, S comes as precomputed
+// fragments of the same split, and z = hi*hi + 2^-11 (hi*lo + lo*hi) keeps
+// ~22 bits, far inside the margin at which a sign may legitimately differ;
+// finished tiles leave through 16-byte stores to the pages named by the block
+// table.
 #include "common.cuh"
 
 namespace tq {
@@ -33,10 +37,42 @@ struct EncArgs {
   int num_blocks;
   int hkv;
   const float* signs;
-  const float* sketch_t;  // [d][m]
+  const uint4* sfrag;     // S^T as mma.sync B fragments (k = coordinate, n = sketch row), hi / lo
   CodeTables tab;
   uint32_t* err;
 };
+
+__device__ __forceinline__ void mma_f16_acc(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+
+// S^T as B fragments of mma.sync m16n8k16 for z = r S^T with k = coordinate i and n = sketch
+// row j: entry (ks, nt, lane) holds, for i0 = 16 ks + 2 (lane % 4) and j = 8 nt + lane / 4, the
+// fp16 pairs (S[j][i0], S[j][i0+1]), (S[j][i0+8], S[j][i0+9]) — high parts, then the low parts
+// (S - high) * 2^11.
+__global__ void sketch_frag_enc_kernel(const float* __restrict__ s, int d, uint4* __restrict__ frag) {
+  const int total = (d / 16) * (d / 8) * 32;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= total) return;
+  const int lane = idx & 31, unit = idx >> 5;
+  const int nt = unit % (d / 8), ks = unit / (d / 8);
+  const int i0 = 16 * ks + 2 * (lane & 3), j = 8 * nt + (lane >> 2);
+  const int cols[4] = {i0, i0 + 1, i0 + 8, i0 + 9};
+  unsigned short hi[4], lo[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const float v = s[(size_t)j * d + cols[r]];
+    const __half h = __float2half_rn(v);
+    hi[r] = __half_as_ushort(h);
+    lo[r] = __half_as_ushort(__float2half_rn((v - __half2float(h)) * 2048.f));
+  }
+  frag[idx] = make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16, lo[0] | (uint32_t)lo[1] << 16,
+                         lo[2] | (uint32_t)lo[3] << 16);
+}
 
 // ------------------------------------------------------------------ main layout
 template <int D>
@@ -45,15 +81,11 @@ struct MainEnc {
   static constexpr int TB = D <= 128 ? 128 : (D == 256 ? 64 : 32);
   static constexpr int TILE = 12 * D + 64;
   static constexpr int THREADS = 256;
-  static constexpr int JT = D <= 128 ? 1 : D / 128;    // sketch rows (words) per thread
-  static constexpr int SLICE = D / JT;                 // threads sharing a token slice
-  static constexpr int NSLICE = THREADS / SLICE;
-  static constexpr int TT = TB / NSLICE;               // tokens per thread in S r
-  static constexpr size_t SMEM_R = sizeof(float) * TB * D;
+  static constexpr int RS = D + 8;                     // residual row stride (halves): conflict-free fragments
+  static constexpr size_t SMEM_R = 2 * sizeof(__half) * TB * RS;  // high and low parts
   static constexpr size_t SMEM_TILES = (size_t)(TB / 16) * TILE;
   static constexpr size_t SMEM_CODES = (size_t)TB * D;
   static constexpr size_t SMEM = SMEM_R + SMEM_TILES + SMEM_CODES;
-  static_assert(TT * JT <= 64, "accumulator budget");
 };
 
 // Copy `npages` staged tiles to the pool pages of (b, h) starting at token `start`.
@@ -78,7 +110,8 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
   using C = MainEnc<D>;
   constexpr int E = C::E;
   constexpr int TB = C::TB;
-  float* rbuf = reinterpret_cast<float*>(smem);                 // [TB][D]
+  __half* rh = reinterpret_cast<__half*>(smem);                 // [TB][RS] residual, fp16 high part
+  __half* rl = rh + TB * C::RS;                                 // [TB][RS] (r - high) * 2^11
   uint8_t* tiles = smem + C::SMEM_R;                            // [TB/16][TILE]
   uint8_t* vcodes = tiles + C::SMEM_TILES;                      // [TB][D]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -116,7 +149,9 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
       const int idx = (y >= a.tab.b[0]) + (y >= a.tab.b[1]) + (y >= a.tab.b[2]);
       const float r = y - sel4(a.tab, idx);
       rr = fmaf(r, r, rr);
-      rbuf[tt * D + coord_of(e, lane)] = r;
+      const __half r_hi = __float2half_rn(r);
+      rh[tt * C::RS + coord_of(e, lane)] = r_hi;
+      rl[tt * C::RS + coord_of(e, lane)] = __float2half_rn((r - __half2float(r_hi)) * 2048.f);
       const unsigned hi = __ballot_sync(kFull, idx >> 1);
       const unsigned lo = __ballot_sync(kFull, idx & 1);
       if (lane == 0) {
@@ -143,47 +178,63 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
   }
   __syncthreads();
 
-  // ---- phase 2: QJL sketch z = S r for all tokens, sign bits by ballot
+  // ---- phase 2: QJL sketch z = S r on the tensor cores; one unit = 16 tokens x one plane word
+  // (32 sketch rows = 4 n-tiles); sign bits gathered into the word by two shuffles
   {
-    const int slice = threadIdx.x / C::SLICE;
-    const int ts = threadIdx.x % C::SLICE;
-    const int wsl = ts >> 5;  // warp within slice
-    int jrow[C::JT];
+    constexpr int NG = 4;
+    constexpr int UNITS = (TB / 16) * (D / 32);
+    const int g = lane >> 2, t = lane & 3;
+    for (int u = warp; u < UNITS; u += C::THREADS / 32) {
+      const int tile16 = u / (D / 32), wd = u % (D / 32);
+      const int row0 = (tile16 * 16 + g) * C::RS, row1 = row0 + 8 * C::RS;
+      float acc[NG][4], cor[NG][4];
 #pragma unroll
-    for (int u = 0; u < C::JT; ++u) jrow[u] = 32 * (wsl * C::JT + u) + 2 * (lane & 15) + (lane >> 4);
-    float acc[C::JT][C::TT];
+      for (int j = 0; j < NG; ++j)
 #pragma unroll
-    for (int u = 0; u < C::JT; ++u)
+        for (int r = 0; r < 4; ++r) acc[j][r] = cor[j][r] = 0.f;
+#pragma unroll 2
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int k0 = 16 * ks + 2 * t;
+        uint4 ah, al;
+        ah.x = *reinterpret_cast<const uint32_t*>(rh + row0 + k0);
+        ah.y = *reinterpret_cast<const uint32_t*>(rh + row1 + k0);
+        ah.z = *reinterpret_cast<const uint32_t*>(rh + row0 + k0 + 8);
+        ah.w = *reinterpret_cast<const uint32_t*>(rh + row1 + k0 + 8);
+        al.x = *reinterpret_cast<const uint32_t*>(rl + row0 + k0);
+        al.y = *reinterpret_cast<const uint32_t*>(rl + row1 + k0);
+        al.z = *reinterpret_cast<const uint32_t*>(rl + row0 + k0 + 8);
+        al.w = *reinterpret_cast<const uint32_t*>(rl + row1 + k0 + 8);
+        const uint4* bf = a.sfrag + ((size_t)ks * (D / 8) + NG * wd) * 32 + lane;
 #pragma unroll
-      for (int t = 0; t < C::TT; ++t) acc[u][t] = 0.f;
-    const int t0 = slice * C::TT;
-    for (int i = 0; i < D; i += 4) {
-      float s4[C::JT][4];
-#pragma unroll
-      for (int u = 0; u < C::JT; ++u)
-#pragma unroll
-        for (int ii = 0; ii < 4; ++ii) s4[u][ii] = __ldg(a.sketch_t + (size_t)(i + ii) * D + jrow[u]);
-#pragma unroll
-      for (int t = 0; t < C::TT; ++t) {
-        const float4 r4 = *reinterpret_cast<const float4*>(rbuf + (t0 + t) * D + i);
-#pragma unroll
-        for (int u = 0; u < C::JT; ++u) {
-          acc[u][t] = fmaf(s4[u][0], r4.x, acc[u][t]);
-          acc[u][t] = fmaf(s4[u][1], r4.y, acc[u][t]);
-          acc[u][t] = fmaf(s4[u][2], r4.z, acc[u][t]);
-          acc[u][t] = fmaf(s4[u][3], r4.w, acc[u][t]);
+        for (int j = 0; j < NG; ++j) {
+          const uint4 bv = __ldg(bf + j * 32);
+          mma_f16_acc(acc[j], ah, bv.x, bv.y);
+          mma_f16_acc(cor[j], ah, bv.z, bv.w);
+          mma_f16_acc(cor[j], al, bv.x, bv.y);
         }
       }
-    }
+      // sketch row 32 wd + 8 j + 2 t + e sits at bit 16 e + 4 j + t of plane word wd
+      uint32_t w0 = 0u, w1 = 0u;  // tokens g and g + 8
 #pragma unroll
-    for (int t = 0; t < C::TT; ++t) {
-      const int tt = t0 + t;
+      for (int j = 0; j < NG; ++j) {
+        const int jj = 4 * j + t;
+        w0 |= (fmaf(cor[j][0], 1.f / 2048.f, acc[j][0]) >= 0.f ? 1u : 0u) << jj;
+        w0 |= (fmaf(cor[j][1], 1.f / 2048.f, acc[j][1]) >= 0.f ? 1u : 0u) << (16 + jj);
+        w1 |= (fmaf(cor[j][2], 1.f / 2048.f, acc[j][2]) >= 0.f ? 1u : 0u) << jj;
+        w1 |= (fmaf(cor[j][3], 1.f / 2048.f, acc[j][3]) >= 0.f ? 1u : 0u) << (16 + jj);
+      }
+      w0 |= __shfl_xor_sync(kFull, w0, 1);
+      w0 |= __shfl_xor_sync(kFull, w0, 2);
+      w1 |= __shfl_xor_sync(kFull, w1, 1);
+      w1 |= __shfl_xor_sync(kFull, w1, 2);
+      if (t == 0) {
 #pragma unroll
-      for (int u = 0; u < C::JT; ++u) {
-        const unsigned bits = __ballot_sync(kFull, acc[u][t] >= 0.f);
-        if (lane == 0 && tt < ntok) {
-          uint8_t* tile = tiles + (size_t)(tt >> 4) * C::TILE;
-          reinterpret_cast<uint32_t*>(tile + 4 * D + (tt & 15) * (D / 8))[wsl * C::JT + u] = bits;
+        for (int hh = 0; hh < 2; ++hh) {
+          const int tt = tile16 * 16 + g + 8 * hh;
+          if (tt < ntok) {
+            uint8_t* tile = tiles + (size_t)(tt >> 4) * C::TILE;
+            reinterpret_cast<uint32_t*>(tile + 4 * D + (tt & 15) * (D / 8))[wd] = hh ? w1 : w0;
+          }
         }
       }
     }
@@ -378,7 +429,7 @@ EncArgs make_args(tq_ctx* ctx, const void* k, const void* v, int src_tokens, int
   a.num_blocks = num_blocks;
   a.hkv = ctx->cfg.num_kv_heads;
   a.signs = ctx->d_signs;
-  a.sketch_t = ctx->d_sketch_t;
+  a.sfrag = ctx->d_sfrag_enc;
   a.tab = ctx->tab;
   a.err = ctx->d_err;
   return a;
@@ -424,6 +475,13 @@ cudaError_t launch_append(tq_ctx* ctx, const void* k_new, const void* v_new, con
   }
   if (e == cudaSuccess) ctx->launches++;
   return e;
+}
+
+cudaError_t build_sketch_frags_enc(const float* sketch, int d, void* frag) {
+  const int total = (d / 16) * (d / 8) * 32;
+  sketch_frag_enc_kernel<<<(total + 255) / 256, 256>>>(sketch, d, static_cast<uint4*>(frag));
+  cudaError_t e = cudaGetLastError();
+  return e != cudaSuccess ? e : cudaDeviceSynchronize();
 }
 
 }  // namespace tq

@@ -172,6 +172,8 @@ tq_status finish_create(const tq_config* cfg, std::vector<float> cent, std::vect
     ok = ok && cudaMemcpy(ctx->d_sketch_t, st.data(), sizeof(float) * m * d, cudaMemcpyHostToDevice) == cudaSuccess;
     ok = ok && cudaMalloc(&ctx->d_sfrag, tq::sketch_frag_bytes(d)) == cudaSuccess;
     ok = ok && tq::build_sketch_frags(ctx->d_sketch, d, ctx->d_sfrag) == cudaSuccess;
+    ok = ok && cudaMalloc(&ctx->d_sfrag_enc, tq::sketch_frag_bytes(d)) == cudaSuccess;
+    ok = ok && tq::build_sketch_frags_enc(ctx->d_sketch, d, ctx->d_sfrag_enc) == cudaSuccess;
   }
   if (!ok) {
     tq_destroy(ctx);
@@ -352,6 +354,7 @@ void tq_destroy(tq_ctx* ctx) {
   cudaFree(ctx->d_sketch);
   cudaFree(ctx->d_sketch_t);
   cudaFree(ctx->d_sfrag);
+  cudaFree(ctx->d_sfrag_enc);
   cudaFree(ctx->d_err);
   for (auto& p : ctx->prof)
     for (auto& e : p.ev) {

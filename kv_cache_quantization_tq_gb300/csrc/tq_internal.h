@@ -43,6 +43,7 @@ struct tq_ctx {
   float* d_sketch = nullptr;    // [m][d]
   float* d_sketch_t = nullptr;  // [d][m]
   uint4* d_sfrag = nullptr;     // S as fp16 high/low mma.sync B fragments (back-projection)
+  uint4* d_sfrag_enc = nullptr; // S^T as fp16 high/low mma.sync B fragments (encode projection)
   uint32_t* d_err = nullptr;    // device error word
   int64_t launches = 0;
   bool profiling = false;
@@ -86,6 +87,7 @@ cudaError_t launch_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, con
                               cudaStream_t s);
 size_t sketch_frag_bytes(int d);
 cudaError_t build_sketch_frags(const float* sketch, int d, void* frag);
+cudaError_t build_sketch_frags_enc(const float* sketch, int d, void* frag);
 cudaError_t launch_pack(const uint8_t* codes, int64_t n, int bits, void* dst, cudaStream_t s);
 cudaError_t launch_unpack(const void* src, int64_t n, int bits, uint8_t* codes, cudaStream_t s);
 
