@@ -105,9 +105,9 @@ def aggregate_gbs(bytes_per_rank: int, ms_max: float, world: int) -> float:
 # profiles/ (dram__bytes_read.sum + dram__bytes_write.sum).  An entry is valid only for the
 # kernel source it was captured on; a workload without one reports null.
 NCU_TRAFFIC = {
-    ("qwen3-0.6b-32k", "tc_decode_kernel"): 13.229824e6,   # profiles/tc_decode_kernel__qwen3-0.6b-32k.md
-    ("qwen2.5-7b-b8", "tc_decode_kernel"): 108.803584e6,   # profiles/tc_decode_kernel__qwen2.5-7b-b8.md
-    ("alt-d128", "decode_alt_v2_kernel"): 411.482112e6,    # profiles/decode_alt_v2_kernel__alt-d128.md
+    ("qwen3-0.6b-32k", "tc_decode_kernel"): 13230848,     # profiles/tc_decode_kernel__qwen3-0.6b-32k.md
+    ("qwen2.5-7b-b8", "tc_decode_kernel"): 108628224,     # profiles/tc_decode_kernel__qwen2.5-7b-b8.md
+    ("alt-d128", "decode_alt_v2_kernel"): 411806976,      # profiles/decode_alt_v2_kernel__alt-d128.md
 }
 
 
@@ -259,6 +259,32 @@ def encode_throughput(tq, torch, w, layers, k1, v1, reps=3):
             "ms_per_call": ms, "tokens_per_call": toks}
 
 
+def dequant_throughput(torch, w, lay, lengths, reps=3, cap=32768):
+    """Time tq_dequantize (prefill materialisation) of one layer: every sequence's compressed prefix
+    (at most ``cap`` tokens each) read back as dense fp16 K and V."""
+    bsz, hkv, d = w["batch"], w["hkv"], w["d"]
+    n_c = [min(ring_split(L)[0] if w["layout"] == "main" else L, cap) // 16 * 16 for L in lengths]
+    max_tokens = max(max(n_c), 16)
+    ncd = torch.tensor(n_c, dtype=torch.int32, device="cuda")
+    k_out = torch.empty((bsz, hkv, max_tokens, d), dtype=torch.float16, device="cuda")
+    v_out = torch.empty_like(k_out)
+    for _ in range(2):
+        lay.ctx.dequantize(lay.pool, lay.bt, ncd, k_out, v_out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        lay.ctx.dequantize(lay.pool, lay.bt, ncd, k_out, v_out)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    th = sum(n_c) * hkv
+    nbytes = th * (record_bytes(w) + 4 * d)  # compressed record in, fp16 k and v out
+    del k_out, v_out
+    return {"token_heads_per_s": th / (ms * 1e-3), "gbs": nbytes / (ms * 1e-3) / 1e9, "ms_per_call": ms,
+            "tokens_per_call": sum(n_c), "bytes_per_call": nbytes}
+
+
 class StepGraph:
     """One decode step of every layer, captured once as a CUDA graph and replayed.
 
@@ -342,6 +368,7 @@ def run_gpu(args, w, rank, world):
     lengths, k1, v1, layers = build_gpu_state(tq, torch, w, steps_total)
     encode_prefix(tq, torch, w, lengths, k1, v1, layers)
     enc = encode_throughput(tq, torch, w, layers, k1, v1)
+    deq = dequant_throughput(torch, w, layers[0], lengths)
     bsz, hq, hkv, d, nl = w["batch"], w["hq"], w["hkv"], w["d"], w["layers"]
     main = w["layout"] == "main"
     g = torch.Generator(device="cuda")
@@ -418,7 +445,7 @@ def run_gpu(args, w, rank, world):
 
     e2e = run_e2e(torch, w, layers, pos, max_ctx, ws, q, kn, vn, bytes_at)
     return {
-        "value": value, "ms_per_step": ms / args.steps, "roofline": roofline, "encode": enc, "e2e": e2e,
+        "value": value, "ms_per_step": ms / args.steps, "roofline": roofline, "encode": enc, "dequantize": deq, "e2e": e2e,
         "gpu_launches": int(launches_per_step * args.steps), "clocks": clk.summary(), "lengths": lengths,
     }
 
@@ -589,7 +616,7 @@ def main():
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
         "frac_of_hbm_peak": res["value"] / world / peak,
         "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"], "gpu_launches": res["gpu_launches"],
-        "clocks": res["clocks"], "encode": res["encode"],
+        "clocks": res["clocks"], "encode": res["encode"], "dequantize": res["dequantize"],
     }
     print(json.dumps(line))
     if world > 1:
