@@ -656,7 +656,7 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
     t.max_ctx = max_ctx;
     t.out = out;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    t.afrag = reinterpret_cast<uint4*>(ws);
+    t.afrag = plan.fused_prep ? nullptr : reinterpret_cast<uint4*>(ws);
     t.parts = reinterpret_cast<float*>(ws + plan.q_bytes);
     t.chunk_pages = plan.chunk_tokens / kPage;
     t.n_chunks = plan.n_chunks;
@@ -667,8 +667,7 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
     t.groups = (ctx->n_rep + kMaxRep - 1) / kMaxRep;
     t.nrg = ctx->n_rep / t.groups;
     t.signs = ctx->d_signs;
-    t.sketch = ctx->d_sketch;
-    t.sketch_t = ctx->d_sketch_t;
+    t.sfrag_enc = ctx->d_sfrag_enc;
     t.err = ctx->d_err;
     return launch_decode_tc(ctx, t, batch, s);
   }

@@ -129,22 +129,19 @@ __device__ __forceinline__ int tc_nb(const TcArgs& a, int b) {
   return nb;
 }
 
-// ------------------------------------------------------------------ prep
-// Per (KV-head group, sequence): q_r = H (D q) / sqrt(d), t = S q_r and the
-// score-side A fragments (-x q_r, -y q_r, -t as fp16 high/low rows) in the
-// exact register order of mma.sync m16n8k16: fragment (k-step, lane) holds
+// ------------------------------------------------------------------ query side
+// Per CTA, before its pages are scored (the first pages are already in flight):
+// q_r = H (D q) / sqrt(d) for the group's heads, t = S q_r on the tensor cores
+// (rows 0..7 = heads as fp16 high parts, rows 8..15 = their low parts x 2^11;
+// B = S^T as high and low x 2^11 fragments), and the score-side A fragments
+// (-x q_r, -y q_r, -t as fp16 high/low rows) in the exact register order of
+// mma.sync m16n8k16: fragment (k-step, lane) holds
 //   reg0 = row g,   cols 2t..2t+1     reg1 = row g+8, cols 2t..2t+1
 //   reg2 = row g,   cols 2t+8..2t+9   reg3 = row g+8, cols 2t+8..2t+9
 // with g = lane / 4, t = lane % 4; row g is head g (high part), row g+8 the
 // same head's low part.
-constexpr int kPrepSlices = 8;
-__global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
-  __shared__ __align__(16) float qr[kMaxRep][D];
-  __shared__ float qt[kMaxRep][16];
-  const int hg = blockIdx.x, b = blockIdx.y, slice = blockIdx.z;
-  const int kvh = hg / a.groups;
-  const int h0 = kvh * a.n_rep + (hg % a.groups) * a.nrg;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ __forceinline__ void build_query_frags(const TcArgs& a, int b, int h0, uint4* sA, float (*qr)[D],
+                                                  float (*qt)[D], int tid, int lane, int warp) {
   const float rs = rsqrtf((float)D);
   for (int h = warp; h < kMaxRep; h += NWARP) {
     float x[D / 32];
@@ -159,28 +156,42 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
   }
   __syncthreads();
   {
-    // t_j for the 16 sketch rows j of this slice: thread (j, head) streams row j of S
-    const int jl = tid >> 3, h = tid & 7, j = slice * 16 + jl;
-    const float4* row = reinterpret_cast<const float4*>(a.sketch + (size_t)j * D);
-    const float4* qv = reinterpret_cast<const float4*>(qr[h]);
-    float acc = 0.f;
-#pragma unroll 8
-    for (int i4 = 0; i4 < D / 4; ++i4) {
-      const float4 sv = __ldg(row + i4);
-      const float4 q4 = qv[i4];
-      acc = fmaf(sv.x, q4.x, fmaf(sv.y, q4.y, fmaf(sv.z, q4.z, fmaf(sv.w, q4.w, acc))));
+    // t[h][j] = sum_i S[j][i] q_r[h][i]; warp w covers sketch rows 32w .. 32w+31
+    const int g = lane >> 2, t = lane & 3;
+    float ch[4][4], cl[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) ch[j][r] = cl[j][r] = 0.f;
+#pragma unroll 2
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int k0 = 16 * ks + 2 * t;
+      uint4 A;
+      split2(qr[g][k0], qr[g][k0 + 1], A.x, A.y);
+      split2(qr[g][k0 + 8], qr[g][k0 + 9], A.z, A.w);
+      const uint4* bf = a.sfrag_enc + ((size_t)ks * (D / 8) + 4 * warp) * 32 + lane;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 bv = __ldg(bf + j * 32);
+        mma_f16(ch[j], A, bv.x, bv.y);
+        mma_f16(cl[j], A, bv.z, bv.w);
+      }
     }
-    qt[h][jl] = acc;
+    // high x high + 2^-11 (low x high + high x low); low x low (2^-22) is dropped
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = 32 * warp + 8 * j + 2 * t;
+      qt[g][col] = fmaf(ch[j][2] + cl[j][0], kLoUnscale, ch[j][0]);
+      qt[g][col + 1] = fmaf(ch[j][3] + cl[j][1], kLoUnscale, ch[j][1]);
+    }
   }
   __syncthreads();
-  uint32_t* dst = reinterpret_cast<uint32_t*>(a.afrag + ((size_t)b * a.hkv * a.groups + hg) * AFRAG_U4);
-  for (int idx = tid; idx < 3 * 32 * 4; idx += 128) {
-    const int r = idx & 3, L = (idx >> 2) & 31, which = idx >> 7;  // which: 0, 1 = Lloyd-Max planes, 2 = QJL
-    const int ks = which == 0 ? slice : which == 1 ? slice + 8 : 16 + slice;
+  uint32_t* dst = reinterpret_cast<uint32_t*>(sA);
+  for (int idx = tid; idx < KSTEPS * 32 * 2; idx += NWARP * 32) {
+    const int half = idx & 1, L = (idx >> 1) & 31, ks = idx >> 6;  // k-step: 0..7 high bit, 8..15 low, 16..23 QJL
     const int plane = ks >> 3, kb = ks & 7;
     const int g = L >> 2, t = L & 3;
-    const int col = 2 * t + ((r >> 1) ? 8 : 0);
-    const int dim = kb * 16 + col;
+    const int dim = kb * 16 + 2 * t + 8 * half;
     float v0, v1;
     if (plane == 0) {
       v0 = a.neg_x * qr[g][dim];
@@ -189,12 +200,79 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
       v0 = a.neg_y * qr[g][dim];
       v1 = a.neg_y * qr[g][dim + 1];
     } else {
-      v0 = -qt[g][col];
-      v1 = -qt[g][col + 1];
+      v0 = -qt[g][dim];
+      v1 = -qt[g][dim + 1];
     }
     uint32_t hi, lo;
     split2(v0, v1, hi, lo);
-    dst[(ks * 32 + L) * 4 + r] = (r & 1) ? lo : hi;
+    dst[(ks * 32 + L) * 4 + 2 * half] = hi;
+    dst[(ks * 32 + L) * 4 + 2 * half + 1] = lo;
+  }
+  __syncthreads();
+}
+
+// When the decode grid is too large for every CTA to build its own fragments they are built
+// once per (KV-head group, sequence) into the workspace, split over kPrepSlices CTAs: slice s
+// writes k-steps s, 8 + s and 16 + s, i.e. sketch rows 16 s .. 16 s + 15 of t (two MMA n-tiles).
+constexpr int kPrepSlices = 8;
+__global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
+  __shared__ __align__(16) float qr[kMaxRep][D];
+  __shared__ float qt[kMaxRep][16];
+  const int hg = blockIdx.x, b = blockIdx.y, slice = blockIdx.z;
+  const int h0 = (hg / a.groups) * a.n_rep + (hg % a.groups) * a.nrg;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const float rs = rsqrtf((float)D);
+  for (int h = warp; h < kMaxRep; h += NWARP) {
+    float x[D / 32];
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) {
+      const int c = coord_of(e, lane);
+      x[e] = h < a.nrg ? __half2float(a.q[((size_t)b * a.hq + h0 + h) * D + c]) * a.signs[c] : 0.f;
+    }
+    wht_warp<D / 32>(x, lane);
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) qr[h][coord_of(e, lane)] = x[e] * rs;
+  }
+  __syncthreads();
+  if (warp < 2) {
+    float ch[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int k0 = 16 * ks + 2 * t;
+      uint4 A;
+      split2(qr[g][k0], qr[g][k0 + 1], A.x, A.y);
+      split2(qr[g][k0 + 8], qr[g][k0 + 9], A.z, A.w);
+      const uint4 bv = __ldg(a.sfrag_enc + ((size_t)ks * (D / 8) + 2 * slice + warp) * 32 + lane);
+      mma_f16(ch, A, bv.x, bv.y);
+      mma_f16(cl, A, bv.z, bv.w);
+    }
+    const int col = 8 * warp + 2 * t;
+    qt[g][col] = fmaf(ch[2] + cl[0], kLoUnscale, ch[0]);
+    qt[g][col + 1] = fmaf(ch[3] + cl[1], kLoUnscale, ch[1]);
+  }
+  __syncthreads();
+  uint32_t* dst = reinterpret_cast<uint32_t*>(a.afrag + ((size_t)b * a.hkv * a.groups + hg) * AFRAG_U4);
+  for (int idx = tid; idx < 3 * 32 * 2; idx += NWARP * 32) {
+    const int half = idx & 1, L = (idx >> 1) & 31, plane = idx >> 6;
+    const int ks = plane * 8 + slice;
+    const int gg = L >> 2, tt = L & 3;
+    const int col = 2 * tt + 8 * half, dim = slice * 16 + col;
+    float v0, v1;
+    if (plane == 0) {
+      v0 = a.neg_x * qr[gg][dim];
+      v1 = a.neg_x * qr[gg][dim + 1];
+    } else if (plane == 1) {
+      v0 = a.neg_y * qr[gg][dim];
+      v1 = a.neg_y * qr[gg][dim + 1];
+    } else {
+      v0 = -qt[gg][col];
+      v1 = -qt[gg][col + 1];
+    }
+    uint32_t hi, lo;
+    split2(v0, v1, hi, lo);
+    dst[(ks * 32 + L) * 4 + 2 * half] = hi;
+    dst[(ks * 32 + L) * 4 + 2 * half + 1] = lo;
   }
 }
 
@@ -364,6 +442,8 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
   uint8_t* stage = smem + SMEM_A;
   __shared__ float wm[NWARP][kMaxRep], wl[NWARP][kMaxRep];
   __shared__ int sblk[NWARP][STAGES];
+  __shared__ __align__(16) float qr[kMaxRep][D];
+  __shared__ __align__(16) float qt[kMaxRep][D];
 
   const int part = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int kvh = hg / a.groups;
@@ -394,9 +474,11 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
   float vscale = 4.f;  // value codes entered as 1 + q/4; the offset is removed through st.mn
 
   if (!ring) {
-    const uint4* af = a.afrag + ((size_t)b * a.hkv * a.groups + hg) * AFRAG_U4;
-    for (int i = tid; i < AFRAG_U4; i += blockDim.x) cp16(&sA[i], &af[i]);
-    cp_commit();
+    if (a.afrag) {
+      const uint4* af = a.afrag + ((size_t)b * a.hkv * a.groups + hg) * AFRAG_U4;
+      for (int i = tid; i < AFRAG_U4; i += blockDim.x) cp16(&sA[i], &af[i]);
+      cp_commit();
+    }
     const int pbeg = part * a.chunk_pages;
     const int npg = min(npages, pbeg + a.chunk_pages) - pbeg;
     const int nw = npg > warp ? (npg - warp + NWARP - 1) / NWARP : 0;
@@ -420,8 +502,12 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
 #pragma unroll
     for (int k = 0; k < STAGES - 1; ++k) issue(k, blk_of(k));
     int nxt = blk_of(STAGES - 1);
-    cp_wait<STAGES - 1>();
-    __syncthreads();  // every thread's share of the A fragments has landed
+    if (a.afrag) {
+      cp_wait<STAGES - 1>();
+      __syncthreads();  // every thread's share of the fragments has landed
+    } else {
+      build_query_frags(a, b, h0, sA, qr, qt, tid, lane, warp);  // ends with __syncthreads
+    }
     for (int k = 0; k < nw; ++k) {
       __syncwarp();  // every lane is done with the slot and stage that are refilled next
       const int cur = nxt;
@@ -588,10 +674,13 @@ cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) 
   a.neg_y = -0.5f * (c3 - c2);
   a.qjl_coef = 1.2533141373155003f / (float)ctx->cfg.qjl_m;
   a.logit_scale = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
-  tc_prep_kernel<<<dim3(hgroups, batch, kPrepSlices), 128, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  ctx->launches++;
+  cudaError_t e = cudaSuccess;
+  if (a.afrag) {
+    tc_prep_kernel<<<dim3(hgroups, batch, kPrepSlices), 128, 0, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ctx->launches++;
+  }
   e = cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TOTAL);
   if (e != cudaSuccess) return e;
   prof_start(ctx, kProfDecode, s);

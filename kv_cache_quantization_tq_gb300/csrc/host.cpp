@@ -253,9 +253,14 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
   pl.chunk_tokens = (int)(per * kPage);
   pl.n_chunks = (int)((pages + per - 1) / per);
   pl.n_parts = pl.n_chunks + 1;
-  if (pl.tensor_core)
-    pl.q_bytes = align((size_t)batch * hkv * groups * 24 * 32 * 16);
-  else
+  if (pl.tensor_core) {
+    // A grid that fits in one wave (3 CTAs per SM) builds the query fragments in every CTA,
+    // saving a kernel; larger grids build them once per (sequence, head group) in a prep
+    // kernel, because there the per-CTA cost (~3 us) outweighs the saved launch.
+    const int64_t ctas = (int64_t)pl.n_parts * hkv * groups * batch;
+    pl.fused_prep = ctas <= (int64_t)ctx->sm_count * 3;
+    pl.q_bytes = pl.fused_prep ? 0 : align((size_t)batch * hkv * groups * 24 * 32 * 16);
+  } else
     pl.q_bytes = ctx->cfg.layout == TQ_LAYOUT_MAIN ? align(sizeof(float) * batch * hq * 2 * d) : 0;
   pl.part_bytes = align(sizeof(float) * (size_t)batch * hq * pl.n_parts * (d + (pl.tensor_core ? 4 : 2)));
   pl.total = pl.q_bytes + pl.part_bytes;

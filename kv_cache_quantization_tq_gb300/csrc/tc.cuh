@@ -20,13 +20,12 @@ struct TcArgs {
   const int32_t* n_buf;
   int max_ctx;
   float* out;
-  uint4* afrag;    // [B][Hkv * groups][24 k-steps][32 lanes] score-side A fragments
+  uint4* afrag;    // [B][Hkv * groups][24 k-steps][32 lanes] query fragments, or NULL: built per CTA
   float* parts;    // [B][Hq][n_parts][d + 4] split-K partials (o, m, l, pad)
   int chunk_pages, n_chunks, n_parts;
   int hq, hkv, n_rep, nrg, groups;
   const float* signs;
-  const float* sketch;    // [m][d]
-  const float* sketch_t;  // [d][m]
+  const uint4* sfrag_enc;  // S^T as mma.sync B fragments (k = coordinate, n = sketch row), hi / lo
   uint32_t* err;
   float neg_x, neg_y, qjl_coef, logit_scale;
 };

@@ -61,6 +61,7 @@ void prof_stop(tq_ctx* ctx, int kind, cudaStream_t s);
 // Decode chunking policy shared by tq_workspace_size and tq_decode_attention.
 struct DecodePlan {
   bool tensor_core;   // main layout, head_dim 128: decode_tc.cu
+  bool fused_prep;    // tensor-core path: each CTA builds its own query fragments (one-wave grids)
   int chunk_tokens;   // compressed tokens per split-K chunk (multiple of 16)
   int n_chunks;       // chunks for max_ctx compressed tokens
   int n_parts;        // n_chunks + 1 (ring part)
