@@ -37,8 +37,9 @@ def encode_main_range(pool, block_table, start, k16, v16, signs, centroids, s_ma
     k16 = np.asarray(k16, dtype=np.float16)
     bsz, hkv, t, d = k16.shape
     assert start % layout.P == 0 and t % layout.P == 0
+    vbits = layout.main_value_bits(pool.shape[-1], d)
     enc = quant.encode_keys(k16, signs, centroids, s_mat)
-    vq, vs, vmn = quant.encode_values(v16, group)
+    vq, vs, vmn = quant.encode_values(v16, group, vbits)
     npg = t // layout.P
     tiles = layout.pack_main_tiles(
         enc["idx"].reshape(bsz, hkv, npg, 16, d),
@@ -48,6 +49,7 @@ def encode_main_range(pool, block_table, start, k16, v16, signs, centroids, s_ma
         vmn.reshape(bsz, hkv, npg, 16, d // group),
         enc["n_k"].reshape(bsz, hkv, npg, 16),
         enc["n_r"].reshape(bsz, hkv, npg, 16),
+        vbits,
     )
     pages = start // layout.P + np.arange(npg)
     blocks = np.asarray(block_table)[:, pages]  # [B, npg]

@@ -108,20 +108,38 @@ def plane_words_to_bits(words: np.ndarray) -> np.ndarray:
     return b.reshape(words.shape[:-1] + (words.shape[-1] * 32,)).astype(np.uint8)
 
 
-def codes_to_vq_words(codes: np.ndarray) -> np.ndarray:
-    """2-bit codes [..., 16 tokens, d] -> uint32 [..., d] (dimension-major)."""
+def codes_to_vq_words(codes: np.ndarray, bits: int = 2) -> np.ndarray:
+    """Value codes [..., 16 tokens, d] -> uint32 words (dimension-major).
+
+    2-bit: one word per dimension, token 2j + e at bit 16 e + 2 j -> [..., d].
+    4-bit: two words per dimension, word w holding tokens 8 w + 2 j + e at bit 16 e + 4 j;
+    all words of w = 0 first, then all of w = 1 -> [..., 2 d].
+    """
     c = np.asarray(codes, dtype=np.uint64)
     d = c.shape[-1]
-    c = c.reshape(c.shape[:-2] + (8, 2, d))  # token = 2j + e
-    sh = (16 * np.arange(2)[None, :] + 2 * np.arange(8)[:, None]).astype(np.uint64)[..., None]
-    return (c << sh).sum(axis=(-3, -2)).astype(np.uint32)
+    if bits == 2:
+        c = c.reshape(c.shape[:-2] + (8, 2, d))  # token = 2j + e
+        sh = (16 * np.arange(2)[None, :] + 2 * np.arange(8)[:, None]).astype(np.uint64)[..., None]
+        return (c << sh).sum(axis=(-3, -2)).astype(np.uint32)
+    assert bits == 4
+    c = c.reshape(c.shape[:-2] + (2, 4, 2, d))  # token = 8w + 2j + e
+    sh = (16 * np.arange(2)[None, :] + 4 * np.arange(4)[:, None]).astype(np.uint64)[..., None]
+    w = (c << sh).sum(axis=(-3, -2)).astype(np.uint32)  # [..., 2, d]
+    return w.reshape(w.shape[:-2] + (2 * d,))
 
 
-def vq_words_to_codes(words: np.ndarray) -> np.ndarray:
-    w = np.asarray(words, dtype=np.uint64)[..., None, None, :]
-    sh = (16 * np.arange(2)[None, :] + 2 * np.arange(8)[:, None]).astype(np.uint64)[..., None]
-    c = (w >> sh) & np.uint64(3)
-    return c.reshape(words.shape[:-1] + (16, words.shape[-1])).astype(np.uint8)
+def vq_words_to_codes(words: np.ndarray, bits: int = 2) -> np.ndarray:
+    if bits == 2:
+        w = np.asarray(words, dtype=np.uint64)[..., None, None, :]
+        sh = (16 * np.arange(2)[None, :] + 2 * np.arange(8)[:, None]).astype(np.uint64)[..., None]
+        c = (w >> sh) & np.uint64(3)
+        return c.reshape(words.shape[:-1] + (16, words.shape[-1])).astype(np.uint8)
+    assert bits == 4
+    d = words.shape[-1] // 2
+    w = np.asarray(words, dtype=np.uint64).reshape(words.shape[:-1] + (2, 1, 1, d))
+    sh = (16 * np.arange(2)[None, :] + 4 * np.arange(4)[:, None]).astype(np.uint64)[..., None]
+    c = (w >> sh) & np.uint64(15)  # [..., 2, 4, 2, d]
+    return c.reshape(words.shape[:-1] + (16, d)).astype(np.uint8)
 
 
 def _u32_bytes(words: np.ndarray) -> np.ndarray:
@@ -135,20 +153,28 @@ def _f16_bytes(x: np.ndarray) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- main layout
-def main_tile_bytes(d: int) -> int:
-    return 12 * d + 64
+def main_tile_bytes(d: int, vbits: int = 2) -> int:
+    """Key planes 6d, value codes 2 vbits d, value scale/minimum 2d, two norm rows 64 B."""
+    return (8 + 2 * vbits) * d + 64
 
 
-def main_bytes_per_token_head(d: int) -> float:
-    return main_tile_bytes(d) / P
+def main_bytes_per_token_head(d: int, vbits: int = 2) -> float:
+    return main_tile_bytes(d, vbits) / P
 
 
-def pack_main_tiles(idx, sigma, vq, vs16, vmn16, nk16, nr16) -> np.ndarray:
+def main_value_bits(tile_bytes: int, d: int) -> int:
+    """Value bit width of a main-layout tile of the given size."""
+    vbits = (tile_bytes - 64 - 8 * d) // (2 * d)
+    assert vbits in (2, 4) and main_tile_bytes(d, vbits) == tile_bytes, (tile_bytes, d)
+    return vbits
+
+
+def pack_main_tiles(idx, sigma, vq, vs16, vmn16, nk16, nr16, vbits: int = 2) -> np.ndarray:
     """Build main-layout tiles.
 
     Leading shape [..., 16 tokens]: idx, sigma, vq are [..., 16, d] uint8;
     vs16/vmn16 [..., 16, d/32] fp16; nk16/nr16 [..., 16] fp16.
-    Returns uint8 [..., 12 d + 64].
+    Returns uint8 [..., (8 + 2 vbits) d + 64].
     """
     idx = np.asarray(idx, dtype=np.uint8)
     d = idx.shape[-1]
@@ -156,13 +182,13 @@ def pack_main_tiles(idx, sigma, vq, vs16, vmn16, nk16, nr16) -> np.ndarray:
     kh = _u32_bytes(bits_to_plane_words(idx >> 1)).reshape(lead + (2 * d,))
     kl = _u32_bytes(bits_to_plane_words(idx & 1)).reshape(lead + (2 * d,))
     ks = _u32_bytes(bits_to_plane_words(sigma)).reshape(lead + (2 * d,))
-    vqb = _u32_bytes(codes_to_vq_words(vq))
+    vqb = _u32_bytes(codes_to_vq_words(vq, vbits))
     sm = np.stack([np.asarray(vs16, np.float16), np.asarray(vmn16, np.float16)], axis=-1)
     vsm = _f16_bytes(sm.reshape(lead + (16 * (d // 32) * 2,)))
     kn = _f16_bytes(nk16)
     rn = _f16_bytes(nr16)
     out = np.concatenate([kh, kl, ks, vqb, vsm, kn, rn], axis=-1)
-    assert out.shape[-1] == main_tile_bytes(d)
+    assert out.shape[-1] == main_tile_bytes(d, vbits)
     return out
 
 
@@ -170,6 +196,9 @@ def unpack_main_tiles(tiles: np.ndarray, d: int) -> dict:
     t = np.asarray(tiles, dtype=np.uint8)
     lead = t.shape[:-1]
     g = d // 32
+    vb = main_value_bits(t.shape[-1], d)
+    o_sm = (6 + 2 * vb) * d
+    o_n = o_sm + 2 * d
 
     def words(off, nbytes):
         return np.ascontiguousarray(t[..., off:off + nbytes]).view("<u4")
@@ -177,10 +206,10 @@ def unpack_main_tiles(tiles: np.ndarray, d: int) -> dict:
     kh = plane_words_to_bits(words(0, 2 * d).reshape(lead + (16, d // 32)))
     kl = plane_words_to_bits(words(2 * d, 2 * d).reshape(lead + (16, d // 32)))
     ks = plane_words_to_bits(words(4 * d, 2 * d).reshape(lead + (16, d // 32)))
-    vq = vq_words_to_codes(words(6 * d, 4 * d))
-    sm = np.ascontiguousarray(t[..., 10 * d:12 * d]).view("<f2").reshape(lead + (16, g, 2))
-    nk = np.ascontiguousarray(t[..., 12 * d:12 * d + 32]).view("<f2")
-    nr = np.ascontiguousarray(t[..., 12 * d + 32:12 * d + 64]).view("<f2")
+    vq = vq_words_to_codes(words(6 * d, 2 * vb * d), vb)
+    sm = np.ascontiguousarray(t[..., o_sm:o_sm + 2 * d]).view("<f2").reshape(lead + (16, g, 2))
+    nk = np.ascontiguousarray(t[..., o_n:o_n + 32]).view("<f2")
+    nr = np.ascontiguousarray(t[..., o_n + 32:o_n + 64]).view("<f2")
     return {
         "idx": (2 * kh + kl).astype(np.uint8),
         "sigma": ks,

@@ -127,9 +127,10 @@ def group_dequant(q: np.ndarray, scale16: np.ndarray, min16: np.ndarray, group: 
     return out.reshape(shape)
 
 
-def encode_values(v16: np.ndarray, group: int = 32):
-    """Main-layout values: 2-bit codes, fp16 scale, fp16 minimum per group."""
-    return group_quant(v16, group, 3)
+def encode_values(v16: np.ndarray, group: int = 32, bits: int = 2):
+    """Main-layout values: ``bits``-bit codes (2 or 4; turboquant vLLM guide, --value-bits),
+    fp16 scale, fp16 minimum per group."""
+    return group_quant(v16, group, (1 << bits) - 1)
 
 
 def dequant_keys(enc: dict, signs: np.ndarray, centroids: np.ndarray, s_mat: np.ndarray) -> np.ndarray:

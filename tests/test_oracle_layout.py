@@ -69,6 +69,47 @@ def test_vq_words_brute_force():
     assert np.array_equal(layout.vq_words_to_codes(words), codes)
 
 
+def test_vq_words_4bit_brute_force_and_hand_worked():
+    # word w of a dimension holds tokens 8w + 2j + e at bit 16e + 4j; all w = 0 words first
+    codes = synth.random_codes(3, 16 * 32, 4).reshape(16, 32)
+    words = layout.codes_to_vq_words(codes, 4)
+    assert words.shape == (64,)
+    for i in range(32):
+        for w in range(2):
+            want = 0
+            for t in range(8):
+                j, e = divmod(t, 2)
+                want |= int(codes[8 * w + t, i]) << (16 * e + 4 * j)
+            assert int(words[w * 32 + i]) == want
+    assert np.array_equal(layout.vq_words_to_codes(words, 4), codes)
+    # token t carries code t in every dimension
+    ramp = np.repeat(np.arange(16, dtype=np.uint8)[:, None], 4, axis=1)
+    w = layout.codes_to_vq_words(ramp, 4)
+    assert int(w[0]) == 0x75316420 and int(w[4]) == 0xFDB9ECA8
+
+
+@pytest.mark.parametrize("d", [64, 256])
+def test_main_tile_round_trip_4bit_values(d):
+    g = np.random.default_rng(d + 1)
+    f = {
+        "idx": g.integers(0, 4, (2, 16, d), dtype=np.uint8),
+        "sigma": g.integers(0, 2, (2, 16, d), dtype=np.uint8),
+        "vq": g.integers(0, 16, (2, 16, d), dtype=np.uint8),
+        "vs": g.standard_normal((2, 16, d // 32)).astype(np.float16),
+        "vmn": g.standard_normal((2, 16, d // 32)).astype(np.float16),
+        "n_k": g.standard_normal((2, 16)).astype(np.float16),
+        "n_r": g.standard_normal((2, 16)).astype(np.float16),
+    }
+    t = layout.pack_main_tiles(f["idx"], f["sigma"], f["vq"], f["vs"], f["vmn"], f["n_k"], f["n_r"], 4)
+    assert t.shape == (2, layout.main_tile_bytes(d, 4)) and layout.main_tile_bytes(d, 4) == 16 * d + 64
+    assert layout.main_value_bits(t.shape[-1], d) == 4
+    back = layout.unpack_main_tiles(t, d)
+    for k, v in f.items():
+        assert np.array_equal(back[k].view(np.uint8), v.view(np.uint8)), k
+    # norms follow the 8d bytes of value codes and the 2d bytes of scale / minimum
+    assert np.array_equal(t[1, 16 * d:16 * d + 32].view("<f2"), f["n_k"][1])
+
+
 @pytest.mark.parametrize("d", [64, 128, 256])
 def test_main_tile_round_trip(d):
     g = np.random.default_rng(d)
@@ -119,6 +160,8 @@ def test_alt_tile_round_trip(d):
 
 def test_bytes_per_token_closed_form():
     assert layout.main_bytes_per_token_head(128) == 100
+    # 4-bit values: 48 bytes of key bits, 64 of value codes, 16 of group scale/minimum, 4 of norms
+    assert layout.main_bytes_per_token_head(128, 4) == 48 + 64 + 16 + 4 == 132
     # 32 + 16 bytes of key bits, 32 bytes of value codes, 4 groups x 4 bytes, 2 norms
     assert 128 * 3 // 8 + 128 * 2 // 8 + 4 * 4 + 2 + 2 == 100
     for d in (64, 128, 256, 512):

@@ -71,3 +71,38 @@ def test_alt_materialised_history_reproduces_the_decode():
         k0 = k[b, :, :L].astype(np.float64).reshape(hkv, L, d // 32, 32)
         step = (k0.max(-1) - k0.min(-1)) / 255.0
         assert np.all(np.abs(kk.reshape(hkv, L, d // 32, 32) - k0) <= step[..., None] * (0.5 + 2e-3) + 1e-6)
+
+
+def test_main_layout_with_4bit_values():
+    # the same pins with 4-bit value codes (15 levels per group of 32)
+    seed, d, hkv, n_rep = 6, 64, 2, 2
+    sg = rng.signs(seed, d)
+    c, _ = codebook.lloyd_max(d, 2)
+    s = rng.gaussian_matrix(seed, d, d)
+    lengths = [300, 129]
+    k, v = synth.kv_main(seed, 2, hkv, 304, d)
+    bt = synth.block_table(seed, 2, 19, True)
+    pool = np.zeros((38, hkv, layout.main_tile_bytes(d, 4)), np.uint8)
+    ring_k = np.zeros((2, hkv, 128, d), np.float16)
+    ring_v = np.zeros_like(ring_k)
+    n_c, n_b = np.zeros(2, np.int64), np.zeros(2, np.int64)
+    for b, L in enumerate(lengths):
+        nc, nb = cache.ring_split(L)
+        n_c[b], n_b[b] = nc, nb
+        cache.encode_main_range(pool, bt[b:b + 1], 0, k[b:b + 1, :, :nc], v[b:b + 1, :, :nc], sg, c, s)
+        ring_k[b, :, :nb] = k[b, :, nc:nc + nb]
+        ring_v[b, :, :nb] = v[b, :, nc:nc + nb]
+    q = synth.queries(seed, 2, hkv * n_rep, d)
+    ref = attention.decode_main(q, pool, bt, n_c, ring_k, ring_v, n_b, sg, c, s, hkv)
+    brute = attention.decode_main_bruteforce(q, pool, bt, n_c, ring_k, ring_v, n_b, sg, c, s, hkv)
+    assert np.allclose(ref, brute, rtol=0, atol=1e-12)
+    for b in range(2):
+        nc, nb = int(n_c[b]), int(n_b[b])
+        kk, vv = cache.materialize_main(pool, bt, b, nc, ring_k, ring_v, nb, sg, c, s, d)
+        assert np.allclose(_attend(q[b], kk, vv, hkv), ref[b], rtol=0, atol=1e-12)
+        v0 = v[b, :, :nc].astype(np.float64).reshape(hkv, nc, d // 32, 32)
+        step = (v0.max(-1) - v0.min(-1)) / 15.0
+        err = np.abs(vv[:, :nc].reshape(hkv, nc, d // 32, 32) - v0)
+        assert np.all(err <= step[..., None] * (0.5 + 2e-3) + 1e-6)
+        # 4-bit codes are finer than 2-bit ones: mean error well under the 2-bit half step
+        assert err.mean() < (step[..., None] * 15 / 3 * 0.25).mean()
