@@ -89,7 +89,7 @@ typedef struct {
   int ring_capacity; /* exact recent-token buffer: must be 128 */
   int layout;        /* tq_layout */
   int key_bits;      /* main: 3 (2-bit Lloyd-Max + 1-bit QJL); alt: 8 */
-  int value_bits;    /* main: 2; alt: 3 */
+  int value_bits;    /* main: 2 (default) or 4 (turboquant vLLM guide, --value-bits); alt: 3 */
   int group_size;    /* value group / key block: must be 32 */
   int qjl_m;         /* main: sketch rows m, must equal head_dim; alt: 0 */
   uint64_t seed;     /* table seed; one table set per layer (base seed + layer) */

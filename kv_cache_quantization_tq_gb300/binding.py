@@ -186,8 +186,10 @@ class Context:
     """Owner of one tq_ctx (one layer's tables on the current CUDA device)."""
 
     def __init__(self, layout: int, head_dim: int, num_q_heads: int, num_kv_heads: int, seed: int = 0,
-                 centroids=None, signs=None, sketch=None):
+                 centroids=None, signs=None, sketch=None, value_bits=None):
         self.cfg = tq_config_init(layout, head_dim, num_q_heads, num_kv_heads, seed)
+        if value_bits is not None:
+            self.cfg.value_bits = value_bits  # main layout: 2 or 4
         ptr = C.c_void_p()
         if centroids is None:
             _check(lib.tq_create(C.byref(self.cfg), C.byref(ptr)), "tq_create")

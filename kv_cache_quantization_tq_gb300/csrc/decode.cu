@@ -222,20 +222,23 @@ __device__ void write_part(const DecArgs& a, int b, int h0, int part, const Soft
 }
 
 // ------------------------------------------------------------------ main layout
-template <int D, int NR>
+// VB = value bits (2 or 4): value codes take VB * d / 8 bytes per token.
+template <int D, int NR, int VB>
 struct MainDec {
-  static constexpr int TILE = 12 * D + 64;
+  static constexpr int TILE = (8 + 2 * VB) * D + 64;
+  static constexpr int O_VSM = (6 + 2 * VB) * D;
+  static constexpr int O_NORM = (8 + 2 * VB) * D;
   static constexpr int G = D / 32;
 };
 
-template <int D, int NR>
+template <int D, int NR, int VB>
 __global__ void __launch_bounds__(128) decode_main_kernel(DecArgs a) {
-  using C = MainDec<D, NR>;
+  using C = MainDec<D, NR, VB>;
   constexpr int G = C::G;
   constexpr int DPT = (D + 127) / 128;
   __shared__ float qr[NR][D];
   __shared__ float qt[NR][D];
-  __shared__ __align__(16) uint8_t tile[C::TILE];
+  extern __shared__ __align__(16) uint8_t tile[];  // one page of one KV head (C::TILE bytes)
   __shared__ float sc[NR][16];
   __shared__ float pbuf[16][NR];
   __shared__ float pw[G][16][NR];
@@ -298,9 +301,9 @@ __global__ void __launch_bounds__(128) decode_main_kernel(DecArgs a) {
   const uint32_t* kl_w = reinterpret_cast<const uint32_t*>(tile + 2 * D);
   const uint32_t* ks_w = reinterpret_cast<const uint32_t*>(tile + 4 * D);
   const uint32_t* vq_w = reinterpret_cast<const uint32_t*>(tile + 6 * D);
-  const __half* vsm = reinterpret_cast<const __half*>(tile + 10 * D);
-  const __half* kn = reinterpret_cast<const __half*>(tile + 12 * D);
-  const __half* rn = reinterpret_cast<const __half*>(tile + 12 * D + 32);
+  const __half* vsm = reinterpret_cast<const __half*>(tile + C::O_VSM);
+  const __half* kn = reinterpret_cast<const __half*>(tile + C::O_NORM);
+  const __half* rn = reinterpret_cast<const __half*>(tile + C::O_NORM + 32);
 
   for (int t0 = tbeg; t0 < tend; t0 += kPage) {
     const int page = t0 >> 4;
@@ -374,12 +377,16 @@ __global__ void __launch_bounds__(128) decode_main_kernel(DecArgs a) {
       const int i = tid + 128 * r;
       if (i < D) {
         const int g = i >> 5;
+        // 2-bit: token 2j+e at bits 16e+2j of word i; 4-bit: tokens 8w+2j+e at bits 16e+4j of
+        // word w*d + i
         const uint32_t w = vq_w[i];
+        const uint32_t w1 = VB == 4 ? vq_w[D + i] : 0u;
 #pragma unroll
         for (int h = 0; h < NR; ++h) o[r][h] *= st.alpha[h];
 #pragma unroll
         for (int tk = 0; tk < 16; ++tk) {
-          const float cf = (float)((w >> (16 * (tk & 1) + 2 * (tk >> 1))) & 3u);
+          const float cf = VB == 2 ? (float)((w >> (16 * (tk & 1) + 2 * (tk >> 1))) & 3u)
+                                   : (float)(((tk < 8 ? w : w1) >> (16 * (tk & 1) + 4 * ((tk & 7) >> 1))) & 15u);
 #pragma unroll
           for (int h = 0; h < NR; ++h) o[r][h] = fmaf(pw[g][tk][h], cf, o[r][h]);
         }
@@ -619,21 +626,31 @@ __global__ void __launch_bounds__(128) merge_kernel(DecArgs a, int d) {
   }
 }
 
-template <int D, int NR>
-cudaError_t launch_tpl(const DecArgs& a, bool main, dim3 grid, cudaStream_t s) {
-  if (main)
-    decode_main_kernel<D, NR><<<grid, 128, 0, s>>>(a);
-  else
-    decode_alt_kernel<D, NR><<<grid, 128, 0, s>>>(a);
+template <int D, int NR, int VB>
+cudaError_t launch_main_vb(const DecArgs& a, dim3 grid, cudaStream_t s) {
+  auto kern = decode_main_kernel<D, NR, VB>;
+  constexpr int TILE = MainDec<D, NR, VB>::TILE;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TILE);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 128, TILE, s>>>(a);
   return cudaGetLastError();
 }
 
+template <int D, int NR>
+cudaError_t launch_tpl(const DecArgs& a, int vb, dim3 grid, cudaStream_t s) {
+  if (vb == 4) return launch_main_vb<D, NR, 4>(a, grid, s);
+  if (vb == 2) return launch_main_vb<D, NR, 2>(a, grid, s);
+  decode_alt_kernel<D, NR><<<grid, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+// vb: value bits of the main layout (2 or 4), 0 for the alternate layout
 template <int D>
-cudaError_t launch_d(const DecArgs& a, bool main, dim3 grid, cudaStream_t s) {
-  if (a.nrg <= 1) return launch_tpl<D, 1>(a, main, grid, s);
-  if (a.nrg <= 2) return launch_tpl<D, 2>(a, main, grid, s);
-  if (a.nrg <= 4) return launch_tpl<D, 4>(a, main, grid, s);
-  return launch_tpl<D, 8>(a, main, grid, s);
+cudaError_t launch_d(const DecArgs& a, int vb, dim3 grid, cudaStream_t s) {
+  if (a.nrg <= 1) return launch_tpl<D, 1>(a, vb, grid, s);
+  if (a.nrg <= 2) return launch_tpl<D, 2>(a, vb, grid, s);
+  if (a.nrg <= 4) return launch_tpl<D, 4>(a, vb, grid, s);
+  return launch_tpl<D, 8>(a, vb, grid, s);
 }
 
 }  // namespace
@@ -736,10 +753,10 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
   if (!done || n_buf) {
     if (!done) prof_start(ctx, kProfDecode, s);
     switch (d) {
-      case 64: e = launch_d<64>(a, main, grid, s); break;
-      case 128: e = launch_d<128>(a, main, grid, s); break;
-      case 256: e = launch_d<256>(a, main, grid, s); break;
-      case 512: e = launch_d<512>(a, main, grid, s); break;
+      case 64: e = launch_d<64>(a, main ? ctx->cfg.value_bits : 0, grid, s); break;
+      case 128: e = launch_d<128>(a, main ? ctx->cfg.value_bits : 0, grid, s); break;
+      case 256: e = launch_d<256>(a, main ? ctx->cfg.value_bits : 0, grid, s); break;
+      case 512: e = launch_d<512>(a, main ? ctx->cfg.value_bits : 0, grid, s); break;
     }
     if (!done) prof_stop(ctx, kProfDecode, s);
     if (e != cudaSuccess) return e;

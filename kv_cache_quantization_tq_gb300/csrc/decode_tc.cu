@@ -39,15 +39,23 @@ namespace tq {
 namespace {
 
 constexpr int D = 128;
-constexpr int TILE = 12 * D + 64;  // 1600 bytes
 constexpr int NWARP = 4;
 constexpr int STAGES = 4;
 constexpr int KSTEPS = 24;         // 3 planes x 8 k-steps of 16 coordinates
 constexpr int AFRAG_U4 = KSTEPS * 32;
 constexpr size_t SMEM_A = AFRAG_U4 * sizeof(uint4);
-constexpr size_t SMEM_STAGE = (size_t)NWARP * STAGES * TILE;
-constexpr size_t SMEM_TOTAL = SMEM_A + SMEM_STAGE;
-static_assert((size_t)NWARP * kMaxRep * D * sizeof(float) <= SMEM_STAGE, "combine buffer fits the stages");
+
+// Tile of the main layout with VB value bits (2: 1600 bytes, 4: 2112 bytes at d = 128).
+template <int VB>
+struct TcTile {
+  static constexpr int TILE = (8 + 2 * VB) * D + 64;
+  static constexpr int O_VQ = 6 * D;
+  static constexpr int O_VSM = (6 + 2 * VB) * D;
+  static constexpr int O_NORM = (8 + 2 * VB) * D;
+  static constexpr size_t SMEM_STAGE = (size_t)NWARP * STAGES * TILE;
+  static constexpr size_t SMEM_TOTAL = SMEM_A + SMEM_STAGE;
+  static_assert((size_t)NWARP * kMaxRep * D * sizeof(float) <= SMEM_STAGE, "combine buffer fits the stages");
+};
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kPartStride = D + 4;  // floats per split-K partial: o[D], m, l, pad (16-byte rows)
@@ -304,8 +312,10 @@ __device__ __forceinline__ void softmax_update(WarpState& st, float (&s)[4], flo
 }
 
 // One compressed page (16 tokens) of the warp's KV head.
+template <int VB>
 __device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA, const uint8_t* T, WarpState& st,
                                                 int lane) {
+  using L = TcTile<VB>;
   const int g = lane >> 2, t = lane & 3;
   uint4 rw[3][2];
 #pragma unroll
@@ -341,8 +351,8 @@ __device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA
   float s[4];
 #pragma unroll
   for (int n = 0; n < 2; ++n) {
-    const float2 nk = __half22float2(*reinterpret_cast<const __half2*>(T + 12 * D + (8 * n + 2 * t) * 2));
-    const float2 nr = __half22float2(*reinterpret_cast<const __half2*>(T + 12 * D + 32 + (8 * n + 2 * t) * 2));
+    const float2 nk = __half22float2(*reinterpret_cast<const __half2*>(T + L::O_NORM + (8 * n + 2 * t) * 2));
+    const float2 nr = __half22float2(*reinterpret_cast<const __half2*>(T + L::O_NORM + 32 + (8 * n + 2 * t) * 2));
     const float lm0 = fmaf(acc[0][n][2], kLoUnscale, acc[0][n][0]);
     const float lm1 = fmaf(acc[0][n][3], kLoUnscale, acc[0][n][1]);
     const float qj0 = fmaf(acc[1][n][2], kLoUnscale, acc[1][n][0]);
@@ -357,7 +367,7 @@ __device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int tok = (k >> 1) * 8 + 2 * t + (k & 1);
-    sm[k] = *reinterpret_cast<const uint4*>(T + 10 * D + tok * 16);
+    sm[k] = *reinterpret_cast<const uint4*>(T + L::O_VSM + tok * 16);
   }
   uint4 Ap[4];
 #pragma unroll
@@ -375,21 +385,29 @@ __device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA
     for (int k = 0; k < 4; ++k) w[k] = p[k] * sc[k];
     split2(w[0], w[1], Ap[gg].x, Ap[gg].y);
     split2(w[2], w[3], Ap[gg].z, Ap[gg].w);
-    // group minimum, minus the 1 of the code encoding below (4 w, as the codes are scaled by 4)
+    // group minimum, minus the 1 of the code encoding below (2^VB w, as the codes are scaled by 2^VB)
     float acc_mn = st.mn[gg];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) acc_mn = fmaf(p[k], mn[k], fmaf(-4.f, w[k], acc_mn));
+    for (int k = 0; k < 4; ++k) acc_mn = fmaf(p[k], mn[k], fmaf(-(float)(1 << VB), w[k], acc_mn));
     st.mn[gg] = acc_mn;
   }
-  // 2-bit code q of tokens 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1) as the normal fp16 value 1 + q/4
-  // (bit pattern 0x3C00 | q << 8): exact, and free of the reduced accumulation precision
-  // that subnormal operands get when products are chained.
-  const uint32_t* vq = reinterpret_cast<const uint32_t*>(T + 6 * D);
+  // VB-bit code q of tokens 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1) as the normal fp16 value
+  // 1 + q / 2^VB (bit pattern 0x3C00 | q << (10 - VB)): exact, and free of the reduced
+  // accumulation precision that subnormal operands get when products are chained.
+  const uint32_t* vq = reinterpret_cast<const uint32_t*>(T + L::O_VQ);
 #pragma unroll
   for (int nt = 0; nt < 16; ++nt) {
-    const uint32_t wv = vq[nt * 8 + g];
-    const uint32_t b0 = ((wv << (8 - 2 * t)) & 0x03000300u) | 0x3C003C00u;
-    const uint32_t b1 = ((wv >> (2 * t)) & 0x03000300u) | 0x3C003C00u;
+    uint32_t b0, b1;
+    if (VB == 2) {
+      const uint32_t wv = vq[nt * 8 + g];
+      b0 = ((wv << (8 - 2 * t)) & 0x03000300u) | 0x3C003C00u;
+      b1 = ((wv >> (2 * t)) & 0x03000300u) | 0x3C003C00u;
+    } else {
+      // word 0 holds tokens 0..7, word 1 tokens 8..15; pair t at bits 4t and 16 + 4t
+      const uint32_t w0 = vq[nt * 8 + g], w1 = vq[D + nt * 8 + g];
+      b0 = (((w0 >> (4 * t)) << 6) & 0x03C003C0u) | 0x3C003C00u;
+      b1 = (((w1 >> (4 * t)) << 6) & 0x03C003C0u) | 0x3C003C00u;
+    }
     mma_f16(st.o[nt], Ap[nt >> 2], b0, b1);
   }
 }
@@ -436,7 +454,9 @@ __device__ __forceinline__ void page_ring(const TcArgs& a, const uint4 (&Aq)[8],
   }
 }
 
+template <int VB>
 __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
+  using L = TcTile<VB>;
   extern __shared__ __align__(16) uint8_t smem[];
   uint4* sA = reinterpret_cast<uint4*>(smem);
   uint8_t* stage = smem + SMEM_A;
@@ -471,7 +491,7 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
     for (int r = 0; r < 4; ++r) st.o[nt][r] = 0.f;
 #pragma unroll
   for (int k = 0; k < 4; ++k) st.mn[k] = 0.f;
-  float vscale = 4.f;  // value codes entered as 1 + q/4; the offset is removed through st.mn
+  float vscale = (float)(1 << VB);  // value codes entered as 1 + q/2^VB; the offset is removed through st.mn
 
   if (!ring) {
     if (a.afrag) {
@@ -482,7 +502,7 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
     const int pbeg = part * a.chunk_pages;
     const int npg = min(npages, pbeg + a.chunk_pages) - pbeg;
     const int nw = npg > warp ? (npg - warp + NWARP - 1) / NWARP : 0;
-    uint8_t* wst = stage + (size_t)warp * STAGES * TILE;
+    uint8_t* wst = stage + (size_t)warp * STAGES * L::TILE;
     const int32_t* btb = a.block_table + (size_t)b * a.max_blocks;
     // Block ids: the id of the next page to copy is read one page ahead, so the table read
     // never holds up a copy (or the compute queued behind it); the ids of the pages in flight
@@ -492,9 +512,9 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
       if (k < nw) {
         if (lane == 0) sblk[warp][k % STAGES] = blk;
         if (blk >= 0 && blk < a.num_blocks) {
-          const uint8_t* gsrc = a.pool + ((size_t)blk * a.hkv + kvh) * TILE;
-          uint8_t* sdst = wst + (k % STAGES) * TILE;
-          for (int c = lane; c < TILE / 16; c += 32) cp16(sdst + c * 16, gsrc + c * 16);
+          const uint8_t* gsrc = a.pool + ((size_t)blk * a.hkv + kvh) * L::TILE;
+          uint8_t* sdst = wst + (k % STAGES) * L::TILE;
+          for (int c = lane; c < L::TILE / 16; c += 32) cp16(sdst + c * 16, gsrc + c * 16);
         }
       }
       cp_commit();
@@ -520,7 +540,7 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
         if (lane == 0) flag_error(a.err, TQ_DEVERR_BLOCK_ID);
         continue;
       }
-      page_compressed(a, sA, wst + (k % STAGES) * TILE, st, lane);
+      page_compressed<VB>(a, sA, wst + (k % STAGES) * L::TILE, st, lane);
       __syncwarp();
     }
     cp_wait<0>();
@@ -681,10 +701,12 @@ cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     ctx->launches++;
   }
-  e = cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TOTAL);
+  auto kern = ctx->cfg.value_bits == 4 ? tc_decode_kernel<4> : tc_decode_kernel<2>;
+  const size_t smem = ctx->cfg.value_bits == 4 ? TcTile<4>::SMEM_TOTAL : TcTile<2>::SMEM_TOTAL;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   prof_start(ctx, kProfDecode, s);
-  tc_decode_kernel<<<dim3(a.n_parts, hgroups, batch), 128, SMEM_TOTAL, s>>>(a);
+  kern<<<dim3(a.n_parts, hgroups, batch), 128, smem, s>>>(a);
   prof_stop(ctx, kProfDecode, s);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

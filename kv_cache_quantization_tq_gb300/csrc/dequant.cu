@@ -110,11 +110,14 @@ __device__ bool load_tiles(const DqArgs& a, uint8_t* tiles, int b, int h, int pa
 }
 
 // ------------------------------------------------------------------ main layout
-template <int D>
+// VB = value bits (2 or 4): value codes take VB * d / 8 bytes per token.
+template <int D, int VB>
 struct MainDq {
   static constexpr int E = D / 32;
   static constexpr int TB = D >= 512 ? 16 : 32;          // tokens per CTA
-  static constexpr int TILE = 12 * D + 64;
+  static constexpr int TILE = (8 + 2 * VB) * D + 64;
+  static constexpr int O_VSM = (6 + 2 * VB) * D;
+  static constexpr int O_NORM = (8 + 2 * VB) * D;
   static constexpr int THREADS = 256;
   static constexpr int PAGES = TB / 16;
   static constexpr int WPP = (THREADS / 32) / PAGES;       // warps per page
@@ -125,9 +128,9 @@ struct MainDq {
   static constexpr size_t SMEM = SMEM_TILES + SMEM_CORR;
 };
 
-template <int D>
+template <int D, int VB>
 __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
-  using C = MainDq<D>;
+  using C = MainDq<D, VB>;
   constexpr int E = C::E;
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* tiles = smem;
@@ -199,8 +202,8 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
     const int slot = tt & 15;
     const uint32_t* kh = reinterpret_cast<const uint32_t*>(tile + slot * (D / 8));
     const uint32_t* kl = reinterpret_cast<const uint32_t*>(tile + 2 * D + slot * (D / 8));
-    const float nk = __half2float(reinterpret_cast<const __half*>(tile + 12 * D)[slot]);
-    const float nr = __half2float(reinterpret_cast<const __half*>(tile + 12 * D + 32)[slot]);
+    const float nk = __half2float(reinterpret_cast<const __half*>(tile + C::O_NORM)[slot]);
+    const float nr = __half2float(reinterpret_cast<const __half*>(tile + C::O_NORM + 32)[slot]);
     const int bit = 16 * (lane >> 4) + (lane & 15);
     float x[E];
 #pragma unroll
@@ -210,14 +213,15 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
     }
     wht_warp<E>(x, lane);
     const size_t row = (((size_t)b * a.hkv + h) * a.max_tokens + tok0 + tt) * D;
-    const uint32_t* vq = reinterpret_cast<const uint32_t*>(tile + 6 * D);
-    const int vbit = 16 * (slot & 1) + 2 * (slot >> 1);
+    // 2-bit: token 2j+e at bits 16e+2j of word c; 4-bit: tokens 8w+2j+e at bits 16e+4j of word w*d+c
+    const uint32_t* vq = reinterpret_cast<const uint32_t*>(tile + 6 * D) + (VB == 4 && slot >= 8 ? D : 0);
+    const int vbit = VB == 2 ? 16 * (slot & 1) + 2 * (slot >> 1) : 16 * (slot & 1) + 4 * ((slot & 7) >> 1);
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int c = coord_of(e, lane);
       a.k_out[row + c] = __float2half_rn(nk * (x[e] * sg[e] * rs));
-      const __half2 smn = *reinterpret_cast<const __half2*>(tile + 10 * D + (slot * (D / 32) + e) * 4);
-      const float q = (float)((vq[c] >> vbit) & 3u);
+      const __half2 smn = *reinterpret_cast<const __half2*>(tile + C::O_VSM + (slot * (D / 32) + e) * 4);
+      const float q = (float)((vq[c] >> vbit) & ((1u << VB) - 1u));
       a.v_out[row + c] = __float2half_rn(fmaf(__low2float(smn), q, __high2float(smn)));
     }
   }
@@ -335,16 +339,21 @@ cudaError_t launch_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, con
   a.err = ctx->d_err;
   const int d = ctx->cfg.head_dim;
   const bool main = ctx->cfg.layout == TQ_LAYOUT_MAIN;
+  const int vb = ctx->cfg.value_bits;
   cudaError_t e = cudaErrorInvalidValue;
   if (max_tokens > 0) {
     switch (d) {
-      case 64: e = main ? launch_dq<MainDq<64>>(dequant_main_kernel<64>, a, batch, s)
+      case 64: e = main ? (vb == 4 ? launch_dq<MainDq<64, 4>>(dequant_main_kernel<64, 4>, a, batch, s)
+                                  : launch_dq<MainDq<64, 2>>(dequant_main_kernel<64, 2>, a, batch, s))
                         : launch_dq<AltDq<64>>(dequant_alt_kernel<64>, a, batch, s); break;
-      case 128: e = main ? launch_dq<MainDq<128>>(dequant_main_kernel<128>, a, batch, s)
+      case 128: e = main ? (vb == 4 ? launch_dq<MainDq<128, 4>>(dequant_main_kernel<128, 4>, a, batch, s)
+                                  : launch_dq<MainDq<128, 2>>(dequant_main_kernel<128, 2>, a, batch, s))
                          : launch_dq<AltDq<128>>(dequant_alt_kernel<128>, a, batch, s); break;
-      case 256: e = main ? launch_dq<MainDq<256>>(dequant_main_kernel<256>, a, batch, s)
+      case 256: e = main ? (vb == 4 ? launch_dq<MainDq<256, 4>>(dequant_main_kernel<256, 4>, a, batch, s)
+                                  : launch_dq<MainDq<256, 2>>(dequant_main_kernel<256, 2>, a, batch, s))
                          : launch_dq<AltDq<256>>(dequant_alt_kernel<256>, a, batch, s); break;
-      case 512: e = main ? launch_dq<MainDq<512>>(dequant_main_kernel<512>, a, batch, s)
+      case 512: e = main ? (vb == 4 ? launch_dq<MainDq<512, 4>>(dequant_main_kernel<512, 4>, a, batch, s)
+                                  : launch_dq<MainDq<512, 2>>(dequant_main_kernel<512, 2>, a, batch, s))
                          : launch_dq<AltDq<512>>(dequant_alt_kernel<512>, a, batch, s); break;
     }
     if (e != cudaSuccess) return e;

@@ -75,11 +75,16 @@ __global__ void sketch_frag_enc_kernel(const float* __restrict__ s, int d, uint4
 }
 
 // ------------------------------------------------------------------ main layout
-template <int D>
+// VB = value bits (2 or 4): the value-code plane is VB * d / 8 bytes per token (turboquant
+// vLLM guide, --value-bits), followed by the group scale / minimum and the two norm rows.
+template <int D, int VB>
 struct MainEnc {
   static constexpr int E = D / 32;
   static constexpr int TB = D <= 128 ? 128 : (D == 256 ? 64 : 32);
-  static constexpr int TILE = 12 * D + 64;
+  static constexpr int TILE = (8 + 2 * VB) * D + 64;
+  static constexpr int O_VQ = 6 * D;                   // value codes
+  static constexpr int O_VSM = (6 + 2 * VB) * D;       // fp16 scale, minimum per (token, group)
+  static constexpr int O_NORM = (8 + 2 * VB) * D;      // fp16 key norms, then residual norms
   static constexpr int THREADS = 256;
   static constexpr int RS = D + 8;                     // residual row stride (halves): conflict-free fragments
   static constexpr size_t SMEM_R = 2 * sizeof(__half) * TB * RS;  // high and low parts
@@ -105,9 +110,9 @@ __device__ void store_tiles(const EncArgs& a, const uint8_t* tiles, int npages, 
   }
 }
 
-template <int D>
+template <int D, int VB>
 __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int ntok, int start, uint8_t* smem) {
-  using C = MainEnc<D>;
+  using C = MainEnc<D, VB>;
   constexpr int E = C::E;
   constexpr int TB = C::TB;
   __half* rh = reinterpret_cast<__half*>(smem);                 // [TB][RS] residual, fp16 high part
@@ -161,16 +166,16 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
     }
     const float nr = sqrtf(warp_sum(rr));
     if (lane == 0) {
-      reinterpret_cast<__half*>(tile + 12 * D)[slot] = __float2half_rn(nk);
-      reinterpret_cast<__half*>(tile + 12 * D + 32)[slot] = __float2half_rn(nr);
+      reinterpret_cast<__half*>(tile + C::O_NORM)[slot] = __float2half_rn(nk);
+      reinterpret_cast<__half*>(tile + C::O_NORM + 32)[slot] = __float2half_rn(nr);
     }
     // values: group e = coordinates 32e..32e+31, one per lane
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      GroupCode g = group_quant_lane(vv[e], 3.f);
+      GroupCode g = group_quant_lane(vv[e], (float)((1 << VB) - 1));
       vcodes[tt * D + coord_of(e, lane)] = (uint8_t)g.q;
       if (lane == 0) {
-        __half* sm = reinterpret_cast<__half*>(tile + 10 * D + (slot * (D / 32) + e) * 4);
+        __half* sm = reinterpret_cast<__half*>(tile + C::O_VSM + (slot * (D / 32) + e) * 4);
         sm[0] = g.s;
         sm[1] = g.mn;
       }
@@ -239,13 +244,22 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
       }
     }
   }
-  // ---- phase 3: dimension-major value-code words (token 2j+e at bits 16e+2j)
-  for (int w = threadIdx.x; w < (ntok >> 4) * D; w += C::THREADS) {
-    const int p = w / D, i = w % D;
+  // ---- phase 3: dimension-major value-code words. 2-bit: one word per dimension, token 2j+e at
+  // bits 16e+2j. 4-bit: two words per dimension (all first words, then all second words), word w
+  // holding tokens 8w+2j+e at bits 16e+4j.
+  for (int w = threadIdx.x; w < (ntok >> 4) * D * (VB / 2); w += C::THREADS) {
+    const int p = w / (D * (VB / 2)), i = w % (D * (VB / 2));
     uint32_t word = 0;
+    if (VB == 2) {
 #pragma unroll
-    for (int s = 0; s < 16; ++s) word |= (uint32_t)vcodes[(p * 16 + s) * D + i] << (16 * (s & 1) + 2 * (s >> 1));
-    reinterpret_cast<uint32_t*>(tiles + (size_t)p * C::TILE + 6 * D)[i] = word;
+      for (int s = 0; s < 16; ++s) word |= (uint32_t)vcodes[(p * 16 + s) * D + i] << (16 * (s & 1) + 2 * (s >> 1));
+    } else {
+      const int half = i / D, dim = i % D;
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        word |= (uint32_t)vcodes[(p * 16 + 8 * half + s) * D + dim] << (16 * (s & 1) + 4 * (s >> 1));
+    }
+    reinterpret_cast<uint32_t*>(tiles + (size_t)p * C::TILE + C::O_VQ)[i] = word;
   }
   __syncthreads();
   store_tiles<C::TILE>(a, tiles, ntok >> 4, b, h, (start + tok0) >> 4);
@@ -335,11 +349,12 @@ __device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int n
 }
 
 // ------------------------------------------------------------------ kernels
-template <int D, bool MAIN>
+// VB: value bits of the main layout (2 or 4), 0 for the alternate layout.
+template <int D, int VB>
 __global__ void __launch_bounds__(256) encode_kernel(EncArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int b = blockIdx.z, h = blockIdx.y;
-  constexpr int TB = MAIN ? MainEnc<D>::TB : AltEnc<D>::TB;
+  constexpr int TB = VB ? MainEnc<D, (VB ? VB : 2)>::TB : AltEnc<D>::TB;
   const int tok0 = blockIdx.x * TB;
   const int ntok = min(TB, a.n_tokens - tok0);
   const int start = a.start_pos[b];
@@ -347,8 +362,8 @@ __global__ void __launch_bounds__(256) encode_kernel(EncArgs a) {
     if (threadIdx.x == 0) flag_error(a.err, TQ_DEVERR_POSITION);
     return;
   }
-  if (MAIN)
-    encode_main_block<D>(a, b, h, tok0, ntok, start, smem);
+  if (VB)
+    encode_main_block<D, (VB ? VB : 2)>(a, b, h, tok0, ntok, start, smem);
   else
     encode_alt_block<D>(a, b, h, tok0, ntok, start, smem);
 }
@@ -362,7 +377,7 @@ struct AppendArgs {
   __half* ring_v;
 };
 
-template <int D, bool MAIN>
+template <int D, int VB>
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int b = blockIdx.y, h = blockIdx.x;
@@ -373,11 +388,11 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   }
   if (pos > 0 && (pos % kRing) == 0) {
     const int start = pos - kRing;
-    constexpr int TB = MAIN ? MainEnc<D>::TB : AltEnc<D>::TB;
+    constexpr int TB = VB ? MainEnc<D, (VB ? VB : 2)>::TB : AltEnc<D>::TB;
     static_assert(kRing % TB == 0, "ring flush is a whole number of encode batches");
     for (int t0 = 0; t0 < kRing; t0 += TB) {
-      if (MAIN)
-        encode_main_block<D>(a.enc, b, h, t0, TB, start, smem);
+      if (VB)
+        encode_main_block<D, (VB ? VB : 2)>(a.enc, b, h, t0, TB, start, smem);
       else
         encode_alt_block<D>(a.enc, b, h, t0, TB, start, smem);
       __syncthreads();
@@ -392,11 +407,11 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   }
 }
 
-template <int D, bool MAIN>
+template <int D, int VB>
 cudaError_t launch_encode_t(const EncArgs& a, int batch, cudaStream_t s) {
-  constexpr int TB = MAIN ? MainEnc<D>::TB : AltEnc<D>::TB;
-  constexpr size_t SMEM = MAIN ? MainEnc<D>::SMEM : AltEnc<D>::SMEM;
-  auto kern = encode_kernel<D, MAIN>;
+  constexpr int TB = VB ? MainEnc<D, (VB ? VB : 2)>::TB : AltEnc<D>::TB;
+  constexpr size_t SMEM = VB ? MainEnc<D, (VB ? VB : 2)>::SMEM : AltEnc<D>::SMEM;
+  auto kern = encode_kernel<D, VB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((a.n_tokens + TB - 1) / TB, a.hkv, batch);
@@ -404,10 +419,10 @@ cudaError_t launch_encode_t(const EncArgs& a, int batch, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int D, bool MAIN>
+template <int D, int VB>
 cudaError_t launch_append_t(const AppendArgs& a, int batch, cudaStream_t s) {
-  constexpr size_t SMEM = MAIN ? MainEnc<D>::SMEM : AltEnc<D>::SMEM;
-  auto kern = append_kernel<D, MAIN>;
+  constexpr size_t SMEM = VB ? MainEnc<D, (VB ? VB : 2)>::SMEM : AltEnc<D>::SMEM;
+  auto kern = append_kernel<D, VB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(a.enc.hkv, batch);
@@ -441,14 +456,14 @@ cudaError_t launch_encode(tq_ctx* ctx, const void* k, const void* v, int batch, 
                           const int32_t* start_pos, const int32_t* block_table, int max_blocks, void* pool,
                           int num_blocks, cudaStream_t s) {
   EncArgs a = make_args(ctx, k, v, src_tokens, n_tokens, start_pos, block_table, max_blocks, pool, num_blocks);
-  const bool main = ctx->cfg.layout == TQ_LAYOUT_MAIN;
+  const int vb = ctx->cfg.layout == TQ_LAYOUT_MAIN ? ctx->cfg.value_bits : 0;
   cudaError_t e = cudaErrorInvalidValue;
   prof_start(ctx, kProfEncode, s);
   switch (ctx->cfg.head_dim) {
-    case 64: e = main ? launch_encode_t<64, true>(a, batch, s) : launch_encode_t<64, false>(a, batch, s); break;
-    case 128: e = main ? launch_encode_t<128, true>(a, batch, s) : launch_encode_t<128, false>(a, batch, s); break;
-    case 256: e = main ? launch_encode_t<256, true>(a, batch, s) : launch_encode_t<256, false>(a, batch, s); break;
-    case 512: e = main ? launch_encode_t<512, true>(a, batch, s) : launch_encode_t<512, false>(a, batch, s); break;
+    case 64: e = vb == 4 ? launch_encode_t<64, 4>(a, batch, s) : vb == 2 ? launch_encode_t<64, 2>(a, batch, s) : launch_encode_t<64, 0>(a, batch, s); break;
+    case 128: e = vb == 4 ? launch_encode_t<128, 4>(a, batch, s) : vb == 2 ? launch_encode_t<128, 2>(a, batch, s) : launch_encode_t<128, 0>(a, batch, s); break;
+    case 256: e = vb == 4 ? launch_encode_t<256, 4>(a, batch, s) : vb == 2 ? launch_encode_t<256, 2>(a, batch, s) : launch_encode_t<256, 0>(a, batch, s); break;
+    case 512: e = vb == 4 ? launch_encode_t<512, 4>(a, batch, s) : vb == 2 ? launch_encode_t<512, 2>(a, batch, s) : launch_encode_t<512, 0>(a, batch, s); break;
   }
   prof_stop(ctx, kProfEncode, s);
   if (e == cudaSuccess) ctx->launches++;
@@ -465,13 +480,13 @@ cudaError_t launch_append(tq_ctx* ctx, const void* k_new, const void* v_new, con
   a.pos = pos;
   a.ring_k = static_cast<__half*>(ring_k);
   a.ring_v = static_cast<__half*>(ring_v);
-  const bool main = ctx->cfg.layout == TQ_LAYOUT_MAIN;
+  const int vb = ctx->cfg.layout == TQ_LAYOUT_MAIN ? ctx->cfg.value_bits : 0;
   cudaError_t e = cudaErrorInvalidValue;
   switch (ctx->cfg.head_dim) {
-    case 64: e = main ? launch_append_t<64, true>(a, batch, s) : launch_append_t<64, false>(a, batch, s); break;
-    case 128: e = main ? launch_append_t<128, true>(a, batch, s) : launch_append_t<128, false>(a, batch, s); break;
-    case 256: e = main ? launch_append_t<256, true>(a, batch, s) : launch_append_t<256, false>(a, batch, s); break;
-    case 512: e = main ? launch_append_t<512, true>(a, batch, s) : launch_append_t<512, false>(a, batch, s); break;
+    case 64: e = vb == 4 ? launch_append_t<64, 4>(a, batch, s) : vb == 2 ? launch_append_t<64, 2>(a, batch, s) : launch_append_t<64, 0>(a, batch, s); break;
+    case 128: e = vb == 4 ? launch_append_t<128, 4>(a, batch, s) : vb == 2 ? launch_append_t<128, 2>(a, batch, s) : launch_append_t<128, 0>(a, batch, s); break;
+    case 256: e = vb == 4 ? launch_append_t<256, 4>(a, batch, s) : vb == 2 ? launch_append_t<256, 2>(a, batch, s) : launch_append_t<256, 0>(a, batch, s); break;
+    case 512: e = vb == 4 ? launch_append_t<512, 4>(a, batch, s) : vb == 2 ? launch_append_t<512, 2>(a, batch, s) : launch_append_t<512, 0>(a, batch, s); break;
   }
   if (e == cudaSuccess) ctx->launches++;
   return e;

@@ -130,7 +130,8 @@ tq_status check_config(const tq_config* c) {
   const int groups = (n_rep + tq::kMaxRep - 1) / tq::kMaxRep;
   if (n_rep % groups) return TQ_ERR_UNSUPPORTED;
   if (c->layout == TQ_LAYOUT_MAIN) {
-    if (c->key_bits != 3 || c->value_bits != 2 || c->qjl_m != c->head_dim) return TQ_ERR_UNSUPPORTED;
+    if (c->key_bits != 3 || (c->value_bits != 2 && c->value_bits != 4) || c->qjl_m != c->head_dim)
+      return TQ_ERR_UNSUPPORTED;
   } else if (c->layout == TQ_LAYOUT_ALT) {
     if (c->key_bits != 8 || c->value_bits != 3) return TQ_ERR_UNSUPPORTED;
   } else {
@@ -381,7 +382,10 @@ tq_status tq_get_tables(const tq_ctx* ctx, float* centroids, float* boundaries, 
 size_t tq_bytes_per_token_head(const tq_ctx* ctx) {
   if (!ctx) return 0;
   const size_t d = ctx->cfg.head_dim;
-  return ctx->cfg.layout == TQ_LAYOUT_MAIN ? (3 * d) / 4 + 4 : (3 * d) / 2 + 2;
+  // main: 3 key bits, value_bits value bits and one fp16 scale + minimum per group of 32 per
+  // coordinate, two fp16 norms; alternate: 8-bit keys + 4 B per block of 32, 3-bit values, fp16 norm
+  const size_t vb = ctx->cfg.value_bits;
+  return ctx->cfg.layout == TQ_LAYOUT_MAIN ? (3 * d) / 8 + (vb * d) / 8 + d / 8 + 4 : (3 * d) / 2 + 2;
 }
 
 size_t tq_page_bytes(const tq_ctx* ctx) { return tq::kPage * tq_bytes_per_token_head(ctx); }

@@ -22,10 +22,10 @@ def oracle_tables(seed, d, layout_main=True):
     return c32, signs, sketch
 
 
-def make_ctx(tq, layout_main, d, hq, hkv, seed):
+def make_ctx(tq, layout_main, d, hq, hkv, seed, value_bits=None):
     c32, signs, sketch = oracle_tables(seed, d, layout_main)
     lay = tq.TQ_LAYOUT_MAIN if layout_main else tq.TQ_LAYOUT_ALT
-    ctx = tq.Context(lay, d, hq, hkv, seed, centroids=c32, signs=signs, sketch=sketch)
+    ctx = tq.Context(lay, d, hq, hkv, seed, centroids=c32, signs=signs, sketch=sketch, value_bits=value_bits)
     return ctx, c32.astype(np.float64), signs.astype(np.float64), sketch
 
 
@@ -48,6 +48,7 @@ def plane_bits(words_u32):
 def main_fields(tiles, d):
     t = np.ascontiguousarray(tiles)
     lead = t.shape[:-1]
+    o_n = t.shape[-1] - 64  # norms sit in the last 64 bytes (2- or 4-bit value codes before them)
     w = lambda off, n: np.ascontiguousarray(t[..., off:off + n]).view("<u4")
     kh = plane_bits(w(0, 2 * d).reshape(lead + (16, d // 32)))
     kl = plane_bits(w(2 * d, 2 * d).reshape(lead + (16, d // 32)))
@@ -55,9 +56,9 @@ def main_fields(tiles, d):
     return {
         "idx": 2 * kh + kl,
         "sigma": ks,
-        "v_bytes": t[..., 6 * d:12 * d],
-        "kn": np.ascontiguousarray(t[..., 12 * d:12 * d + 32]).view("<i2"),
-        "rn": np.ascontiguousarray(t[..., 12 * d + 32:12 * d + 64]).view("<i2"),
+        "v_bytes": t[..., 6 * d:o_n],
+        "kn": np.ascontiguousarray(t[..., o_n:o_n + 32]).view("<i2"),
+        "rn": np.ascontiguousarray(t[..., o_n + 32:o_n + 64]).view("<i2"),
     }
 
 
@@ -92,7 +93,7 @@ def allclose_report(got, ref, atol=2e-3, rtol=1e-3):
 
 
 # ---------------------------------------------------------------- decode scenarios
-def build_main_cache(seed, d, hkv, lengths, centroids, signs, sketch, shuffled=True, extra_blocks=0):
+def build_main_cache(seed, d, hkv, lengths, centroids, signs, sketch, shuffled=True, extra_blocks=0, value_bits=2):
     """Oracle-encoded pool + ring for sequences of the given total lengths."""
     bsz = len(lengths)
     lmax = max(max(lengths), 1)
@@ -101,7 +102,7 @@ def build_main_cache(seed, d, hkv, lengths, centroids, signs, sketch, shuffled=T
     max_blocks = max(t_all // 16, 1)
     bt = synth.block_table(seed, bsz, max_blocks, shuffled)
     nblk = bsz * max_blocks + extra_blocks
-    pool = np.zeros((nblk, hkv, layout.main_tile_bytes(d)), np.uint8)
+    pool = np.zeros((nblk, hkv, layout.main_tile_bytes(d, value_bits)), np.uint8)
     n_c = np.zeros(bsz, np.int32)
     n_b = np.zeros(bsz, np.int32)
     ring_k = np.zeros((bsz, hkv, 128, d), np.float16)
