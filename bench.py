@@ -52,6 +52,9 @@ WORKLOADS = {
     "alt-d512": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=512, ctx=65536, shuffled=False, seed=0),
     "qwen2.5-32b-ragged": dict(layout="main", layers=1, batch=16, hq=40, hkv=8, d=128, ctx=None, lo=1024, hi=131072,
                                shuffled=True, seed=7),
+    # the batch-8 geometry with 4-bit value codes (--value-bits 4)
+    "qwen2.5-7b-b8-v4": dict(layout="main", layers=28, batch=8, hq=28, hkv=4, d=128, ctx=32768, shuffled=True, seed=0,
+                             vbits=4),
 }
 DEFAULT_WORKLOAD = "qwen3-0.6b-32k"
 
@@ -66,7 +69,7 @@ def ring_split(length: int):
 
 def record_bytes(w) -> int:
     d = w["d"]
-    return (3 * d) // 4 + 4 if w["layout"] == "main" else (3 * d) // 2 + 2
+    return (3 * d) // 8 + (w.get("vbits", 2) * d) // 8 + d // 8 + 4 if w["layout"] == "main" else (3 * d) // 2 + 2
 
 
 def step_bytes(w, lengths_after_append):
@@ -180,7 +183,8 @@ class Layer:
 
     def __init__(self, tq, torch, w, layer_idx, lengths, max_len, bt_np):
         lay = tq.TQ_LAYOUT_MAIN if w["layout"] == "main" else tq.TQ_LAYOUT_ALT
-        self.ctx = tq.Context(lay, w["d"], w["hq"], w["hkv"], w["seed"] + layer_idx)
+        self.ctx = tq.Context(lay, w["d"], w["hq"], w["hkv"], w["seed"] + layer_idx,
+                              value_bits=w.get("vbits") if w["layout"] == "main" else None)
         self.max_blocks = bt_np.shape[1]
         self.bt = torch.from_numpy(bt_np).cuda()
         nblk = bt_np.shape[0] * bt_np.shape[1]
@@ -494,7 +498,7 @@ def oracle_layer_step(w, seed, sample_len):
         sg, sk = rng.signs(seed, d), rng.gaussian_matrix(seed, d, d)
         k, v = synth.kv_main(seed, 1, hkv, L, d)
         bt = np.arange((L + 15) // 16, dtype=np.int32)[None, :]
-        pool = np.zeros((bt.shape[1], hkv, layout.main_tile_bytes(d)), np.uint8)
+        pool = np.zeros((bt.shape[1], hkv, layout.main_tile_bytes(d, w.get("vbits", 2))), np.uint8)
         cache.encode_main_range(pool, bt, 0, k[:, :, :nc], v[:, :, :nc], sg, c, sk)
         ring_k = np.zeros((1, hkv, 128, d), np.float16)
         ring_v = np.zeros_like(ring_k)
@@ -572,6 +576,8 @@ def main():
               "q_heads": w["hq"], "kv_heads": w["hkv"], "head_dim": w["d"],
               "context": w["ctx"] if w["ctx"] is not None else f"U[{w['lo']},{w['hi']}]",
               "l2": "inputs larger than L2 (every step reads all layers' pools)"}
+    if w["layout"] == "main":
+        config["value_bits"] = w.get("vbits", 2)
 
     if args.impl == "reference":
         if rank != 0:
