@@ -108,7 +108,6 @@ def aggregate_gbs(bytes_per_rank: int, ms_max: float, world: int) -> float:
 # profiles/ (dram__bytes_read.sum + dram__bytes_write.sum).  An entry is valid only for the
 # kernel source it was captured on; a workload without one reports null.
 NCU_TRAFFIC = {
-    ("alt-d128", "decode_alt_v2_kernel"): 411806976,      # profiles/decode_alt_v2_kernel__alt-d128.md
 }
 
 
@@ -134,24 +133,38 @@ class ClockSampler:
         self.gpu = ids[local_index].strip() if local_index < len(ids) else str(local_index)
         self.proc = None
         self.lines = []
+        self.stamped = []
 
     def __enter__(self):
+        # The sampler is started and its first sample awaited before the timed region, and the
+        # region is bracketed by timestamps: samples from 50 ms before it to 50 ms after it count,
+        # and at least one sample after its end is awaited, so a region shorter than the 20 ms
+        # sampling period still gets the samples around it.
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.time() + 5.0
+            while not self.stamped and time.time() < deadline:
+                time.sleep(0.005)
         except (OSError, FileNotFoundError):
             self.proc = None
+        self.t0 = time.time()
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.stamped.append((time.time(), line.strip()))
 
     def __exit__(self, *exc):
+        self.t1 = time.time()
         if self.proc is not None:
+            deadline = time.time() + 1.0
+            while time.time() < deadline and not any(ts > self.t1 for ts, _ in self.stamped):
+                time.sleep(0.005)
+            self.lines = [ln for ts, ln in self.stamped if self.t0 - 0.05 <= ts <= self.t1 + 0.05]
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)

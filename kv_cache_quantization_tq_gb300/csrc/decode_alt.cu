@@ -7,9 +7,15 @@
 // pages: each warp walks its own pages through a cp.async pipeline, lane l
 // owns the E = d/32 consecutive dimensions [l E, l E + E):
 //
-//   logit_t = sum_b s_b <q_b, code_b> + mn_b sum(q_b)       (per lane: its block)
-//   the 16 per-lane partials of a page are summed over the warp with a
-//   transposed butterfly (16 shuffles per page), so lane l ends with token l/2;
+//   logit_t = sum_b s_b <q_b, code_b> + mn_b sum(q_b)
+//   The block dots <q_b, code_b> of a page are one small dense product on the
+//   tensor cores (mma.sync m16n8k16): rows = the 16 tokens, k = coordinates,
+//   columns = (query head, block of 32) with B holding q restricted to the
+//   block.  Codes enter as the exact fp16 value 1024 + code (one byte-permute
+//   per pair), the 1024 sum(q_b) offset is removed per block in fp32.  The key
+//   rows are XOR-swizzled by 16-byte chunk as they are copied in, so the
+//   fragment loads are free of bank conflicts.  Scores then move to lane
+//   l = token l/2 for the softmax and value steps;
 //   online softmax per head; v_rot += p_t n_v,t c[idx_t] in the rotated domain;
 //   one inverse rotation per chunk ("TurboQuant-MLX overview", GPU kernel
 //   section: butterfly pulled out of the value sum).
@@ -59,9 +65,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// byte k of w as a float (exact): the byte becomes the low mantissa of 2^23 + byte
-__device__ __forceinline__ float byte_f(uint32_t w, int k) {
-  return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | (uint32_t)k)) - 8388608.f;
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
 template <int D>
@@ -72,36 +81,22 @@ struct AltCfg {
   static constexpr size_t SMEM = (size_t)kWarps * STAGES * TILE;
 };
 
-// Sum of 16 per-lane values over the warp; lane l returns the total of value l/2.
-__device__ __forceinline__ float transpose_sum16(float (&v)[16], int lane) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const bool up = lane & 16;
-    const float send = up ? v[i] : v[i + 8];
-    const float keep = up ? v[i + 8] : v[i];
-    v[i] = keep + __shfl_xor_sync(kFull, send, 16);
+// 16-byte chunk c of key row r sits at chunk c ^ kq_swizzle(r) in shared memory: the
+// fragment loads of 8 rows at the same chunk then fall in distinct banks.
+// Whether n-tile j of the score product (columns 8j .. 8j+7 of NRG = heads x blocks) has a
+// column of block blk (G blocks per head).
+template <int G, int NRG>
+__device__ constexpr bool tile_has_block(int j, int blk) {
+  for (int c = 0; c < 8; ++c) {
+    const int n = 8 * j + c;
+    if (n < NRG && n % G == blk) return true;
   }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const bool up = lane & 8;
-    const float send = up ? v[i] : v[i + 4];
-    const float keep = up ? v[i + 4] : v[i];
-    v[i] = keep + __shfl_xor_sync(kFull, send, 8);
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const bool up = lane & 4;
-    const float send = up ? v[i] : v[i + 2];
-    const float keep = up ? v[i + 2] : v[i];
-    v[i] = keep + __shfl_xor_sync(kFull, send, 4);
-  }
-  {
-    const bool up = lane & 2;
-    const float send = up ? v[0] : v[1];
-    const float keep = up ? v[1] : v[0];
-    v[0] = keep + __shfl_xor_sync(kFull, send, 2);
-  }
-  return v[0] + __shfl_xor_sync(kFull, v[0], 1);
+  return false;
+}
+
+template <int D>
+__device__ __forceinline__ int kq_swizzle(int row) {
+  return D == 64 ? ((row >> 1) & 3) : (row & 7);
 }
 
 template <int D, int NR>
@@ -114,6 +109,7 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
   __shared__ float wm[kWarps][NR], wl[kWarps][NR];
   __shared__ float wo[kWarps][NR][D];
   __shared__ int sblk[kWarps][C::STAGES];
+  __shared__ float qsum_s[NR * G];
 
   const int part = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int kvh = hg / a.groups;
@@ -134,16 +130,30 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
     lut[tid] = c;
   }
 
-  // queries: lane's E dimensions of every head, and their sums (per lane)
-  float qv[NR][E], qs[NR];
+  // Score product: columns n = (head n / G, block n % G), NT n-tiles of 8.  Lane (g, t) holds
+  // the B fragment of column 8j + g for the two k-steps of its block (k-step ks covers block
+  // ks / 2; within a k-step, k = 2t + u is coordinate 4t + u and k = 2t + 8 + u is 4t + 2 + u).
+  constexpr int NT = (NR * G + 7) / 8;
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t bq[NT][2][2];
 #pragma unroll
-  for (int h = 0; h < NR; ++h) {
-    qs[h] = 0.f;
+  for (int j = 0; j < NT; ++j) {
+    const int n = 8 * j + g, hh = n / G, blk = n % G;
+    const bool valid = n < NR * G && hh < a.nrg;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      qv[h][e] = h < a.nrg ? __half2float(a.q[((size_t)b * a.hq + h0 + h) * D + lane * E + e]) : 0.f;
-      qs[h] += qv[h][e];
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t* qw = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * a.hq + h0 + (valid ? hh : 0)) * D +
+                                                             16 * (2 * blk + u) + 4 * t);
+      bq[j][u][0] = valid ? qw[0] : 0u;
+      bq[j][u][1] = valid ? qw[1] : 0u;
     }
+  }
+  // sum of q over each (head, block), for the C columns 8j + 2t + u this lane holds
+  for (int idx = warp; idx < NR * G; idx += kWarps) {
+    const int hh = idx / G, blk = idx % G;
+    float v = hh < a.nrg ? __half2float(a.q[((size_t)b * a.hq + h0 + hh) * D + 32 * blk + lane]) : 0.f;
+    v = warp_sum(v);
+    if (lane == 0) qsum_s[idx] = v;
   }
   float m_run[NR], l_run[NR], acc[NR][E];
 #pragma unroll
@@ -153,7 +163,15 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[h][e] = 0.f;
   }
-  __syncthreads();  // lut
+  __syncthreads();  // lut, qsum_s
+  float qsc[NT][2];
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int n = 8 * j + 2 * t + u;
+      qsc[j][u] = n < NR * G ? qsum_s[n] : 0.f;
+    }
 
   const float scale = kLog2e / sqrtf((float)D);
   const int pbeg = tbeg >> 4;
@@ -169,7 +187,14 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
       if (blk >= 0 && blk < a.num_blocks) {
         const uint8_t* src = a.pool + ((size_t)blk * a.hkv + kvh) * C::TILE;
         uint8_t* dst = wst + (k % C::STAGES) * C::TILE;
-        for (int c = lane; c < C::TILE / 16; c += 32) cp16(dst + c * 16, src + c * 16);
+        for (int c = lane; c < C::TILE / 16; c += 32) {
+          int cd = c;
+          if (c < D) {  // key rows: 16 rows x D/16 chunks, swizzled
+            const int row = c / (D / 16), ch = c % (D / 16);
+            cd = row * (D / 16) + (ch ^ kq_swizzle<D>(row));
+          }
+          cp16(dst + cd * 16, src + c * 16);
+        }
       }
     }
     cp_commit();
@@ -177,8 +202,6 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
 #pragma unroll
   for (int k = 0; k < C::STAGES - 1; ++k) issue(k, blk_of(k));
   int nxt = blk_of(C::STAGES - 1);
-  const int blk_lane = lane * E;  // first dimension of this lane
-  const int my_block = blk_lane >> 5;
   for (int k = 0; k < nw; ++k) {
     __syncwarp();  // every lane is done with the slot and stage that are refilled next
     const int cur = nxt;
@@ -192,32 +215,62 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
       continue;
     }
     const uint8_t* T = wst + (k % C::STAGES) * C::TILE;
-    const __half* ksm = reinterpret_cast<const __half*>(T + 16 * D);
+    const __half2* ksm2 = reinterpret_cast<const __half2*>(T + 16 * D);
     const uint32_t* vi = reinterpret_cast<const uint32_t*>(T + 18 * D);
     const __half* vn = reinterpret_cast<const __half*>(T + 24 * D);
+    // C[token][column] = sum over the column's block of (1024 + code) q_head
+    float cacc[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) cacc[j][r] = 0.f;
+    {
+      const uint8_t* r0 = T + g * D + 4 * t;
+      const uint8_t* r1 = T + (g + 8) * D + 4 * t;
+      const int sw0 = kq_swizzle<D>(g), sw1 = kq_swizzle<D>(g + 8);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(r0 + 16 * (ks ^ sw0));
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(r1 + 16 * (ks ^ sw1));
+        uint4 A;
+        A.x = __byte_perm(w0, 0x64646464u, 0x4140u);  // row g: coordinates 4t, 4t+1 as 1024 + code
+        A.y = __byte_perm(w1, 0x64646464u, 0x4140u);  // row g + 8
+        A.z = __byte_perm(w0, 0x64646464u, 0x4342u);  // row g: coordinates 4t+2, 4t+3
+        A.w = __byte_perm(w1, 0x64646464u, 0x4342u);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          if (tile_has_block<G, NR * G>(j, ks / 2)) {
+            const bool mine = (8 * j + g) % G == ks / 2;
+            mma_f16(cacc[j], A, mine ? bq[j][ks & 1][0] : 0u, mine ? bq[j][ks & 1][1] : 0u);
+          }
+        }
+      }
+    }
 #pragma unroll
     for (int h = 0; h < NR; ++h) {
       if (h >= a.nrg) break;
-      float sc[16];
+      float p0 = 0.f, p1 = 0.f;  // tokens g and g + 8
 #pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const uint8_t* row = T + t * D + blk_lane;
-        float dot = 0.f;
-        if (E == 2) {
-          const uint32_t w = *reinterpret_cast<const uint16_t*>(row);
-          dot = fmaf(qv[h][0], byte_f(w, 0), qv[h][1] * byte_f(w, 1));
-        } else {
+      for (int j = 0; j < NT; ++j)
 #pragma unroll
-          for (int c = 0; c < E / 4; ++c) {
-            const uint32_t w = reinterpret_cast<const uint32_t*>(row)[c];
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) dot = fmaf(qv[h][4 * c + kk], byte_f(w, kk), dot);
+        for (int u = 0; u < 2; ++u) {
+          const int n = 8 * j + 2 * t + u;
+          if (n < NR * G && n / G == h) {
+            const int blk = n % G;
+            const float2 s0 = __half22float2(ksm2[g * G + blk]);
+            const float2 s1 = __half22float2(ksm2[(g + 8) * G + blk]);
+            const float qb = qsc[j][u];
+            p0 = fmaf(s0.x, fmaf(-1024.f, qb, cacc[j][u]), fmaf(s0.y, qb, p0));
+            p1 = fmaf(s1.x, fmaf(-1024.f, qb, cacc[j][2 + u]), fmaf(s1.y, qb, p1));
           }
         }
-        const float2 sm = __half22float2(*reinterpret_cast<const __half2*>(ksm + (t * G + my_block) * 2));
-        sc[t] = fmaf(sm.x, dot, sm.y * qs[h]);
-      }
-      const float s_tok = transpose_sum16(sc, lane) * scale;  // token lane/2
+      p0 += __shfl_xor_sync(kFull, p0, 1);
+      p0 += __shfl_xor_sync(kFull, p0, 2);
+      p1 += __shfl_xor_sync(kFull, p1, 1);
+      p1 += __shfl_xor_sync(kFull, p1, 2);
+      const int src = 4 * ((lane >> 1) & 7);
+      const float a0 = __shfl_sync(kFull, p0, src), a1 = __shfl_sync(kFull, p1, src);
+      const float s_tok = (lane < 16 ? a0 : a1) * scale;  // token lane/2
       float mx = s_tok;
 #pragma unroll
       for (int o = 16; o >= 2; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
