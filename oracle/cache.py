@@ -37,7 +37,8 @@ def encode_main_range(pool, block_table, start, k16, v16, signs, centroids, s_ma
     k16 = np.asarray(k16, dtype=np.float16)
     bsz, hkv, t, d = k16.shape
     assert start % layout.P == 0 and t % layout.P == 0
-    vbits = layout.main_value_bits(pool.shape[-1], d)
+    kbits, vbits = layout.main_bits(pool.shape[-1], d)
+    assert len(centroids) == 1 << (kbits - 1), "codebook size does not match the pool's key bits"
     enc = quant.encode_keys(k16, signs, centroids, s_mat)
     vq, vs, vmn = quant.encode_values(v16, group, vbits)
     npg = t // layout.P
@@ -50,6 +51,7 @@ def encode_main_range(pool, block_table, start, k16, v16, signs, centroids, s_ma
         enc["n_k"].reshape(bsz, hkv, npg, 16),
         enc["n_r"].reshape(bsz, hkv, npg, 16),
         vbits,
+        kbits,
     )
     pages = start // layout.P + np.arange(npg)
     blocks = np.asarray(block_table)[:, pages]  # [B, npg]

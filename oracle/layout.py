@@ -153,42 +153,52 @@ def _f16_bytes(x: np.ndarray) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- main layout
-def main_tile_bytes(d: int, vbits: int = 2) -> int:
-    """Key planes 6d, value codes 2 vbits d, value scale/minimum 2d, two norm rows 64 B."""
-    return (8 + 2 * vbits) * d + 64
+def main_tile_bytes(d: int, vbits: int = 2, kbits: int = 3) -> int:
+    """Key planes 2 kbits d (kbits - 1 Lloyd-Max index bits + 1 QJL bit per coordinate), value
+    codes 2 vbits d, value scale/minimum 2d, two norm rows 64 B."""
+    return (2 * kbits + 2 * vbits + 2) * d + 64
 
 
-def main_bytes_per_token_head(d: int, vbits: int = 2) -> float:
-    return main_tile_bytes(d, vbits) / P
+def main_bytes_per_token_head(d: int, vbits: int = 2, kbits: int = 3) -> float:
+    return main_tile_bytes(d, vbits, kbits) / P
+
+
+def main_bits(tile_bytes: int, d: int):
+    """(key bits, value bits) of a main-layout tile of the given size; key bits 2 or 3, value bits
+    2 or 4 (their sums 4..7 are distinct, so the size decides)."""
+    for kbits in (3, 2):
+        for vbits in (2, 4):
+            if main_tile_bytes(d, vbits, kbits) == tile_bytes:
+                return kbits, vbits
+    raise AssertionError((tile_bytes, d))
 
 
 def main_value_bits(tile_bytes: int, d: int) -> int:
     """Value bit width of a main-layout tile of the given size."""
-    vbits = (tile_bytes - 64 - 8 * d) // (2 * d)
-    assert vbits in (2, 4) and main_tile_bytes(d, vbits) == tile_bytes, (tile_bytes, d)
-    return vbits
+    return main_bits(tile_bytes, d)[1]
 
 
-def pack_main_tiles(idx, sigma, vq, vs16, vmn16, nk16, nr16, vbits: int = 2) -> np.ndarray:
+def pack_main_tiles(idx, sigma, vq, vs16, vmn16, nk16, nr16, vbits: int = 2, kbits: int = 3) -> np.ndarray:
     """Build main-layout tiles.
 
     Leading shape [..., 16 tokens]: idx, sigma, vq are [..., 16, d] uint8;
     vs16/vmn16 [..., 16, d/32] fp16; nk16/nr16 [..., 16] fp16.
-    Returns uint8 [..., (8 + 2 vbits) d + 64].
+    Key planes: the Lloyd-Max index bits, high bit first (one plane for 2-bit keys, two for
+    3-bit keys), then the QJL sign bits.  Returns uint8 [..., main_tile_bytes(d, vbits, kbits)].
     """
     idx = np.asarray(idx, dtype=np.uint8)
     d = idx.shape[-1]
     lead = idx.shape[:-2]
-    kh = _u32_bytes(bits_to_plane_words(idx >> 1)).reshape(lead + (2 * d,))
-    kl = _u32_bytes(bits_to_plane_words(idx & 1)).reshape(lead + (2 * d,))
+    lm_planes = [idx >> 1, idx & 1] if kbits == 3 else [idx]
+    kp = [_u32_bytes(bits_to_plane_words(pl)).reshape(lead + (2 * d,)) for pl in lm_planes]
     ks = _u32_bytes(bits_to_plane_words(sigma)).reshape(lead + (2 * d,))
     vqb = _u32_bytes(codes_to_vq_words(vq, vbits))
     sm = np.stack([np.asarray(vs16, np.float16), np.asarray(vmn16, np.float16)], axis=-1)
     vsm = _f16_bytes(sm.reshape(lead + (16 * (d // 32) * 2,)))
     kn = _f16_bytes(nk16)
     rn = _f16_bytes(nr16)
-    out = np.concatenate([kh, kl, ks, vqb, vsm, kn, rn], axis=-1)
-    assert out.shape[-1] == main_tile_bytes(d, vbits)
+    out = np.concatenate(kp + [ks, vqb, vsm, kn, rn], axis=-1)
+    assert out.shape[-1] == main_tile_bytes(d, vbits, kbits)
     return out
 
 
@@ -196,22 +206,25 @@ def unpack_main_tiles(tiles: np.ndarray, d: int) -> dict:
     t = np.asarray(tiles, dtype=np.uint8)
     lead = t.shape[:-1]
     g = d // 32
-    vb = main_value_bits(t.shape[-1], d)
-    o_sm = (6 + 2 * vb) * d
+    kb, vb = main_bits(t.shape[-1], d)
+    o_vq = 2 * kb * d
+    o_sm = o_vq + 2 * vb * d
     o_n = o_sm + 2 * d
 
     def words(off, nbytes):
         return np.ascontiguousarray(t[..., off:off + nbytes]).view("<u4")
 
-    kh = plane_words_to_bits(words(0, 2 * d).reshape(lead + (16, d // 32)))
-    kl = plane_words_to_bits(words(2 * d, 2 * d).reshape(lead + (16, d // 32)))
-    ks = plane_words_to_bits(words(4 * d, 2 * d).reshape(lead + (16, d // 32)))
-    vq = vq_words_to_codes(words(6 * d, 2 * vb * d), vb)
+    def plane(i):
+        return plane_words_to_bits(words(2 * d * i, 2 * d).reshape(lead + (16, d // 32)))
+
+    idx = 2 * plane(0) + plane(1) if kb == 3 else plane(0)
+    ks = plane(kb - 1)
+    vq = vq_words_to_codes(words(o_vq, 2 * vb * d), vb)
     sm = np.ascontiguousarray(t[..., o_sm:o_sm + 2 * d]).view("<f2").reshape(lead + (16, g, 2))
     nk = np.ascontiguousarray(t[..., o_n:o_n + 32]).view("<f2")
     nr = np.ascontiguousarray(t[..., o_n + 32:o_n + 64]).view("<f2")
     return {
-        "idx": (2 * kh + kl).astype(np.uint8),
+        "idx": idx.astype(np.uint8),
         "sigma": ks,
         "vq": vq,
         "vs": sm[..., 0].astype(np.float16),

@@ -198,3 +198,34 @@ def test_ring_split():
     assert cache.ring_split(129) == (128, 1)
     assert cache.ring_split(1024) == (896, 128)
     assert cache.ring_split(32768) == (32640, 128)
+
+
+@pytest.mark.parametrize("vbits", [2, 4])
+def test_main_tile_round_trip_2bit_keys(vbits):
+    # 2-bit keys: one Lloyd-Max plane (the 1-bit index) and the QJL plane
+    d = 128
+    g = np.random.default_rng(vbits)
+    f = {
+        "idx": g.integers(0, 2, (2, 16, d), dtype=np.uint8),
+        "sigma": g.integers(0, 2, (2, 16, d), dtype=np.uint8),
+        "vq": g.integers(0, 1 << vbits, (2, 16, d), dtype=np.uint8),
+        "vs": g.standard_normal((2, 16, d // 32)).astype(np.float16),
+        "vmn": g.standard_normal((2, 16, d // 32)).astype(np.float16),
+        "n_k": g.standard_normal((2, 16)).astype(np.float16),
+        "n_r": g.standard_normal((2, 16)).astype(np.float16),
+    }
+    t = layout.pack_main_tiles(f["idx"], f["sigma"], f["vq"], f["vs"], f["vmn"], f["n_k"], f["n_r"], vbits, 2)
+    assert t.shape[-1] == (6 + 2 * vbits) * d + 64 and layout.main_bits(t.shape[-1], d) == (2, vbits)
+    back = layout.unpack_main_tiles(t, d)
+    for k, v in f.items():
+        assert np.array_equal(back[k].view(np.uint8), v.view(np.uint8)), k
+    # the QJL plane follows the single index plane
+    assert np.array_equal(t[:, 2 * d:4 * d], layout.pack_main_tiles(
+        f["sigma"], f["sigma"], f["vq"], f["vs"], f["vmn"], f["n_k"], f["n_r"], vbits, 2)[:, 0:2 * d])
+
+
+def test_bytes_per_token_2bit_keys():
+    # 16 bytes of index bits + 16 of QJL bits, 32 of value codes, 16 of group scale/minimum, 4 of norms
+    assert layout.main_bytes_per_token_head(128, 2, 2) == 16 + 16 + 32 + 16 + 4 == 84
+    assert {layout.main_bits(layout.main_tile_bytes(64, vb, kb), 64) for kb in (2, 3) for vb in (2, 4)} == \
+        {(2, 2), (2, 4), (3, 2), (3, 4)}

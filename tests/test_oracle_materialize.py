@@ -106,3 +106,33 @@ def test_main_layout_with_4bit_values():
         assert np.all(err <= step[..., None] * (0.5 + 2e-3) + 1e-6)
         # 4-bit codes are finer than 2-bit ones: mean error well under the 2-bit half step
         assert err.mean() < (step[..., None] * 15 / 3 * 0.25).mean()
+
+
+def test_main_layout_with_2bit_keys():
+    # 1-bit Lloyd-Max index (centroids +-E|x|) plus the QJL bit: same estimator and reconstruction pins
+    seed, d, hkv, n_rep = 8, 64, 2, 3
+    sg = rng.signs(seed, d)
+    c, _ = codebook.lloyd_max(d, 1)
+    s = rng.gaussian_matrix(seed, d, d)
+    lengths = [280, 140]
+    k, v = synth.kv_main(seed, 2, hkv, 288, d)
+    bt = synth.block_table(seed, 2, 18, True)
+    pool = np.zeros((36, hkv, layout.main_tile_bytes(d, 2, 2)), np.uint8)
+    ring_k = np.zeros((2, hkv, 128, d), np.float16)
+    ring_v = np.zeros_like(ring_k)
+    n_c, n_b = np.zeros(2, np.int64), np.zeros(2, np.int64)
+    for b, L in enumerate(lengths):
+        nc, nb = cache.ring_split(L)
+        n_c[b], n_b[b] = nc, nb
+        cache.encode_main_range(pool, bt[b:b + 1], 0, k[b:b + 1, :, :nc], v[b:b + 1, :, :nc], sg, c, s)
+        ring_k[b, :, :nb] = k[b, :, nc:nc + nb]
+        ring_v[b, :, :nb] = v[b, :, nc:nc + nb]
+    q = synth.queries(seed, 2, hkv * n_rep, d)
+    ref = attention.decode_main(q, pool, bt, n_c, ring_k, ring_v, n_b, sg, c, s, hkv)
+    brute = attention.decode_main_bruteforce(q, pool, bt, n_c, ring_k, ring_v, n_b, sg, c, s, hkv)
+    assert np.allclose(ref, brute, rtol=0, atol=1e-12)
+    f = cache.read_main(pool, bt, 0, int(n_c[0]), d)
+    assert set(np.unique(f["idx"])) <= {0, 1}
+    for b in range(2):
+        kk, vv = cache.materialize_main(pool, bt, b, int(n_c[b]), ring_k, ring_v, int(n_b[b]), sg, c, s, d)
+        assert np.allclose(_attend(q[b], kk, vv, hkv), ref[b], rtol=0, atol=1e-12)
