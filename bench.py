@@ -204,7 +204,7 @@ class Layer:
         self.pool = torch.empty((nblk, w["hkv"], self.ctx.page_bytes), dtype=torch.uint8, device="cuda")
         self.ring_k = torch.zeros((w["batch"], w["hkv"], 128, w["d"]), dtype=torch.float16, device="cuda")
         self.ring_v = torch.zeros_like(self.ring_k)
-        self.out = torch.empty((w["batch"], w["hq"], w["d"]), dtype=torch.float32, device="cuda")
+        self.out = None  # a view of the step's [layers, batch, Hq, d] output buffer (build_gpu_state)
 
 
 def build_gpu_state(tq, torch, w, steps_total):
@@ -225,6 +225,10 @@ def build_gpu_state(tq, torch, w, steps_total):
     k1 = torch.from_numpy(k_np).cuda()
     v1 = torch.from_numpy(v_np).cuda()
     layers = [Layer(tq, torch, w, li, lengths, max_len, bt_np) for li in range(w["layers"])]
+    out_all = torch.empty((w["layers"], bsz, w["hq"], d), dtype=torch.float32, device="cuda")
+    for li, lay in enumerate(layers):
+        lay.out = out_all[li]
+        lay.out_all = out_all
     return lengths, k1, v1, layers
 
 
@@ -337,8 +341,9 @@ class StepGraph:
             lay.ctx.decode_attention(self.q[li], lay.pool, lay.bt, self.nc, lay.ring_k if self.main else None,
                                      lay.ring_v if self.main else None, self.nb if self.main else None,
                                      self.max_ctx, lay.out, self.ws)
-            if self.out_host is not None:
-                self.out_host[li].copy_(lay.out, non_blocking=True)
+
+        if self.out_host is not None:  # every layer's output in one copy
+            self.out_host.copy_(self.layers[0].out_all, non_blocking=True)
         if self.main:
             self.pos.add_(1)
 
@@ -474,7 +479,7 @@ def run_e2e(torch, w, layers, pos, max_ctx, ws, q, kn, vn, bytes_at, steps=16):
     qh = torch.from_numpy(rng.standard_normal(tuple(q.shape)).astype(np.float16)).pin_memory()
     kh = torch.from_numpy(rng.standard_normal(tuple(kn.shape)).astype(np.float16)).pin_memory()
     vh = torch.from_numpy(rng.standard_normal(tuple(vn.shape)).astype(np.float16)).pin_memory()
-    out_h = torch.empty((nl,) + tuple(layers[0].out.shape), dtype=torch.float32).pin_memory()
+    out_h = torch.empty(tuple(layers[0].out_all.shape), dtype=torch.float32).pin_memory()
     sg = StepGraph(torch, w, layers, pos, max_ctx, ws, q, kn, vn, out_host=out_h, in_host=(qh, kh, vh))
     sg.capture()
     torch.cuda.synchronize()

@@ -88,7 +88,8 @@ typedef struct {
   int page_size;     /* tokens per page: must be 16 */
   int ring_capacity; /* exact recent-token buffer: must be 128 */
   int layout;        /* tq_layout */
-  int key_bits;      /* main: 3 (2-bit Lloyd-Max + 1-bit QJL); alt: 8 */
+  int key_bits;      /* main: 3 (2-bit Lloyd-Max + 1-bit QJL, default) or 2 (1-bit Lloyd-Max +
+                        1-bit QJL; turboquant vLLM guide, --key-bits); alt: 8 */
   int value_bits;    /* main: 2 (default) or 4 (turboquant vLLM guide, --value-bits); alt: 3 */
   int group_size;    /* value group / key block: must be 32 */
   int qjl_m;         /* main: sketch rows m, must equal head_dim; alt: 0 */
@@ -128,7 +129,7 @@ tq_status tq_create(const tq_config* cfg, tq_ctx** out);
 
 /* As tq_create, with caller-supplied host tables instead of the generated
  * ones: centroids [2^bits] ascending and antisymmetric (c[j] == -c[K-1-j],
- * bits = 2 for main keys, 3 for alt values), signs [head_dim] of +-1, sketch
+ * bits = key_bits - 1 for main keys, 3 for alt values), signs [head_dim] of +-1, sketch
  * [qjl_m][head_dim] row-major (main only; may be NULL for alt).  Decision
  * boundaries are the midpoints of consecutive centroids. */
 tq_status tq_create_with_tables(const tq_config* cfg, const float* centroids, const float* signs,

@@ -186,10 +186,12 @@ class Context:
     """Owner of one tq_ctx (one layer's tables on the current CUDA device)."""
 
     def __init__(self, layout: int, head_dim: int, num_q_heads: int, num_kv_heads: int, seed: int = 0,
-                 centroids=None, signs=None, sketch=None, value_bits=None):
+                 centroids=None, signs=None, sketch=None, value_bits=None, key_bits=None):
         self.cfg = tq_config_init(layout, head_dim, num_q_heads, num_kv_heads, seed)
         if value_bits is not None:
             self.cfg.value_bits = value_bits  # main layout: 2 or 4
+        if key_bits is not None:
+            self.cfg.key_bits = key_bits  # main layout: 3 or 2
         ptr = C.c_void_p()
         if centroids is None:
             _check(lib.tq_create(C.byref(self.cfg), C.byref(ptr)), "tq_create")
@@ -232,7 +234,7 @@ class Context:
         return n.value
 
     def get_tables(self):
-        k = 4 if self.layout == TQ_LAYOUT_MAIN else 8
+        k = 1 << (self.cfg.key_bits - 1) if self.layout == TQ_LAYOUT_MAIN else 8
         d = self.head_dim
         c = np.zeros(k, np.float32)
         b = np.zeros(k - 1, np.float32)

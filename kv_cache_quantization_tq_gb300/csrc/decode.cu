@@ -51,6 +51,7 @@ struct DecArgs {
   int hq, hkv, n_rep, nrg, groups;
   const float* signs;
   const float* sketch_t;
+  int kb;  // main layout key bits (3 or 2)
   CodeTables tab;
   uint32_t* err;
 };
@@ -222,12 +223,12 @@ __device__ void write_part(const DecArgs& a, int b, int h0, int part, const Soft
 }
 
 // ------------------------------------------------------------------ main layout
-// VB = value bits (2 or 4): value codes take VB * d / 8 bytes per token.
+// VB = value bits (2 or 4): value codes take VB * d / 8 bytes per token.  The key bits (3 or 2:
+// one or two Lloyd-Max index planes before the QJL plane) are a run-time value; the page buffer
+// is sized for 3.
 template <int D, int NR, int VB>
 struct MainDec {
   static constexpr int TILE = (8 + 2 * VB) * D + 64;
-  static constexpr int O_VSM = (6 + 2 * VB) * D;
-  static constexpr int O_NORM = (8 + 2 * VB) * D;
   static constexpr int G = D / 32;
 };
 
@@ -297,13 +298,14 @@ __global__ void __launch_bounds__(128) decode_main_kernel(DecArgs a) {
 
   const float coef = 1.2533141373155003f / (float)D;  // sqrt(pi/2) / m, m = d
   const float scale = rsqrtf((float)D) * kLog2e;
+  const int kb = a.kb, tile_bytes = (2 * kb + 2 * VB + 2) * D + 64;
   const uint32_t* kh_w = reinterpret_cast<const uint32_t*>(tile);
-  const uint32_t* kl_w = reinterpret_cast<const uint32_t*>(tile + 2 * D);
-  const uint32_t* ks_w = reinterpret_cast<const uint32_t*>(tile + 4 * D);
-  const uint32_t* vq_w = reinterpret_cast<const uint32_t*>(tile + 6 * D);
-  const __half* vsm = reinterpret_cast<const __half*>(tile + C::O_VSM);
-  const __half* kn = reinterpret_cast<const __half*>(tile + C::O_NORM);
-  const __half* rn = reinterpret_cast<const __half*>(tile + C::O_NORM + 32);
+  const uint32_t* kl_w = reinterpret_cast<const uint32_t*>(tile + 2 * D);  // 3-bit keys only
+  const uint32_t* ks_w = reinterpret_cast<const uint32_t*>(tile + 2 * (kb - 1) * D);
+  const uint32_t* vq_w = reinterpret_cast<const uint32_t*>(tile + 2 * kb * D);
+  const __half* vsm = reinterpret_cast<const __half*>(tile + (2 * kb + 2 * VB) * D);
+  const __half* kn = reinterpret_cast<const __half*>(tile + (2 * kb + 2 * VB + 2) * D);
+  const __half* rn = kn + 16;
 
   for (int t0 = tbeg; t0 < tend; t0 += kPage) {
     const int page = t0 >> 4;
@@ -312,8 +314,8 @@ __global__ void __launch_bounds__(128) decode_main_kernel(DecArgs a) {
       if (tid == 0) flag_error(a.err, TQ_DEVERR_BLOCK_ID);
       continue;
     }
-    const uint4* src = reinterpret_cast<const uint4*>(a.pool + ((size_t)blk * a.hkv + kvh) * C::TILE);
-    for (int i = tid; i < C::TILE / 16; i += 128) reinterpret_cast<uint4*>(tile)[i] = src[i];
+    const uint4* src = reinterpret_cast<const uint4*>(a.pool + ((size_t)blk * a.hkv + kvh) * tile_bytes);
+    for (int i = tid; i < tile_bytes / 16; i += 128) reinterpret_cast<uint4*>(tile)[i] = src[i];
     __syncthreads();
     // ---- scores: 8 threads per token
     {
@@ -328,7 +330,7 @@ __global__ void __launch_bounds__(128) decode_main_kernel(DecArgs a) {
       for (int k = 0; k < D / 8; ++k) {
         const int dim = pp * (D / 8) + k;
         const int w = dim >> 5, bp = 16 * (dim & 1) + ((dim & 31) >> 1);
-        const int idx = (((khr[w] >> bp) & 1) << 1) | ((klr[w] >> bp) & 1);
+        const int idx = kb == 3 ? (int)((((khr[w] >> bp) & 1) << 1) | ((klr[w] >> bp) & 1)) : (int)((khr[w] >> bp) & 1);
         const float cv = sel4(a.tab, idx);
         const float sv = ((ksr[w] >> bp) & 1) ? 1.f : -1.f;
 #pragma unroll
@@ -685,6 +687,7 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
     t.nrg = ctx->n_rep / t.groups;
     t.signs = ctx->d_signs;
     t.sfrag_enc = ctx->d_sfrag_enc;
+    t.kb = ctx->cfg.key_bits;
     t.err = ctx->d_err;
     return launch_decode_tc(ctx, t, batch, s);
   }
@@ -714,6 +717,7 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
   a.signs = ctx->d_signs;
   a.sketch_t = ctx->d_sketch_t;
   a.tab = ctx->tab;
+  a.kb = ctx->cfg.key_bits;
   a.err = ctx->d_err;
   const int d = ctx->cfg.head_dim;
   const bool main = ctx->cfg.layout == TQ_LAYOUT_MAIN;

@@ -41,17 +41,18 @@ namespace {
 constexpr int D = 128;
 constexpr int NWARP = 4;
 constexpr int STAGES = 4;
-constexpr int KSTEPS = 24;         // 3 planes x 8 k-steps of 16 coordinates
+constexpr int KSTEPS = 24;         // up to 3 planes x 8 k-steps of 16 coordinates (8 per key bit)
 constexpr int AFRAG_U4 = KSTEPS * 32;
 constexpr size_t SMEM_A = AFRAG_U4 * sizeof(uint4);
 
-// Tile of the main layout with VB value bits (2: 1600 bytes, 4: 2112 bytes at d = 128).
-template <int VB>
+// Tile of the main layout with KB key bits (KB bit planes of 2d bytes: the Lloyd-Max index
+// bits, high first, then the QJL signs) and VB value bits (1600 bytes at KB = 3, VB = 2).
+template <int KB, int VB>
 struct TcTile {
-  static constexpr int TILE = (8 + 2 * VB) * D + 64;
-  static constexpr int O_VQ = 6 * D;
-  static constexpr int O_VSM = (6 + 2 * VB) * D;
-  static constexpr int O_NORM = (8 + 2 * VB) * D;
+  static constexpr int TILE = (2 * KB + 2 * VB + 2) * D + 64;
+  static constexpr int O_VQ = 2 * KB * D;
+  static constexpr int O_VSM = (2 * KB + 2 * VB) * D;
+  static constexpr int O_NORM = (2 * KB + 2 * VB + 2) * D;
   static constexpr size_t SMEM_STAGE = (size_t)NWARP * STAGES * TILE;
   static constexpr size_t SMEM_TOTAL = SMEM_A + SMEM_STAGE;
   static_assert((size_t)NWARP * kMaxRep * D * sizeof(float) <= SMEM_STAGE, "combine buffer fits the stages");
@@ -195,21 +196,21 @@ __device__ __forceinline__ void build_query_frags(const TcArgs& a, int b, int h0
   }
   __syncthreads();
   uint32_t* dst = reinterpret_cast<uint32_t*>(sA);
-  for (int idx = tid; idx < KSTEPS * 32 * 2; idx += NWARP * 32) {
+  for (int idx = tid; idx < a.kb * 8 * 32 * 2; idx += NWARP * 32) {
     const int half = idx & 1, L = (idx >> 1) & 31, ks = idx >> 6;  // k-step: 0..7 high bit, 8..15 low, 16..23 QJL
     const int plane = ks >> 3, kb = ks & 7;
     const int g = L >> 2, t = L & 3;
     const int dim = kb * 16 + 2 * t + 8 * half;
     float v0, v1;
-    if (plane == 0) {
-      v0 = a.neg_x * qr[g][dim];
-      v1 = a.neg_x * qr[g][dim + 1];
-    } else if (plane == 1) {
-      v0 = a.neg_y * qr[g][dim];
-      v1 = a.neg_y * qr[g][dim + 1];
-    } else {
+    if (plane == a.kb - 1) {  // QJL plane
       v0 = -qt[g][dim];
       v1 = -qt[g][dim + 1];
+    } else if (plane == 0) {
+      v0 = a.neg_x * qr[g][dim];
+      v1 = a.neg_x * qr[g][dim + 1];
+    } else {
+      v0 = a.neg_y * qr[g][dim];
+      v1 = a.neg_y * qr[g][dim + 1];
     }
     uint32_t hi, lo;
     split2(v0, v1, hi, lo);
@@ -261,21 +262,21 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
   }
   __syncthreads();
   uint32_t* dst = reinterpret_cast<uint32_t*>(a.afrag + ((size_t)b * a.hkv * a.groups + hg) * AFRAG_U4);
-  for (int idx = tid; idx < 3 * 32 * 2; idx += NWARP * 32) {
+  for (int idx = tid; idx < a.kb * 32 * 2; idx += NWARP * 32) {
     const int half = idx & 1, L = (idx >> 1) & 31, plane = idx >> 6;
     const int ks = plane * 8 + slice;
     const int gg = L >> 2, tt = L & 3;
     const int col = 2 * tt + 8 * half, dim = slice * 16 + col;
     float v0, v1;
-    if (plane == 0) {
-      v0 = a.neg_x * qr[gg][dim];
-      v1 = a.neg_x * qr[gg][dim + 1];
-    } else if (plane == 1) {
-      v0 = a.neg_y * qr[gg][dim];
-      v1 = a.neg_y * qr[gg][dim + 1];
-    } else {
+    if (plane == a.kb - 1) {  // QJL plane
       v0 = -qt[gg][col];
       v1 = -qt[gg][col + 1];
+    } else if (plane == 0) {
+      v0 = a.neg_x * qr[gg][dim];
+      v1 = a.neg_x * qr[gg][dim + 1];
+    } else {
+      v0 = a.neg_y * qr[gg][dim];
+      v1 = a.neg_y * qr[gg][dim + 1];
     }
     uint32_t hi, lo;
     split2(v0, v1, hi, lo);
@@ -312,14 +313,14 @@ __device__ __forceinline__ void softmax_update(WarpState& st, float (&s)[4], flo
 }
 
 // One compressed page (16 tokens) of the warp's KV head.
-template <int VB>
+template <int KB, int VB>
 __device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA, const uint8_t* T, WarpState& st,
                                                 int lane) {
-  using L = TcTile<VB>;
+  using L = TcTile<KB, VB>;
   const int g = lane >> 2, t = lane & 3;
-  uint4 rw[3][2];
+  uint4 rw[KB][2];
 #pragma unroll
-  for (int p = 0; p < 3; ++p) {
+  for (int p = 0; p < KB; ++p) {
     rw[p][0] = *reinterpret_cast<const uint4*>(T + 256 * p + g * 16);
     rw[p][1] = *reinterpret_cast<const uint4*>(T + 256 * p + (g + 8) * 16);
   }
@@ -333,7 +334,7 @@ __device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA
   // bit j = 8 half + t (b0) and j + 4 (b1) of each plane word, moved to bit 15
   const uint32_t mul[4] = {1u << (15 - t), 1u << (11 - t), 1u << (7 - t), 1u << (3 - t)};
 #pragma unroll
-  for (int p = 0; p < 3; ++p) {
+  for (int p = 0; p < KB; ++p) {
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       const uint32_t w0 = word_of(rw[p][0], w), w1 = word_of(rw[p][1], w);
@@ -341,8 +342,8 @@ __device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA
       for (int half = 0; half < 2; ++half) {
         const uint4 A = sA[(p * 8 + w * 2 + half) * 32 + lane];
         const uint32_t m0 = mul[2 * half], m1 = mul[2 * half + 1];
-        mma_f16(acc[p == 2][0], A, sgn_pair(w0, m0), sgn_pair(w0, m1));
-        mma_f16(acc[p == 2][1], A, sgn_pair(w1, m0), sgn_pair(w1, m1));
+        mma_f16(acc[p == KB - 1][0], A, sgn_pair(w0, m0), sgn_pair(w0, m1));
+        mma_f16(acc[p == KB - 1][1], A, sgn_pair(w1, m0), sgn_pair(w1, m1));
       }
     }
   }
@@ -454,9 +455,9 @@ __device__ __forceinline__ void page_ring(const TcArgs& a, const uint4 (&Aq)[8],
   }
 }
 
-template <int VB>
+template <int KB, int VB>
 __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
-  using L = TcTile<VB>;
+  using L = TcTile<KB, VB>;
   extern __shared__ __align__(16) uint8_t smem[];
   uint4* sA = reinterpret_cast<uint4*>(smem);
   uint8_t* stage = smem + SMEM_A;
@@ -540,7 +541,7 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
         if (lane == 0) flag_error(a.err, TQ_DEVERR_BLOCK_ID);
         continue;
       }
-      page_compressed<VB>(a, sA, wst + (k % STAGES) * L::TILE, st, lane);
+      page_compressed<KB, VB>(a, sA, wst + (k % STAGES) * L::TILE, st, lane);
       __syncwarp();
     }
     cp_wait<0>();
@@ -690,8 +691,15 @@ bool tc_supported(const tq_ctx* ctx) {
 cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) {
   const int hgroups = a.hkv * a.groups;
   const float c2 = ctx->tab.c[2], c3 = ctx->tab.c[3];
-  a.neg_x = -0.5f * (c3 + c2);
-  a.neg_y = -0.5f * (c3 - c2);
+  // Lloyd-Max row weights: 2-bit index c = x a + y b (a, b = +-1 from the two bits, x = (c3+c2)/2,
+  // y = (c3-c2)/2); 1-bit index c = c1 a.  The bits enter the products as -a, -b.
+  if (ctx->cfg.key_bits == 3) {
+    a.neg_x = -0.5f * (c3 + c2);
+    a.neg_y = -0.5f * (c3 - c2);
+  } else {
+    a.neg_x = -ctx->tab.c[1];
+    a.neg_y = 0.f;
+  }
   a.qjl_coef = 1.2533141373155003f / (float)ctx->cfg.qjl_m;
   a.logit_scale = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
   cudaError_t e = cudaSuccess;
@@ -701,8 +709,11 @@ cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     ctx->launches++;
   }
-  auto kern = ctx->cfg.value_bits == 4 ? tc_decode_kernel<4> : tc_decode_kernel<2>;
-  const size_t smem = ctx->cfg.value_bits == 4 ? TcTile<4>::SMEM_TOTAL : TcTile<2>::SMEM_TOTAL;
+  const bool k3 = ctx->cfg.key_bits == 3, v4 = ctx->cfg.value_bits == 4;
+  auto kern = k3 ? (v4 ? tc_decode_kernel<3, 4> : tc_decode_kernel<3, 2>)
+                 : (v4 ? tc_decode_kernel<2, 4> : tc_decode_kernel<2, 2>);
+  const size_t smem = k3 ? (v4 ? TcTile<3, 4>::SMEM_TOTAL : TcTile<3, 2>::SMEM_TOTAL)
+                         : (v4 ? TcTile<2, 4>::SMEM_TOTAL : TcTile<2, 2>::SMEM_TOTAL);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   prof_start(ctx, kProfDecode, s);

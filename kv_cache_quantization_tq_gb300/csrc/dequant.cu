@@ -40,6 +40,7 @@ struct DqArgs {
   int hkv;
   const float* signs;
   const uint4* sfrag;   // S as mma.sync B fragments (back-projection order), fp16 high / low
+  int kb;               // main layout key bits (3 or 2)
   CodeTables tab;
   float qjl_coef;       // sqrt(pi/2) / m
   uint32_t* err;
@@ -87,9 +88,10 @@ __device__ __forceinline__ int dq_ntok(const DqArgs& a, int b) {
   return n;
 }
 
-// Copies this CTA's pages into shared memory; returns false (and flags) if a block id is bad.
-template <int TILE>
-__device__ bool load_tiles(const DqArgs& a, uint8_t* tiles, int b, int h, int page0, int npages, bool* ok) {
+// Copies this CTA's pages (`tile` bytes each, staged `stride` bytes apart) into shared memory;
+// a bad block id is flagged and its page marked in ok[].
+__device__ void load_tiles(const DqArgs& a, uint8_t* tiles, int stride, int tile, int b, int h, int page0,
+                           int npages, bool* ok) {
   const int32_t* bt = a.block_table + (size_t)b * a.max_blocks;
   for (int p = 0; p < npages; ++p) {
     const int blk = bt[page0 + p];
@@ -101,23 +103,21 @@ __device__ bool load_tiles(const DqArgs& a, uint8_t* tiles, int b, int h, int pa
       continue;
     }
     if (threadIdx.x == 0) ok[p] = true;
-    const uint4* src = reinterpret_cast<const uint4*>(a.pool + ((size_t)blk * a.hkv + h) * TILE);
-    uint4* dst = reinterpret_cast<uint4*>(tiles + (size_t)p * TILE);
-    for (int i = threadIdx.x; i < TILE / 16; i += blockDim.x) dst[i] = src[i];
+    const uint4* src = reinterpret_cast<const uint4*>(a.pool + ((size_t)blk * a.hkv + h) * tile);
+    uint4* dst = reinterpret_cast<uint4*>(tiles + (size_t)p * stride);
+    for (int i = threadIdx.x; i < tile / 16; i += blockDim.x) dst[i] = src[i];
   }
   __syncthreads();
-  return true;
 }
 
 // ------------------------------------------------------------------ main layout
-// VB = value bits (2 or 4): value codes take VB * d / 8 bytes per token.
+// VB = value bits (2 or 4): value codes take VB * d / 8 bytes per token.  The key bits (3 or 2)
+// are a run-time value; the staging stride is the 3-bit tile.
 template <int D, int VB>
 struct MainDq {
   static constexpr int E = D / 32;
   static constexpr int TB = D >= 512 ? 16 : 32;          // tokens per CTA
-  static constexpr int TILE = (8 + 2 * VB) * D + 64;
-  static constexpr int O_VSM = (6 + 2 * VB) * D;
-  static constexpr int O_NORM = (8 + 2 * VB) * D;
+  static constexpr int TILE = (8 + 2 * VB) * D + 64;     // staging stride
   static constexpr int THREADS = 256;
   static constexpr int PAGES = TB / 16;
   static constexpr int WPP = (THREADS / 32) / PAGES;       // warps per page
@@ -141,7 +141,8 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
   const int n = dq_ntok(a, b);
   if (tok0 >= n) return;
   const int ntok = min(C::TB, n - tok0);  // multiple of 16
-  load_tiles<C::TILE>(a, tiles, b, h, tok0 >> 4, ntok >> 4, ok);
+  const int kb = a.kb, o_vq = 2 * kb * D, o_vsm = o_vq + 2 * VB * D, o_norm = o_vsm + 2 * D;
+  load_tiles(a, tiles, C::TILE, o_norm + 64, b, h, tok0 >> 4, ntok >> 4, ok);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   // corr[t][i] = sum_j (2 sigma_tj - 1) S[j][i]: warp -> (page, NT n-tiles); A = -(2 sigma - 1)
@@ -149,7 +150,8 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
     const int page = warp / C::WPP, nt0 = (warp % C::WPP) * C::NT;
     const int g = lane >> 2, t = lane & 3;
     if (page * 16 < ntok) {
-      const uint32_t* ks0 = reinterpret_cast<const uint32_t*>(tiles + (size_t)page * C::TILE + 4 * D + g * (D / 8));
+      const uint32_t* ks0 = reinterpret_cast<const uint32_t*>(tiles + (size_t)page * C::TILE + 2 * (kb - 1) * D +
+                                                             g * (D / 8));
       const uint32_t* ks1 = ks0 + 8 * (D / 32);  // token g + 8
       float acc[C::NT][4];
 #pragma unroll
@@ -202,25 +204,25 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
     const int slot = tt & 15;
     const uint32_t* kh = reinterpret_cast<const uint32_t*>(tile + slot * (D / 8));
     const uint32_t* kl = reinterpret_cast<const uint32_t*>(tile + 2 * D + slot * (D / 8));
-    const float nk = __half2float(reinterpret_cast<const __half*>(tile + C::O_NORM)[slot]);
-    const float nr = __half2float(reinterpret_cast<const __half*>(tile + C::O_NORM + 32)[slot]);
+    const float nk = __half2float(reinterpret_cast<const __half*>(tile + o_norm)[slot]);
+    const float nr = __half2float(reinterpret_cast<const __half*>(tile + o_norm + 32)[slot]);
     const int bit = 16 * (lane >> 4) + (lane & 15);
     float x[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      const int idx = (int)(((kh[e] >> bit) & 1u) << 1 | ((kl[e] >> bit) & 1u));
+      const int idx = kb == 3 ? (int)(((kh[e] >> bit) & 1u) << 1 | ((kl[e] >> bit) & 1u)) : (int)((kh[e] >> bit) & 1u);
       x[e] = fmaf(a.qjl_coef * nr, corr[tt * D + coord_of(e, lane)], sel4(a.tab, idx));
     }
     wht_warp<E>(x, lane);
     const size_t row = (((size_t)b * a.hkv + h) * a.max_tokens + tok0 + tt) * D;
     // 2-bit: token 2j+e at bits 16e+2j of word c; 4-bit: tokens 8w+2j+e at bits 16e+4j of word w*d+c
-    const uint32_t* vq = reinterpret_cast<const uint32_t*>(tile + 6 * D) + (VB == 4 && slot >= 8 ? D : 0);
+    const uint32_t* vq = reinterpret_cast<const uint32_t*>(tile + o_vq) + (VB == 4 && slot >= 8 ? D : 0);
     const int vbit = VB == 2 ? 16 * (slot & 1) + 2 * (slot >> 1) : 16 * (slot & 1) + 4 * ((slot & 7) >> 1);
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int c = coord_of(e, lane);
       a.k_out[row + c] = __float2half_rn(nk * (x[e] * sg[e] * rs));
-      const __half2 smn = *reinterpret_cast<const __half2*>(tile + C::O_VSM + (slot * (D / 32) + e) * 4);
+      const __half2 smn = *reinterpret_cast<const __half2*>(tile + o_vsm + (slot * (D / 32) + e) * 4);
       const float q = (float)((vq[c] >> vbit) & ((1u << VB) - 1u));
       a.v_out[row + c] = __float2half_rn(fmaf(__low2float(smn), q, __high2float(smn)));
     }
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
   const int n = dq_ntok(a, b);
   if (tok0 >= n) return;
   const int ntok = min(C::TB, n - tok0);
-  load_tiles<C::TILE>(a, smem, b, h, tok0 >> 4, ntok >> 4, ok);
+  load_tiles(a, smem, C::TILE, C::TILE, b, h, tok0 >> 4, ntok >> 4, ok);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float rs = rsqrtf((float)D);
   float sg[E];
@@ -334,6 +336,7 @@ cudaError_t launch_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, con
   a.hkv = ctx->cfg.num_kv_heads;
   a.signs = ctx->d_signs;
   a.sfrag = ctx->d_sfrag;
+  a.kb = ctx->cfg.key_bits;
   a.tab = ctx->tab;
   a.qjl_coef = (float)(1.2533141373155003 / (double)ctx->cfg.qjl_m);
   a.err = ctx->d_err;

@@ -38,6 +38,7 @@ struct EncArgs {
   int hkv;
   const float* signs;
   const uint4* sfrag;     // S^T as mma.sync B fragments (k = coordinate, n = sketch row), hi / lo
+  int kb;                 // main layout: key bits, 3 (2-bit Lloyd-Max index) or 2 (1-bit index)
   CodeTables tab;
   uint32_t* err;
 };
@@ -75,16 +76,14 @@ __global__ void sketch_frag_enc_kernel(const float* __restrict__ s, int d, uint4
 }
 
 // ------------------------------------------------------------------ main layout
-// VB = value bits (2 or 4): the value-code plane is VB * d / 8 bytes per token (turboquant
-// vLLM guide, --value-bits), followed by the group scale / minimum and the two norm rows.
+// Main tile: key bit planes (kb - 1 Lloyd-Max index planes, high bit first, then the QJL plane;
+// turboquant vLLM guide, --key-bits 3 or 2), VB-bit value codes (--value-bits 2 or 4), the group
+// scale / minimum, the two norm rows.  Staging in shared memory is sized for kb = 3.
 template <int D, int VB>
 struct MainEnc {
   static constexpr int E = D / 32;
   static constexpr int TB = D <= 128 ? 128 : (D == 256 ? 64 : 32);
-  static constexpr int TILE = (8 + 2 * VB) * D + 64;
-  static constexpr int O_VQ = 6 * D;                   // value codes
-  static constexpr int O_VSM = (6 + 2 * VB) * D;       // fp16 scale, minimum per (token, group)
-  static constexpr int O_NORM = (8 + 2 * VB) * D;      // fp16 key norms, then residual norms
+  static constexpr int TILE = (8 + 2 * VB) * D + 64;  // largest tile (kb = 3): staging stride
   static constexpr int THREADS = 256;
   static constexpr int RS = D + 8;                     // residual row stride (halves): conflict-free fragments
   static constexpr size_t SMEM_R = 2 * sizeof(__half) * TB * RS;  // high and low parts
@@ -93,9 +92,10 @@ struct MainEnc {
   static constexpr size_t SMEM = SMEM_R + SMEM_TILES + SMEM_CODES;
 };
 
-// Copy `npages` staged tiles to the pool pages of (b, h) starting at token `start`.
-template <int TILE>
-__device__ void store_tiles(const EncArgs& a, const uint8_t* tiles, int npages, int b, int h, int first_page) {
+// Copy `npages` staged tiles (staging stride `stride`, `tile` bytes each) to the pool pages of (b, h)
+// starting at token `start`.
+__device__ void store_tiles(const EncArgs& a, const uint8_t* tiles, int stride, int tile, int npages, int b, int h,
+                            int first_page) {
   for (int p = 0; p < npages; ++p) {
     const int page = first_page + p;
     int blk = -1;
@@ -104,9 +104,9 @@ __device__ void store_tiles(const EncArgs& a, const uint8_t* tiles, int npages, 
       if (threadIdx.x == 0) flag_error(a.err, page >= a.max_blocks ? TQ_DEVERR_POSITION : TQ_DEVERR_BLOCK_ID);
       continue;
     }
-    uint4* dst = reinterpret_cast<uint4*>(a.pool + ((size_t)blk * a.hkv + h) * TILE);
-    const uint4* src = reinterpret_cast<const uint4*>(tiles + (size_t)p * TILE);
-    for (int i = threadIdx.x; i < TILE / 16; i += blockDim.x) dst[i] = src[i];
+    uint4* dst = reinterpret_cast<uint4*>(a.pool + ((size_t)blk * a.hkv + h) * tile);
+    const uint4* src = reinterpret_cast<const uint4*>(tiles + (size_t)p * stride);
+    for (int i = threadIdx.x; i < tile / 16; i += blockDim.x) dst[i] = src[i];
   }
 }
 
@@ -128,6 +128,8 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
   const float sqrt_d = sqrtf((float)D);
 
   // ---- phase 1: one warp per token
+  const int o_ks = 2 * (a.kb - 1) * D, o_vq = 2 * a.kb * D;      // QJL plane, value codes
+  const int o_vsm = o_vq + 2 * VB * D, o_norm = o_vsm + 2 * D;     // scale / minimum, norms
   for (int tt = warp; tt < ntok; tt += C::THREADS / 32) {
     const __half* kp = a.k + (base + tok0 + tt) * D;
     const __half* vp = a.v + (base + tok0 + tt) * D;
@@ -151,23 +153,28 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const float y = x[e] * inv;
-      const int idx = (y >= a.tab.b[0]) + (y >= a.tab.b[1]) + (y >= a.tab.b[2]);
+      const int idx = a.kb == 3 ? (y >= a.tab.b[0]) + (y >= a.tab.b[1]) + (y >= a.tab.b[2]) : (y >= a.tab.b[0]);
       const float r = y - sel4(a.tab, idx);
       rr = fmaf(r, r, rr);
       const __half r_hi = __float2half_rn(r);
       rh[tt * C::RS + coord_of(e, lane)] = r_hi;
       rl[tt * C::RS + coord_of(e, lane)] = __float2half_rn((r - __half2float(r_hi)) * 2048.f);
-      const unsigned hi = __ballot_sync(kFull, idx >> 1);
-      const unsigned lo = __ballot_sync(kFull, idx & 1);
-      if (lane == 0) {
-        reinterpret_cast<uint32_t*>(tile + slot * (D / 8))[e] = hi;
-        reinterpret_cast<uint32_t*>(tile + 2 * D + slot * (D / 8))[e] = lo;
+      if (a.kb == 3) {
+        const unsigned hi = __ballot_sync(kFull, idx >> 1);
+        const unsigned lo = __ballot_sync(kFull, idx & 1);
+        if (lane == 0) {
+          reinterpret_cast<uint32_t*>(tile + slot * (D / 8))[e] = hi;
+          reinterpret_cast<uint32_t*>(tile + 2 * D + slot * (D / 8))[e] = lo;
+        }
+      } else {
+        const unsigned bits = __ballot_sync(kFull, idx);
+        if (lane == 0) reinterpret_cast<uint32_t*>(tile + slot * (D / 8))[e] = bits;
       }
     }
     const float nr = sqrtf(warp_sum(rr));
     if (lane == 0) {
-      reinterpret_cast<__half*>(tile + C::O_NORM)[slot] = __float2half_rn(nk);
-      reinterpret_cast<__half*>(tile + C::O_NORM + 32)[slot] = __float2half_rn(nr);
+      reinterpret_cast<__half*>(tile + o_norm)[slot] = __float2half_rn(nk);
+      reinterpret_cast<__half*>(tile + o_norm + 32)[slot] = __float2half_rn(nr);
     }
     // values: group e = coordinates 32e..32e+31, one per lane
 #pragma unroll
@@ -175,7 +182,7 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
       GroupCode g = group_quant_lane(vv[e], (float)((1 << VB) - 1));
       vcodes[tt * D + coord_of(e, lane)] = (uint8_t)g.q;
       if (lane == 0) {
-        __half* sm = reinterpret_cast<__half*>(tile + C::O_VSM + (slot * (D / 32) + e) * 4);
+        __half* sm = reinterpret_cast<__half*>(tile + o_vsm + (slot * (D / 32) + e) * 4);
         sm[0] = g.s;
         sm[1] = g.mn;
       }
@@ -238,7 +245,7 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
           const int tt = tile16 * 16 + g + 8 * hh;
           if (tt < ntok) {
             uint8_t* tile = tiles + (size_t)(tt >> 4) * C::TILE;
-            reinterpret_cast<uint32_t*>(tile + 4 * D + (tt & 15) * (D / 8))[wd] = hh ? w1 : w0;
+            reinterpret_cast<uint32_t*>(tile + o_ks + (tt & 15) * (D / 8))[wd] = hh ? w1 : w0;
           }
         }
       }
@@ -259,10 +266,10 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
       for (int s = 0; s < 8; ++s)
         word |= (uint32_t)vcodes[(p * 16 + 8 * half + s) * D + dim] << (16 * (s & 1) + 4 * (s >> 1));
     }
-    reinterpret_cast<uint32_t*>(tiles + (size_t)p * C::TILE + C::O_VQ)[i] = word;
+    reinterpret_cast<uint32_t*>(tiles + (size_t)p * C::TILE + o_vq)[i] = word;
   }
   __syncthreads();
-  store_tiles<C::TILE>(a, tiles, ntok >> 4, b, h, (start + tok0) >> 4);
+  store_tiles(a, tiles, C::TILE, o_norm + 64, ntok >> 4, b, h, (start + tok0) >> 4);
 }
 
 // ------------------------------------------------------------------ alternate layout
@@ -345,7 +352,7 @@ __device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int n
     dst[2] = o[2];
   }
   __syncthreads();
-  store_tiles<C::TILE>(a, tiles, ntok >> 4, b, h, (start + tok0) >> 4);
+  store_tiles(a, tiles, C::TILE, C::TILE, ntok >> 4, b, h, (start + tok0) >> 4);
 }
 
 // ------------------------------------------------------------------ kernels
@@ -445,6 +452,7 @@ EncArgs make_args(tq_ctx* ctx, const void* k, const void* v, int src_tokens, int
   a.hkv = ctx->cfg.num_kv_heads;
   a.signs = ctx->d_signs;
   a.sfrag = ctx->d_sfrag_enc;
+  a.kb = ctx->cfg.key_bits;
   a.tab = ctx->tab;
   a.err = ctx->d_err;
   return a;

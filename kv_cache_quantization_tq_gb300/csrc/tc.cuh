@@ -24,6 +24,7 @@ struct TcArgs {
   float* parts;    // [B][Hq][n_parts][d + 4] split-K partials (o, m, l, pad)
   int chunk_pages, n_chunks, n_parts;
   int hq, hkv, n_rep, nrg, groups;
+  int kb;          // key bits: 3 (planes: index high, index low, QJL) or 2 (index, QJL)
   const float* signs;
   const uint4* sfrag_enc;  // S^T as mma.sync B fragments (k = coordinate, n = sketch row), hi / lo
   uint32_t* err;

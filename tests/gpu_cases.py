@@ -13,8 +13,8 @@ from oracle import cache, codebook, layout, quant, rng
 MARGIN = 1e-5  # oracle values this close to a decision boundary may legitimately differ
 
 
-def oracle_tables(seed, d, layout_main=True):
-    bits = 2 if layout_main else 3
+def oracle_tables(seed, d, layout_main=True, key_bits=3):
+    bits = key_bits - 1 if layout_main else 3
     c, _ = codebook.lloyd_max(d, bits)
     c32 = c.astype(np.float32)
     signs = rng.signs(seed, d).astype(np.float32)
@@ -22,10 +22,11 @@ def oracle_tables(seed, d, layout_main=True):
     return c32, signs, sketch
 
 
-def make_ctx(tq, layout_main, d, hq, hkv, seed, value_bits=None):
-    c32, signs, sketch = oracle_tables(seed, d, layout_main)
+def make_ctx(tq, layout_main, d, hq, hkv, seed, value_bits=None, key_bits=None):
+    c32, signs, sketch = oracle_tables(seed, d, layout_main, key_bits or 3)
     lay = tq.TQ_LAYOUT_MAIN if layout_main else tq.TQ_LAYOUT_ALT
-    ctx = tq.Context(lay, d, hq, hkv, seed, centroids=c32, signs=signs, sketch=sketch, value_bits=value_bits)
+    ctx = tq.Context(lay, d, hq, hkv, seed, centroids=c32, signs=signs, sketch=sketch, value_bits=value_bits,
+                     key_bits=key_bits)
     return ctx, c32.astype(np.float64), signs.astype(np.float64), sketch
 
 
@@ -49,14 +50,15 @@ def main_fields(tiles, d):
     t = np.ascontiguousarray(tiles)
     lead = t.shape[:-1]
     o_n = t.shape[-1] - 64  # norms sit in the last 64 bytes (2- or 4-bit value codes before them)
+    # key bits from the tile size: (2 kb + 2 vb + 2) d + 64 with kb in {2, 3}, vb in {2, 4}
+    units = (t.shape[-1] - 64) // (2 * d) - 1  # kb + vb
+    kb = 3 if units in (5, 7) else 2
     w = lambda off, n: np.ascontiguousarray(t[..., off:off + n]).view("<u4")
-    kh = plane_bits(w(0, 2 * d).reshape(lead + (16, d // 32)))
-    kl = plane_bits(w(2 * d, 2 * d).reshape(lead + (16, d // 32)))
-    ks = plane_bits(w(4 * d, 2 * d).reshape(lead + (16, d // 32)))
+    pl = [plane_bits(w(2 * d * i, 2 * d).reshape(lead + (16, d // 32))) for i in range(kb)]
     return {
-        "idx": 2 * kh + kl,
-        "sigma": ks,
-        "v_bytes": t[..., 6 * d:o_n],
+        "idx": 2 * pl[0] + pl[1] if kb == 3 else pl[0],
+        "sigma": pl[kb - 1],
+        "v_bytes": t[..., 2 * kb * d:o_n],
         "kn": np.ascontiguousarray(t[..., o_n:o_n + 32]).view("<i2"),
         "rn": np.ascontiguousarray(t[..., o_n + 32:o_n + 64]).view("<i2"),
     }
@@ -93,7 +95,8 @@ def allclose_report(got, ref, atol=2e-3, rtol=1e-3):
 
 
 # ---------------------------------------------------------------- decode scenarios
-def build_main_cache(seed, d, hkv, lengths, centroids, signs, sketch, shuffled=True, extra_blocks=0, value_bits=2):
+def build_main_cache(seed, d, hkv, lengths, centroids, signs, sketch, shuffled=True, extra_blocks=0, value_bits=2,
+                     key_bits=3):
     """Oracle-encoded pool + ring for sequences of the given total lengths."""
     bsz = len(lengths)
     lmax = max(max(lengths), 1)
@@ -102,7 +105,7 @@ def build_main_cache(seed, d, hkv, lengths, centroids, signs, sketch, shuffled=T
     max_blocks = max(t_all // 16, 1)
     bt = synth.block_table(seed, bsz, max_blocks, shuffled)
     nblk = bsz * max_blocks + extra_blocks
-    pool = np.zeros((nblk, hkv, layout.main_tile_bytes(d, value_bits)), np.uint8)
+    pool = np.zeros((nblk, hkv, layout.main_tile_bytes(d, value_bits, key_bits)), np.uint8)
     n_c = np.zeros(bsz, np.int32)
     n_b = np.zeros(bsz, np.int32)
     ring_k = np.zeros((bsz, hkv, 128, d), np.float16)

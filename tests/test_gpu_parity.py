@@ -26,16 +26,16 @@ def _need_gpu():
 
 
 # ====================================================================== encode
-def _encode_main_both(d, hkv, n_tok, starts, seed, src_extra=0, value_bits=2):
+def _encode_main_both(d, hkv, n_tok, starts, seed, src_extra=0, value_bits=2, key_bits=3):
     bsz = len(starts)
-    ctx, c, s, sk = make_ctx(tq, True, d, hkv, hkv, seed, value_bits=value_bits)
+    ctx, c, s, sk = make_ctx(tq, True, d, hkv, hkv, seed, value_bits=value_bits, key_bits=key_bits)
     k, v = synth.kv_main(seed, bsz, hkv, n_tok + src_extra, d)
     k[0, 0, 3] = 0  # a zero key
     v[0, 0, 5, :32] = np.float16(0.75)  # a constant value group (scale 0)
     max_blocks = (max(starts) + n_tok) // 16 + 2
     bt = synth.block_table(seed, bsz, max_blocks, True)
     nblk = bsz * max_blocks
-    pool_o = np.zeros((nblk, hkv, layout.main_tile_bytes(d, value_bits)), np.uint8)
+    pool_o = np.zeros((nblk, hkv, layout.main_tile_bytes(d, value_bits, key_bits)), np.uint8)
     encs = []
     for b in range(bsz):
         encs.append(cache.encode_main_range(pool_o, bt[b:b + 1], starts[b], k[b:b + 1, :, :n_tok], v[b:b + 1, :, :n_tok],
