@@ -56,7 +56,7 @@ def decode_main(q16, pool, block_table, n_c, ring_k, ring_v, n_buf, signs, centr
     for b in range(bsz):
         nc = int(n_c[b])
         nb = int(n_buf[b])
-        f = cache.read_main(pool, block_table, b, nc, d) if nc else None
+        f = cache.read_main(pool, block_table, b, nc, d, cache.key_bits_of(centroids)) if nc else None
         for g in range(n_kv):
             q = q16[b, g * n_rep:(g + 1) * n_rep].astype(np.float64)
             logits = []
@@ -90,7 +90,7 @@ def decode_main_bruteforce(q16, pool, block_table, n_c, ring_k, ring_v, n_buf, s
     for b in range(bsz):
         nc = int(n_c[b])
         nb = int(n_buf[b])
-        f = cache.read_main(pool, block_table, b, nc, d) if nc else None
+        f = cache.read_main(pool, block_table, b, nc, d, cache.key_bits_of(centroids)) if nc else None
         for h in range(hq):
             g = h // n_rep
             q = q16[b, h].astype(np.float64)

@@ -37,8 +37,7 @@ def encode_main_range(pool, block_table, start, k16, v16, signs, centroids, s_ma
     k16 = np.asarray(k16, dtype=np.float16)
     bsz, hkv, t, d = k16.shape
     assert start % layout.P == 0 and t % layout.P == 0
-    kbits, vbits = layout.main_bits(pool.shape[-1], d)
-    assert len(centroids) == 1 << (kbits - 1), "codebook size does not match the pool's key bits"
+    kbits, vbits = layout.main_bits(pool.shape[-1], d, key_bits_of(centroids))
     enc = quant.encode_keys(k16, signs, centroids, s_mat)
     vq, vs, vmn = quant.encode_values(v16, group, vbits)
     npg = t // layout.P
@@ -80,11 +79,18 @@ def encode_alt_range(pool, block_table, start, k16, v16, signs, centroids3):
     return venc
 
 
-def read_main(pool, block_table, b, n_c, d):
+def key_bits_of(centroids) -> int:
+    """Main-layout key bits for a Lloyd-Max codebook: its index bits plus the QJL bit."""
+    k = len(centroids)
+    assert k in (2, 4, 8), k
+    return k.bit_length()
+
+
+def read_main(pool, block_table, b, n_c, d, kbits=None):
     """Unpack the first n_c tokens of sequence b: fields [Hkv, n_c, ...]."""
     npg = n_c // layout.P
     tiles = pool[np.asarray(block_table)[b, :npg]]  # [npg, Hkv, tile]
-    f = layout.unpack_main_tiles(tiles, d)
+    f = layout.unpack_main_tiles(tiles, d, kbits)
     out = {}
     for key, val in f.items():
         val = np.moveaxis(val, 1, 0)  # [Hkv, npg, 16, ...]
@@ -110,7 +116,7 @@ def materialize_main(pool, block_table, b, n_c, ring_k, ring_v, n_buf, signs, ce
     compressed tokens become the explicit reconstruction k^ (quant.dequant_keys) and
     mn + s q (quant.group_dequant); the ring tokens follow unchanged.
     """
-    f = read_main(pool, block_table, b, n_c, d) if n_c else None
+    f = read_main(pool, block_table, b, n_c, d, key_bits_of(centroids)) if n_c else None
     hkv = pool.shape[1]
     ks, vs = [], []
     for g in range(hkv):

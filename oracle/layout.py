@@ -163,14 +163,19 @@ def main_bytes_per_token_head(d: int, vbits: int = 2, kbits: int = 3) -> float:
     return main_tile_bytes(d, vbits, kbits) / P
 
 
-def main_bits(tile_bytes: int, d: int):
-    """(key bits, value bits) of a main-layout tile of the given size; key bits 2 or 3, value bits
-    2 or 4 (their sums 4..7 are distinct, so the size decides)."""
-    for kbits in (3, 2):
+def main_bits(tile_bytes: int, d: int, kbits: int = None):
+    """(key bits, value bits) of a main-layout tile of the given size.
+
+    Key bits 2, 3 or 4, value bits 2 or 4.  With the key bits given, the size gives the value
+    bits; without, the size alone decides for key bits 2 and 3 (sums 4..7 are distinct); in the
+    one tie (4-bit keys with 2-bit values are as large as 2-bit keys with 4-bit values) the latter
+    is returned, so readers of 4-bit-key tiles pass the key bits (from the codebook size).
+    """
+    for kb in ((kbits,) if kbits else (3, 2, 4)):
         for vbits in (2, 4):
-            if main_tile_bytes(d, vbits, kbits) == tile_bytes:
-                return kbits, vbits
-    raise AssertionError((tile_bytes, d))
+            if main_tile_bytes(d, vbits, kb) == tile_bytes:
+                return kb, vbits
+    raise AssertionError((tile_bytes, d, kbits))
 
 
 def main_value_bits(tile_bytes: int, d: int) -> int:
@@ -183,13 +188,13 @@ def pack_main_tiles(idx, sigma, vq, vs16, vmn16, nk16, nr16, vbits: int = 2, kbi
 
     Leading shape [..., 16 tokens]: idx, sigma, vq are [..., 16, d] uint8;
     vs16/vmn16 [..., 16, d/32] fp16; nk16/nr16 [..., 16] fp16.
-    Key planes: the Lloyd-Max index bits, high bit first (one plane for 2-bit keys, two for
-    3-bit keys), then the QJL sign bits.  Returns uint8 [..., main_tile_bytes(d, vbits, kbits)].
+    Key planes: the Lloyd-Max index bits, high bit first (kbits - 1 planes), then the QJL sign
+    bits.  Returns uint8 [..., main_tile_bytes(d, vbits, kbits)].
     """
     idx = np.asarray(idx, dtype=np.uint8)
     d = idx.shape[-1]
     lead = idx.shape[:-2]
-    lm_planes = [idx >> 1, idx & 1] if kbits == 3 else [idx]
+    lm_planes = [(idx >> (kbits - 2 - i)) & 1 for i in range(kbits - 1)]
     kp = [_u32_bytes(bits_to_plane_words(pl)).reshape(lead + (2 * d,)) for pl in lm_planes]
     ks = _u32_bytes(bits_to_plane_words(sigma)).reshape(lead + (2 * d,))
     vqb = _u32_bytes(codes_to_vq_words(vq, vbits))
@@ -202,11 +207,11 @@ def pack_main_tiles(idx, sigma, vq, vs16, vmn16, nk16, nr16, vbits: int = 2, kbi
     return out
 
 
-def unpack_main_tiles(tiles: np.ndarray, d: int) -> dict:
+def unpack_main_tiles(tiles: np.ndarray, d: int, kbits: int = None) -> dict:
     t = np.asarray(tiles, dtype=np.uint8)
     lead = t.shape[:-1]
     g = d // 32
-    kb, vb = main_bits(t.shape[-1], d)
+    kb, vb = main_bits(t.shape[-1], d, kbits)
     o_vq = 2 * kb * d
     o_sm = o_vq + 2 * vb * d
     o_n = o_sm + 2 * d
@@ -217,7 +222,9 @@ def unpack_main_tiles(tiles: np.ndarray, d: int) -> dict:
     def plane(i):
         return plane_words_to_bits(words(2 * d * i, 2 * d).reshape(lead + (16, d // 32)))
 
-    idx = 2 * plane(0) + plane(1) if kb == 3 else plane(0)
+    idx = np.zeros(lead + (16, d), np.int64)
+    for i in range(kb - 1):
+        idx = 2 * idx + plane(i)
     ks = plane(kb - 1)
     vq = vq_words_to_codes(words(o_vq, 2 * vb * d), vb)
     sm = np.ascontiguousarray(t[..., o_sm:o_sm + 2 * d]).view("<f2").reshape(lead + (16, g, 2))

@@ -83,3 +83,27 @@ def test_codebook_is_mse_optimal_among_perturbations():
     base = mse(c)
     for eps in [0.05, -0.05]:
         assert mse(c * (1 + eps)) > base
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3])
+def test_symmetric_codebook_is_odd_parity_combination(bits):
+    # A codebook with c[K-1-i] = -c[i] is odd under flipping every index bit, so in the +-1
+    # variables P_i = 1 - 2 b_i it is a combination of odd parity products only: one plane per
+    # bit for 1 and 2 bits, the three planes plus P0 P1 P2 for 3 bits (Walsh expansion).
+    import itertools
+    c, _ = codebook.lloyd_max(128, bits)
+    K = 1 << bits
+    idx = np.arange(K)
+    P = [1 - 2 * ((idx >> i) & 1) for i in range(bits)]  # P[i] for bit i (bit 0 = lowest)
+    for r in range(bits + 1):
+        for S in itertools.combinations(range(bits), r):
+            chi = np.prod([P[i] for i in S], axis=0) if S else np.ones(K)
+            coef = float(np.dot(c, chi)) / K
+            if r % 2 == 0:
+                assert abs(coef) < 1e-12, (S, coef)
+    recon = np.zeros(K)
+    for r in range(1, bits + 1, 2):
+        for S in itertools.combinations(range(bits), r):
+            chi = np.prod([P[i] for i in S], axis=0)
+            recon += float(np.dot(c, chi)) / K * chi
+    assert np.allclose(recon, c, atol=1e-12)

@@ -229,3 +229,27 @@ def test_bytes_per_token_2bit_keys():
     assert layout.main_bytes_per_token_head(128, 2, 2) == 16 + 16 + 32 + 16 + 4 == 84
     assert {layout.main_bits(layout.main_tile_bytes(64, vb, kb), 64) for kb in (2, 3) for vb in (2, 4)} == \
         {(2, 2), (2, 4), (3, 2), (3, 4)}
+
+
+def test_main_tile_round_trip_4bit_keys():
+    # 4-bit keys: three Lloyd-Max index planes (high bit first) and the QJL plane
+    d = 64
+    g = np.random.default_rng(44)
+    f = {
+        "idx": g.integers(0, 8, (2, 16, d), dtype=np.uint8),
+        "sigma": g.integers(0, 2, (2, 16, d), dtype=np.uint8),
+        "vq": g.integers(0, 4, (2, 16, d), dtype=np.uint8),
+        "vs": g.standard_normal((2, 16, d // 32)).astype(np.float16),
+        "vmn": g.standard_normal((2, 16, d // 32)).astype(np.float16),
+        "n_k": g.standard_normal((2, 16)).astype(np.float16),
+        "n_r": g.standard_normal((2, 16)).astype(np.float16),
+    }
+    t = layout.pack_main_tiles(f["idx"], f["sigma"], f["vq"], f["vs"], f["vmn"], f["n_k"], f["n_r"], 2, 4)
+    assert t.shape[-1] == 14 * d + 64 and layout.main_bits(t.shape[-1], d, 4) == (4, 2)
+    back = layout.unpack_main_tiles(t, d, 4)
+    for k, v in f.items():
+        assert np.array_equal(back[k].view(np.uint8), v.view(np.uint8)), k
+    # plane 0 holds the high index bit
+    hi = layout.pack_main_tiles(f["idx"] >> 2, f["sigma"], f["vq"], f["vs"], f["vmn"], f["n_k"], f["n_r"], 2, 2)
+    assert np.array_equal(t[:, :2 * d], hi[:, :2 * d])
+    assert layout.main_bytes_per_token_head(128, 2, 4) == 64 + 32 + 16 + 4 == 116

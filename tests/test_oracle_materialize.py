@@ -136,3 +136,41 @@ def test_main_layout_with_2bit_keys():
     for b in range(2):
         kk, vv = cache.materialize_main(pool, bt, b, int(n_c[b]), ring_k, ring_v, int(n_b[b]), sg, c, s, d)
         assert np.allclose(_attend(q[b], kk, vv, hkv), ref[b], rtol=0, atol=1e-12)
+
+
+def test_main_layout_with_4bit_keys():
+    # 3-bit Lloyd-Max index (8 centroids) plus the QJL bit; the readers take the key width from
+    # the codebook (the tile size alone would not tell it from 2-bit keys with 4-bit values)
+    seed, d, hkv, n_rep = 9, 64, 2, 2
+    sg = rng.signs(seed, d)
+    c, _ = codebook.lloyd_max(d, 3)
+    s = rng.gaussian_matrix(seed, d, d)
+    lengths = [300, 150]
+    k, v = synth.kv_main(seed, 2, hkv, 304, d)
+    bt = synth.block_table(seed, 2, 19, True)
+    pool = np.zeros((38, hkv, layout.main_tile_bytes(d, 2, 4)), np.uint8)
+    ring_k = np.zeros((2, hkv, 128, d), np.float16)
+    ring_v = np.zeros_like(ring_k)
+    n_c, n_b = np.zeros(2, np.int64), np.zeros(2, np.int64)
+    for b, L in enumerate(lengths):
+        nc, nb = cache.ring_split(L)
+        n_c[b], n_b[b] = nc, nb
+        cache.encode_main_range(pool, bt[b:b + 1], 0, k[b:b + 1, :, :nc], v[b:b + 1, :, :nc], sg, c, s)
+        ring_k[b, :, :nb] = k[b, :, nc:nc + nb]
+        ring_v[b, :, :nb] = v[b, :, nc:nc + nb]
+    q = synth.queries(seed, 2, hkv * n_rep, d)
+    ref = attention.decode_main(q, pool, bt, n_c, ring_k, ring_v, n_b, sg, c, s, hkv)
+    brute = attention.decode_main_bruteforce(q, pool, bt, n_c, ring_k, ring_v, n_b, sg, c, s, hkv)
+    assert np.allclose(ref, brute, rtol=0, atol=1e-12)
+    f = cache.read_main(pool, bt, 0, int(n_c[0]), d, 4)
+    assert f["idx"].max() > 3  # all eight cells in use
+    for b in range(2):
+        kk, vv = cache.materialize_main(pool, bt, b, int(n_c[b]), ring_k, ring_v, int(n_b[b]), sg, c, s, d)
+        assert np.allclose(_attend(q[b], kk, vv, hkv), ref[b], rtol=0, atol=1e-12)
+    # finer keys: the Lloyd-Max part alone is closer to the rotated key than with the 2-bit index
+    from oracle import quant
+    y = quant.encode_keys(k[0, :, :256], sg, c, s)["y"]
+    c2, _ = codebook.lloyd_max(d, 2)
+    e3 = np.mean((y - c[quant.assign(y, quant.boundaries_of(c))]) ** 2)
+    e2 = np.mean((y - c2[quant.assign(y, quant.boundaries_of(c2))]) ** 2)
+    assert e3 < 0.4 * e2
