@@ -88,8 +88,8 @@ typedef struct {
   int page_size;     /* tokens per page: must be 16 */
   int ring_capacity; /* exact recent-token buffer: must be 128 */
   int layout;        /* tq_layout */
-  int key_bits;      /* main: 3 (2-bit Lloyd-Max + 1-bit QJL, default) or 2 (1-bit Lloyd-Max +
-                        1-bit QJL; turboquant vLLM guide, --key-bits); alt: 8 */
+  int key_bits;      /* main: 3 (2-bit Lloyd-Max + 1-bit QJL, default), 2 or 4 (1- or 3-bit
+                        Lloyd-Max + 1-bit QJL; turboquant vLLM guide, --key-bits); alt: 8 */
   int value_bits;    /* main: 2 (default) or 4 (turboquant vLLM guide, --value-bits); alt: 3 */
   int group_size;    /* value group / key block: must be 32 */
   int qjl_m;         /* main: sketch rows m, must equal head_dim; alt: 0 */

@@ -100,6 +100,14 @@ __device__ __forceinline__ float sel4(const CodeTables& t, int i) {
   return r;
 }
 
+// c[i] of a codebook of up to 8 centroids without an indexed (local-memory) access.
+__device__ __forceinline__ float sel8(const CodeTables& t, int i) {
+  float r = t.c[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j) r = i == j ? t.c[j] : r;
+  return r;
+}
+
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }
 
 }  // namespace tq

@@ -223,12 +223,12 @@ __device__ void write_part(const DecArgs& a, int b, int h0, int part, const Soft
 }
 
 // ------------------------------------------------------------------ main layout
-// VB = value bits (2 or 4): value codes take VB * d / 8 bytes per token.  The key bits (3 or 2:
-// one or two Lloyd-Max index planes before the QJL plane) are a run-time value; the page buffer
-// is sized for 3.
+// VB = value bits (2 or 4): value codes take VB * d / 8 bytes per token.  The key bits (2, 3 or 4:
+// kb - 1 Lloyd-Max index planes before the QJL plane) are a run-time value; the page buffer is
+// sized for 4.
 template <int D, int NR, int VB>
 struct MainDec {
-  static constexpr int TILE = (8 + 2 * VB) * D + 64;
+  static constexpr int TILE = (10 + 2 * VB) * D + 64;
   static constexpr int G = D / 32;
 };
 
@@ -300,7 +300,8 @@ __global__ void __launch_bounds__(128) decode_main_kernel(DecArgs a) {
   const float scale = rsqrtf((float)D) * kLog2e;
   const int kb = a.kb, tile_bytes = (2 * kb + 2 * VB + 2) * D + 64;
   const uint32_t* kh_w = reinterpret_cast<const uint32_t*>(tile);
-  const uint32_t* kl_w = reinterpret_cast<const uint32_t*>(tile + 2 * D);  // 3-bit keys only
+  const uint32_t* kl_w = reinterpret_cast<const uint32_t*>(tile + 2 * D);  // 3- and 4-bit keys
+  const uint32_t* k3_w = reinterpret_cast<const uint32_t*>(tile + 4 * D);  // 4-bit keys
   const uint32_t* ks_w = reinterpret_cast<const uint32_t*>(tile + 2 * (kb - 1) * D);
   const uint32_t* vq_w = reinterpret_cast<const uint32_t*>(tile + 2 * kb * D);
   const __half* vsm = reinterpret_cast<const __half*>(tile + (2 * kb + 2 * VB) * D);
@@ -325,13 +326,16 @@ __global__ void __launch_bounds__(128) decode_main_kernel(DecArgs a) {
       for (int h = 0; h < NR; ++h) lm[h] = qj[h] = 0.f;
       const uint32_t* khr = kh_w + tok * (D / 32);
       const uint32_t* klr = kl_w + tok * (D / 32);
+      const uint32_t* k3r = k3_w + tok * (D / 32);
       const uint32_t* ksr = ks_w + tok * (D / 32);
 #pragma unroll 4
       for (int k = 0; k < D / 8; ++k) {
         const int dim = pp * (D / 8) + k;
         const int w = dim >> 5, bp = 16 * (dim & 1) + ((dim & 31) >> 1);
-        const int idx = kb == 3 ? (int)((((khr[w] >> bp) & 1) << 1) | ((klr[w] >> bp) & 1)) : (int)((khr[w] >> bp) & 1);
-        const float cv = sel4(a.tab, idx);
+        int idx = (int)((khr[w] >> bp) & 1);
+        if (kb >= 3) idx = (idx << 1) | (int)((klr[w] >> bp) & 1);
+        if (kb == 4) idx = (idx << 1) | (int)((k3r[w] >> bp) & 1);
+        const float cv = sel8(a.tab, idx);
         const float sv = ((ksr[w] >> bp) & 1) ? 1.f : -1.f;
 #pragma unroll
         for (int h = 0; h < NR; ++h) {

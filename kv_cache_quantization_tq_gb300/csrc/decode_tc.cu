@@ -41,14 +41,18 @@ namespace {
 constexpr int D = 128;
 constexpr int NWARP = 4;
 constexpr int STAGES = 4;
-constexpr int KSTEPS = 24;         // up to 3 planes x 8 k-steps of 16 coordinates (8 per key bit)
-constexpr int AFRAG_U4 = KSTEPS * 32;
-constexpr size_t SMEM_A = AFRAG_U4 * sizeof(uint4);
+// Score-side A planes for KB key bits: the Lloyd-Max planes (one per stored index bit, plus the
+// XOR of the three bits for 4-bit keys) and the QJL plane; 8 k-steps of 16 coordinates each.
+constexpr int a_planes(int kb) { return kb == 4 ? 5 : kb; }
+constexpr int KSTEPS_MAX = 8 * a_planes(4);
+constexpr int AFRAG_U4 = KSTEPS_MAX * 32;  // workspace stride per (sequence, head group)
 
 // Tile of the main layout with KB key bits (KB bit planes of 2d bytes: the Lloyd-Max index
 // bits, high first, then the QJL signs) and VB value bits (1600 bytes at KB = 3, VB = 2).
 template <int KB, int VB>
 struct TcTile {
+  static constexpr int NA = a_planes(KB);
+  static constexpr size_t SMEM_A = (size_t)NA * 8 * 32 * sizeof(uint4);
   static constexpr int TILE = (2 * KB + 2 * VB + 2) * D + 64;
   static constexpr int O_VQ = 2 * KB * D;
   static constexpr int O_VSM = (2 * KB + 2 * VB) * D;
@@ -196,21 +200,19 @@ __device__ __forceinline__ void build_query_frags(const TcArgs& a, int b, int h0
   }
   __syncthreads();
   uint32_t* dst = reinterpret_cast<uint32_t*>(sA);
-  for (int idx = tid; idx < a.kb * 8 * 32 * 2; idx += NWARP * 32) {
-    const int half = idx & 1, L = (idx >> 1) & 31, ks = idx >> 6;  // k-step: 0..7 high bit, 8..15 low, 16..23 QJL
+  for (int idx = tid; idx < (a.n_lm + 1) * 8 * 32 * 2; idx += NWARP * 32) {
+    const int half = idx & 1, L = (idx >> 1) & 31, ks = idx >> 6;  // k-steps: 8 per A plane, QJL last
     const int plane = ks >> 3, kb = ks & 7;
     const int g = L >> 2, t = L & 3;
     const int dim = kb * 16 + 2 * t + 8 * half;
     float v0, v1;
-    if (plane == a.kb - 1) {  // QJL plane
+    if (plane == a.n_lm) {  // QJL plane
       v0 = -qt[g][dim];
       v1 = -qt[g][dim + 1];
-    } else if (plane == 0) {
-      v0 = a.neg_x * qr[g][dim];
-      v1 = a.neg_x * qr[g][dim + 1];
     } else {
-      v0 = a.neg_y * qr[g][dim];
-      v1 = a.neg_y * qr[g][dim + 1];
+      const float wl = plane == 0 ? a.lm_w[0] : plane == 1 ? a.lm_w[1] : plane == 2 ? a.lm_w[2] : a.lm_w[3];
+      v0 = wl * qr[g][dim];
+      v1 = wl * qr[g][dim + 1];
     }
     uint32_t hi, lo;
     split2(v0, v1, hi, lo);
@@ -262,21 +264,19 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
   }
   __syncthreads();
   uint32_t* dst = reinterpret_cast<uint32_t*>(a.afrag + ((size_t)b * a.hkv * a.groups + hg) * AFRAG_U4);
-  for (int idx = tid; idx < a.kb * 32 * 2; idx += NWARP * 32) {
+  for (int idx = tid; idx < (a.n_lm + 1) * 32 * 2; idx += NWARP * 32) {
     const int half = idx & 1, L = (idx >> 1) & 31, plane = idx >> 6;
     const int ks = plane * 8 + slice;
     const int gg = L >> 2, tt = L & 3;
     const int col = 2 * tt + 8 * half, dim = slice * 16 + col;
     float v0, v1;
-    if (plane == a.kb - 1) {  // QJL plane
+    if (plane == a.n_lm) {  // QJL plane
       v0 = -qt[gg][col];
       v1 = -qt[gg][col + 1];
-    } else if (plane == 0) {
-      v0 = a.neg_x * qr[gg][dim];
-      v1 = a.neg_x * qr[gg][dim + 1];
     } else {
-      v0 = a.neg_y * qr[gg][dim];
-      v1 = a.neg_y * qr[gg][dim + 1];
+      const float wl = plane == 0 ? a.lm_w[0] : plane == 1 ? a.lm_w[1] : plane == 2 ? a.lm_w[2] : a.lm_w[3];
+      v0 = wl * qr[gg][dim];
+      v1 = wl * qr[gg][dim + 1];
     }
     uint32_t hi, lo;
     split2(v0, v1, hi, lo);
@@ -333,17 +333,28 @@ __device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA
       for (int r = 0; r < 4; ++r) acc[i][n][r] = 0.f;
   // bit j = 8 half + t (b0) and j + 4 (b1) of each plane word, moved to bit 15
   const uint32_t mul[4] = {1u << (15 - t), 1u << (11 - t), 1u << (7 - t), 1u << (3 - t)};
+  constexpr int NA = L::NA;
 #pragma unroll
-  for (int p = 0; p < KB; ++p) {
+  for (int p = 0; p < NA; ++p) {
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      const uint32_t w0 = word_of(rw[p][0], w), w1 = word_of(rw[p][1], w);
+      // A plane p: stored plane p, except for 4-bit keys: plane 3 = XOR of the three index
+      // planes (the odd parity product), plane 4 = the QJL plane (stored plane 3)
+      uint32_t w0, w1;
+      if (KB == 4 && p == 3) {
+        w0 = word_of(rw[0][0], w) ^ word_of(rw[1][0], w) ^ word_of(rw[2][0], w);
+        w1 = word_of(rw[0][1], w) ^ word_of(rw[1][1], w) ^ word_of(rw[2][1], w);
+      } else {
+        const int sp = (KB == 4 && p == 4) ? 3 : (p < KB ? p : KB - 1);
+        w0 = word_of(rw[sp][0], w);
+        w1 = word_of(rw[sp][1], w);
+      }
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const uint4 A = sA[(p * 8 + w * 2 + half) * 32 + lane];
         const uint32_t m0 = mul[2 * half], m1 = mul[2 * half + 1];
-        mma_f16(acc[p == KB - 1][0], A, sgn_pair(w0, m0), sgn_pair(w0, m1));
-        mma_f16(acc[p == KB - 1][1], A, sgn_pair(w1, m0), sgn_pair(w1, m1));
+        mma_f16(acc[p == NA - 1][0], A, sgn_pair(w0, m0), sgn_pair(w0, m1));
+        mma_f16(acc[p == NA - 1][1], A, sgn_pair(w1, m0), sgn_pair(w1, m1));
       }
     }
   }
@@ -460,7 +471,7 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
   using L = TcTile<KB, VB>;
   extern __shared__ __align__(16) uint8_t smem[];
   uint4* sA = reinterpret_cast<uint4*>(smem);
-  uint8_t* stage = smem + SMEM_A;
+  uint8_t* stage = smem + L::SMEM_A;
   __shared__ float wm[NWARP][kMaxRep], wl[NWARP][kMaxRep];
   __shared__ int sblk[NWARP][STAGES];
   __shared__ __align__(16) float qr[kMaxRep][D];
@@ -497,7 +508,7 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
   if (!ring) {
     if (a.afrag) {
       const uint4* af = a.afrag + ((size_t)b * a.hkv * a.groups + hg) * AFRAG_U4;
-      for (int i = tid; i < AFRAG_U4; i += blockDim.x) cp16(&sA[i], &af[i]);
+      for (int i = tid; i < L::NA * 8 * 32; i += blockDim.x) cp16(&sA[i], &af[i]);
       cp_commit();
     }
     const int pbeg = part * a.chunk_pages;
@@ -690,15 +701,27 @@ bool tc_supported(const tq_ctx* ctx) {
 
 cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) {
   const int hgroups = a.hkv * a.groups;
-  const float c2 = ctx->tab.c[2], c3 = ctx->tab.c[3];
-  // Lloyd-Max row weights: 2-bit index c = x a + y b (a, b = +-1 from the two bits, x = (c3+c2)/2,
-  // y = (c3-c2)/2); 1-bit index c = c1 a.  The bits enter the products as -a, -b.
-  if (ctx->cfg.key_bits == 3) {
-    a.neg_x = -0.5f * (c3 + c2);
-    a.neg_y = -0.5f * (c3 - c2);
-  } else {
-    a.neg_x = -ctx->tab.c[1];
-    a.neg_y = 0.f;
+  // Lloyd-Max row weights.  A bit enters the products as P = 1 - 2 bit = +-1, and a symmetric
+  // codebook (c[K-1-i] = -c[i]) is odd under flipping every index bit, so c[idx] is a combination
+  // of the odd parity products of the P's: one term per index bit, plus P0 P1 P2 for a 3-bit
+  // index (whose plane is the XOR of the three stored planes).  Each weight is a Walsh
+  // coefficient: (1/K) sum_idx c[idx] chi(idx).
+  {
+    const int nb = ctx->cfg.key_bits - 1, K = 1 << nb;
+    a.n_lm = nb == 3 ? 4 : nb;
+    for (int p = 0; p < a.n_lm; ++p) {
+      double w = 0.0;
+      for (int idx = 0; idx < K; ++idx) {
+        int par = 0;  // parity of the bits in the product
+        if (p < nb)
+          par = (idx >> (nb - 1 - p)) & 1;  // plane p = index bit nb-1-p (high bit first)
+        else
+          par = ((idx >> 2) ^ (idx >> 1) ^ idx) & 1;
+        w += (double)ctx->h_centroids[idx] * (par ? -1.0 : 1.0);
+      }
+      a.lm_w[p] = (float)(w / K);
+    }
+    for (int p = a.n_lm; p < 4; ++p) a.lm_w[p] = 0.f;
   }
   a.qjl_coef = 1.2533141373155003f / (float)ctx->cfg.qjl_m;
   a.logit_scale = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
@@ -709,11 +732,14 @@ cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     ctx->launches++;
   }
-  const bool k3 = ctx->cfg.key_bits == 3, v4 = ctx->cfg.value_bits == 4;
-  auto kern = k3 ? (v4 ? tc_decode_kernel<3, 4> : tc_decode_kernel<3, 2>)
-                 : (v4 ? tc_decode_kernel<2, 4> : tc_decode_kernel<2, 2>);
-  const size_t smem = k3 ? (v4 ? TcTile<3, 4>::SMEM_TOTAL : TcTile<3, 2>::SMEM_TOTAL)
-                         : (v4 ? TcTile<2, 4>::SMEM_TOTAL : TcTile<2, 2>::SMEM_TOTAL);
+  const int kb = ctx->cfg.key_bits;
+  const bool v4 = ctx->cfg.value_bits == 4;
+  auto kern = kb == 4 ? (v4 ? tc_decode_kernel<4, 4> : tc_decode_kernel<4, 2>)
+            : kb == 3 ? (v4 ? tc_decode_kernel<3, 4> : tc_decode_kernel<3, 2>)
+                      : (v4 ? tc_decode_kernel<2, 4> : tc_decode_kernel<2, 2>);
+  const size_t smem = kb == 4 ? (v4 ? TcTile<4, 4>::SMEM_TOTAL : TcTile<4, 2>::SMEM_TOTAL)
+                    : kb == 3 ? (v4 ? TcTile<3, 4>::SMEM_TOTAL : TcTile<3, 2>::SMEM_TOTAL)
+                              : (v4 ? TcTile<2, 4>::SMEM_TOTAL : TcTile<2, 2>::SMEM_TOTAL);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   prof_start(ctx, kProfDecode, s);

@@ -111,13 +111,13 @@ __device__ void load_tiles(const DqArgs& a, uint8_t* tiles, int stride, int tile
 }
 
 // ------------------------------------------------------------------ main layout
-// VB = value bits (2 or 4): value codes take VB * d / 8 bytes per token.  The key bits (3 or 2)
-// are a run-time value; the staging stride is the 3-bit tile.
+// VB = value bits (2 or 4): value codes take VB * d / 8 bytes per token.  The key bits (2, 3 or
+// 4) are a run-time value; the staging stride is the 4-bit-key tile.
 template <int D, int VB>
 struct MainDq {
   static constexpr int E = D / 32;
   static constexpr int TB = D >= 512 ? 16 : 32;          // tokens per CTA
-  static constexpr int TILE = (8 + 2 * VB) * D + 64;     // staging stride
+  static constexpr int TILE = (10 + 2 * VB) * D + 64;    // staging stride
   static constexpr int THREADS = 256;
   static constexpr int PAGES = TB / 16;
   static constexpr int WPP = (THREADS / 32) / PAGES;       // warps per page
@@ -204,14 +204,17 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
     const int slot = tt & 15;
     const uint32_t* kh = reinterpret_cast<const uint32_t*>(tile + slot * (D / 8));
     const uint32_t* kl = reinterpret_cast<const uint32_t*>(tile + 2 * D + slot * (D / 8));
+    const uint32_t* k3 = reinterpret_cast<const uint32_t*>(tile + 4 * D + slot * (D / 8));
     const float nk = __half2float(reinterpret_cast<const __half*>(tile + o_norm)[slot]);
     const float nr = __half2float(reinterpret_cast<const __half*>(tile + o_norm + 32)[slot]);
     const int bit = 16 * (lane >> 4) + (lane & 15);
     float x[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      const int idx = kb == 3 ? (int)(((kh[e] >> bit) & 1u) << 1 | ((kl[e] >> bit) & 1u)) : (int)((kh[e] >> bit) & 1u);
-      x[e] = fmaf(a.qjl_coef * nr, corr[tt * D + coord_of(e, lane)], sel4(a.tab, idx));
+      int idx = (int)((kh[e] >> bit) & 1u);
+      if (kb >= 3) idx = (idx << 1) | (int)((kl[e] >> bit) & 1u);
+      if (kb == 4) idx = (idx << 1) | (int)((k3[e] >> bit) & 1u);
+      x[e] = fmaf(a.qjl_coef * nr, corr[tt * D + coord_of(e, lane)], sel8(a.tab, idx));
     }
     wht_warp<E>(x, lane);
     const size_t row = (((size_t)b * a.hkv + h) * a.max_tokens + tok0 + tt) * D;

@@ -77,13 +77,13 @@ __global__ void sketch_frag_enc_kernel(const float* __restrict__ s, int d, uint4
 
 // ------------------------------------------------------------------ main layout
 // Main tile: key bit planes (kb - 1 Lloyd-Max index planes, high bit first, then the QJL plane;
-// turboquant vLLM guide, --key-bits 3 or 2), VB-bit value codes (--value-bits 2 or 4), the group
-// scale / minimum, the two norm rows.  Staging in shared memory is sized for kb = 3.
+// turboquant vLLM guide, --key-bits 2, 3 or 4), VB-bit value codes (--value-bits 2 or 4), the
+// group scale / minimum, the two norm rows.  Staging in shared memory is sized for kb = 4.
 template <int D, int VB>
 struct MainEnc {
   static constexpr int E = D / 32;
   static constexpr int TB = D <= 128 ? 128 : (D == 256 ? 64 : 32);
-  static constexpr int TILE = (8 + 2 * VB) * D + 64;  // largest tile (kb = 3): staging stride
+  static constexpr int TILE = (10 + 2 * VB) * D + 64;  // largest tile (kb = 4): staging stride
   static constexpr int THREADS = 256;
   static constexpr int RS = D + 8;                     // residual row stride (halves): conflict-free fragments
   static constexpr size_t SMEM_R = 2 * sizeof(__half) * TB * RS;  // high and low parts
@@ -153,22 +153,17 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const float y = x[e] * inv;
-      const int idx = a.kb == 3 ? (y >= a.tab.b[0]) + (y >= a.tab.b[1]) + (y >= a.tab.b[2]) : (y >= a.tab.b[0]);
-      const float r = y - sel4(a.tab, idx);
+      int idx = 0;  // #{boundaries <= y} over the 2^(kb-1) - 1 boundaries
+#pragma unroll
+      for (int j = 0; j < 7; ++j) idx += (j < (1 << (a.kb - 1)) - 1 && y >= a.tab.b[j]) ? 1 : 0;
+      const float r = y - sel8(a.tab, idx);
       rr = fmaf(r, r, rr);
       const __half r_hi = __float2half_rn(r);
       rh[tt * C::RS + coord_of(e, lane)] = r_hi;
       rl[tt * C::RS + coord_of(e, lane)] = __float2half_rn((r - __half2float(r_hi)) * 2048.f);
-      if (a.kb == 3) {
-        const unsigned hi = __ballot_sync(kFull, idx >> 1);
-        const unsigned lo = __ballot_sync(kFull, idx & 1);
-        if (lane == 0) {
-          reinterpret_cast<uint32_t*>(tile + slot * (D / 8))[e] = hi;
-          reinterpret_cast<uint32_t*>(tile + 2 * D + slot * (D / 8))[e] = lo;
-        }
-      } else {
-        const unsigned bits = __ballot_sync(kFull, idx);
-        if (lane == 0) reinterpret_cast<uint32_t*>(tile + slot * (D / 8))[e] = bits;
+      for (int i = 0; i < a.kb - 1; ++i) {  // index planes, high bit first
+        const unsigned bits = __ballot_sync(kFull, (idx >> (a.kb - 2 - i)) & 1);
+        if (lane == 0) reinterpret_cast<uint32_t*>(tile + 2 * i * D + slot * (D / 8))[e] = bits;
       }
     }
     const float nr = sqrtf(warp_sum(rr));

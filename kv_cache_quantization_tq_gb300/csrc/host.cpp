@@ -130,7 +130,7 @@ tq_status check_config(const tq_config* c) {
   const int groups = (n_rep + tq::kMaxRep - 1) / tq::kMaxRep;
   if (n_rep % groups) return TQ_ERR_UNSUPPORTED;
   if (c->layout == TQ_LAYOUT_MAIN) {
-    if ((c->key_bits != 3 && c->key_bits != 2) || (c->value_bits != 2 && c->value_bits != 4) ||
+    if (c->key_bits < 2 || c->key_bits > 4 || (c->value_bits != 2 && c->value_bits != 4) ||
         c->qjl_m != c->head_dim)
       return TQ_ERR_UNSUPPORTED;
   } else if (c->layout == TQ_LAYOUT_ALT) {
@@ -261,7 +261,7 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
     // kernel, because there the per-CTA cost (~3 us) outweighs the saved launch.
     const int64_t ctas = (int64_t)pl.n_parts * hkv * groups * batch;
     pl.fused_prep = ctas <= (int64_t)ctx->sm_count * 3;
-    pl.q_bytes = pl.fused_prep ? 0 : align((size_t)batch * hkv * groups * 24 * 32 * 16);
+    pl.q_bytes = pl.fused_prep ? 0 : align((size_t)batch * hkv * groups * 40 * 32 * 16);  // <= 5 A planes x 8
   } else
     pl.q_bytes = ctx->cfg.layout == TQ_LAYOUT_MAIN ? align(sizeof(float) * batch * hq * 2 * d) : 0;
   pl.part_bytes = align(sizeof(float) * (size_t)batch * hq * pl.n_parts * (d + (pl.tensor_core ? 4 : 2)));

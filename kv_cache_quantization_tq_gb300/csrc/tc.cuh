@@ -24,11 +24,13 @@ struct TcArgs {
   float* parts;    // [B][Hq][n_parts][d + 4] split-K partials (o, m, l, pad)
   int chunk_pages, n_chunks, n_parts;
   int hq, hkv, n_rep, nrg, groups;
-  int kb;          // key bits: 3 (planes: index high, index low, QJL) or 2 (index, QJL)
+  int kb;          // key bits: 2, 3 or 4 (kb - 1 stored index planes, high bit first, then QJL)
   const float* signs;
   const uint4* sfrag_enc;  // S^T as mma.sync B fragments (k = coordinate, n = sketch row), hi / lo
   uint32_t* err;
-  float neg_x, neg_y, qjl_coef, logit_scale;
+  int n_lm;        // Lloyd-Max A planes: 1 (2-bit keys), 2 (3-bit), 4 (4-bit: three bits + their XOR)
+  float lm_w[4];   // weight of each Lloyd-Max A plane (Walsh coefficient of the codebook)
+  float qjl_coef, logit_scale;
 };
 
 bool tc_supported(const tq_ctx* ctx);

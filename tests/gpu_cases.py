@@ -46,17 +46,23 @@ def plane_bits(words_u32):
     return b.reshape(words_u32.shape[:-1] + (words_u32.shape[-1] * 32,)).astype(np.uint8)
 
 
-def main_fields(tiles, d):
+def main_fields(tiles, d, kb=None):
+    """Fields of main-layout tiles; kb = key bits (2, 3 or 4), taken from the tile size when not
+    given (the size alone cannot tell 4-bit keys with 2-bit values from 2-bit keys with 4-bit
+    values)."""
     t = np.ascontiguousarray(tiles)
     lead = t.shape[:-1]
     o_n = t.shape[-1] - 64  # norms sit in the last 64 bytes (2- or 4-bit value codes before them)
-    # key bits from the tile size: (2 kb + 2 vb + 2) d + 64 with kb in {2, 3}, vb in {2, 4}
-    units = (t.shape[-1] - 64) // (2 * d) - 1  # kb + vb
-    kb = 3 if units in (5, 7) else 2
+    if kb is None:  # (2 kb + 2 vb + 2) d + 64 with kb in {2, 3}, vb in {2, 4}
+        units = (t.shape[-1] - 64) // (2 * d) - 1  # kb + vb
+        kb = 3 if units in (5, 7) else 2
     w = lambda off, n: np.ascontiguousarray(t[..., off:off + n]).view("<u4")
     pl = [plane_bits(w(2 * d * i, 2 * d).reshape(lead + (16, d // 32))) for i in range(kb)]
+    idx = np.zeros_like(pl[0])
+    for i in range(kb - 1):
+        idx = 2 * idx + pl[i]
     return {
-        "idx": 2 * pl[0] + pl[1] if kb == 3 else pl[0],
+        "idx": idx,
         "sigma": pl[kb - 1],
         "v_bytes": t[..., 2 * kb * d:o_n],
         "kn": np.ascontiguousarray(t[..., o_n:o_n + 32]).view("<i2"),

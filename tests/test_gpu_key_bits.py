@@ -1,8 +1,10 @@
-"""2-bit keys in the main layout (turboquant vLLM guide, --key-bits 2) on the GPU: a 1-bit
-Lloyd-Max index (centroids +-E|x|) and the 1-bit QJL sketch, with 2- or 4-bit values.
+"""2- and 4-bit keys in the main layout (turboquant vLLM guide, --key-bits) on the GPU: a 1-bit
+Lloyd-Max index (centroids +-E|x|) or a 3-bit one (8 centroids), each with the 1-bit QJL sketch,
+and 2- or 4-bit values.
 
-Same parity bar as the default layout; d = 128 runs the tensor-core decoder (two bit planes
-instead of three), other head dims the CUDA-core one.
+Same parity bar as the default layout; d = 128 runs the tensor-core decoder (two bit planes for
+2-bit keys; for 4-bit keys the three index planes, their XOR and the QJL plane), other head dims
+the CUDA-core one.
 """
 import numpy as np
 import pytest
@@ -28,6 +30,34 @@ def _need_gpu():
         pytest.skip("no CUDA device")
 
 
+def test_record_size_4bit_keys():
+    ctx, c, *_ = make_ctx(tq, True, 128, 4, 4, 0, key_bits=4)
+    assert ctx.bytes_per_token_head == 116 and len(c) == 8
+    lib_ctx = tq.Context(tq.TQ_LAYOUT_MAIN, 128, 4, 4, 0, key_bits=4)
+    assert np.allclose(lib_ctx.get_tables()["centroids"], c, rtol=1e-6)
+
+
+@pytest.mark.parametrize("kb", [2, 4])
+def test_dequantize(kb):
+    d, hkv, seed = 128, 2, 90 + kb
+    ctx, c, s, sk = make_ctx(tq, True, d, hkv, hkv, seed, key_bits=kb)
+    e = build_main_cache(seed, d, hkv, [400, 200], c, s, sk, key_bits=kb)
+    k_out = torch.zeros((2, hkv, 416, d), dtype=torch.float16, device="cuda")
+    v_out = torch.zeros_like(k_out)
+    ctx.dequantize(to_dev(e["pool"]), to_dev(e["bt"]), to_dev(e["n_c"]), k_out, v_out, to_dev(e["ring_k"]),
+                   to_dev(e["ring_v"]), to_dev(e["n_b"]))
+    torch.cuda.synchronize()
+    assert ctx.device_errors() == 0
+    kg, vg = k_out.cpu().numpy().astype(np.float64), v_out.cpu().numpy().astype(np.float64)
+    for b in range(2):
+        nc, nb = int(e["n_c"][b]), int(e["n_b"][b])
+        kr, vr = cache.materialize_main(e["pool"], e["bt"], b, nc, e["ring_k"], e["ring_v"], nb, s, c, sk, d)
+        for got, ref in ((kg[b, :, :nc + nb], kr), (vg[b, :, :nc + nb], vr)):
+            half_ulp = np.maximum(np.abs(ref), 2.0 ** -14) * 2.0 ** -11
+            row = np.linalg.norm(ref, axis=-1, keepdims=True)
+            assert np.all(np.abs(got - ref) <= half_ulp * 1.01 + 2e-6 * row + 1e-7)
+
+
 def test_record_size_and_codebook():
     ctx, c, *_ = make_ctx(tq, True, 128, 4, 4, 0, key_bits=2)
     assert ctx.bytes_per_token_head == 84 and ctx.page_bytes == layout.main_tile_bytes(128, 2, 2)
@@ -37,25 +67,28 @@ def test_record_size_and_codebook():
     assert np.allclose(ctx2.get_tables()["centroids"], c, rtol=1e-6)
 
 
-@pytest.mark.parametrize("d,vb", [(128, 2), (64, 4), (512, 2)])
-def test_encode_parity(d, vb):
+@pytest.mark.parametrize("d,vb,kb", [(128, 2, 2), (64, 4, 2), (512, 2, 2), (128, 2, 4), (256, 4, 4)])
+def test_encode_parity(d, vb, kb):
     n_tok = 256 if d <= 128 else 128
     starts = [0, 32]
-    ctx, pool_o, pool_g, encs, bt, c = _encode_main_both(d, 2, n_tok, starts, seed=70 + d, value_bits=vb, key_bits=2)
+    ctx, pool_o, pool_g, encs, bt, c = _encode_main_both(d, 2, n_tok, starts, seed=70 + d, value_bits=vb, key_bits=kb)
     _compare_main(pool_o, pool_g, encs, bt, starts, n_tok, d, c)
 
 
-@pytest.mark.parametrize("d,vb,hkv,n_rep,lengths", [
-    (128, 2, 2, 4, [1500, 129, 16]),   # tensor-core decoder
-    (128, 4, 2, 7, [700]),
-    (64, 2, 2, 2, [900]),              # CUDA-core decoder
-    (256, 4, 1, 3, [640]),
+@pytest.mark.parametrize("d,vb,kb,hkv,n_rep,lengths", [
+    (128, 2, 2, 2, 4, [1500, 129, 16]),   # tensor-core decoder
+    (128, 4, 2, 2, 7, [700]),
+    (64, 2, 2, 2, 2, [900]),              # CUDA-core decoder
+    (256, 4, 2, 1, 3, [640]),
+    (128, 2, 4, 2, 4, [1500, 129, 16]),   # 4-bit keys: tensor-core
+    (128, 4, 4, 1, 8, [900]),
+    (64, 2, 4, 2, 2, [700]),              # 4-bit keys: CUDA-core
 ])
-def test_decode_parity(d, vb, hkv, n_rep, lengths):
-    seed = 80 + d + n_rep
+def test_decode_parity(d, vb, kb, hkv, n_rep, lengths):
+    seed = 80 + d + n_rep + kb
     hq = hkv * n_rep
-    ctx, c, s, sk = make_ctx(tq, True, d, hq, hkv, seed, value_bits=vb, key_bits=2)
-    e = build_main_cache(seed, d, hkv, lengths, c, s, sk, value_bits=vb, key_bits=2)
+    ctx, c, s, sk = make_ctx(tq, True, d, hq, hkv, seed, value_bits=vb, key_bits=kb)
+    e = build_main_cache(seed, d, hkv, lengths, c, s, sk, value_bits=vb, key_bits=kb)
     q = synth.queries(seed, len(lengths), hq, d)
     out = torch.empty((len(lengths), hq, d), dtype=torch.float32, device="cuda")
     ws = torch.empty(ctx.workspace_size(len(lengths), e["max_ctx"]), dtype=torch.uint8, device="cuda")

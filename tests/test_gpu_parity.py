@@ -52,8 +52,9 @@ def _compare_main(pool_o, pool_g, encs, bt, starts, n_tok, d, c):
     written = np.zeros(pool_o.shape[0], bool)
     written[blocks.ravel()] = True
     assert np.array_equal(pool_g[~written], pool_o[~written])  # untouched pages stay untouched
-    fo = main_fields(pool_o[blocks], d)  # [B, pages, Hkv, 16, ...]
-    fg = main_fields(pool_g[blocks], d)
+    kb = len(c).bit_length()  # key bits: Lloyd-Max index bits + the QJL bit
+    fo = main_fields(pool_o[blocks], d, kb)  # [B, pages, Hkv, 16, ...]
+    fg = main_fields(pool_g[blocks], d, kb)
     # value planes: bit-exact
     assert np.array_equal(fg["v_bytes"], fo["v_bytes"])
     npg = n_tok // 16
