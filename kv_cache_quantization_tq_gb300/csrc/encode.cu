@@ -110,7 +110,7 @@ __device__ void store_tiles(const EncArgs& a, const uint8_t* tiles, int stride, 
   }
 }
 
-template <int D, int VB>
+template <int D, int VB, int KB>
 __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int ntok, int start, uint8_t* smem) {
   using C = MainEnc<D, VB>;
   constexpr int E = C::E;
@@ -128,8 +128,8 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
   const float sqrt_d = sqrtf((float)D);
 
   // ---- phase 1: one warp per token
-  const int o_ks = 2 * (a.kb - 1) * D, o_vq = 2 * a.kb * D;      // QJL plane, value codes
-  const int o_vsm = o_vq + 2 * VB * D, o_norm = o_vsm + 2 * D;     // scale / minimum, norms
+  constexpr int o_ks = 2 * (KB - 1) * D, o_vq = 2 * KB * D;      // QJL plane, value codes
+  constexpr int o_vsm = o_vq + 2 * VB * D, o_norm = o_vsm + 2 * D; // scale / minimum, norms
   for (int tt = warp; tt < ntok; tt += C::THREADS / 32) {
     const __half* kp = a.k + (base + tok0 + tt) * D;
     const __half* vp = a.v + (base + tok0 + tt) * D;
@@ -153,17 +153,47 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const float y = x[e] * inv;
-      int idx = 0;  // #{boundaries <= y} over the 2^(kb-1) - 1 boundaries
+      // #{boundaries <= y} over the 2^(kb-1) - 1 boundaries (straight-line code per key width)
+      int idx;
+      float cy;
+      if (KB == 3) {
+        idx = (y >= a.tab.b[0]) + (y >= a.tab.b[1]) + (y >= a.tab.b[2]);
+        cy = sel4(a.tab, idx);
+      } else if (KB == 2) {
+        idx = y >= a.tab.b[0];
+        cy = idx ? a.tab.c[1] : a.tab.c[0];
+      } else {
+        idx = 0;
 #pragma unroll
-      for (int j = 0; j < 7; ++j) idx += (j < (1 << (a.kb - 1)) - 1 && y >= a.tab.b[j]) ? 1 : 0;
-      const float r = y - sel8(a.tab, idx);
+        for (int j = 0; j < 7; ++j) idx += y >= a.tab.b[j];
+        cy = sel8(a.tab, idx);
+      }
+      const float r = y - cy;
       rr = fmaf(r, r, rr);
       const __half r_hi = __float2half_rn(r);
       rh[tt * C::RS + coord_of(e, lane)] = r_hi;
       rl[tt * C::RS + coord_of(e, lane)] = __float2half_rn((r - __half2float(r_hi)) * 2048.f);
-      for (int i = 0; i < a.kb - 1; ++i) {  // index planes, high bit first
-        const unsigned bits = __ballot_sync(kFull, (idx >> (a.kb - 2 - i)) & 1);
-        if (lane == 0) reinterpret_cast<uint32_t*>(tile + 2 * i * D + slot * (D / 8))[e] = bits;
+      // index planes, high bit first
+      uint32_t* kp0 = reinterpret_cast<uint32_t*>(tile + slot * (D / 8)) + e;
+      if (KB == 3) {
+        const unsigned hi = __ballot_sync(kFull, idx >> 1);
+        const unsigned lo = __ballot_sync(kFull, idx & 1);
+        if (lane == 0) {
+          kp0[0] = hi;
+          kp0[2 * D / 4] = lo;
+        }
+      } else if (KB == 2) {
+        const unsigned bits = __ballot_sync(kFull, idx);
+        if (lane == 0) kp0[0] = bits;
+      } else {
+        const unsigned b2 = __ballot_sync(kFull, idx >> 2);
+        const unsigned b1 = __ballot_sync(kFull, (idx >> 1) & 1);
+        const unsigned b0 = __ballot_sync(kFull, idx & 1);
+        if (lane == 0) {
+          kp0[0] = b2;
+          kp0[2 * D / 4] = b1;
+          kp0[4 * D / 4] = b0;
+        }
       }
     }
     const float nr = sqrtf(warp_sum(rr));
@@ -364,10 +394,14 @@ __global__ void __launch_bounds__(256) encode_kernel(EncArgs a) {
     if (threadIdx.x == 0) flag_error(a.err, TQ_DEVERR_POSITION);
     return;
   }
-  if (VB)
-    encode_main_block<D, (VB ? VB : 2)>(a, b, h, tok0, ntok, start, smem);
-  else
+  if (!VB)
     encode_alt_block<D>(a, b, h, tok0, ntok, start, smem);
+  else if (a.kb == 3)
+    encode_main_block<D, (VB ? VB : 2), 3>(a, b, h, tok0, ntok, start, smem);
+  else if (a.kb == 2)
+    encode_main_block<D, (VB ? VB : 2), 2>(a, b, h, tok0, ntok, start, smem);
+  else
+    encode_main_block<D, (VB ? VB : 2), 4>(a, b, h, tok0, ntok, start, smem);
 }
 
 struct AppendArgs {
@@ -393,8 +427,12 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
     constexpr int TB = VB ? MainEnc<D, (VB ? VB : 2)>::TB : AltEnc<D>::TB;
     static_assert(kRing % TB == 0, "ring flush is a whole number of encode batches");
     for (int t0 = 0; t0 < kRing; t0 += TB) {
-      if (VB)
-        encode_main_block<D, (VB ? VB : 2)>(a.enc, b, h, t0, TB, start, smem);
+      if (VB && a.enc.kb == 3)
+        encode_main_block<D, (VB ? VB : 2), 3>(a.enc, b, h, t0, TB, start, smem);
+      else if (VB && a.enc.kb == 2)
+        encode_main_block<D, (VB ? VB : 2), 2>(a.enc, b, h, t0, TB, start, smem);
+      else if (VB)
+        encode_main_block<D, (VB ? VB : 2), 4>(a.enc, b, h, t0, TB, start, smem);
       else
         encode_alt_block<D>(a.enc, b, h, t0, TB, start, smem);
       __syncthreads();
