@@ -292,17 +292,23 @@ struct WarpState {
   float mn[4];
 };
 
+// Online softmax with a lazily updated reference maximum.  The running state (m, l, o, mn) is
+// only rescaled when some head's page maximum exceeds its reference by more than 2^kLazyLog2 (or
+// on the first page); otherwise the reference stays and weights p = 2^(s - m) may reach
+// 2^kLazyLog2.  The result is exact either way (l and o share the reference, and so do the
+// split-K partials); weights up to 256 are exact in fp32 and far inside the fp16 range of the
+// value operands.  A warp sees few pages, so an eager update rescaled the 68 accumulators on most
+// of them.
+constexpr float kLazyLog2 = 8.f;
 __device__ __forceinline__ void softmax_update(WarpState& st, float (&s)[4], float (&p)[4]) {
   float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
   mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-  const float m_new = fmaxf(st.m, mx);
-  const float alpha = fast_exp2(st.m - m_new);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) p[k] = fast_exp2(s[k] - m_new);
-  st.l = st.l * alpha + (p[0] + p[1]) + (p[2] + p[3]);
-  st.m = m_new;
-  if (__any_sync(kFull, alpha != 1.f)) {
+  if (__any_sync(kFull, mx > st.m + kLazyLog2)) {
+    const float m_new = fmaxf(st.m, mx);
+    const float alpha = fast_exp2(st.m - m_new);
+    st.l *= alpha;
+    st.m = m_new;
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt)
 #pragma unroll
@@ -310,6 +316,9 @@ __device__ __forceinline__ void softmax_update(WarpState& st, float (&s)[4], flo
 #pragma unroll
     for (int g = 0; g < 4; ++g) st.mn[g] *= alpha;
   }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) p[k] = fast_exp2(s[k] - st.m);
+  st.l += (p[0] + p[1]) + (p[2] + p[3]);
 }
 
 // One compressed page (16 tokens) of the warp's KV head.
