@@ -236,11 +236,12 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
   pl.tensor_core = ctx->cfg.layout == TQ_LAYOUT_MAIN && d == 128;
   int64_t per;
   if (pl.tensor_core) {
-    // About 1.75 CTAs per SM, i.e. one wave at the occupancy the kernel gets, with 16..64 pages
-    // per chunk (4..16 per warp).  Measured on GB300 over 8K..65K-page decode steps: fewer,
-    // longer chunks leave SMs idle; shorter ones pay the per-CTA fragment load and combine
-    // more often than they gain parallelism.
-    const int64_t target = std::max<int64_t>(1, (int64_t)ctx->sm_count * 7 / 4);
+    // About 2 CTAs per SM, i.e. one wave at the occupancy the kernel gets, with 16..64 pages
+    // per chunk (4..16 per warp).  Measured on GB300 over 8K..65K-page decode steps (16..64-page
+    // sweeps): fewer, longer chunks leave SMs idle; shorter ones pay the per-CTA query fragments
+    // and combine more often than they gain parallelism.  Large steps stay at 64 pages, where
+    // whole-wave chunk counts (36..56 pages) measured no better.
+    const int64_t target = std::max<int64_t>(1, (int64_t)ctx->sm_count * 2);
     per = (total_pages + target - 1) / target;
     per = std::max<int64_t>(16, std::min<int64_t>(64, per));
     per = (per + 3) / 4 * 4;
