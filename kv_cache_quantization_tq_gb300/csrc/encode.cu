@@ -202,9 +202,11 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
       reinterpret_cast<__half*>(tile + o_norm + 32)[slot] = __float2half_rn(nr);
     }
     // values: group e = coordinates 32e..32e+31, one per lane
+    float vmn[E], vmx[E];
+    group_minmax<E>(vv, vmn, vmx);
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      GroupCode g = group_quant_lane(vv[e], (float)((1 << VB) - 1));
+      GroupCode g = group_quant_mm(vv[e], vmn[e], vmx[e], (float)((1 << VB) - 1));
       vcodes[tt * D + coord_of(e, lane)] = (uint8_t)g.q;
       if (lane == 0) {
         __half* sm = reinterpret_cast<__half*>(tile + o_vsm + (slot * (D / 32) + e) * 4);
@@ -326,13 +328,18 @@ __device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int n
     const __half* vp = a.v + (base + tok0 + tt) * D;
     uint8_t* tile = tiles + (size_t)(tt >> 4) * C::TILE;
     const int slot = tt & 15;
-    float vv[E];
+    float vv[E], kx[E], kmn[E], kmx[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int c = coord_of(e, lane);
-      const float kx = __half2float(kp[c]);
+      kx[e] = __half2float(kp[c]);
       vv[e] = __half2float(vp[c]);
-      GroupCode g = group_quant_lane(kx, 255.f);
+    }
+    group_minmax<E>(kx, kmn, kmx);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int c = coord_of(e, lane);
+      GroupCode g = group_quant_mm(kx[e], kmn[e], kmx[e], 255.f);
       tile[slot * D + c] = (uint8_t)g.q;
       if (lane == 0) {
         __half* sm = reinterpret_cast<__half*>(tile + 16 * D + (slot * (D / 32) + e) * 4);
