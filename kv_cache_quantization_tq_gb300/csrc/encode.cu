@@ -231,7 +231,7 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
       for (int j = 0; j < NG; ++j)
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc[j][r] = cor[j][r] = 0.f;
-#pragma unroll 2
+#pragma unroll 4  // measured: 4 k-steps of fragment loads in flight (+9% encode), 8 is slower
       for (int ks = 0; ks < D / 16; ++ks) {
         const int k0 = 16 * ks + 2 * t;
         uint4 ah, al;
