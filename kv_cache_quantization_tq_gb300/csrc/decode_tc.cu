@@ -176,7 +176,7 @@ __device__ __forceinline__ void build_query_frags(const TcArgs& a, int b, int h0
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int r = 0; r < 4; ++r) ch[j][r] = cl[j][r] = 0.f;
-#pragma unroll 2
+#pragma unroll 4  // four k-steps of sketch fragments in flight
     for (int ks = 0; ks < D / 16; ++ks) {
       const int k0 = 16 * ks + 2 * t;
       uint4 A;
