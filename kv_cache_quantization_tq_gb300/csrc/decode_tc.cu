@@ -10,11 +10,14 @@
 //     rows 0..7 = heads (fp16 high part), rows 8..15 = the same heads (fp16
 //     low part, (value - high) * 2^11), so each product is good to ~22 bits;
 //     K = three bit planes of 128 coordinates: the high and the low bit of
-//     the 2-bit Lloyd-Max index and the QJL sign bit.  Each bit enters as an
-//     exact +-1.  With a symmetric 2-bit codebook, c[idx] = x a + y b for
-//     a, b = +-1 taken from the two index bits (x = (c3+c2)/2, y = (c3-c2)/2),
-//     so the Lloyd-Max dot <q_r, c[idx]> and the QJL dot <S q_r, 2 sigma - 1>
-//     are plain +-1 contractions, with -x q_r, -y q_r and -S q_r as the rows.
+//     the 2-bit Lloyd-Max index and the QJL sign bit.  With a symmetric 2-bit
+//     codebook, c[idx] = x a + y b for a, b = +-1 taken from the two index bits
+//     (x = (c3+c2)/2, y = (c3-c2)/2), so the Lloyd-Max dot <q_r, c[idx]> and
+//     the QJL dot <S q_r, 2 sigma - 1> are +-1 contractions, with -x q_r,
+//     -y q_r and -S q_r as the rows.  Each bit enters the MMA at the position
+//     it already has after one shift per word (an fp16 exponent or sign bit,
+//     see enc12 .. enc15), the affine map from that value to +-1 being folded
+//     into the query rows and the accumulators' start values.
 //     logit = n_k (lm + sqrt(pi/2)/m n_r qjl) / sqrt(d)   (turboquant vLLM
 //     guide, section 2 step 3, unbiased inner-product estimator).
 //   values  O[16 x 128] += P'_g[16 x 16 tok] . C[16 tok x 128]
@@ -45,7 +48,12 @@ constexpr int STAGES = 4;
 // XOR of the three bits for 4-bit keys) and the QJL plane; 8 k-steps of 16 coordinates each.
 constexpr int a_planes(int kb) { return kb == 4 ? 5 : kb; }
 constexpr int KSTEPS_MAX = 8 * a_planes(4);
-constexpr int AFRAG_U4 = KSTEPS_MAX * 32;  // workspace stride per (sequence, head group)
+// Query workspace per (sequence, head group): the A fragments, then the partial score offsets of
+// each prep slice ([slice][Lloyd-Max / QJL][head] floats).
+constexpr int kPrepSlices = 4;
+constexpr int AFRAG_U4 = KSTEPS_MAX * 32 + kPrepSlices * 2 * kMaxRep / 4;
+static_assert(AFRAG_U4 == kTcQueryU4, "query workspace layout");
+static_assert(NWARP == kPrepSlices, "the fused prep's warps fill the offset slots of the prep slices");
 
 // Tile of the main layout with KB key bits (KB bit planes of 2d bytes: the Lloyd-Max index
 // bits, high first, then the QJL signs) and VB value bits (1600 bytes at KB = 3, VB = 2).
@@ -73,14 +81,36 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint4& a, uint32_t 
       : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
-// Bits j and j+16 of w as an fp16 pair: +1 where the bit is clear, -1 where set.
-// The shift is a multiplication by mul = 2^(15 - j) (an integer multiply-add
-// runs on the FMA pipe and leaves the ALU pipe to the bit select).
-__device__ __forceinline__ uint32_t sgn_pair(uint32_t w, uint32_t mul) {
-  uint32_t x;
-  asm("mul.lo.u32 %0, %1, %2;" : "=r"(x) : "r"(w), "r"(mul));
-  return (x & 0x80008000u) | 0x3C003C00u;
+// Key bits as fp16 operands without a shift per element.  Lane t of an MMA takes bit pairs
+// j = 4t .. 4t+3 of a plane word (bits j and j + 16: coordinates 32w + 2j and 32w + 2j + 1).  One
+// multiplication by 2^(12 - 4t) moves them to bits 12..15 (and 28..31), i.e. onto fp16 exponent
+// bits 2, 3, 4 and the sign bit, and one bit select per register then gives an fp16 pair whose
+// value is affine in the bit, B = beta0 + (beta1 - beta0) b:
+//   bit 12: 1/16 or 1        bit 13: 1/256 or 1        bit 14: 0 or 2        bit 15: 1 or -1
+// The query side carries A' = -2 A / (beta1 - beta0) and the accumulator starts at the offset
+// sum_k A_k (1 + 2 beta0 / (beta1 - beta0)); then offset + sum_k A'_k B_k = sum_k A_k (1 - 2 b_k),
+// the +-1 contraction of the method.  No product carries an offset larger than |A| beside a
+// signal of 2 |A|, so the fp32 accumulation keeps the precision of the plain +-1 form.  The bit
+// position of coordinate c is 12 + ((c >> 1) & 3); its scale and offset factor:
+__device__ __forceinline__ float bitenc_scale(int q2) {
+  return q2 == 0 ? -32.f / 15.f : q2 == 1 ? -512.f / 255.f : q2 == 2 ? -1.f : 1.f;
 }
+__device__ __forceinline__ float bitenc_offset(int q2) {
+  return q2 == 0 ? 17.f / 15.f : q2 == 1 ? 257.f / 255.f : q2 == 2 ? 1.f : 0.f;
+}
+__device__ __forceinline__ uint32_t enc12(uint32_t x) { return (x & 0x10001000u) | 0x2C002C00u; }
+__device__ __forceinline__ uint32_t enc13(uint32_t x) { return (x & 0x20002000u) | 0x1C001C00u; }
+__device__ __forceinline__ uint32_t enc14(uint32_t x) { return x & 0x40004000u; }
+__device__ __forceinline__ uint32_t enc15(uint32_t x) { return (x & 0x80008000u) | 0x3C003C00u; }
+// The shift as an integer multiply (FMA pipe), leaving the ALU pipe to the bit selects.
+__device__ __forceinline__ uint32_t mul_lo(uint32_t a, uint32_t b) {
+  uint32_t x;
+  asm("mul.lo.u32 %0, %1, %2;" : "=r"(x) : "r"(a), "r"(b));
+  return x;
+}
+// Coordinate of A-fragment register pair rh (0: regs 0/1, 1: regs 2/3) of lane group t in k-step kb
+// of a plane (first of two adjacent coordinates).
+__device__ __forceinline__ int frag_dim(int kb, int t, int rh) { return 32 * (kb >> 1) + 8 * t + 4 * (kb & 1) + 2 * rh; }
 
 // 2^x for x <= 0 (log2-domain softmax weights); -inf gives +0.
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -154,7 +184,8 @@ __device__ __forceinline__ int tc_nb(const TcArgs& a, int b) {
 // with g = lane / 4, t = lane % 4; row g is head g (high part), row g+8 the
 // same head's low part.
 __device__ __forceinline__ void build_query_frags(const TcArgs& a, int b, int h0, uint4* sA, float (*qr)[D],
-                                                  float (*qt)[D], int tid, int lane, int warp) {
+                                                  float (*qt)[D], float (*soff)[2][kMaxRep], int tid, int lane,
+                                                  int warp) {
   const float rs = rsqrtf((float)D);
   for (int h = warp; h < kMaxRep; h += NWARP) {
     float x[D / 32];
@@ -169,19 +200,24 @@ __device__ __forceinline__ void build_query_frags(const TcArgs& a, int b, int h0
   }
   __syncthreads();
   {
-    // t[h][j] = sum_i S[j][i] q_r[h][i]; warp w covers sketch rows 32w .. 32w+31
+    // t[h][j] = sum_i S[j][i] q_r[h][i]; warp w covers sketch rows 32w .. 32w+31.  Every coordinate
+    // this lane touches (16 ks + 2t + {0, 1, 8, 9} of q_r, 32w + 8j + 2t + {0, 1} of t) has bit
+    // position 12 + t, so the lane's share of the score offsets is one factor times plain sums.
     const int g = lane >> 2, t = lane & 3;
     float ch[4][4], cl[4][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int r = 0; r < 4; ++r) ch[j][r] = cl[j][r] = 0.f;
+    float sl = 0.f;
 #pragma unroll 4  // four k-steps of sketch fragments in flight
     for (int ks = 0; ks < D / 16; ++ks) {
       const int k0 = 16 * ks + 2 * t;
       uint4 A;
-      split2(qr[g][k0], qr[g][k0 + 1], A.x, A.y);
-      split2(qr[g][k0 + 8], qr[g][k0 + 9], A.z, A.w);
+      const float q0 = qr[g][k0], q1 = qr[g][k0 + 1], q8 = qr[g][k0 + 8], q9 = qr[g][k0 + 9];
+      sl += (q0 + q1) + (q8 + q9);
+      split2(q0, q1, A.x, A.y);
+      split2(q8, q9, A.z, A.w);
       const uint4* bf = a.sfrag_enc + ((size_t)ks * (D / 8) + 4 * warp) * 32 + lane;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -191,11 +227,26 @@ __device__ __forceinline__ void build_query_frags(const TcArgs& a, int b, int h0
       }
     }
     // high x high + 2^-11 (low x high + high x low); low x low (2^-22) is dropped
+    float sq = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int col = 32 * warp + 8 * j + 2 * t;
-      qt[g][col] = fmaf(ch[j][2] + cl[j][0], kLoUnscale, ch[j][0]);
-      qt[g][col + 1] = fmaf(ch[j][3] + cl[j][1], kLoUnscale, ch[j][1]);
+      const float t0 = fmaf(ch[j][2] + cl[j][0], kLoUnscale, ch[j][0]);
+      const float t1 = fmaf(ch[j][3] + cl[j][1], kLoUnscale, ch[j][1]);
+      qt[g][col] = t0;
+      qt[g][col + 1] = t1;
+      sq += t0 + t1;
+    }
+    const float cf = bitenc_offset(t);
+    sl *= cf;
+    sq *= cf;
+    sl += __shfl_xor_sync(kFull, sl, 1);
+    sl += __shfl_xor_sync(kFull, sl, 2);
+    sq += __shfl_xor_sync(kFull, sq, 1);
+    sq += __shfl_xor_sync(kFull, sq, 2);
+    if (t == 0) {
+      soff[warp][1][g] = -sq;  // QJL: this warp's sketch rows
+      soff[warp][0][g] = warp == 0 ? ((a.lm_w[0] + a.lm_w[1]) + (a.lm_w[2] + a.lm_w[3])) * sl : 0.f;
     }
   }
   __syncthreads();
@@ -204,7 +255,8 @@ __device__ __forceinline__ void build_query_frags(const TcArgs& a, int b, int h0
     const int half = idx & 1, L = (idx >> 1) & 31, ks = idx >> 6;  // k-steps: 8 per A plane, QJL last
     const int plane = ks >> 3, kb = ks & 7;
     const int g = L >> 2, t = L & 3;
-    const int dim = kb * 16 + 2 * t + 8 * half;
+    const int dim = frag_dim(kb, t, half);
+    const float sc = bitenc_scale(2 * (kb & 1) + half);
     float v0, v1;
     if (plane == a.n_lm) {  // QJL plane
       v0 = -qt[g][dim];
@@ -215,7 +267,7 @@ __device__ __forceinline__ void build_query_frags(const TcArgs& a, int b, int h0
       v1 = wl * qr[g][dim + 1];
     }
     uint32_t hi, lo;
-    split2(v0, v1, hi, lo);
+    split2(v0 * sc, v1 * sc, hi, lo);
     dst[(ks * 32 + L) * 4 + 2 * half] = hi;
     dst[(ks * 32 + L) * 4 + 2 * half + 1] = lo;
   }
@@ -224,11 +276,11 @@ __device__ __forceinline__ void build_query_frags(const TcArgs& a, int b, int h0
 
 // When the decode grid is too large for every CTA to build its own fragments they are built
 // once per (KV-head group, sequence) into the workspace, split over kPrepSlices CTAs: slice s
-// writes k-steps s, 8 + s and 16 + s, i.e. sketch rows 16 s .. 16 s + 15 of t (two MMA n-tiles).
-constexpr int kPrepSlices = 8;
+// covers coordinates 32 s .. 32 s + 31, i.e. k-steps 2s and 2s + 1 of every plane and sketch rows
+// 32 s .. 32 s + 31 of t (four MMA n-tiles, one per warp), and writes its part of the score offsets.
 __global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
   __shared__ __align__(16) float qr[kMaxRep][D];
-  __shared__ float qt[kMaxRep][16];
+  __shared__ float qt[kMaxRep][32];
   const int hg = blockIdx.x, b = blockIdx.y, slice = blockIdx.z;
   const int h0 = (hg / a.groups) * a.n_rep + (hg % a.groups) * a.nrg;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -246,7 +298,7 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
     for (int e = 0; e < D / 32; ++e) qr[h][coord_of(e, lane)] = x[e] * rs;
   }
   __syncthreads();
-  if (warp < 2) {
+  {
     float ch[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
     for (int ks = 0; ks < D / 16; ++ks) {
@@ -254,7 +306,7 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
       uint4 A;
       split2(qr[g][k0], qr[g][k0 + 1], A.x, A.y);
       split2(qr[g][k0 + 8], qr[g][k0 + 9], A.z, A.w);
-      const uint4 bv = __ldg(a.sfrag_enc + ((size_t)ks * (D / 8) + 2 * slice + warp) * 32 + lane);
+      const uint4 bv = __ldg(a.sfrag_enc + ((size_t)ks * (D / 8) + 4 * slice + warp) * 32 + lane);
       mma_f16(ch, A, bv.x, bv.y);
       mma_f16(cl, A, bv.z, bv.w);
     }
@@ -263,25 +315,42 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
     qt[g][col + 1] = fmaf(ch[3] + cl[1], kLoUnscale, ch[1]);
   }
   __syncthreads();
-  uint32_t* dst = reinterpret_cast<uint32_t*>(a.afrag + ((size_t)b * a.hkv * a.groups + hg) * AFRAG_U4);
-  for (int idx = tid; idx < (a.n_lm + 1) * 32 * 2; idx += NWARP * 32) {
-    const int half = idx & 1, L = (idx >> 1) & 31, plane = idx >> 6;
-    const int ks = plane * 8 + slice;
+  uint4* base = a.afrag + ((size_t)b * a.hkv * a.groups + hg) * AFRAG_U4;
+  uint32_t* dst = reinterpret_cast<uint32_t*>(base);
+  for (int idx = tid; idx < (a.n_lm + 1) * 2 * 32 * 2; idx += NWARP * 32) {
+    const int half = idx & 1, L = (idx >> 1) & 31, r = idx >> 6;  // r = plane * 2 + k-step of the slice
+    const int plane = r >> 1, kb = 2 * slice + (r & 1);
+    const int ks = plane * 8 + kb;
     const int gg = L >> 2, tt = L & 3;
-    const int col = 2 * tt + 8 * half, dim = slice * 16 + col;
+    const int dim = frag_dim(kb, tt, half), loc = dim - 32 * slice;
+    const float sc = bitenc_scale(2 * (kb & 1) + half);
     float v0, v1;
     if (plane == a.n_lm) {  // QJL plane
-      v0 = -qt[gg][col];
-      v1 = -qt[gg][col + 1];
+      v0 = -qt[gg][loc];
+      v1 = -qt[gg][loc + 1];
     } else {
       const float wl = plane == 0 ? a.lm_w[0] : plane == 1 ? a.lm_w[1] : plane == 2 ? a.lm_w[2] : a.lm_w[3];
       v0 = wl * qr[gg][dim];
       v1 = wl * qr[gg][dim + 1];
     }
     uint32_t hi, lo;
-    split2(v0, v1, hi, lo);
+    split2(v0 * sc, v1 * sc, hi, lo);
     dst[(ks * 32 + L) * 4 + 2 * half] = hi;
     dst[(ks * 32 + L) * 4 + 2 * half + 1] = lo;
+  }
+  // this slice's part of the score offsets (coordinate 32 slice + lane)
+  {
+    const float cf = bitenc_offset((lane >> 1) & 3);
+    const float lsum = (a.lm_w[0] + a.lm_w[1]) + (a.lm_w[2] + a.lm_w[3]);
+    float* off = reinterpret_cast<float*>(base + KSTEPS_MAX * 32) + slice * 2 * kMaxRep;
+    for (int h = warp; h < kMaxRep; h += NWARP) {
+      const float sl = warp_sum(qr[h][32 * slice + lane] * cf);
+      const float sq = warp_sum(qt[h][lane] * cf);
+      if (lane == 0) {
+        off[h] = lsum * sl;
+        off[kMaxRep + h] = -sq;
+      }
+    }
   }
 }
 
@@ -321,50 +390,53 @@ __device__ __forceinline__ void softmax_update(WarpState& st, float (&s)[4], flo
   st.l += (p[0] + p[1]) + (p[2] + p[3]);
 }
 
-// One compressed page (16 tokens) of the warp's KV head.
+// One compressed page (16 tokens) of the warp's KV head.  off_lm / off_qj: this lane's head's score
+// offsets (the accumulators' start values, see bitenc_scale).
 template <int KB, int VB>
 __device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA, const uint8_t* T, WarpState& st,
-                                                int lane) {
+                                                float off_lm, float off_qj, int lane) {
   using L = TcTile<KB, VB>;
   const int g = lane >> 2, t = lane & 3;
-  uint4 rw[KB][2];
-#pragma unroll
-  for (int p = 0; p < KB; ++p) {
-    rw[p][0] = *reinterpret_cast<const uint4*>(T + 256 * p + g * 16);
-    rw[p][1] = *reinterpret_cast<const uint4*>(T + 256 * p + (g + 8) * 16);
-  }
+  // accumulators: rows g (high parts) start at the offset, rows g + 8 (low parts) at 0
   float acc[2][2][4];
 #pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) acc[i][n][r] = 0.f;
-  // bit j = 8 half + t (b0) and j + 4 (b1) of each plane word, moved to bit 15
-  const uint32_t mul[4] = {1u << (15 - t), 1u << (11 - t), 1u << (7 - t), 1u << (3 - t)};
+  for (int n = 0; n < 2; ++n) {
+    acc[0][n][0] = acc[0][n][1] = off_lm;
+    acc[1][n][0] = acc[1][n][1] = off_qj;
+    acc[0][n][2] = acc[0][n][3] = acc[1][n][2] = acc[1][n][3] = 0.f;
+  }
+  // bit pairs 4t .. 4t+3 of each plane word to bits 12..15 (see enc12 .. enc15)
+  const uint32_t shm = 1u << (12 - 4 * t);
   constexpr int NA = L::NA;
+  uint4 xr0 = make_uint4(0u, 0u, 0u, 0u), xr1 = xr0;  // 4-bit keys: XOR of the index planes so far
 #pragma unroll
   for (int p = 0; p < NA; ++p) {
+    // A plane p: stored plane p (tokens g and g + 8), except for 4-bit keys: plane 3 = XOR of the
+    // three index planes (the odd parity product), plane 4 = the QJL plane (stored plane 3)
+    uint4 r0, r1;
+    if (KB == 4 && p == 3) {
+      r0 = xr0;
+      r1 = xr1;
+    } else {
+      const int sp = (KB == 4 && p == 4) ? 3 : p;
+      r0 = *reinterpret_cast<const uint4*>(T + 256 * sp + g * 16);
+      r1 = *reinterpret_cast<const uint4*>(T + 256 * sp + (g + 8) * 16);
+      if (KB == 4 && p < 3) {
+        xr0 = make_uint4(xr0.x ^ r0.x, xr0.y ^ r0.y, xr0.z ^ r0.z, xr0.w ^ r0.w);
+        xr1 = make_uint4(xr1.x ^ r1.x, xr1.y ^ r1.y, xr1.z ^ r1.z, xr1.w ^ r1.w);
+      }
+    }
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      // A plane p: stored plane p, except for 4-bit keys: plane 3 = XOR of the three index
-      // planes (the odd parity product), plane 4 = the QJL plane (stored plane 3)
-      uint32_t w0, w1;
-      if (KB == 4 && p == 3) {
-        w0 = word_of(rw[0][0], w) ^ word_of(rw[1][0], w) ^ word_of(rw[2][0], w);
-        w1 = word_of(rw[0][1], w) ^ word_of(rw[1][1], w) ^ word_of(rw[2][1], w);
-      } else {
-        const int sp = (KB == 4 && p == 4) ? 3 : (p < KB ? p : KB - 1);
-        w0 = word_of(rw[sp][0], w);
-        w1 = word_of(rw[sp][1], w);
-      }
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const uint4 A = sA[(p * 8 + w * 2 + half) * 32 + lane];
-        const uint32_t m0 = mul[2 * half], m1 = mul[2 * half + 1];
-        mma_f16(acc[p == NA - 1][0], A, sgn_pair(w0, m0), sgn_pair(w0, m1));
-        mma_f16(acc[p == NA - 1][1], A, sgn_pair(w1, m0), sgn_pair(w1, m1));
-      }
+      const uint32_t w0 = word_of(r0, w), w1 = word_of(r1, w);
+      const uint32_t x0 = mul_lo(w0, shm), x1 = mul_lo(w1, shm);
+      // k-step 2w: bits 12 (b0) and 13 (b1); k-step 2w + 1: bits 14 and 15
+      const uint4 A0 = sA[(p * 8 + 2 * w) * 32 + lane];
+      const uint4 A1 = sA[(p * 8 + 2 * w + 1) * 32 + lane];
+      mma_f16(acc[p == NA - 1][0], A0, enc12(x0), enc13(x0));
+      mma_f16(acc[p == NA - 1][1], A0, enc12(x1), enc13(x1));
+      mma_f16(acc[p == NA - 1][0], A1, enc14(x0), enc15(x0));
+      mma_f16(acc[p == NA - 1][1], A1, enc14(x1), enc15(x1));
     }
   }
   // logits of tokens 2t, 2t+1 (n-tile 0) and 8+2t, 9+2t (n-tile 1), log2 domain
@@ -475,8 +547,10 @@ __device__ __forceinline__ void page_ring(const TcArgs& a, const uint4 (&Aq)[8],
   }
 }
 
-template <int KB, int VB>
-__global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
+// MINB: CTAs per SM the register allocation must allow (3 for multi-wave grids; 2 for grids that
+// fit in one wave at 2 CTAs per SM, where the extra registers remove spills from the page loop).
+template <int KB, int VB, int MINB>
+__global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
   using L = TcTile<KB, VB>;
   extern __shared__ __align__(16) uint8_t smem[];
   uint4* sA = reinterpret_cast<uint4*>(smem);
@@ -485,6 +559,7 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
   __shared__ int sblk[NWARP][STAGES];
   __shared__ __align__(16) float qr[kMaxRep][D];
   __shared__ __align__(16) float qt[kMaxRep][D];
+  __shared__ __align__(16) float soff[kPrepSlices][2][kMaxRep];  // score offsets (partial sums)
 
   const int part = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int kvh = hg / a.groups;
@@ -518,6 +593,7 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
     if (a.afrag) {
       const uint4* af = a.afrag + ((size_t)b * a.hkv * a.groups + hg) * AFRAG_U4;
       for (int i = tid; i < L::NA * 8 * 32; i += blockDim.x) cp16(&sA[i], &af[i]);
+      if (tid < kPrepSlices * 2 * kMaxRep / 4) cp16(reinterpret_cast<uint4*>(&soff[0][0][0]) + tid, &af[KSTEPS_MAX * 32 + tid]);
       cp_commit();
     }
     const int pbeg = part * a.chunk_pages;
@@ -547,7 +623,15 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
       cp_wait<STAGES - 1>();
       __syncthreads();  // every thread's share of the fragments has landed
     } else {
-      build_query_frags(a, b, h0, sA, qr, qt, tid, lane, warp);  // ends with __syncthreads
+      build_query_frags(a, b, h0, sA, qr, qt, soff, tid, lane, warp);  // ends with __syncthreads
+    }
+    // score offsets of this lane's head: the four partial sums (prep slices, or the fused prep's
+    // warps) added once, outside the page loop
+    float off_lm = 0.f, off_qj = 0.f;
+#pragma unroll
+    for (int sl = 0; sl < kPrepSlices; ++sl) {
+      off_lm += soff[sl][0][g];
+      off_qj += soff[sl][1][g];
     }
     for (int k = 0; k < nw; ++k) {
       __syncwarp();  // every lane is done with the slot and stage that are refilled next
@@ -561,7 +645,7 @@ __global__ void __launch_bounds__(128, 3) tc_decode_kernel(TcArgs a) {
         if (lane == 0) flag_error(a.err, TQ_DEVERR_BLOCK_ID);
         continue;
       }
-      page_compressed<KB, VB>(a, sA, wst + (k % STAGES) * L::TILE, st, lane);
+      page_compressed<KB, VB>(a, sA, wst + (k % STAGES) * L::TILE, st, off_lm, off_qj, lane);
       __syncwarp();
     }
     cp_wait<0>();
@@ -743,9 +827,13 @@ cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) 
   }
   const int kb = ctx->cfg.key_bits;
   const bool v4 = ctx->cfg.value_bits == 4;
-  auto kern = kb == 4 ? (v4 ? tc_decode_kernel<4, 4> : tc_decode_kernel<4, 2>)
-            : kb == 3 ? (v4 ? tc_decode_kernel<3, 4> : tc_decode_kernel<3, 2>)
-                      : (v4 ? tc_decode_kernel<2, 4> : tc_decode_kernel<2, 2>);
+  const bool wide = (int64_t)a.n_parts * hgroups * batch <= 2 * (int64_t)ctx->sm_count;  // one wave at 2 per SM
+  auto kern = wide ? (kb == 4 ? (v4 ? tc_decode_kernel<4, 4, 2> : tc_decode_kernel<4, 2, 2>)
+                    : kb == 3 ? (v4 ? tc_decode_kernel<3, 4, 2> : tc_decode_kernel<3, 2, 2>)
+                              : (v4 ? tc_decode_kernel<2, 4, 2> : tc_decode_kernel<2, 2, 2>))
+                   : (kb == 4 ? (v4 ? tc_decode_kernel<4, 4, 3> : tc_decode_kernel<4, 2, 3>)
+                    : kb == 3 ? (v4 ? tc_decode_kernel<3, 4, 3> : tc_decode_kernel<3, 2, 3>)
+                              : (v4 ? tc_decode_kernel<2, 4, 3> : tc_decode_kernel<2, 2, 3>));
   const size_t smem = kb == 4 ? (v4 ? TcTile<4, 4>::SMEM_TOTAL : TcTile<4, 2>::SMEM_TOTAL)
                     : kb == 3 ? (v4 ? TcTile<3, 4>::SMEM_TOTAL : TcTile<3, 2>::SMEM_TOTAL)
                               : (v4 ? TcTile<2, 4>::SMEM_TOTAL : TcTile<2, 2>::SMEM_TOTAL);

@@ -262,7 +262,7 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
     // kernel, because there the per-CTA cost (~3 us) outweighs the saved launch.
     const int64_t ctas = (int64_t)pl.n_parts * hkv * groups * batch;
     pl.fused_prep = ctas <= (int64_t)ctx->sm_count * 3;
-    pl.q_bytes = pl.fused_prep ? 0 : align((size_t)batch * hkv * groups * 40 * 32 * 16);  // <= 5 A planes x 8
+    pl.q_bytes = pl.fused_prep ? 0 : align((size_t)batch * hkv * groups * kTcQueryU4 * 16);
   } else
     pl.q_bytes = ctx->cfg.layout == TQ_LAYOUT_MAIN ? align(sizeof(float) * batch * hq * 2 * d) : 0;
   pl.part_bytes = align(sizeof(float) * (size_t)batch * hq * pl.n_parts * (d + (pl.tensor_core ? 4 : 2)));

@@ -20,7 +20,7 @@ struct TcArgs {
   const int32_t* n_buf;
   int max_ctx;
   float* out;
-  uint4* afrag;    // [B][Hkv * groups][24 k-steps][32 lanes] query fragments, or NULL: built per CTA
+  uint4* afrag;    // [B][Hkv * groups][kTcQueryU4] query fragments and score offsets, or NULL: built per CTA
   float* parts;    // [B][Hq][n_parts][d + 4] split-K partials (o, m, l, pad)
   int chunk_pages, n_chunks, n_parts;
   int hq, hkv, n_rep, nrg, groups;

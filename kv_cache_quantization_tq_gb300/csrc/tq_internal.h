@@ -17,6 +17,10 @@ constexpr int kRing = 128;       // exact recent-token buffer
 constexpr int kGroup = 32;       // value group / key block
 constexpr int kMaxRep = 8;       // query heads handled by one decode CTA
 constexpr int kMaxChunks = 8192;  // split-K chunks per sequence (merge weights in shared memory)
+// Tensor-core decode query workspace per (sequence, head group), in 16-byte units: the score A
+// fragments of up to 5 planes x 8 k-steps x 32 lanes, then 4 prep slices x 2 x kMaxRep partial
+// score offsets (floats).
+constexpr int kTcQueryU4 = 5 * 8 * 32 + 4 * 2 * kMaxRep / 4;
 
 // Small per-context tables passed by value as kernel parameters.
 struct CodeTables {
