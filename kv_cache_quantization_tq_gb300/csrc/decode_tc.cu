@@ -183,6 +183,7 @@ __device__ __forceinline__ int tc_nb(const TcArgs& a, int b) {
 //   reg2 = row g,   cols 2t+8..2t+9   reg3 = row g+8, cols 2t+8..2t+9
 // with g = lane / 4, t = lane % 4; row g is head g (high part), row g+8 the
 // same head's low part.
+template <int NA>
 __device__ __forceinline__ void build_query_frags(const TcArgs& a, int b, int h0, uint4* sA, float (*qr)[D],
                                                   float (*qt)[D], float (*soff)[2][kMaxRep], int tid, int lane,
                                                   int warp) {
@@ -250,15 +251,19 @@ __device__ __forceinline__ void build_query_frags(const TcArgs& a, int b, int h0
     }
   }
   __syncthreads();
+  // NA planes x 8 k-steps x 32 lanes x 2 register pairs, NWARP * 32 items per pass: the plane of
+  // every pass is a compile-time constant (a pass covers two k-steps of one plane)
+  static_assert(NWARP * 32 == 128, "two k-steps per pass");
   uint32_t* dst = reinterpret_cast<uint32_t*>(sA);
-  for (int idx = tid; idx < (a.n_lm + 1) * 8 * 32 * 2; idx += NWARP * 32) {
-    const int half = idx & 1, L = (idx >> 1) & 31, ks = idx >> 6;  // k-steps: 8 per A plane, QJL last
-    const int plane = ks >> 3, kb = ks & 7;
-    const int g = L >> 2, t = L & 3;
+  const int half = tid & 1, L = (tid >> 1) & 31, g = L >> 2, t = L & 3;
+#pragma unroll
+  for (int it = 0; it < NA * 4; ++it) {
+    const int ks = 2 * it + (tid >> 6);  // k-steps: 8 per A plane, QJL last
+    const int plane = it >> 2, kb = ks & 7;
     const int dim = frag_dim(kb, t, half);
     const float sc = bitenc_scale(2 * (kb & 1) + half);
     float v0, v1;
-    if (plane == a.n_lm) {  // QJL plane
+    if (plane == NA - 1) {  // QJL plane
       v0 = -qt[g][dim];
       v1 = -qt[g][dim + 1];
     } else {
@@ -623,7 +628,7 @@ __global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
       cp_wait<STAGES - 1>();
       __syncthreads();  // every thread's share of the fragments has landed
     } else {
-      build_query_frags(a, b, h0, sA, qr, qt, soff, tid, lane, warp);  // ends with __syncthreads
+      build_query_frags<L::NA>(a, b, h0, sA, qr, qt, soff, tid, lane, warp);  // ends with __syncthreads
     }
     // score offsets of this lane's head: the four partial sums (prep slices, or the fused prep's
     // warps) added once, outside the page loop
