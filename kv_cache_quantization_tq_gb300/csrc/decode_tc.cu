@@ -70,7 +70,7 @@ struct TcTile {
   static_assert((size_t)NWARP * kMaxRep * D * sizeof(float) <= SMEM_STAGE, "combine buffer fits the stages");
 };
 
-constexpr float kLog2e = 1.4426950408889634f;
+
 constexpr int kPartStride = D + 4;  // floats per split-K partial: o[D], m, l, pad (16-byte rows)
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
@@ -183,21 +183,36 @@ __device__ __forceinline__ int tc_nb(const TcArgs& a, int b) {
 //   reg2 = row g,   cols 2t+8..2t+9   reg3 = row g+8, cols 2t+8..2t+9
 // with g = lane / 4, t = lane % 4; row g is head g (high part), row g+8 the
 // same head's low part.
+// The query values this lane rotates (heads warp and warp + NWARP, coordinates coord_of(e, lane)),
+// times the random signs: loaded at the top of the kernel, together with the sequence's counts
+// and its first block ids, so that these round trips to memory overlap.
+static_assert(kMaxRep == 2 * NWARP, "two heads per warp in the query rotation");
+struct QueryRegs {
+  float x[2][D / 32];
+};
+__device__ __forceinline__ void load_query(const TcArgs& a, int b, int h0, int lane, int warp, QueryRegs& r) {
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) {
+    const int c = coord_of(e, lane);
+    const float sg = a.signs[c];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int h = warp + NWARP * i;
+      r.x[i][e] = h < a.nrg ? __half2float(a.q[((size_t)b * a.hq + h0 + h) * D + c]) * sg : 0.f;
+    }
+  }
+}
+
 template <int NA>
-__device__ __forceinline__ void build_query_frags(const TcArgs& a, int b, int h0, uint4* sA, float (*qr)[D],
+__device__ __forceinline__ void build_query_frags(const TcArgs& a, QueryRegs& qx, uint4* sA, float (*qr)[D],
                                                   float (*qt)[D], float (*soff)[2][kMaxRep], int tid, int lane,
                                                   int warp) {
   const float rs = rsqrtf((float)D);
-  for (int h = warp; h < kMaxRep; h += NWARP) {
-    float x[D / 32];
 #pragma unroll
-    for (int e = 0; e < D / 32; ++e) {
-      const int c = coord_of(e, lane);
-      x[e] = h < a.nrg ? __half2float(a.q[((size_t)b * a.hq + h0 + h) * D + c]) * a.signs[c] : 0.f;
-    }
-    wht_warp<D / 32>(x, lane);
+  for (int i = 0; i < 2; ++i) {
+    wht_warp<D / 32>(qx.x[i], lane);
 #pragma unroll
-    for (int e = 0; e < D / 32; ++e) qr[h][coord_of(e, lane)] = x[e] * rs;
+    for (int e = 0; e < D / 32; ++e) qr[warp + NWARP * i][coord_of(e, lane)] = qx.x[i][e] * rs;
   }
   __syncthreads();
   {
@@ -571,6 +586,19 @@ __global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
   const int h0 = kvh * a.n_rep + (hg % a.groups) * a.nrg;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
+  // Requested before the sequence's counts arrive (they decide what is used): the block ids of
+  // this warp's first STAGES pages of the chunk (any index inside the block-table row is a valid
+  // read) and, when this CTA builds its own query fragments, the query.
+  const int32_t* btb = a.block_table + (size_t)b * a.max_blocks;
+  const int pbeg = part * a.chunk_pages;
+  int blk_pre[STAGES];
+#pragma unroll
+  for (int k = 0; k < STAGES; ++k) {
+    const int idx = pbeg + warp + NWARP * k;
+    blk_pre[k] = (part < a.n_chunks && idx < a.max_blocks) ? __ldg(btb + idx) : -1;
+  }
+  QueryRegs qx;
+  if (!a.afrag && part < a.n_chunks) load_query(a, b, h0, lane, warp, qx);
   const int nc = tc_nc(a, b), nb = tc_nb(a, b);
   const int npages = nc >> 4;
   const int nch = (npages + a.chunk_pages - 1) / a.chunk_pages;
@@ -601,11 +629,9 @@ __global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
       if (tid < kPrepSlices * 2 * kMaxRep / 4) cp16(reinterpret_cast<uint4*>(&soff[0][0][0]) + tid, &af[KSTEPS_MAX * 32 + tid]);
       cp_commit();
     }
-    const int pbeg = part * a.chunk_pages;
     const int npg = min(npages, pbeg + a.chunk_pages) - pbeg;
     const int nw = npg > warp ? (npg - warp + NWARP - 1) / NWARP : 0;
     uint8_t* wst = stage + (size_t)warp * STAGES * L::TILE;
-    const int32_t* btb = a.block_table + (size_t)b * a.max_blocks;
     // Block ids: the id of the next page to copy is read one page ahead, so the table read
     // never holds up a copy (or the compute queued behind it); the ids of the pages in flight
     // are kept per warp in shared memory.
@@ -622,13 +648,13 @@ __global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
       cp_commit();
     };
 #pragma unroll
-    for (int k = 0; k < STAGES - 1; ++k) issue(k, blk_of(k));
-    int nxt = blk_of(STAGES - 1);
+    for (int k = 0; k < STAGES - 1; ++k) issue(k, k < nw ? blk_pre[k] : -1);
+    int nxt = STAGES - 1 < nw ? blk_pre[STAGES - 1] : -1;
     if (a.afrag) {
       cp_wait<STAGES - 1>();
       __syncthreads();  // every thread's share of the fragments has landed
     } else {
-      build_query_frags<L::NA>(a, b, h0, sA, qr, qt, soff, tid, lane, warp);  // ends with __syncthreads
+      build_query_frags<L::NA>(a, qx, sA, qr, qt, soff, tid, lane, warp);  // ends with __syncthreads
     }
     // score offsets of this lane's head: the four partial sums (prep slices, or the fused prep's
     // warps) added once, outside the page loop
@@ -697,21 +723,30 @@ __global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
     wl[warp][g] = l;
   }
   __syncthreads();
+  // per head: the CTA maximum, each warp's weight 2^(m_w - M) (in place of m_w) and the normaliser
+  __shared__ float hM[kMaxRep], hden[kMaxRep];
+  if (tid < kMaxRep) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) M = fmaxf(M, wm[w][tid]);
+    float den = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) {
+      const float f = M == -INFINITY ? 0.f : exp2f(wm[w][tid] - M);
+      wm[w][tid] = f;
+      den = fmaf(f, wl[w][tid], den);
+    }
+    hM[tid] = M;
+    hden[tid] = den;
+  }
+  __syncthreads();
   const bool direct = nparts == 1;  // sole contributor: write the output itself
   for (int i = tid; i < a.nrg * D; i += blockDim.x) {
     const int h = i / D, dim = i % D;
-    float M = -INFINITY;
+    const float M = hM[h], den = hden[h];
+    float num = 0.f;
 #pragma unroll
-    for (int w = 0; w < NWARP; ++w) M = fmaxf(M, wm[w][h]);
-    float num = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < NWARP; ++w) {
-        const float f = exp2f(wm[w][h] - M);
-        num = fmaf(f, wo[((size_t)w * kMaxRep + h) * D + dim], num);
-        den = fmaf(f, wl[w][h], den);
-      }
-    }
+    for (int w = 0; w < NWARP; ++w) num = fmaf(wm[w][h], wo[((size_t)w * kMaxRep + h) * D + dim], num);
     if (direct) {
       a.out[((size_t)b * a.hq + h0 + h) * D + dim] = den > 0.f ? num / den : 0.f;
     } else {
@@ -732,17 +767,84 @@ __global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
 // and weighted sums are reduced over all partials by the whole CTA, then 16
 // slices of partials x 8 lanes of 16-byte loads cover the 32 dimensions.
 constexpr int kMergeSplit = 4;  // dimension quarters per head
+constexpr int kMergeBatch = 8;  // chunk slots per thread on the one-round-trip path (<= 128 chunks)
 __global__ void __launch_bounds__(128) tc_merge_kernel(TcArgs a) {
   extern __shared__ float sw[];  // [n_parts] weights
   __shared__ float4 red[16][8];
   __shared__ float s_m[NWARP], s_l[NWARP];
   const int h = blockIdx.x, b = blockIdx.y, quarter = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* base = a.parts + ((size_t)b * a.hq + h) * a.n_parts * kPartStride;
+  const int slice = tid >> 3, q4 = tid & 7;  // 16 partial slices, 8 float4 of this quarter
+  const int col4 = quarter * 8 + q4;
+  if (a.n_chunks <= 16 * kMergeBatch) {
+    // Up to 16 x kMergeBatch chunk slots (and the ring slot): every slot this thread may need is
+    // requested at once, together with the sequence's counts, and the slots past the sequence's
+    // chunk count are dropped afterwards, so the whole merge costs one round trip to L2.
+    float m[kMergeBatch], l[kMergeBatch];
+    float4 v[kMergeBatch];
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) {
+      const int i = slice + 16 * j;
+      if (i < a.n_chunks) {
+        const float* pp = base + (size_t)i * kPartStride;
+        m[j] = __ldcg(pp + D);
+        l[j] = __ldcg(pp + D + 1);
+        v[j] = __ldcg(reinterpret_cast<const float4*>(pp) + col4);
+      }
+    }
+    const float* pr = base + (size_t)a.n_chunks * kPartStride;  // ring slot
+    const float mr = __ldcg(pr + D), lr = __ldcg(pr + D + 1);
+    const float4 vr = __ldcg(reinterpret_cast<const float4*>(pr) + col4);
+    const int nc = tc_nc(a, b), nb = tc_nb(a, b);
+    const int nch = ((nc >> 4) + a.chunk_pages - 1) / a.chunk_pages;
+    if (nch + (nb > 0 ? 1 : 0) <= 1) return;  // written by the decode kernel itself
+    float M = nb > 0 ? mr : -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j)
+      if (slice + 16 * j < nch) M = fmaxf(M, m[j]);
+    M = warp_max(M);
+    if (lane == 0) s_m[warp] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](float mi, float li, const float4& vi) {
+      const float w = exp2f(mi - M);
+      den = fmaf(w, li, den);
+      acc.x = fmaf(w, vi.x, acc.x);
+      acc.y = fmaf(w, vi.y, acc.y);
+      acc.z = fmaf(w, vi.z, acc.z);
+      acc.w = fmaf(w, vi.w, acc.w);
+    };
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j)
+        if (slice + 16 * j < nch) add(m[j], l[j], v[j]);
+      if (nb > 0 && slice == 0) add(mr, lr, vr);
+    }
+    red[slice][q4] = acc;
+    den = q4 == 0 ? den : 0.f;  // each slice's normaliser counted once
+    den = warp_sum(den);
+    if (lane == 0) s_l[warp] = den;
+    __syncthreads();
+    if (tid < 32) {
+      den = (s_l[0] + s_l[1]) + (s_l[2] + s_l[3]);
+      const int c = tid >> 2, comp = tid & 3;  // 8 float4 x 4 components = 32 dimensions
+      float o = 0.f;
+#pragma unroll
+      for (int sl = 0; sl < 16; ++sl) {
+        const float4 r = red[sl][c];
+        o += comp == 0 ? r.x : comp == 1 ? r.y : comp == 2 ? r.z : r.w;
+      }
+      a.out[((size_t)b * a.hq + h) * D + quarter * 32 + tid] = den > 0.f ? o / den : 0.f;
+    }
+    return;
+  }
   const int nc = tc_nc(a, b), nb = tc_nb(a, b);
   const int nch = ((nc >> 4) + a.chunk_pages - 1) / a.chunk_pages;
   const int nparts = nch + (nb > 0 ? 1 : 0);
   if (nparts <= 1) return;
-  const float* base = a.parts + ((size_t)b * a.hq + h) * a.n_parts * kPartStride;
   auto part = [&](int i) { return base + (size_t)(i < nch ? i : a.n_chunks) * kPartStride; };
   float M = -INFINITY;
   for (int i = tid; i < nparts; i += 128) {
@@ -765,8 +867,6 @@ __global__ void __launch_bounds__(128) tc_merge_kernel(TcArgs a) {
   if (lane == 0) s_l[warp] = den;
   __syncthreads();
   den = (s_l[0] + s_l[1]) + (s_l[2] + s_l[3]);
-  const int slice = tid >> 3, q4 = tid & 7;  // 16 partial slices, 8 float4 of this quarter
-  const int col4 = quarter * 8 + q4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int i = slice; i < nparts; i += 16) {

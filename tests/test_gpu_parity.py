@@ -160,6 +160,20 @@ def test_decode_main_without_ring_argument():
     assert allclose_report(got, ref)[0]
 
 
+def test_decode_main_many_chunk_slots():
+    """max_ctx far above the contexts: over 128 split-K chunk slots (the merge's general path) and a
+    grid large enough for the separate query-fragment kernel."""
+    d, hkv, n_rep, seed = 128, 1, 4, 91
+    ctx, c, s, sk = make_ctx(tq, True, d, hkv * n_rep, hkv, seed)
+    e = build_main_cache(seed, d, hkv, [2000, 700], c, s, sk)
+    e["max_ctx"] = 320000
+    q = synth.queries(seed, 2, hkv * n_rep, d)
+    got = _run_decode(ctx, e, q, hkv * n_rep, d)
+    ref = attention.decode_main(q, e["pool"], e["bt"], e["n_c"], e["ring_k"], e["ring_v"], e["n_b"], s, c, sk, hkv)
+    ok, maxerr, nbad = allclose_report(got, ref)
+    assert ok, f"max abs err {maxerr}, {nbad} elements outside 2e-3 + 1e-3|ref|"
+
+
 def test_decode_empty_sequence_gives_zeros():
     d, hkv, seed = 128, 2, 5
     ctx, c, s, sk = make_ctx(tq, True, d, 4, hkv, seed)
