@@ -108,8 +108,8 @@ def aggregate_gbs(bytes_per_rank: int, ms_max: float, world: int) -> float:
 # profiles/ (dram__bytes_read.sum + dram__bytes_write.sum).  An entry is valid only for the
 # kernel source it was captured on; a workload without one reports null.
 NCU_TRAFFIC = {
-    ("qwen3-0.6b-32k", "tc_decode_kernel"): 13259776,     # profiles/tc_decode_kernel__qwen3-0.6b-32k.md
-    ("qwen2.5-7b-b8", "tc_decode_kernel"): 108829696,     # profiles/tc_decode_kernel__qwen2.5-7b-b8.md
+    ("qwen3-0.6b-32k", "tc_decode_kernel"): 13262080,     # profiles/tc_decode_kernel__qwen3-0.6b-32k.md
+    ("qwen2.5-7b-b8", "tc_decode_kernel"): 109771520,     # profiles/tc_decode_kernel__qwen2.5-7b-b8.md
     ("alt-d128", "decode_alt_v2_kernel"): 412410624,      # profiles/decode_alt_v2_kernel__alt-d128.md
 }
 
@@ -445,6 +445,27 @@ def run_gpu(args, w, rank, world):
     torch.cuda.synchronize()
     prof = [lay.ctx.profile_end() for lay in layers]  # events of the last replay
     del timed_graph, prof_graph
+    # The same decode calls (decode + merge kernels of every layer, at the last step's counts)
+    # captured back to back with no events between them, timed by one event pair: the per-launch
+    # event pairs above each add the front end's drain and launch latency to the kernel they
+    # bracket, which this figure does not contain.
+    def decode_calls():
+        for li, lay in enumerate(layers):
+            lay.ctx.decode_attention(q[li], lay.pool, lay.bt, sg.nc, lay.ring_k if main else None,
+                                     lay.ring_v if main else None, sg.nb if main else None, max_ctx, lay.out, ws)
+    dgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(dgraph, capture_error_mode="thread_local"):
+        decode_calls()
+    dgraph.replay()
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record()
+    for _ in range(prof_steps):
+        dgraph.replay()
+    d1.record()
+    torch.cuda.synchronize()
+    call_us = d0.elapsed_time(d1) / (prof_steps * nl) * 1e3
+    del dgraph
     if world > 1:
         ms = max_over_ranks(ms, device="cuda")
         torch.distributed.barrier()
@@ -464,6 +485,7 @@ def run_gpu(args, w, rank, world):
                 "kernel": decode_kernel_name(w),
                 "peak_source": peak_kind, "launches": dec_n, "avg_launch_us": dec_ms / max(dec_n, 1) * 1e3,
                 "merge_us_per_launch": sum(p["merge_ms"] for p in prof) / max(dec_n, 1) * 1e3,
+                "decode_call_us_back_to_back": call_us,
                 "bytes_per_launch": per_launch_bytes}
 
     e2e = run_e2e(torch, w, layers, pos, max_ctx, ws, q, kn, vn, bytes_at)
