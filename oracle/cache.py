@@ -58,8 +58,16 @@ def encode_main_range(pool, block_table, start, k16, v16, signs, centroids, s_ma
     return enc
 
 
+def value_bits_of(centroids) -> int:
+    """Alternate-layout value bits for a Lloyd-Max codebook of 2^bits centroids."""
+    k = len(centroids)
+    assert k in (4, 8, 16), k
+    return k.bit_length() - 1
+
+
 def encode_alt_range(pool, block_table, start, k16, v16, signs, centroids3):
-    """Alternate layout: encode fp16 k/v [B, Hkv, T, d] into ``pool``."""
+    """Alternate layout: encode fp16 k/v [B, Hkv, T, d] into ``pool`` (value bits from the codebook
+    size: 4, 8 or 16 centroids)."""
     k16 = np.asarray(k16, dtype=np.float16)
     bsz, hkv, t, d = k16.shape
     assert start % layout.P == 0 and t % layout.P == 0
@@ -72,6 +80,7 @@ def encode_alt_range(pool, block_table, start, k16, v16, signs, centroids3):
         kmn.reshape(bsz, hkv, npg, 16, d // 32),
         venc["idx"].reshape(bsz, hkv, npg, 16, d),
         venc["n_v"].reshape(bsz, hkv, npg, 16),
+        value_bits_of(centroids3),
     )
     pages = start // layout.P + np.arange(npg)
     blocks = np.asarray(block_table)[:, pages]

@@ -242,26 +242,35 @@ def unpack_main_tiles(tiles: np.ndarray, d: int, kbits: int = None) -> dict:
 
 
 # ---------------------------------------------------------------- alternate layout
-def alt_tile_bytes(d: int) -> int:
-    return 24 * d + 32
+def alt_tile_bytes(d: int, vbits: int = 3) -> int:
+    """One page of the alternate layout: 16 x (d 8-bit key codes + d/32 fp16 (scale, minimum)
+    pairs + a dense vbits-bit stream of value indices + one fp16 value norm)."""
+    return 18 * d + 2 * vbits * d + 32
 
 
-def alt_bytes_per_token_head(d: int) -> float:
-    return alt_tile_bytes(d) / P
+def alt_bytes_per_token_head(d: int, vbits: int = 3) -> float:
+    return alt_tile_bytes(d, vbits) / P
 
 
-def pack_alt_tiles(kq, ks16, kmn16, vidx, nv16) -> np.ndarray:
-    """kq [..., 16, d] uint8; ks16/kmn16 [..., 16, d/32]; vidx [..., 16, d] (3-bit); nv16 [..., 16]."""
+def alt_value_bits(tile_bytes: int, d: int) -> int:
+    """Value bits of an alternate-layout tile from its size (the size is 18d + 2 vbits d + 32)."""
+    vb, rem = divmod(tile_bytes - 18 * d - 32, 2 * d)
+    assert rem == 0 and vb in (2, 3, 4), (tile_bytes, d)
+    return vb
+
+
+def pack_alt_tiles(kq, ks16, kmn16, vidx, nv16, vbits: int = 3) -> np.ndarray:
+    """kq [..., 16, d] uint8; ks16/kmn16 [..., 16, d/32]; vidx [..., 16, d] (vbits-bit); nv16 [..., 16]."""
     kq = np.asarray(kq, dtype=np.uint8)
     d = kq.shape[-1]
     lead = kq.shape[:-2]
     kqb = kq.reshape(lead + (16 * d,))
     sm = np.stack([np.asarray(ks16, np.float16), np.asarray(kmn16, np.float16)], axis=-1)
     ksm = _f16_bytes(sm.reshape(lead + (16 * (d // 32) * 2,)))
-    vi = pack_rows(vidx, 3).reshape(lead + (16 * 3 * d // 8,))
+    vi = pack_rows(vidx, vbits).reshape(lead + (16 * vbits * d // 8,))
     vn = _f16_bytes(nv16)
     out = np.concatenate([kqb, ksm, vi, vn], axis=-1)
-    assert out.shape[-1] == alt_tile_bytes(d)
+    assert out.shape[-1] == alt_tile_bytes(d, vbits)
     return out
 
 
@@ -269,10 +278,12 @@ def unpack_alt_tiles(tiles: np.ndarray, d: int) -> dict:
     t = np.asarray(tiles, dtype=np.uint8)
     lead = t.shape[:-1]
     g = d // 32
+    vb = alt_value_bits(t.shape[-1], d)
+    o_n = 18 * d + 2 * vb * d
     kq = t[..., : 16 * d].reshape(lead + (16, d))
     sm = np.ascontiguousarray(t[..., 16 * d:18 * d]).view("<f2").reshape(lead + (16, g, 2))
-    vi = unpack_rows(t[..., 18 * d:24 * d].reshape(lead + (16, 3 * d // 8)), d, 3)
-    nv = np.ascontiguousarray(t[..., 24 * d:24 * d + 32]).view("<f2")
+    vi = unpack_rows(t[..., 18 * d:o_n].reshape(lead + (16, vb * d // 8)), d, vb)
+    nv = np.ascontiguousarray(t[..., o_n:o_n + 32]).view("<f2")
     return {
         "kq": kq.copy(),
         "ks": sm[..., 0].astype(np.float16),

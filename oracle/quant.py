@@ -149,7 +149,7 @@ def encode_alt_keys(k16: np.ndarray, block: int = 32):
 
 
 def encode_alt_values(v16: np.ndarray, signs: np.ndarray, centroids: np.ndarray):
-    """Alternate-layout values: (idx uint8 3-bit, n_v fp16, y float64)."""
+    """Alternate-layout values: (idx uint8 Lloyd-Max index, n_v fp16, y float64)."""
     v = np.asarray(v16, dtype=np.float16).astype(np.float64)
     nv = np.sqrt(np.sum(v * v, axis=-1))
     safe = np.where(nv > 0, nv, 1.0)

@@ -43,7 +43,7 @@ def test_one_bit_closed_form(d):
     assert b.shape == (1,) and b[0] == 0.0
 
 
-@pytest.mark.parametrize("d,bits", [(64, 2), (128, 2), (128, 3), (256, 2), (512, 3), (128, 4)])
+@pytest.mark.parametrize("d,bits", [(64, 2), (128, 2), (128, 3), (256, 2), (512, 3), (128, 4), (64, 4), (512, 4)])
 def test_fixed_point_conditions_by_quadrature(d, bits):
     c, b = codebook.lloyd_max(d, bits)
     k = 1 << bits

@@ -140,22 +140,27 @@ def test_main_tile_round_trip(d):
 
 
 @pytest.mark.parametrize("d", [64, 128, 256, 512])
-def test_alt_tile_round_trip(d):
-    g = np.random.default_rng(d + 1)
+@pytest.mark.parametrize("vbits", [2, 3, 4])
+def test_alt_tile_round_trip(d, vbits):
+    g = np.random.default_rng(d + vbits)
     f = {
         "kq": g.integers(0, 256, (2, 16, d), dtype=np.uint8),
         "ks": g.standard_normal((2, 16, d // 32)).astype(np.float16),
         "kmn": g.standard_normal((2, 16, d // 32)).astype(np.float16),
-        "vidx": g.integers(0, 8, (2, 16, d), dtype=np.uint8),
+        "vidx": g.integers(0, 1 << vbits, (2, 16, d), dtype=np.uint8),
         "n_v": g.standard_normal((2, 16)).astype(np.float16),
     }
-    t = layout.pack_alt_tiles(f["kq"], f["ks"], f["kmn"], f["vidx"], f["n_v"])
-    assert t.shape == (2, layout.alt_tile_bytes(d))
+    t = layout.pack_alt_tiles(f["kq"], f["ks"], f["kmn"], f["vidx"], f["n_v"], vbits)
+    assert t.shape == (2, layout.alt_tile_bytes(d, vbits))
     back = layout.unpack_alt_tiles(t, d)
     for k, v in f.items():
         assert np.array_equal(back[k].view(np.uint8), v.view(np.uint8)), k
-    row = t[1, 18 * d + 5 * (3 * d // 8):18 * d + 6 * (3 * d // 8)]
-    assert np.array_equal(row, _pack_bigint(f["vidx"][1, 5], 3))
+    row_bytes = vbits * d // 8
+    row = t[1, 18 * d + 5 * row_bytes:18 * d + 6 * row_bytes]
+    assert np.array_equal(row, _pack_bigint(f["vidx"][1, 5], vbits))
+    # the value norms follow the index stream
+    o_n = 18 * d + 16 * row_bytes
+    assert np.array_equal(t[0, o_n:o_n + 32].view("<f2"), f["n_v"][0])
 
 
 def test_bytes_per_token_closed_form():
@@ -167,6 +172,11 @@ def test_bytes_per_token_closed_form():
     for d in (64, 128, 256, 512):
         assert layout.alt_bytes_per_token_head(d) == 1.5 * d + 2
         assert layout.main_tile_bytes(d) % 16 == 0 and layout.alt_tile_bytes(d) % 16 == 0
+        for vb in (2, 3, 4):
+            # d 8-bit key codes, 4 B per key block of 32, vb bits per value index, one fp16 norm
+            assert layout.alt_bytes_per_token_head(d, vb) == d + 4 * (d // 32) + vb * d / 8 + 2
+            assert layout.alt_tile_bytes(d, vb) % 16 == 0
+            assert layout.alt_value_bits(layout.alt_tile_bytes(d, vb), d) == vb
 
 
 def test_memory_table_of_the_benchmark_page():
@@ -187,8 +197,11 @@ def test_vllm_metal_compression_table_reading():
     for row in golden("vllm_metal_compression.json")["rows"]:
         per = row["k_bits"] * d / 8 + 16 + row["v_bits"] * d / 8 + 8
         assert round(2 * d * 2 / per, 2) == row["ratio_printed"]
-    # this project's alternate layout (int8 K + 3-bit V) is tighter by 6 B
+    # this project's alternate layout (int8 K + 3-bit V) is tighter by 6 B: one fp16 norm per value
+    # vector in place of the table's 8 B; the same holds at 2- and 4-bit values
     assert layout.alt_bytes_per_token_head(128) == 194
+    for vb in (2, 3, 4):
+        assert layout.alt_bytes_per_token_head(128, vb) == (8 * 128 / 8 + 16) + (vb * 128 / 8 + 8) - 6
 
 
 def test_ring_split():

@@ -1,5 +1,6 @@
 """Pins for the oracle's prefill materialisation (dense history from the compressed pool)."""
 import numpy as np
+import pytest
 
 import synth
 from oracle import attention, cache, codebook, layout, rng
@@ -51,14 +52,15 @@ def test_main_materialised_rows_keep_ring_exact_and_values_within_half_a_step():
     assert cos.mean() > 0.8
 
 
-def test_alt_materialised_history_reproduces_the_decode():
+@pytest.mark.parametrize("vbits", [2, 3, 4])
+def test_alt_materialised_history_reproduces_the_decode(vbits):
     seed, d, hkv, bsz = 5, 64, 2, 2
     sg = rng.signs(seed, d)
-    c3, _ = codebook.lloyd_max(d, 3)
+    c3, _ = codebook.lloyd_max(d, vbits)
     lengths = [160, 96]
     k, v = synth.kv_alt(seed, bsz, hkv, 160, d)
     bt = synth.block_table(seed, bsz, 10, True)
-    pool = np.zeros((bsz * 10, hkv, layout.alt_tile_bytes(d)), np.uint8)
+    pool = np.zeros((bsz * 10, hkv, layout.alt_tile_bytes(d, vbits)), np.uint8)
     for b, L in enumerate(lengths):
         cache.encode_alt_range(pool, bt[b:b + 1], 0, k[b:b + 1, :, :L], v[b:b + 1, :, :L], sg, c3)
     q = synth.queries(seed, bsz, hkv, d)
