@@ -55,6 +55,9 @@ WORKLOADS = {
     # the batch-8 geometry with 4-bit value codes (--value-bits 4)
     "qwen2.5-7b-b8-v4": dict(layout="main", layers=28, batch=8, hq=28, hkv=4, d=128, ctx=32768, shuffled=True, seed=0,
                              vbits=4),
+    # the alternate layout with 4-bit value indices (8-bit keys + 4-bit values: the K8+V4 mix)
+    "alt-d128-v4": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=128, ctx=65536, shuffled=False, seed=0,
+                        vbits=4),
 }
 DEFAULT_WORKLOAD = "qwen3-0.6b-32k"
 
@@ -69,7 +72,9 @@ def ring_split(length: int):
 
 def record_bytes(w) -> int:
     d = w["d"]
-    return (3 * d) // 8 + (w.get("vbits", 2) * d) // 8 + d // 8 + 4 if w["layout"] == "main" else (3 * d) // 2 + 2
+    if w["layout"] == "main":
+        return (3 * d) // 8 + (w.get("vbits", 2) * d) // 8 + d // 8 + 4
+    return d + 4 * (d // 32) + (w.get("vbits", 3) * d) // 8 + 2  # 8-bit keys, block (scale, min), indices, norm
 
 
 def step_bytes(w, lengths_after_append):
@@ -200,7 +205,7 @@ class Layer:
     def __init__(self, tq, torch, w, layer_idx, lengths, max_len, bt_np):
         lay = tq.TQ_LAYOUT_MAIN if w["layout"] == "main" else tq.TQ_LAYOUT_ALT
         self.ctx = tq.Context(lay, w["d"], w["hq"], w["hkv"], w["seed"] + layer_idx,
-                              value_bits=w.get("vbits") if w["layout"] == "main" else None)
+                              value_bits=w.get("vbits"))
         self.max_blocks = bt_np.shape[1]
         self.bt = torch.from_numpy(bt_np).cuda()
         nblk = bt_np.shape[0] * bt_np.shape[1]
@@ -553,11 +558,12 @@ def oracle_layer_step(w, seed, sample_len):
             attention.decode_main(q, pool, bt, np.array([nc]), ring_k, ring_v, np.array([nb]), sg, c, sk, hkv)
         nbytes = hkv * (nc * record_bytes(w) + nb * 4 * d) + hq * d * 6
     else:
-        c3, _ = codebook.lloyd_max(d, 3)
+        vb = w.get("vbits", 3)
+        c3, _ = codebook.lloyd_max(d, vb)
         sg = rng.signs(seed, d)
         k, v = synth.kv_alt(seed, 1, hkv, L, d)
         bt = np.arange(L // 16, dtype=np.int32)[None, :]
-        pool = np.zeros((bt.shape[1], hkv, layout.alt_tile_bytes(d)), np.uint8)
+        pool = np.zeros((bt.shape[1], hkv, layout.alt_tile_bytes(d, vb)), np.uint8)
         cache.encode_alt_range(pool, bt, 0, k, v, sg, c3)
         q = synth.queries(seed, 1, hq, d)
 
@@ -619,8 +625,7 @@ def main():
               "q_heads": w["hq"], "kv_heads": w["hkv"], "head_dim": w["d"],
               "context": w["ctx"] if w["ctx"] is not None else f"U[{w['lo']},{w['hi']}]",
               "l2": "inputs larger than L2 (every step reads all layers' pools)"}
-    if w["layout"] == "main":
-        config["value_bits"] = w.get("vbits", 2)
+    config["value_bits"] = w.get("vbits", 2 if w["layout"] == "main" else 3)
 
     if args.impl == "reference":
         if rank != 0:

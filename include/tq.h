@@ -90,7 +90,9 @@ typedef struct {
   int layout;        /* tq_layout */
   int key_bits;      /* main: 3 (2-bit Lloyd-Max + 1-bit QJL, default), 2 or 4 (1- or 3-bit
                         Lloyd-Max + 1-bit QJL; turboquant vLLM guide, --key-bits); alt: 8 */
-  int value_bits;    /* main: 2 (default) or 4 (turboquant vLLM guide, --value-bits); alt: 3 */
+  int value_bits;    /* main: 2 (default) or 4 (turboquant vLLM guide, --value-bits); alt: 3
+                        (default), 2 or 4 Lloyd-Max index bits per value coordinate (the
+                        vllm-metal guide's q2_0 .. q4_0 value formats; 8 + 4 is its K8+V4) */
   int group_size;    /* value group / key block: must be 32 */
   int qjl_m;         /* main: sketch rows m, must equal head_dim; alt: 0 */
   uint64_t seed;     /* table seed; one table set per layer (base seed + layer) */
@@ -115,7 +117,8 @@ typedef struct {
 const char* tq_status_string(tq_status s);
 
 /* Fill *cfg with the main (key_bits 3 / value_bits 2) or alternate (8 / 3)
- * layout defaults: page 16, ring 128, group 32, qjl_m = head_dim (main). */
+ * layout defaults: page 16, ring 128, group 32, qjl_m = head_dim (main).
+ * key_bits / value_bits may be changed afterwards within the ranges above. */
 tq_status tq_config_init(tq_config* cfg, int layout, int head_dim, int num_q_heads, int num_kv_heads,
                          uint64_t seed);
 
@@ -129,7 +132,7 @@ tq_status tq_create(const tq_config* cfg, tq_ctx** out);
 
 /* As tq_create, with caller-supplied host tables instead of the generated
  * ones: centroids [2^bits] ascending and antisymmetric (c[j] == -c[K-1-j],
- * bits = key_bits - 1 for main keys, 3 for alt values), signs [head_dim] of +-1, sketch
+ * bits = key_bits - 1 for main keys, value_bits for alt values), signs [head_dim] of +-1, sketch
  * [qjl_m][head_dim] row-major (main only; may be NULL for alt).  Decision
  * boundaries are the midpoints of consecutive centroids. */
 tq_status tq_create_with_tables(const tq_config* cfg, const float* centroids, const float* signs,

@@ -189,7 +189,7 @@ class Context:
                  centroids=None, signs=None, sketch=None, value_bits=None, key_bits=None):
         self.cfg = tq_config_init(layout, head_dim, num_q_heads, num_kv_heads, seed)
         if value_bits is not None:
-            self.cfg.value_bits = value_bits  # main layout: 2 or 4
+            self.cfg.value_bits = value_bits  # main layout: 2 or 4; alternate layout: 2, 3 or 4
         if key_bits is not None:
             self.cfg.key_bits = key_bits  # main layout: 3 or 2
         ptr = C.c_void_p()
@@ -234,7 +234,7 @@ class Context:
         return n.value
 
     def get_tables(self):
-        k = 1 << (self.cfg.key_bits - 1) if self.layout == TQ_LAYOUT_MAIN else 8
+        k = 1 << (self.cfg.key_bits - 1 if self.layout == TQ_LAYOUT_MAIN else self.cfg.value_bits)
         d = self.head_dim
         c = np.zeros(k, np.float32)
         b = np.zeros(k - 1, np.float32)

@@ -52,6 +52,7 @@ struct DecArgs {
   const float* signs;
   const float* sketch_t;
   int kb;  // main layout key bits (3 or 2)
+  int avb;  // alternate layout value index bits (2, 3 or 4)
   CodeTables tab;
   uint32_t* err;
 };
@@ -406,13 +407,14 @@ __global__ void __launch_bounds__(128) decode_main_kernel(DecArgs a) {
 // ------------------------------------------------------------------ alternate layout
 template <int D, int NR>
 __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
-  constexpr int TILE = 24 * D + 32;
+  // page: 18 D + 2 vb D + 32 bytes for vb-bit value indices; the staging buffer fits vb = 4
+  constexpr int TILE_MAX = 26 * D + 32;
   constexpr int G = D / 32;
   constexpr int DPT = (D + 127) / 128;
   constexpr int E = D / 32;
   __shared__ float qf[NR][D];
   __shared__ float qsum[NR][G];
-  __shared__ __align__(16) uint8_t tile[TILE];
+  __shared__ __align__(16) uint8_t tile[TILE_MAX];
   __shared__ float sc[NR][16];
   __shared__ float pbuf[16][NR];
   __shared__ float ob[NR][D];
@@ -463,9 +465,11 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
   }
 
   const float scale = rsqrtf((float)D) * kLog2e;
+  const int vb = a.avb, TILE = 18 * D + 2 * vb * D + 32;
+  const uint32_t vmask = (1u << vb) - 1u;
   const __half* ksm = reinterpret_cast<const __half*>(tile + 16 * D);
   const uint32_t* vi = reinterpret_cast<const uint32_t*>(tile + 18 * D);
-  const __half* vn = reinterpret_cast<const __half*>(tile + 24 * D);
+  const __half* vn = reinterpret_cast<const __half*>(tile + 18 * D + 2 * vb * D);
 
   for (int t0 = tbeg; t0 < tend; t0 += kPage) {
     const int page = t0 >> 4;
@@ -539,15 +543,15 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
       if (i < D) {
 #pragma unroll
         for (int h = 0; h < NR; ++h) o[r][h] *= st.alpha[h];
-        const int bit = 3 * i;
+        const int bit = vb * i;  // index i of each token's little-endian vb-bit stream
         for (int tk = 0; tk < 16; ++tk) {
-          const uint32_t* row = vi + tk * (3 * D / 32);
+          const uint32_t* row = vi + tk * (vb * D / 32);
           uint32_t v = row[bit >> 5] >> (bit & 31);
-          if ((bit & 31) > 29) v |= row[(bit >> 5) + 1] << (32 - (bit & 31));
-          const int idx = v & 7u;
+          if ((bit & 31) + vb > 32) v |= row[(bit >> 5) + 1] << (32 - (bit & 31));
+          const int idx = v & vmask;
           float cv = a.tab.c[0];
 #pragma unroll
-          for (int j = 1; j < 8; ++j) cv = idx == j ? a.tab.c[j] : cv;
+          for (int j = 1; j < 16; ++j) cv = idx == j ? a.tab.c[j] : cv;
 #pragma unroll
           for (int h = 0; h < NR; ++h) o[r][h] = fmaf(pbuf[tk][h], cv, o[r][h]);
         }
@@ -722,6 +726,7 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
   a.sketch_t = ctx->d_sketch_t;
   a.tab = ctx->tab;
   a.kb = ctx->cfg.key_bits;
+  a.avb = ctx->cfg.value_bits;
   a.err = ctx->d_err;
   const int d = ctx->cfg.head_dim;
   const bool main = ctx->cfg.layout == TQ_LAYOUT_MAIN;

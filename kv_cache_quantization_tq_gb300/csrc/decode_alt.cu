@@ -1,8 +1,8 @@
 // Alternate-layout decode attention, one warp per page (CUDA cores).
 //
 // Keys are 8-bit affine codes per block of 32 (no rotation), values are
-// 3-bit Lloyd-Max indices of the rotated unit value with an fp16 norm
-// (vllm-metal TurboQuant guide, quantisation table).  With one query head per
+// VB-bit (2, 3 or 4) Lloyd-Max indices of the rotated unit value with an fp16
+// norm (vllm-metal TurboQuant guide, quantisation table: q2_0 .. q4_0 values).  With one query head per
 // KV head the work per byte is small, so the kernel is written to stream the
 // pages: each warp walks its own pages through a cp.async pipeline, lane l
 // owns the E = d/32 consecutive dimensions [l E, l E + E):
@@ -73,10 +73,10 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint4& a, uint32_t 
       : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
-template <int D>
+template <int D, int VB>
 struct AltCfg {
   static constexpr int E = D / 32;      // dimensions per lane
-  static constexpr int TILE = 24 * D + 32;
+  static constexpr int TILE = 18 * D + 2 * VB * D + 32;  // VB-bit value indices
   static constexpr int STAGES = TILE <= 3200 ? 4 : (TILE <= 6400 ? 3 : 2);
   static constexpr size_t SMEM = (size_t)kWarps * STAGES * TILE;
 };
@@ -99,13 +99,14 @@ __device__ __forceinline__ int kq_swizzle(int row) {
   return D == 64 ? ((row >> 1) & 3) : (row & 7);
 }
 
-template <int D, int NR>
+template <int D, int NR, int VB>
 __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
-  using C = AltCfg<D>;
+  using C = AltCfg<D, VB>;
+  constexpr int NC = 1 << VB;  // centroids
   constexpr int E = C::E;
   constexpr int G = D / 32;
   extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ float lut[8];
+  __shared__ float lut[NC];
   __shared__ float wm[kWarps][NR], wl[kWarps][NR];
   __shared__ float wo[kWarps][NR][D];
   __shared__ int sblk[kWarps][C::STAGES];
@@ -123,10 +124,10 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
   const int tbeg = part * a.chunk_tokens;
   const int tend = min(nc, tbeg + a.chunk_tokens);
   if (tbeg >= tend) return;
-  if (tid < 8) {
+  if (tid < NC) {
     float c = a.tab.c[0];
 #pragma unroll
-    for (int j = 1; j < 8; ++j) c = tid == j ? a.tab.c[j] : c;
+    for (int j = 1; j < NC; ++j) c = tid == j ? a.tab.c[j] : c;
     lut[tid] = c;
   }
 
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
     const uint8_t* T = wst + (k % C::STAGES) * C::TILE;
     const __half2* ksm2 = reinterpret_cast<const __half2*>(T + 16 * D);
     const uint32_t* vi = reinterpret_cast<const uint32_t*>(T + 18 * D);
-    const __half* vn = reinterpret_cast<const __half*>(T + 24 * D);
+    const __half* vn = reinterpret_cast<const __half*>(T + 18 * D + 2 * VB * D);
     // C[token][column] = sum over the column's block of (1024 + code) q_head
     float cacc[NT][4];
 #pragma unroll
@@ -285,28 +286,22 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
 #pragma unroll
       for (int e = 0; e < E; ++e) acc[h][e] *= alpha;
       const float w = p * __half2float(vn[lane >> 1]);
-      // v_rot += w_t c[idx_t] for the lane's E dimensions (3E bits at bit 3 E lane of the row)
-      const int bit0 = 3 * E * lane;
+      // v_rot += w_t c[idx_t] for the lane's E dimensions: VB E bits at bit VB E lane of the token's
+      // index stream, read in pieces of up to 8 indices (at most 32 bits, one funnel shift each)
 #pragma unroll
       for (int t = 0; t < 16; ++t) {
         const float wt = __shfl_sync(kFull, w, 2 * t);
-        const uint32_t* row = vi + t * (3 * D / 32);
-        const uint32_t lo = row[bit0 >> 5];
-        const uint32_t hi = ((bit0 & 31) + 3 * E > 32) ? row[(bit0 >> 5) + 1] : 0u;
-        const uint32_t bits = __funnelshift_r(lo, hi, bit0 & 31);
-        if (E <= 8) {
+        const uint32_t* row = vi + t * (VB * D / 32);
 #pragma unroll
-          for (int e = 0; e < E; ++e) acc[h][e] = fmaf(wt, lut[(bits >> (3 * e)) & 7u], acc[h][e]);
-        } else {
-          // 48 bits: second part from the following word pair
-          const int bit1 = bit0 + 24;
-          const uint32_t lo2 = row[bit1 >> 5];
-          const uint32_t hi2 = ((bit1 & 31) + 24 > 32) ? row[(bit1 >> 5) + 1] : 0u;
-          const uint32_t bits2 = __funnelshift_r(lo2, hi2, bit1 & 31);
+        for (int c0 = 0; c0 < E; c0 += 8) {
+          constexpr int PIECE = E < 8 ? E : 8;
+          const int bitc = VB * (E * lane + c0);
+          const uint32_t lo = row[bitc >> 5];
+          const uint32_t hi = ((bitc & 31) + VB * PIECE > 32) ? row[(bitc >> 5) + 1] : 0u;
+          const uint32_t bits = __funnelshift_r(lo, hi, bitc & 31);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(wt, lut[(bits >> (3 * e)) & 7u], acc[h][e]);
-#pragma unroll
-          for (int e = 8; e < E; ++e) acc[h][e] = fmaf(wt, lut[(bits2 >> (3 * (e - 8))) & 7u], acc[h][e]);
+          for (int e = 0; e < PIECE; ++e)
+            acc[h][c0 + e] = fmaf(wt, lut[(bits >> (VB * e)) & (NC - 1)], acc[h][c0 + e]);
         }
       }
     }
@@ -359,14 +354,21 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
   }
 }
 
-template <int D, int NR>
-cudaError_t launch_alt(const AltArgs& a, dim3 grid, cudaStream_t s) {
-  auto kern = decode_alt_v2_kernel<D, NR>;
-  constexpr size_t SMEM = AltCfg<D>::SMEM;
+template <int D, int NR, int VB>
+cudaError_t launch_alt_vb(const AltArgs& a, dim3 grid, cudaStream_t s) {
+  auto kern = decode_alt_v2_kernel<D, NR, VB>;
+  constexpr size_t SMEM = AltCfg<D, VB>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, 128, SMEM, s>>>(a);
   return cudaGetLastError();
+}
+
+template <int D, int NR>
+cudaError_t launch_alt(const AltArgs& a, int vb, dim3 grid, cudaStream_t s) {
+  return vb == 2 ? launch_alt_vb<D, NR, 2>(a, grid, s)
+       : vb == 4 ? launch_alt_vb<D, NR, 4>(a, grid, s)
+                 : launch_alt_vb<D, NR, 3>(a, grid, s);
 }
 
 }  // namespace
@@ -397,23 +399,23 @@ cudaError_t launch_decode_alt_v2(tq_ctx* ctx, const void* q, const void* pool, i
   a.tab = ctx->tab;
   a.err = ctx->d_err;
   dim3 grid(n_chunks, a.hkv * a.groups, batch);
-  const int d = ctx->cfg.head_dim, nr = a.nrg;
+  const int d = ctx->cfg.head_dim, nr = a.nrg, vb = ctx->cfg.value_bits;
   if (nr == 1) {
     switch (d) {
-      case 64: return launch_alt<64, 1>(a, grid, s);
-      case 128: return launch_alt<128, 1>(a, grid, s);
-      case 256: return launch_alt<256, 1>(a, grid, s);
-      case 512: return launch_alt<512, 1>(a, grid, s);
+      case 64: return launch_alt<64, 1>(a, vb, grid, s);
+      case 128: return launch_alt<128, 1>(a, vb, grid, s);
+      case 256: return launch_alt<256, 1>(a, vb, grid, s);
+      case 512: return launch_alt<512, 1>(a, vb, grid, s);
     }
   } else if (nr == 2) {
     switch (d) {
-      case 64: return launch_alt<64, 2>(a, grid, s);
-      case 128: return launch_alt<128, 2>(a, grid, s);
-      case 256: return launch_alt<256, 2>(a, grid, s);
+      case 64: return launch_alt<64, 2>(a, vb, grid, s);
+      case 128: return launch_alt<128, 2>(a, vb, grid, s);
+      case 256: return launch_alt<256, 2>(a, vb, grid, s);
     }
   } else if (nr <= 4) {
-    if (d == 64) return launch_alt<64, 4>(a, grid, s);
-    if (d == 128) return launch_alt<128, 4>(a, grid, s);
+    if (d == 64) return launch_alt<64, 4>(a, vb, grid, s);
+    if (d == 128) return launch_alt<128, 4>(a, vb, grid, s);
   }
   return cudaErrorNotSupported;
 }

@@ -41,6 +41,7 @@ struct DqArgs {
   const float* signs;
   const uint4* sfrag;   // S as mma.sync B fragments (back-projection order), fp16 high / low
   int kb;               // main layout key bits (3 or 2)
+  int avb;              // alternate layout value index bits (2, 3 or 4)
   CodeTables tab;
   float qjl_coef;       // sqrt(pi/2) / m
   uint32_t* err;
@@ -233,13 +234,14 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
 }
 
 // ------------------------------------------------------------------ alternate layout
+// Alternate-layout page: 18 d + 2 vb d + 32 bytes for vb-bit value indices (staging sized for vb 4).
 template <int D>
 struct AltDq {
   static constexpr int E = D / 32;
   static constexpr int TB = 32;
-  static constexpr int TILE = 24 * D + 32;
+  static constexpr int TILE_MAX = 26 * D + 32;
   static constexpr int THREADS = 256;
-  static constexpr size_t SMEM = (size_t)(TB / 16) * TILE;
+  static constexpr size_t SMEM = (size_t)(TB / 16) * TILE_MAX;
 };
 
 template <int D>
@@ -248,12 +250,16 @@ __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
   constexpr int E = C::E;
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ bool ok[C::TB / 16];
+  __shared__ float lut[16];
   const int b = blockIdx.z, h = blockIdx.y;
   const int tok0 = blockIdx.x * C::TB;
   const int n = dq_ntok(a, b);
   if (tok0 >= n) return;
   const int ntok = min(C::TB, n - tok0);
-  load_tiles(a, smem, C::TILE, C::TILE, b, h, tok0 >> 4, ntok >> 4, ok);
+  const int vb = a.avb, tile_bytes = 18 * D + 2 * vb * D + 32;
+  const uint32_t mask = (1u << vb) - 1u;
+  if (threadIdx.x < 16) lut[threadIdx.x] = a.tab.c[threadIdx.x & mask];
+  load_tiles(a, smem, tile_bytes, tile_bytes, b, h, tok0 >> 4, ntok >> 4, ok);  // ends with __syncthreads
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float rs = rsqrtf((float)D);
   float sg[E];
@@ -261,25 +267,21 @@ __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
   for (int e = 0; e < E; ++e) sg[e] = a.signs[coord_of(e, lane)];
   for (int tt = warp; tt < ntok; tt += C::THREADS / 32) {
     if (!ok[tt >> 4]) continue;
-    const uint8_t* tile = smem + (size_t)(tt >> 4) * C::TILE;
+    const uint8_t* tile = smem + (size_t)(tt >> 4) * tile_bytes;
     const int slot = tt & 15;
     const size_t row = (((size_t)b * a.hkv + h) * a.max_tokens + tok0 + tt) * D;
-    const uint32_t* vi = reinterpret_cast<const uint32_t*>(tile + 18 * D + slot * (3 * D / 8));
-    const float nv = __half2float(reinterpret_cast<const __half*>(tile + 24 * D)[slot]);
+    const uint32_t* vi = reinterpret_cast<const uint32_t*>(tile + 18 * D + slot * (vb * D / 8));
+    const float nv = __half2float(reinterpret_cast<const __half*>(tile + 18 * D + 2 * vb * D)[slot]);
     float x[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int c = coord_of(e, lane);
       const __half2 smn = *reinterpret_cast<const __half2*>(tile + 16 * D + (slot * (D / 32) + e) * 4);
       a.k_out[row + c] = __float2half_rn(fmaf(__low2float(smn), (float)tile[slot * D + c], __high2float(smn)));
-      const int bit = 3 * c;
+      const int bit = vb * c;  // index c of the token's little-endian vb-bit stream
       const uint32_t lo = vi[bit >> 5];
-      const uint32_t hi = (bit & 31) > 29 ? vi[(bit >> 5) + 1] : 0u;
-      const int idx = (int)(__funnelshift_r(lo, hi, bit & 31) & 7u);
-      float cv = a.tab.c[0];
-#pragma unroll
-      for (int j = 1; j < 8; ++j) cv = idx == j ? a.tab.c[j] : cv;
-      x[e] = cv;
+      const uint32_t hi = (bit & 31) + vb > 32 ? vi[(bit >> 5) + 1] : 0u;
+      x[e] = lut[__funnelshift_r(lo, hi, bit & 31) & mask];
     }
     wht_warp<E>(x, lane);
 #pragma unroll
@@ -340,6 +342,7 @@ cudaError_t launch_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, con
   a.signs = ctx->d_signs;
   a.sfrag = ctx->d_sfrag;
   a.kb = ctx->cfg.key_bits;
+  a.avb = ctx->cfg.value_bits;
   a.tab = ctx->tab;
   a.qjl_coef = (float)(1.2533141373155003 / (double)ctx->cfg.qjl_m);
   a.err = ctx->d_err;

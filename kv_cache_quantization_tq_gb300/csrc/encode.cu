@@ -39,6 +39,7 @@ struct EncArgs {
   const float* signs;
   const uint4* sfrag;     // S^T as mma.sync B fragments (k = coordinate, n = sketch row), hi / lo
   int kb;                 // main layout: key bits, 3 (2-bit Lloyd-Max index) or 2 (1-bit index)
+  int avb;                // alternate layout: value index bits, 2, 3 or 4
   CodeTables tab;
   uint32_t* err;
 };
@@ -300,20 +301,47 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
 }
 
 // ------------------------------------------------------------------ alternate layout
+// Alternate-layout page: 16 x d 8-bit key codes, 16 x d/32 (scale, minimum) fp16 pairs, a dense
+// vb-bit stream of value indices per token (index i at bit vb i), 16 fp16 value norms:
+// 18 d + 2 vb d + 32 bytes.  Shared memory is sized for the largest (vb = 4).
+__host__ __device__ constexpr int alt_tile_bytes(int d, int vb) { return 18 * d + 2 * vb * d + 32; }
 template <int D>
 struct AltEnc {
   static constexpr int E = D / 32;
   static constexpr int TB = 32;
-  static constexpr int TILE = 24 * D + 32;
+  static constexpr int TILE_MAX = alt_tile_bytes(D, 4);
   static constexpr int THREADS = 256;
-  static constexpr size_t SMEM_TILES = (size_t)(TB / 16) * TILE;
+  static constexpr size_t SMEM_TILES = (size_t)(TB / 16) * TILE_MAX;
   static constexpr size_t SMEM = SMEM_TILES + (size_t)TB * D;
 };
+
+// Index kk of a chunk of 32 at bit VB kk of the chunk's VB words (a little-endian bit stream).
+template <int D, int VB>
+__device__ __forceinline__ void pack_value_stream(const uint8_t* vcodes, uint8_t* tiles, int tile_bytes, int ntok) {
+  for (int w = threadIdx.x; w < ntok * (D / 32); w += AltEnc<D>::THREADS) {
+    const int tt = w / (D / 32), chunk = w % (D / 32);
+    uint32_t o[VB];
+#pragma unroll
+    for (int i = 0; i < VB; ++i) o[i] = 0u;
+#pragma unroll
+    for (int kk = 0; kk < 32; ++kk) {
+      const uint32_t code = vcodes[tt * D + chunk * 32 + kk];
+      const int bit = VB * kk;
+      o[bit >> 5] |= code << (bit & 31);
+      if ((bit & 31) + VB > 32) o[(bit >> 5) + 1] |= code >> (32 - (bit & 31));
+    }
+    uint32_t* dst = reinterpret_cast<uint32_t*>(tiles + (size_t)(tt >> 4) * tile_bytes + 18 * D +
+                                                (tt & 15) * (VB * D / 8) + chunk * 4 * VB);
+#pragma unroll
+    for (int i = 0; i < VB; ++i) dst[i] = o[i];
+  }
+}
 
 template <int D>
 __device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int ntok, int start, uint8_t* smem) {
   using C = AltEnc<D>;
   constexpr int E = C::E;
+  const int vb = a.avb, tile_bytes = alt_tile_bytes(D, vb), nbound = (1 << vb) - 1;
   uint8_t* tiles = smem;
   uint8_t* vcodes = smem + C::SMEM_TILES;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -326,7 +354,7 @@ __device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int n
   for (int tt = warp; tt < ntok; tt += C::THREADS / 32) {
     const __half* kp = a.k + (base + tok0 + tt) * D;
     const __half* vp = a.v + (base + tok0 + tt) * D;
-    uint8_t* tile = tiles + (size_t)(tt >> 4) * C::TILE;
+    uint8_t* tile = tiles + (size_t)(tt >> 4) * tile_bytes;
     const int slot = tt & 15;
     float vv[E], kx[E], kmn[E], kmx[E];
 #pragma unroll
@@ -360,31 +388,21 @@ __device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int n
       const float y = vv[e] * inv;
       int idx = 0;
 #pragma unroll
-      for (int j = 0; j < 7; ++j) idx += (y >= a.tab.b[j]);
+      for (int j = 0; j < 15; ++j) idx += (j < nbound && y >= a.tab.b[j]);
       vcodes[tt * D + coord_of(e, lane)] = (uint8_t)idx;
     }
-    if (lane == 0) reinterpret_cast<__half*>(tile + 24 * D)[slot] = __float2half_rn(nv);
+    if (lane == 0) reinterpret_cast<__half*>(tile + 18 * D + 2 * vb * D)[slot] = __float2half_rn(nv);
   }
   __syncthreads();
-  // dense 3-bit stream per token: 32 indices -> 3 words
-  for (int w = threadIdx.x; w < ntok * (D / 32); w += C::THREADS) {
-    const int tt = w / (D / 32), chunk = w % (D / 32);
-    uint32_t o[3] = {0u, 0u, 0u};
-#pragma unroll
-    for (int kk = 0; kk < 32; ++kk) {
-      const uint32_t code = vcodes[tt * D + chunk * 32 + kk];
-      const int bit = 3 * kk;
-      o[bit >> 5] |= code << (bit & 31);
-      if ((bit & 31) > 29) o[(bit >> 5) + 1] |= code >> (32 - (bit & 31));
-    }
-    uint32_t* dst = reinterpret_cast<uint32_t*>(tiles + (size_t)(tt >> 4) * C::TILE + 18 * D +
-                                                (tt & 15) * (3 * D / 8) + chunk * 12);
-    dst[0] = o[0];
-    dst[1] = o[1];
-    dst[2] = o[2];
-  }
+  // dense vb-bit stream per token: 32 indices -> vb words
+  if (vb == 2)
+    pack_value_stream<D, 2>(vcodes, tiles, tile_bytes, ntok);
+  else if (vb == 4)
+    pack_value_stream<D, 4>(vcodes, tiles, tile_bytes, ntok);
+  else
+    pack_value_stream<D, 3>(vcodes, tiles, tile_bytes, ntok);
   __syncthreads();
-  store_tiles(a, tiles, C::TILE, C::TILE, ntok >> 4, b, h, (start + tok0) >> 4);
+  store_tiles(a, tiles, tile_bytes, tile_bytes, ntok >> 4, b, h, (start + tok0) >> 4);
 }
 
 // ------------------------------------------------------------------ kernels
@@ -493,6 +511,7 @@ EncArgs make_args(tq_ctx* ctx, const void* k, const void* v, int src_tokens, int
   a.signs = ctx->d_signs;
   a.sfrag = ctx->d_sfrag_enc;
   a.kb = ctx->cfg.key_bits;
+  a.avb = ctx->cfg.value_bits;
   a.tab = ctx->tab;
   a.err = ctx->d_err;
   return a;

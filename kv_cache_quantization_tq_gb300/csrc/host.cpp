@@ -134,7 +134,7 @@ tq_status check_config(const tq_config* c) {
         c->qjl_m != c->head_dim)
       return TQ_ERR_UNSUPPORTED;
   } else if (c->layout == TQ_LAYOUT_ALT) {
-    if (c->key_bits != 8 || c->value_bits != 3) return TQ_ERR_UNSUPPORTED;
+    if (c->key_bits != 8 || c->value_bits < 2 || c->value_bits > 4) return TQ_ERR_UNSUPPORTED;
   } else {
     return TQ_ERR_INVALID_ARG;
   }
@@ -327,8 +327,8 @@ tq_status tq_create(const tq_config* cfg, tq_ctx** out) {
   tq_status st = check_config(cfg);
   if (st != TQ_OK) return st;
   const int d = cfg->head_dim;
-  // main: key_bits - 1 Lloyd-Max bits (one key bit is the QJL sign); alternate: 3-bit values
-  const int bits = cfg->layout == TQ_LAYOUT_MAIN ? cfg->key_bits - 1 : 3;
+  // main: key_bits - 1 Lloyd-Max bits (one key bit is the QJL sign); alternate: value_bits
+  const int bits = cfg->layout == TQ_LAYOUT_MAIN ? cfg->key_bits - 1 : cfg->value_bits;
   std::vector<double> c64(1 << bits);
   lloyd_max(d, bits, c64.data(), nullptr);
   std::vector<float> cent(c64.begin(), c64.end());
@@ -344,7 +344,7 @@ tq_status tq_create_with_tables(const tq_config* cfg, const float* centroids, co
   tq_status st = check_config(cfg);
   if (st != TQ_OK) return st;
   const int d = cfg->head_dim;
-  const int k = cfg->layout == TQ_LAYOUT_MAIN ? 1 << (cfg->key_bits - 1) : 8;
+  const int k = 1 << (cfg->layout == TQ_LAYOUT_MAIN ? cfg->key_bits - 1 : cfg->value_bits);
   if (cfg->layout == TQ_LAYOUT_MAIN && !sketch) return TQ_ERR_INVALID_ARG;
   for (int j = 0; j < k; ++j) {
     if (!(centroids[j] == -centroids[k - 1 - j])) return TQ_ERR_INVALID_ARG;
@@ -386,10 +386,12 @@ size_t tq_bytes_per_token_head(const tq_ctx* ctx) {
   if (!ctx) return 0;
   const size_t d = ctx->cfg.head_dim;
   // main: key_bits key bits, value_bits value bits and one fp16 scale + minimum per group of 32 per
-  // coordinate, two fp16 norms; alternate: 8-bit keys + 4 B per block of 32, 3-bit values, fp16 norm
+  // coordinate, two fp16 norms; alternate: 8-bit keys + 4 B per block of 32, value_bits-bit
+  // value indices, fp16 norm
   const size_t vb = ctx->cfg.value_bits;
   const size_t kb = ctx->cfg.key_bits;
-  return ctx->cfg.layout == TQ_LAYOUT_MAIN ? (kb * d) / 8 + (vb * d) / 8 + d / 8 + 4 : (3 * d) / 2 + 2;
+  return ctx->cfg.layout == TQ_LAYOUT_MAIN ? (kb * d) / 8 + (vb * d) / 8 + d / 8 + 4
+                                           : d + (d / 32) * 4 + (vb * d) / 8 + 2;
 }
 
 size_t tq_page_bytes(const tq_ctx* ctx) { return tq::kPage * tq_bytes_per_token_head(ctx); }

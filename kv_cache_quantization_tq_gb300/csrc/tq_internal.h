@@ -24,8 +24,8 @@ constexpr int kTcQueryU4 = 5 * 8 * 32 + 4 * 2 * kMaxRep / 4;
 
 // Small per-context tables passed by value as kernel parameters.
 struct CodeTables {
-  float c[8];   // centroids, ascending (4 used by main keys, 8 by alt values)
-  float b[8];   // decision boundaries (midpoints), K-1 used
+  float c[16];  // centroids, ascending (2..8 used by main keys, 4..16 by alt values)
+  float b[16];  // decision boundaries (midpoints), K-1 used
 };
 
 struct ProfileKind {

@@ -13,8 +13,8 @@ from oracle import cache, codebook, layout, quant, rng
 MARGIN = 1e-5  # oracle values this close to a decision boundary may legitimately differ
 
 
-def oracle_tables(seed, d, layout_main=True, key_bits=3):
-    bits = key_bits - 1 if layout_main else 3
+def oracle_tables(seed, d, layout_main=True, key_bits=3, value_bits=3):
+    bits = key_bits - 1 if layout_main else value_bits
     c, _ = codebook.lloyd_max(d, bits)
     c32 = c.astype(np.float32)
     signs = rng.signs(seed, d).astype(np.float32)
@@ -23,7 +23,7 @@ def oracle_tables(seed, d, layout_main=True, key_bits=3):
 
 
 def make_ctx(tq, layout_main, d, hq, hkv, seed, value_bits=None, key_bits=None):
-    c32, signs, sketch = oracle_tables(seed, d, layout_main, key_bits or 3)
+    c32, signs, sketch = oracle_tables(seed, d, layout_main, key_bits or 3, value_bits or 3)
     lay = tq.TQ_LAYOUT_MAIN if layout_main else tq.TQ_LAYOUT_ALT
     ctx = tq.Context(lay, d, hq, hkv, seed, centroids=c32, signs=signs, sketch=sketch, value_bits=value_bits,
                      key_bits=key_bits)
@@ -71,15 +71,18 @@ def main_fields(tiles, d, kb=None):
 
 
 def alt_fields(tiles, d):
+    """Fields of alternate-layout tiles (value bits vb from the size 18d + 2 vb d + 32)."""
     t = np.ascontiguousarray(tiles)
     lead = t.shape[:-1]
-    vi = t[..., 18 * d:24 * d].reshape(lead + (16, 3 * d // 8))
-    bits = np.unpackbits(vi, axis=-1, bitorder="little").reshape(lead + (16, d, 3)).astype(np.uint8)
-    idx = bits[..., 0] + 2 * bits[..., 1] + 4 * bits[..., 2]
+    vb = (t.shape[-1] - 18 * d - 32) // (2 * d)
+    o_n = 18 * d + 2 * vb * d
+    vi = t[..., 18 * d:o_n].reshape(lead + (16, vb * d // 8))
+    bits = np.unpackbits(vi, axis=-1, bitorder="little").reshape(lead + (16, d, vb)).astype(np.uint8)
+    idx = sum(bits[..., i].astype(np.int32) << i for i in range(vb)).astype(np.uint8)
     return {
         "k_bytes": t[..., :18 * d],
         "vidx": idx,
-        "vn": np.ascontiguousarray(t[..., 24 * d:24 * d + 32]).view("<i2"),
+        "vn": np.ascontiguousarray(t[..., o_n:o_n + 32]).view("<i2"),
     }
 
 
@@ -132,7 +135,7 @@ def build_alt_cache(seed, d, hkv, lengths, centroids3, signs, shuffled=True):
     k, v = synth.kv_alt(seed, bsz, hkv, t_all, d)
     max_blocks = t_all // 16
     bt = synth.block_table(seed, bsz, max_blocks, shuffled)
-    pool = np.zeros((bsz * max_blocks, hkv, layout.alt_tile_bytes(d)), np.uint8)
+    pool = np.zeros((bsz * max_blocks, hkv, layout.alt_tile_bytes(d, cache.value_bits_of(centroids3))), np.uint8)
     n_c = np.array(lengths, np.int32)
     for b, L in enumerate(lengths):
         cache.encode_alt_range(pool, bt[b:b + 1], 0, k[b:b + 1, :, :L], v[b:b + 1, :, :L], signs, centroids3)

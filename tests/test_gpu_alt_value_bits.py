@@ -1,0 +1,104 @@
+"""Alternate layout with 2- or 4-bit value indices on the GPU (vllm-metal TurboQuant guide,
+quantisation table: q2_0 / q4_0 values; 8-bit keys with 4-bit values is its K8+V4 mix).
+
+The same parity bar as the 3-bit default: key bytes bit-exact against the oracle's encoder, value
+indices equal away from decision boundaries, value norms within one fp16 ulp, decode within
+2e-3 + 1e-3 |ref| (the tensor-core warp-per-page decoder for 1, 2 or 4 heads per KV head, the
+CUDA-core one for 8), dequantised history against the oracle's materialisation.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_cases import allclose_report, alt_fields, build_alt_cache, make_ctx, near_boundary, tile_index, to_dev
+from oracle import attention, cache, layout
+from test_gpu_dequant import _check_close, _outputs, _untouched
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from kv_cache_quantization_tq_gb300.build import build
+
+    build()
+    import kv_cache_quantization_tq_gb300 as tq
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+@pytest.mark.parametrize("vb", [2, 4])
+@pytest.mark.parametrize("d", [64, 512])
+def test_record_size(d, vb):
+    ctx, c, *_ = make_ctx(tq, False, d, 2, 2, 0, value_bits=vb)
+    assert len(c) == 1 << vb
+    assert ctx.bytes_per_token_head == d + 4 * (d // 32) + vb * d // 8 + 2
+    assert ctx.page_bytes == layout.alt_tile_bytes(d, vb)
+
+
+@pytest.mark.parametrize("vb", [2, 4])
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+def test_encode_parity(d, vb):
+    hkv, n_tok, starts, seed = 2, 96, [0, 32], 60 + d + vb
+    ctx, c, s, _ = make_ctx(tq, False, d, hkv, hkv, seed, value_bits=vb)
+    k, v = synth.kv_alt(seed, 2, hkv, n_tok, d)
+    v[1, 1, 7] = 0  # zero value vector
+    max_blocks = 10
+    bt = synth.block_table(seed, 2, max_blocks, True)
+    pool_o = np.zeros((2 * max_blocks, hkv, layout.alt_tile_bytes(d, vb)), np.uint8)
+    encs = [cache.encode_alt_range(pool_o, bt[b:b + 1], starts[b], k[b:b + 1], v[b:b + 1], s, c) for b in range(2)]
+    pool_g = torch.zeros(pool_o.shape, dtype=torch.uint8, device="cuda")
+    ctx.encode_flush(to_dev(k), to_dev(v), to_dev(np.array(starts, np.int32)), to_dev(bt), pool_g)
+    pool_g = pool_g.cpu().numpy()
+    assert ctx.device_errors() == 0
+    blocks = tile_index(bt, starts, n_tok)
+    fo = alt_fields(pool_o[blocks], d)
+    fg = alt_fields(pool_g[blocks], d)
+    assert np.array_equal(fg["k_bytes"], fo["k_bytes"])  # affine int8 keys: bit-exact
+    assert np.max(np.abs(fg["vn"].astype(np.int32) - fo["vn"].astype(np.int32))) <= 1
+    y = np.stack([e["y"][0] for e in encs]).reshape(2, hkv, n_tok // 16, 16, d).transpose(0, 2, 1, 3, 4)
+    near = near_boundary(y, c)
+    assert not ((fg["vidx"] != fo["vidx"]) & ~near).any()
+    assert fg["vidx"].max() == (1 << vb) - 1  # every level reachable: the stream width is used
+
+
+@pytest.mark.parametrize("vb", [2, 4])
+@pytest.mark.parametrize("d,n_rep", [(64, 1), (128, 2), (128, 4), (256, 1), (512, 1), (128, 8)])
+def test_decode_parity(d, n_rep, vb):
+    seed, hkv = 70 + d + n_rep + vb, 2
+    hq = hkv * n_rep
+    ctx, c, s, _ = make_ctx(tq, False, d, hq, hkv, seed, value_bits=vb)
+    e = build_alt_cache(seed, d, hkv, [544, 96], c, s)
+    q = synth.queries(seed, 2, hq, d)
+    out = torch.empty((2, hq, d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(ctx.workspace_size(2, e["max_ctx"]), dtype=torch.uint8, device="cuda")
+    ctx.decode_attention(to_dev(q), to_dev(e["pool"]), to_dev(e["bt"]), to_dev(e["n_c"]), None, None, None,
+                         e["max_ctx"], out, ws)
+    got = out.cpu().numpy()
+    assert ctx.device_errors() == 0
+    ref = attention.decode_alt(q, e["pool"], e["bt"], e["n_c"], None, None, None, s, c, hkv)
+    ok, maxerr, nbad = allclose_report(got, ref)
+    assert ok, f"max abs err {maxerr}, {nbad} bad"
+
+
+@pytest.mark.parametrize("vb", [2, 4])
+@pytest.mark.parametrize("d", [64, 256])
+def test_dense_history(d, vb):
+    seed, hkv = 80 + d + vb, 2
+    ctx, c, s, _ = make_ctx(tq, False, d, hkv, hkv, seed, value_bits=vb)
+    lengths = [320, 48]
+    e = build_alt_cache(seed, d, hkv, lengths, c, s)
+    max_tokens = 336
+    k_out, v_out = _outputs(len(lengths), hkv, max_tokens, d)
+    ctx.dequantize(to_dev(e["pool"]), to_dev(e["bt"]), to_dev(e["n_c"]), k_out, v_out)
+    torch.cuda.synchronize()
+    assert ctx.device_errors() == 0
+    kg, vg = k_out.cpu().numpy(), v_out.cpu().numpy()
+    for b, L in enumerate(lengths):
+        kr, vr = cache.materialize_alt(e["pool"], e["bt"], b, L, None, None, 0, s, c, d)
+        _check_close(kg[b, :, :L], kr, f"keys b={b}")
+        _check_close(vg[b, :, :L], vr, f"values b={b}")
+        assert _untouched(k_out, b, L)
