@@ -122,7 +122,7 @@ def decode_alt(q16, pool, block_table, n_c, ring_k, ring_v, n_buf, signs, centro
     for b in range(bsz):
         nc = int(n_c[b])
         nb = int(n_buf[b]) if n_buf is not None else 0
-        f = cache.read_alt(pool, block_table, b, nc, d) if nc else None
+        f = cache.read_alt(pool, block_table, b, nc, d, cache.value_bits_of(centroids3)) if nc else None
         for g in range(n_kv):
             q = q16[b, g * n_rep:(g + 1) * n_rep].astype(np.float64)
             logits = []

@@ -67,11 +67,13 @@ def value_bits_of(centroids) -> int:
 
 def encode_alt_range(pool, block_table, start, k16, v16, signs, centroids3):
     """Alternate layout: encode fp16 k/v [B, Hkv, T, d] into ``pool`` (value bits from the codebook
-    size: 4, 8 or 16 centroids)."""
+    size: 4, 8 or 16 centroids; key bits from the pool's tile size: 8 or 4)."""
     k16 = np.asarray(k16, dtype=np.float16)
     bsz, hkv, t, d = k16.shape
     assert start % layout.P == 0 and t % layout.P == 0
-    kq, ks, kmn = quant.encode_alt_keys(k16)
+    vb = value_bits_of(centroids3)
+    kb = layout.alt_key_bits(pool.shape[-1], d, vb)
+    kq, ks, kmn = quant.encode_alt_keys(k16, bits=kb)
     venc = quant.encode_alt_values(v16, signs, centroids3)
     npg = t // layout.P
     tiles = layout.pack_alt_tiles(
@@ -80,7 +82,8 @@ def encode_alt_range(pool, block_table, start, k16, v16, signs, centroids3):
         kmn.reshape(bsz, hkv, npg, 16, d // 32),
         venc["idx"].reshape(bsz, hkv, npg, 16, d),
         venc["n_v"].reshape(bsz, hkv, npg, 16),
-        value_bits_of(centroids3),
+        vb,
+        kb,
     )
     pages = start // layout.P + np.arange(npg)
     blocks = np.asarray(block_table)[:, pages]
@@ -107,10 +110,10 @@ def read_main(pool, block_table, b, n_c, d, kbits=None):
     return out
 
 
-def read_alt(pool, block_table, b, n_c, d):
+def read_alt(pool, block_table, b, n_c, d, vbits=None):
     npg = n_c // layout.P
     tiles = pool[np.asarray(block_table)[b, :npg]]
-    f = layout.unpack_alt_tiles(tiles, d)
+    f = layout.unpack_alt_tiles(tiles, d, vbits)
     out = {}
     for key, val in f.items():
         val = np.moveaxis(val, 1, 0)
@@ -144,7 +147,7 @@ def materialize_main(pool, block_table, b, n_c, ring_k, ring_v, n_buf, signs, ce
 
 def materialize_alt(pool, block_table, b, n_c, ring_k, ring_v, n_buf, signs, centroids3, d):
     """Dense history of sequence b as float64 (k, v) [Hkv, n_c + n_buf, d] (alternate layout)."""
-    f = read_alt(pool, block_table, b, n_c, d) if n_c else None
+    f = read_alt(pool, block_table, b, n_c, d, value_bits_of(centroids3)) if n_c else None
     hkv = pool.shape[1]
     ks, vs = [], []
     for g in range(hkv):

@@ -242,47 +242,63 @@ def unpack_main_tiles(tiles: np.ndarray, d: int, kbits: int = None) -> dict:
 
 
 # ---------------------------------------------------------------- alternate layout
-def alt_tile_bytes(d: int, vbits: int = 3) -> int:
-    """One page of the alternate layout: 16 x (d 8-bit key codes + d/32 fp16 (scale, minimum)
-    pairs + a dense vbits-bit stream of value indices + one fp16 value norm)."""
-    return 18 * d + 2 * vbits * d + 32
+def alt_tile_bytes(d: int, vbits: int = 3, kbits: int = 8) -> int:
+    """One page of the alternate layout: 16 x (a dense kbits-bit stream of key codes (bytes for 8
+    bits) + d/32 fp16 (scale, minimum) pairs + a dense vbits-bit stream of value indices + one fp16
+    value norm)."""
+    return 2 * kbits * d + 2 * d + 2 * vbits * d + 32
 
 
-def alt_bytes_per_token_head(d: int, vbits: int = 3) -> float:
-    return alt_tile_bytes(d, vbits) / P
+def alt_bytes_per_token_head(d: int, vbits: int = 3, kbits: int = 8) -> float:
+    return alt_tile_bytes(d, vbits, kbits) / P
 
 
-def alt_value_bits(tile_bytes: int, d: int) -> int:
-    """Value bits of an alternate-layout tile from its size (the size is 18d + 2 vbits d + 32)."""
-    vb, rem = divmod(tile_bytes - 18 * d - 32, 2 * d)
-    assert rem == 0 and vb in (2, 3, 4), (tile_bytes, d)
+def alt_value_bits(tile_bytes: int, d: int, kbits: int = 8) -> int:
+    """Value bits of an alternate-layout tile from its size and key bits."""
+    vb, rem = divmod(tile_bytes - (2 * kbits + 2) * d - 32, 2 * d)
+    assert rem == 0 and vb in (2, 3, 4), (tile_bytes, d, kbits)
     return vb
 
 
-def pack_alt_tiles(kq, ks16, kmn16, vidx, nv16, vbits: int = 3) -> np.ndarray:
-    """kq [..., 16, d] uint8; ks16/kmn16 [..., 16, d/32]; vidx [..., 16, d] (vbits-bit); nv16 [..., 16]."""
+def alt_key_bits(tile_bytes: int, d: int, vbits: int) -> int:
+    """Key bits of an alternate-layout tile from its size and value bits."""
+    kb, rem = divmod(tile_bytes - (2 + 2 * vbits) * d - 32, 2 * d)
+    assert rem == 0 and kb in (4, 8), (tile_bytes, d, vbits)
+    return kb
+
+
+def pack_alt_tiles(kq, ks16, kmn16, vidx, nv16, vbits: int = 3, kbits: int = 8) -> np.ndarray:
+    """kq [..., 16, d] (kbits-bit codes); ks16/kmn16 [..., 16, d/32]; vidx [..., 16, d] (vbits-bit);
+    nv16 [..., 16]."""
     kq = np.asarray(kq, dtype=np.uint8)
     d = kq.shape[-1]
     lead = kq.shape[:-2]
-    kqb = kq.reshape(lead + (16 * d,))
+    kqb = pack_rows(kq, kbits).reshape(lead + (16 * kbits * d // 8,))
     sm = np.stack([np.asarray(ks16, np.float16), np.asarray(kmn16, np.float16)], axis=-1)
     ksm = _f16_bytes(sm.reshape(lead + (16 * (d // 32) * 2,)))
     vi = pack_rows(vidx, vbits).reshape(lead + (16 * vbits * d // 8,))
     vn = _f16_bytes(nv16)
     out = np.concatenate([kqb, ksm, vi, vn], axis=-1)
-    assert out.shape[-1] == alt_tile_bytes(d, vbits)
+    assert out.shape[-1] == alt_tile_bytes(d, vbits, kbits)
     return out
 
 
-def unpack_alt_tiles(tiles: np.ndarray, d: int) -> dict:
+def unpack_alt_tiles(tiles: np.ndarray, d: int, vbits: int = None) -> dict:
+    """Fields of alternate-layout tiles.  Without vbits the keys are taken as 8-bit and the value
+    bits are read off the size; with vbits (the codebook's) the key bits are read off the size."""
     t = np.asarray(tiles, dtype=np.uint8)
     lead = t.shape[:-1]
     g = d // 32
-    vb = alt_value_bits(t.shape[-1], d)
-    o_n = 18 * d + 2 * vb * d
-    kq = t[..., : 16 * d].reshape(lead + (16, d))
-    sm = np.ascontiguousarray(t[..., 16 * d:18 * d]).view("<f2").reshape(lead + (16, g, 2))
-    vi = unpack_rows(t[..., 18 * d:o_n].reshape(lead + (16, vb * d // 8)), d, vb)
+    if vbits is None:
+        kb, vb = 8, alt_value_bits(t.shape[-1], d)
+    else:
+        kb, vb = alt_key_bits(t.shape[-1], d, vbits), vbits
+    o_sm = 2 * kb * d
+    o_vi = o_sm + 2 * d
+    o_n = o_vi + 2 * vb * d
+    kq = unpack_rows(t[..., :o_sm].reshape(lead + (16, kb * d // 8)), d, kb)
+    sm = np.ascontiguousarray(t[..., o_sm:o_vi]).view("<f2").reshape(lead + (16, g, 2))
+    vi = unpack_rows(t[..., o_vi:o_n].reshape(lead + (16, vb * d // 8)), d, vb)
     nv = np.ascontiguousarray(t[..., o_n:o_n + 32]).view("<f2")
     return {
         "kq": kq.copy(),

@@ -143,9 +143,9 @@ def dequant_keys(enc: dict, signs: np.ndarray, centroids: np.ndarray, s_mat: np.
     return enc["n_k"].astype(np.float64)[..., None] * rotation.unrotate(x, signs)
 
 
-def encode_alt_keys(k16: np.ndarray, block: int = 32):
-    """Alternate-layout keys: 8-bit affine codes per block of 32."""
-    return group_quant(k16, block, 255)
+def encode_alt_keys(k16: np.ndarray, block: int = 32, bits: int = 8):
+    """Alternate-layout keys: bits-bit affine codes per block of 32 (2^bits - 1 steps)."""
+    return group_quant(k16, block, (1 << bits) - 1)
 
 
 def encode_alt_values(v16: np.ndarray, signs: np.ndarray, centroids: np.ndarray):

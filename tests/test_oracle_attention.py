@@ -76,18 +76,19 @@ def test_compressed_logits_track_exact_logits():
     assert np.corrcoef(est, exact)[0, 1] > 0.85
 
 
-@pytest.mark.parametrize("vbits", [2, 3, 4])
-def test_alt_layout_decode_matches_torch_sdpa_on_dequantised_cache(vbits):
+@pytest.mark.parametrize("vbits,kbits", [(2, 8), (3, 8), (4, 8), (3, 4)])
+def test_alt_layout_decode_matches_torch_sdpa_on_dequantised_cache(vbits, kbits):
     d, hkv, n_rep = 64, 2, 1
     sg = rng.signs(5, d)
     c3, _ = codebook.lloyd_max(d, vbits)
     k, v = synth.kv_alt(5, 1, hkv, 64, d)
     bt = synth.block_table(5, 1, 4, True)
-    pool = np.zeros((4, hkv, layout.alt_tile_bytes(d, vbits)), np.uint8)
+    pool = np.zeros((4, hkv, layout.alt_tile_bytes(d, vbits, kbits)), np.uint8)
     cache.encode_alt_range(pool, bt, 0, k, v, sg, c3)
     q = synth.queries(5, 1, hkv * n_rep, d)
     out = attention.decode_alt(q, pool, bt, np.array([64]), None, None, None, sg, c3, hkv)
-    kq, ks, kmn = quant.encode_alt_keys(k)
+    kq, ks, kmn = quant.encode_alt_keys(k, bits=kbits)
+    assert kq.max() == (1 << kbits) - 1
     khat = quant.group_dequant(kq, ks, kmn, 32)
     venc = quant.encode_alt_values(v, sg, c3)
     # butterfly pulled out: sum_t p_t * unrotate(x_t) == unrotate(sum_t p_t x_t)

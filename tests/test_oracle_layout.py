@@ -140,26 +140,32 @@ def test_main_tile_round_trip(d):
 
 
 @pytest.mark.parametrize("d", [64, 128, 256, 512])
-@pytest.mark.parametrize("vbits", [2, 3, 4])
-def test_alt_tile_round_trip(d, vbits):
-    g = np.random.default_rng(d + vbits)
+@pytest.mark.parametrize("vbits,kbits", [(2, 8), (3, 8), (4, 8), (3, 4), (4, 4)])
+def test_alt_tile_round_trip(d, vbits, kbits):
+    g = np.random.default_rng(d + vbits + kbits)
     f = {
-        "kq": g.integers(0, 256, (2, 16, d), dtype=np.uint8),
+        "kq": g.integers(0, 1 << kbits, (2, 16, d), dtype=np.uint8),
         "ks": g.standard_normal((2, 16, d // 32)).astype(np.float16),
         "kmn": g.standard_normal((2, 16, d // 32)).astype(np.float16),
         "vidx": g.integers(0, 1 << vbits, (2, 16, d), dtype=np.uint8),
         "n_v": g.standard_normal((2, 16)).astype(np.float16),
     }
-    t = layout.pack_alt_tiles(f["kq"], f["ks"], f["kmn"], f["vidx"], f["n_v"], vbits)
-    assert t.shape == (2, layout.alt_tile_bytes(d, vbits))
-    back = layout.unpack_alt_tiles(t, d)
+    t = layout.pack_alt_tiles(f["kq"], f["ks"], f["kmn"], f["vidx"], f["n_v"], vbits, kbits)
+    assert t.shape == (2, layout.alt_tile_bytes(d, vbits, kbits))
+    back = layout.unpack_alt_tiles(t, d, vbits)
     for k, v in f.items():
         assert np.array_equal(back[k].view(np.uint8), v.view(np.uint8)), k
+    if kbits == 8:
+        assert np.array_equal(layout.unpack_alt_tiles(t, d)["vidx"], f["vidx"])  # sizes alone suffice
+    # key codes: token 3's kbits-bit stream, then the scale/minimum pairs, then the value streams
+    krow = kbits * d // 8
+    assert np.array_equal(t[0, 3 * krow:4 * krow], _pack_bigint(f["kq"][0, 3], kbits))
+    o_vi = 16 * krow + 2 * d
     row_bytes = vbits * d // 8
-    row = t[1, 18 * d + 5 * row_bytes:18 * d + 6 * row_bytes]
+    row = t[1, o_vi + 5 * row_bytes:o_vi + 6 * row_bytes]
     assert np.array_equal(row, _pack_bigint(f["vidx"][1, 5], vbits))
     # the value norms follow the index stream
-    o_n = 18 * d + 16 * row_bytes
+    o_n = o_vi + 16 * row_bytes
     assert np.array_equal(t[0, o_n:o_n + 32].view("<f2"), f["n_v"][0])
 
 
@@ -173,9 +179,11 @@ def test_bytes_per_token_closed_form():
         assert layout.alt_bytes_per_token_head(d) == 1.5 * d + 2
         assert layout.main_tile_bytes(d) % 16 == 0 and layout.alt_tile_bytes(d) % 16 == 0
         for vb in (2, 3, 4):
-            # d 8-bit key codes, 4 B per key block of 32, vb bits per value index, one fp16 norm
-            assert layout.alt_bytes_per_token_head(d, vb) == d + 4 * (d // 32) + vb * d / 8 + 2
-            assert layout.alt_tile_bytes(d, vb) % 16 == 0
+            for kb in (4, 8):
+                # kb bits per key code, 4 B per key block of 32, vb bits per value index, one fp16 norm
+                assert layout.alt_bytes_per_token_head(d, vb, kb) == kb * d / 8 + 4 * (d // 32) + vb * d / 8 + 2
+                assert layout.alt_tile_bytes(d, vb, kb) % 16 == 0
+                assert layout.alt_key_bits(layout.alt_tile_bytes(d, vb, kb), d, vb) == kb
             assert layout.alt_value_bits(layout.alt_tile_bytes(d, vb), d) == vb
 
 
@@ -202,6 +210,10 @@ def test_vllm_metal_compression_table_reading():
     assert layout.alt_bytes_per_token_head(128) == 194
     for vb in (2, 3, 4):
         assert layout.alt_bytes_per_token_head(128, vb) == (8 * 128 / 8 + 16) + (vb * 128 / 8 + 8) - 6
+    # ... and for the table's 4-bit keys (q4_0 / q3_0)
+    row = [r for r in golden("vllm_metal_compression.json")["rows"] if r["k_quant"] == "q4_0"][0]
+    per = row["k_bits"] * 128 / 8 + 16 + row["v_bits"] * 128 / 8 + 8
+    assert layout.alt_bytes_per_token_head(128, row["v_bits"], row["k_bits"]) == per - 6
 
 
 def test_ring_split():

@@ -52,15 +52,15 @@ def test_main_materialised_rows_keep_ring_exact_and_values_within_half_a_step():
     assert cos.mean() > 0.8
 
 
-@pytest.mark.parametrize("vbits", [2, 3, 4])
-def test_alt_materialised_history_reproduces_the_decode(vbits):
+@pytest.mark.parametrize("vbits,kbits", [(2, 8), (3, 8), (4, 8), (3, 4)])
+def test_alt_materialised_history_reproduces_the_decode(vbits, kbits):
     seed, d, hkv, bsz = 5, 64, 2, 2
     sg = rng.signs(seed, d)
     c3, _ = codebook.lloyd_max(d, vbits)
     lengths = [160, 96]
     k, v = synth.kv_alt(seed, bsz, hkv, 160, d)
     bt = synth.block_table(seed, bsz, 10, True)
-    pool = np.zeros((bsz * 10, hkv, layout.alt_tile_bytes(d, vbits)), np.uint8)
+    pool = np.zeros((bsz * 10, hkv, layout.alt_tile_bytes(d, vbits, kbits)), np.uint8)
     for b, L in enumerate(lengths):
         cache.encode_alt_range(pool, bt[b:b + 1], 0, k[b:b + 1, :, :L], v[b:b + 1, :, :L], sg, c3)
     q = synth.queries(seed, bsz, hkv, d)
@@ -69,9 +69,9 @@ def test_alt_materialised_history_reproduces_the_decode(vbits):
     for b, L in enumerate(lengths):
         kk, vv = cache.materialize_alt(pool, bt, b, L, None, None, 0, sg, c3, d)
         assert np.allclose(_attend(q[b], kk, vv, hkv), ref[b], rtol=0, atol=1e-12)
-        # keys: 255-level affine codes per block of 32, error at most half a step
+        # keys: (2^kbits - 1)-step affine codes per block of 32, error at most half a step
         k0 = k[b, :, :L].astype(np.float64).reshape(hkv, L, d // 32, 32)
-        step = (k0.max(-1) - k0.min(-1)) / 255.0
+        step = (k0.max(-1) - k0.min(-1)) / ((1 << kbits) - 1.0)
         assert np.all(np.abs(kk.reshape(hkv, L, d // 32, 32) - k0) <= step[..., None] * (0.5 + 2e-3) + 1e-6)
 
 
