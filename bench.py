@@ -58,6 +58,9 @@ WORKLOADS = {
     # the alternate layout with 4-bit value indices (8-bit keys + 4-bit values: the K8+V4 mix)
     "alt-d128-v4": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=128, ctx=65536, shuffled=False, seed=0,
                         vbits=4),
+    # the alternate layout with 4-bit keys (q4_0 keys + 3-bit values: the guide's low-memory option)
+    "alt-d128-k4": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=128, ctx=65536, shuffled=False, seed=0,
+                        kbits=4),
 }
 DEFAULT_WORKLOAD = "qwen3-0.6b-32k"
 
@@ -74,7 +77,8 @@ def record_bytes(w) -> int:
     d = w["d"]
     if w["layout"] == "main":
         return (3 * d) // 8 + (w.get("vbits", 2) * d) // 8 + d // 8 + 4
-    return d + 4 * (d // 32) + (w.get("vbits", 3) * d) // 8 + 2  # 8-bit keys, block (scale, min), indices, norm
+    # key codes, block (scale, min), value indices, norm
+    return (w.get("kbits", 8) * d) // 8 + 4 * (d // 32) + (w.get("vbits", 3) * d) // 8 + 2
 
 
 def step_bytes(w, lengths_after_append):
@@ -205,7 +209,7 @@ class Layer:
     def __init__(self, tq, torch, w, layer_idx, lengths, max_len, bt_np):
         lay = tq.TQ_LAYOUT_MAIN if w["layout"] == "main" else tq.TQ_LAYOUT_ALT
         self.ctx = tq.Context(lay, w["d"], w["hq"], w["hkv"], w["seed"] + layer_idx,
-                              value_bits=w.get("vbits"))
+                              value_bits=w.get("vbits"), key_bits=w.get("kbits"))
         self.max_blocks = bt_np.shape[1]
         self.bt = torch.from_numpy(bt_np).cuda()
         nblk = bt_np.shape[0] * bt_np.shape[1]
@@ -563,7 +567,7 @@ def oracle_layer_step(w, seed, sample_len):
         sg = rng.signs(seed, d)
         k, v = synth.kv_alt(seed, 1, hkv, L, d)
         bt = np.arange(L // 16, dtype=np.int32)[None, :]
-        pool = np.zeros((bt.shape[1], hkv, layout.alt_tile_bytes(d, vb)), np.uint8)
+        pool = np.zeros((bt.shape[1], hkv, layout.alt_tile_bytes(d, vb, w.get("kbits", 8))), np.uint8)
         cache.encode_alt_range(pool, bt, 0, k, v, sg, c3)
         q = synth.queries(seed, 1, hq, d)
 
@@ -626,6 +630,7 @@ def main():
               "context": w["ctx"] if w["ctx"] is not None else f"U[{w['lo']},{w['hi']}]",
               "l2": "inputs larger than L2 (every step reads all layers' pools)"}
     config["value_bits"] = w.get("vbits", 2 if w["layout"] == "main" else 3)
+    config["key_bits"] = w.get("kbits", 3 if w["layout"] == "main" else 8)
 
     if args.impl == "reference":
         if rank != 0:

@@ -407,7 +407,8 @@ __global__ void __launch_bounds__(128) decode_main_kernel(DecArgs a) {
 // ------------------------------------------------------------------ alternate layout
 template <int D, int NR>
 __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
-  // page: 18 D + 2 vb D + 32 bytes for vb-bit value indices; the staging buffer fits vb = 4
+  // page: (2 kb + 2 + 2 vb) D + 32 bytes for kb-bit key codes and vb-bit value indices; the
+  // staging buffer fits kb = 8, vb = 4
   constexpr int TILE_MAX = 26 * D + 32;
   constexpr int G = D / 32;
   constexpr int DPT = (D + 127) / 128;
@@ -465,11 +466,11 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
   }
 
   const float scale = rsqrtf((float)D) * kLog2e;
-  const int vb = a.avb, TILE = 18 * D + 2 * vb * D + 32;
+  const int vb = a.avb, kb = a.kb, TILE = (2 * kb + 2 + 2 * vb) * D + 32;
   const uint32_t vmask = (1u << vb) - 1u;
-  const __half* ksm = reinterpret_cast<const __half*>(tile + 16 * D);
-  const uint32_t* vi = reinterpret_cast<const uint32_t*>(tile + 18 * D);
-  const __half* vn = reinterpret_cast<const __half*>(tile + 18 * D + 2 * vb * D);
+  const __half* ksm = reinterpret_cast<const __half*>(tile + 2 * kb * D);
+  const uint32_t* vi = reinterpret_cast<const uint32_t*>(tile + 2 * kb * D + 2 * D);
+  const __half* vn = reinterpret_cast<const __half*>(tile + 2 * kb * D + 2 * D + 2 * vb * D);
 
   for (int t0 = tbeg; t0 < tend; t0 += kPage) {
     const int page = t0 >> 4;
@@ -486,7 +487,7 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
       float acc[NR];
 #pragma unroll
       for (int h = 0; h < NR; ++h) acc[h] = 0.f;
-      const uint8_t* kq = tile + tok * D;
+      const uint8_t* kq = tile + tok * (kb * D / 8);  // the token's key codes (bytes or nibbles)
       // D/8 dims per thread, inside whole 32-blocks or half of one
       constexpr int SEG = D / 8 < 32 ? D / 8 : 32;
 #pragma unroll
@@ -498,7 +499,8 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
         for (int h = 0; h < NR; ++h) part_acc[h] = 0.f;
 #pragma unroll 8
         for (int k = 0; k < SEG; ++k) {
-          const float cv = (float)kq[dim0 + k];
+          const int i = dim0 + k;
+          const float cv = kb == 8 ? (float)kq[i] : (float)((kq[i >> 1] >> (4 * (i & 1))) & 15);
 #pragma unroll
           for (int h = 0; h < NR; ++h) part_acc[h] = fmaf(qf[h][dim0 + k], cv, part_acc[h]);
         }

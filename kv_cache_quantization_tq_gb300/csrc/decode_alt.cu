@@ -400,6 +400,7 @@ cudaError_t launch_decode_alt_v2(tq_ctx* ctx, const void* q, const void* pool, i
   a.err = ctx->d_err;
   dim3 grid(n_chunks, a.hkv * a.groups, batch);
   const int d = ctx->cfg.head_dim, nr = a.nrg, vb = ctx->cfg.value_bits;
+  if (ctx->cfg.key_bits != 8) return cudaErrorNotSupported;  // the block dots read byte codes
   if (nr == 1) {
     switch (d) {
       case 64: return launch_alt<64, 1>(a, vb, grid, s);

@@ -234,7 +234,8 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
 }
 
 // ------------------------------------------------------------------ alternate layout
-// Alternate-layout page: 18 d + 2 vb d + 32 bytes for vb-bit value indices (staging sized for vb 4).
+// Alternate-layout page: (2 kb + 2 + 2 vb) d + 32 bytes for kb-bit key codes and vb-bit value
+// indices (staging sized for kb = 8, vb = 4).
 template <int D>
 struct AltDq {
   static constexpr int E = D / 32;
@@ -256,7 +257,8 @@ __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
   const int n = dq_ntok(a, b);
   if (tok0 >= n) return;
   const int ntok = min(C::TB, n - tok0);
-  const int vb = a.avb, tile_bytes = 18 * D + 2 * vb * D + 32;
+  const int vb = a.avb, kb = a.kb, tile_bytes = (2 * kb + 2 + 2 * vb) * D + 32;
+  const int o_ksm = 2 * kb * D, o_vi = o_ksm + 2 * D, o_vn = o_vi + 2 * vb * D;
   const uint32_t mask = (1u << vb) - 1u;
   if (threadIdx.x < 16) lut[threadIdx.x] = a.tab.c[threadIdx.x & mask];
   load_tiles(a, smem, tile_bytes, tile_bytes, b, h, tok0 >> 4, ntok >> 4, ok);  // ends with __syncthreads
@@ -270,14 +272,16 @@ __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
     const uint8_t* tile = smem + (size_t)(tt >> 4) * tile_bytes;
     const int slot = tt & 15;
     const size_t row = (((size_t)b * a.hkv + h) * a.max_tokens + tok0 + tt) * D;
-    const uint32_t* vi = reinterpret_cast<const uint32_t*>(tile + 18 * D + slot * (vb * D / 8));
-    const float nv = __half2float(reinterpret_cast<const __half*>(tile + 18 * D + 2 * vb * D)[slot]);
+    const uint32_t* vi = reinterpret_cast<const uint32_t*>(tile + o_vi + slot * (vb * D / 8));
+    const float nv = __half2float(reinterpret_cast<const __half*>(tile + o_vn)[slot]);
     float x[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int c = coord_of(e, lane);
-      const __half2 smn = *reinterpret_cast<const __half2*>(tile + 16 * D + (slot * (D / 32) + e) * 4);
-      a.k_out[row + c] = __float2half_rn(fmaf(__low2float(smn), (float)tile[slot * D + c], __high2float(smn)));
+      const __half2 smn = *reinterpret_cast<const __half2*>(tile + o_ksm + (slot * (D / 32) + e) * 4);
+      // key code: a byte (8-bit keys) or nibble c of the token's 4-bit stream
+      const int kq = kb == 8 ? tile[slot * D + c] : (tile[slot * (D / 2) + (c >> 1)] >> (4 * (c & 1))) & 15;
+      a.k_out[row + c] = __float2half_rn(fmaf(__low2float(smn), (float)kq, __high2float(smn)));
       const int bit = vb * c;  // index c of the token's little-endian vb-bit stream
       const uint32_t lo = vi[bit >> 5];
       const uint32_t hi = (bit & 31) + vb > 32 ? vi[(bit >> 5) + 1] : 0u;

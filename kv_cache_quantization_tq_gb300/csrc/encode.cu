@@ -301,23 +301,26 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
 }
 
 // ------------------------------------------------------------------ alternate layout
-// Alternate-layout page: 16 x d 8-bit key codes, 16 x d/32 (scale, minimum) fp16 pairs, a dense
-// vb-bit stream of value indices per token (index i at bit vb i), 16 fp16 value norms:
-// 18 d + 2 vb d + 32 bytes.  Shared memory is sized for the largest (vb = 4).
-__host__ __device__ constexpr int alt_tile_bytes(int d, int vb) { return 18 * d + 2 * vb * d + 32; }
+// Alternate-layout page: a dense kb-bit stream of key codes per token (8 bits: one byte per
+// coordinate), 16 x d/32 (scale, minimum) fp16 pairs, a dense vb-bit stream of value indices per
+// token (index i at bit vb i), 16 fp16 value norms: (2 kb + 2 + 2 vb) d + 32 bytes.  Shared
+// memory is sized for the largest (kb = 8, vb = 4).
+__host__ __device__ constexpr int alt_tile_bytes(int d, int kb, int vb) { return (2 * kb + 2 + 2 * vb) * d + 32; }
 template <int D>
 struct AltEnc {
   static constexpr int E = D / 32;
   static constexpr int TB = 32;
-  static constexpr int TILE_MAX = alt_tile_bytes(D, 4);
+  static constexpr int TILE_MAX = alt_tile_bytes(D, 8, 4);
   static constexpr int THREADS = 256;
   static constexpr size_t SMEM_TILES = (size_t)(TB / 16) * TILE_MAX;
-  static constexpr size_t SMEM = SMEM_TILES + (size_t)TB * D;
+  static constexpr size_t SMEM = SMEM_TILES + 2 * (size_t)TB * D;  // tiles, value and key codes
 };
 
-// Index kk of a chunk of 32 at bit VB kk of the chunk's VB words (a little-endian bit stream).
+// Codes of every staged token as a dense little-endian VB-bit stream at byte `offset` of its page
+// (VB d / 8 bytes per token): index kk of a chunk of 32 at bit VB kk of the chunk's VB words.
 template <int D, int VB>
-__device__ __forceinline__ void pack_value_stream(const uint8_t* vcodes, uint8_t* tiles, int tile_bytes, int ntok) {
+__device__ __forceinline__ void pack_value_stream(const uint8_t* vcodes, uint8_t* tiles, int tile_bytes, int ntok,
+                                                  int offset) {
   for (int w = threadIdx.x; w < ntok * (D / 32); w += AltEnc<D>::THREADS) {
     const int tt = w / (D / 32), chunk = w % (D / 32);
     uint32_t o[VB];
@@ -330,7 +333,7 @@ __device__ __forceinline__ void pack_value_stream(const uint8_t* vcodes, uint8_t
       o[bit >> 5] |= code << (bit & 31);
       if ((bit & 31) + VB > 32) o[(bit >> 5) + 1] |= code >> (32 - (bit & 31));
     }
-    uint32_t* dst = reinterpret_cast<uint32_t*>(tiles + (size_t)(tt >> 4) * tile_bytes + 18 * D +
+    uint32_t* dst = reinterpret_cast<uint32_t*>(tiles + (size_t)(tt >> 4) * tile_bytes + offset +
                                                 (tt & 15) * (VB * D / 8) + chunk * 4 * VB);
 #pragma unroll
     for (int i = 0; i < VB; ++i) dst[i] = o[i];
@@ -341,9 +344,11 @@ template <int D>
 __device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int ntok, int start, uint8_t* smem) {
   using C = AltEnc<D>;
   constexpr int E = C::E;
-  const int vb = a.avb, tile_bytes = alt_tile_bytes(D, vb), nbound = (1 << vb) - 1;
+  const int vb = a.avb, kb = a.kb, tile_bytes = alt_tile_bytes(D, kb, vb), nbound = (1 << vb) - 1;
+  const int o_ksm = 2 * kb * D, o_vi = o_ksm + 2 * D, o_vn = o_vi + 2 * vb * D;
   uint8_t* tiles = smem;
   uint8_t* vcodes = smem + C::SMEM_TILES;
+  uint8_t* kcodes = vcodes + C::TB * D;  // 4-bit keys: staged, then packed
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const size_t base = ((size_t)b * a.hkv + h) * a.src_tokens;
   float sg[E];
@@ -367,10 +372,13 @@ __device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int n
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int c = coord_of(e, lane);
-      GroupCode g = group_quant_mm(kx[e], kmn[e], kmx[e], 255.f);
-      tile[slot * D + c] = (uint8_t)g.q;
+      GroupCode g = group_quant_mm(kx[e], kmn[e], kmx[e], (float)((1 << kb) - 1));
+      if (kb == 8)
+        tile[slot * D + c] = (uint8_t)g.q;
+      else
+        kcodes[tt * D + c] = (uint8_t)g.q;
       if (lane == 0) {
-        __half* sm = reinterpret_cast<__half*>(tile + 16 * D + (slot * (D / 32) + e) * 4);
+        __half* sm = reinterpret_cast<__half*>(tile + o_ksm + (slot * (D / 32) + e) * 4);
         sm[0] = g.s;
         sm[1] = g.mn;
       }
@@ -391,16 +399,17 @@ __device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int n
       for (int j = 0; j < 15; ++j) idx += (j < nbound && y >= a.tab.b[j]);
       vcodes[tt * D + coord_of(e, lane)] = (uint8_t)idx;
     }
-    if (lane == 0) reinterpret_cast<__half*>(tile + 18 * D + 2 * vb * D)[slot] = __float2half_rn(nv);
+    if (lane == 0) reinterpret_cast<__half*>(tile + o_vn)[slot] = __float2half_rn(nv);
   }
   __syncthreads();
-  // dense vb-bit stream per token: 32 indices -> vb words
+  // dense vb-bit stream per token: 32 indices -> vb words; 4-bit keys likewise
   if (vb == 2)
-    pack_value_stream<D, 2>(vcodes, tiles, tile_bytes, ntok);
+    pack_value_stream<D, 2>(vcodes, tiles, tile_bytes, ntok, o_vi);
   else if (vb == 4)
-    pack_value_stream<D, 4>(vcodes, tiles, tile_bytes, ntok);
+    pack_value_stream<D, 4>(vcodes, tiles, tile_bytes, ntok, o_vi);
   else
-    pack_value_stream<D, 3>(vcodes, tiles, tile_bytes, ntok);
+    pack_value_stream<D, 3>(vcodes, tiles, tile_bytes, ntok, o_vi);
+  if (kb == 4) pack_value_stream<D, 4>(kcodes, tiles, tile_bytes, ntok, 0);
   __syncthreads();
   store_tiles(a, tiles, tile_bytes, tile_bytes, ntok >> 4, b, h, (start + tok0) >> 4);
 }

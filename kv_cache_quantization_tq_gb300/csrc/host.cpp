@@ -134,7 +134,7 @@ tq_status check_config(const tq_config* c) {
         c->qjl_m != c->head_dim)
       return TQ_ERR_UNSUPPORTED;
   } else if (c->layout == TQ_LAYOUT_ALT) {
-    if (c->key_bits != 8 || c->value_bits < 2 || c->value_bits > 4) return TQ_ERR_UNSUPPORTED;
+    if ((c->key_bits != 8 && c->key_bits != 4) || c->value_bits < 2 || c->value_bits > 4) return TQ_ERR_UNSUPPORTED;
   } else {
     return TQ_ERR_INVALID_ARG;
   }
@@ -386,12 +386,12 @@ size_t tq_bytes_per_token_head(const tq_ctx* ctx) {
   if (!ctx) return 0;
   const size_t d = ctx->cfg.head_dim;
   // main: key_bits key bits, value_bits value bits and one fp16 scale + minimum per group of 32 per
-  // coordinate, two fp16 norms; alternate: 8-bit keys + 4 B per block of 32, value_bits-bit
-  // value indices, fp16 norm
+  // coordinate, two fp16 norms; alternate: key_bits-bit key codes + 4 B per block of 32,
+  // value_bits-bit value indices, fp16 norm
   const size_t vb = ctx->cfg.value_bits;
   const size_t kb = ctx->cfg.key_bits;
   return ctx->cfg.layout == TQ_LAYOUT_MAIN ? (kb * d) / 8 + (vb * d) / 8 + d / 8 + 4
-                                           : d + (d / 32) * 4 + (vb * d) / 8 + 2;
+                                           : (kb * d) / 8 + (d / 32) * 4 + (vb * d) / 8 + 2;
 }
 
 size_t tq_page_bytes(const tq_ctx* ctx) { return tq::kPage * tq_bytes_per_token_head(ctx); }

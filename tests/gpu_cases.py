@@ -70,17 +70,19 @@ def main_fields(tiles, d, kb=None):
     }
 
 
-def alt_fields(tiles, d):
-    """Fields of alternate-layout tiles (value bits vb from the size 18d + 2 vb d + 32)."""
+def alt_fields(tiles, d, kb=8):
+    """Fields of alternate-layout tiles with kb-bit keys (value bits vb from the size
+    (2 kb + 2 + 2 vb) d + 32)."""
     t = np.ascontiguousarray(tiles)
     lead = t.shape[:-1]
-    vb = (t.shape[-1] - 18 * d - 32) // (2 * d)
-    o_n = 18 * d + 2 * vb * d
-    vi = t[..., 18 * d:o_n].reshape(lead + (16, vb * d // 8))
+    o_vi = (2 * kb + 2) * d
+    vb = (t.shape[-1] - o_vi - 32) // (2 * d)
+    o_n = o_vi + 2 * vb * d
+    vi = t[..., o_vi:o_n].reshape(lead + (16, vb * d // 8))
     bits = np.unpackbits(vi, axis=-1, bitorder="little").reshape(lead + (16, d, vb)).astype(np.uint8)
     idx = sum(bits[..., i].astype(np.int32) << i for i in range(vb)).astype(np.uint8)
     return {
-        "k_bytes": t[..., :18 * d],
+        "k_bytes": t[..., :o_vi],  # key codes and their (scale, minimum) pairs
         "vidx": idx,
         "vn": np.ascontiguousarray(t[..., o_n:o_n + 32]).view("<i2"),
     }
@@ -129,13 +131,14 @@ def build_main_cache(seed, d, hkv, lengths, centroids, signs, sketch, shuffled=T
     return dict(k=k, v=v, bt=bt, pool=pool, n_c=n_c, n_b=n_b, ring_k=ring_k, ring_v=ring_v, max_ctx=int(n_c.max()) if bsz else 0)
 
 
-def build_alt_cache(seed, d, hkv, lengths, centroids3, signs, shuffled=True):
+def build_alt_cache(seed, d, hkv, lengths, centroids3, signs, shuffled=True, key_bits=8):
     bsz = len(lengths)
     t_all = ((max(lengths) + 15) // 16) * 16
     k, v = synth.kv_alt(seed, bsz, hkv, t_all, d)
     max_blocks = t_all // 16
     bt = synth.block_table(seed, bsz, max_blocks, shuffled)
-    pool = np.zeros((bsz * max_blocks, hkv, layout.alt_tile_bytes(d, cache.value_bits_of(centroids3))), np.uint8)
+    pool = np.zeros((bsz * max_blocks, hkv, layout.alt_tile_bytes(d, cache.value_bits_of(centroids3), key_bits)),
+                    np.uint8)
     n_c = np.array(lengths, np.int32)
     for b, L in enumerate(lengths):
         cache.encode_alt_range(pool, bt[b:b + 1], 0, k[b:b + 1, :, :L], v[b:b + 1, :, :L], signs, centroids3)
