@@ -1,6 +1,6 @@
 // Alternate-layout decode attention, one warp per page (CUDA cores).
 //
-// Keys are 8-bit affine codes per block of 32 (no rotation), values are
+// Keys are 8- or 4-bit affine codes per block of 32 (no rotation), values are
 // VB-bit (2, 3 or 4) Lloyd-Max indices of the rotated unit value with an fp16
 // norm (vllm-metal TurboQuant guide, quantisation table: q2_0 .. q4_0 values).  With one query head per
 // KV head the work per byte is small, so the kernel is written to stream the
@@ -73,10 +73,10 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint4& a, uint32_t 
       : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
-template <int D, int VB>
+template <int D, int VB, int KB>
 struct AltCfg {
   static constexpr int E = D / 32;      // dimensions per lane
-  static constexpr int TILE = 18 * D + 2 * VB * D + 32;  // VB-bit value indices
+  static constexpr int TILE = (2 * KB + 2 + 2 * VB) * D + 32;  // KB-bit key codes, VB-bit value indices
   static constexpr int STAGES = TILE <= 3200 ? 4 : (TILE <= 6400 ? 3 : 2);
   static constexpr size_t SMEM = (size_t)kWarps * STAGES * TILE;
 };
@@ -99,9 +99,16 @@ __device__ __forceinline__ int kq_swizzle(int row) {
   return D == 64 ? ((row >> 1) & 3) : (row & 7);
 }
 
-template <int D, int NR, int VB>
+// 4-bit key codes: the nibbles n0..n3 of w (coordinates 4t .. 4t+3) as the fp16 pairs
+// (1024 + n0, 1024 + n1) and (1024 + n2, 1024 + n3).
+__device__ __forceinline__ uint32_t nib_pair_lo(uint32_t w) { return (w & 0xFu) | ((w << 12) & 0xF0000u) | 0x64006400u; }
+__device__ __forceinline__ uint32_t nib_pair_hi(uint32_t w) {
+  return ((w >> 8) & 0xFu) | ((w << 4) & 0xF0000u) | 0x64006400u;
+}
+
+template <int D, int NR, int VB, int KB>
 __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
-  using C = AltCfg<D, VB>;
+  using C = AltCfg<D, VB, KB>;
   constexpr int NC = 1 << VB;  // centroids
   constexpr int E = C::E;
   constexpr int G = D / 32;
@@ -190,7 +197,7 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
         uint8_t* dst = wst + (k % C::STAGES) * C::TILE;
         for (int c = lane; c < C::TILE / 16; c += 32) {
           int cd = c;
-          if (c < D) {  // key rows: 16 rows x D/16 chunks, swizzled
+          if (KB == 8 && c < D) {  // 8-bit key rows: 16 rows x D/16 chunks, swizzled
             const int row = c / (D / 16), ch = c % (D / 16);
             cd = row * (D / 16) + (ch ^ kq_swizzle<D>(row));
           }
@@ -216,9 +223,9 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
       continue;
     }
     const uint8_t* T = wst + (k % C::STAGES) * C::TILE;
-    const __half2* ksm2 = reinterpret_cast<const __half2*>(T + 16 * D);
-    const uint32_t* vi = reinterpret_cast<const uint32_t*>(T + 18 * D);
-    const __half* vn = reinterpret_cast<const __half*>(T + 18 * D + 2 * VB * D);
+    const __half2* ksm2 = reinterpret_cast<const __half2*>(T + 2 * KB * D);
+    const uint32_t* vi = reinterpret_cast<const uint32_t*>(T + (2 * KB + 2) * D);
+    const __half* vn = reinterpret_cast<const __half*>(T + (2 * KB + 2 + 2 * VB) * D);
     // C[token][column] = sum over the column's block of (1024 + code) q_head
     float cacc[NT][4];
 #pragma unroll
@@ -226,18 +233,27 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
 #pragma unroll
       for (int r = 0; r < 4; ++r) cacc[j][r] = 0.f;
     {
-      const uint8_t* r0 = T + g * D + 4 * t;
-      const uint8_t* r1 = T + (g + 8) * D + 4 * t;
+      const uint8_t* r0 = T + g * (KB * D / 8) + KB * t / 2;  // coordinate 4t of the row
+      const uint8_t* r1 = T + (g + 8) * (KB * D / 8) + KB * t / 2;
       const int sw0 = kq_swizzle<D>(g), sw1 = kq_swizzle<D>(g + 8);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(r0 + 16 * (ks ^ sw0));
-        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(r1 + 16 * (ks ^ sw1));
         uint4 A;
-        A.x = __byte_perm(w0, 0x64646464u, 0x4140u);  // row g: coordinates 4t, 4t+1 as 1024 + code
-        A.y = __byte_perm(w1, 0x64646464u, 0x4140u);  // row g + 8
-        A.z = __byte_perm(w0, 0x64646464u, 0x4342u);  // row g: coordinates 4t+2, 4t+3
-        A.w = __byte_perm(w1, 0x64646464u, 0x4342u);
+        if (KB == 8) {
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(r0 + 16 * (ks ^ sw0));
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(r1 + 16 * (ks ^ sw1));
+          A.x = __byte_perm(w0, 0x64646464u, 0x4140u);  // row g: coordinates 4t, 4t+1 as 1024 + code
+          A.y = __byte_perm(w1, 0x64646464u, 0x4140u);  // row g + 8
+          A.z = __byte_perm(w0, 0x64646464u, 0x4342u);  // row g: coordinates 4t+2, 4t+3
+          A.w = __byte_perm(w1, 0x64646464u, 0x4342u);
+        } else {  // 4-bit keys: the four codes of coordinates 16 ks + 4t .. + 3 are 16 bits of the row
+          const uint32_t w0 = *reinterpret_cast<const uint16_t*>(r0 + 8 * ks);
+          const uint32_t w1 = *reinterpret_cast<const uint16_t*>(r1 + 8 * ks);
+          A.x = nib_pair_lo(w0);
+          A.y = nib_pair_lo(w1);
+          A.z = nib_pair_hi(w0);
+          A.w = nib_pair_hi(w1);
+        }
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
           if (tile_has_block<G, NR * G>(j, ks / 2)) {
@@ -354,21 +370,26 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
   }
 }
 
-template <int D, int NR, int VB>
+template <int D, int NR, int VB, int KB>
 cudaError_t launch_alt_vb(const AltArgs& a, dim3 grid, cudaStream_t s) {
-  auto kern = decode_alt_v2_kernel<D, NR, VB>;
-  constexpr size_t SMEM = AltCfg<D, VB>::SMEM;
+  auto kern = decode_alt_v2_kernel<D, NR, VB, KB>;
+  constexpr size_t SMEM = AltCfg<D, VB, KB>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, 128, SMEM, s>>>(a);
   return cudaGetLastError();
 }
 
+template <int D, int NR, int KB>
+cudaError_t launch_alt_kb(const AltArgs& a, int vb, dim3 grid, cudaStream_t s) {
+  return vb == 2 ? launch_alt_vb<D, NR, 2, KB>(a, grid, s)
+       : vb == 4 ? launch_alt_vb<D, NR, 4, KB>(a, grid, s)
+                 : launch_alt_vb<D, NR, 3, KB>(a, grid, s);
+}
+
 template <int D, int NR>
-cudaError_t launch_alt(const AltArgs& a, int vb, dim3 grid, cudaStream_t s) {
-  return vb == 2 ? launch_alt_vb<D, NR, 2>(a, grid, s)
-       : vb == 4 ? launch_alt_vb<D, NR, 4>(a, grid, s)
-                 : launch_alt_vb<D, NR, 3>(a, grid, s);
+cudaError_t launch_alt(const AltArgs& a, int vb, int kb, dim3 grid, cudaStream_t s) {
+  return kb == 4 ? launch_alt_kb<D, NR, 4>(a, vb, grid, s) : launch_alt_kb<D, NR, 8>(a, vb, grid, s);
 }
 
 }  // namespace
@@ -399,24 +420,23 @@ cudaError_t launch_decode_alt_v2(tq_ctx* ctx, const void* q, const void* pool, i
   a.tab = ctx->tab;
   a.err = ctx->d_err;
   dim3 grid(n_chunks, a.hkv * a.groups, batch);
-  const int d = ctx->cfg.head_dim, nr = a.nrg, vb = ctx->cfg.value_bits;
-  if (ctx->cfg.key_bits != 8) return cudaErrorNotSupported;  // the block dots read byte codes
+  const int d = ctx->cfg.head_dim, nr = a.nrg, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
   if (nr == 1) {
     switch (d) {
-      case 64: return launch_alt<64, 1>(a, vb, grid, s);
-      case 128: return launch_alt<128, 1>(a, vb, grid, s);
-      case 256: return launch_alt<256, 1>(a, vb, grid, s);
-      case 512: return launch_alt<512, 1>(a, vb, grid, s);
+      case 64: return launch_alt<64, 1>(a, vb, kb, grid, s);
+      case 128: return launch_alt<128, 1>(a, vb, kb, grid, s);
+      case 256: return launch_alt<256, 1>(a, vb, kb, grid, s);
+      case 512: return launch_alt<512, 1>(a, vb, kb, grid, s);
     }
   } else if (nr == 2) {
     switch (d) {
-      case 64: return launch_alt<64, 2>(a, vb, grid, s);
-      case 128: return launch_alt<128, 2>(a, vb, grid, s);
-      case 256: return launch_alt<256, 2>(a, vb, grid, s);
+      case 64: return launch_alt<64, 2>(a, vb, kb, grid, s);
+      case 128: return launch_alt<128, 2>(a, vb, kb, grid, s);
+      case 256: return launch_alt<256, 2>(a, vb, kb, grid, s);
     }
   } else if (nr <= 4) {
-    if (d == 64) return launch_alt<64, 4>(a, vb, grid, s);
-    if (d == 128) return launch_alt<128, 4>(a, vb, grid, s);
+    if (d == 64) return launch_alt<64, 4>(a, vb, kb, grid, s);
+    if (d == 128) return launch_alt<128, 4>(a, vb, kb, grid, s);
   }
   return cudaErrorNotSupported;
 }
