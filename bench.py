@@ -119,7 +119,7 @@ def aggregate_gbs(bytes_per_rank: int, ms_max: float, world: int) -> float:
 NCU_TRAFFIC = {
     ("qwen3-0.6b-32k", "tc_decode_kernel"): 13262080,     # profiles/tc_decode_kernel__qwen3-0.6b-32k.md
     ("qwen2.5-7b-b8", "tc_decode_kernel"): 109771520,     # profiles/tc_decode_kernel__qwen2.5-7b-b8.md
-    ("alt-d128", "decode_alt_v2_kernel"): 412410624,      # profiles/decode_alt_v2_kernel__alt-d128.md
+    ("alt-d128", "decode_alt_v2_kernel"): 412128768,      # profiles/decode_alt_v2_kernel__alt-d128.md
 }
 
 
