@@ -698,6 +698,7 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
     t.signs = ctx->d_signs;
     t.sfrag_enc = ctx->d_sfrag_enc;
     t.kb = ctx->cfg.key_bits;
+    t.cta_warps = plan.cta_warps;
     t.err = ctx->d_err;
     return launch_decode_tc(ctx, t, batch, s);
   }

@@ -53,11 +53,11 @@ constexpr int KSTEPS_MAX = 8 * a_planes(4);
 constexpr int kPrepSlices = 4;
 constexpr int AFRAG_U4 = KSTEPS_MAX * 32 + kPrepSlices * 2 * kMaxRep / 4;
 static_assert(AFRAG_U4 == kTcQueryU4, "query workspace layout");
-static_assert(NWARP == kPrepSlices, "the fused prep's warps fill the offset slots of the prep slices");
+static_assert(NWARP == kPrepSlices, "one prep slice per warp of the prep kernel");
 
 // Tile of the main layout with KB key bits (KB bit planes of 2d bytes: the Lloyd-Max index
 // bits, high first, then the QJL signs) and VB value bits (1600 bytes at KB = 3, VB = 2).
-template <int KB, int VB>
+template <int KB, int VB, int NW = NWARP>
 struct TcTile {
   static constexpr int NA = a_planes(KB);
   static constexpr size_t SMEM_A = (size_t)NA * 8 * 32 * sizeof(uint4);
@@ -65,9 +65,9 @@ struct TcTile {
   static constexpr int O_VQ = 2 * KB * D;
   static constexpr int O_VSM = (2 * KB + 2 * VB) * D;
   static constexpr int O_NORM = (2 * KB + 2 * VB + 2) * D;
-  static constexpr size_t SMEM_STAGE = (size_t)NWARP * STAGES * TILE;
+  static constexpr size_t SMEM_STAGE = (size_t)NW * STAGES * TILE;
   static constexpr size_t SMEM_TOTAL = SMEM_A + SMEM_STAGE;
-  static_assert((size_t)NWARP * kMaxRep * D * sizeof(float) <= SMEM_STAGE, "combine buffer fits the stages");
+  static_assert((size_t)NW * kMaxRep * D * sizeof(float) <= SMEM_STAGE, "combine buffer fits the stages");
 };
 
 
@@ -183,46 +183,52 @@ __device__ __forceinline__ int tc_nb(const TcArgs& a, int b) {
 //   reg2 = row g,   cols 2t+8..2t+9   reg3 = row g+8, cols 2t+8..2t+9
 // with g = lane / 4, t = lane % 4; row g is head g (high part), row g+8 the
 // same head's low part.
-// The query values this lane rotates (heads warp and warp + NWARP, coordinates coord_of(e, lane)),
-// times the random signs: loaded at the top of the kernel, together with the sequence's counts
-// and its first block ids, so that these round trips to memory overlap.
-static_assert(kMaxRep == 2 * NWARP, "two heads per warp in the query rotation");
+// The query values this lane rotates (heads warp + NW i, coordinates coord_of(e, lane)), times the
+// random signs: loaded at the top of the kernel, together with the sequence's counts and its first
+// block ids, so that these round trips to memory overlap.
+template <int NW>
 struct QueryRegs {
-  float x[2][D / 32];
+  static constexpr int HPW = kMaxRep / NW;  // heads per warp
+  float x[HPW][D / 32];
 };
-__device__ __forceinline__ void load_query(const TcArgs& a, int b, int h0, int lane, int warp, QueryRegs& r) {
+template <int NW>
+__device__ __forceinline__ void load_query(const TcArgs& a, int b, int h0, int lane, int warp, QueryRegs<NW>& r) {
 #pragma unroll
   for (int e = 0; e < D / 32; ++e) {
     const int c = coord_of(e, lane);
     const float sg = a.signs[c];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int h = warp + NWARP * i;
+    for (int i = 0; i < QueryRegs<NW>::HPW; ++i) {
+      const int h = warp + NW * i;
       r.x[i][e] = h < a.nrg ? __half2float(a.q[((size_t)b * a.hq + h0 + h) * D + c]) * sg : 0.f;
     }
   }
 }
 
-template <int NA>
-__device__ __forceinline__ void build_query_frags(const TcArgs& a, QueryRegs& qx, uint4* sA, float (*qr)[D],
+// Query side of one CTA of NW warps: rotation; t = S q_r with warp w computing sketch rows
+// (D / NW) w .. (D / NW)(w + 1) - 1; score offsets (slot w: this warp's part of the QJL offset,
+// slot 0 also the Lloyd-Max offset); the fragments.  Ends with __syncthreads.
+template <int NA, int NW>
+__device__ __forceinline__ void build_query_frags(const TcArgs& a, QueryRegs<NW>& qx, uint4* sA, float (*qr)[D],
                                                   float (*qt)[D], float (*soff)[2][kMaxRep], int tid, int lane,
                                                   int warp) {
+  constexpr int NJ = D / (8 * NW);  // sketch-row n-tiles per warp
   const float rs = rsqrtf((float)D);
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < QueryRegs<NW>::HPW; ++i) {
     wht_warp<D / 32>(qx.x[i], lane);
 #pragma unroll
-    for (int e = 0; e < D / 32; ++e) qr[warp + NWARP * i][coord_of(e, lane)] = qx.x[i][e] * rs;
+    for (int e = 0; e < D / 32; ++e) qr[warp + NW * i][coord_of(e, lane)] = qx.x[i][e] * rs;
   }
   __syncthreads();
   {
-    // t[h][j] = sum_i S[j][i] q_r[h][i]; warp w covers sketch rows 32w .. 32w+31.  Every coordinate
-    // this lane touches (16 ks + 2t + {0, 1, 8, 9} of q_r, 32w + 8j + 2t + {0, 1} of t) has bit
-    // position 12 + t, so the lane's share of the score offsets is one factor times plain sums.
+    // t[h][j] = sum_i S[j][i] q_r[h][i].  Every coordinate this lane touches (16 ks + 2t +
+    // {0, 1, 8, 9} of q_r, sketch rows 8 (NJ w + j) + 2t + {0, 1} of t) has bit position 12 + t, so
+    // the lane's share of the score offsets is one factor times plain sums.
     const int g = lane >> 2, t = lane & 3;
-    float ch[4][4], cl[4][4];
+    float ch[NJ][4], cl[NJ][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < NJ; ++j)
 #pragma unroll
       for (int r = 0; r < 4; ++r) ch[j][r] = cl[j][r] = 0.f;
     float sl = 0.f;
@@ -234,9 +240,9 @@ __device__ __forceinline__ void build_query_frags(const TcArgs& a, QueryRegs& qx
       sl += (q0 + q1) + (q8 + q9);
       split2(q0, q1, A.x, A.y);
       split2(q8, q9, A.z, A.w);
-      const uint4* bf = a.sfrag_enc + ((size_t)ks * (D / 8) + 4 * warp) * 32 + lane;
+      const uint4* bf = a.sfrag_enc + ((size_t)ks * (D / 8) + NJ * warp) * 32 + lane;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < NJ; ++j) {
         const uint4 bv = __ldg(bf + j * 32);
         mma_f16(ch[j], A, bv.x, bv.y);
         mma_f16(cl[j], A, bv.z, bv.w);
@@ -245,8 +251,8 @@ __device__ __forceinline__ void build_query_frags(const TcArgs& a, QueryRegs& qx
     // high x high + 2^-11 (low x high + high x low); low x low (2^-22) is dropped
     float sq = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int col = 32 * warp + 8 * j + 2 * t;
+    for (int j = 0; j < NJ; ++j) {
+      const int col = 8 * (NJ * warp + j) + 2 * t;
       const float t0 = fmaf(ch[j][2] + cl[j][0], kLoUnscale, ch[j][0]);
       const float t1 = fmaf(ch[j][3] + cl[j][1], kLoUnscale, ch[j][1]);
       qt[g][col] = t0;
@@ -266,15 +272,16 @@ __device__ __forceinline__ void build_query_frags(const TcArgs& a, QueryRegs& qx
     }
   }
   __syncthreads();
-  // NA planes x 8 k-steps x 32 lanes x 2 register pairs, NWARP * 32 items per pass: the plane of
-  // every pass is a compile-time constant (a pass covers two k-steps of one plane)
-  static_assert(NWARP * 32 == 128, "two k-steps per pass");
+  // NA planes x 8 k-steps x 32 lanes x 2 register pairs, NW * 32 items per pass: a pass covers
+  // NW / 2 k-steps of one plane, so the plane of every pass is a compile-time constant
+  constexpr int KPP = NW / 2;  // k-steps per pass
+  static_assert(8 % KPP == 0, "whole passes per plane");
   uint32_t* dst = reinterpret_cast<uint32_t*>(sA);
   const int half = tid & 1, L = (tid >> 1) & 31, g = L >> 2, t = L & 3;
 #pragma unroll
-  for (int it = 0; it < NA * 4; ++it) {
-    const int ks = 2 * it + (tid >> 6);  // k-steps: 8 per A plane, QJL last
-    const int plane = it >> 2, kb = ks & 7;
+  for (int it = 0; it < NA * (8 / KPP); ++it) {
+    const int ks = KPP * it + (tid >> 6);  // k-steps: 8 per A plane, QJL last
+    const int plane = it / (8 / KPP), kb = ks & 7;
     const int dim = frag_dim(kb, t, half);
     const float sc = bitenc_scale(2 * (kb & 1) + half);
     float v0, v1;
@@ -567,19 +574,23 @@ __device__ __forceinline__ void page_ring(const TcArgs& a, const uint4 (&Aq)[8],
   }
 }
 
-// MINB: CTAs per SM the register allocation must allow (3 for multi-wave grids; 2 for grids that
-// fit in one wave at 2 CTAs per SM, where the extra registers remove spills from the page loop).
-template <int KB, int VB, int MINB>
-__global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
-  using L = TcTile<KB, VB>;
+// NW warps per CTA; MINB: CTAs per SM the register allocation must allow.
+//   NW 8, MINB 1: grids of at most one CTA per SM (the query side is built once per SM, by 8 warps);
+//   NW 4, MINB 2: grids that fit in one wave at 2 CTAs per SM (the extra registers remove spills
+//                 from the page loop);
+//   NW 4, MINB 3: larger grids, with the query fragments from tc_prep_kernel.
+template <int KB, int VB, int MINB, int NW>
+__global__ void __launch_bounds__(32 * NW, MINB) tc_decode_kernel(TcArgs a) {
+  using L = TcTile<KB, VB, NW>;
+  constexpr int NSLOT = NW > kPrepSlices ? NW : kPrepSlices;  // score-offset slots
   extern __shared__ __align__(16) uint8_t smem[];
   uint4* sA = reinterpret_cast<uint4*>(smem);
   uint8_t* stage = smem + L::SMEM_A;
-  __shared__ float wm[NWARP][kMaxRep], wl[NWARP][kMaxRep];
-  __shared__ int sblk[NWARP][STAGES];
+  __shared__ float wm[NW][kMaxRep], wl[NW][kMaxRep];
+  __shared__ int sblk[NW][STAGES];
   __shared__ __align__(16) float qr[kMaxRep][D];
   __shared__ __align__(16) float qt[kMaxRep][D];
-  __shared__ __align__(16) float soff[kPrepSlices][2][kMaxRep];  // score offsets (partial sums)
+  __shared__ __align__(16) float soff[NSLOT][2][kMaxRep];  // score offsets (partial sums)
 
   const int part = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int kvh = hg / a.groups;
@@ -594,11 +605,11 @@ __global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
   int blk_pre[STAGES];
 #pragma unroll
   for (int k = 0; k < STAGES; ++k) {
-    const int idx = pbeg + warp + NWARP * k;
+    const int idx = pbeg + warp + NW * k;
     blk_pre[k] = (part < a.n_chunks && idx < a.max_blocks) ? __ldg(btb + idx) : -1;
   }
-  QueryRegs qx;
-  if (!a.afrag && part < a.n_chunks) load_query(a, b, h0, lane, warp, qx);
+  QueryRegs<NW> qx;
+  if (!a.afrag && part < a.n_chunks) load_query<NW>(a, b, h0, lane, warp, qx);
   const int nc = tc_nc(a, b), nb = tc_nb(a, b);
   const int npages = nc >> 4;
   const int nch = (npages + a.chunk_pages - 1) / a.chunk_pages;
@@ -630,12 +641,12 @@ __global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
       cp_commit();
     }
     const int npg = min(npages, pbeg + a.chunk_pages) - pbeg;
-    const int nw = npg > warp ? (npg - warp + NWARP - 1) / NWARP : 0;
+    const int nw = npg > warp ? (npg - warp + NW - 1) / NW : 0;
     uint8_t* wst = stage + (size_t)warp * STAGES * L::TILE;
     // Block ids: the id of the next page to copy is read one page ahead, so the table read
     // never holds up a copy (or the compute queued behind it); the ids of the pages in flight
     // are kept per warp in shared memory.
-    auto blk_of = [&](int k) { return k < nw ? __ldg(btb + pbeg + warp + NWARP * k) : -1; };
+    auto blk_of = [&](int k) { return k < nw ? __ldg(btb + pbeg + warp + NW * k) : -1; };
     auto issue = [&](int k, int blk) {
       if (k < nw) {
         if (lane == 0) sblk[warp][k % STAGES] = blk;
@@ -654,15 +665,18 @@ __global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
       cp_wait<STAGES - 1>();
       __syncthreads();  // every thread's share of the fragments has landed
     } else {
-      build_query_frags<L::NA>(a, qx, sA, qr, qt, soff, tid, lane, warp);  // ends with __syncthreads
+      build_query_frags<L::NA, NW>(a, qx, sA, qr, qt, soff, tid, lane, warp);  // ends with __syncthreads
     }
-    // score offsets of this lane's head: the four partial sums (prep slices, or the fused prep's
-    // warps) added once, outside the page loop
+    // score offsets of this lane's head: the partial sums (prep slices, or the warps of this CTA's
+    // query side) added once, outside the page loop
+    const int nslot = a.afrag ? kPrepSlices : NW;
     float off_lm = 0.f, off_qj = 0.f;
 #pragma unroll
-    for (int sl = 0; sl < kPrepSlices; ++sl) {
-      off_lm += soff[sl][0][g];
-      off_qj += soff[sl][1][g];
+    for (int sl = 0; sl < NSLOT; ++sl) {
+      if (sl < nslot) {
+        off_lm += soff[sl][0][g];
+        off_qj += soff[sl][1][g];
+      }
     }
     for (int k = 0; k < nw; ++k) {
       __syncwarp();  // every lane is done with the slot and stage that are refilled next
@@ -694,7 +708,7 @@ __global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
     }
     const __half* rk = a.ring_k + ((size_t)b * a.hkv + kvh) * kRing * D;
     const __half* rv = a.ring_v + ((size_t)b * a.hkv + kvh) * kRing * D;
-    for (int t0 = warp * 16; t0 < nb; t0 += NWARP * 16) page_ring(a, Aq, rk, rv, t0, min(16, nb - t0), st, lane);
+    for (int t0 = warp * 16; t0 < nb; t0 += NW * 16) page_ring(a, Aq, rk, rv, t0, min(16, nb - t0), st, lane);
   }
 
   // ---- per-warp results: head g, dims nt*8 + 2t + {0,1}
@@ -709,7 +723,7 @@ __global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
     mn[gg] += __shfl_xor_sync(kFull, mn[gg], 2);
   }
   __syncthreads();  // stage buffers are free: reuse them for the combine
-  float* wo = reinterpret_cast<float*>(stage);  // [NWARP][kMaxRep][D]
+  float* wo = reinterpret_cast<float*>(stage);  // [NW][kMaxRep][D]
 #pragma unroll
   for (int nt = 0; nt < 16; ++nt) {
 #pragma unroll
@@ -728,10 +742,10 @@ __global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
   if (tid < kMaxRep) {
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NWARP; ++w) M = fmaxf(M, wm[w][tid]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, wm[w][tid]);
     float den = 0.f;
 #pragma unroll
-    for (int w = 0; w < NWARP; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const float f = M == -INFINITY ? 0.f : exp2f(wm[w][tid] - M);
       wm[w][tid] = f;
       den = fmaf(f, wl[w][tid], den);
@@ -746,7 +760,7 @@ __global__ void __launch_bounds__(128, MINB) tc_decode_kernel(TcArgs a) {
     const float M = hM[h], den = hden[h];
     float num = 0.f;
 #pragma unroll
-    for (int w = 0; w < NWARP; ++w) num = fmaf(wm[w][h], wo[((size_t)w * kMaxRep + h) * D + dim], num);
+    for (int w = 0; w < NW; ++w) num = fmaf(wm[w][h], wo[((size_t)w * kMaxRep + h) * D + dim], num);
     if (direct) {
       a.out[((size_t)b * a.hq + h0 + h) * D + dim] = den > 0.f ? num / den : 0.f;
     } else {
@@ -932,20 +946,35 @@ cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) 
   }
   const int kb = ctx->cfg.key_bits;
   const bool v4 = ctx->cfg.value_bits == 4;
-  const bool wide = (int64_t)a.n_parts * hgroups * batch <= 2 * (int64_t)ctx->sm_count;  // one wave at 2 per SM
-  auto kern = wide ? (kb == 4 ? (v4 ? tc_decode_kernel<4, 4, 2> : tc_decode_kernel<4, 2, 2>)
-                    : kb == 3 ? (v4 ? tc_decode_kernel<3, 4, 2> : tc_decode_kernel<3, 2, 2>)
-                              : (v4 ? tc_decode_kernel<2, 4, 2> : tc_decode_kernel<2, 2, 2>))
-                   : (kb == 4 ? (v4 ? tc_decode_kernel<4, 4, 3> : tc_decode_kernel<4, 2, 3>)
-                    : kb == 3 ? (v4 ? tc_decode_kernel<3, 4, 3> : tc_decode_kernel<3, 2, 3>)
-                              : (v4 ? tc_decode_kernel<2, 4, 3> : tc_decode_kernel<2, 2, 3>));
-  const size_t smem = kb == 4 ? (v4 ? TcTile<4, 4>::SMEM_TOTAL : TcTile<4, 2>::SMEM_TOTAL)
-                    : kb == 3 ? (v4 ? TcTile<3, 4>::SMEM_TOTAL : TcTile<3, 2>::SMEM_TOTAL)
-                              : (v4 ? TcTile<2, 4>::SMEM_TOTAL : TcTile<2, 2>::SMEM_TOTAL);
+  // 8-warp CTAs when the plan gives at most one CTA per SM (a.cta_warps == 8); otherwise 4-warp CTAs,
+  // with the 2-CTA-per-SM register budget when the grid fits one wave at 2 per SM
+  const bool w8 = a.cta_warps == 8;
+  const bool wide = (int64_t)a.n_parts * hgroups * batch <= 2 * (int64_t)ctx->sm_count;
+  using KernFn = void (*)(TcArgs);
+  KernFn kern;
+  size_t smem;
+  if (w8) {
+    kern = kb == 4 ? (v4 ? tc_decode_kernel<4, 4, 1, 8> : tc_decode_kernel<4, 2, 1, 8>)
+         : kb == 3 ? (v4 ? tc_decode_kernel<3, 4, 1, 8> : tc_decode_kernel<3, 2, 1, 8>)
+                   : (v4 ? tc_decode_kernel<2, 4, 1, 8> : tc_decode_kernel<2, 2, 1, 8>);
+    smem = kb == 4 ? (v4 ? TcTile<4, 4, 8>::SMEM_TOTAL : TcTile<4, 2, 8>::SMEM_TOTAL)
+         : kb == 3 ? (v4 ? TcTile<3, 4, 8>::SMEM_TOTAL : TcTile<3, 2, 8>::SMEM_TOTAL)
+                   : (v4 ? TcTile<2, 4, 8>::SMEM_TOTAL : TcTile<2, 2, 8>::SMEM_TOTAL);
+  } else {
+    kern = wide ? (kb == 4 ? (v4 ? tc_decode_kernel<4, 4, 2, 4> : tc_decode_kernel<4, 2, 2, 4>)
+                 : kb == 3 ? (v4 ? tc_decode_kernel<3, 4, 2, 4> : tc_decode_kernel<3, 2, 2, 4>)
+                           : (v4 ? tc_decode_kernel<2, 4, 2, 4> : tc_decode_kernel<2, 2, 2, 4>))
+                : (kb == 4 ? (v4 ? tc_decode_kernel<4, 4, 3, 4> : tc_decode_kernel<4, 2, 3, 4>)
+                 : kb == 3 ? (v4 ? tc_decode_kernel<3, 4, 3, 4> : tc_decode_kernel<3, 2, 3, 4>)
+                           : (v4 ? tc_decode_kernel<2, 4, 3, 4> : tc_decode_kernel<2, 2, 3, 4>));
+    smem = kb == 4 ? (v4 ? TcTile<4, 4>::SMEM_TOTAL : TcTile<4, 2>::SMEM_TOTAL)
+         : kb == 3 ? (v4 ? TcTile<3, 4>::SMEM_TOTAL : TcTile<3, 2>::SMEM_TOTAL)
+                   : (v4 ? TcTile<2, 4>::SMEM_TOTAL : TcTile<2, 2>::SMEM_TOTAL);
+  }
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   prof_start(ctx, kProfDecode, s);
-  kern<<<dim3(a.n_parts, hgroups, batch), 128, smem, s>>>(a);
+  kern<<<dim3(a.n_parts, hgroups, batch), w8 ? 256 : 128, smem, s>>>(a);
   prof_stop(ctx, kProfDecode, s);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -235,16 +235,28 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
   auto align = [](size_t x) { return (x + 255) & ~(size_t)255; };
   pl.tensor_core = ctx->cfg.layout == TQ_LAYOUT_MAIN && d == 128;
   int64_t per;
+  pl.cta_warps = 4;
   if (pl.tensor_core) {
-    // About 2 CTAs per SM, i.e. one wave at the occupancy the kernel gets, with 16..64 pages
-    // per chunk (4..16 per warp).  Measured on GB300 over 8K..65K-page decode steps (16..64-page
-    // sweeps): fewer, longer chunks leave SMs idle; shorter ones pay the per-CTA query fragments
-    // and combine more often than they gain parallelism.  Large steps stay at 64 pages, where
-    // whole-wave chunk counts (36..56 pages) measured no better.
-    const int64_t target = std::max<int64_t>(1, (int64_t)ctx->sm_count * 2);
-    per = (total_pages + target - 1) / target;
-    per = std::max<int64_t>(16, std::min<int64_t>(64, per));
-    per = (per + 3) / 4 * 4;
+    // At most one 8-warp CTA per SM when that fits in one wave with chunks of up to 64 pages (a
+    // multiple of 8, one page per warp and round): each SM then builds the query side once, and
+    // the merge sees half the partials.
+    int64_t per8 = (total_pages + ctx->sm_count - 1) / std::max(1, ctx->sm_count);
+    per8 = std::max<int64_t>(16, (per8 + 7) / 8 * 8);
+    const int64_t parts8 = (pages + per8 - 1) / per8 + 1;
+    if (per8 <= 64 && pages <= (int64_t)per8 * kMaxChunks && parts8 * hkv * groups * batch <= ctx->sm_count) {
+      pl.cta_warps = 8;
+      per = per8;
+    } else {
+      // About 2 CTAs per SM, i.e. one wave at the occupancy the kernel gets, with 16..64 pages
+      // per chunk (4..16 per warp).  Measured on GB300 over 8K..65K-page decode steps (16..64-page
+      // sweeps): fewer, longer chunks leave SMs idle; shorter ones pay the per-CTA query fragments
+      // and combine more often than they gain parallelism.  Large steps stay at 64 pages, where
+      // whole-wave chunk counts (36..56 pages) measured no better.
+      const int64_t target = std::max<int64_t>(1, (int64_t)ctx->sm_count * 2);
+      per = (total_pages + target - 1) / target;
+      per = std::max<int64_t>(16, std::min<int64_t>(64, per));
+      per = (per + 3) / 4 * 4;
+    }
   } else {
     // about 8 CTAs per SM worth of split-K chunks, each between 4 and 64 pages
     per = (total_pages + 1215) / 1216;
@@ -252,7 +264,7 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
   }
   // at most kMaxChunks chunks per sequence: the merge keeps one weight per part in shared memory
   per = std::max<int64_t>(per, (pages + kMaxChunks - 1) / kMaxChunks);
-  if (pl.tensor_core) per = (per + 3) / 4 * 4;
+  if (pl.tensor_core) per = (per + pl.cta_warps - 1) / pl.cta_warps * pl.cta_warps;
   pl.chunk_tokens = (int)(per * kPage);
   pl.n_chunks = (int)((pages + per - 1) / per);
   pl.n_parts = pl.n_chunks + 1;
@@ -261,7 +273,7 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
     // saving a kernel; larger grids build them once per (sequence, head group) in a prep
     // kernel, because there the per-CTA cost (~3 us) outweighs the saved launch.
     const int64_t ctas = (int64_t)pl.n_parts * hkv * groups * batch;
-    pl.fused_prep = ctas <= (int64_t)ctx->sm_count * 3;
+    pl.fused_prep = pl.cta_warps == 8 || ctas <= (int64_t)ctx->sm_count * 3;
     pl.q_bytes = pl.fused_prep ? 0 : align((size_t)batch * hkv * groups * kTcQueryU4 * 16);
   } else
     pl.q_bytes = ctx->cfg.layout == TQ_LAYOUT_MAIN ? align(sizeof(float) * batch * hq * 2 * d) : 0;

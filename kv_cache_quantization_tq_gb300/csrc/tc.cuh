@@ -25,6 +25,7 @@ struct TcArgs {
   int chunk_pages, n_chunks, n_parts;
   int hq, hkv, n_rep, nrg, groups;
   int kb;          // key bits: 2, 3 or 4 (kb - 1 stored index planes, high bit first, then QJL)
+  int cta_warps;   // warps per decode CTA: 8 (at most one CTA per SM) or 4
   const float* signs;
   const uint4* sfrag_enc;  // S^T as mma.sync B fragments (k = coordinate, n = sketch row), hi / lo
   uint32_t* err;

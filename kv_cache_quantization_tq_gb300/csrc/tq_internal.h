@@ -66,6 +66,7 @@ void prof_stop(tq_ctx* ctx, int kind, cudaStream_t s);
 struct DecodePlan {
   bool tensor_core;   // main layout, head_dim 128: decode_tc.cu
   bool fused_prep;    // tensor-core path: each CTA builds its own query fragments (one-wave grids)
+  int cta_warps;      // tensor-core path: 8 (at most one CTA per SM) or 4 warps per decode CTA
   int chunk_tokens;   // compressed tokens per split-K chunk (multiple of 16)
   int n_chunks;       // chunks for max_ctx compressed tokens
   int n_parts;        // n_chunks + 1 (ring part)

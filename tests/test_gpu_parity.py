@@ -132,6 +132,7 @@ def _run_decode(ctx, e, q, hq, d, use_ring=True):
     (128, 2, 7, [1500, 300, 17, 128]),   # GQA 7, ragged, ring-only rows
     (128, 2, 5, [2049, 129]),            # GQA 5, one-token rings
     (128, 1, 16, [700]),                 # n_rep 16 -> two head groups
+    (128, 1, 4, [300] * 80),             # 80 sequences: 4-warp CTAs at 2 per SM (8-warp grid > 1 per SM)
     (128, 3, 1, [333]),
     (64, 2, 2, [900, 1]),
     (256, 2, 3, [640]),
