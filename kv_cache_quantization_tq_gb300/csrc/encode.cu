@@ -310,10 +310,12 @@ template <int D>
 struct AltEnc {
   static constexpr int E = D / 32;
   static constexpr int TB = 32;
-  static constexpr int TILE_MAX = alt_tile_bytes(D, 8, 4);
   static constexpr int THREADS = 256;
-  static constexpr size_t SMEM_TILES = (size_t)(TB / 16) * TILE_MAX;
-  static constexpr size_t SMEM = SMEM_TILES + 2 * (size_t)TB * D;  // tiles, value and key codes
+  // staged tiles, value codes, and (keys below 8 bits) key codes before packing
+  static constexpr size_t smem(int kb, int vb) {
+    return (size_t)(TB / 16) * alt_tile_bytes(D, kb, vb) + (size_t)TB * D + (kb == 8 ? 0 : (size_t)TB * D);
+  }
+  static constexpr size_t SMEM = smem(4, 4) > smem(8, 4) ? smem(4, 4) : smem(8, 4);  // the largest
 };
 
 // Codes of every staged token as a dense little-endian VB-bit stream at byte `offset` of its page
@@ -340,15 +342,16 @@ __device__ __forceinline__ void pack_value_stream(const uint8_t* vcodes, uint8_t
   }
 }
 
-template <int D>
-__device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int ntok, int start, uint8_t* smem) {
+template <int D, int VB>
+__device__ void encode_alt_block_vb(const EncArgs& a, int b, int h, int tok0, int ntok, int start, uint8_t* smem) {
   using C = AltEnc<D>;
   constexpr int E = C::E;
-  const int vb = a.avb, kb = a.kb, tile_bytes = alt_tile_bytes(D, kb, vb), nbound = (1 << vb) - 1;
+  constexpr int vb = VB, nbound = (1 << VB) - 1;
+  const int kb = a.kb, tile_bytes = alt_tile_bytes(D, kb, vb);
   const int o_ksm = 2 * kb * D, o_vi = o_ksm + 2 * D, o_vn = o_vi + 2 * vb * D;
   uint8_t* tiles = smem;
-  uint8_t* vcodes = smem + C::SMEM_TILES;
-  uint8_t* kcodes = vcodes + C::TB * D;  // 4-bit keys: staged, then packed
+  uint8_t* vcodes = smem + (size_t)(C::TB / 16) * tile_bytes;
+  uint8_t* kcodes = vcodes + C::TB * D;  // keys below 8 bits: staged, then packed
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const size_t base = ((size_t)b * a.hkv + h) * a.src_tokens;
   float sg[E];
@@ -394,24 +397,30 @@ __device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int n
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const float y = vv[e] * inv;
+      // #{boundaries <= y} over the 2^vb - 1 ascending boundaries
       int idx = 0;
 #pragma unroll
-      for (int j = 0; j < 15; ++j) idx += (j < nbound && y >= a.tab.b[j]);
+      for (int j = 0; j < nbound; ++j) idx += y >= a.tab.b[j];
       vcodes[tt * D + coord_of(e, lane)] = (uint8_t)idx;
     }
     if (lane == 0) reinterpret_cast<__half*>(tile + o_vn)[slot] = __float2half_rn(nv);
   }
   __syncthreads();
   // dense vb-bit stream per token: 32 indices -> vb words; 4-bit keys likewise
-  if (vb == 2)
-    pack_value_stream<D, 2>(vcodes, tiles, tile_bytes, ntok, o_vi);
-  else if (vb == 4)
-    pack_value_stream<D, 4>(vcodes, tiles, tile_bytes, ntok, o_vi);
-  else
-    pack_value_stream<D, 3>(vcodes, tiles, tile_bytes, ntok, o_vi);
+  pack_value_stream<D, VB>(vcodes, tiles, tile_bytes, ntok, o_vi);
   if (kb == 4) pack_value_stream<D, 4>(kcodes, tiles, tile_bytes, ntok, 0);
   __syncthreads();
   store_tiles(a, tiles, tile_bytes, tile_bytes, ntok >> 4, b, h, (start + tok0) >> 4);
+}
+
+template <int D>
+__device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int ntok, int start, uint8_t* smem) {
+  if (a.avb == 2)
+    encode_alt_block_vb<D, 2>(a, b, h, tok0, ntok, start, smem);
+  else if (a.avb == 4)
+    encode_alt_block_vb<D, 4>(a, b, h, tok0, ntok, start, smem);
+  else
+    encode_alt_block_vb<D, 3>(a, b, h, tok0, ntok, start, smem);
 }
 
 // ------------------------------------------------------------------ kernels
@@ -481,26 +490,33 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   }
 }
 
+// Dynamic shared memory of one launch: the main layout's fixed staging, or the alternate layout's
+// for its key and value widths (the function attribute allows the largest).
+template <int D, int VB>
+size_t enc_smem(const EncArgs& a) {
+  return VB ? MainEnc<D, (VB ? VB : 2)>::SMEM : AltEnc<D>::smem(a.kb, a.avb);
+}
+
 template <int D, int VB>
 cudaError_t launch_encode_t(const EncArgs& a, int batch, cudaStream_t s) {
   constexpr int TB = VB ? MainEnc<D, (VB ? VB : 2)>::TB : AltEnc<D>::TB;
-  constexpr size_t SMEM = VB ? MainEnc<D, (VB ? VB : 2)>::SMEM : AltEnc<D>::SMEM;
+  constexpr size_t SMEM_MAX = VB ? MainEnc<D, (VB ? VB : 2)>::SMEM : AltEnc<D>::SMEM;
   auto kern = encode_kernel<D, VB>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
   if (e != cudaSuccess) return e;
   dim3 grid((a.n_tokens + TB - 1) / TB, a.hkv, batch);
-  kern<<<grid, 256, SMEM, s>>>(a);
+  kern<<<grid, 256, enc_smem<D, VB>(a), s>>>(a);
   return cudaGetLastError();
 }
 
 template <int D, int VB>
 cudaError_t launch_append_t(const AppendArgs& a, int batch, cudaStream_t s) {
-  constexpr size_t SMEM = VB ? MainEnc<D, (VB ? VB : 2)>::SMEM : AltEnc<D>::SMEM;
+  constexpr size_t SMEM_MAX = VB ? MainEnc<D, (VB ? VB : 2)>::SMEM : AltEnc<D>::SMEM;
   auto kern = append_kernel<D, VB>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
   if (e != cudaSuccess) return e;
   dim3 grid(a.enc.hkv, batch);
-  kern<<<grid, 256, SMEM, s>>>(a);
+  kern<<<grid, 256, enc_smem<D, VB>(a.enc), s>>>(a);
   return cudaGetLastError();
 }
 
