@@ -57,14 +57,21 @@ static_assert(NWARP == kPrepSlices, "one prep slice per warp of the prep kernel"
 
 // Tile of the main layout with KB key bits (KB bit planes of 2d bytes: the Lloyd-Max index
 // bits, high first, then the QJL signs) and VB value bits (1600 bytes at KB = 3, VB = 2).
-template <int KB, int VB, int NW = NWARP>
-struct TcTile {
+template <int KB, int VB>
+struct TcLayout {
   static constexpr int NA = a_planes(KB);
   static constexpr size_t SMEM_A = (size_t)NA * 8 * 32 * sizeof(uint4);
   static constexpr int TILE = (2 * KB + 2 * VB + 2) * D + 64;
   static constexpr int O_VQ = 2 * KB * D;
   static constexpr int O_VSM = (2 * KB + 2 * VB) * D;
   static constexpr int O_NORM = (2 * KB + 2 * VB + 2) * D;
+};
+// ... and its staging in a CTA of NW warps (STAGES pages per warp, then the query fragments)
+template <int KB, int VB, int NW = NWARP>
+struct TcTile : TcLayout<KB, VB> {
+  using TcLayout<KB, VB>::NA;
+  using TcLayout<KB, VB>::SMEM_A;
+  using TcLayout<KB, VB>::TILE;
   static constexpr size_t SMEM_STAGE = (size_t)NW * STAGES * TILE;
   static constexpr size_t SMEM_TOTAL = SMEM_A + SMEM_STAGE;
   static_assert((size_t)NW * kMaxRep * D * sizeof(float) <= SMEM_STAGE, "combine buffer fits the stages");
