@@ -83,7 +83,9 @@ __global__ void sketch_frag_enc_kernel(const float* __restrict__ s, int d, uint4
 template <int D, int VB>
 struct MainEnc {
   static constexpr int E = D / 32;
-  static constexpr int TB = D <= 128 ? 128 : (D == 256 ? 64 : 32);
+  // tokens per CTA: 64 at d <= 128 (about 50 KB of shared memory, 4 CTAs per SM; 128 tokens per CTA
+  // fit only 2 per SM and encoded 21% fewer tokens per second), fewer for larger d
+  static constexpr int TB = D <= 128 ? 64 : (D == 256 ? 64 : 32);
   static constexpr int TILE = (10 + 2 * VB) * D + 64;  // largest tile (kb = 4): staging stride
   static constexpr int THREADS = 256;
   static constexpr int RS = D + 8;                     // residual row stride (halves): conflict-free fragments
