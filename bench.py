@@ -118,7 +118,7 @@ def aggregate_gbs(bytes_per_rank: int, ms_max: float, world: int) -> float:
 # kernel source it was captured on; a workload without one reports null.
 NCU_TRAFFIC = {
     ("qwen3-0.6b-32k", "tc_decode_kernel"): 13254144,     # profiles/tc_decode_kernel__qwen3-0.6b-32k.md
-    ("qwen2.5-7b-b8", "tc_decode_kernel"): 109771520,     # profiles/tc_decode_kernel__qwen2.5-7b-b8.md
+    ("qwen2.5-7b-b8", "tc_decode_kernel"): 109436928,     # profiles/tc_decode_kernel__qwen2.5-7b-b8.md
     ("alt-d128", "decode_alt_v2_kernel"): 412128768,      # profiles/decode_alt_v2_kernel__alt-d128.md
 }
 
