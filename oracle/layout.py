@@ -263,7 +263,7 @@ def alt_value_bits(tile_bytes: int, d: int, kbits: int = 8) -> int:
 def alt_key_bits(tile_bytes: int, d: int, vbits: int) -> int:
     """Key bits of an alternate-layout tile from its size and value bits."""
     kb, rem = divmod(tile_bytes - (2 + 2 * vbits) * d - 32, 2 * d)
-    assert rem == 0 and kb in (4, 8), (tile_bytes, d, vbits)
+    assert rem == 0 and kb in (2, 4, 5, 8), (tile_bytes, d, vbits)
     return kb
 
 

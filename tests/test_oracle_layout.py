@@ -140,7 +140,7 @@ def test_main_tile_round_trip(d):
 
 
 @pytest.mark.parametrize("d", [64, 128, 256, 512])
-@pytest.mark.parametrize("vbits,kbits", [(2, 8), (3, 8), (4, 8), (3, 4), (4, 4)])
+@pytest.mark.parametrize("vbits,kbits", [(2, 8), (3, 8), (4, 8), (3, 4), (4, 4), (3, 5), (4, 5), (3, 2), (2, 2)])
 def test_alt_tile_round_trip(d, vbits, kbits):
     g = np.random.default_rng(d + vbits + kbits)
     f = {
@@ -179,7 +179,7 @@ def test_bytes_per_token_closed_form():
         assert layout.alt_bytes_per_token_head(d) == 1.5 * d + 2
         assert layout.main_tile_bytes(d) % 16 == 0 and layout.alt_tile_bytes(d) % 16 == 0
         for vb in (2, 3, 4):
-            for kb in (4, 8):
+            for kb in (2, 4, 5, 8):
                 # kb bits per key code, 4 B per key block of 32, vb bits per value index, one fp16 norm
                 assert layout.alt_bytes_per_token_head(d, vb, kb) == kb * d / 8 + 4 * (d // 32) + vb * d / 8 + 2
                 assert layout.alt_tile_bytes(d, vb, kb) % 16 == 0
@@ -210,10 +210,12 @@ def test_vllm_metal_compression_table_reading():
     assert layout.alt_bytes_per_token_head(128) == 194
     for vb in (2, 3, 4):
         assert layout.alt_bytes_per_token_head(128, vb) == (8 * 128 / 8 + 16) + (vb * 128 / 8 + 8) - 6
-    # ... and for the table's 4-bit keys (q4_0 / q3_0)
-    row = [r for r in golden("vllm_metal_compression.json")["rows"] if r["k_quant"] == "q4_0"][0]
-    per = row["k_bits"] * 128 / 8 + 16 + row["v_bits"] * 128 / 8 + 8
-    assert layout.alt_bytes_per_token_head(128, row["v_bits"], row["k_bits"]) == per - 6
+    # ... and for the table's other key formats (q5_0, q4_0 and uint2 keys with q3_0 values)
+    rows = {r["k_quant"]: r for r in golden("vllm_metal_compression.json")["rows"]}
+    for name in ("q5_0", "q4_0", "uint2"):
+        row = rows[name]
+        per = row["k_bits"] * 128 / 8 + 16 + row["v_bits"] * 128 / 8 + 8
+        assert layout.alt_bytes_per_token_head(128, row["v_bits"], row["k_bits"]) == per - 6
 
 
 def test_ring_split():

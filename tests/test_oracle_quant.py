@@ -30,7 +30,7 @@ def _brute_group_codes(x16, group, levels):
     return out
 
 
-@pytest.mark.parametrize("levels", [3, 15, 255])
+@pytest.mark.parametrize("levels", [3, 15, 31, 255])
 def test_group_quant_brute_force(levels):
     g = np.random.default_rng(levels)
     x = (g.standard_normal((6, 64)) * g.lognormal(size=(6, 1))).astype(np.float16)
