@@ -61,6 +61,12 @@ WORKLOADS = {
     # the alternate layout with 4-bit keys (q4_0 keys + 3-bit values: the guide's low-memory option)
     "alt-d128-k4": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=128, ctx=65536, shuffled=False, seed=0,
                         kbits=4),
+    # 5-bit keys (q5_0 keys + 3-bit values: the guide's next step down in memory)
+    "alt-d128-k5": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=128, ctx=65536, shuffled=False, seed=0,
+                        kbits=5),
+    # 2-bit keys (uint2 keys + 3-bit values: the guide's aggressive row)
+    "alt-d128-k2": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=128, ctx=65536, shuffled=False, seed=0,
+                        kbits=2),
 }
 DEFAULT_WORKLOAD = "qwen3-0.6b-32k"
 

@@ -487,7 +487,9 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
       float acc[NR];
 #pragma unroll
       for (int h = 0; h < NR; ++h) acc[h] = 0.f;
-      const uint8_t* kq = tile + tok * (kb * D / 8);  // the token's key codes (bytes or nibbles)
+      const uint8_t* kq = tile + tok * (kb * D / 8);  // the token's key codes (a kb-bit stream)
+      const uint32_t* kw = reinterpret_cast<const uint32_t*>(kq);
+      const uint32_t kmask = (1u << kb) - 1u;
       // D/8 dims per thread, inside whole 32-blocks or half of one
       constexpr int SEG = D / 8 < 32 ? D / 8 : 32;
 #pragma unroll
@@ -500,7 +502,15 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
 #pragma unroll 8
         for (int k = 0; k < SEG; ++k) {
           const int i = dim0 + k;
-          const float cv = kb == 8 ? (float)kq[i] : (float)((kq[i >> 1] >> (4 * (i & 1))) & 15);
+          float cv;
+          if (kb == 8) {
+            cv = (float)kq[i];
+          } else {
+            const int kbit = kb * i;
+            const uint32_t klo = kw[kbit >> 5];
+            const uint32_t khi = (kbit & 31) + kb > 32 ? kw[(kbit >> 5) + 1] : 0u;
+            cv = (float)(__funnelshift_r(klo, khi, kbit & 31) & kmask);
+          }
 #pragma unroll
           for (int h = 0; h < NR; ++h) part_acc[h] = fmaf(qf[h][dim0 + k], cv, part_acc[h]);
         }

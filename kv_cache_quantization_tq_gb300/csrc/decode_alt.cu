@@ -1,6 +1,7 @@
 // Alternate-layout decode attention, one warp per page (CUDA cores).
 //
-// Keys are 8- or 4-bit affine codes per block of 32 (no rotation), values are
+// Keys are 8-, 5-, 4- or 2-bit affine codes per block of 32 (no rotation; the vllm-metal
+// TurboQuant guide's q8_0 / q5_0 / q4_0 / uint2 key formats), values are
 // VB-bit (2, 3 or 4) Lloyd-Max indices of the rotated unit value with an fp16
 // norm (vllm-metal TurboQuant guide, quantisation table: q2_0 .. q4_0 values).  With one query head per
 // KV head the work per byte is small, so the kernel is written to stream the
@@ -11,8 +12,12 @@
 //   The block dots <q_b, code_b> of a page are one small dense product on the
 //   tensor cores (mma.sync m16n8k16): rows = the 16 tokens, k = coordinates,
 //   columns = (query head, block of 32) with B holding q restricted to the
-//   block.  Codes enter as the exact fp16 value 1024 + code (one byte-permute
-//   per pair), the 1024 sum(q_b) offset is removed per block in fp32.  The key
+//   block.  8- and 4-bit codes enter as the exact fp16 value 1024 + code (one
+//   byte-permute or two bit selects per pair), the 1024 sum(q_b) offset is
+//   removed per block in fp32; 5- and 2-bit codes enter as 1 + code 2^-kb (the
+//   code in the top mantissa bits), so only sum(q_b) is removed and the product
+//   is scaled by 2^kb: with few levels, a 1024 offset would cancel most of the
+//   fp32 accumulator's bits.  The key
 //   rows are XOR-swizzled by 16-byte chunk as they are copied in, so the
 //   fragment loads are free of bank conflicts.  Scores then move to lane
 //   l = token l/2 for the softmax and value steps;
@@ -106,8 +111,35 @@ __device__ __forceinline__ uint32_t nib_pair_hi(uint32_t w) {
   return ((w >> 8) & 0xFu) | ((w << 4) & 0xF0000u) | 0x64006400u;
 }
 
+// 2-bit key codes: the four codes of w's low byte (coordinates 4t .. 4t+3) as the fp16 pairs
+// (1 + c0/4, 1 + c1/4) and (1 + c2/4, 1 + c3/4).
+__device__ __forceinline__ uint32_t q2_pair_lo(uint32_t w) {
+  return ((w << 8) & 0x300u) | ((w << 22) & 0x3000000u) | 0x3C003C00u;
+}
+__device__ __forceinline__ uint32_t q2_pair_hi(uint32_t w) {
+  return ((w << 4) & 0x300u) | ((w << 18) & 0x3000000u) | 0x3C003C00u;
+}
+// 5-bit key codes: the four codes in bits 0..19 of x as (1 + c0/32, 1 + c1/32) and
+// (1 + c2/32, 1 + c3/32).
+__device__ __forceinline__ uint32_t q5_pair_lo(uint32_t x) {
+  return ((x << 5) & 0x3E0u) | ((x << 16) & 0x3E00000u) | 0x3C003C00u;
+}
+__device__ __forceinline__ uint32_t q5_pair_hi(uint32_t x) {
+  return ((x >> 5) & 0x3E0u) | ((x << 6) & 0x3E00000u) | 0x3C003C00u;
+}
+
+// How KB-bit codes enter the score product: as offset + code / scale, so that
+// sum(code q) = scale (dot - offset sum(q)).
+template <int KB>
+struct KeyEntry {
+  static constexpr bool kBiased = KB == 8 || KB == 4;  // 1024 + code
+  static constexpr float kOffset = kBiased ? 1024.f : 1.f;
+  static constexpr float kScale = kBiased ? 1.f : (float)(1 << KB);
+};
+
 template <int D, int NR, int VB, int KB>
 __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
+  static_assert(KB == 8 || KB == 5 || KB == 4 || KB == 2, "key code widths");
   using C = AltCfg<D, VB, KB>;
   constexpr int NC = 1 << VB;  // centroids
   constexpr int E = C::E;
@@ -233,8 +265,10 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
 #pragma unroll
       for (int r = 0; r < 4; ++r) cacc[j][r] = 0.f;
     {
-      const uint8_t* r0 = T + g * (KB * D / 8) + KB * t / 2;  // coordinate 4t of the row
-      const uint8_t* r1 = T + (g + 8) * (KB * D / 8) + KB * t / 2;
+      const uint8_t* r0 = T + g * (KB * D / 8) + (KB * t) / 2;  // coordinate 4t of the row (KB != 5)
+      const uint8_t* r1 = T + (g + 8) * (KB * D / 8) + (KB * t) / 2;
+      const uint32_t* w0r = reinterpret_cast<const uint32_t*>(T + g * (KB * D / 8));  // 5-bit rows
+      const uint32_t* w1r = reinterpret_cast<const uint32_t*>(T + (g + 8) * (KB * D / 8));
       const int sw0 = kq_swizzle<D>(g), sw1 = kq_swizzle<D>(g + 8);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
@@ -246,13 +280,29 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
           A.y = __byte_perm(w1, 0x64646464u, 0x4140u);  // row g + 8
           A.z = __byte_perm(w0, 0x64646464u, 0x4342u);  // row g: coordinates 4t+2, 4t+3
           A.w = __byte_perm(w1, 0x64646464u, 0x4342u);
-        } else {  // 4-bit keys: the four codes of coordinates 16 ks + 4t .. + 3 are 16 bits of the row
+        } else if (KB == 4) {  // the four codes of coordinates 16 ks + 4t .. + 3 are 16 bits of the row
           const uint32_t w0 = *reinterpret_cast<const uint16_t*>(r0 + 8 * ks);
           const uint32_t w1 = *reinterpret_cast<const uint16_t*>(r1 + 8 * ks);
           A.x = nib_pair_lo(w0);
           A.y = nib_pair_lo(w1);
           A.z = nib_pair_hi(w0);
           A.w = nib_pair_hi(w1);
+        } else if (KB == 2) {  // ... 8 bits of the row
+          const uint32_t w0 = r0[4 * ks];
+          const uint32_t w1 = r1[4 * ks];
+          A.x = q2_pair_lo(w0);
+          A.y = q2_pair_lo(w1);
+          A.z = q2_pair_hi(w0);
+          A.w = q2_pair_hi(w1);
+        } else {  // 5 bits: 20 bits of the row from bit 80 ks + 20 t, across at most two words
+          const int bit = 80 * ks + 20 * t, wi = bit >> 5, sh = bit & 31;
+          const bool two = sh + 20 > 32;
+          const uint32_t x0 = __funnelshift_r(w0r[wi], two ? w0r[wi + 1] : 0u, sh);
+          const uint32_t x1 = __funnelshift_r(w1r[wi], two ? w1r[wi + 1] : 0u, sh);
+          A.x = q5_pair_lo(x0);
+          A.y = q5_pair_lo(x1);
+          A.z = q5_pair_hi(x0);
+          A.w = q5_pair_hi(x1);
         }
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
@@ -277,8 +327,11 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
             const float2 s0 = __half22float2(ksm2[g * G + blk]);
             const float2 s1 = __half22float2(ksm2[(g + 8) * G + blk]);
             const float qb = qsc[j][u];
-            p0 = fmaf(s0.x, fmaf(-1024.f, qb, cacc[j][u]), fmaf(s0.y, qb, p0));
-            p1 = fmaf(s1.x, fmaf(-1024.f, qb, cacc[j][2 + u]), fmaf(s1.y, qb, p1));
+            using KE = KeyEntry<KB>;
+            const float sc0 = KE::kBiased ? s0.x : s0.x * KE::kScale;
+            const float sc1 = KE::kBiased ? s1.x : s1.x * KE::kScale;
+            p0 = fmaf(sc0, fmaf(-KE::kOffset, qb, cacc[j][u]), fmaf(s0.y, qb, p0));
+            p1 = fmaf(sc1, fmaf(-KE::kOffset, qb, cacc[j][2 + u]), fmaf(s1.y, qb, p1));
           }
         }
       p0 += __shfl_xor_sync(kFull, p0, 1);
@@ -389,7 +442,12 @@ cudaError_t launch_alt_kb(const AltArgs& a, int vb, dim3 grid, cudaStream_t s) {
 
 template <int D, int NR>
 cudaError_t launch_alt(const AltArgs& a, int vb, int kb, dim3 grid, cudaStream_t s) {
-  return kb == 4 ? launch_alt_kb<D, NR, 4>(a, vb, grid, s) : launch_alt_kb<D, NR, 8>(a, vb, grid, s);
+  switch (kb) {
+    case 2: return launch_alt_kb<D, NR, 2>(a, vb, grid, s);
+    case 4: return launch_alt_kb<D, NR, 4>(a, vb, grid, s);
+    case 5: return launch_alt_kb<D, NR, 5>(a, vb, grid, s);
+    default: return launch_alt_kb<D, NR, 8>(a, vb, grid, s);
+  }
 }
 
 }  // namespace

@@ -279,8 +279,17 @@ __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
     for (int e = 0; e < E; ++e) {
       const int c = coord_of(e, lane);
       const __half2 smn = *reinterpret_cast<const __half2*>(tile + o_ksm + (slot * (D / 32) + e) * 4);
-      // key code: a byte (8-bit keys) or nibble c of the token's 4-bit stream
-      const int kq = kb == 8 ? tile[slot * D + c] : (tile[slot * (D / 2) + (c >> 1)] >> (4 * (c & 1))) & 15;
+      // key code: a byte (8-bit keys) or code c of the token's little-endian kb-bit stream
+      int kq;
+      if (kb == 8) {
+        kq = tile[slot * D + c];
+      } else {
+        const uint32_t* kw = reinterpret_cast<const uint32_t*>(tile + slot * (kb * D / 8));
+        const int kbit = kb * c;
+        const uint32_t klo = kw[kbit >> 5];
+        const uint32_t khi = (kbit & 31) + kb > 32 ? kw[(kbit >> 5) + 1] : 0u;
+        kq = (int)(__funnelshift_r(klo, khi, kbit & 31) & ((1u << kb) - 1u));
+      }
       a.k_out[row + c] = __float2half_rn(fmaf(__low2float(smn), (float)kq, __high2float(smn)));
       const int bit = vb * c;  // index c of the token's little-endian vb-bit stream
       const uint32_t lo = vi[bit >> 5];

@@ -303,10 +303,10 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
 }
 
 // ------------------------------------------------------------------ alternate layout
-// Alternate-layout page: a dense kb-bit stream of key codes per token (8 bits: one byte per
-// coordinate), 16 x d/32 (scale, minimum) fp16 pairs, a dense vb-bit stream of value indices per
-// token (index i at bit vb i), 16 fp16 value norms: (2 kb + 2 + 2 vb) d + 32 bytes.  Shared
-// memory is sized for the largest (kb = 8, vb = 4).
+// Alternate-layout page: a dense kb-bit stream of key codes per token (kb = 8, 5, 4 or 2; 8 bits:
+// one byte per coordinate), 16 x d/32 (scale, minimum) fp16 pairs, a dense vb-bit stream of value
+// indices per token (index i at bit vb i), 16 fp16 value norms: (2 kb + 2 + 2 vb) d + 32 bytes.
+// The function attribute allows the largest staging (kb = 5, vb = 4).
 __host__ __device__ constexpr int alt_tile_bytes(int d, int kb, int vb) { return (2 * kb + 2 + 2 * vb) * d + 32; }
 template <int D>
 struct AltEnc {
@@ -317,7 +317,8 @@ struct AltEnc {
   static constexpr size_t smem(int kb, int vb) {
     return (size_t)(TB / 16) * alt_tile_bytes(D, kb, vb) + (size_t)TB * D + (kb == 8 ? 0 : (size_t)TB * D);
   }
-  static constexpr size_t SMEM = smem(4, 4) > smem(8, 4) ? smem(4, 4) : smem(8, 4);  // the largest
+  static constexpr size_t SMEM = smem(5, 4) > smem(8, 4) ? smem(5, 4) : smem(8, 4);  // the largest
+  static_assert(smem(5, 4) >= smem(4, 4) && smem(5, 4) >= smem(2, 4), "kb = 5 bounds the packed-key widths");
 };
 
 // Codes of every staged token as a dense little-endian VB-bit stream at byte `offset` of its page
@@ -408,9 +409,14 @@ __device__ void encode_alt_block_vb(const EncArgs& a, int b, int h, int tok0, in
     if (lane == 0) reinterpret_cast<__half*>(tile + o_vn)[slot] = __float2half_rn(nv);
   }
   __syncthreads();
-  // dense vb-bit stream per token: 32 indices -> vb words; 4-bit keys likewise
+  // dense vb-bit stream per token: 32 indices -> vb words; keys below 8 bits likewise (kb words)
   pack_value_stream<D, VB>(vcodes, tiles, tile_bytes, ntok, o_vi);
-  if (kb == 4) pack_value_stream<D, 4>(kcodes, tiles, tile_bytes, ntok, 0);
+  if (kb == 4)
+    pack_value_stream<D, 4>(kcodes, tiles, tile_bytes, ntok, 0);
+  else if (kb == 5)
+    pack_value_stream<D, 5>(kcodes, tiles, tile_bytes, ntok, 0);
+  else if (kb == 2)
+    pack_value_stream<D, 2>(kcodes, tiles, tile_bytes, ntok, 0);
   __syncthreads();
   store_tiles(a, tiles, tile_bytes, tile_bytes, ntok >> 4, b, h, (start + tok0) >> 4);
 }

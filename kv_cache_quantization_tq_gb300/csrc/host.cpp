@@ -134,7 +134,9 @@ tq_status check_config(const tq_config* c) {
         c->qjl_m != c->head_dim)
       return TQ_ERR_UNSUPPORTED;
   } else if (c->layout == TQ_LAYOUT_ALT) {
-    if ((c->key_bits != 8 && c->key_bits != 4) || c->value_bits < 2 || c->value_bits > 4) return TQ_ERR_UNSUPPORTED;
+    const int kb = c->key_bits;
+    if ((kb != 8 && kb != 5 && kb != 4 && kb != 2) || c->value_bits < 2 || c->value_bits > 4)
+      return TQ_ERR_UNSUPPORTED;
   } else {
     return TQ_ERR_INVALID_ARG;
   }

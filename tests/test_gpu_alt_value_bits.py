@@ -1,6 +1,6 @@
-"""Alternate layout with 2- or 4-bit value indices, and with 4-bit keys, on the GPU (vllm-metal
-TurboQuant guide, quantisation table: q2_0 / q4_0 values, q4_0 keys; 8-bit keys with 4-bit values is
-its K8+V4 mix).
+"""Alternate layout with 2- or 4-bit value indices, and with 5-, 4- or 2-bit keys, on the GPU
+(vllm-metal TurboQuant guide, quantisation table: q2_0 / q4_0 values, q5_0 / q4_0 / uint2 keys; 8-bit
+keys with 4-bit values is its K8+V4 mix).
 
 The same parity bar as the 3-bit default: key bytes bit-exact against the oracle's encoder, value
 indices equal away from decision boundaries, value norms within one fp16 ulp, decode within
@@ -105,38 +105,43 @@ def test_dense_history(d, vb):
         assert _untouched(k_out, b, L)
 
 
-# ---- 4-bit keys (q4_0: 15-step affine codes per block of 32, a nibble stream per token)
+# ---- keys below 8 bits (q5_0 / q4_0 / uint2: 31-, 15- or 3-step affine codes per block of 32, a
+# dense kb-bit stream per token)
+@pytest.mark.parametrize("kb", [5, 4, 2])
 @pytest.mark.parametrize("vb", [3, 4])
 @pytest.mark.parametrize("d", [64, 128, 512])
-def test_encode_parity_4bit_keys(d, vb):
-    hkv, n_tok, starts, seed = 2, 96, [0, 32], 90 + d + vb
-    ctx, c, s, _ = make_ctx(tq, False, d, hkv, hkv, seed, value_bits=vb, key_bits=4)
-    assert ctx.bytes_per_token_head == d // 2 + 4 * (d // 32) + vb * d // 8 + 2
-    assert ctx.page_bytes == layout.alt_tile_bytes(d, vb, 4)
+def test_encode_parity_low_bit_keys(d, vb, kb):
+    hkv, n_tok, starts, seed = 2, 96, [0, 32], 90 + d + vb + 7 * kb
+    ctx, c, s, _ = make_ctx(tq, False, d, hkv, hkv, seed, value_bits=vb, key_bits=kb)
+    assert ctx.bytes_per_token_head == kb * d // 8 + 4 * (d // 32) + vb * d // 8 + 2
+    assert ctx.page_bytes == layout.alt_tile_bytes(d, vb, kb)
     k, v = synth.kv_alt(seed, 2, hkv, n_tok, d)
     max_blocks = 10
     bt = synth.block_table(seed, 2, max_blocks, True)
-    pool_o = np.zeros((2 * max_blocks, hkv, layout.alt_tile_bytes(d, vb, 4)), np.uint8)
+    pool_o = np.zeros((2 * max_blocks, hkv, layout.alt_tile_bytes(d, vb, kb)), np.uint8)
     encs = [cache.encode_alt_range(pool_o, bt[b:b + 1], starts[b], k[b:b + 1], v[b:b + 1], s, c) for b in range(2)]
     pool_g = torch.zeros(pool_o.shape, dtype=torch.uint8, device="cuda")
     ctx.encode_flush(to_dev(k), to_dev(v), to_dev(np.array(starts, np.int32)), to_dev(bt), pool_g)
     pool_g = pool_g.cpu().numpy()
     assert ctx.device_errors() == 0
     blocks = tile_index(bt, starts, n_tok)
-    fo = alt_fields(pool_o[blocks], d, 4)
-    fg = alt_fields(pool_g[blocks], d, 4)
-    assert np.array_equal(fg["k_bytes"], fo["k_bytes"])  # affine 4-bit keys and their scales: bit-exact
+    fo = alt_fields(pool_o[blocks], d, kb)
+    fg = alt_fields(pool_g[blocks], d, kb)
+    assert np.array_equal(fg["k_bytes"], fo["k_bytes"])  # affine key codes and their scales: bit-exact
     assert np.max(np.abs(fg["vn"].astype(np.int32) - fo["vn"].astype(np.int32))) <= 1
     y = np.stack([e["y"][0] for e in encs]).reshape(2, hkv, n_tok // 16, 16, d).transpose(0, 2, 1, 3, 4)
     assert not ((fg["vidx"] != fo["vidx"]) & ~near_boundary(y, c)).any()
+    kq = layout.unpack_alt_tiles(pool_g[blocks], d, vb)["kq"]
+    assert kq.max() == (1 << kb) - 1  # the top code is reached: the stream width is used
 
 
-@pytest.mark.parametrize("d,n_rep", [(64, 1), (128, 2), (256, 1), (512, 1), (128, 8)])
-def test_decode_parity_4bit_keys(d, n_rep):
-    seed, hkv, vb = 100 + d + n_rep, 2, 3
+@pytest.mark.parametrize("kb", [5, 4, 2])
+@pytest.mark.parametrize("d,n_rep", [(64, 1), (128, 2), (256, 1), (512, 1), (128, 4), (128, 8)])
+def test_decode_parity_low_bit_keys(d, n_rep, kb):
+    seed, hkv, vb = 100 + d + n_rep + 7 * kb, 2, 3
     hq = hkv * n_rep
-    ctx, c, s, _ = make_ctx(tq, False, d, hq, hkv, seed, value_bits=vb, key_bits=4)
-    e = build_alt_cache(seed, d, hkv, [544, 96], c, s, key_bits=4)
+    ctx, c, s, _ = make_ctx(tq, False, d, hq, hkv, seed, value_bits=vb, key_bits=kb)
+    e = build_alt_cache(seed, d, hkv, [544, 96], c, s, key_bits=kb)
     q = synth.queries(seed, 2, hq, d)
     out = torch.empty((2, hq, d), dtype=torch.float32, device="cuda")
     ws = torch.empty(ctx.workspace_size(2, e["max_ctx"]), dtype=torch.uint8, device="cuda")
@@ -149,12 +154,13 @@ def test_decode_parity_4bit_keys(d, n_rep):
     assert ok, f"max abs err {maxerr}, {nbad} bad"
 
 
+@pytest.mark.parametrize("kb", [5, 4, 2])
 @pytest.mark.parametrize("d", [64, 256])
-def test_dense_history_4bit_keys(d):
-    seed, hkv, vb = 110 + d, 2, 3
-    ctx, c, s, _ = make_ctx(tq, False, d, hkv, hkv, seed, value_bits=vb, key_bits=4)
+def test_dense_history_low_bit_keys(d, kb):
+    seed, hkv, vb = 110 + d + 7 * kb, 2, 3
+    ctx, c, s, _ = make_ctx(tq, False, d, hkv, hkv, seed, value_bits=vb, key_bits=kb)
     lengths = [320, 48]
-    e = build_alt_cache(seed, d, hkv, lengths, c, s, key_bits=4)
+    e = build_alt_cache(seed, d, hkv, lengths, c, s, key_bits=kb)
     max_tokens = 336
     k_out, v_out = _outputs(len(lengths), hkv, max_tokens, d)
     ctx.dequantize(to_dev(e["pool"]), to_dev(e["bt"]), to_dev(e["n_c"]), k_out, v_out)
