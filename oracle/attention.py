@@ -128,7 +128,7 @@ def decode_alt(q16, pool, block_table, n_c, ring_k, ring_v, n_buf, signs, centro
             logits = []
             vals = []
             if nc:
-                khat = quant.group_dequant(f["kq"][g], f["ks"][g], f["kmn"][g], 32)
+                khat = quant.alt_keys({key: val[g] for key, val in f.items()})
                 logits.append(q @ khat.T / np.sqrt(d))
                 vals.append(quant.dequant_alt_values(f["vidx"][g], f["n_v"][g], signs, centroids3))
             kr, vr = _ring(ring_k, ring_v, b, g, nb) if nb else (None, None)

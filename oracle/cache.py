@@ -67,7 +67,8 @@ def value_bits_of(centroids) -> int:
 
 def encode_alt_range(pool, block_table, start, k16, v16, signs, centroids3):
     """Alternate layout: encode fp16 k/v [B, Hkv, T, d] into ``pool`` (value bits from the codebook
-    size: 4, 8 or 16 centroids; key bits from the pool's tile size: 8 or 4)."""
+    size: 4, 8 or 16 centroids; key bits from the pool's tile size: 8, 5, 4, 2, or 16 for fp16
+    keys)."""
     k16 = np.asarray(k16, dtype=np.float16)
     bsz, hkv, t, d = k16.shape
     assert start % layout.P == 0 and t % layout.P == 0
@@ -78,8 +79,8 @@ def encode_alt_range(pool, block_table, start, k16, v16, signs, centroids3):
     npg = t // layout.P
     tiles = layout.pack_alt_tiles(
         kq.reshape(bsz, hkv, npg, 16, d),
-        ks.reshape(bsz, hkv, npg, 16, d // 32),
-        kmn.reshape(bsz, hkv, npg, 16, d // 32),
+        None if ks is None else ks.reshape(bsz, hkv, npg, 16, d // 32),
+        None if kmn is None else kmn.reshape(bsz, hkv, npg, 16, d // 32),
         venc["idx"].reshape(bsz, hkv, npg, 16, d),
         venc["n_v"].reshape(bsz, hkv, npg, 16),
         vb,
@@ -153,7 +154,7 @@ def materialize_alt(pool, block_table, b, n_c, ring_k, ring_v, n_buf, signs, cen
     for g in range(hkv):
         kk, vv = [], []
         if n_c:
-            kk.append(quant.group_dequant(f["kq"][g], f["ks"][g], f["kmn"][g], 32))
+            kk.append(quant.alt_keys({key: val[g] for key, val in f.items()}))
             vv.append(quant.dequant_alt_values(f["vidx"][g], f["n_v"][g], signs, centroids3))
         if n_buf:
             kk.append(np.asarray(ring_k[b, g, :n_buf], np.float64))

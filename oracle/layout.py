@@ -39,6 +39,10 @@ Alternate layout tile, 24 d + 32 bytes = 16 x (1.5 d + 2):
     16d      2d     KSM per token and 32-block: fp16 scale, fp16 minimum
     18d      6d     VI  3-bit value indices, per token a 3d/8-byte generic stream
     24d      32     VN  fp16 value norm per token
+
+  With fp16 keys (kbits 16: keys kept exact and only the values quantised,
+  the V-only mode of the "TurboQuant-MLX overview") KQ is 32d bytes of fp16
+  keys and there is no KSM plane: 16 x (2d + vbits d/8 + 2) bytes.
 """
 from __future__ import annotations
 
@@ -242,11 +246,17 @@ def unpack_main_tiles(tiles: np.ndarray, d: int, kbits: int = None) -> dict:
 
 
 # ---------------------------------------------------------------- alternate layout
+def alt_key_plane_bytes(d: int, kbits: int = 8) -> int:
+    """Key bytes of one alternate-layout page: the code streams and their (scale, minimum) pairs,
+    or the fp16 keys alone (kbits 16)."""
+    return 32 * d if kbits == 16 else 2 * kbits * d + 2 * d
+
+
 def alt_tile_bytes(d: int, vbits: int = 3, kbits: int = 8) -> int:
     """One page of the alternate layout: 16 x (a dense kbits-bit stream of key codes (bytes for 8
     bits) + d/32 fp16 (scale, minimum) pairs + a dense vbits-bit stream of value indices + one fp16
-    value norm)."""
-    return 2 * kbits * d + 2 * d + 2 * vbits * d + 32
+    value norm); with kbits 16, 16 x (d fp16 keys + the value stream + the norm)."""
+    return alt_key_plane_bytes(d, kbits) + 2 * vbits * d + 32
 
 
 def alt_bytes_per_token_head(d: int, vbits: int = 3, kbits: int = 8) -> float:
@@ -255,37 +265,45 @@ def alt_bytes_per_token_head(d: int, vbits: int = 3, kbits: int = 8) -> float:
 
 def alt_value_bits(tile_bytes: int, d: int, kbits: int = 8) -> int:
     """Value bits of an alternate-layout tile from its size and key bits."""
-    vb, rem = divmod(tile_bytes - (2 * kbits + 2) * d - 32, 2 * d)
+    vb, rem = divmod(tile_bytes - alt_key_plane_bytes(d, kbits) - 32, 2 * d)
     assert rem == 0 and vb in (2, 3, 4), (tile_bytes, d, kbits)
     return vb
 
 
 def alt_key_bits(tile_bytes: int, d: int, vbits: int) -> int:
     """Key bits of an alternate-layout tile from its size and value bits."""
-    kb, rem = divmod(tile_bytes - (2 + 2 * vbits) * d - 32, 2 * d)
+    key = tile_bytes - 2 * vbits * d - 32
+    if key == 32 * d:
+        return 16
+    kb, rem = divmod(key - 2 * d, 2 * d)
     assert rem == 0 and kb in (2, 4, 5, 8), (tile_bytes, d, vbits)
     return kb
 
 
 def pack_alt_tiles(kq, ks16, kmn16, vidx, nv16, vbits: int = 3, kbits: int = 8) -> np.ndarray:
-    """kq [..., 16, d] (kbits-bit codes); ks16/kmn16 [..., 16, d/32]; vidx [..., 16, d] (vbits-bit);
-    nv16 [..., 16]."""
-    kq = np.asarray(kq, dtype=np.uint8)
-    d = kq.shape[-1]
-    lead = kq.shape[:-2]
-    kqb = pack_rows(kq, kbits).reshape(lead + (16 * kbits * d // 8,))
-    sm = np.stack([np.asarray(ks16, np.float16), np.asarray(kmn16, np.float16)], axis=-1)
-    ksm = _f16_bytes(sm.reshape(lead + (16 * (d // 32) * 2,)))
+    """kq [..., 16, d] (kbits-bit codes, or the fp16 keys for kbits 16); ks16/kmn16 [..., 16, d/32]
+    (unused for kbits 16); vidx [..., 16, d] (vbits-bit); nv16 [..., 16]."""
+    vidx = np.asarray(vidx, dtype=np.uint8)
+    d = vidx.shape[-1]
+    lead = vidx.shape[:-2]
+    if kbits == 16:
+        keys = [_f16_bytes(np.asarray(kq, np.float16).reshape(lead + (16 * d,)))]
+    else:
+        kq = np.asarray(kq, dtype=np.uint8)
+        kqb = pack_rows(kq, kbits).reshape(lead + (16 * kbits * d // 8,))
+        sm = np.stack([np.asarray(ks16, np.float16), np.asarray(kmn16, np.float16)], axis=-1)
+        keys = [kqb, _f16_bytes(sm.reshape(lead + (16 * (d // 32) * 2,)))]
     vi = pack_rows(vidx, vbits).reshape(lead + (16 * vbits * d // 8,))
     vn = _f16_bytes(nv16)
-    out = np.concatenate([kqb, ksm, vi, vn], axis=-1)
+    out = np.concatenate(keys + [vi, vn], axis=-1)
     assert out.shape[-1] == alt_tile_bytes(d, vbits, kbits)
     return out
 
 
 def unpack_alt_tiles(tiles: np.ndarray, d: int, vbits: int = None) -> dict:
     """Fields of alternate-layout tiles.  Without vbits the keys are taken as 8-bit and the value
-    bits are read off the size; with vbits (the codebook's) the key bits are read off the size."""
+    bits are read off the size; with vbits (the codebook's) the key bits are read off the size.
+    Tiles with fp16 keys give the field "k16" in place of "kq", "ks" and "kmn"."""
     t = np.asarray(tiles, dtype=np.uint8)
     lead = t.shape[:-1]
     g = d // 32
@@ -293,13 +311,16 @@ def unpack_alt_tiles(tiles: np.ndarray, d: int, vbits: int = None) -> dict:
         kb, vb = 8, alt_value_bits(t.shape[-1], d)
     else:
         kb, vb = alt_key_bits(t.shape[-1], d, vbits), vbits
-    o_sm = 2 * kb * d
-    o_vi = o_sm + 2 * d
+    o_vi = alt_key_plane_bytes(d, kb)
     o_n = o_vi + 2 * vb * d
-    kq = unpack_rows(t[..., :o_sm].reshape(lead + (16, kb * d // 8)), d, kb)
-    sm = np.ascontiguousarray(t[..., o_sm:o_vi]).view("<f2").reshape(lead + (16, g, 2))
     vi = unpack_rows(t[..., o_vi:o_n].reshape(lead + (16, vb * d // 8)), d, vb)
     nv = np.ascontiguousarray(t[..., o_n:o_n + 32]).view("<f2")
+    if kb == 16:
+        k16 = np.ascontiguousarray(t[..., :o_vi]).view("<f2").reshape(lead + (16, d))
+        return {"k16": k16.astype(np.float16), "vidx": vi, "n_v": nv.astype(np.float16)}
+    o_sm = 2 * kb * d
+    kq = unpack_rows(t[..., :o_sm].reshape(lead + (16, kb * d // 8)), d, kb)
+    sm = np.ascontiguousarray(t[..., o_sm:o_vi]).view("<f2").reshape(lead + (16, g, 2))
     return {
         "kq": kq.copy(),
         "ks": sm[..., 0].astype(np.float16),

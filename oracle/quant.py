@@ -144,8 +144,19 @@ def dequant_keys(enc: dict, signs: np.ndarray, centroids: np.ndarray, s_mat: np.
 
 
 def encode_alt_keys(k16: np.ndarray, block: int = 32, bits: int = 8):
-    """Alternate-layout keys: bits-bit affine codes per block of 32 (2^bits - 1 steps)."""
+    """Alternate-layout keys: bits-bit affine codes per block of 32 (2^bits - 1 steps).  With 16
+    bits the keys stay as they are (fp16): only the values are quantised (the V-only mode of the
+    "TurboQuant-MLX overview", usage paths)."""
+    if bits == 16:
+        return np.asarray(k16, dtype=np.float16), None, None
     return group_quant(k16, block, (1 << bits) - 1)
+
+
+def alt_keys(fields) -> np.ndarray:
+    """Keys of unpacked alternate-layout tiles in float64: the fp16 keys, or mn + s q."""
+    if "k16" in fields:
+        return np.asarray(fields["k16"], dtype=np.float64)
+    return group_dequant(fields["kq"], fields["ks"], fields["kmn"], 32)
 
 
 def encode_alt_values(v16: np.ndarray, signs: np.ndarray, centroids: np.ndarray):

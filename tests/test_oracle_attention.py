@@ -101,6 +101,28 @@ def test_alt_layout_decode_matches_torch_sdpa_on_dequantised_cache(vbits, kbits)
     assert np.allclose(out, ref.numpy(), atol=1e-10)
 
 
+@pytest.mark.parametrize("vbits", [2, 3, 4])
+def test_alt_layout_fp16_keys_decode_matches_torch_sdpa(vbits):
+    # keys kept as fp16, values rotated and Lloyd-Max quantised ("TurboQuant-MLX overview", usage
+    # paths: the V-only cache): the logits are the exact q k / sqrt(d) of the fp16 keys
+    d, hkv, n_rep = 64, 2, 2
+    sg = rng.signs(7, d)
+    c, _ = codebook.lloyd_max(d, vbits)
+    k, v = synth.kv_alt(7, 1, hkv, 96, d)
+    bt = synth.block_table(7, 1, 6, True)
+    pool = np.zeros((6, hkv, layout.alt_tile_bytes(d, vbits, 16)), np.uint8)
+    cache.encode_alt_range(pool, bt, 0, k, v, sg, c)
+    q = synth.queries(7, 1, hkv * n_rep, d)
+    out = attention.decode_alt(q, pool, bt, np.array([96]), None, None, None, sg, c, hkv)
+    venc = quant.encode_alt_values(v, sg, c)
+    vhat = quant.dequant_alt_values(venc["idx"], venc["n_v"], sg, c)
+    kk = torch.tensor(k.astype(np.float64)).repeat_interleave(n_rep, dim=1)
+    vv = torch.tensor(vhat).repeat_interleave(n_rep, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.tensor(q.astype(np.float64))[:, :, None, :], kk, vv)[:, :, 0, :]
+    assert np.allclose(out, ref.numpy(), atol=1e-10)
+
+
 def test_empty_and_zero_key_cases():
     e = _setup_main(6, 2, 1, 2, 64, [1, 130])
     # zero a compressed key: its logit becomes exactly 0

@@ -169,6 +169,26 @@ def test_alt_tile_round_trip(d, vbits, kbits):
     assert np.array_equal(t[0, o_n:o_n + 32].view("<f2"), f["n_v"][0])
 
 
+@pytest.mark.parametrize("d", [64, 512])
+@pytest.mark.parametrize("vbits", [2, 3, 4])
+def test_alt_tile_round_trip_fp16_keys(d, vbits):
+    # keys kept as fp16 (only the values quantised): 2d key bytes per token, no scale/minimum plane
+    g = np.random.default_rng(d + vbits)
+    k16 = g.standard_normal((2, 16, d)).astype(np.float16)
+    vidx = g.integers(0, 1 << vbits, (2, 16, d), dtype=np.uint8)
+    nv = g.standard_normal((2, 16)).astype(np.float16)
+    t = layout.pack_alt_tiles(k16, None, None, vidx, nv, vbits, 16)
+    assert t.shape == (2, 32 * d + 2 * vbits * d + 32) == (2, layout.alt_tile_bytes(d, vbits, 16))
+    assert layout.alt_key_bits(t.shape[-1], d, vbits) == 16
+    assert np.array_equal(t[1, 3 * 2 * d:4 * 2 * d].view("<f2"), k16[1, 3])  # token 3's keys, little-endian
+    back = layout.unpack_alt_tiles(t, d, vbits)
+    assert set(back) == {"k16", "vidx", "n_v"}
+    assert np.array_equal(back["k16"].view(np.uint16), k16.view(np.uint16))
+    assert np.array_equal(back["vidx"], vidx) and np.array_equal(back["n_v"].view(np.uint16), nv.view(np.uint16))
+    # the value stream starts right after the keys
+    assert np.array_equal(t[0, 32 * d:32 * d + vbits * d // 8], _pack_bigint(vidx[0, 0], vbits))
+
+
 def test_bytes_per_token_closed_form():
     assert layout.main_bytes_per_token_head(128) == 100
     # 4-bit values: 48 bytes of key bits, 64 of value codes, 16 of group scale/minimum, 4 of norms
@@ -185,6 +205,9 @@ def test_bytes_per_token_closed_form():
                 assert layout.alt_tile_bytes(d, vb, kb) % 16 == 0
                 assert layout.alt_key_bits(layout.alt_tile_bytes(d, vb, kb), d, vb) == kb
             assert layout.alt_value_bits(layout.alt_tile_bytes(d, vb), d) == vb
+            # fp16 keys: 2d bytes per token, then the value indices and the norm
+            assert layout.alt_bytes_per_token_head(d, vb, 16) == 2 * d + vb * d / 8 + 2
+            assert layout.alt_value_bits(layout.alt_tile_bytes(d, vb, 16), d, 16) == vb
 
 
 def test_memory_table_of_the_benchmark_page():

@@ -75,6 +75,21 @@ def test_alt_materialised_history_reproduces_the_decode(vbits, kbits):
         assert np.all(np.abs(kk.reshape(hkv, L, d // 32, 32) - k0) <= step[..., None] * (0.5 + 2e-3) + 1e-6)
 
 
+def test_alt_materialised_fp16_keys_are_the_inputs():
+    seed, d, hkv, vbits = 9, 64, 2, 3
+    sg = rng.signs(seed, d)
+    c3, _ = codebook.lloyd_max(d, vbits)
+    k, v = synth.kv_alt(seed, 1, hkv, 64, d)
+    bt = synth.block_table(seed, 1, 4, True)
+    pool = np.zeros((4, hkv, layout.alt_tile_bytes(d, vbits, 16)), np.uint8)
+    cache.encode_alt_range(pool, bt, 0, k, v, sg, c3)
+    kk, vv = cache.materialize_alt(pool, bt, 0, 64, None, None, 0, sg, c3, d)
+    assert np.array_equal(kk, k[0].astype(np.float64))  # no key quantisation at all
+    q = synth.queries(seed, 1, hkv, d)
+    ref = attention.decode_alt(q, pool, bt, np.array([64]), None, None, None, sg, c3, hkv)
+    assert np.allclose(_attend(q[0], kk, vv, hkv), ref[0], rtol=0, atol=1e-12)
+
+
 def test_main_layout_with_4bit_values():
     # the same pins with 4-bit value codes (15 levels per group of 32)
     seed, d, hkv, n_rep = 6, 64, 2, 2
