@@ -67,6 +67,9 @@ WORKLOADS = {
     # 2-bit keys (uint2 keys + 3-bit values: the guide's aggressive row)
     "alt-d128-k2": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=128, ctx=65536, shuffled=False, seed=0,
                         kbits=2),
+    # fp16 keys, 3-bit values (the V-only cache)
+    "alt-d128-vonly": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=128, ctx=65536, shuffled=False, seed=0,
+                           kbits=16),
 }
 DEFAULT_WORKLOAD = "qwen3-0.6b-32k"
 
@@ -83,8 +86,9 @@ def record_bytes(w) -> int:
     d = w["d"]
     if w["layout"] == "main":
         return (3 * d) // 8 + (w.get("vbits", 2) * d) // 8 + d // 8 + 4
-    # key codes, block (scale, min), value indices, norm
-    return (w.get("kbits", 8) * d) // 8 + 4 * (d // 32) + (w.get("vbits", 3) * d) // 8 + 2
+    # key codes, block (scale, min), value indices, norm; fp16 keys (16 bits) have no (scale, min)
+    kb = w.get("kbits", 8)
+    return (kb * d) // 8 + (0 if kb == 16 else 4 * (d // 32)) + (w.get("vbits", 3) * d) // 8 + 2
 
 
 def step_bytes(w, lengths_after_append):

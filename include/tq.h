@@ -91,7 +91,9 @@ typedef struct {
   int key_bits;      /* main: 3 (2-bit Lloyd-Max + 1-bit QJL, default), 2 or 4 (1- or 3-bit
                         Lloyd-Max + 1-bit QJL; turboquant vLLM guide, --key-bits); alt: 8
                         (default), 5, 4 or 2 bits per affine key code (the vllm-metal guide's
-                        q8_0 / q5_0 / q4_0 / uint2 key formats) */
+                        q8_0 / q5_0 / q4_0 / uint2 key formats), or 16: keys kept as fp16 and
+                        only the values quantised (the V-only cache of the TurboQuant-MLX
+                        overview) */
   int value_bits;    /* main: 2 (default) or 4 (turboquant vLLM guide, --value-bits); alt: 3
                         (default), 2 or 4 Lloyd-Max index bits per value coordinate (the
                         vllm-metal guide's q2_0 .. q4_0 value formats; 8 + 4 is its K8+V4) */

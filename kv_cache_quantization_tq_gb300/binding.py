@@ -191,7 +191,7 @@ class Context:
         if value_bits is not None:
             self.cfg.value_bits = value_bits  # main layout: 2 or 4; alternate layout: 2, 3 or 4
         if key_bits is not None:
-            self.cfg.key_bits = key_bits  # main layout: 3, 2 or 4; alternate layout: 8, 5, 4 or 2
+            self.cfg.key_bits = key_bits  # main layout: 3, 2 or 4; alternate layout: 8, 5, 4, 2 or 16 (fp16 keys)
         ptr = C.c_void_p()
         if centroids is None:
             _check(lib.tq_create(C.byref(self.cfg), C.byref(ptr)), "tq_create")

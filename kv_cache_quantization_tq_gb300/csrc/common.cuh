@@ -22,6 +22,12 @@ constexpr unsigned kFull = 0xffffffffu;
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int coord_of(int e, int lane) { return 32 * e + 2 * (lane & 15) + (lane >> 4); }
 
+// Alternate-layout page of 16 tokens: the key bytes (a kb-bit code stream per token and 16 x d/32
+// fp16 (scale, minimum) pairs, or with kb = 16 the fp16 keys themselves and no pairs), a dense
+// vb-bit stream of value indices per token, 16 fp16 value norms.
+__host__ __device__ constexpr int alt_key_bytes(int d, int kb) { return kb == 16 ? 32 * d : (2 * kb + 2) * d; }
+__host__ __device__ constexpr int alt_tile_bytes(int d, int kb, int vb) { return alt_key_bytes(d, kb) + 2 * vb * d + 32; }
+
 // Sylvester Walsh-Hadamard transform (unnormalised) of a warp-distributed
 // vector, y_i = sum_j (-1)^popcount(i & j) x_j.  Index bit 0 is lane bit 4,
 // index bits 1..4 are lane bits 0..3, index bits >= 5 are the element index.

@@ -407,15 +407,14 @@ __global__ void __launch_bounds__(128) decode_main_kernel(DecArgs a) {
 // ------------------------------------------------------------------ alternate layout
 template <int D, int NR>
 __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
-  // page: (2 kb + 2 + 2 vb) D + 32 bytes for kb-bit key codes and vb-bit value indices; the
-  // staging buffer fits kb = 8, vb = 4
-  constexpr int TILE_MAX = 26 * D + 32;
+  // page: alt_tile_bytes(D, kb, vb) for kb-bit key codes (or fp16 keys) and vb-bit value
+  // indices, staged in dynamic shared memory
   constexpr int G = D / 32;
   constexpr int DPT = (D + 127) / 128;
   constexpr int E = D / 32;
   __shared__ float qf[NR][D];
   __shared__ float qsum[NR][G];
-  __shared__ __align__(16) uint8_t tile[TILE_MAX];
+  extern __shared__ __align__(16) uint8_t tile[];
   __shared__ float sc[NR][16];
   __shared__ float pbuf[16][NR];
   __shared__ float ob[NR][D];
@@ -466,11 +465,11 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
   }
 
   const float scale = rsqrtf((float)D) * kLog2e;
-  const int vb = a.avb, kb = a.kb, TILE = (2 * kb + 2 + 2 * vb) * D + 32;
+  const int vb = a.avb, kb = a.kb, TILE = alt_tile_bytes(D, kb, vb);
   const uint32_t vmask = (1u << vb) - 1u;
-  const __half* ksm = reinterpret_cast<const __half*>(tile + 2 * kb * D);
-  const uint32_t* vi = reinterpret_cast<const uint32_t*>(tile + 2 * kb * D + 2 * D);
-  const __half* vn = reinterpret_cast<const __half*>(tile + 2 * kb * D + 2 * D + 2 * vb * D);
+  const __half* ksm = reinterpret_cast<const __half*>(tile + 2 * kb * D);  // (scale, minimum); none for fp16 keys
+  const uint32_t* vi = reinterpret_cast<const uint32_t*>(tile + alt_key_bytes(D, kb));
+  const __half* vn = reinterpret_cast<const __half*>(tile + alt_key_bytes(D, kb) + 2 * vb * D);
 
   for (int t0 = tbeg; t0 < tend; t0 += kPage) {
     const int page = t0 >> 4;
@@ -487,7 +486,8 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
       float acc[NR];
 #pragma unroll
       for (int h = 0; h < NR; ++h) acc[h] = 0.f;
-      const uint8_t* kq = tile + tok * (kb * D / 8);  // the token's key codes (a kb-bit stream)
+      const uint8_t* kq = tile + tok * (kb * D / 8);  // the token's key codes (a kb-bit stream) or fp16 keys
+      const __half* kh = reinterpret_cast<const __half*>(kq);
       const uint32_t* kw = reinterpret_cast<const uint32_t*>(kq);
       const uint32_t kmask = (1u << kb) - 1u;
       // D/8 dims per thread, inside whole 32-blocks or half of one
@@ -503,7 +503,9 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
         for (int k = 0; k < SEG; ++k) {
           const int i = dim0 + k;
           float cv;
-          if (kb == 8) {
+          if (kb == 16) {
+            cv = __half2float(kh[i]);
+          } else if (kb == 8) {
             cv = (float)kq[i];
           } else {
             const int kbit = kb * i;
@@ -514,8 +516,8 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
 #pragma unroll
           for (int h = 0; h < NR; ++h) part_acc[h] = fmaf(qf[h][dim0 + k], cv, part_acc[h]);
         }
-        const float s = __half2float(ksm[(tok * G + g) * 2]);
-        const float mn = __half2float(ksm[(tok * G + g) * 2 + 1]);
+        const float s = kb == 16 ? 1.f : __half2float(ksm[(tok * G + g) * 2]);
+        const float mn = kb == 16 ? 0.f : __half2float(ksm[(tok * G + g) * 2 + 1]);
         float qs[NR];
         if (SEG == 32) {
 #pragma unroll
@@ -662,7 +664,10 @@ template <int D, int NR>
 cudaError_t launch_tpl(const DecArgs& a, int vb, dim3 grid, cudaStream_t s) {
   if (vb == 4) return launch_main_vb<D, NR, 4>(a, grid, s);
   if (vb == 2) return launch_main_vb<D, NR, 2>(a, grid, s);
-  decode_alt_kernel<D, NR><<<grid, 128, 0, s>>>(a);
+  auto kern = decode_alt_kernel<D, NR>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, alt_tile_bytes(D, 16, 4));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 128, alt_tile_bytes(D, a.kb, a.avb), s>>>(a);
   return cudaGetLastError();
 }
 

@@ -1,7 +1,8 @@
 // Alternate-layout decode attention, one warp per page (CUDA cores).
 //
 // Keys are 8-, 5-, 4- or 2-bit affine codes per block of 32 (no rotation; the vllm-metal
-// TurboQuant guide's q8_0 / q5_0 / q4_0 / uint2 key formats), values are
+// TurboQuant guide's q8_0 / q5_0 / q4_0 / uint2 key formats) or the fp16 keys themselves (the
+// V-only cache of the "TurboQuant-MLX overview", usage paths), values are
 // VB-bit (2, 3 or 4) Lloyd-Max indices of the rotated unit value with an fp16
 // norm (vllm-metal TurboQuant guide, quantisation table: q2_0 .. q4_0 values).  With one query head per
 // KV head the work per byte is small, so the kernel is written to stream the
@@ -17,7 +18,7 @@
 //   removed per block in fp32; 5- and 2-bit codes enter as 1 + code 2^-kb (the
 //   code in the top mantissa bits), so only sum(q_b) is removed and the product
 //   is scaled by 2^kb: with few levels, a 1024 offset would cancel most of the
-//   fp32 accumulator's bits.  The key
+//   fp32 accumulator's bits.  fp16 keys are the A operand as they are.  The key
 //   rows are XOR-swizzled by 16-byte chunk as they are copied in, so the
 //   fragment loads are free of bank conflicts.  Scores then move to lane
 //   l = token l/2 for the softmax and value steps;
@@ -81,7 +82,8 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint4& a, uint32_t 
 template <int D, int VB, int KB>
 struct AltCfg {
   static constexpr int E = D / 32;      // dimensions per lane
-  static constexpr int TILE = (2 * KB + 2 + 2 * VB) * D + 32;  // KB-bit key codes, VB-bit value indices
+  static constexpr int KEYB = alt_key_bytes(D, KB);  // KB-bit key codes and (scale, minimum), or fp16 keys
+  static constexpr int TILE = alt_tile_bytes(D, KB, VB);
   static constexpr int STAGES = TILE <= 3200 ? 4 : (TILE <= 6400 ? 3 : 2);
   static constexpr size_t SMEM = (size_t)kWarps * STAGES * TILE;
 };
@@ -103,6 +105,7 @@ template <int D>
 __device__ __forceinline__ int kq_swizzle(int row) {
   return D == 64 ? ((row >> 1) & 3) : (row & 7);
 }
+// fp16 key rows (D/8 >= 8 chunks each): chunk c of row r sits at chunk c ^ (r & 7).
 
 // 4-bit key codes: the nibbles n0..n3 of w (coordinates 4t .. 4t+3) as the fp16 pairs
 // (1024 + n0, 1024 + n1) and (1024 + n2, 1024 + n3).
@@ -139,7 +142,7 @@ struct KeyEntry {
 
 template <int D, int NR, int VB, int KB>
 __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
-  static_assert(KB == 8 || KB == 5 || KB == 4 || KB == 2, "key code widths");
+  static_assert(KB == 16 || KB == 8 || KB == 5 || KB == 4 || KB == 2, "key widths");
   using C = AltCfg<D, VB, KB>;
   constexpr int NC = 1 << VB;  // centroids
   constexpr int E = C::E;
@@ -232,6 +235,9 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
           if (KB == 8 && c < D) {  // 8-bit key rows: 16 rows x D/16 chunks, swizzled
             const int row = c / (D / 16), ch = c % (D / 16);
             cd = row * (D / 16) + (ch ^ kq_swizzle<D>(row));
+          } else if (KB == 16 && c < 2 * D) {  // fp16 key rows: 16 rows x D/8 chunks, swizzled
+            const int row = c / (D / 8), ch = c % (D / 8);
+            cd = row * (D / 8) + (ch ^ (row & 7));
           }
           cp16(dst + cd * 16, src + c * 16);
         }
@@ -255,9 +261,9 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
       continue;
     }
     const uint8_t* T = wst + (k % C::STAGES) * C::TILE;
-    const __half2* ksm2 = reinterpret_cast<const __half2*>(T + 2 * KB * D);
-    const uint32_t* vi = reinterpret_cast<const uint32_t*>(T + (2 * KB + 2) * D);
-    const __half* vn = reinterpret_cast<const __half*>(T + (2 * KB + 2 + 2 * VB) * D);
+    const __half2* ksm2 = reinterpret_cast<const __half2*>(T + 2 * KB * D);  // not read for fp16 keys
+    const uint32_t* vi = reinterpret_cast<const uint32_t*>(T + C::KEYB);
+    const __half* vn = reinterpret_cast<const __half*>(T + C::KEYB + 2 * VB * D);
     // C[token][column] = sum over the column's block of (1024 + code) q_head
     float cacc[NT][4];
 #pragma unroll
@@ -273,7 +279,15 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         uint4 A;
-        if (KB == 8) {
+        if (KB == 16) {  // coordinates 16 ks + 4t .. + 3: 8 bytes of chunk 2 ks + t/2 (swizzled)
+          const int ch = 2 * ks + (t >> 1);
+          const uint2 k0 = *reinterpret_cast<const uint2*>(T + g * (2 * D) + 16 * (ch ^ (g & 7)) + 8 * (t & 1));
+          const uint2 k1 = *reinterpret_cast<const uint2*>(T + (g + 8) * (2 * D) + 16 * (ch ^ (g & 7)) + 8 * (t & 1));
+          A.x = k0.x;
+          A.y = k1.x;
+          A.z = k0.y;
+          A.w = k1.y;
+        } else if (KB == 8) {
           const uint32_t w0 = *reinterpret_cast<const uint32_t*>(r0 + 16 * (ks ^ sw0));
           const uint32_t w1 = *reinterpret_cast<const uint32_t*>(r1 + 16 * (ks ^ sw1));
           A.x = __byte_perm(w0, 0x64646464u, 0x4140u);  // row g: coordinates 4t, 4t+1 as 1024 + code
@@ -322,7 +336,10 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int n = 8 * j + 2 * t + u;
-          if (n < NR * G && n / G == h) {
+          if (n < NR * G && n / G == h && KB == 16) {  // the block dots of fp16 keys are the score
+            p0 += cacc[j][u];
+            p1 += cacc[j][2 + u];
+          } else if (n < NR * G && n / G == h) {
             const int blk = n % G;
             const float2 s0 = __half22float2(ksm2[g * G + blk]);
             const float2 s1 = __half22float2(ksm2[(g + 8) * G + blk]);
@@ -443,6 +460,7 @@ cudaError_t launch_alt_kb(const AltArgs& a, int vb, dim3 grid, cudaStream_t s) {
 template <int D, int NR>
 cudaError_t launch_alt(const AltArgs& a, int vb, int kb, dim3 grid, cudaStream_t s) {
   switch (kb) {
+    case 16: return launch_alt_kb<D, NR, 16>(a, vb, grid, s);
     case 2: return launch_alt_kb<D, NR, 2>(a, vb, grid, s);
     case 4: return launch_alt_kb<D, NR, 4>(a, vb, grid, s);
     case 5: return launch_alt_kb<D, NR, 5>(a, vb, grid, s);

@@ -234,16 +234,35 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
 }
 
 // ------------------------------------------------------------------ alternate layout
-// Alternate-layout page: (2 kb + 2 + 2 vb) d + 32 bytes for kb-bit key codes and vb-bit value
-// indices (staging sized for kb = 8, vb = 4).
+// Alternate-layout page: alt_tile_bytes(d, kb, vb) for kb-bit key codes (or fp16 keys) and vb-bit
+// value indices (staging sized for fp16 keys and vb = 4).
 template <int D>
 struct AltDq {
   static constexpr int E = D / 32;
   static constexpr int TB = 32;
-  static constexpr int TILE_MAX = 26 * D + 32;
+  static constexpr int TILE_MAX = alt_tile_bytes(D, 16, 4);
   static constexpr int THREADS = 256;
   static constexpr size_t SMEM = (size_t)(TB / 16) * TILE_MAX;
 };
+
+// Key coordinate c of token `slot` of a staged alternate-layout page: the fp16 key itself (kb 16),
+// or mn + s code with the code a byte (kb 8) or taken from the token's little-endian kb-bit stream.
+template <int D>
+__device__ __forceinline__ __half alt_key(const uint8_t* tile, int o_ksm, int slot, int c, int kb) {
+  if (kb == 16) return reinterpret_cast<const __half*>(tile)[slot * D + c];
+  const __half2 smn = *reinterpret_cast<const __half2*>(tile + o_ksm + (slot * (D / 32) + (c >> 5)) * 4);
+  int kq;
+  if (kb == 8) {
+    kq = tile[slot * D + c];
+  } else {
+    const uint32_t* kw = reinterpret_cast<const uint32_t*>(tile + slot * (kb * D / 8));
+    const int kbit = kb * c;
+    const uint32_t klo = kw[kbit >> 5];
+    const uint32_t khi = (kbit & 31) + kb > 32 ? kw[(kbit >> 5) + 1] : 0u;
+    kq = (int)(__funnelshift_r(klo, khi, kbit & 31) & ((1u << kb) - 1u));
+  }
+  return __float2half_rn(fmaf(__low2float(smn), (float)kq, __high2float(smn)));
+}
 
 template <int D>
 __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
@@ -257,8 +276,8 @@ __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
   const int n = dq_ntok(a, b);
   if (tok0 >= n) return;
   const int ntok = min(C::TB, n - tok0);
-  const int vb = a.avb, kb = a.kb, tile_bytes = (2 * kb + 2 + 2 * vb) * D + 32;
-  const int o_ksm = 2 * kb * D, o_vi = o_ksm + 2 * D, o_vn = o_vi + 2 * vb * D;
+  const int vb = a.avb, kb = a.kb, tile_bytes = alt_tile_bytes(D, kb, vb);
+  const int o_ksm = 2 * kb * D, o_vi = alt_key_bytes(D, kb), o_vn = o_vi + 2 * vb * D;
   const uint32_t mask = (1u << vb) - 1u;
   if (threadIdx.x < 16) lut[threadIdx.x] = a.tab.c[threadIdx.x & mask];
   load_tiles(a, smem, tile_bytes, tile_bytes, b, h, tok0 >> 4, ntok >> 4, ok);  // ends with __syncthreads
@@ -278,19 +297,7 @@ __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int c = coord_of(e, lane);
-      const __half2 smn = *reinterpret_cast<const __half2*>(tile + o_ksm + (slot * (D / 32) + e) * 4);
-      // key code: a byte (8-bit keys) or code c of the token's little-endian kb-bit stream
-      int kq;
-      if (kb == 8) {
-        kq = tile[slot * D + c];
-      } else {
-        const uint32_t* kw = reinterpret_cast<const uint32_t*>(tile + slot * (kb * D / 8));
-        const int kbit = kb * c;
-        const uint32_t klo = kw[kbit >> 5];
-        const uint32_t khi = (kbit & 31) + kb > 32 ? kw[(kbit >> 5) + 1] : 0u;
-        kq = (int)(__funnelshift_r(klo, khi, kbit & 31) & ((1u << kb) - 1u));
-      }
-      a.k_out[row + c] = __float2half_rn(fmaf(__low2float(smn), (float)kq, __high2float(smn)));
+      a.k_out[row + c] = alt_key<D>(tile, o_ksm, slot, c, kb);
       const int bit = vb * c;  // index c of the token's little-endian vb-bit stream
       const uint32_t lo = vi[bit >> 5];
       const uint32_t hi = (bit & 31) + vb > 32 ? vi[(bit >> 5) + 1] : 0u;

@@ -303,11 +303,10 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
 }
 
 // ------------------------------------------------------------------ alternate layout
-// Alternate-layout page: a dense kb-bit stream of key codes per token (kb = 8, 5, 4 or 2; 8 bits:
-// one byte per coordinate), 16 x d/32 (scale, minimum) fp16 pairs, a dense vb-bit stream of value
-// indices per token (index i at bit vb i), 16 fp16 value norms: (2 kb + 2 + 2 vb) d + 32 bytes.
-// The function attribute allows the largest staging (kb = 5, vb = 4).
-__host__ __device__ constexpr int alt_tile_bytes(int d, int kb, int vb) { return (2 * kb + 2 + 2 * vb) * d + 32; }
+// Alternate-layout page (alt_tile_bytes): a dense kb-bit stream of key codes per token (kb = 8, 5,
+// 4 or 2; 8 bits: one byte per coordinate) and 16 x d/32 (scale, minimum) fp16 pairs, or the fp16
+// keys (kb = 16); a dense vb-bit stream of value indices per token (index i at bit vb i); 16 fp16
+// value norms.  The function attribute allows the largest staging (kb = 16, vb = 4).
 template <int D>
 struct AltEnc {
   static constexpr int E = D / 32;
@@ -315,10 +314,12 @@ struct AltEnc {
   static constexpr int THREADS = 256;
   // staged tiles, value codes, and (keys below 8 bits) key codes before packing
   static constexpr size_t smem(int kb, int vb) {
-    return (size_t)(TB / 16) * alt_tile_bytes(D, kb, vb) + (size_t)TB * D + (kb == 8 ? 0 : (size_t)TB * D);
+    return (size_t)(TB / 16) * alt_tile_bytes(D, kb, vb) + (size_t)TB * D + (kb == 8 || kb == 16 ? 0 : (size_t)TB * D);
   }
-  static constexpr size_t SMEM = smem(5, 4) > smem(8, 4) ? smem(5, 4) : smem(8, 4);  // the largest
-  static_assert(smem(5, 4) >= smem(4, 4) && smem(5, 4) >= smem(2, 4), "kb = 5 bounds the packed-key widths");
+  static constexpr size_t SMEM = smem(16, 4);  // the largest
+  static_assert(smem(16, 4) >= smem(8, 4) && smem(16, 4) >= smem(5, 4) && smem(16, 4) >= smem(4, 4) &&
+                    smem(16, 4) >= smem(2, 4),
+                "fp16 keys bound the staging");
 };
 
 // Codes of every staged token as a dense little-endian VB-bit stream at byte `offset` of its page
@@ -351,7 +352,7 @@ __device__ void encode_alt_block_vb(const EncArgs& a, int b, int h, int tok0, in
   constexpr int E = C::E;
   constexpr int vb = VB, nbound = (1 << VB) - 1;
   const int kb = a.kb, tile_bytes = alt_tile_bytes(D, kb, vb);
-  const int o_ksm = 2 * kb * D, o_vi = o_ksm + 2 * D, o_vn = o_vi + 2 * vb * D;
+  const int o_ksm = 2 * kb * D, o_vi = alt_key_bytes(D, kb), o_vn = o_vi + 2 * vb * D;
   uint8_t* tiles = smem;
   uint8_t* vcodes = smem + (size_t)(C::TB / 16) * tile_bytes;
   uint8_t* kcodes = vcodes + C::TB * D;  // keys below 8 bits: staged, then packed
@@ -374,19 +375,25 @@ __device__ void encode_alt_block_vb(const EncArgs& a, int b, int h, int tok0, in
       kx[e] = __half2float(kp[c]);
       vv[e] = __half2float(vp[c]);
     }
-    group_minmax<E>(kx, kmn, kmx);
+    if (kb == 16) {  // keys kept as they are: the fp16 inputs (exact through fp32)
+      __half* kh = reinterpret_cast<__half*>(tile) + slot * D;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int c = coord_of(e, lane);
-      GroupCode g = group_quant_mm(kx[e], kmn[e], kmx[e], (float)((1 << kb) - 1));
-      if (kb == 8)
-        tile[slot * D + c] = (uint8_t)g.q;
-      else
-        kcodes[tt * D + c] = (uint8_t)g.q;
-      if (lane == 0) {
-        __half* sm = reinterpret_cast<__half*>(tile + o_ksm + (slot * (D / 32) + e) * 4);
-        sm[0] = g.s;
-        sm[1] = g.mn;
+      for (int e = 0; e < E; ++e) kh[coord_of(e, lane)] = __float2half_rn(kx[e]);
+    } else {
+      group_minmax<E>(kx, kmn, kmx);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int c = coord_of(e, lane);
+        GroupCode g = group_quant_mm(kx[e], kmn[e], kmx[e], (float)((1 << kb) - 1));
+        if (kb == 8)
+          tile[slot * D + c] = (uint8_t)g.q;
+        else
+          kcodes[tt * D + c] = (uint8_t)g.q;
+        if (lane == 0) {
+          __half* sm = reinterpret_cast<__half*>(tile + o_ksm + (slot * (D / 32) + e) * 4);
+          sm[0] = g.s;
+          sm[1] = g.mn;
+        }
       }
     }
     float ss = 0.f;

@@ -135,7 +135,7 @@ tq_status check_config(const tq_config* c) {
       return TQ_ERR_UNSUPPORTED;
   } else if (c->layout == TQ_LAYOUT_ALT) {
     const int kb = c->key_bits;
-    if ((kb != 8 && kb != 5 && kb != 4 && kb != 2) || c->value_bits < 2 || c->value_bits > 4)
+    if ((kb != 16 && kb != 8 && kb != 5 && kb != 4 && kb != 2) || c->value_bits < 2 || c->value_bits > 4)
       return TQ_ERR_UNSUPPORTED;
   } else {
     return TQ_ERR_INVALID_ARG;
@@ -400,12 +400,12 @@ size_t tq_bytes_per_token_head(const tq_ctx* ctx) {
   if (!ctx) return 0;
   const size_t d = ctx->cfg.head_dim;
   // main: key_bits key bits, value_bits value bits and one fp16 scale + minimum per group of 32 per
-  // coordinate, two fp16 norms; alternate: key_bits-bit key codes + 4 B per block of 32,
-  // value_bits-bit value indices, fp16 norm
+  // coordinate, two fp16 norms; alternate: key_bits-bit key codes + 4 B per block of 32 (or fp16
+  // keys alone, key_bits 16), value_bits-bit value indices, fp16 norm
   const size_t vb = ctx->cfg.value_bits;
   const size_t kb = ctx->cfg.key_bits;
   return ctx->cfg.layout == TQ_LAYOUT_MAIN ? (kb * d) / 8 + (vb * d) / 8 + d / 8 + 4
-                                           : (kb * d) / 8 + (d / 32) * 4 + (vb * d) / 8 + 2;
+                                           : (kb * d) / 8 + (kb == 16 ? 0 : (d / 32) * 4) + (vb * d) / 8 + 2;
 }
 
 size_t tq_page_bytes(const tq_ctx* ctx) { return tq::kPage * tq_bytes_per_token_head(ctx); }

@@ -71,18 +71,18 @@ def main_fields(tiles, d, kb=None):
 
 
 def alt_fields(tiles, d, kb=8):
-    """Fields of alternate-layout tiles with kb-bit keys (value bits vb from the size
-    (2 kb + 2 + 2 vb) d + 32)."""
+    """Fields of alternate-layout tiles with kb-bit keys, or fp16 keys for kb = 16 (value bits vb
+    from the size: key bytes + 2 vb d + 32)."""
     t = np.ascontiguousarray(tiles)
     lead = t.shape[:-1]
-    o_vi = (2 * kb + 2) * d
+    o_vi = 32 * d if kb == 16 else (2 * kb + 2) * d
     vb = (t.shape[-1] - o_vi - 32) // (2 * d)
     o_n = o_vi + 2 * vb * d
     vi = t[..., o_vi:o_n].reshape(lead + (16, vb * d // 8))
     bits = np.unpackbits(vi, axis=-1, bitorder="little").reshape(lead + (16, d, vb)).astype(np.uint8)
     idx = sum(bits[..., i].astype(np.int32) << i for i in range(vb)).astype(np.uint8)
     return {
-        "k_bytes": t[..., :o_vi],  # key codes and their (scale, minimum) pairs
+        "k_bytes": t[..., :o_vi],  # key codes and their (scale, minimum) pairs, or fp16 keys
         "vidx": idx,
         "vn": np.ascontiguousarray(t[..., o_n:o_n + 32]).view("<i2"),
     }

@@ -1,6 +1,7 @@
-"""Alternate layout with 2- or 4-bit value indices, and with 5-, 4- or 2-bit keys, on the GPU
-(vllm-metal TurboQuant guide, quantisation table: q2_0 / q4_0 values, q5_0 / q4_0 / uint2 keys; 8-bit
-keys with 4-bit values is its K8+V4 mix).
+"""Alternate layout with 2- or 4-bit value indices, and with 5-, 4- or 2-bit keys or fp16 keys, on
+the GPU (vllm-metal TurboQuant guide, quantisation table: q2_0 / q4_0 values, q5_0 / q4_0 / uint2
+keys; 8-bit keys with 4-bit values is its K8+V4 mix; fp16 keys are the V-only cache of the
+"TurboQuant-MLX overview").
 
 The same parity bar as the 3-bit default: key bytes bit-exact against the oracle's encoder, value
 indices equal away from decision boundaries, value norms within one fp16 ulp, decode within
@@ -135,7 +136,7 @@ def test_encode_parity_low_bit_keys(d, vb, kb):
     assert kq.max() == (1 << kb) - 1  # the top code is reached: the stream width is used
 
 
-@pytest.mark.parametrize("kb", [5, 4, 2])
+@pytest.mark.parametrize("kb", [5, 4, 2, 16])
 @pytest.mark.parametrize("d,n_rep", [(64, 1), (128, 2), (256, 1), (512, 1), (128, 4), (128, 8)])
 def test_decode_parity_low_bit_keys(d, n_rep, kb):
     seed, hkv, vb = 100 + d + n_rep + 7 * kb, 2, 3
@@ -154,7 +155,7 @@ def test_decode_parity_low_bit_keys(d, n_rep, kb):
     assert ok, f"max abs err {maxerr}, {nbad} bad"
 
 
-@pytest.mark.parametrize("kb", [5, 4, 2])
+@pytest.mark.parametrize("kb", [5, 4, 2, 16])
 @pytest.mark.parametrize("d", [64, 256])
 def test_dense_history_low_bit_keys(d, kb):
     seed, hkv, vb = 110 + d + 7 * kb, 2, 3
@@ -172,3 +173,31 @@ def test_dense_history_low_bit_keys(d, kb):
         _check_close(kg[b, :, :L], kr, f"keys b={b}")
         _check_close(vg[b, :, :L], vr, f"values b={b}")
         assert _untouched(k_out, b, L)
+
+
+# ---- fp16 keys, quantised values only (the V-only cache)
+@pytest.mark.parametrize("vb", [2, 3, 4])
+@pytest.mark.parametrize("d", [64, 128, 512])
+def test_encode_parity_fp16_keys(d, vb):
+    hkv, n_tok, starts, seed = 2, 96, [0, 32], 120 + d + vb
+    ctx, c, s, _ = make_ctx(tq, False, d, hkv, hkv, seed, value_bits=vb, key_bits=16)
+    assert ctx.bytes_per_token_head == 2 * d + vb * d // 8 + 2
+    assert ctx.page_bytes == layout.alt_tile_bytes(d, vb, 16)
+    k, v = synth.kv_alt(seed, 2, hkv, n_tok, d)
+    max_blocks = 10
+    bt = synth.block_table(seed, 2, max_blocks, True)
+    pool_o = np.zeros((2 * max_blocks, hkv, layout.alt_tile_bytes(d, vb, 16)), np.uint8)
+    encs = [cache.encode_alt_range(pool_o, bt[b:b + 1], starts[b], k[b:b + 1], v[b:b + 1], s, c) for b in range(2)]
+    pool_g = torch.zeros(pool_o.shape, dtype=torch.uint8, device="cuda")
+    ctx.encode_flush(to_dev(k), to_dev(v), to_dev(np.array(starts, np.int32)), to_dev(bt), pool_g)
+    pool_g = pool_g.cpu().numpy()
+    assert ctx.device_errors() == 0
+    blocks = tile_index(bt, starts, n_tok)
+    fo = alt_fields(pool_o[blocks], d, 16)
+    fg = alt_fields(pool_g[blocks], d, 16)
+    assert np.array_equal(fg["k_bytes"], fo["k_bytes"])  # the fp16 keys, bit for bit
+    k16 = layout.unpack_alt_tiles(pool_g[blocks], d, vb)["k16"]
+    assert np.array_equal(k16[0, 0, 0].view(np.uint16), k[0, 0, :16].view(np.uint16))
+    assert np.max(np.abs(fg["vn"].astype(np.int32) - fo["vn"].astype(np.int32))) <= 1
+    y = np.stack([e["y"][0] for e in encs]).reshape(2, hkv, n_tok // 16, 16, d).transpose(0, 2, 1, 3, 4)
+    assert not ((fg["vidx"] != fo["vidx"]) & ~near_boundary(y, c)).any()
