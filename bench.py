@@ -130,6 +130,7 @@ NCU_TRAFFIC = {
     ("qwen3-0.6b-32k", "tc_decode_kernel"): 13254144,     # profiles/tc_decode_kernel__qwen3-0.6b-32k.md
     ("qwen2.5-7b-b8", "tc_decode_kernel"): 109436928,     # profiles/tc_decode_kernel__qwen2.5-7b-b8.md
     ("alt-d128", "decode_alt_v2_kernel"): 412128768,      # profiles/decode_alt_v2_kernel__alt-d128.md
+    ("alt-d128-vonly", "decode_alt_v2_kernel"): 647770624,  # profiles/decode_alt_v2_kernel__alt-d128-vonly.md
 }
 
 

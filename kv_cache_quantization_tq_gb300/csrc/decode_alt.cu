@@ -105,7 +105,9 @@ template <int D>
 __device__ __forceinline__ int kq_swizzle(int row) {
   return D == 64 ? ((row >> 1) & 3) : (row & 7);
 }
-// fp16 key rows (D/8 >= 8 chunks each): chunk c of row r sits at chunk c ^ (r & 7).
+// fp16 key rows (D/8 >= 8 chunks each): chunk c of row r sits at chunk c ^ 2 (r & 3).  A half-warp's
+// 8-byte fragment loads (rows g..g+3, chunks 2 ks and 2 ks + 1) then land in 8 distinct chunk slots.
+__device__ __forceinline__ int kh_swizzle(int row) { return 2 * (row & 3); }
 
 // 4-bit key codes: the nibbles n0..n3 of w (coordinates 4t .. 4t+3) as the fp16 pairs
 // (1024 + n0, 1024 + n1) and (1024 + n2, 1024 + n3).
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
             cd = row * (D / 16) + (ch ^ kq_swizzle<D>(row));
           } else if (KB == 16 && c < 2 * D) {  // fp16 key rows: 16 rows x D/8 chunks, swizzled
             const int row = c / (D / 8), ch = c % (D / 8);
-            cd = row * (D / 8) + (ch ^ (row & 7));
+            cd = row * (D / 8) + (ch ^ kh_swizzle(row));
           }
           cp16(dst + cd * 16, src + c * 16);
         }
@@ -281,8 +283,9 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
         uint4 A;
         if (KB == 16) {  // coordinates 16 ks + 4t .. + 3: 8 bytes of chunk 2 ks + t/2 (swizzled)
           const int ch = 2 * ks + (t >> 1);
-          const uint2 k0 = *reinterpret_cast<const uint2*>(T + g * (2 * D) + 16 * (ch ^ (g & 7)) + 8 * (t & 1));
-          const uint2 k1 = *reinterpret_cast<const uint2*>(T + (g + 8) * (2 * D) + 16 * (ch ^ (g & 7)) + 8 * (t & 1));
+          const uint2 k0 = *reinterpret_cast<const uint2*>(T + g * (2 * D) + 16 * (ch ^ kh_swizzle(g)) + 8 * (t & 1));
+          const uint2 k1 =
+              *reinterpret_cast<const uint2*>(T + (g + 8) * (2 * D) + 16 * (ch ^ kh_swizzle(g + 8)) + 8 * (t & 1));
           A.x = k0.x;
           A.y = k1.x;
           A.z = k0.y;
