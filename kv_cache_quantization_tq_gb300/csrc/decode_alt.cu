@@ -88,8 +88,6 @@ struct AltCfg {
   static constexpr size_t SMEM = (size_t)kWarps * STAGES * TILE;
 };
 
-// 16-byte chunk c of key row r sits at chunk c ^ kq_swizzle(r) in shared memory: the
-// fragment loads of 8 rows at the same chunk then fall in distinct banks.
 // Whether n-tile j of the score product (columns 8j .. 8j+7 of NRG = heads x blocks) has a
 // column of block blk (G blocks per head).
 template <int G, int NRG>
@@ -101,9 +99,15 @@ __device__ constexpr bool tile_has_block(int j, int blk) {
   return false;
 }
 
-template <int D>
+// KB-bit key rows (KB = 8, 4, 2; KB D / 8 bytes, NCH = KB D / 128 chunks of 16 bytes): chunk c of
+// row r sits at chunk c ^ kq_swizzle(r).  Rows whose starts share a 128-byte bank window get
+// different XORs, so the fragment loads of rows g = 0..7 at one k-step fall in distinct banks
+// (without it, nibble rows of 64 bytes are 4-way and 2-bit rows of 32 bytes 2-way conflicted).
+template <int D, int KB>
 __device__ __forceinline__ int kq_swizzle(int row) {
-  return D == 64 ? ((row >> 1) & 3) : (row & 7);
+  constexpr int NCH = KB * D / 128;
+  if (NCH <= 1) return 0;
+  return NCH >= 8 ? (row & 7) : ((row * NCH) >> 3) & (NCH - 1);
 }
 // fp16 key rows (D/8 >= 8 chunks each): chunk c of row r sits at chunk c ^ 2 (r & 3).  A half-warp's
 // 8-byte fragment loads (rows g..g+3, chunks 2 ks and 2 ks + 1) then land in 8 distinct chunk slots.
@@ -234,9 +238,10 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
         uint8_t* dst = wst + (k % C::STAGES) * C::TILE;
         for (int c = lane; c < C::TILE / 16; c += 32) {
           int cd = c;
-          if (KB == 8 && c < D) {  // 8-bit key rows: 16 rows x D/16 chunks, swizzled
-            const int row = c / (D / 16), ch = c % (D / 16);
-            cd = row * (D / 16) + (ch ^ kq_swizzle<D>(row));
+          if ((KB == 8 || KB == 4 || KB == 2) && c < KB * D / 8) {  // key rows: 16 x KB D / 128 chunks
+            constexpr int NCH = KB * D / 128 > 0 ? KB * D / 128 : 1;
+            const int row = c / NCH, ch = c % NCH;
+            cd = row * NCH + (ch ^ kq_swizzle<D, KB>(row));
           } else if (KB == 16 && c < 2 * D) {  // fp16 key rows: 16 rows x D/8 chunks, swizzled
             const int row = c / (D / 8), ch = c % (D / 8);
             cd = row * (D / 8) + (ch ^ kh_swizzle(row));
@@ -273,11 +278,11 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
 #pragma unroll
       for (int r = 0; r < 4; ++r) cacc[j][r] = 0.f;
     {
-      const uint8_t* r0 = T + g * (KB * D / 8) + (KB * t) / 2;  // coordinate 4t of the row (KB != 5)
-      const uint8_t* r1 = T + (g + 8) * (KB * D / 8) + (KB * t) / 2;
       const uint32_t* w0r = reinterpret_cast<const uint32_t*>(T + g * (KB * D / 8));  // 5-bit rows
       const uint32_t* w1r = reinterpret_cast<const uint32_t*>(T + (g + 8) * (KB * D / 8));
-      const int sw0 = kq_swizzle<D>(g), sw1 = kq_swizzle<D>(g + 8);
+      const uint8_t* rb0 = T + g * (KB * D / 8);  // row starts (chunks swizzled for KB = 8, 4, 2)
+      const uint8_t* rb1 = T + (g + 8) * (KB * D / 8);
+      const int sw0 = kq_swizzle<D, KB>(g), sw1 = kq_swizzle<D, KB>(g + 8);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         uint4 A;
@@ -291,22 +296,25 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
           A.z = k0.y;
           A.w = k1.y;
         } else if (KB == 8) {
-          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(r0 + 16 * (ks ^ sw0));
-          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(r1 + 16 * (ks ^ sw1));
+          // byte 16 ks + 4t of the row: chunk ks, byte 4t within it
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(rb0 + 16 * (ks ^ sw0) + 4 * t);
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(rb1 + 16 * (ks ^ sw1) + 4 * t);
           A.x = __byte_perm(w0, 0x64646464u, 0x4140u);  // row g: coordinates 4t, 4t+1 as 1024 + code
           A.y = __byte_perm(w1, 0x64646464u, 0x4140u);  // row g + 8
           A.z = __byte_perm(w0, 0x64646464u, 0x4342u);  // row g: coordinates 4t+2, 4t+3
           A.w = __byte_perm(w1, 0x64646464u, 0x4342u);
         } else if (KB == 4) {  // the four codes of coordinates 16 ks + 4t .. + 3 are 16 bits of the row
-          const uint32_t w0 = *reinterpret_cast<const uint16_t*>(r0 + 8 * ks);
-          const uint32_t w1 = *reinterpret_cast<const uint16_t*>(r1 + 8 * ks);
+          // byte 8 ks + 2t of the row: chunk ks / 2, byte 8 (ks & 1) + 2t within it
+          const uint32_t w0 = *reinterpret_cast<const uint16_t*>(rb0 + 16 * ((ks >> 1) ^ sw0) + 8 * (ks & 1) + 2 * t);
+          const uint32_t w1 = *reinterpret_cast<const uint16_t*>(rb1 + 16 * ((ks >> 1) ^ sw1) + 8 * (ks & 1) + 2 * t);
           A.x = nib_pair_lo(w0);
           A.y = nib_pair_lo(w1);
           A.z = nib_pair_hi(w0);
           A.w = nib_pair_hi(w1);
         } else if (KB == 2) {  // ... 8 bits of the row
-          const uint32_t w0 = r0[4 * ks];
-          const uint32_t w1 = r1[4 * ks];
+          // byte 4 ks + t of the row: chunk ks / 4, byte 4 (ks & 3) + t within it
+          const uint32_t w0 = rb0[16 * ((ks >> 2) ^ sw0) + 4 * (ks & 3) + t];
+          const uint32_t w1 = rb1[16 * ((ks >> 2) ^ sw1) + 4 * (ks & 3) + t];
           A.x = q2_pair_lo(w0);
           A.y = q2_pair_lo(w1);
           A.z = q2_pair_hi(w0);
