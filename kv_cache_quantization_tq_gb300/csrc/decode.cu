@@ -15,6 +15,7 @@
 //            Main:  logit = n_k (<q_r, c[idx]> + sqrt(pi/2)/m n_r <t, 2 sigma - 1>) / sqrt(d)
 //                   o += p (mn_g + s_g q)          (mn part summed once per group)
 //            Alt:   logit = sum_blocks s_b <q_b, code_b> + mn_b sum(q_b), / sqrt(d)
+//                   (fp16 keys: <q, k> / sqrt(d))
 //                   o_rot += p n_v c[idx], one inverse rotation per chunk
 //                   ("TurboQuant-MLX overview": butterfly pulled out of the V sum)
 //  3. merge  o = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i per query head.

@@ -1,4 +1,4 @@
-// Alternate-layout decode attention, one warp per page (CUDA cores).
+// Alternate-layout decode attention, one warp per page (block dots on the tensor cores).
 //
 // Keys are 8-, 5-, 4- or 2-bit affine codes per block of 32 (no rotation; the vllm-metal
 // TurboQuant guide's q8_0 / q5_0 / q4_0 / uint2 key formats) or the fp16 keys themselves (the

@@ -9,7 +9,7 @@
 //   k^  = n_k * D (H x) / sqrt(d)                     (inverse rotation)
 //   v^  = mn_g + s_g q                                 (turboquant-bench: asymmetric groups)
 // Alternate layout (vllm-metal TurboQuant guide, quantisation table):
-//   k^  = mn_b + s_b q ;  v^ = n_v * D (H c[idx]) / sqrt(d).
+//   k^  = mn_b + s_b q (or the stored fp16 key) ;  v^ = n_v * D (H c[idx]) / sqrt(d).
 //
 // One CTA handles TB tokens (whole pages) of one (sequence, KV head).  The
 // QJL back-projection Z = (2 sigma - 1) S of a page (16 tokens x m sketch

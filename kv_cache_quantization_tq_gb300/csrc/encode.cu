@@ -7,8 +7,9 @@
 //   r = y - c[idx]; n_r = ||r||; sigma_j = [(S r)_j >= 0];
 //   values: asymmetric 2-bit min/max quantisation in groups of 32.
 // Alternate layout (vllm-metal TurboQuant guide, quantisation table):
-//   keys: 8-bit affine per block of 32; values: n_v = ||v||,
-//   3-bit Lloyd-Max index of H (D v) / (sqrt(d) n_v).
+//   keys: 8-, 5-, 4- or 2-bit affine codes per block of 32, or the fp16 keys unchanged (the
+//   V-only cache of the "TurboQuant-MLX overview"); values: n_v = ||v||, the 2-, 3- or 4-bit
+//   Lloyd-Max index of H (D v) / (sqrt(d) n_v).
 //
 // One CTA encodes up to TB tokens of one (sequence, KV head): a warp per
 // token computes norms, the rotation (registers + shuffles), the Lloyd-Max
