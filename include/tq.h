@@ -126,6 +126,13 @@ const char* tq_status_string(tq_status s);
 tq_status tq_config_init(tq_config* cfg, int layout, int head_dim, int num_q_heads, int num_kv_heads,
                          uint64_t seed);
 
+/* Check a configuration without creating a context and without any CUDA call:
+ * TQ_OK, TQ_ERR_INVALID_ARG or TQ_ERR_UNSUPPORTED, the answer tq_create gives
+ * for it.  When the configuration is valid and bytes_per_token_head is not
+ * NULL, it receives the pool bytes one token of one KV head occupies (what
+ * tq_bytes_per_token_head returns for a context made from it). */
+tq_status tq_config_check(const tq_config* cfg, size_t* bytes_per_token_head);
+
 /* Create a context on the current CUDA device.  Computes on the host the
  * Lloyd-Max codebook for the rotated-coordinate density of head_dim
  * (tq_lloyd_max) and the random tables of cfg->seed (tq_generate_tables),

@@ -66,6 +66,7 @@ _vp, _i, _i64, _u64, _sz = C.c_void_p, C.c_int, C.c_int64, C.c_uint64, C.c_size_
 _SIGS = {
     "tq_status_string": (C.c_char_p, [_i]),
     "tq_config_init": (_i, [C.POINTER(tq_config), _i, _i, _i, _i, _u64]),
+    "tq_config_check": (_i, [C.POINTER(tq_config), C.POINTER(_sz)]),
     "tq_create": (_i, [C.POINTER(tq_config), C.POINTER(_vp)]),
     "tq_create_with_tables": (_i, [C.POINTER(tq_config), _vp, _vp, _vp, C.POINTER(_vp)]),
     "tq_destroy": (None, [_vp]),
@@ -139,6 +140,13 @@ def tq_config_init(layout: int, head_dim: int, num_q_heads: int, num_kv_heads: i
     cfg = tq_config()
     _check(lib.tq_config_init(C.byref(cfg), layout, head_dim, num_q_heads, num_kv_heads, seed), "tq_config_init")
     return cfg
+
+
+def tq_config_check(cfg: tq_config) -> int:
+    """Bytes per token and KV head of a valid configuration (no CUDA call); TQError otherwise."""
+    n = C.c_size_t(0)
+    _check(lib.tq_config_check(C.byref(cfg), C.byref(n)), "tq_config_check")
+    return n.value
 
 
 # ---------------------------------------------------------------- device calls

@@ -396,17 +396,25 @@ tq_status tq_get_tables(const tq_ctx* ctx, float* centroids, float* boundaries, 
   return TQ_OK;
 }
 
-size_t tq_bytes_per_token_head(const tq_ctx* ctx) {
-  if (!ctx) return 0;
-  const size_t d = ctx->cfg.head_dim;
-  // main: key_bits key bits, value_bits value bits and one fp16 scale + minimum per group of 32 per
-  // coordinate, two fp16 norms; alternate: key_bits-bit key codes + 4 B per block of 32 (or fp16
-  // keys alone, key_bits 16), value_bits-bit value indices, fp16 norm
-  const size_t vb = ctx->cfg.value_bits;
-  const size_t kb = ctx->cfg.key_bits;
-  return ctx->cfg.layout == TQ_LAYOUT_MAIN ? (kb * d) / 8 + (vb * d) / 8 + d / 8 + 4
-                                           : (kb * d) / 8 + (kb == 16 ? 0 : (d / 32) * 4) + (vb * d) / 8 + 2;
+namespace {
+// main: key_bits key bits, value_bits value bits and one fp16 scale + minimum per group of 32 per
+// coordinate, two fp16 norms; alternate: key_bits-bit key codes + 4 B per block of 32 (or fp16
+// keys alone, key_bits 16), value_bits-bit value indices, fp16 norm
+size_t record_bytes(const tq_config& c) {
+  const size_t d = c.head_dim, vb = c.value_bits, kb = c.key_bits;
+  return c.layout == TQ_LAYOUT_MAIN ? (kb * d) / 8 + (vb * d) / 8 + d / 8 + 4
+                                    : (kb * d) / 8 + (kb == 16 ? 0 : (d / 32) * 4) + (vb * d) / 8 + 2;
 }
+}  // namespace
+
+tq_status tq_config_check(const tq_config* cfg, size_t* bytes_per_token_head) {
+  if (!cfg) return TQ_ERR_INVALID_ARG;
+  const tq_status st = check_config(cfg);
+  if (st == TQ_OK && bytes_per_token_head) *bytes_per_token_head = record_bytes(*cfg);
+  return st;
+}
+
+size_t tq_bytes_per_token_head(const tq_ctx* ctx) { return ctx ? record_bytes(ctx->cfg) : 0; }
 
 size_t tq_page_bytes(const tq_ctx* ctx) { return tq::kPage * tq_bytes_per_token_head(ctx); }
 

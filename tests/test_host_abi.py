@@ -95,6 +95,48 @@ def test_config_validation():
     assert e.value.status == B.TQ_ERR_UNSUPPORTED
 
 
+def _cfg(lay, d, kb, vb, hq=8, hkv=4):
+    cfg = B.tq_config_init(lay, d, hq, hkv)
+    cfg.key_bits, cfg.value_bits = kb, vb
+    return cfg
+
+
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+def test_config_check_record_bytes_match_the_oracle_layouts(d):
+    # every supported width: the C++ record size equals the oracle's tile size / 16
+    for kb in (2, 3, 4):
+        for vb in (2, 4):
+            got = B.tq_config_check(_cfg(B.TQ_LAYOUT_MAIN, d, kb, vb))
+            assert got == layout.main_bytes_per_token_head(d, vb, kb), (kb, vb)
+    for kb in (2, 4, 5, 8, 16):
+        for vb in (2, 3, 4):
+            got = B.tq_config_check(_cfg(B.TQ_LAYOUT_ALT, d, kb, vb))
+            assert got == layout.alt_bytes_per_token_head(d, vb, kb), (kb, vb)
+    assert B.tq_config_check(B.tq_config_init(B.TQ_LAYOUT_MAIN, d, 16, 4)) == 0.75 * d + 4
+    assert B.tq_config_check(B.tq_config_init(B.TQ_LAYOUT_ALT, d, 8, 8)) == 1.5 * d + 2
+
+
+def test_config_check_rejects_unsupported_widths():
+    bad = [(B.TQ_LAYOUT_MAIN, 5, 2), (B.TQ_LAYOUT_MAIN, 1, 2), (B.TQ_LAYOUT_MAIN, 3, 3), (B.TQ_LAYOUT_MAIN, 3, 8),
+           (B.TQ_LAYOUT_ALT, 3, 3), (B.TQ_LAYOUT_ALT, 6, 3), (B.TQ_LAYOUT_ALT, 7, 3), (B.TQ_LAYOUT_ALT, 12, 3),
+           (B.TQ_LAYOUT_ALT, 8, 1), (B.TQ_LAYOUT_ALT, 8, 5), (B.TQ_LAYOUT_ALT, 16, 8)]
+    for lay, kb, vb in bad:
+        with pytest.raises(B.TQError) as e:
+            B.tq_config_check(_cfg(lay, 128, kb, vb))
+        assert e.value.status == B.TQ_ERR_UNSUPPORTED, (lay, kb, vb)
+    cfg = _cfg(B.TQ_LAYOUT_MAIN, 128, 3, 2)
+    cfg.qjl_m = 64  # the sketch is square
+    with pytest.raises(B.TQError) as e:
+        B.tq_config_check(cfg)
+    assert e.value.status == B.TQ_ERR_UNSUPPORTED
+    cfg = _cfg(B.TQ_LAYOUT_MAIN, 128, 3, 2)
+    cfg.page_size = 32
+    with pytest.raises(B.TQError) as e:
+        B.tq_config_check(cfg)
+    assert e.value.status == B.TQ_ERR_UNSUPPORTED
+    assert B.lib.tq_config_check(None, None) == B.TQ_ERR_INVALID_ARG
+
+
 def test_null_context_calls_are_rejected_without_cuda():
     lib = B.lib
     assert lib.tq_encode_flush(None, None, None, 1, 16, 16, None, None, 1, None, 1, None) == B.TQ_ERR_INVALID_ARG
