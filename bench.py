@@ -6,8 +6,9 @@ new token's k, v are appended to the exact ring (flushing 128 tokens into
 the compressed pages when the ring is full) and decode attention runs for
 all query heads over the compressed history plus the ring.  ``value`` is the
 decode-attention throughput in GB/s of algorithmic bytes: compressed records
-read (100 B per token-head in the main layout, 1.5 d + 2 B in the alternate
-one) + fp16 ring tokens (4 d B per token-head) + fp16 queries + fp32 outputs.
+read (at the default widths 100 B per token-head in the main layout, 1.5 d + 2 B
+in the alternate one) + fp16 ring tokens (4 d B per token-head) + fp16 queries
++ fp32 outputs.
 
 Workloads (synthetic inputs from ``synth``; no weights or datasets):
   qwen3-0.6b-32k   28 layers, 16 q / 4 KV heads, d 128, batch 1, 32768-token prefix
@@ -16,6 +17,10 @@ Workloads (synthetic inputs from ``synth``; no weights or datasets):
   qwen2.5-7b-b8    28 layers, 28 / 4, d 128, batch 8, 32768 tokens each, shuffled pages
   alt-d{64,128,256,512}  alternate layout, 8 / 8, batch 4, 65536 tokens, no ring
   qwen2.5-32b-ragged     1 of 64 layers, 40 / 8, d 128, batch 16, lengths U[1024, 131072]
+  qwen2.5-7b-b8-v4       the batch-8 workload with 4-bit value codes
+  alt-d128-v4 / -k4 / -k5 / -k2 / -vonly
+                   the d 128 alternate workload with 4-bit values (K8+V4), 4-, 5- or
+                   2-bit keys (q4_0 / q5_0 / uint2), or fp16 keys (the V-only cache)
 
 Launch: ``python bench.py [--gpus N --steps K --warmup W --workload NAME]``;
 for N > 1 under torchrun, each rank runs the same per-GPU workload (weak
@@ -85,7 +90,8 @@ def ring_split(length: int):
 def record_bytes(w) -> int:
     d = w["d"]
     if w["layout"] == "main":
-        return (3 * d) // 8 + (w.get("vbits", 2) * d) // 8 + d // 8 + 4
+        # key bits (Lloyd-Max index + QJL), value codes, group (scale, min), two norms
+        return (w.get("kbits", 3) * d) // 8 + (w.get("vbits", 2) * d) // 8 + d // 8 + 4
     # key codes, block (scale, min), value indices, norm; fp16 keys (16 bits) have no (scale, min)
     kb = w.get("kbits", 8)
     return (kb * d) // 8 + (0 if kb == 16 else 4 * (d // 32)) + (w.get("vbits", 3) * d) // 8 + 2
