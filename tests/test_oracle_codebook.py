@@ -43,7 +43,8 @@ def test_one_bit_closed_form(d):
     assert b.shape == (1,) and b[0] == 0.0
 
 
-@pytest.mark.parametrize("d,bits", [(64, 2), (128, 2), (128, 3), (256, 2), (512, 3), (128, 4), (64, 4), (512, 4)])
+@pytest.mark.parametrize("d,bits", [(64, 2), (128, 2), (128, 3), (256, 2), (512, 3), (128, 4), (64, 4), (512, 4),
+                                    (64, 5), (128, 6), (512, 7), (128, 8)])
 def test_fixed_point_conditions_by_quadrature(d, bits):
     c, b = codebook.lloyd_max(d, bits)
     k = 1 << bits
@@ -107,3 +108,38 @@ def test_symmetric_codebook_is_odd_parity_combination(bits):
             chi = np.prod([P[i] for i in S], axis=0)
             recon += float(np.dot(c, chi)) / K * chi
     assert np.allclose(recon, c, atol=1e-12)
+
+
+@pytest.mark.parametrize("d", [64, 512])
+def test_large_codebooks_approach_the_panter_dite_limit(d):
+    """High-resolution theory (Panter & Dite 1951): the optimal K-level quantiser's MSE tends to
+    (1/12) (int f^(1/3))^3 / K^2.  The 32..256-level codebooks approach it from below, the gap
+    roughly halving per bit."""
+    pdc, _ = integrate.quad(lambda x: codebook.pdf(x, d) ** (1 / 3), -1, 1, points=[0.0], limit=200)
+    limit = pdc ** 3 / 12
+    ratios = []
+    for bits in (5, 6, 7, 8):
+        c, b = codebook.lloyd_max(d, bits)
+        edges = np.concatenate(([-1.0], b, [1.0]))
+        mse = sum(integrate.quad(lambda x: (x - c[j]) ** 2 * codebook.pdf(x, d), edges[j], edges[j + 1],
+                                 epsabs=1e-18)[0] for j in range(len(c)))
+        ratios.append(mse * 4 ** bits / limit)
+    assert all(0.9 < r < 1.0 for r in ratios) and ratios[-1] > 0.99
+    gaps = [1 - r for r in ratios]
+    assert all(0.4 < gaps[i + 1] / gaps[i] < 0.6 for i in range(3))
+
+
+@pytest.mark.parametrize("d,bits", [(64, 5), (512, 8)])
+def test_large_codebook_is_a_fixed_point_of_lloyds_map(d, bits):
+    """Lloyd's map (midpoint boundaries, then conditional means) leaves the solved codebook where it
+    is: 1000 iterations from it move no centroid by more than 1e-10 / sqrt(d).  (The drift that
+    remains is rounding in the far-tail cell probabilities, which Lloyd's slow contraction at 256
+    levels does not damp; a wrong fixed point moves by orders of magnitude more.)"""
+    c0, _ = codebook.lloyd_max(d, bits)
+    c = c0.copy()
+    for _ in range(1000):
+        edges = np.concatenate(([-1.0], 0.5 * (c[:-1] + c[1:]), [1.0]))
+        p = codebook.cdf(edges[1:], d) - codebook.cdf(edges[:-1], d)
+        c = codebook.partial_first_moment(edges[:-1], edges[1:], d) / p
+    assert np.max(np.abs(c - c0)) * np.sqrt(d) < 1e-10
+
