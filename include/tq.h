@@ -160,7 +160,9 @@ tq_status tq_get_tables(const tq_ctx* ctx, float* centroids, float* boundaries, 
  * uniformly rotated unit vector of dimension d (density proportional to
  * (1 - x^2)^((d-3)/2) on [-1, 1]; turboquant vLLM guide, section 2 step 2,
  * "Beta distribution" codebook): centroids [2^bits] ascending, boundaries
- * [2^bits - 1] = midpoints.  d >= 8, 1 <= bits <= 4. */
+ * [2^bits - 1] = midpoints.  d >= 8, 1 <= bits <= 8 (5..8 bits: the 32- to
+ * 256-level codebooks of the vllm-metal guide's q5_0 .. q8_0 value formats,
+ * solved by Newton's method on the same fixed-point conditions). */
 tq_status tq_lloyd_max(int d, int bits, double* centroids, double* boundaries);
 
 /* Host only, no CUDA.  The random tables for a seed (SplitMix64 counter

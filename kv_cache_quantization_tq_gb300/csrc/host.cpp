@@ -71,12 +71,85 @@ struct SphereCoord {
   }
 };
 
+// Standard normal quantile by bisection on Phi(x) = erfc(-x / sqrt 2) / 2 (start values only).
+double normal_quantile(double u) {
+  double lo = -40.0, hi = 40.0;
+  for (int it = 0; it < 200; ++it) {
+    const double mid = 0.5 * (lo + hi);
+    (0.5 * erfc(-mid / sqrt(2.0)) < u ? lo : hi) = mid;
+  }
+  return 0.5 * (lo + hi);
+}
+
+// 32 levels and up (the q5_0 .. q8_0 value formats of the vllm-metal TurboQuant guide): Lloyd's
+// iteration contracts too slowly there, so the same conditions are solved by Newton's method on
+// F(c) = c - T(c).  T_j depends only on its cell's edges (dT/db = f(b)(b - T)/P,
+// dT/da = f(a)(T - a)/P) and each inner edge is the midpoint of two centroids, so the Jacobian
+// is tridiagonal (Thomas algorithm).  A step is halved while the residual does not shrink.
+void lloyd_newton(const SphereCoord& f, std::vector<double>& c) {
+  const int k = (int)c.size();
+  std::vector<double> e(k + 1), t(k), p(k), F(k), lo(k), di(k), up(k), r(k), cn(k), en(k + 1), tn(k), pn(k), Fn(k);
+  auto eval = [&](const std::vector<double>& cc, std::vector<double>& ee, std::vector<double>& tt,
+                  std::vector<double>& pp, std::vector<double>& ff) {
+    ee[0] = -1.0;
+    ee[k] = 1.0;
+    for (int j = 1; j < k; ++j) ee[j] = 0.5 * (cc[j - 1] + cc[j]);
+    double worst = 0.0;
+    for (int j = 0; j < k; ++j) {
+      pp[j] = f.prob(ee[j], ee[j + 1]);
+      tt[j] = f.moment(ee[j], ee[j + 1]) / pp[j];
+      ff[j] = cc[j] - tt[j];
+      worst = std::max(worst, fabs(ff[j]));
+    }
+    return worst;
+  };
+  double res = eval(c, e, t, p, F);
+  for (int it = 0; it < 100 && res > 1e-15; ++it) {
+    for (int j = 0; j < k; ++j) {
+      const double dta = f.pdf(e[j]) * (t[j] - e[j]) / p[j];
+      const double dtb = f.pdf(e[j + 1]) * (e[j + 1] - t[j]) / p[j];
+      di[j] = 1.0 - 0.5 * (dta + dtb);
+      lo[j] = -0.5 * dta;  // coefficient of c_{j-1}
+      up[j] = -0.5 * dtb;  // coefficient of c_{j+1}
+      r[j] = -F[j];
+    }
+    for (int j = 1; j < k; ++j) {  // forward elimination
+      const double m = lo[j] / di[j - 1];
+      di[j] -= m * up[j - 1];
+      r[j] -= m * r[j - 1];
+    }
+    r[k - 1] /= di[k - 1];
+    for (int j = k - 2; j >= 0; --j) r[j] = (r[j] - up[j] * r[j + 1]) / di[j];
+    double lam = 1.0, rn = res;
+    for (;;) {
+      for (int j = 0; j < k; ++j) cn[j] = c[j] + lam * r[j];
+      bool sorted = true;
+      for (int j = 1; j < k; ++j) sorted = sorted && cn[j] > cn[j - 1];
+      if (sorted) rn = eval(cn, en, tn, pn, Fn);
+      if ((sorted && rn < res) || lam < 1e-6) break;
+      lam *= 0.5;
+    }
+    if (!(rn < res)) break;  // no further progress at this precision
+    c.swap(cn);
+    e.swap(en);
+    t.swap(tn);
+    p.swap(pn);
+    F.swap(Fn);
+    res = rn;
+  }
+}
+
 void lloyd_max(int d, int bits, double* cent, double* bound) {
   const int k = 1 << bits;
   SphereCoord f(d);
   std::vector<double> c(k), edges(k + 1), cn(k);
-  for (int j = 0; j < k; ++j) c[j] = (2.0 * j + 1.0 - k) / k * 2.0 / sqrt((double)d);
-  for (int it = 0; it < 200000; ++it) {
+  if (bits >= 5) {
+    for (int j = 0; j < k; ++j) c[j] = normal_quantile((j + 0.5) / k) / sqrt((double)d);
+    lloyd_newton(f, c);
+  } else {
+    for (int j = 0; j < k; ++j) c[j] = (2.0 * j + 1.0 - k) / k * 2.0 / sqrt((double)d);
+  }
+  for (int it = 0; it < (bits >= 5 ? 0 : 200000); ++it) {
     edges[0] = -1.0;
     edges[k] = 1.0;
     for (int j = 1; j < k; ++j) edges[j] = 0.5 * (c[j - 1] + c[j]);
@@ -325,7 +398,7 @@ tq_status tq_config_init(tq_config* cfg, int layout, int head_dim, int num_q_hea
 }
 
 tq_status tq_lloyd_max(int d, int bits, double* centroids, double* boundaries) {
-  if (!centroids || d < 8 || bits < 1 || bits > 4) return TQ_ERR_INVALID_ARG;
+  if (!centroids || d < 8 || bits < 1 || bits > 8) return TQ_ERR_INVALID_ARG;
   lloyd_max(d, bits, centroids, boundaries);
   return TQ_OK;
 }

@@ -50,6 +50,23 @@ def test_host_codebook_matches_oracle(d, bits):
     assert np.array_equal(c, -c[::-1])
 
 
+@pytest.mark.parametrize("d,bits", [(64, 5), (128, 6), (512, 7), (64, 8), (512, 8)])
+def test_host_large_codebook_matches_oracle(d, bits):
+    # 32..256 levels (q5_0 .. q8_0 values): both sides solve the fixed point by Newton's method,
+    # the host with its own quadrature.  The host codebook satisfies the oracle's centroid
+    # conditions to 1e-10 (scaled by sqrt(d)); at 256 levels the fixed point is weakly determined
+    # (Lloyd's map contracts by 1 - O(1/K^2)), so that residual allows ~1e-9 between solutions.
+    c, b = B.tq_lloyd_max(d, bits)
+    co, bo = codebook.lloyd_max(d, bits)
+    t, _, _ = codebook._cell_means(c, d)
+    assert np.max(np.abs(t - c)) * np.sqrt(d) < 1e-10
+    assert np.max(np.abs(c - co)) * np.sqrt(d) < 1e-8
+    assert np.max(np.abs(b - bo)) * np.sqrt(d) < 1e-8
+    assert np.array_equal(c, -c[::-1]) and np.all(np.diff(c) > 0)
+    with pytest.raises(B.TQError):
+        B.tq_lloyd_max(d, 9)
+
+
 @pytest.mark.parametrize("seed", [0, 1, 12345, 2**63 + 7])
 def test_host_tables_match_oracle_generator(seed):
     d = 128
