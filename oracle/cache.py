@@ -59,15 +59,16 @@ def encode_main_range(pool, block_table, start, k16, v16, signs, centroids, s_ma
 
 
 def value_bits_of(centroids) -> int:
-    """Alternate-layout value bits for a Lloyd-Max codebook of 2^bits centroids."""
+    """Alternate-layout value bits for a Lloyd-Max codebook of 2^bits centroids (2 to 8 bits: the
+    vllm-metal TurboQuant guide's q2_0 .. q8_0 value formats)."""
     k = len(centroids)
-    assert k in (4, 8, 16), k
+    assert k in (4, 8, 16, 32, 64, 128, 256), k
     return k.bit_length() - 1
 
 
 def encode_alt_range(pool, block_table, start, k16, v16, signs, centroids3):
     """Alternate layout: encode fp16 k/v [B, Hkv, T, d] into ``pool`` (value bits from the codebook
-    size: 4, 8 or 16 centroids; key bits from the pool's tile size: 8, 5, 4, 2, or 16 for fp16
+    size: 4 to 256 centroids; key bits from the pool's tile size: 8, 5, 4, 2, or 16 for fp16
     keys)."""
     k16 = np.asarray(k16, dtype=np.float16)
     bsz, hkv, t, d = k16.shape

@@ -266,7 +266,7 @@ def alt_bytes_per_token_head(d: int, vbits: int = 3, kbits: int = 8) -> float:
 def alt_value_bits(tile_bytes: int, d: int, kbits: int = 8) -> int:
     """Value bits of an alternate-layout tile from its size and key bits."""
     vb, rem = divmod(tile_bytes - alt_key_plane_bytes(d, kbits) - 32, 2 * d)
-    assert rem == 0 and vb in (2, 3, 4), (tile_bytes, d, kbits)
+    assert rem == 0 and 2 <= vb <= 8, (tile_bytes, d, kbits)
     return vb
 
 

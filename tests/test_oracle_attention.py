@@ -76,7 +76,7 @@ def test_compressed_logits_track_exact_logits():
     assert np.corrcoef(est, exact)[0, 1] > 0.85
 
 
-@pytest.mark.parametrize("vbits,kbits", [(2, 8), (3, 8), (4, 8), (3, 4), (3, 5), (3, 2), (2, 2)])
+@pytest.mark.parametrize("vbits,kbits", [(2, 8), (3, 8), (4, 8), (3, 4), (3, 5), (3, 2), (2, 2), (5, 8), (8, 8)])
 def test_alt_layout_decode_matches_torch_sdpa_on_dequantised_cache(vbits, kbits):
     d, hkv, n_rep = 64, 2, 1
     sg = rng.signs(5, d)

@@ -140,7 +140,8 @@ def test_main_tile_round_trip(d):
 
 
 @pytest.mark.parametrize("d", [64, 128, 256, 512])
-@pytest.mark.parametrize("vbits,kbits", [(2, 8), (3, 8), (4, 8), (3, 4), (4, 4), (3, 5), (4, 5), (3, 2), (2, 2)])
+@pytest.mark.parametrize("vbits,kbits", [(2, 8), (3, 8), (4, 8), (3, 4), (4, 4), (3, 5), (4, 5), (3, 2), (2, 2),
+                                         (5, 8), (6, 8), (7, 4), (8, 8), (8, 2)])
 def test_alt_tile_round_trip(d, vbits, kbits):
     g = np.random.default_rng(d + vbits + kbits)
     f = {

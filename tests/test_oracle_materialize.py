@@ -52,7 +52,7 @@ def test_main_materialised_rows_keep_ring_exact_and_values_within_half_a_step():
     assert cos.mean() > 0.8
 
 
-@pytest.mark.parametrize("vbits,kbits", [(2, 8), (3, 8), (4, 8), (3, 4), (3, 5), (3, 2), (2, 2)])
+@pytest.mark.parametrize("vbits,kbits", [(2, 8), (3, 8), (4, 8), (3, 4), (3, 5), (3, 2), (2, 2), (6, 8), (8, 4)])
 def test_alt_materialised_history_reproduces_the_decode(vbits, kbits):
     seed, d, hkv, bsz = 5, 64, 2, 2
     sg = rng.signs(seed, d)
