@@ -126,6 +126,31 @@ def test_qjl_estimator_unbiased_over_seeds():
     assert abs(true - true16) < 1e-2
 
 
+@pytest.mark.parametrize("lm_bits", [1, 3])
+def test_qjl_estimator_unbiased_at_other_key_widths(lm_bits):
+    """The same unbiasedness with 1- and 3-bit Lloyd-Max indices (2- and 4-bit keys, turboquant vLLM
+    guide, --key-bits): the QJL term removes the bias of any codebook, d = 64, 10k seeds."""
+    d = 64
+    g = np.random.default_rng(12 + lm_bits)
+    k = g.standard_normal(d)
+    q = 0.5 * k + g.standard_normal(d)
+    c, _ = codebook.lloyd_max(d, lm_bits)
+    n = 10_000
+    est = np.empty(n)
+    est_lm = np.empty(n)
+    for seed in range(n):
+        sg = rng.signs(seed, d)
+        s = rng.gaussian_matrix(seed, d, d)
+        enc = quant.encode_keys(k.astype(np.float16), sg, c, s)
+        est[seed] = quant.inner_product_estimate(q, enc["n_k_exact"], enc["idx"], enc["n_r_exact"], enc["sigma"], sg, c, s)
+        est_lm[seed] = enc["n_k_exact"] * np.dot(rotation.rotate(q, sg), c[enc["idx"]])
+    true16 = float(q @ k.astype(np.float16).astype(np.float64))
+    se = est.std(ddof=1) / math.sqrt(n)
+    assert abs(est.mean() - true16) < 3 * se, (est.mean(), true16, se)
+    se_lm = est_lm.std(ddof=1) / math.sqrt(n)
+    assert abs(est_lm.mean() - true16) > 10 * max(se_lm, se)  # the Lloyd-Max part alone shrinks it
+
+
 def test_alt_value_encoder():
     d = 256
     sg = rng.signs(2, d)
