@@ -619,6 +619,24 @@ def run_oracle(w, reps, sample_len, budget_s=10.0):
     return nbytes / dt / 1e9, dt, nbytes, n
 
 
+def oracle_one_thread(workload: str):
+    """GB/s of the oracle arm re-run in a child process with one BLAS / OpenMP thread (None if the
+    child fails): the single-core figure beside the all-cores one."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        env.pop(k, None)
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", workload,
+           "--steps", "1", "--warmup", "0"]
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, env=env)
+        for line in r.stdout.splitlines():
+            if line.startswith("{"):
+                return float(json.loads(line)["value"])
+    except (OSError, subprocess.SubprocessError, ValueError, KeyError):
+        pass
+    return None
+
+
 def oracle_sample_len(w):
     base = w["ctx"] if w["ctx"] is not None else 32768
     return int(min(base, 32768 if w["layout"] == "main" else 16384))
@@ -682,7 +700,8 @@ def main():
         val, dt, nbytes, reps = run_oracle(w, 20, sample_len, budget_s=10.0)
         cpu = {"value": val, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle",
                "sample": f"{reps} oracle decodes of one sequence x {w['hkv']} KV heads at {sample_len} tokens "
-                         f"({nbytes / 1e6:.1f} MB of records each), {dt:.2f} s each"}
+                         f"({nbytes / 1e6:.1f} MB of records each), {dt:.2f} s each",
+               "value_one_thread": oracle_one_thread(args.workload)}
     peak, _ = measured_peaks()
     line = {
         "metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
