@@ -628,7 +628,7 @@ def oracle_one_thread(workload: str):
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", workload,
            "--steps", "1", "--warmup", "0"]
     try:
-        r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, env=env)
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=120, env=env)
         for line in r.stdout.splitlines():
             if line.startswith("{"):
                 return float(json.loads(line)["value"])
