@@ -53,6 +53,16 @@
  *     [16d, 18d)    KSM token t, block g at (t*d/32+g)*4: fp16 scale, fp16 minimum
  *     [18d, 24d)    VI  per token a 3d/8-byte stream of 3-bit value indices (tq_pack order)
  *     [24d, +32)    VN  fp16 value norm per token
+ *
+ * Other widths (tq_config key_bits / value_bits) keep the plane order:
+ *   main: kb - 1 Lloyd-Max index planes (high bit first) then KS, each 2d
+ *     bytes; VQ 2 vb d bytes (4-bit codes: two sub-planes of one uint32 per
+ *     dimension, tokens 0-7 then 8-15, token 8w+2j+e at bits 16e+4j of word
+ *     w); tile (2 kb + 2 vb + 2) d + 64 bytes.
+ *   alternate: KQ is a dense kb-bit code stream per token (code c at bit
+ *     kb c), 2 kb d bytes, followed by KSM; with key_bits 16 KQ holds the
+ *     fp16 keys (32 d bytes) and there is no KSM.  VI is a dense vb-bit
+ *     stream per token, 2 vb d bytes.  tq_config_check gives the size.
  */
 #ifndef TQ_H_
 #define TQ_H_
