@@ -90,6 +90,14 @@ typedef enum { TQ_LAYOUT_MAIN = 0, TQ_LAYOUT_ALT = 1 } tq_layout;
 #define TQ_DEVERR_POSITION   0x2u /* position / length beyond the block table or not page aligned */
 #define TQ_DEVERR_RING       0x4u /* n_buf outside [0, ring_capacity] */
 #define TQ_DEVERR_CHUNKS     0x8u /* n_compressed larger than the max_ctx given to decode */
+#define TQ_DEVERR_TIMEOUT    0x10u /* a decode CTA gave up waiting (about a second) for its own
+                                      copies or tensor-core products; its output rows are not written */
+
+/* Decode kernels for the main layout at head_dim 128 (tq_set_decode_path). */
+#define TQ_DECODE_AUTO     0 /* the library chooses per call (default) */
+#define TQ_DECODE_MMA_SYNC 1 /* scores and values on mma.sync (every key / value width) */
+#define TQ_DECODE_TCGEN05  2 /* scores on tcgen05 (fp8 operands in tensor memory), values on mma.sync:
+                                3-bit keys and 2-bit values only (other widths use mma.sync) */
 
 typedef struct {
   int head_dim;      /* d: 64, 128, 256 or 512 (the sizes the pages' rotation kernels accept) */
@@ -123,6 +131,7 @@ typedef struct {
   double encode_ms;
   int64_t merge_launches;  /* split-K merge kernel */
   double merge_ms;
+  const char* decode_kernel; /* name of the decode kernel of the last decode call (static string), or NULL */
 } tq_profile;
 
 /* ------------------------------------------------------------------ setup */
@@ -187,8 +196,16 @@ size_t tq_bytes_per_token_head(const tq_ctx* ctx);
 size_t tq_page_bytes(const tq_ctx* ctx);
 
 /* Workspace bytes tq_decode_attention needs for `batch` sequences whose
- * compressed lengths are all <= max_ctx tokens. */
+ * compressed lengths are all <= max_ctx tokens (for the decode path selected
+ * when it is called: query the size again after tq_set_decode_path). */
 tq_status tq_workspace_size(const tq_ctx* ctx, int batch, int max_ctx, size_t* bytes);
+
+/* Select the main-layout decode kernels (TQ_DECODE_AUTO, TQ_DECODE_MMA_SYNC or
+ * TQ_DECODE_TCGEN05).  The results agree within the decode tolerance; the
+ * choice only changes speed and workspace size.  This switch has no
+ * counterpart in the source pages: it exists to compare and test the two
+ * tensor-core designs.  Host only; TQ_ERR_INVALID_ARG for another value. */
+tq_status tq_set_decode_path(tq_ctx* ctx, int path);
 
 /* ------------------------------------------------------------------ write path */
 
@@ -255,10 +272,14 @@ tq_status tq_decode_attention(tq_ctx* ctx, const void* q, int batch, const void*
  * The scratch is one file-scope device array of 16 MiB (16 << 20 bytes) that
  * every GPU which loads libtq holds until the process exits; a call whose
  * tq_workspace_size(batch, max_ctx) exceeds 16 MiB returns TQ_ERR_WORKSPACE
- * and launches nothing.  The first call on a device looks up that device's
- * address of the array (cudaGetSymbolAddress, with the device current); make
- * that first call before any stream capture.  The call itself allocates no
- * device memory.  All calls share the one array and it keeps the last call's
+ * and launches nothing.  Every call made outside stream capture looks up the
+ * current context's address of the array (cudaGetSymbolAddress, with the
+ * device current) and remembers it per device; a call made while `stream` is
+ * capturing uses the remembered address, so make one uncaptured call on a
+ * device (again after cudaDeviceReset or a change of context) before
+ * capturing; otherwise the captured call returns TQ_ERR_CUDA.  Arguments are
+ * checked as by tq_decode_attention, in the same order, before the size.  The
+ * call itself allocates no device memory.  All calls share the one array and it keeps the last call's
  * contents (nothing in it needs to start at zero): calls that can overlap on
  * the GPU (different streams, or different host threads without ordering)
  * race on it, so keep them ordered on one stream. */

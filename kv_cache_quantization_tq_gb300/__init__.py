@@ -8,6 +8,9 @@ of its names, so ``kv_cache_quantization_tq_gb300.build`` works before the
 library exists; using the binding without a built library raises ImportError.
 """
 _EXPORTS = (
+    "TQ_DECODE_AUTO",
+    "TQ_DECODE_MMA_SYNC",
+    "TQ_DECODE_TCGEN05",
     "TQ_LAYOUT_ALT",
     "TQ_LAYOUT_MAIN",
     "Context",

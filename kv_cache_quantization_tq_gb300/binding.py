@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_HERE, "libtq.so")
 
 TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_WORKSPACE, TQ_ERR_CUDA = range(5)
 TQ_LAYOUT_MAIN, TQ_LAYOUT_ALT = 0, 1
-TQ_DEVERR_BLOCK_ID, TQ_DEVERR_POSITION, TQ_DEVERR_RING, TQ_DEVERR_CHUNKS = 1, 2, 4, 8
+TQ_DEVERR_BLOCK_ID, TQ_DEVERR_POSITION, TQ_DEVERR_RING, TQ_DEVERR_CHUNKS, TQ_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+TQ_DECODE_AUTO, TQ_DECODE_MMA_SYNC, TQ_DECODE_TCGEN05 = 0, 1, 2
 
 
 class TQError(RuntimeError):
@@ -51,6 +52,7 @@ class tq_profile(C.Structure):
         ("encode_ms", C.c_double),
         ("merge_launches", C.c_int64),
         ("merge_ms", C.c_double),
+        ("decode_kernel", C.c_char_p),
     ]
 
 
@@ -87,6 +89,7 @@ _SIGS = {
     "tq_unpack_host": (_i, [_vp, _i64, _i, _vp]),
     "tq_get_device_errors": (_i, [_vp, C.POINTER(C.c_uint32), _vp]),
     "tq_launch_count": (_i64, [_vp]),
+    "tq_set_decode_path": (_i, [_vp, _i]),
     "tq_profile_begin": (_i, [_vp]),
     "tq_profile_end": (_i, [_vp, C.POINTER(tq_profile)]),
 }
@@ -241,6 +244,10 @@ class Context:
         _check(lib.tq_workspace_size(self.ptr, batch, max_ctx, C.byref(n)), "tq_workspace_size")
         return n.value
 
+    def set_decode_path(self, path: int):
+        """TQ_DECODE_AUTO, TQ_DECODE_MMA_SYNC or TQ_DECODE_TCGEN05 (main layout, head_dim 128)."""
+        _check(lib.tq_set_decode_path(self.ptr, path), "tq_set_decode_path")
+
     def get_tables(self):
         k = 1 << (self.cfg.key_bits - 1 if self.layout == TQ_LAYOUT_MAIN else self.cfg.value_bits)
         d = self.head_dim
@@ -377,4 +384,6 @@ class Context:
     def profile_end(self) -> dict:
         p = tq_profile()
         _check(lib.tq_profile_end(self.ptr, C.byref(p)), "tq_profile_end")
-        return {f: getattr(p, f) for f, _ in tq_profile._fields_}
+        r = {f: getattr(p, f) for f, _ in tq_profile._fields_}
+        r["decode_kernel"] = r["decode_kernel"].decode() if r["decode_kernel"] else None
+        return r

@@ -21,7 +21,7 @@ LIB = os.path.join(HERE, "libtq.so")
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 
-CU = ["encode.cu", "decode.cu", "decode_tc.cu", "decode_alt.cu", "decode_static.cu", "dequant.cu", "pack.cu"]
+CU = ["encode.cu", "decode.cu", "decode_tc.cu", "decode_hy.cu", "decode_alt.cu", "decode_static.cu", "dequant.cu", "pack.cu"]
 CPP = ["host.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -701,7 +701,7 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
     t.max_ctx = max_ctx;
     t.out = out;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    t.afrag = plan.fused_prep ? nullptr : reinterpret_cast<uint4*>(ws);
+    t.afrag = (plan.fused_prep || plan.hybrid) ? nullptr : reinterpret_cast<uint4*>(ws);
     t.parts = reinterpret_cast<float*>(ws + plan.q_bytes);
     t.chunk_pages = plan.chunk_tokens / kPage;
     t.n_chunks = plan.n_chunks;
@@ -716,6 +716,7 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
     t.kb = ctx->cfg.key_bits;
     t.cta_warps = plan.cta_warps;
     t.err = ctx->d_err;
+    if (plan.hybrid) return launch_decode_hy(ctx, t, batch, ws, s);
     return launch_decode_tc(ctx, t, batch, s);
   }
   DecArgs a;
@@ -767,6 +768,7 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
   bool done = false;
   if (!main) {
     // compressed chunks: warp-per-page kernel; the exact buffer (if any): the part kernel below
+    ctx->decode_kernel = "decode_alt_v2_kernel";
     prof_start(ctx, kProfDecode, s);
     e = launch_decode_alt_v2(ctx, q, pool, num_blocks, block_table, max_blocks, n_compressed, max_ctx, a.parts,
                              plan.chunk_tokens, plan.n_chunks, plan.n_parts, batch, s);
@@ -783,7 +785,10 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
     }
   }
   if (!done || n_buf) {
-    if (!done) prof_start(ctx, kProfDecode, s);
+    if (!done) {
+      ctx->decode_kernel = main ? "decode_main_kernel" : "decode_alt_kernel";
+      prof_start(ctx, kProfDecode, s);
+    }
     switch (d) {
       case 64: e = launch_d<64>(a, main ? ctx->cfg.value_bits : 0, grid, s); break;
       case 128: e = launch_d<128>(a, main ? ctx->cfg.value_bits : 0, grid, s); break;

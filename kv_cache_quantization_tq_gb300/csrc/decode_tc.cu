@@ -35,8 +35,7 @@
 // (a sequence whose work fits one CTA is written directly).  The exact
 // recent buffer is one more work item of the same kernel, scored from the raw
 // fp16 keys and values with the same tensor-core path.
-#include "common.cuh"
-#include "tc.cuh"
+#include "tc_mma.cuh"
 
 namespace tq {
 namespace {
@@ -80,14 +79,6 @@ struct TcTile : TcLayout<KB, VB> {
 
 constexpr int kPartStride = D + 4;  // floats per split-K partial: o[D], m, l, pad (16-byte rows)
 
-__device__ __forceinline__ void mma_f16(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
-}
-
 // Key bits as fp16 operands without a shift per element.  Lane t of an MMA takes bit pairs
 // j = 4t .. 4t+3 of a plane word (bits j and j + 16: coordinates 32w + 2j and 32w + 2j + 1).  One
 // multiplication by 2^(12 - 4t) moves them to bits 12..15 (and 28..31), i.e. onto fp16 exponent
@@ -118,66 +109,6 @@ __device__ __forceinline__ uint32_t mul_lo(uint32_t a, uint32_t b) {
 // Coordinate of A-fragment register pair rh (0: regs 0/1, 1: regs 2/3) of lane group t in k-step kb
 // of a plane (first of two adjacent coordinates).
 __device__ __forceinline__ int frag_dim(int kb, int t, int rh) { return 32 * (kb >> 1) + 8 * t + 4 * (kb & 1) + 2 * rh; }
-
-// 2^x for x <= 0 (log2-domain softmax weights); -inf gives +0.
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
-  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-
-// fp16 high/low split of a pair: high = fp16(v), low = fp16((v - high) * 2^11).
-// The low part is stored scaled so that it has the magnitude of the high part
-// (|v - high| <= 2^-11 |v|): it never becomes subnormal before the high part
-// does, and the scale cannot overflow.  Rows of low parts accumulate into
-// their own accumulator rows, which are multiplied by 2^-11 in the epilogue.
-constexpr float kLoScale = 2048.f;
-constexpr float kLoUnscale = 1.f / 2048.f;
-__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(a, b);
-  const float2 hf = __half22float2(h);
-  hi = h2_bits(h);
-  lo = h2_bits(__floats2half2_rn((a - hf.x) * kLoScale, (b - hf.y) * kLoScale));
-}
-
-__device__ __forceinline__ void cp16(void* smem, const void* gmem) {
-  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
-
-__device__ __forceinline__ int tc_nc(const TcArgs& a, int b) {
-  const int nc = a.n_compressed[b];
-  if (nc < 0 || (nc & 15) || nc > a.max_blocks * kPage) {
-    if (threadIdx.x == 0) flag_error(a.err, TQ_DEVERR_POSITION);
-    return 0;
-  }
-  if (nc > a.max_ctx) {
-    if (threadIdx.x == 0) flag_error(a.err, TQ_DEVERR_CHUNKS);
-    return 0;
-  }
-  return nc;
-}
-
-__device__ __forceinline__ int tc_nb(const TcArgs& a, int b) {
-  if (!a.n_buf) return 0;
-  const int nb = a.n_buf[b];
-  if (nb < 0 || nb > kRing) {
-    if (threadIdx.x == 0) flag_error(a.err, TQ_DEVERR_RING);
-    return 0;
-  }
-  return nb;
-}
 
 // ------------------------------------------------------------------ query side
 // Per CTA, before its pages are scored (the first pages are already in flight):
@@ -388,42 +319,6 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(TcArgs a) {
   }
 }
 
-// ------------------------------------------------------------------ decode
-struct WarpState {
-  float m, l;
-  float o[16][4];
-  float mn[4];
-};
-
-// Online softmax with a lazily updated reference maximum.  The running state (m, l, o, mn) is
-// only rescaled when some head's page maximum exceeds its reference by more than 2^kLazyLog2 (or
-// on the first page); otherwise the reference stays and weights p = 2^(s - m) may reach
-// 2^kLazyLog2.  The result is exact either way (l and o share the reference, and so do the
-// split-K partials); weights up to 256 are exact in fp32 and far inside the fp16 range of the
-// value operands.  A warp sees few pages, so an eager update rescaled the 68 accumulators on most
-// of them.
-constexpr float kLazyLog2 = 8.f;
-__device__ __forceinline__ void softmax_update(WarpState& st, float (&s)[4], float (&p)[4]) {
-  float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
-  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-  if (__any_sync(kFull, mx > st.m + kLazyLog2)) {
-    const float m_new = fmaxf(st.m, mx);
-    const float alpha = fast_exp2(st.m - m_new);
-    st.l *= alpha;
-    st.m = m_new;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) st.o[nt][r] *= alpha;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) st.mn[g] *= alpha;
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) p[k] = fast_exp2(s[k] - st.m);
-  st.l += (p[0] + p[1]) + (p[2] + p[3]);
-}
-
 // One compressed page (16 tokens) of the warp's KV head.  off_lm / off_qj: this lane's head's score
 // offsets (the accumulators' start values, see bitenc_scale).
 template <int KB, int VB>
@@ -510,8 +405,9 @@ __device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA
     float w[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) w[k] = p[k] * sc[k];
-    split2(w[0], w[1], Ap[gg].x, Ap[gg].y);
-    split2(w[2], w[3], Ap[gg].z, Ap[gg].w);
+    // operands p * s * 2^-kLazyLog2 (< 2^16, see kWeightScale); the output is scaled back by vscale
+    split2(w[0] * kWeightScale, w[1] * kWeightScale, Ap[gg].x, Ap[gg].y);
+    split2(w[2] * kWeightScale, w[3] * kWeightScale, Ap[gg].z, Ap[gg].w);
     // group minimum, minus the 1 of the code encoding below (2^VB w, as the codes are scaled by 2^VB)
     float acc_mn = st.mn[gg];
 #pragma unroll
@@ -536,48 +432,6 @@ __device__ __forceinline__ void page_compressed(const TcArgs& a, const uint4* sA
       b1 = (((w1 >> (4 * t)) << 6) & 0x03C003C0u) | 0x3C003C00u;
     }
     mma_f16(st.o[nt], Ap[nt >> 2], b0, b1);
-  }
-}
-
-// One ring page: tokens t0 .. t0+cnt-1 of the exact fp16 buffer.
-__device__ __forceinline__ void page_ring(const TcArgs& a, const uint4 (&Aq)[8], const __half* rk, const __half* rv,
-                                          int t0, int cnt, WarpState& st, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  float acc[2][4];
-#pragma unroll
-  for (int n = 0; n < 2; ++n)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) acc[n][r] = 0.f;
-  const uint32_t* k0 = reinterpret_cast<const uint32_t*>(rk + (size_t)(t0 + g) * D);
-  const uint32_t* k1 = reinterpret_cast<const uint32_t*>(rk + (size_t)(t0 + g + 8) * D);
-#pragma unroll
-  for (int kb = 0; kb < 8; ++kb) {
-    const int c = kb * 8 + t;  // uint32 index of dims kb*16 + 2t, +1
-    mma_f16(acc[0], Aq[kb], k0[c], k0[c + 4]);
-    mma_f16(acc[1], Aq[kb], k1[c], k1[c + 4]);
-  }
-  float s[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int tok = (k >> 1) * 8 + 2 * t + (k & 1);
-    s[k] = tok < cnt ? acc[k >> 1][k & 1] * a.logit_scale : -INFINITY;
-  }
-  float p[4];
-  softmax_update(st, s, p);
-  uint4 Ap;
-  split2(p[0], p[1], Ap.x, Ap.y);
-  split2(p[2], p[3], Ap.z, Ap.w);
-  const unsigned short* v16 = reinterpret_cast<const unsigned short*>(rv);
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    const int dim = nt * 8 + g;
-    uint32_t e[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int tok = (k >> 1) * 8 + 2 * t + (k & 1);
-      e[k] = tok < cnt ? (uint32_t)v16[(size_t)(t0 + tok) * D + dim] : 0u;
-    }
-    mma_f16(st.o[nt], Ap, e[0] | (e[1] << 16), e[2] | (e[3] << 16));
   }
 }
 
@@ -638,7 +492,8 @@ __global__ void __launch_bounds__(32 * NW, MINB) tc_decode_kernel(TcArgs a) {
     for (int r = 0; r < 4; ++r) st.o[nt][r] = 0.f;
 #pragma unroll
   for (int k = 0; k < 4; ++k) st.mn[k] = 0.f;
-  float vscale = (float)(1 << VB);  // value codes entered as 1 + q/2^VB; the offset is removed through st.mn
+  // value codes entered as 1 + q/2^VB (the offset is removed through st.mn), weights scaled by kWeightScale
+  float vscale = (float)(1 << VB) / kWeightScale;
 
   if (!ring) {
     if (a.afrag) {
@@ -918,32 +773,43 @@ bool tc_supported(const tq_ctx* ctx) {
   return ctx->cfg.layout == TQ_LAYOUT_MAIN && ctx->cfg.head_dim == D;
 }
 
-cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) {
-  const int hgroups = a.hkv * a.groups;
+void tc_set_score_constants(const tq_ctx* ctx, TcArgs& a) {
   // Lloyd-Max row weights.  A bit enters the products as P = 1 - 2 bit = +-1, and a symmetric
   // codebook (c[K-1-i] = -c[i]) is odd under flipping every index bit, so c[idx] is a combination
   // of the odd parity products of the P's: one term per index bit, plus P0 P1 P2 for a 3-bit
   // index (whose plane is the XOR of the three stored planes).  Each weight is a Walsh
   // coefficient: (1/K) sum_idx c[idx] chi(idx).
-  {
-    const int nb = ctx->cfg.key_bits - 1, K = 1 << nb;
-    a.n_lm = nb == 3 ? 4 : nb;
-    for (int p = 0; p < a.n_lm; ++p) {
-      double w = 0.0;
-      for (int idx = 0; idx < K; ++idx) {
-        int par = 0;  // parity of the bits in the product
-        if (p < nb)
-          par = (idx >> (nb - 1 - p)) & 1;  // plane p = index bit nb-1-p (high bit first)
-        else
-          par = ((idx >> 2) ^ (idx >> 1) ^ idx) & 1;
-        w += (double)ctx->h_centroids[idx] * (par ? -1.0 : 1.0);
-      }
-      a.lm_w[p] = (float)(w / K);
+  const int nb = ctx->cfg.key_bits - 1, K = 1 << nb;
+  a.n_lm = nb == 3 ? 4 : nb;
+  for (int p = 0; p < a.n_lm; ++p) {
+    double w = 0.0;
+    for (int idx = 0; idx < K; ++idx) {
+      int par = 0;  // parity of the bits in the product
+      if (p < nb)
+        par = (idx >> (nb - 1 - p)) & 1;  // plane p = index bit nb-1-p (high bit first)
+      else
+        par = ((idx >> 2) ^ (idx >> 1) ^ idx) & 1;
+      w += (double)ctx->h_centroids[idx] * (par ? -1.0 : 1.0);
     }
-    for (int p = a.n_lm; p < 4; ++p) a.lm_w[p] = 0.f;
+    a.lm_w[p] = (float)(w / K);
   }
+  for (int p = a.n_lm; p < 4; ++p) a.lm_w[p] = 0.f;
   a.qjl_coef = 1.2533141373155003f / (float)ctx->cfg.qjl_m;
   a.logit_scale = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
+}
+
+cudaError_t launch_tc_merge(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) {
+  prof_start(ctx, kProfMerge, s);
+  tc_merge_kernel<<<dim3(a.hq, batch, kMergeSplit), 128, sizeof(float) * a.n_parts, s>>>(a);
+  prof_stop(ctx, kProfMerge, s);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ctx->launches++;
+  return e;
+}
+
+cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) {
+  const int hgroups = a.hkv * a.groups;
+  tc_set_score_constants(ctx, a);
   cudaError_t e = cudaSuccess;
   if (a.afrag) {
     tc_prep_kernel<<<dim3(hgroups, batch, kPrepSlices), 128, 0, s>>>(a);
@@ -980,18 +846,14 @@ cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s) 
   }
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  ctx->decode_kernel = "tc_decode_kernel";
   prof_start(ctx, kProfDecode, s);
   kern<<<dim3(a.n_parts, hgroups, batch), w8 ? 256 : 128, smem, s>>>(a);
   prof_stop(ctx, kProfDecode, s);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ctx->launches++;
-  prof_start(ctx, kProfMerge, s);
-  tc_merge_kernel<<<dim3(a.hq, batch, kMergeSplit), 128, sizeof(float) * a.n_parts, s>>>(a);
-  prof_stop(ctx, kProfMerge, s);
-  e = cudaGetLastError();
-  if (e == cudaSuccess) ctx->launches++;
-  return e;
+  return launch_tc_merge(ctx, a, batch, s);
 }
 
 }  // namespace tq

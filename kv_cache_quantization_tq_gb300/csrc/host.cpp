@@ -337,9 +337,27 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
     per = (total_pages + 1215) / 1216;
     per = std::max<int64_t>(4, std::min<int64_t>(64, per));
   }
+  // The tcgen05 score path (decode_hy.cu): 3-bit keys, 2-bit values, m = d.  Its CTAs hold 256
+  // tensor-memory columns, two per SM, and walk their chunk in tiles of 8 pages; the chunks of a
+  // sequence are sized so that all chunks of a uniform batch (plus its ring items) fit in one wave
+  // of two CTAs per SM.
+  const bool hy_ok = pl.tensor_core && ctx->cfg.key_bits == 3 && ctx->cfg.value_bits == 2 && ctx->cfg.qjl_m == d;
+  // TQ_DECODE_AUTO keeps the mma.sync kernels: on GB300 they measured faster (88 against 125 us
+  // per launch at batch 8 x 32K, 28 / 4 heads).
+  pl.hybrid = hy_ok && ctx->decode_path == TQ_DECODE_TCGEN05;
+  if (pl.hybrid) {
+    const int64_t bh = (int64_t)batch * hkv * groups;
+    const int64_t slots = 2 * (int64_t)std::max(1, ctx->sm_count);
+    const int64_t cps = std::max<int64_t>(1, (slots - bh) / std::max<int64_t>(1, bh));
+    per = (pages + cps - 1) / cps;
+    per = std::max<int64_t>(64, std::min<int64_t>(512, (per + 7) / 8 * 8));
+  }
   // at most kMaxChunks chunks per sequence: the merge keeps one weight per part in shared memory
   per = std::max<int64_t>(per, (pages + kMaxChunks - 1) / kMaxChunks);
-  if (pl.tensor_core) per = (per + pl.cta_warps - 1) / pl.cta_warps * pl.cta_warps;
+  if (pl.hybrid)
+    per = (per + 7) / 8 * 8;
+  else if (pl.tensor_core)
+    per = (per + pl.cta_warps - 1) / pl.cta_warps * pl.cta_warps;
   pl.chunk_tokens = (int)(per * kPage);
   pl.n_chunks = (int)((pages + per - 1) / per);
   pl.n_parts = pl.n_chunks + 1;
@@ -348,8 +366,13 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
     // saving a kernel; larger grids build them once per (sequence, head group) in a prep
     // kernel, because there the per-CTA cost (~3 us) outweighs the saved launch.
     const int64_t ctas = (int64_t)pl.n_parts * hkv * groups * batch;
-    pl.fused_prep = pl.cta_warps == 8 || ctas <= (int64_t)ctx->sm_count * 3;
-    pl.q_bytes = pl.fused_prep ? 0 : align((size_t)batch * hkv * groups * kTcQueryU4 * 16);
+    pl.fused_prep = !pl.hybrid && (pl.cta_warps == 8 || ctas <= (int64_t)ctx->sm_count * 3);
+    if (pl.hybrid) {
+      pl.cta_warps = 4;
+      pl.q_bytes = align((size_t)batch * hkv * groups * kHyQueryBytes);
+    } else {
+      pl.q_bytes = pl.fused_prep ? 0 : align((size_t)batch * hkv * groups * kTcQueryU4 * 16);
+    }
   } else
     pl.q_bytes = ctx->cfg.layout == TQ_LAYOUT_MAIN ? align(sizeof(float) * batch * hq * 2 * d) : 0;
   pl.part_bytes = align(sizeof(float) * (size_t)batch * hq * pl.n_parts * (d + (pl.tensor_core ? 4 : 2)));
@@ -610,6 +633,12 @@ tq_status tq_get_device_errors(tq_ctx* ctx, uint32_t* flags, cudaStream_t stream
 
 int64_t tq_launch_count(const tq_ctx* ctx) { return ctx ? ctx->launches : 0; }
 
+tq_status tq_set_decode_path(tq_ctx* ctx, int path) {
+  if (!ctx || path < TQ_DECODE_AUTO || path > TQ_DECODE_TCGEN05) return TQ_ERR_INVALID_ARG;
+  ctx->decode_path = path;
+  return TQ_OK;
+}
+
 tq_status tq_profile_begin(tq_ctx* ctx) {
   if (!ctx) return TQ_ERR_INVALID_ARG;
   for (auto& p : ctx->prof) p.used = 0;
@@ -639,6 +668,7 @@ tq_status tq_profile_end(tq_ctx* ctx, tq_profile* out) {
   out->encode_ms = ms[1];
   out->merge_launches = n[2];
   out->merge_ms = ms[2];
+  out->decode_kernel = ctx->decode_kernel;
   return TQ_OK;
 }
 

@@ -36,5 +36,12 @@ struct TcArgs {
 
 bool tc_supported(const tq_ctx* ctx);
 cudaError_t launch_decode_tc(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s);
+// Score constants of a context (Lloyd-Max Walsh weights, QJL coefficient, logit scale) into a.
+void tc_set_score_constants(const tq_ctx* ctx, TcArgs& a);
+// Split-K merge of the partials in a.parts (sequences with one part were written directly).
+cudaError_t launch_tc_merge(tq_ctx* ctx, TcArgs& a, int batch, cudaStream_t s);
+// tcgen05 score path (decode_hy.cu): 3-bit keys, 2-bit values, head_dim 128.
+bool hy_supported(const tq_ctx* ctx);
+cudaError_t launch_decode_hy(tq_ctx* ctx, TcArgs& a, int batch, uint8_t* qrec, cudaStream_t s);
 
 }  // namespace tq

@@ -21,6 +21,9 @@ constexpr int kMaxChunks = 8192;  // split-K chunks per sequence (merge weights 
 // fragments of up to 5 planes x 8 k-steps x 32 lanes, then 4 prep slices x 2 x kMaxRep partial
 // score offsets (floats).
 constexpr int kTcQueryU4 = 5 * 8 * 32 + 4 * 2 * kMaxRep / 4;
+// tcgen05 decode (decode_hy.cu) query record per (sequence, head group), bytes: the e4m3 query
+// operand (12 K-slices x 48 columns x 32 bytes), then 2 x 2 x kMaxRep floats (scales, offsets).
+constexpr int kHyQueryBytes = 12 * 48 * 32 + 4 * 4 * kMaxRep;
 
 // Small per-context tables passed by value as kernel parameters.
 struct CodeTables {
@@ -50,6 +53,8 @@ struct tq_ctx {
   uint4* d_sfrag_enc = nullptr; // S^T as fp16 high/low mma.sync B fragments (encode projection)
   uint32_t* d_err = nullptr;    // device error word
   int64_t launches = 0;
+  int decode_path = 0;          // TQ_DECODE_AUTO / _MMA_SYNC / _TCGEN05
+  const char* decode_kernel = nullptr;  // kernel of the last decode call (profiling reports)
   bool profiling = false;
   tq::ProfileKind prof[3];      // 0 decode, 1 encode, 2 merge
 };
@@ -64,7 +69,8 @@ void prof_stop(tq_ctx* ctx, int kind, cudaStream_t s);
 
 // Decode chunking policy shared by tq_workspace_size and tq_decode_attention.
 struct DecodePlan {
-  bool tensor_core;   // main layout, head_dim 128: decode_tc.cu
+  bool tensor_core;   // main layout, head_dim 128: decode_tc.cu (or decode_hy.cu)
+  bool hybrid;        // tensor-core path with the score on tcgen05: decode_hy.cu
   bool fused_prep;    // tensor-core path: each CTA builds its own query fragments (one-wave grids)
   int cta_warps;      // tensor-core path: 8 (at most one CTA per SM) or 4 warps per decode CTA
   int chunk_tokens;   // compressed tokens per split-K chunk (multiple of 16)

@@ -107,12 +107,15 @@ def allclose_report(got, ref, atol=2e-3, rtol=1e-3):
 
 # ---------------------------------------------------------------- decode scenarios
 def build_main_cache(seed, d, hkv, lengths, centroids, signs, sketch, shuffled=True, extra_blocks=0, value_bits=2,
-                     key_bits=3):
-    """Oracle-encoded pool + ring for sequences of the given total lengths."""
+                     key_bits=3, v_scale=1.0):
+    """Oracle-encoded pool + ring for sequences of the given total lengths (values multiplied by
+    v_scale before rounding to fp16, for large-magnitude value groups)."""
     bsz = len(lengths)
     lmax = max(max(lengths), 1)
     t_all = ((lmax + 15) // 16) * 16
     k, v = synth.kv_main(seed, bsz, hkv, t_all, d)
+    if v_scale != 1.0:
+        v = (v.astype(np.float32) * np.float32(v_scale)).astype(np.float16)
     max_blocks = max(t_all // 16, 1)
     bt = synth.block_table(seed, bsz, max_blocks, shuffled)
     nblk = bsz * max_blocks + extra_blocks

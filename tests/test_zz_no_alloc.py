@@ -9,12 +9,15 @@ entry point on the same inputs, for two calls in a row with different
 inputs, and check that a request larger than the array is refused.  This file
 is collected last so that a failure here comes after every other test.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
 
 import synth
 from gpu_cases import allclose_report, build_main_cache, make_ctx, to_dev
+from oracle import attention
 
 pytestmark = pytest.mark.gpu
 
@@ -47,18 +50,45 @@ def _both(ctx, e, q, hq, d):
     return out.cpu().numpy(), ref.cpu().numpy()
 
 
-def test_static_entry_point_matches_workspace_entry_point_twice(tq):
+@pytest.mark.parametrize("path", ["auto", "tcgen05"])
+def test_static_entry_point_matches_workspace_entry_point_twice(tq, path):
+    """Both entry points run the same kernels on the same plan, so their outputs are bit-identical;
+    both also agree with the oracle to the decode tolerance."""
     d, hkv, n_rep = 128, 4, 7
     hq = hkv * n_rep
     ctx, c, s, sk = make_ctx(tq, True, d, hq, hkv, 21)
+    ctx.set_decode_path(tq.TQ_DECODE_AUTO if path == "auto" else tq.TQ_DECODE_TCGEN05)
     for call, (seed, lengths) in enumerate([(21, [3000, 130, 1]), (22, [700, 2049, 64, 5000])]):
         e = build_main_cache(seed, d, hkv, lengths, c, s, sk)
         assert ctx.workspace_size(len(lengths), e["max_ctx"]) <= STATIC_BYTES
         q = synth.queries(seed, len(lengths), hq, d)
         got, ref = _both(ctx, e, q, hq, d)
-        ok, maxerr, nbad = allclose_report(got, ref)
-        assert ok, f"call {call}: max abs err {maxerr}, {nbad} bad"
-        assert np.all(np.isfinite(got))
+        assert np.array_equal(got, ref), f"call {call}: outputs differ (max {np.max(np.abs(got - ref))})"
+        orc = attention.decode_main(q, e["pool"], e["bt"], e["n_c"], e["ring_k"], e["ring_v"], e["n_b"], s, c, sk,
+                                    hkv)
+        ok, maxerr, nbad = allclose_report(got, orc)
+        assert ok, f"call {call}: max abs err {maxerr} against the oracle, {nbad} bad"
+
+
+def test_static_entry_point_checks_arguments_like_the_workspace_one(tq):
+    """Identical status codes for identical bad arguments, before the scratch-size check; batch 0 is
+    a no-op."""
+    lib, vp = tq.binding.lib, ctypes.c_void_p
+    ctx, c, s, sk = make_ctx(tq, True, 128, 8, 2, 25)
+    dummy = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    p = vp(dummy.data_ptr())
+    ws = vp(dummy.data_ptr())
+
+    def both(q, batch, max_ctx):
+        a = lib.tq_decode_attention(ctx.ptr, q, batch, p, 1, p, 1, p, None, None, None, max_ctx, p, ws,
+                                    dummy.numel(), None)
+        b = lib.tq_decode_attention_static(ctx.ptr, q, batch, p, 1, p, 1, p, None, None, None, max_ctx, p, None)
+        return a, b
+
+    assert both(p, 1, 100) == (tq.binding.TQ_ERR_INVALID_ARG,) * 2  # max_ctx not a multiple of 16
+    assert both(None, 1, 64) == (tq.binding.TQ_ERR_INVALID_ARG,) * 2  # NULL q
+    assert both(p, -1, 64) == (tq.binding.TQ_ERR_INVALID_ARG,) * 2
+    assert both(p, 0, 64) == (tq.binding.TQ_OK,) * 2
 
 
 def test_static_entry_point_refuses_oversized_requests(tq):
