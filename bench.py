@@ -11,10 +11,11 @@ in the alternate one) + fp16 ring tokens (4 d B per token-head) + fp16 queries
 + fp32 outputs.
 
 Workloads (synthetic inputs from ``synth``; no weights or datasets):
+  qwen2.5-7b-b8    28 layers, 28 / 4 heads, d 128, batch 8, 32768 tokens each, shuffled
+                   pages (default: the largest single-GPU workload)
   qwen3-0.6b-32k   28 layers, 16 q / 4 KV heads, d 128, batch 1, 32768-token prefix
-                   compressed in 128-token flushes, then decode steps (default)
+                   compressed in 128-token flushes, then decode steps
   tiny-1k          1 layer, 16 / 4, d 128, batch 1, 1024 tokens
-  qwen2.5-7b-b8    28 layers, 28 / 4, d 128, batch 8, 32768 tokens each, shuffled pages
   alt-d{64,128,256,512}  alternate layout, 8 / 8, batch 4, 65536 tokens, no ring
   qwen2.5-32b-ragged     1 of 64 layers, 40 / 8, d 128, batch 16, lengths U[1024, 131072]
   qwen2.5-7b-b8-v4       the batch-8 workload with 4-bit value codes
@@ -26,6 +27,14 @@ Launch: ``python bench.py [--gpus N --steps K --warmup W --workload NAME]``;
 for N > 1 under torchrun, each rank runs the same per-GPU workload (weak
 scaling, no data-path collective) and rank 0 prints one JSON line.
 ``--impl reference`` times the CPU oracle instead (the reference arm).
+
+On one GPU the line also carries ``configs``: every workload of CONFIG_SET
+(tiny-1k, qwen3-0.6b-32k, qwen2.5-7b-b8, alt-d64..512, qwen2.5-32b-ragged)
+timed a few steps each (--config-steps), with its decode-kernel fraction of
+the HBM peak, the back-to-back decode call time and the end-to-end figure;
+the Qwen3-0.6B entry adds the encode timed as 128-token ring flushes.  A
+workload whose step reads less than twice the L2 size is timed with an L2
+flush between steps.
 """
 from __future__ import annotations
 
@@ -76,7 +85,7 @@ WORKLOADS = {
     "alt-d128-vonly": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=128, ctx=65536, shuffled=False, seed=0,
                            kbits=16),
 }
-DEFAULT_WORKLOAD = "qwen3-0.6b-32k"
+DEFAULT_WORKLOAD = "qwen2.5-7b-b8"
 
 
 # ---------------------------------------------------------------------- helpers
@@ -127,17 +136,6 @@ def max_over_ranks(value: float, device="cpu") -> float:
 def aggregate_gbs(bytes_per_rank: int, ms_max: float, world: int) -> float:
     """Whole-job throughput: every rank moves ``bytes_per_rank`` (weak scaling) in ``ms_max``."""
     return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
-
-
-# DRAM bytes (read + write) of one decode-kernel launch, from the ncu captures summarised in
-# profiles/ (dram__bytes_read.sum + dram__bytes_write.sum).  An entry is valid only for the
-# kernel source it was captured on; a workload without one reports null.
-NCU_TRAFFIC = {
-    ("qwen3-0.6b-32k", "tc_decode_kernel"): 13254144,     # profiles/tc_decode_kernel__qwen3-0.6b-32k.md
-    ("qwen2.5-7b-b8", "tc_decode_kernel"): 109436928,     # profiles/tc_decode_kernel__qwen2.5-7b-b8.md
-    ("alt-d128", "decode_alt_v2_kernel"): 412128768,      # profiles/decode_alt_v2_kernel__alt-d128.md
-    ("alt-d128-vonly", "decode_alt_v2_kernel"): 647770624,  # profiles/decode_alt_v2_kernel__alt-d128-vonly.md
-}
 
 
 def measured_peaks():
@@ -227,6 +225,8 @@ class Layer:
         lay = tq.TQ_LAYOUT_MAIN if w["layout"] == "main" else tq.TQ_LAYOUT_ALT
         self.ctx = tq.Context(lay, w["d"], w["hq"], w["hkv"], w["seed"] + layer_idx,
                               value_bits=w.get("vbits"), key_bits=w.get("kbits"))
+        self.ctx.set_decode_path({"auto": tq.TQ_DECODE_AUTO, "mma_sync": tq.TQ_DECODE_MMA_SYNC,
+                                  "tcgen05": tq.TQ_DECODE_TCGEN05}[w.get("decode_path", "auto")])
         self.max_blocks = bt_np.shape[1]
         self.bt = torch.from_numpy(bt_np).cuda()
         nblk = bt_np.shape[0] * bt_np.shape[1]
@@ -284,8 +284,53 @@ def encode_prefix(tq, torch, w, lengths, k1, v1, layers, timed=True):
     return ev0.elapsed_time(ev1), n_tok_total
 
 
-def encode_throughput(tq, torch, w, layers, k1, v1, reps=3):
-    """Time tq_encode_flush alone on a 32768-token (or shorter) page-aligned prefix per layer."""
+L2_BYTES = 129 * 2**20  # GB300 L2
+
+
+class L2Flush:
+    """Writes a buffer four times the L2 size: called between timed steps whose inputs fit in L2."""
+
+    def __init__(self, torch):
+        self.buf = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def fp32_peak_tflops():
+    """FP32 FFMA peak from the unit counts: 152 SMs x 128 FP32 lanes x 2 FLOP x the measured maximum
+    SM clock (MEASURED_PEAKS.json sm_max_mhz, else the 2070 MHz nominal)."""
+    mhz = 2070.0
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    return 152 * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def encode_io_bytes(w):
+    """Algorithmic bytes per token-head of the encode: fp16 k and v in, the compressed record out."""
+    return 4 * w["d"] + record_bytes(w)
+
+
+def encode_fp32_flop(w):
+    """Algorithmic FP32 work per token-head of the main encode: the dense QJL projection S r (d x m
+    FFMA, m = d); the rotation, assignment and value quantisation add ~10 d operations."""
+    return 2 * w["d"] * w["d"] + 10 * w["d"] if w["layout"] == "main" else 12 * w["d"]
+
+
+def encode_fracs(w, token_heads_per_s):
+    hbm, _ = measured_peaks()
+    gbs = token_heads_per_s * encode_io_bytes(w) / 1e9
+    tflops = token_heads_per_s * encode_fp32_flop(w) / 1e12
+    return {"gbs": gbs, "frac_hbm": gbs / hbm, "tflops_fp32_equiv": tflops, "frac_fp32": tflops / fp32_peak_tflops(),
+            "io_bytes_per_token_head": encode_io_bytes(w), "fp32_flop_per_token_head": encode_fp32_flop(w)}
+
+
+def encode_throughput(tq, torch, w, layers, k1, v1, flush, reps=3):
+    """tq_encode_flush alone: (a) one call over a page-aligned prefix of up to 32768 tokens, and
+    (b) the same prefix as consecutive 128-token flushes, one call each (the ring-flush size of
+    the decode step), with an L2 flush before each repetition."""
     n = min(k1.shape[2], 32768) // 128 * 128
     kb, vb = k1[:, :, :n].contiguous(), v1[:, :, :n].contiguous()
     start = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -296,15 +341,48 @@ def encode_throughput(tq, torch, w, layers, k1, v1, reps=3):
         ctx.encode_flush(kb, vb, start, bt, scratch)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
+    ms_one = 0.0
     for _ in range(reps):
+        flush()
+        e0.record()
         ctx.encode_flush(kb, vb, start, bt, scratch)
-    e1.record()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_one += e0.elapsed_time(e1)
+    ms_one /= reps
+    # 128-token flushes: the prefix cut into ring buffers of 128 tokens ([1, Hkv, 128, d] each, as the
+    # decode step flushes them), start positions 0, 128, ... (captured in one graph)
+    nf = n // 128
+    rings_k = kb.view(1, w["hkv"], nf, 128, w["d"]).permute(2, 0, 1, 3, 4).contiguous()
+    rings_v = vb.view(1, w["hkv"], nf, 128, w["d"]).permute(2, 0, 1, 3, 4).contiguous()
+    slices_k = [rings_k[i] for i in range(nf)]
+    slices_v = [rings_v[i] for i in range(nf)]
+    starts = torch.arange(0, n, 128, dtype=torch.int32, device="cuda").view(nf, 1)
+
+    def flushes():
+        for i in range(nf):
+            ctx.encode_flush(slices_k[i], slices_v[i], starts[i], bt, scratch, n_tokens=128)
+    flushes()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
-    toks = n
-    return {"tokens_per_s": toks / (ms * 1e-3), "token_heads_per_s": toks * w["hkv"] / (ms * 1e-3),
-            "ms_per_call": ms, "tokens_per_call": toks}
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        flushes()
+    ms_fl = 0.0
+    for _ in range(reps):
+        flush()
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_fl += e0.elapsed_time(e1)
+    ms_fl /= reps
+    del g
+    th_one = n * w["hkv"] / (ms_one * 1e-3)
+    th_fl = n * w["hkv"] / (ms_fl * 1e-3)
+    return {"tokens_per_call": n, "ms_per_call": ms_one, "token_heads_per_s": th_one, "tokens_per_s": n / (ms_one * 1e-3),
+            **encode_fracs(w, th_one),
+            "flush128": {"calls": nf, "us_per_flush": ms_fl * 1e3 / nf, "token_heads_per_s": th_fl,
+                         "tokens_per_s": n / (ms_fl * 1e-3), **encode_fracs(w, th_fl)}}
 
 
 def dequant_throughput(torch, w, lay, lengths, reps=3, cap=32768):
@@ -391,33 +469,40 @@ class StepGraph:
         self.graph.replay()
 
 
-def decode_kernel_name(w):
-    """The decode kernel the library launches for this workload's compressed pages."""
-    n_rep = w["hq"] // w["hkv"]
-    if w["layout"] == "main":
-        return "tc_decode_kernel" if w["d"] == 128 else "decode_main_kernel"
-    nrg = n_rep // -(-n_rep // 8)
-    ok = (nrg == 1) or (nrg == 2 and w["d"] <= 256) or (nrg <= 4 and w["d"] <= 128)
-    return "decode_alt_v2_kernel" if ok else "decode_alt_kernel"
+def timed_replays(torch, fn, n, flush=None):
+    """Total ms of n calls of fn: one event pair around all of them, or, with an L2 flush between
+    calls (inputs smaller than L2), one event pair per call with the flush outside."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if flush is None:
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+    tot = 0.0
+    for _ in range(n):
+        flush()
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        tot += e0.elapsed_time(e1)
+    return tot
 
 
-def run_gpu(args, w, rank, world):
-    import torch
-
-    from kv_cache_quantization_tq_gb300.build import build
-
-    if rank == 0 or world == 1:
-        build()
-    if world > 1:
-        torch.distributed.barrier()
-    import kv_cache_quantization_tq_gb300 as tq
-
+def run_gpu(tq, torch, w, rank, world, steps, warmup, extras=True, sample_clocks=True):
+    """One workload on this rank's GPU: the timed decode steps, the per-launch decode-kernel times,
+    the back-to-back decode calls, the end-to-end step through host buffers, and (extras) the
+    encode and dequantise timings."""
     prof_steps = 3  # replays of the profiled graph (roofline events)
-    steps_total = args.warmup + args.steps + prof_steps + 64  # + end-to-end steps
+    steps_total = warmup + steps + prof_steps + 64  # + end-to-end steps
     lengths, k1, v1, layers = build_gpu_state(tq, torch, w, steps_total)
+    flush_op = L2Flush(torch)
     encode_prefix(tq, torch, w, lengths, k1, v1, layers)
-    enc = encode_throughput(tq, torch, w, layers, k1, v1)
-    deq = dequant_throughput(torch, w, layers[0], lengths)
+    enc = encode_throughput(tq, torch, w, layers, k1, v1, flush_op) if extras else None
+    deq = dequant_throughput(torch, w, layers[0], lengths) if extras else None
     bsz, hq, hkv, d, nl = w["batch"], w["hq"], w["hkv"], w["d"], w["layers"]
     main = w["layout"] == "main"
     g = torch.Generator(device="cuda")
@@ -432,9 +517,12 @@ def run_gpu(args, w, rank, world):
         after = [p + 1 for p in pos_list] if main else list(pos_list)
         return nl * step_bytes(w, after)
 
+    # a step whose inputs fit in L2 is timed with an L2 flush between steps
+    small = bytes_at(lengths) < 2 * L2_BYTES
+    flush = flush_op if small else None
     sg = StepGraph(torch, w, layers, lengths, max_ctx, ws, q, kn, vn)
     pos = list(lengths)
-    for _ in range(args.warmup):  # eager warm-up steps (same calls as the graph)
+    for _ in range(warmup):  # eager warm-up steps (same calls as the graph)
         sg.body()
         if main:
             pos = [p + 1 for p in pos]
@@ -446,25 +534,25 @@ def run_gpu(args, w, rank, world):
     if world > 1:
         torch.distributed.barrier()
     timed_bytes = 0
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        torch.cuda.synchronize()
-        e0.record()
-        for _ in range(args.steps):
-            sg.replay()
-        e1.record()
-        torch.cuda.synchronize()
-    for _ in range(args.steps):
+    if sample_clocks:
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            ms = timed_replays(torch, sg.replay, steps, flush)
+        clocks = clk.summary()
+    else:
+        ms = timed_replays(torch, sg.replay, steps, flush)
+        clocks = None
+    for _ in range(steps):
         timed_bytes += bytes_at(pos)
         if main:
             pos = [p + 1 for p in pos]
-    ms = e0.elapsed_time(e1)
     # the same step captured again with the library's CUDA events around every decode and merge
     # launch; a few replays after the timed region give the per-kernel durations
     for lay in layers:
         lay.ctx.profile_begin()
     prof_graph = sg.capture()
     for _ in range(prof_steps):
+        if flush:
+            flush()
         prof_graph.replay()
         if main:
             pos = [p + 1 for p in pos]
@@ -484,48 +572,48 @@ def run_gpu(args, w, rank, world):
         decode_calls()
     dgraph.replay()
     torch.cuda.synchronize()
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    d0.record()
-    for _ in range(prof_steps):
-        dgraph.replay()
-    d1.record()
-    torch.cuda.synchronize()
-    call_us = d0.elapsed_time(d1) / (prof_steps * nl) * 1e3
+    call_us = timed_replays(torch, dgraph.replay, prof_steps, flush) / (prof_steps * nl) * 1e3
     del dgraph
     if world > 1:
         ms = max_over_ranks(ms, device="cuda")
         torch.distributed.barrier()
     value = aggregate_gbs(timed_bytes, ms, world)
 
-    # dominant kernel: the fused decode kernel, timed by the library's CUDA
-    # events captured into the profiled step graph (its last replay)
+    # dominant kernel: the fused decode kernel, timed by the library's CUDA events captured into
+    # the profiled step graph (its last replay)
     dec_ms = sum(p["decode_ms"] for p in prof)
     dec_n = sum(p["decode_launches"] for p in prof)
+    kernel = prof[-1]["decode_kernel"]
     peak, peak_kind = measured_peaks()
     last_pos = [p - 1 for p in pos] if main else pos
     per_launch_bytes = bytes_at(last_pos) / nl
     achieved = per_launch_bytes / (dec_ms / max(dec_n, 1) * 1e-3) / 1e9 if dec_n else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak if achieved else None,
-                "traffic": NCU_TRAFFIC.get((args.workload, decode_kernel_name(w))),
-                "kernel": decode_kernel_name(w),
+                "traffic": ncu_traffic(w["name"], kernel),
+                "kernel": kernel,
                 "peak_source": peak_kind, "launches": dec_n, "avg_launch_us": dec_ms / max(dec_n, 1) * 1e3,
                 "merge_us_per_launch": sum(p["merge_ms"] for p in prof) / max(dec_n, 1) * 1e3,
                 "decode_call_us_back_to_back": call_us,
                 "bytes_per_launch": per_launch_bytes}
 
-    e2e = run_e2e(torch, w, layers, pos, max_ctx, ws, q, kn, vn, bytes_at)
-    return {
-        "value": value, "ms_per_step": ms / args.steps, "roofline": roofline, "encode": enc, "dequantize": deq, "e2e": e2e,
-        "gpu_launches": int(launches_per_step * args.steps), "clocks": clk.summary(), "lengths": lengths,
+    e2e = run_e2e(torch, w, layers, pos, max_ctx, ws, q, kn, vn, bytes_at, flush)
+    res = {
+        "value": value, "ms_per_step": ms / steps, "roofline": roofline, "encode": enc, "dequantize": deq, "e2e": e2e,
+        "gpu_launches": int(launches_per_step * steps), "clocks": clocks, "lengths": lengths,
+        "l2": ("L2 flushed between timed steps (step inputs below 2x L2)" if small
+               else "inputs larger than L2 (every step reads all layers' pools)"),
     }
+    del layers, k1, v1, q, kn, vn, ws, sg, flush_op
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
 
 
-def run_e2e(torch, w, layers, pos, max_ctx, ws, q, kn, vn, bytes_at, steps=16):
+def run_e2e(torch, w, layers, pos, max_ctx, ws, q, kn, vn, bytes_at, flush=None, steps=16):
     """Same decode step through the same C ABI, with the step's q, k, v copied in from pinned host
     memory and every layer's output copied back to pinned host memory inside the timed region
     (captured in the step graph)."""
-    nl = w["layers"]
     rng = np.random.default_rng(5)
     qh = torch.from_numpy(rng.standard_normal(tuple(q.shape)).astype(np.float16)).pin_memory()
     kh = torch.from_numpy(rng.standard_normal(tuple(kn.shape)).astype(np.float16)).pin_memory()
@@ -534,13 +622,7 @@ def run_e2e(torch, w, layers, pos, max_ctx, ws, q, kn, vn, bytes_at, steps=16):
     sg = StepGraph(torch, w, layers, pos, max_ctx, ws, q, kn, vn, out_host=out_h, in_host=(qh, kh, vh))
     sg.capture()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        sg.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    ms = timed_replays(torch, sg.replay, steps, flush)
     tot = 0
     main = w["layout"] == "main"
     p = list(pos)
@@ -552,6 +634,29 @@ def run_e2e(torch, w, layers, pos, max_ctx, ws, q, kn, vn, bytes_at, steps=16):
     d2h = out_h.numel() * 4
     return {"value": tot / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+def ncu_traffic(workload, kernel):
+    """DRAM bytes (read + write) of one launch of `kernel` on `workload`, from the ncu capture listed
+    in profiles/dram_traffic.json, if that capture was taken on the current source of the files the
+    kernel is built from (sha256 of each); otherwise None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not kernel or not os.path.exists(path):
+        return None
+    import hashlib
+
+    with open(path) as f:
+        entry = json.load(f).get(workload)
+    if not entry or entry.get("kernel") != kernel:
+        return None
+    for src, digest in entry.get("sources", {}).items():
+        p = os.path.join(ROOT, "kv_cache_quantization_tq_gb300", "csrc", src)
+        if not os.path.exists(p):
+            return None
+        with open(p, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != digest:
+                return None
+    return int(entry["dram_bytes"])
 
 
 # ---------------------------------------------------------------------- CPU oracle arm
@@ -643,6 +748,22 @@ def oracle_sample_len(w):
 
 
 # ---------------------------------------------------------------------- main
+CONFIG_SET = ["tiny-1k", "qwen3-0.6b-32k", "qwen2.5-7b-b8", "alt-d64", "alt-d128", "alt-d256", "alt-d512",
+              "qwen2.5-32b-ragged"]
+
+
+def config_summary(res, peak):
+    r = res["roofline"]
+    out = {"value": res["value"], "unit": "GB/s", "frac_of_hbm_peak": res["value"] / peak,
+           "ms_per_step": res["ms_per_step"], "decode_kernel": r["kernel"], "decode_kernel_gbs": r["achieved"],
+           "decode_kernel_frac": r["frac"], "decode_kernel_avg_launch_us": r["avg_launch_us"],
+           "decode_call_us_back_to_back": r["decode_call_us_back_to_back"], "e2e_gbs": res["e2e"]["value"],
+           "l2": res["l2"]}
+    if res.get("encode"):
+        out["encode"] = res["encode"]
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -651,21 +772,31 @@ def main():
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload block of the other configs")
+    ap.add_argument("--config-steps", type=int, default=10, help="timed steps of each workload in that block")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling runs)")
+    ap.add_argument("--decode-path", default="auto", choices=["auto", "mma_sync", "tcgen05"],
+                    help="main-layout decode kernels at head_dim 128 (tq_set_decode_path)")
     args = ap.parse_args()
-    w = dict(WORKLOADS[args.workload])
-    if args.layers:
-        w["layers"] = args.layers
 
+    def workload(name):
+        w = dict(WORKLOADS[name])
+        w["name"] = name
+        if args.layers:
+            w["layers"] = args.layers
+        w["decode_path"] = args.decode_path
+        return w
+
+    w = workload(args.workload)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     config = {"workload": args.workload, "layout": w["layout"], "layers": w["layers"], "batch": w["batch"],
               "q_heads": w["hq"], "kv_heads": w["hkv"], "head_dim": w["d"],
-              "context": w["ctx"] if w["ctx"] is not None else f"U[{w['lo']},{w['hi']}]",
-              "l2": "inputs larger than L2 (every step reads all layers' pools)"}
+              "context": w["ctx"] if w["ctx"] is not None else f"U[{w['lo']},{w['hi']}]"}
     config["value_bits"] = w.get("vbits", 2 if w["layout"] == "main" else 3)
     config["key_bits"] = w.get("kbits", 3 if w["layout"] == "main" else 8)
+    config["decode_path"] = args.decode_path
 
     if args.impl == "reference":
         if rank != 0:
@@ -675,6 +806,7 @@ def main():
             run_oracle(w, 1, sample_len, budget_s=0)
         val, dt, nbytes, reps = run_oracle(w, max(1, args.steps), sample_len, budget_s=60.0)
         sample = f"oracle decode of one sequence x {w['hkv']} KV heads at {sample_len} tokens per step"
+        config["l2"] = "host oracle (CPU)"
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
                 "steps": reps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
@@ -689,7 +821,28 @@ def main():
     if world > 1:
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
-    res = run_gpu(args, w, rank, world)
+    from kv_cache_quantization_tq_gb300.build import build
+
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        torch.distributed.barrier()
+    import kv_cache_quantization_tq_gb300 as tq
+
+    res = run_gpu(tq, torch, w, rank, world, args.steps, args.warmup)
+    config["l2"] = res["l2"]
+    peak, _ = measured_peaks()
+    configs = None
+    if world == 1 and not args.no_configs:
+        # every other workload of the set, a few steps each, on the same GPU (single-GPU runs only)
+        configs = {}
+        for name in CONFIG_SET:
+            if name == args.workload:
+                continue
+            r = run_gpu(tq, torch, workload(name), rank, world, args.config_steps, 3,
+                        extras=(name == "qwen3-0.6b-32k"), sample_clocks=False)
+            configs[name] = config_summary(r, peak)
+        configs[args.workload] = config_summary(res, peak)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -702,14 +855,13 @@ def main():
                "sample": f"{reps} oracle decodes of one sequence x {w['hkv']} KV heads at {sample_len} tokens "
                          f"({nbytes / 1e6:.1f} MB of records each), {dt:.2f} s each",
                "value_one_thread": oracle_one_thread(args.workload)}
-    peak, _ = measured_peaks()
     line = {
         "metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
         "frac_of_hbm_peak": res["value"] / world / peak,
         "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"], "gpu_launches": res["gpu_launches"],
-        "clocks": res["clocks"], "encode": res["encode"], "dequantize": res["dequantize"],
+        "clocks": res["clocks"], "encode": res["encode"], "dequantize": res["dequantize"], "configs": configs,
     }
     print(json.dumps(line))
     if world > 1:
