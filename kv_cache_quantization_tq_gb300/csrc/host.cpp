@@ -331,6 +331,18 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
       per = (total_pages + target - 1) / target;
       per = std::max<int64_t>(16, std::min<int64_t>(64, per));
       per = (per + 3) / 4 * 4;
+      // One wave: when every sequence's chunks (plus its ring item) fit in kOneWaveCtas CTAs per
+      // SM with chunks of at most kOneWaveMaxPages pages, size the chunks for exactly that, so
+      // no SM idles through a last partial wave.
+      constexpr int kOneWaveCtas = 3;
+      constexpr int64_t kOneWaveMaxPages = 256;
+      const int64_t bh = (int64_t)batch * hkv * groups;
+      const int64_t slots = (int64_t)kOneWaveCtas * std::max(1, ctx->sm_count);
+      const int64_t cps = (slots - bh) / std::max<int64_t>(1, bh);  // chunks per sequence and head group
+      if (cps >= 1) {
+        const int64_t per1 = ((pages + cps - 1) / cps + 3) / 4 * 4;
+        if (per1 > per && per1 <= kOneWaveMaxPages) per = per1;
+      }
     }
   } else {
     // about 8 CTAs per SM worth of split-K chunks, each between 4 and 64 pages
