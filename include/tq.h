@@ -310,6 +310,26 @@ tq_status tq_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, const int
                         const int32_t* n_compressed, const void* ring_k, const void* ring_v, const int32_t* n_buf,
                         int batch, int max_tokens, void* k_out, void* v_out, cudaStream_t stream);
 
+/* tq_dequantize with bfloat16 outputs (the guide's "FP16/BF16" materialisation): the same
+ * reconstruction in fp32, rounded to nearest even bf16; k_out, v_out device bf16
+ * [batch][Hkv][max_tokens][d]; ring rows are converted from fp16.  Same checks and errors. */
+tq_status tq_dequantize_bf16(tq_ctx* ctx, const void* pool, int num_blocks, const int32_t* block_table,
+                             int max_blocks, const int32_t* n_compressed, const void* ring_k, const void* ring_v,
+                             const int32_t* n_buf, int batch, int max_tokens, void* k_out, void* v_out,
+                             cudaStream_t stream);
+
+/* Prefill admission rule of the materialisation (vllm-metal TurboQuant guide, advanced settings,
+ * VLLM_METAL_TQ_PREFILL): a prefill chunk of query_tokens new tokens over history_tokens
+ * compressed tokens materialises the history (tq_dequantize, then dense attention) when
+ *   history_tokens >= 8192, and
+ *   query_tokens >= 64 at head_dim 128 (the calibrated geometry), else >= max(128, head_dim / 2),
+ *   and the dense K and V (history x num_kv_heads x head_dim x 2 tensors x 2 bytes) fit in
+ *   max_mib MiB (VLLM_METAL_TQ_PREFILL_MAX_MIB: max_mib < 0 no cap, 0 never materialise).
+ * Otherwise (decode steps, short suffixes) the compressed path stays.  Host only, no CUDA call.
+ * Returns 1 (materialise), 0 (stay compressed) or -1 (negative counts, head_dim or heads <= 0). */
+int tq_should_materialize(int64_t history_tokens, int64_t query_tokens, int head_dim, int num_kv_heads,
+                          int64_t max_mib);
+
 /* ------------------------------------------------------------------ bit packing */
 
 /* Pack n codes (each < 2^bits, 1 <= bits <= 8) into a little-endian,

@@ -21,6 +21,7 @@ _EXPORTS = (
     "tq_lloyd_max",
     "tq_pack",
     "tq_pack_host",
+    "tq_should_materialize",
     "tq_unpack",
     "tq_unpack_host",
 )

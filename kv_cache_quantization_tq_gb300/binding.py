@@ -83,6 +83,8 @@ _SIGS = {
     "tq_decode_attention": (_i, [_vp, _vp, _i, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "tq_decode_attention_static": (_i, [_vp, _vp, _i, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp]),
     "tq_dequantize": (_i, [_vp, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp]),
+    "tq_dequantize_bf16": (_i, [_vp, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp]),
+    "tq_should_materialize": (_i, [_i64, _i64, _i, _i, _i64]),
     "tq_pack": (_i, [_vp, _i64, _i, _vp, _vp]),
     "tq_unpack": (_i, [_vp, _i64, _i, _vp, _vp]),
     "tq_pack_host": (_i, [_vp, _i64, _i, _vp]),
@@ -143,6 +145,15 @@ def tq_config_init(layout: int, head_dim: int, num_q_heads: int, num_kv_heads: i
     cfg = tq_config()
     _check(lib.tq_config_init(C.byref(cfg), layout, head_dim, num_q_heads, num_kv_heads, seed), "tq_config_init")
     return cfg
+
+
+def tq_should_materialize(history_tokens: int, query_tokens: int, head_dim: int, num_kv_heads: int,
+                          max_mib: int = -1) -> bool:
+    """The prefill admission rule of the materialisation (host only); ValueError on bad arguments."""
+    r = lib.tq_should_materialize(history_tokens, query_tokens, head_dim, num_kv_heads, max_mib)
+    if r < 0:
+        raise ValueError("tq_should_materialize: negative counts, or head_dim / num_kv_heads <= 0")
+    return bool(r)
 
 
 def tq_config_check(cfg: tq_config) -> int:
@@ -350,23 +361,28 @@ class Context:
 
     def dequantize(self, pool, block_table, n_compressed, k_out, v_out, ring_k=None, ring_v=None, n_buf=None,
                    stream=None):
-        """tq_dequantize: rows 0..n_compressed[b]-1 of k_out / v_out [batch, Hkv, max_tokens, d] (fp16) from
-        the pool, followed by the n_buf[b] ring tokens when a ring is given."""
+        """tq_dequantize (fp16 k_out / v_out) or tq_dequantize_bf16 (bf16 k_out / v_out): rows
+        0..n_compressed[b]-1 of k_out / v_out [batch, Hkv, max_tokens, d] from the pool, followed by the
+        n_buf[b] ring tokens when a ring is given."""
         import torch
 
         bsz = k_out.shape[0]
         shape = (bsz, self.num_kv_heads, k_out.shape[2], self.head_dim)
         if tuple(k_out.shape) != shape or tuple(v_out.shape) != shape:
-            raise ValueError("k_out and v_out must be [batch, Hkv, max_tokens, d] fp16")
+            raise ValueError("k_out and v_out must be [batch, Hkv, max_tokens, d]")
+        if k_out.dtype not in (torch.float16, torch.bfloat16) or v_out.dtype != k_out.dtype:
+            raise ValueError("k_out and v_out must both be fp16 or both bf16")
+        fn, name = ((lib.tq_dequantize_bf16, "tq_dequantize_bf16") if k_out.dtype == torch.bfloat16
+                    else (lib.tq_dequantize, "tq_dequantize"))
         self._check_pool(pool)
         self._check_bt(block_table, bsz)
-        _check(lib.tq_dequantize(self.ptr, _dev(pool, torch.uint8, "pool"), pool.shape[0],
-                                 _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
-                                 _dev(n_compressed, torch.int32, "n_compressed"),
-                                 _dev(ring_k, torch.float16, "ring_k"), _dev(ring_v, torch.float16, "ring_v"),
-                                 _dev(n_buf, torch.int32, "n_buf"), bsz, k_out.shape[2],
-                                 _dev(k_out, torch.float16, "k_out"), _dev(v_out, torch.float16, "v_out"),
-                                 _stream(stream)), "tq_dequantize")
+        _check(fn(self.ptr, _dev(pool, torch.uint8, "pool"), pool.shape[0],
+                  _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
+                  _dev(n_compressed, torch.int32, "n_compressed"),
+                  _dev(ring_k, torch.float16, "ring_k"), _dev(ring_v, torch.float16, "ring_v"),
+                  _dev(n_buf, torch.int32, "n_buf"), bsz, k_out.shape[2],
+                  _dev(k_out, k_out.dtype, "k_out"), _dev(v_out, v_out.dtype, "v_out"),
+                  _stream(stream)), name)
 
     # -- diagnostics
     def device_errors(self, stream=None) -> int:

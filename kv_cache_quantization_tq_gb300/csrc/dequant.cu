@@ -20,6 +20,10 @@
 // The rest is warp-per-token work: codes from the bit planes, the butterfly in
 // registers and shuffles, coalesced fp16 stores.  The exact recent buffer is
 // appended after the compressed tokens by a copy kernel.
+#include <cuda_bf16.h>
+
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace tq {
@@ -35,8 +39,8 @@ struct DqArgs {
   const __half* ring_v;
   const int32_t* n_buf;
   int max_tokens;
-  __half* k_out;
-  __half* v_out;
+  void* k_out;   // fp16 or bf16 [batch][Hkv][max_tokens][d] (the kernels' OUT type)
+  void* v_out;
   int hkv;
   const float* signs;
   const uint4* sfrag;   // S as mma.sync B fragments (back-projection order), fp16 high / low
@@ -46,6 +50,10 @@ struct DqArgs {
   float qjl_coef;       // sqrt(pi/2) / m
   uint32_t* err;
 };
+
+// Output element types of the materialisation: fp16 or bf16, rounded to nearest even from fp32.
+__device__ __forceinline__ void store_out(__half* p, float v) { *p = __float2half_rn(v); }
+__device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 __device__ __forceinline__ void mma_f16_acc(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -125,13 +133,18 @@ struct MainDq {
   static constexpr int NT = (D / 8) / WPP;                 // n-tiles (8 outputs) per warp
   static constexpr int KS = D / 16;                        // k-steps (16 sketch rows; m = d)
   static constexpr size_t SMEM_TILES = (size_t)PAGES * TILE;
-  static constexpr size_t SMEM_CORR = sizeof(float) * TB * D; // S^T (2 sigma - 1) as [token][i]
+  // S^T (2 sigma - 1) as [token][i], rows padded by 8 floats so that the fragment stores of a
+  // half-warp (rows g = 0..3 / 4..7, 8-byte pairs 2t) fall on 16 distinct bank pairs
+  static constexpr int CORR_STRIDE = D + 8;
+  static constexpr size_t SMEM_CORR = sizeof(float) * TB * CORR_STRIDE;
   static constexpr size_t SMEM = SMEM_TILES + SMEM_CORR;
 };
 
-template <int D, int VB>
+template <int D, int VB, typename OUT>
 __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
   using C = MainDq<D, VB>;
+  OUT* k_out = static_cast<OUT*>(a.k_out);
+  OUT* v_out = static_cast<OUT*>(a.v_out);
   constexpr int E = C::E;
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* tiles = smem;
@@ -182,8 +195,8 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
           mma_f16_acc(acc[j], al, bv.z, bv.w);
         }
       }
-      float* c0 = corr + (page * 16 + g) * D;
-      float* c1 = c0 + 8 * D;
+      float* c0 = corr + (page * 16 + g) * C::CORR_STRIDE;
+      float* c1 = c0 + 8 * C::CORR_STRIDE;
 #pragma unroll
       for (int j = 0; j < C::NT; ++j) {
         const int i = 8 * (nt0 + j) + 2 * t;
@@ -215,7 +228,7 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
       int idx = (int)((kh[e] >> bit) & 1u);
       if (kb >= 3) idx = (idx << 1) | (int)((kl[e] >> bit) & 1u);
       if (kb == 4) idx = (idx << 1) | (int)((k3[e] >> bit) & 1u);
-      x[e] = fmaf(a.qjl_coef * nr, corr[tt * D + coord_of(e, lane)], sel8(a.tab, idx));
+      x[e] = fmaf(a.qjl_coef * nr, corr[tt * C::CORR_STRIDE + coord_of(e, lane)], sel8(a.tab, idx));
     }
     wht_warp<E>(x, lane);
     const size_t row = (((size_t)b * a.hkv + h) * a.max_tokens + tok0 + tt) * D;
@@ -225,10 +238,10 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int c = coord_of(e, lane);
-      a.k_out[row + c] = __float2half_rn(nk * (x[e] * sg[e] * rs));
+      store_out(k_out + row + c, nk * (x[e] * sg[e] * rs));
       const __half2 smn = *reinterpret_cast<const __half2*>(tile + o_vsm + (slot * (D / 32) + e) * 4);
       const float q = (float)((vq[c] >> vbit) & ((1u << VB) - 1u));
-      a.v_out[row + c] = __float2half_rn(fmaf(__low2float(smn), q, __high2float(smn)));
+      store_out(v_out + row + c, fmaf(__low2float(smn), q, __high2float(smn)));
     }
   }
 }
@@ -248,8 +261,8 @@ struct AltDq {
 // Key coordinate c of token `slot` of a staged alternate-layout page: the fp16 key itself (kb 16),
 // or mn + s code with the code a byte (kb 8) or taken from the token's little-endian kb-bit stream.
 template <int D>
-__device__ __forceinline__ __half alt_key(const uint8_t* tile, int o_ksm, int slot, int c, int kb) {
-  if (kb == 16) return reinterpret_cast<const __half*>(tile)[slot * D + c];
+__device__ __forceinline__ float alt_key(const uint8_t* tile, int o_ksm, int slot, int c, int kb) {
+  if (kb == 16) return __half2float(reinterpret_cast<const __half*>(tile)[slot * D + c]);
   const __half2 smn = *reinterpret_cast<const __half2*>(tile + o_ksm + (slot * (D / 32) + (c >> 5)) * 4);
   int kq;
   if (kb == 8) {
@@ -261,12 +274,14 @@ __device__ __forceinline__ __half alt_key(const uint8_t* tile, int o_ksm, int sl
     const uint32_t khi = (kbit & 31) + kb > 32 ? kw[(kbit >> 5) + 1] : 0u;
     kq = (int)(__funnelshift_r(klo, khi, kbit & 31) & ((1u << kb) - 1u));
   }
-  return __float2half_rn(fmaf(__low2float(smn), (float)kq, __high2float(smn)));
+  return fmaf(__low2float(smn), (float)kq, __high2float(smn));
 }
 
-template <int D>
+template <int D, typename OUT>
 __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
   using C = AltDq<D>;
+  OUT* k_out = static_cast<OUT*>(a.k_out);
+  OUT* v_out = static_cast<OUT*>(a.v_out);
   constexpr int E = C::E;
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ bool ok[C::TB / 16];
@@ -297,7 +312,7 @@ __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int c = coord_of(e, lane);
-      a.k_out[row + c] = alt_key<D>(tile, o_ksm, slot, c, kb);
+      store_out(k_out + row + c, alt_key<D>(tile, o_ksm, slot, c, kb));
       const int bit = vb * c;  // index c of the token's little-endian vb-bit stream
       const uint32_t lo = vi[bit >> 5];
       const uint32_t hi = (bit & 31) + vb > 32 ? vi[(bit >> 5) + 1] : 0u;
@@ -307,13 +322,14 @@ __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int c = coord_of(e, lane);
-      a.v_out[row + c] = __float2half_rn(nv * (x[e] * sg[e] * rs));
+      store_out(v_out + row + c, nv * (x[e] * sg[e] * rs));
     }
   }
 }
 
 // ------------------------------------------------------------------ exact recent buffer
 // Ring slots 0 .. n_buf-1 hold positions n_tokens .. n_tokens + n_buf - 1.
+template <typename OUT>
 __global__ void __launch_bounds__(256) dequant_ring_kernel(DqArgs a, int d) {
   const int b = blockIdx.y, h = blockIdx.x;
   const int n = dq_ntok(a, b);
@@ -324,10 +340,24 @@ __global__ void __launch_bounds__(256) dequant_ring_kernel(DqArgs a, int d) {
   }
   const size_t src = ((size_t)b * a.hkv + h) * kRing * d;
   const size_t dst = (((size_t)b * a.hkv + h) * a.max_tokens + n) * d;
-  const int n16 = nb * d / 8;  // 16-byte chunks (d is a multiple of 64)
+  const int n16 = nb * d / 8;  // 16-byte chunks of fp16 (d is a multiple of 64)
+  OUT* k_out = static_cast<OUT*>(a.k_out);
+  OUT* v_out = static_cast<OUT*>(a.v_out);
   for (int i = threadIdx.x; i < n16; i += blockDim.x) {
-    reinterpret_cast<uint4*>(a.k_out + dst)[i] = reinterpret_cast<const uint4*>(a.ring_k + src)[i];
-    reinterpret_cast<uint4*>(a.v_out + dst)[i] = reinterpret_cast<const uint4*>(a.ring_v + src)[i];
+    const uint4 kv = reinterpret_cast<const uint4*>(a.ring_k + src)[i];
+    const uint4 vv = reinterpret_cast<const uint4*>(a.ring_v + src)[i];
+    if (std::is_same<OUT, __half>::value) {  // fp16 rows are copied as they are
+      reinterpret_cast<uint4*>(k_out + dst)[i] = kv;
+      reinterpret_cast<uint4*>(v_out + dst)[i] = vv;
+    } else {
+      const __half* kh = reinterpret_cast<const __half*>(&kv);
+      const __half* vh = reinterpret_cast<const __half*>(&vv);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        store_out(k_out + dst + 8 * i + j, __half2float(kh[j]));
+        store_out(v_out + dst + 8 * i + j, __half2float(vh[j]));
+      }
+    }
   }
 }
 
@@ -342,10 +372,11 @@ cudaError_t launch_dq(K kern, const DqArgs& a, int batch, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, const int32_t* block_table,
-                              int max_blocks, const int32_t* n_tokens, const void* ring_k, const void* ring_v,
-                              const int32_t* n_buf, int batch, int max_tokens, void* k_out, void* v_out,
-                              cudaStream_t s) {
+template <typename OUT>
+cudaError_t launch_dequantize_t(tq_ctx* ctx, const void* pool, int num_blocks, const int32_t* block_table,
+                                int max_blocks, const int32_t* n_tokens, const void* ring_k, const void* ring_v,
+                                const int32_t* n_buf, int batch, int max_tokens, void* k_out, void* v_out,
+                                cudaStream_t s) {
   DqArgs a{};
   a.pool = static_cast<const uint8_t*>(pool);
   a.num_blocks = num_blocks;
@@ -356,8 +387,8 @@ cudaError_t launch_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, con
   a.ring_v = static_cast<const __half*>(ring_v);
   a.n_buf = n_buf;
   a.max_tokens = max_tokens;
-  a.k_out = static_cast<__half*>(k_out);
-  a.v_out = static_cast<__half*>(v_out);
+  a.k_out = k_out;
+  a.v_out = v_out;
   a.hkv = ctx->cfg.num_kv_heads;
   a.signs = ctx->d_signs;
   a.sfrag = ctx->d_sfrag;
@@ -372,29 +403,39 @@ cudaError_t launch_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, con
   cudaError_t e = cudaErrorInvalidValue;
   if (max_tokens > 0) {
     switch (d) {
-      case 64: e = main ? (vb == 4 ? launch_dq<MainDq<64, 4>>(dequant_main_kernel<64, 4>, a, batch, s)
-                                  : launch_dq<MainDq<64, 2>>(dequant_main_kernel<64, 2>, a, batch, s))
-                        : launch_dq<AltDq<64>>(dequant_alt_kernel<64>, a, batch, s); break;
-      case 128: e = main ? (vb == 4 ? launch_dq<MainDq<128, 4>>(dequant_main_kernel<128, 4>, a, batch, s)
-                                  : launch_dq<MainDq<128, 2>>(dequant_main_kernel<128, 2>, a, batch, s))
-                         : launch_dq<AltDq<128>>(dequant_alt_kernel<128>, a, batch, s); break;
-      case 256: e = main ? (vb == 4 ? launch_dq<MainDq<256, 4>>(dequant_main_kernel<256, 4>, a, batch, s)
-                                  : launch_dq<MainDq<256, 2>>(dequant_main_kernel<256, 2>, a, batch, s))
-                         : launch_dq<AltDq<256>>(dequant_alt_kernel<256>, a, batch, s); break;
-      case 512: e = main ? (vb == 4 ? launch_dq<MainDq<512, 4>>(dequant_main_kernel<512, 4>, a, batch, s)
-                                  : launch_dq<MainDq<512, 2>>(dequant_main_kernel<512, 2>, a, batch, s))
-                         : launch_dq<AltDq<512>>(dequant_alt_kernel<512>, a, batch, s); break;
+      case 64: e = main ? (vb == 4 ? launch_dq<MainDq<64, 4>>(dequant_main_kernel<64, 4, OUT>, a, batch, s)
+                                  : launch_dq<MainDq<64, 2>>(dequant_main_kernel<64, 2, OUT>, a, batch, s))
+                        : launch_dq<AltDq<64>>(dequant_alt_kernel<64, OUT>, a, batch, s); break;
+      case 128: e = main ? (vb == 4 ? launch_dq<MainDq<128, 4>>(dequant_main_kernel<128, 4, OUT>, a, batch, s)
+                                  : launch_dq<MainDq<128, 2>>(dequant_main_kernel<128, 2, OUT>, a, batch, s))
+                         : launch_dq<AltDq<128>>(dequant_alt_kernel<128, OUT>, a, batch, s); break;
+      case 256: e = main ? (vb == 4 ? launch_dq<MainDq<256, 4>>(dequant_main_kernel<256, 4, OUT>, a, batch, s)
+                                  : launch_dq<MainDq<256, 2>>(dequant_main_kernel<256, 2, OUT>, a, batch, s))
+                         : launch_dq<AltDq<256>>(dequant_alt_kernel<256, OUT>, a, batch, s); break;
+      case 512: e = main ? (vb == 4 ? launch_dq<MainDq<512, 4>>(dequant_main_kernel<512, 4, OUT>, a, batch, s)
+                                  : launch_dq<MainDq<512, 2>>(dequant_main_kernel<512, 2, OUT>, a, batch, s))
+                         : launch_dq<AltDq<512>>(dequant_alt_kernel<512, OUT>, a, batch, s); break;
     }
     if (e != cudaSuccess) return e;
     ctx->launches++;
   }
   if (n_buf) {
-    dequant_ring_kernel<<<dim3(a.hkv, batch), 256, 0, s>>>(a, d);
+    dequant_ring_kernel<OUT><<<dim3(a.hkv, batch), 256, 0, s>>>(a, d);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ctx->launches++;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, const int32_t* block_table,
+                              int max_blocks, const int32_t* n_tokens, const void* ring_k, const void* ring_v,
+                              const int32_t* n_buf, int batch, int max_tokens, void* k_out, void* v_out,
+                              bool bf16, cudaStream_t s) {
+  return bf16 ? launch_dequantize_t<__nv_bfloat16>(ctx, pool, num_blocks, block_table, max_blocks, n_tokens, ring_k,
+                                                   ring_v, n_buf, batch, max_tokens, k_out, v_out, s)
+              : launch_dequantize_t<__half>(ctx, pool, num_blocks, block_table, max_blocks, n_tokens, ring_k, ring_v,
+                                            n_buf, batch, max_tokens, k_out, v_out, s);
 }
 
 size_t sketch_frag_bytes(int d) { return (size_t)(d / 16) * (d / 8) * 32 * sizeof(uint4); }

@@ -572,9 +572,10 @@ tq_status tq_decode_attention(tq_ctx* ctx, const void* q, int batch, const void*
                                        ring_k, ring_v, n_buf, max_ctx, out, workspace, stream));
 }
 
-tq_status tq_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, const int32_t* block_table, int max_blocks,
-                        const int32_t* n_compressed, const void* ring_k, const void* ring_v, const int32_t* n_buf,
-                        int batch, int max_tokens, void* k_out, void* v_out, cudaStream_t stream) {
+static tq_status dequantize_common(tq_ctx* ctx, const void* pool, int num_blocks, const int32_t* block_table,
+                                   int max_blocks, const int32_t* n_compressed, const void* ring_k, const void* ring_v,
+                                   const int32_t* n_buf, int batch, int max_tokens, void* k_out, void* v_out, bool bf16,
+                                   cudaStream_t stream) {
   if (!ctx || batch < 0 || max_blocks < 0 || num_blocks < 0 || max_tokens < 0) return TQ_ERR_INVALID_ARG;
   if (batch == 0 || max_tokens == 0) return TQ_OK;
   if (!k_out || !v_out || !n_compressed || !block_table || !pool) return TQ_ERR_INVALID_ARG;
@@ -582,7 +583,37 @@ tq_status tq_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, const int
   if ((((uintptr_t)k_out) | ((uintptr_t)v_out)) & 15) return TQ_ERR_INVALID_ARG;
   if (n_buf && ((((uintptr_t)ring_k) | ((uintptr_t)ring_v)) & 15)) return TQ_ERR_INVALID_ARG;
   return cuda_status(tq::launch_dequantize(ctx, pool, num_blocks, block_table, max_blocks, n_compressed, ring_k,
-                                           ring_v, n_buf, batch, max_tokens, k_out, v_out, stream));
+                                           ring_v, n_buf, batch, max_tokens, k_out, v_out, bf16, stream));
+}
+
+tq_status tq_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, const int32_t* block_table, int max_blocks,
+                        const int32_t* n_compressed, const void* ring_k, const void* ring_v, const int32_t* n_buf,
+                        int batch, int max_tokens, void* k_out, void* v_out, cudaStream_t stream) {
+  return dequantize_common(ctx, pool, num_blocks, block_table, max_blocks, n_compressed, ring_k, ring_v, n_buf, batch,
+                           max_tokens, k_out, v_out, false, stream);
+}
+
+tq_status tq_dequantize_bf16(tq_ctx* ctx, const void* pool, int num_blocks, const int32_t* block_table,
+                             int max_blocks, const int32_t* n_compressed, const void* ring_k, const void* ring_v,
+                             const int32_t* n_buf, int batch, int max_tokens, void* k_out, void* v_out,
+                             cudaStream_t stream) {
+  return dequantize_common(ctx, pool, num_blocks, block_table, max_blocks, n_compressed, ring_k, ring_v, n_buf, batch,
+                           max_tokens, k_out, v_out, true, stream);
+}
+
+int tq_should_materialize(int64_t history_tokens, int64_t query_tokens, int head_dim, int num_kv_heads,
+                          int64_t max_mib) {
+  if (history_tokens < 0 || query_tokens < 0 || head_dim <= 0 || num_kv_heads <= 0) return -1;
+  if (max_mib == 0) return 0;                          // materialisation switched off
+  if (history_tokens < 8192) return 0;                 // short histories stay on the compressed path
+  const int64_t threshold = head_dim == 128 ? 64 : std::max<int64_t>(128, head_dim / 2);
+  if (query_tokens < threshold) return 0;              // decode steps and short suffixes
+  if (max_mib > 0) {
+    // dense K and V of the history, 2 bytes per element
+    const double bytes = (double)history_tokens * num_kv_heads * head_dim * 2.0 * 2.0;
+    if (bytes > (double)max_mib * 1048576.0) return 0;
+  }
+  return 1;
 }
 
 tq_status tq_pack(const uint8_t* codes, int64_t n, int bits, void* dst, cudaStream_t stream) {

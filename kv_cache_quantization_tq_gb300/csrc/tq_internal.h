@@ -96,7 +96,7 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
 cudaError_t launch_dequantize(tq_ctx* ctx, const void* pool, int num_blocks, const int32_t* block_table,
                               int max_blocks, const int32_t* n_tokens, const void* ring_k, const void* ring_v,
                               const int32_t* n_buf, int batch, int max_tokens, void* k_out, void* v_out,
-                              cudaStream_t s);
+                              bool bf16, cudaStream_t s);
 size_t sketch_frag_bytes(int d);
 cudaError_t build_sketch_frags(const float* sketch, int d, void* frag);
 cudaError_t build_sketch_frags_enc(const float* sketch, int d, void* frag);

@@ -119,3 +119,50 @@ def test_bad_device_values_are_flagged_and_skipped():
                    to_dev(e["ring_k"]), to_dev(e["ring_v"]), to_dev(nb))
     torch.cuda.synchronize()
     assert ctx.device_errors() & tq.binding.TQ_DEVERR_RING
+
+
+def _check_close_bf16(got_bf16, ref64, what):
+    """bf16 outputs: within half a bf16 step of the oracle's value (2^-8 relative at most), plus the
+    fp32 arithmetic of the row's butterfly, as for fp16."""
+    got = got_bf16.float().cpu().numpy().astype(np.float64)
+    half_ulp = np.maximum(np.abs(ref64), 2.0 ** -126) * 2.0 ** -8
+    row = np.linalg.norm(ref64, axis=-1, keepdims=True)
+    err = np.abs(got - ref64)
+    bad = err > half_ulp * 1.01 + 2e-6 * row + 1e-7
+    assert not bad.any(), f"{what}: {bad.sum()} elements off, max err {err.max():.3g}"
+
+
+@pytest.mark.parametrize("layout_main,d", [(True, 128), (True, 64), (False, 128), (False, 256)])
+def test_dense_history_bf16(layout_main, d):
+    """tq_dequantize_bf16 (the guide's FP16/BF16 materialisation): the same reconstruction rounded to
+    bf16, ring rows converted from fp16."""
+    seed, hkv = 41 + d, 2
+    if layout_main:
+        ctx, c, s, sk = make_ctx(tq, True, d, 2 * hkv, hkv, seed)
+        lengths = [300, 1100, 16]
+        e = build_main_cache(seed, d, hkv, lengths, c, s, sk)
+    else:
+        ctx, c, s, sk = make_ctx(tq, False, d, hkv, hkv, seed)
+        lengths = [320, 48]
+        e = build_alt_cache(seed, d, hkv, lengths, c, s)
+    bsz = len(lengths)
+    max_tokens = ((max(lengths) + 15) // 16) * 16 + 32
+    k_out = torch.full((bsz, hkv, max_tokens, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    v_out = torch.full_like(k_out, float("nan"))
+    ring = (to_dev(e["ring_k"]), to_dev(e["ring_v"]), to_dev(e["n_b"])) if layout_main else (None, None, None)
+    ctx.dequantize(to_dev(e["pool"]), to_dev(e["bt"]), to_dev(e["n_c"]), k_out, v_out, *ring)
+    torch.cuda.synchronize()
+    assert ctx.device_errors() == 0
+    for b in range(bsz):
+        nc = int(e["n_c"][b])
+        nb = int(e["n_b"][b]) if layout_main else 0
+        if layout_main:
+            kr, vr = cache.materialize_main(e["pool"], e["bt"], b, nc, e["ring_k"], e["ring_v"], nb, s, c, sk, d)
+        else:
+            kr, vr = cache.materialize_alt(e["pool"], e["bt"], b, nc, None, None, 0, s, c, d)
+        _check_close_bf16(k_out[b, :, :nc + nb], kr, f"keys b={b}")
+        _check_close_bf16(v_out[b, :, :nc + nb], vr, f"values b={b}")
+        if nb:
+            want = torch.from_numpy(e["ring_k"][b, :, :nb]).to(torch.bfloat16)
+            assert torch.equal(k_out[b, :, nc:nc + nb].cpu(), want)
+        assert bool(torch.isnan(k_out[b, :, nc + nb:].float()).all())  # rows past the history untouched

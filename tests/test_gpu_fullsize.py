@@ -123,13 +123,15 @@ def test_qwen3_06b_32k_two_layers():
 def test_qwen25_32b_ragged_batch16():
     """Batch 16, 40 q / 8 KV heads, lengths U[1024, 131072] (seed 7), shuffled pages."""
     lengths = [int(x) for x in synth.ragged_lengths(7, 16, 1024, 131072)]
-    short = int(np.argmin(lengths))
-    _run_main(7, 40, 8, lengths, oracle_seqs={short, 3})
+    short, longest = int(np.argmin(lengths)), int(np.argmax(lengths))
+    # the longest sequence has the most split-K chunk slots of the plan
+    _run_main(7, 40, 8, lengths, oracle_seqs={short, 3, longest})
 
 
 @pytest.mark.parametrize("d", [64, 128, 256, 512])
 def test_alt_layout_65536_head_dim_sweep(d):
-    """Alternate layout, 8 q / 8 KV heads, batch 4, 65536 tokens, no ring; sequence 1 checked."""
+    """Alternate layout, 8 q / 8 KV heads, batch 4, 65536 tokens, no ring; every KV head of sequence 1
+    checked."""
     hq = hkv = 8
     bsz, L, seed = 4, 65536, 11
     ctx, c3, s, _ = make_ctx(tq, False, d, hq, hkv, seed)
@@ -138,7 +140,7 @@ def test_alt_layout_65536_head_dim_sweep(d):
     tile = layout.alt_tile_bytes(d)
     pool = torch.zeros((bsz * max_blocks, hkv, tile), dtype=torch.uint8, device="cuda")
     check_b = 1
-    heads = [0, 5]  # oracle-checked KV heads of the checked sequence
+    heads = list(range(hkv))  # oracle-checked KV heads of the checked sequence
     p_or = None
     for b in range(bsz):
         k, v = synth.kv_alt(seed, 1, hkv, L, d, layer=b)

@@ -165,3 +165,20 @@ def test_null_context_calls_are_rejected_without_cuda():
     assert lib.tq_launch_count(None) == 0
     assert lib.tq_status_string(B.TQ_ERR_WORKSPACE).startswith(b"TQ_ERR_WORKSPACE")
     assert lib.tq_workspace_size(None, 1, 16, C.byref(C.c_size_t())) == B.TQ_ERR_INVALID_ARG
+
+
+def test_prefill_materialisation_rule():
+    """vllm-metal TurboQuant guide, advanced settings: materialise when the history holds >= 8192
+    tokens and the prefill chunk reaches 64 query tokens at head_dim 128, max(128, head_dim / 2)
+    otherwise, within the MiB cap (0 switches materialisation off); decode steps never."""
+    f = B.tq_should_materialize
+    assert f(8192, 64, 128, 8) and not f(8191, 64, 128, 8) and not f(8192, 63, 128, 8)
+    assert not f(100000, 1, 128, 8)                       # a decode step
+    assert f(8192, 128, 64, 8) and not f(8192, 127, 64, 8)  # max(128, 32) = 128
+    assert f(8192, 128, 256, 8) and not f(8192, 127, 256, 8)  # max(128, 128) = 128
+    assert f(8192, 256, 512, 8) and not f(8192, 255, 512, 8)  # max(128, 256) = 256
+    # dense K + V of 8192 tokens x 8 heads x 128 dims x 2 B = 32 MiB
+    assert f(8192, 64, 128, 8, 32) and not f(8192, 64, 128, 8, 31)
+    assert not f(8192, 64, 128, 8, 0) and f(8192, 64, 128, 8, -1)
+    with pytest.raises(ValueError):
+        f(-1, 64, 128, 8)
