@@ -118,7 +118,19 @@ typedef struct {
   int group_size;    /* value group / key block: must be 32 */
   int qjl_m;         /* main: sketch rows m, must equal head_dim; alt: 0 */
   uint64_t seed;     /* table seed; one table set per layer (base seed + layer) */
+  int key_format;    /* alt layout, 2-bit keys: TQ_KEY_AFFINE (0, default: uint2, min/max affine codes)
+                        or TQ_KEY_SIGNED (1: int2, signed symmetric mid-rise codes, see below); must
+                        be 0 otherwise */
 } tq_config;
+
+/* Key formats of the alternate layout at key_bits 2 (the vllm-metal guide lists int2 and uint2,
+ * with the same bytes; the pages give no rule that tells them apart, so this library reads them as):
+ *   uint2 (TQ_KEY_AFFINE): s = fp16((max - min) / 3), mn = min, q = clamp(rint((x - mn) / s), 0, 3);
+ *   int2  (TQ_KEY_SIGNED): s = fp16(max |x| / 1.5), mn = fp16(-1.5 s), q = clamp(rint((x - mn) / s),
+ *         0, 3): the four levels (q - 1.5) s, symmetric about zero (up to the fp16 rounding of mn).
+ * Both store (s, mn) per block of 32 and decode as mn + s q (IEEE fp32 arithmetic, ties to even). */
+#define TQ_KEY_AFFINE 0
+#define TQ_KEY_SIGNED 1
 
 typedef struct tq_ctx tq_ctx;
 

@@ -11,6 +11,8 @@ _EXPORTS = (
     "TQ_DECODE_AUTO",
     "TQ_DECODE_MMA_SYNC",
     "TQ_DECODE_TCGEN05",
+    "TQ_KEY_AFFINE",
+    "TQ_KEY_SIGNED",
     "TQ_LAYOUT_ALT",
     "TQ_LAYOUT_MAIN",
     "Context",

@@ -20,6 +20,7 @@ TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_WORKSPACE, TQ_ERR_CUDA = r
 TQ_LAYOUT_MAIN, TQ_LAYOUT_ALT = 0, 1
 TQ_DEVERR_BLOCK_ID, TQ_DEVERR_POSITION, TQ_DEVERR_RING, TQ_DEVERR_CHUNKS, TQ_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
 TQ_DECODE_AUTO, TQ_DECODE_MMA_SYNC, TQ_DECODE_TCGEN05 = 0, 1, 2
+TQ_KEY_AFFINE, TQ_KEY_SIGNED = 0, 1
 
 
 class TQError(RuntimeError):
@@ -41,6 +42,7 @@ class tq_config(C.Structure):
         ("group_size", C.c_int),
         ("qjl_m", C.c_int),
         ("seed", C.c_uint64),
+        ("key_format", C.c_int),
     ]
 
 
@@ -208,12 +210,14 @@ class Context:
     """Owner of one tq_ctx (one layer's tables on the current CUDA device)."""
 
     def __init__(self, layout: int, head_dim: int, num_q_heads: int, num_kv_heads: int, seed: int = 0,
-                 centroids=None, signs=None, sketch=None, value_bits=None, key_bits=None):
+                 centroids=None, signs=None, sketch=None, value_bits=None, key_bits=None, key_format=None):
         self.cfg = tq_config_init(layout, head_dim, num_q_heads, num_kv_heads, seed)
         if value_bits is not None:
             self.cfg.value_bits = value_bits  # main layout: 2 or 4; alternate layout: 2, 3 or 4
         if key_bits is not None:
             self.cfg.key_bits = key_bits  # main layout: 3, 2 or 4; alternate layout: 8, 5, 4, 2 or 16 (fp16 keys)
+        if key_format is not None:
+            self.cfg.key_format = key_format  # alternate layout, 2-bit keys: TQ_KEY_AFFINE (uint2) or TQ_KEY_SIGNED (int2)
         ptr = C.c_void_p()
         if centroids is None:
             _check(lib.tq_create(C.byref(self.cfg), C.byref(ptr)), "tq_create")

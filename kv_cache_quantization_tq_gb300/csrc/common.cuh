@@ -125,6 +125,26 @@ __device__ __forceinline__ GroupCode group_quant_mm(float v, float mn, float mx,
   return g;
 }
 
+// Signed symmetric mid-rise quantiser of a block with the given max |x| (IEEE float32, no
+// contraction): s = fp16(absmax / (levels / 2)), mn = fp16(-(levels / 2) s),
+// q = clamp(rint((v - mn) / s), 0, levels), q = 0 when s == 0: levels (q - levels/2) s.
+__device__ __forceinline__ GroupCode group_quant_signed(float v, float absmax, float levels) {
+  GroupCode g;
+  const float half = 0.5f * levels;
+  g.s = __float2half_rn(__fdiv_rn(absmax, half));
+  const float s = __half2float(g.s);
+  g.mn = __float2half_rn(__fmul_rn(-half, s));
+  const float mn = __half2float(g.mn);
+  int q = 0;
+  if (s > 0.f) {
+    float t = rintf(__fdiv_rn(__fsub_rn(v, mn), s));
+    t = fminf(fmaxf(t, 0.f), levels);
+    q = (int)t;
+  }
+  g.q = q;
+  return g;
+}
+
 __device__ __forceinline__ GroupCode group_quant_lane(float v, float levels) {
   return group_quant_mm(v, warp_min(v), warp_max(v), levels);
 }

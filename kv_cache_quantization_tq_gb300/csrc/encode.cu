@@ -41,6 +41,7 @@ struct EncArgs {
   const uint4* sfrag;     // S^T as mma.sync B fragments (k = coordinate, n = sketch row), hi / lo
   int kb;                 // main layout: key bits, 3 (2-bit Lloyd-Max index) or 2 (1-bit index)
   int avb;                // alternate layout: value index bits, 2, 3 or 4
+  int key_signed;         // alternate layout, 2-bit keys: signed symmetric codes (int2)
   CodeTables tab;
   uint32_t* err;
 };
@@ -385,7 +386,8 @@ __device__ void encode_alt_block_vb(const EncArgs& a, int b, int h, int tok0, in
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int c = coord_of(e, lane);
-        GroupCode g = group_quant_mm(kx[e], kmn[e], kmx[e], (float)((1 << kb) - 1));
+        GroupCode g = a.key_signed ? group_quant_signed(kx[e], fmaxf(-kmn[e], kmx[e]), (float)((1 << kb) - 1))
+                                   : group_quant_mm(kx[e], kmn[e], kmx[e], (float)((1 << kb) - 1));
         if (kb == 8)
           tile[slot * D + c] = (uint8_t)g.q;
         else
@@ -553,6 +555,7 @@ EncArgs make_args(tq_ctx* ctx, const void* k, const void* v, int src_tokens, int
   a.sfrag = ctx->d_sfrag_enc;
   a.kb = ctx->cfg.key_bits;
   a.avb = ctx->cfg.value_bits;
+  a.key_signed = ctx->cfg.layout == TQ_LAYOUT_ALT && ctx->cfg.key_format == TQ_KEY_SIGNED;
   a.tab = ctx->tab;
   a.err = ctx->d_err;
   return a;

@@ -204,12 +204,13 @@ tq_status check_config(const tq_config* c) {
   if (n_rep % groups) return TQ_ERR_UNSUPPORTED;
   if (c->layout == TQ_LAYOUT_MAIN) {
     if (c->key_bits < 2 || c->key_bits > 4 || (c->value_bits != 2 && c->value_bits != 4) ||
-        c->qjl_m != c->head_dim)
+        c->qjl_m != c->head_dim || c->key_format != TQ_KEY_AFFINE)
       return TQ_ERR_UNSUPPORTED;
   } else if (c->layout == TQ_LAYOUT_ALT) {
     const int kb = c->key_bits;
     if ((kb != 16 && kb != 8 && kb != 5 && kb != 4 && kb != 2) || c->value_bits < 2 || c->value_bits > 4)
       return TQ_ERR_UNSUPPORTED;
+    if (c->key_format != TQ_KEY_AFFINE && !(c->key_format == TQ_KEY_SIGNED && kb == 2)) return TQ_ERR_UNSUPPORTED;
   } else {
     return TQ_ERR_INVALID_ARG;
   }

@@ -66,16 +66,16 @@ def value_bits_of(centroids) -> int:
     return k.bit_length() - 1
 
 
-def encode_alt_range(pool, block_table, start, k16, v16, signs, centroids3):
+def encode_alt_range(pool, block_table, start, k16, v16, signs, centroids3, key_signed=False):
     """Alternate layout: encode fp16 k/v [B, Hkv, T, d] into ``pool`` (value bits from the codebook
     size: 4 to 256 centroids; key bits from the pool's tile size: 8, 5, 4, 2, or 16 for fp16
-    keys)."""
+    keys; key_signed: 2-bit keys as int2 instead of uint2)."""
     k16 = np.asarray(k16, dtype=np.float16)
     bsz, hkv, t, d = k16.shape
     assert start % layout.P == 0 and t % layout.P == 0
     vb = value_bits_of(centroids3)
     kb = layout.alt_key_bits(pool.shape[-1], d, vb)
-    kq, ks, kmn = quant.encode_alt_keys(k16, bits=kb)
+    kq, ks, kmn = quant.encode_alt_keys(k16, bits=kb, signed=key_signed)
     venc = quant.encode_alt_values(v16, signs, centroids3)
     npg = t // layout.P
     tiles = layout.pack_alt_tiles(

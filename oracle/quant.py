@@ -118,6 +118,27 @@ def group_quant(x16: np.ndarray, group: int, levels: int):
     return q.reshape(shape), s16[..., 0], mn.astype(np.float16)[..., 0]
 
 
+def signed_group_quant(x16: np.ndarray, group: int, levels: int):
+    """Signed symmetric mid-rise quantiser in IEEE float32 (this library's reading of the vllm-metal
+    guide's int2 key format, beside the affine uint2): per group, a = max |x|,
+    s = fp16(a / (levels / 2)), mn = fp16(-(levels / 2) s), q = clamp(rint((x - mn) / s), 0, levels)
+    with round-half-even, q = 0 if s == 0.  The levels mn + s q are (q - levels / 2) s up to the fp16
+    rounding of mn.  Returns (codes, scale fp16, minimum fp16) like group_quant."""
+    x = np.asarray(x16, dtype=np.float16).astype(np.float32)
+    shape = x.shape
+    g = x.reshape(shape[:-1] + (shape[-1] // group, group))
+    half = np.float32(levels) / np.float32(2)
+    a = np.abs(g).max(axis=-1, keepdims=True)
+    s16 = (a / half).astype(np.float16)
+    s = s16.astype(np.float32)
+    mn16 = (-half * s).astype(np.float16)
+    mn = mn16.astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        qf = np.rint((g - mn) / s)
+    q = np.where(s > 0, np.clip(qf, 0, levels), 0).astype(np.uint8)
+    return q.reshape(shape), s16[..., 0], mn16[..., 0]
+
+
 def group_dequant(q: np.ndarray, scale16: np.ndarray, min16: np.ndarray, group: int) -> np.ndarray:
     """mn + s * q in float64."""
     q = np.asarray(q, dtype=np.float64)
@@ -143,12 +164,16 @@ def dequant_keys(enc: dict, signs: np.ndarray, centroids: np.ndarray, s_mat: np.
     return enc["n_k"].astype(np.float64)[..., None] * rotation.unrotate(x, signs)
 
 
-def encode_alt_keys(k16: np.ndarray, block: int = 32, bits: int = 8):
-    """Alternate-layout keys: bits-bit affine codes per block of 32 (2^bits - 1 steps).  With 16
-    bits the keys stay as they are (fp16): only the values are quantised (the V-only mode of the
+def encode_alt_keys(k16: np.ndarray, block: int = 32, bits: int = 8, signed: bool = False):
+    """Alternate-layout keys: bits-bit affine codes per block of 32 (2^bits - 1 steps), or with
+    signed=True (2 bits only: int2) the signed symmetric mid-rise codes of signed_group_quant.  With
+    16 bits the keys stay as they are (fp16): only the values are quantised (the V-only mode of the
     "TurboQuant-MLX overview", usage paths)."""
     if bits == 16:
         return np.asarray(k16, dtype=np.float16), None, None
+    if signed:
+        assert bits == 2, "signed keys are the 2-bit int2 format"
+        return signed_group_quant(k16, block, 3)
     return group_quant(k16, block, (1 << bits) - 1)
 
 

@@ -134,7 +134,7 @@ def build_main_cache(seed, d, hkv, lengths, centroids, signs, sketch, shuffled=T
     return dict(k=k, v=v, bt=bt, pool=pool, n_c=n_c, n_b=n_b, ring_k=ring_k, ring_v=ring_v, max_ctx=int(n_c.max()) if bsz else 0)
 
 
-def build_alt_cache(seed, d, hkv, lengths, centroids3, signs, shuffled=True, key_bits=8):
+def build_alt_cache(seed, d, hkv, lengths, centroids3, signs, shuffled=True, key_bits=8, key_signed=False):
     bsz = len(lengths)
     t_all = ((max(lengths) + 15) // 16) * 16
     k, v = synth.kv_alt(seed, bsz, hkv, t_all, d)
@@ -144,5 +144,6 @@ def build_alt_cache(seed, d, hkv, lengths, centroids3, signs, shuffled=True, key
                     np.uint8)
     n_c = np.array(lengths, np.int32)
     for b, L in enumerate(lengths):
-        cache.encode_alt_range(pool, bt[b:b + 1], 0, k[b:b + 1, :, :L], v[b:b + 1, :, :L], signs, centroids3)
+        cache.encode_alt_range(pool, bt[b:b + 1], 0, k[b:b + 1, :, :L], v[b:b + 1, :, :L], signs, centroids3,
+                               key_signed=key_signed)
     return dict(k=k, v=v, bt=bt, pool=pool, n_c=n_c, max_ctx=int(n_c.max()))

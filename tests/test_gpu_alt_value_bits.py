@@ -13,7 +13,8 @@ import pytest
 import torch
 
 import synth
-from gpu_cases import allclose_report, alt_fields, build_alt_cache, make_ctx, near_boundary, tile_index, to_dev
+from gpu_cases import (allclose_report, alt_fields, build_alt_cache, make_ctx, near_boundary, oracle_tables, tile_index,
+                       to_dev)
 from oracle import attention, cache, layout
 from test_gpu_dequant import _check_close, _outputs, _untouched
 
@@ -201,3 +202,49 @@ def test_encode_parity_fp16_keys(d, vb):
     assert np.max(np.abs(fg["vn"].astype(np.int32) - fo["vn"].astype(np.int32))) <= 1
     y = np.stack([e["y"][0] for e in encs]).reshape(2, hkv, n_tok // 16, 16, d).transpose(0, 2, 1, 3, 4)
     assert not ((fg["vidx"] != fo["vidx"]) & ~near_boundary(y, c)).any()
+
+
+# ---- int2 keys: signed symmetric mid-rise 2-bit codes (TQ_KEY_SIGNED), the vllm-metal int2 / q2_0 row
+def _int2_ctx(d, hq, hkv, seed, vb):
+    c32, signs, _ = oracle_tables(seed, d, False, 3, vb)
+    ctx = tq.Context(tq.TQ_LAYOUT_ALT, d, hq, hkv, seed, centroids=c32, signs=signs, value_bits=vb, key_bits=2,
+                     key_format=tq.TQ_KEY_SIGNED)
+    return ctx, c32.astype(np.float64), signs.astype(np.float64)
+
+
+@pytest.mark.parametrize("d,vb", [(128, 2), (64, 3), (512, 2)])
+def test_int2_keys_encode_decode_dequantize(d, vb):
+    hkv, n_tok, starts, seed = 2, 96, [0, 32], 130 + d + vb
+    ctx, c, s = _int2_ctx(d, 2 * hkv, hkv, seed, vb)
+    assert ctx.bytes_per_token_head == 2 * d // 8 + 4 * (d // 32) + vb * d // 8 + 2  # the bytes of uint2
+    k, v = synth.kv_alt(seed, 2, hkv, n_tok, d)
+    max_blocks = 10
+    bt = synth.block_table(seed, 2, max_blocks, True)
+    pool_o = np.zeros((2 * max_blocks, hkv, layout.alt_tile_bytes(d, vb, 2)), np.uint8)
+    for b in range(2):
+        cache.encode_alt_range(pool_o, bt[b:b + 1], starts[b], k[b:b + 1], v[b:b + 1], s, c, key_signed=True)
+    pool_g = torch.zeros(pool_o.shape, dtype=torch.uint8, device="cuda")
+    ctx.encode_flush(to_dev(k), to_dev(v), to_dev(np.array(starts, np.int32)), to_dev(bt), pool_g)
+    pool_g = pool_g.cpu().numpy()
+    assert ctx.device_errors() == 0
+    blocks = tile_index(bt, starts, n_tok)
+    fo, fg = alt_fields(pool_o[blocks], d, 2), alt_fields(pool_g[blocks], d, 2)
+    assert np.array_equal(fg["k_bytes"], fo["k_bytes"])  # signed codes and their (s, mn): bit-exact
+    # decode and dequantise an oracle-encoded int2 cache
+    e = build_alt_cache(seed, d, hkv, [544, 96], c, s, key_bits=2, key_signed=True)
+    q = synth.queries(seed, 2, 2 * hkv, d)
+    out = torch.empty((2, 2 * hkv, d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(ctx.workspace_size(2, e["max_ctx"]), dtype=torch.uint8, device="cuda")
+    ctx.decode_attention(to_dev(q), to_dev(e["pool"]), to_dev(e["bt"]), to_dev(e["n_c"]), None, None, None,
+                         e["max_ctx"], out, ws)
+    assert ctx.device_errors() == 0
+    ref = attention.decode_alt(q, e["pool"], e["bt"], e["n_c"], None, None, None, s, c, hkv)
+    ok, maxerr, nbad = allclose_report(out.cpu().numpy(), ref)
+    assert ok, f"max abs err {maxerr}, {nbad} bad"
+    k_out, v_out = _outputs(2, hkv, 560, d)
+    ctx.dequantize(to_dev(e["pool"]), to_dev(e["bt"]), to_dev(e["n_c"]), k_out, v_out)
+    torch.cuda.synchronize()
+    kg = k_out.cpu().numpy()
+    for b, L in enumerate([544, 96]):
+        kr, _ = cache.materialize_alt(e["pool"], e["bt"], b, L, None, None, 0, s, c, d)
+        _check_close(kg[b, :, :L], kr, f"keys b={b}")

@@ -182,3 +182,16 @@ def test_prefill_materialisation_rule():
     assert not f(8192, 64, 128, 8, 0) and f(8192, 64, 128, 8, -1)
     with pytest.raises(ValueError):
         f(-1, 64, 128, 8)
+
+
+def test_int2_key_format_is_accepted_only_for_alternate_2_bit_keys():
+    cfg = B.tq_config_init(B.TQ_LAYOUT_ALT, 128, 8, 8, 0)
+    cfg.key_bits, cfg.key_format = 2, B.TQ_KEY_SIGNED
+    assert B.tq_config_check(cfg) == 2 * 128 // 8 + 4 * 4 + 3 * 128 // 8 + 2  # the bytes of uint2
+    cfg.key_bits = 8
+    with pytest.raises(B.TQError):
+        B.tq_config_check(cfg)
+    main = B.tq_config_init(B.TQ_LAYOUT_MAIN, 128, 8, 8, 0)
+    main.key_format = B.TQ_KEY_SIGNED
+    with pytest.raises(B.TQError):
+        B.tq_config_check(main)

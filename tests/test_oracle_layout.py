@@ -236,7 +236,7 @@ def test_vllm_metal_compression_table_reading():
         assert layout.alt_bytes_per_token_head(128, vb) == (8 * 128 / 8 + 16) + (vb * 128 / 8 + 8) - 6
     # ... and for the table's other key formats (q5_0, q4_0 and uint2 keys with q3_0 values)
     rows = {r["k_quant"]: r for r in golden("vllm_metal_compression.json")["rows"]}
-    for name in ("q5_0", "q4_0", "uint2"):
+    for name in ("q5_0", "q4_0", "uint2", "int2"):  # int2 (signed codes) has the bytes of uint2
         row = rows[name]
         per = row["k_bits"] * 128 / 8 + 16 + row["v_bits"] * 128 / 8 + 8
         assert layout.alt_bytes_per_token_head(128, row["v_bits"], row["k_bits"]) == per - 6

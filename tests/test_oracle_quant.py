@@ -166,3 +166,41 @@ def test_alt_value_encoder():
     # dequantised vector has norm n_v * ||c[idx]||
     assert np.allclose(np.linalg.norm(vhat, axis=1),
                        enc["n_v"].astype(np.float64) * np.linalg.norm(c3[enc["idx"]], axis=1), rtol=1e-12)
+
+
+def test_signed_group_quant_int2():
+    """int2 keys (signed symmetric mid-rise, this library's reading): s = fp16(max|x| / 1.5),
+    mn = fp16(-1.5 s), codes = the nearest of the four levels mn + s c (brute force, ties to even)."""
+    g = np.random.default_rng(5)
+    x = (g.standard_normal((5, 64)) * g.lognormal(size=(5, 1))).astype(np.float16)
+    x[0, :32] = 0                        # zero block -> scale 0, codes 0
+    x[1, 32:64] = np.abs(x[1, 32:64])    # one-signed block: the symmetric range still spans +-max
+    q, s, mn = quant.signed_group_quant(x, 32, 3)
+    xf = x.astype(np.float32).reshape(5, 2, 32)
+    a = np.abs(xf).max(axis=-1)
+    assert np.array_equal(s, (a / np.float32(1.5)).astype(np.float16))
+    assert np.array_equal(mn, (np.float32(-1.5) * s.astype(np.float32)).astype(np.float16))
+    assert s[0, 0] == 0 and np.all(q[0, :32] == 0)
+    # the same codes as the brute-force nearest level of the affine form with these (s, mn)
+    qq = q.reshape(5, 2, 32)
+    for r in range(5):
+        for b in range(2):
+            sf, mf = np.float32(s[r, b]), np.float32(mn[r, b])
+            for i in range(32):
+                if sf == 0:
+                    continue
+                t = np.float32(np.float32(xf[r, b, i] - mf) / sf)
+                d = [abs(float(t) - c) for c in range(4)]
+                best = min(range(4), key=lambda c: (round(d[c], 12), c % 2))
+                assert qq[r, b, i] == best
+    # levels symmetric about zero up to the fp16 rounding of mn; the block maximum takes the top code
+    lv_lo = mn.astype(np.float64)
+    lv_hi = mn.astype(np.float64) + 3 * s.astype(np.float64)
+    assert np.all(np.abs(lv_lo + lv_hi) <= np.abs(lv_hi) * 2.0 ** -10 + 1e-12)
+    top = np.argmax(np.abs(xf), axis=-1)
+    sign = np.take_along_axis(xf, top[..., None], -1)[..., 0]
+    code = np.take_along_axis(qq, top[..., None], -1)[..., 0]
+    nz = s.astype(np.float32) > 0
+    assert np.all(code[nz & (sign > 0)] == 3) and np.all(code[nz & (sign < 0)] == 0)
+    # the one-signed block: no code below the middle (all values >= 0 sit at the upper levels)
+    assert np.all(qq[1, 1] >= 1)
