@@ -19,9 +19,9 @@ Workloads (synthetic inputs from ``synth``; no weights or datasets):
   alt-d{64,128,256,512}  alternate layout, 8 / 8, batch 4, 65536 tokens, no ring
   qwen2.5-32b-ragged     1 of 64 layers, 40 / 8, d 128, batch 16, lengths U[1024, 131072]
   qwen2.5-7b-b8-v4       the batch-8 workload with 4-bit value codes
-  alt-d128-v4 / -k4 / -k5 / -k2 / -vonly
-                   the d 128 alternate workload with 4-bit values (K8+V4), 4-, 5- or
-                   2-bit keys (q4_0 / q5_0 / uint2), or fp16 keys (the V-only cache)
+  alt-d128-v4 / -v8 / -k4 / -k5 / -k2 / -vonly
+                   the d 128 alternate workload with 4- or 8-bit values (K8+V4, q8_0 / q8_0),
+                   4-, 5- or 2-bit keys (q4_0 / q5_0 / uint2), or fp16 keys (the V-only cache)
 
 Launch: ``python bench.py [--gpus N --steps K --warmup W --workload NAME]``;
 for N > 1 under torchrun, each rank runs the same per-GPU workload (weak
@@ -81,6 +81,9 @@ WORKLOADS = {
     # 2-bit keys (uint2 keys + 3-bit values: the guide's aggressive row)
     "alt-d128-k2": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=128, ctx=65536, shuffled=False, seed=0,
                         kbits=2),
+    # 8-bit keys and 8-bit values (q8_0 / q8_0: the widest value format of the guide)
+    "alt-d128-v8": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=128, ctx=65536, shuffled=False, seed=0,
+                        vbits=8),
     # fp16 keys, 3-bit values (the V-only cache)
     "alt-d128-vonly": dict(layout="alt", layers=1, batch=4, hq=8, hkv=8, d=128, ctx=65536, shuffled=False, seed=0,
                            kbits=16),

@@ -113,8 +113,8 @@ typedef struct {
                         only the values quantised (the V-only cache of the TurboQuant-MLX
                         overview) */
   int value_bits;    /* main: 2 (default) or 4 (turboquant vLLM guide, --value-bits); alt: 3
-                        (default), 2 or 4 Lloyd-Max index bits per value coordinate (the
-                        vllm-metal guide's q2_0 .. q4_0 value formats; 8 + 4 is its K8+V4) */
+                        (default) or 2 .. 8 Lloyd-Max index bits per value coordinate (the
+                        vllm-metal guide's q2_0 .. q8_0 value formats; 8 + 4 is its K8+V4) */
   int group_size;    /* value group / key block: must be 32 */
   int qjl_m;         /* main: sketch rows m, must equal head_dim; alt: 0 */
   uint64_t seed;     /* table seed; one table set per layer (base seed + layer) */

@@ -53,8 +53,9 @@ struct DecArgs {
   const float* signs;
   const float* sketch_t;
   int kb;  // main layout key bits (3 or 2)
-  int avb;  // alternate layout value index bits (2, 3 or 4)
+  int avb;  // alternate layout value index bits (2 .. 8)
   CodeTables tab;
+  const float* vcent;  // alternate layout: value centroids in device memory (2^avb of them)
   uint32_t* err;
 };
 
@@ -420,6 +421,7 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
   __shared__ float pbuf[16][NR];
   __shared__ float ob[NR][D];
   __shared__ SoftState<NR> st;
+  __shared__ float vlut[256];  // value centroids (2^avb used)
 
   const int part = blockIdx.x + a.first_part, hg = blockIdx.y, b = blockIdx.z;
   const int kvh = hg / a.groups;
@@ -441,6 +443,7 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
     st.l[tid] = 0.f;
     st.alpha[tid] = 1.f;
   }
+  for (int i = tid; i < (1 << a.avb); i += 128) vlut[i] = a.vcent[i];
   for (int i = tid; i < NR * D; i += 128) {
     const int h = i / D, c = i % D;
     qf[h][c] = h < a.nrg ? __half2float(a.q[((size_t)b * a.hq + h0 + h) * D + c]) : 0.f;
@@ -563,10 +566,7 @@ __global__ void __launch_bounds__(128) decode_alt_kernel(DecArgs a) {
           const uint32_t* row = vi + tk * (vb * D / 32);
           uint32_t v = row[bit >> 5] >> (bit & 31);
           if ((bit & 31) + vb > 32) v |= row[(bit >> 5) + 1] << (32 - (bit & 31));
-          const int idx = v & vmask;
-          float cv = a.tab.c[0];
-#pragma unroll
-          for (int j = 1; j < 16; ++j) cv = idx == j ? a.tab.c[j] : cv;
+          const float cv = vlut[v & vmask];
 #pragma unroll
           for (int h = 0; h < NR; ++h) o[r][h] = fmaf(pbuf[tk][h], cv, o[r][h]);
         }
@@ -666,7 +666,7 @@ cudaError_t launch_tpl(const DecArgs& a, int vb, dim3 grid, cudaStream_t s) {
   if (vb == 4) return launch_main_vb<D, NR, 4>(a, grid, s);
   if (vb == 2) return launch_main_vb<D, NR, 2>(a, grid, s);
   auto kern = decode_alt_kernel<D, NR>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, alt_tile_bytes(D, 16, 4));
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, alt_tile_bytes(D, 16, 8));
   if (e != cudaSuccess) return e;
   kern<<<grid, 128, alt_tile_bytes(D, a.kb, a.avb), s>>>(a);
   return cudaGetLastError();
@@ -745,6 +745,7 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
   a.signs = ctx->d_signs;
   a.sketch_t = ctx->d_sketch_t;
   a.tab = ctx->tab;
+  a.vcent = ctx->d_vcent;
   a.kb = ctx->cfg.key_bits;
   a.avb = ctx->cfg.value_bits;
   a.err = ctx->d_err;

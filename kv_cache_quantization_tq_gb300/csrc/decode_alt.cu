@@ -508,6 +508,7 @@ cudaError_t launch_decode_alt_v2(tq_ctx* ctx, const void* q, const void* pool, i
   a.err = ctx->d_err;
   dim3 grid(n_chunks, a.hkv * a.groups, batch);
   const int d = ctx->cfg.head_dim, nr = a.nrg, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
+  if (vb > 4) return cudaErrorNotSupported;  // 5- to 8-bit values: the CUDA-core decoder (device codebook)
   if (nr == 1) {
     switch (d) {
       case 64: return launch_alt<64, 1>(a, vb, kb, grid, s);

@@ -45,8 +45,9 @@ struct DqArgs {
   const float* signs;
   const uint4* sfrag;   // S as mma.sync B fragments (back-projection order), fp16 high / low
   int kb;               // main layout key bits (3 or 2)
-  int avb;              // alternate layout value index bits (2, 3 or 4)
+  int avb;              // alternate layout value index bits (2 .. 8)
   CodeTables tab;
+  const float* vcent;   // alternate layout: value centroids in device memory (2^avb of them)
   float qjl_coef;       // sqrt(pi/2) / m
   uint32_t* err;
 };
@@ -253,7 +254,7 @@ template <int D>
 struct AltDq {
   static constexpr int E = D / 32;
   static constexpr int TB = 32;
-  static constexpr int TILE_MAX = alt_tile_bytes(D, 16, 4);
+  static constexpr int TILE_MAX = alt_tile_bytes(D, 16, 8);
   static constexpr int THREADS = 256;
   static constexpr size_t SMEM = (size_t)(TB / 16) * TILE_MAX;
 };
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
   constexpr int E = C::E;
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ bool ok[C::TB / 16];
-  __shared__ float lut[16];
+  __shared__ float lut[256];
   const int b = blockIdx.z, h = blockIdx.y;
   const int tok0 = blockIdx.x * C::TB;
   const int n = dq_ntok(a, b);
@@ -294,7 +295,7 @@ __global__ void __launch_bounds__(256) dequant_alt_kernel(DqArgs a) {
   const int vb = a.avb, kb = a.kb, tile_bytes = alt_tile_bytes(D, kb, vb);
   const int o_ksm = 2 * kb * D, o_vi = alt_key_bytes(D, kb), o_vn = o_vi + 2 * vb * D;
   const uint32_t mask = (1u << vb) - 1u;
-  if (threadIdx.x < 16) lut[threadIdx.x] = a.tab.c[threadIdx.x & mask];
+  for (int i = threadIdx.x; i < (1 << vb); i += C::THREADS) lut[i] = a.vcent[i];
   load_tiles(a, smem, tile_bytes, tile_bytes, b, h, tok0 >> 4, ntok >> 4, ok);  // ends with __syncthreads
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float rs = rsqrtf((float)D);
@@ -395,6 +396,7 @@ cudaError_t launch_dequantize_t(tq_ctx* ctx, const void* pool, int num_blocks, c
   a.kb = ctx->cfg.key_bits;
   a.avb = ctx->cfg.value_bits;
   a.tab = ctx->tab;
+  a.vcent = ctx->d_vcent;
   a.qjl_coef = (float)(1.2533141373155003 / (double)ctx->cfg.qjl_m);
   a.err = ctx->d_err;
   const int d = ctx->cfg.head_dim;

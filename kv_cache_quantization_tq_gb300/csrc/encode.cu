@@ -42,6 +42,7 @@ struct EncArgs {
   int kb;                 // main layout: key bits, 3 (2-bit Lloyd-Max index) or 2 (1-bit index)
   int avb;                // alternate layout: value index bits, 2, 3 or 4
   int key_signed;         // alternate layout, 2-bit keys: signed symmetric codes (int2)
+  const float* vbound;    // alternate layout: value decision boundaries (device, 2^vb - 1)
   CodeTables tab;
   uint32_t* err;
 };
@@ -308,7 +309,7 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
 // Alternate-layout page (alt_tile_bytes): a dense kb-bit stream of key codes per token (kb = 8, 5,
 // 4 or 2; 8 bits: one byte per coordinate) and 16 x d/32 (scale, minimum) fp16 pairs, or the fp16
 // keys (kb = 16); a dense vb-bit stream of value indices per token (index i at bit vb i); 16 fp16
-// value norms.  The function attribute allows the largest staging (kb = 16, vb = 4).
+// value norms.  The function attribute allows the largest staging (kb = 16, vb = 8).
 template <int D>
 struct AltEnc {
   static constexpr int E = D / 32;
@@ -318,10 +319,10 @@ struct AltEnc {
   static constexpr size_t smem(int kb, int vb) {
     return (size_t)(TB / 16) * alt_tile_bytes(D, kb, vb) + (size_t)TB * D + (kb == 8 || kb == 16 ? 0 : (size_t)TB * D);
   }
-  static constexpr size_t SMEM = smem(16, 4);  // the largest
-  static_assert(smem(16, 4) >= smem(8, 4) && smem(16, 4) >= smem(5, 4) && smem(16, 4) >= smem(4, 4) &&
-                    smem(16, 4) >= smem(2, 4),
-                "fp16 keys bound the staging");
+  static constexpr size_t SMEM = smem(16, 8);  // the largest
+  static_assert(smem(16, 8) >= smem(8, 8) && smem(16, 8) >= smem(5, 8) && smem(16, 8) >= smem(4, 8) &&
+                    smem(16, 8) >= smem(2, 8),
+                "fp16 keys and 8-bit values bound the staging");
 };
 
 // Codes of every staged token as a dense little-endian VB-bit stream at byte `offset` of its page
@@ -358,6 +359,13 @@ __device__ void encode_alt_block_vb(const EncArgs& a, int b, int h, int tok0, in
   uint8_t* tiles = smem;
   uint8_t* vcodes = smem + (size_t)(C::TB / 16) * tile_bytes;
   uint8_t* kcodes = vcodes + C::TB * D;  // keys below 8 bits: staged, then packed
+  // 5- to 8-bit values: the boundaries in shared memory for a binary search (the narrower codebooks
+  // compare against the kernel-parameter table)
+  __shared__ float sbound[VB >= 5 ? (1 << VB) : 1];
+  if (VB >= 5) {
+    for (int i = threadIdx.x; i < nbound; i += C::THREADS) sbound[i] = a.vbound[i];
+    __syncthreads();
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const size_t base = ((size_t)b * a.hkv + h) * a.src_tokens;
   float sg[E];
@@ -410,10 +418,16 @@ __device__ void encode_alt_block_vb(const EncArgs& a, int b, int h, int tok0, in
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const float y = vv[e] * inv;
-      // #{boundaries <= y} over the 2^vb - 1 ascending boundaries
+      // #{boundaries <= y} over the 2^vb - 1 ascending boundaries (ties go up)
       int idx = 0;
+      if (VB >= 5) {
+        // binary lifting: idx + step - 1 <= 2^VB - 2 at every step, inside the table
 #pragma unroll
-      for (int j = 0; j < nbound; ++j) idx += y >= a.tab.b[j];
+        for (int step = 1 << (VB - 1); step; step >>= 1) idx += (y >= sbound[idx + step - 1]) ? step : 0;
+      } else {
+#pragma unroll
+        for (int j = 0; j < nbound; ++j) idx += y >= a.tab.b[j];
+      }
       vcodes[tt * D + coord_of(e, lane)] = (uint8_t)idx;
     }
     if (lane == 0) reinterpret_cast<__half*>(tile + o_vn)[slot] = __float2half_rn(nv);
@@ -433,12 +447,15 @@ __device__ void encode_alt_block_vb(const EncArgs& a, int b, int h, int tok0, in
 
 template <int D>
 __device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int ntok, int start, uint8_t* smem) {
-  if (a.avb == 2)
-    encode_alt_block_vb<D, 2>(a, b, h, tok0, ntok, start, smem);
-  else if (a.avb == 4)
-    encode_alt_block_vb<D, 4>(a, b, h, tok0, ntok, start, smem);
-  else
-    encode_alt_block_vb<D, 3>(a, b, h, tok0, ntok, start, smem);
+  switch (a.avb) {
+    case 2: encode_alt_block_vb<D, 2>(a, b, h, tok0, ntok, start, smem); break;
+    case 4: encode_alt_block_vb<D, 4>(a, b, h, tok0, ntok, start, smem); break;
+    case 5: encode_alt_block_vb<D, 5>(a, b, h, tok0, ntok, start, smem); break;
+    case 6: encode_alt_block_vb<D, 6>(a, b, h, tok0, ntok, start, smem); break;
+    case 7: encode_alt_block_vb<D, 7>(a, b, h, tok0, ntok, start, smem); break;
+    case 8: encode_alt_block_vb<D, 8>(a, b, h, tok0, ntok, start, smem); break;
+    default: encode_alt_block_vb<D, 3>(a, b, h, tok0, ntok, start, smem); break;
+  }
 }
 
 // ------------------------------------------------------------------ kernels
@@ -556,6 +573,7 @@ EncArgs make_args(tq_ctx* ctx, const void* k, const void* v, int src_tokens, int
   a.kb = ctx->cfg.key_bits;
   a.avb = ctx->cfg.value_bits;
   a.key_signed = ctx->cfg.layout == TQ_LAYOUT_ALT && ctx->cfg.key_format == TQ_KEY_SIGNED;
+  a.vbound = ctx->d_vbound;
   a.tab = ctx->tab;
   a.err = ctx->d_err;
   return a;

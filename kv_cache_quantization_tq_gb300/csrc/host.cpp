@@ -208,7 +208,7 @@ tq_status check_config(const tq_config* c) {
       return TQ_ERR_UNSUPPORTED;
   } else if (c->layout == TQ_LAYOUT_ALT) {
     const int kb = c->key_bits;
-    if ((kb != 16 && kb != 8 && kb != 5 && kb != 4 && kb != 2) || c->value_bits < 2 || c->value_bits > 4)
+    if ((kb != 16 && kb != 8 && kb != 5 && kb != 4 && kb != 2) || c->value_bits < 2 || c->value_bits > 8)
       return TQ_ERR_UNSUPPORTED;
     if (c->key_format != TQ_KEY_AFFINE && !(c->key_format == TQ_KEY_SIGNED && kb == 2)) return TQ_ERR_UNSUPPORTED;
   } else {
@@ -229,8 +229,10 @@ tq_status finish_create(const tq_config* cfg, std::vector<float> cent, std::vect
   ctx->h_boundaries.resize(cent.size() - 1);
   for (size_t j = 0; j + 1 < cent.size(); ++j)
     ctx->h_boundaries[j] = (float)(0.5 * ((double)cent[j] + (double)cent[j + 1]));
-  for (size_t j = 0; j < cent.size(); ++j) ctx->tab.c[j] = cent[j];
-  for (size_t j = 0; j + 1 < cent.size(); ++j) ctx->tab.b[j] = ctx->h_boundaries[j];
+  // kernel-parameter tables: codebooks of up to 16 entries; wider value codebooks (alternate layout,
+  // 5- to 8-bit values) live in device memory only
+  for (size_t j = 0; j < cent.size() && j < 16; ++j) ctx->tab.c[j] = cent[j];
+  for (size_t j = 0; j + 1 < cent.size() && j < 16; ++j) ctx->tab.b[j] = ctx->h_boundaries[j];
   ctx->h_signs = signs;
   ctx->h_sketch = sketch;
   bool ok = cudaGetDevice(&ctx->device) == cudaSuccess;
@@ -239,6 +241,16 @@ tq_status finish_create(const tq_config* cfg, std::vector<float> cent, std::vect
   ok = ok && cudaMalloc(&ctx->d_err, sizeof(uint32_t)) == cudaSuccess;
   ok = ok && cudaMemcpy(ctx->d_signs, signs.data(), sizeof(float) * d, cudaMemcpyHostToDevice) == cudaSuccess;
   ok = ok && cudaMemset(ctx->d_err, 0, sizeof(uint32_t)) == cudaSuccess;
+  if (ok && cfg->layout == TQ_LAYOUT_ALT) {
+    // value codebook and its decision boundaries as device tables (up to 256 / 255 floats)
+    const size_t nc = cent.size();
+    ok = cudaMalloc(&ctx->d_vcent, sizeof(float) * 256) == cudaSuccess;
+    ok = ok && cudaMalloc(&ctx->d_vbound, sizeof(float) * 256) == cudaSuccess;
+    ok = ok && cudaMemset(ctx->d_vbound, 0, sizeof(float) * 256) == cudaSuccess;
+    ok = ok && cudaMemcpy(ctx->d_vcent, cent.data(), sizeof(float) * nc, cudaMemcpyHostToDevice) == cudaSuccess;
+    ok = ok && cudaMemcpy(ctx->d_vbound, ctx->h_boundaries.data(), sizeof(float) * (nc - 1),
+                          cudaMemcpyHostToDevice) == cudaSuccess;
+  }
   if (ok && cfg->layout == TQ_LAYOUT_MAIN) {
     const int m = cfg->qjl_m;
     std::vector<float> st((size_t)m * d);
@@ -487,6 +499,8 @@ void tq_destroy(tq_ctx* ctx) {
   cudaFree(ctx->d_sketch_t);
   cudaFree(ctx->d_sfrag);
   cudaFree(ctx->d_sfrag_enc);
+  cudaFree(ctx->d_vcent);
+  cudaFree(ctx->d_vbound);
   cudaFree(ctx->d_err);
   for (auto& p : ctx->prof)
     for (auto& e : p.ev) {

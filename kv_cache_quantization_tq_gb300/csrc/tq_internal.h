@@ -51,6 +51,8 @@ struct tq_ctx {
   float* d_sketch_t = nullptr;  // [d][m]
   uint4* d_sfrag = nullptr;     // S as fp16 high/low mma.sync B fragments (back-projection)
   uint4* d_sfrag_enc = nullptr; // S^T as fp16 high/low mma.sync B fragments (encode projection)
+  float* d_vcent = nullptr;     // alternate layout: value centroids [256] (2^value_bits used)
+  float* d_vbound = nullptr;    // alternate layout: their decision boundaries [256] (2^value_bits - 1 used)
   uint32_t* d_err = nullptr;    // device error word
   int64_t launches = 0;
   int decode_path = 0;          // TQ_DECODE_AUTO / _MMA_SYNC / _TCGEN05

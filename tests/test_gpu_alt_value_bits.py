@@ -33,7 +33,7 @@ def _need_gpu():
         pytest.skip("no CUDA device")
 
 
-@pytest.mark.parametrize("vb", [2, 4])
+@pytest.mark.parametrize("vb", [2, 4, 5, 8])
 @pytest.mark.parametrize("d", [64, 512])
 def test_record_size(d, vb):
     ctx, c, *_ = make_ctx(tq, False, d, 2, 2, 0, value_bits=vb)
@@ -42,7 +42,7 @@ def test_record_size(d, vb):
     assert ctx.page_bytes == layout.alt_tile_bytes(d, vb)
 
 
-@pytest.mark.parametrize("vb", [2, 4])
+@pytest.mark.parametrize("vb", [2, 4, 5, 6, 7, 8])  # q2_0 .. q8_0 values (q3_0 is the default)
 @pytest.mark.parametrize("d", [64, 128, 256, 512])
 def test_encode_parity(d, vb):
     hkv, n_tok, starts, seed = 2, 96, [0, 32], 60 + d + vb
@@ -65,10 +65,13 @@ def test_encode_parity(d, vb):
     y = np.stack([e["y"][0] for e in encs]).reshape(2, hkv, n_tok // 16, 16, d).transpose(0, 2, 1, 3, 4)
     near = near_boundary(y, c)
     assert not ((fg["vidx"] != fo["vidx"]) & ~near).any()
-    assert fg["vidx"].max() == (1 << vb) - 1  # every level reachable: the stream width is used
+    if vb <= 4:
+        assert fg["vidx"].max() == (1 << vb) - 1  # every level reachable: the stream width is used
+    else:  # 32..256 levels: the top index bit is used (the outermost cells hold few samples)
+        assert fg["vidx"].max() >= 1 << (vb - 1)
 
 
-@pytest.mark.parametrize("vb", [2, 4])
+@pytest.mark.parametrize("vb", [2, 4, 5, 8])
 @pytest.mark.parametrize("d,n_rep", [(64, 1), (128, 2), (128, 4), (256, 1), (512, 1), (128, 8)])
 def test_decode_parity(d, n_rep, vb):
     seed, hkv = 70 + d + n_rep + vb, 2
@@ -87,7 +90,7 @@ def test_decode_parity(d, n_rep, vb):
     assert ok, f"max abs err {maxerr}, {nbad} bad"
 
 
-@pytest.mark.parametrize("vb", [2, 4])
+@pytest.mark.parametrize("vb", [2, 4, 6, 8])
 @pytest.mark.parametrize("d", [64, 256])
 def test_dense_history(d, vb):
     seed, hkv = 80 + d + vb, 2

@@ -126,7 +126,7 @@ def test_config_check_record_bytes_match_the_oracle_layouts(d):
             got = B.tq_config_check(_cfg(B.TQ_LAYOUT_MAIN, d, kb, vb))
             assert got == layout.main_bytes_per_token_head(d, vb, kb), (kb, vb)
     for kb in (2, 4, 5, 8, 16):
-        for vb in (2, 3, 4):
+        for vb in (2, 3, 4, 5, 6, 7, 8):  # q2_0 .. q8_0 values
             got = B.tq_config_check(_cfg(B.TQ_LAYOUT_ALT, d, kb, vb))
             assert got == layout.alt_bytes_per_token_head(d, vb, kb), (kb, vb)
     assert B.tq_config_check(B.tq_config_init(B.TQ_LAYOUT_MAIN, d, 16, 4)) == 0.75 * d + 4
@@ -136,7 +136,7 @@ def test_config_check_record_bytes_match_the_oracle_layouts(d):
 def test_config_check_rejects_unsupported_widths():
     bad = [(B.TQ_LAYOUT_MAIN, 5, 2), (B.TQ_LAYOUT_MAIN, 1, 2), (B.TQ_LAYOUT_MAIN, 3, 3), (B.TQ_LAYOUT_MAIN, 3, 8),
            (B.TQ_LAYOUT_ALT, 3, 3), (B.TQ_LAYOUT_ALT, 6, 3), (B.TQ_LAYOUT_ALT, 7, 3), (B.TQ_LAYOUT_ALT, 12, 3),
-           (B.TQ_LAYOUT_ALT, 8, 1), (B.TQ_LAYOUT_ALT, 8, 5), (B.TQ_LAYOUT_ALT, 16, 8)]
+           (B.TQ_LAYOUT_ALT, 8, 1), (B.TQ_LAYOUT_ALT, 8, 9), (B.TQ_LAYOUT_ALT, 16, 9)]
     for lay, kb, vb in bad:
         with pytest.raises(B.TQError) as e:
             B.tq_config_check(_cfg(lay, 128, kb, vb))
