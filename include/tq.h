@@ -225,7 +225,8 @@ tq_status tq_set_decode_path(tq_ctx* ctx, int path);
  * the pool: the encode kernel of the write path (turboquant-bench, "batch
  * flush" of 128 tokens; any multiple of 16 is accepted so that a prefix can
  * be compressed in one call).
- *   k, v        device fp16 [batch][Hkv][src_tokens][d]; tokens 0..n_tokens-1 are read
+ *   k, v        device fp16 [batch][Hkv][src_tokens][d], 16-byte aligned; tokens 0..n_tokens-1
+ *               are read
  *   start_pos   device int32 [batch]: position of token 0, a multiple of 16
  *   block_table device int32 [batch][max_blocks]
  *   pool        device uint8 [num_blocks][Hkv][tq_page_bytes()], written
@@ -241,7 +242,7 @@ tq_status tq_encode_flush(tq_ctx* ctx, const void* k, const void* v, int batch, 
  *   k_new, v_new  device fp16 [batch][Hkv][d]
  *   pos           device int32 [batch]: position of the new token (its
  *                 sequence length before the append)
- *   ring_k/v      device fp16 [batch][Hkv][ring_capacity][d]; slot = pos % 128
+ *   ring_k/v      device fp16 [batch][Hkv][ring_capacity][d], 16-byte aligned; slot = pos % 128
  * If pos > 0 and pos % 128 == 0 the ring holds tokens pos-128 .. pos-1: they
  * are first encoded into the pool at positions pos-128.. (same kernel as
  * tq_encode_flush), then the new token is written to slot 0.  After the call

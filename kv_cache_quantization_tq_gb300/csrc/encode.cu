@@ -47,6 +47,11 @@ struct EncArgs {
   uint32_t* err;
 };
 
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
+}
+
 __device__ __forceinline__ void mma_f16_acc(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -94,8 +99,7 @@ struct MainEnc {
   static constexpr int RS = D + 8;                     // residual row stride (halves): conflict-free fragments
   static constexpr size_t SMEM_R = 2 * sizeof(__half) * TB * RS;  // high and low parts
   static constexpr size_t SMEM_TILES = (size_t)(TB / 16) * TILE;
-  static constexpr size_t SMEM_CODES = (size_t)TB * D;
-  static constexpr size_t SMEM = SMEM_R + SMEM_TILES + SMEM_CODES;
+  static constexpr size_t SMEM = SMEM_R + SMEM_TILES;
 };
 
 // Copy `npages` staged tiles (staging stride `stride`, `tile` bytes each) to the pool pages of (b, h)
@@ -124,27 +128,51 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
   __half* rh = reinterpret_cast<__half*>(smem);                 // [TB][RS] residual, fp16 high part
   __half* rl = rh + TB * C::RS;                                 // [TB][RS] (r - high) * 2^11
   uint8_t* tiles = smem + C::SMEM_R;                            // [TB/16][TILE]
-  uint8_t* vcodes = tiles + C::SMEM_TILES;                      // [TB][D]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const size_t base = ((size_t)b * a.hkv + h) * a.src_tokens;
 
+  // ---- phase 0: the block's k and v rows (contiguous in [B][Hkv][src_tokens][d]) staged with
+  // 16-byte cp.async into the residual buffers, row stride RS: token tt's k row sits where its
+  // residual's high part goes and its v row where the low part goes.  Each token's rows are read
+  // and then overwritten by the one warp that encodes it, so no other warp ever sees them change.
+  {
+    constexpr int CH = D / 8;  // 16-byte chunks per row
+    const __half* kb = a.k + (base + tok0) * D;
+    const __half* vb = a.v + (base + tok0) * D;
+    for (int i = threadIdx.x; i < ntok * CH; i += C::THREADS) {
+      const int tt = i / CH, c = i % CH;
+      cp_async16(rh + tt * C::RS + 8 * c, kb + (size_t)tt * D + 8 * c);
+      cp_async16(rl + tt * C::RS + 8 * c, vb + (size_t)tt * D + 8 * c);
+    }
+    asm volatile("cp.async.commit_group;\n" ::);
+  }
+  // value-code words of the block's pages (2 VB d bytes each) start at zero: phase 1 ORs every
+  // code into them
+  {
+    constexpr int WPP = 2 * VB * D / 4;  // words per page
+    for (int i = threadIdx.x; i < (TB / 16) * WPP; i += C::THREADS)
+      reinterpret_cast<uint32_t*>(tiles + (size_t)(i / WPP) * C::TILE + 2 * KB * D)[i % WPP] = 0u;
+  }
   float sg[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) sg[e] = a.signs[coord_of(e, lane)];
   const float sqrt_d = sqrtf((float)D);
+  asm volatile("cp.async.wait_group 0;\n" ::);
+  __syncthreads();
 
   // ---- phase 1: one warp per token
   constexpr int o_ks = 2 * (KB - 1) * D, o_vq = 2 * KB * D;      // QJL plane, value codes
   constexpr int o_vsm = o_vq + 2 * VB * D, o_norm = o_vsm + 2 * D; // scale / minimum, norms
   for (int tt = warp; tt < ntok; tt += C::THREADS / 32) {
-    const __half* kp = a.k + (base + tok0 + tt) * D;
-    const __half* vp = a.v + (base + tok0 + tt) * D;
+    const __half* kp = rh + tt * C::RS;  // staged k and v rows of this token
+    const __half* vp = rl + tt * C::RS;
     float x[E], vv[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       x[e] = __half2float(kp[coord_of(e, lane)]);
       vv[e] = __half2float(vp[coord_of(e, lane)]);
     }
+    __syncwarp();  // every lane has its k and v values before any lane overwrites the rows
     float ss = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) ss = fmaf(x[e], x[e], ss);
@@ -210,10 +238,15 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
     // values: group e = coordinates 32e..32e+31, one per lane
     float vmn[E], vmx[E];
     group_minmax<E>(vv, vmn, vmx);
+    // dimension-major code words: 2-bit: one word per dimension, token 2j+e at bits 16e+2j; 4-bit:
+    // two words per dimension (all first words, then all second words), word w holding tokens
+    // 8w+2j+e at bits 16e+4j.  Tokens of a page come from different warps: OR into the words.
+    uint32_t* vqw = reinterpret_cast<uint32_t*>(tile + o_vq) + (VB == 4 ? (slot >> 3) * D : 0);
+    const int vsh = VB == 2 ? 16 * (slot & 1) + 2 * (slot >> 1) : 16 * (slot & 1) + 4 * ((slot & 7) >> 1);
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       GroupCode g = group_quant_mm(vv[e], vmn[e], vmx[e], (float)((1 << VB) - 1));
-      vcodes[tt * D + coord_of(e, lane)] = (uint8_t)g.q;
+      if (g.q) atomicOr(vqw + coord_of(e, lane), (uint32_t)g.q << vsh);
       if (lane == 0) {
         __half* sm = reinterpret_cast<__half*>(tile + o_vsm + (slot * (D / 32) + e) * 4);
         sm[0] = g.s;
@@ -283,23 +316,6 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
         }
       }
     }
-  }
-  // ---- phase 3: dimension-major value-code words. 2-bit: one word per dimension, token 2j+e at
-  // bits 16e+2j. 4-bit: two words per dimension (all first words, then all second words), word w
-  // holding tokens 8w+2j+e at bits 16e+4j.
-  for (int w = threadIdx.x; w < (ntok >> 4) * D * (VB / 2); w += C::THREADS) {
-    const int p = w / (D * (VB / 2)), i = w % (D * (VB / 2));
-    uint32_t word = 0;
-    if (VB == 2) {
-#pragma unroll
-      for (int s = 0; s < 16; ++s) word |= (uint32_t)vcodes[(p * 16 + s) * D + i] << (16 * (s & 1) + 2 * (s >> 1));
-    } else {
-      const int half = i / D, dim = i % D;
-#pragma unroll
-      for (int s = 0; s < 8; ++s)
-        word |= (uint32_t)vcodes[(p * 16 + 8 * half + s) * D + dim] << (16 * (s & 1) + 4 * (s >> 1));
-    }
-    reinterpret_cast<uint32_t*>(tiles + (size_t)p * C::TILE + o_vq)[i] = word;
   }
   __syncthreads();
   store_tiles(a, tiles, C::TILE, o_norm + 64, ntok >> 4, b, h, (start + tok0) >> 4);

@@ -557,6 +557,7 @@ tq_status tq_encode_flush(tq_ctx* ctx, const void* k, const void* v, int batch, 
   if (n_tokens % tq::kPage) return TQ_ERR_INVALID_ARG;
   if (batch == 0 || n_tokens == 0) return TQ_OK;
   if (!k || !v || !start_pos || !block_table || !pool) return TQ_ERR_INVALID_ARG;
+  if ((((uintptr_t)k) | ((uintptr_t)v)) & 15) return TQ_ERR_INVALID_ARG;  // 16-byte row copies
   return cuda_status(tq::launch_encode(ctx, k, v, batch, src_tokens, n_tokens, start_pos, block_table, max_blocks,
                                        pool, num_blocks, stream));
 }
@@ -567,6 +568,7 @@ tq_status tq_append_token(tq_ctx* ctx, const void* k_new, const void* v_new, con
   if (!ctx || batch < 0 || max_blocks < 0 || num_blocks < 0) return TQ_ERR_INVALID_ARG;
   if (batch == 0) return TQ_OK;
   if (!k_new || !v_new || !pos || !ring_k || !ring_v || !block_table || !pool) return TQ_ERR_INVALID_ARG;
+  if ((((uintptr_t)ring_k) | ((uintptr_t)ring_v)) & 15) return TQ_ERR_INVALID_ARG;  // 16-byte row copies
   return cuda_status(tq::launch_append(ctx, k_new, v_new, pos, batch, ring_k, ring_v, block_table, max_blocks, pool,
                                        num_blocks, stream));
 }
