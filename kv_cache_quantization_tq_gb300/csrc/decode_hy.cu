@@ -36,10 +36,21 @@ namespace tq {
 namespace {
 
 constexpr int D = kTcD;
-constexpr int NW = 4;                  // warps per CTA
+// Warp roles of a CTA (one CTA per SM; it holds all 512 tensor-memory columns):
+//   warps 0..3   score: token t = thread t of the tile; key bytes into tensor memory, epilogue
+//   warp  4      producer: page copies into the stage ring
+//   warp  5      MMA issue (one lane)
+//   warps 6..13  value: warp 6 + v owns page v of every tile
+constexpr int NSW = 4;                 // score warps
+constexpr int NVW = 8;                 // value warps
+constexpr int W_PROD = NSW, W_MMA = NSW + 1, W_VAL0 = NSW + 2;
+constexpr int NWARPS = W_VAL0 + NVW;
+constexpr int NTHREADS = 32 * NWARPS;
+constexpr int NW = NSW;                // warps of the ring item (the mma.sync path)
 constexpr int TILE_PAGES = 8;          // pages per score tile: 128 tokens = M of the MMA
+static_assert(TILE_PAGES == NVW, "one value warp per page of a tile");
 constexpr int TILE_TOK = TILE_PAGES * kPage;
-constexpr int STAGES = 4;              // tiles of pages in shared memory
+constexpr int STAGES = 8;              // tiles of pages in shared memory
 constexpr int PAGE_BYTES = 12 * D + 64;  // main tile, 3-bit keys and 2-bit values: 1600
 constexpr int O_VQ = 6 * D, O_VSM = 10 * D, O_NORM = 12 * D;
 constexpr int NPIECE = 6;
@@ -52,8 +63,9 @@ constexpr int QOP_BYTES = NSLICE * SLICE_BYTES;
 constexpr int QREC_BYTES = QOP_BYTES + 4 * 4 * kMaxRep;
 static_assert(QREC_BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
 static_assert(QREC_BYTES == kHyQueryBytes, "query record size");
-// Tensor-memory columns: key bytes (96), Lloyd-Max and QJL accumulators (48 each).
-constexpr int TM_A = 0, TM_LM = 96, TM_QJ = 144, TM_COLS = 256;
+// Tensor-memory columns, two buffers of each: key bytes (96), Lloyd-Max and QJL accumulators
+// (48 each).
+constexpr int TM_BUF = 192, TM_A = 0, TM_LM = 96, TM_QJ = 144, TM_COLS = 512;
 // tcgen05 instruction descriptor: kind::f8f6f4, A = B = E4M3, D = F32, K-major, N = 48, M = 128.
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(QN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 
@@ -63,22 +75,33 @@ constexpr int OFF_STAGE = QREC_BYTES;
 constexpr int STAGE_BYTES = TILE_PAGES * PAGE_BYTES;
 constexpr int OFF_PBUF = OFF_STAGE + STAGES * STAGE_BYTES;
 constexpr int PBUF_BYTES = kMaxRep * TILE_TOK * 4;
-constexpr int OFF_MISC = OFF_PBUF + 2 * PBUF_BYTES;
-constexpr int OFF_BAR_FULL = OFF_MISC;               // STAGES mbarriers
-constexpr int OFF_BAR_MMA = OFF_MISC + 8 * STAGES;
-constexpr int OFF_BAR_Q = OFF_BAR_MMA + 8;
+constexpr int OFF_WO = OFF_PBUF + 2 * PBUF_BYTES;              // [NVW][kMaxRep][D] value results
+constexpr int OFF_MISC = OFF_WO + NVW * kMaxRep * D * 4;
+// mbarriers (8 bytes each)
+constexpr int OFF_BAR_SFULL = OFF_MISC;                  // [STAGES] pages landed (producer, tx)
+constexpr int OFF_BAR_SEMPTY = OFF_BAR_SFULL + 8 * STAGES;  // [STAGES] score + value warps done
+constexpr int OFF_BAR_AFULL = OFF_BAR_SEMPTY + 8 * STAGES;  // [2] key bytes in tensor memory
+constexpr int OFF_BAR_DFULL = OFF_BAR_AFULL + 16;           // [2] score MMAs complete
+constexpr int OFF_BAR_PFULL = OFF_BAR_DFULL + 16;           // [2] p of a tile written
+constexpr int OFF_BAR_PEMPTY = OFF_BAR_PFULL + 16;          // [2] value warps done with p
+constexpr int OFF_BAR_Q = OFF_BAR_PEMPTY + 16;              // query record landed
 constexpr int OFF_TMEM = OFF_BAR_Q + 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
-constexpr int OFF_VALID = OFF_ABORT + 4;             // [STAGES] valid-page masks
-constexpr int OFF_WRED = OFF_VALID + 4 * STAGES;     // [NW][kMaxRep] floats
-constexpr int OFF_WRED2 = OFF_WRED + 4 * NW * kMaxRep;
-constexpr int MISC_BYTES = OFF_WRED2 + 4 * NW * kMaxRep - OFF_MISC;
+constexpr int OFF_VALID = OFF_ABORT + 4;                    // [STAGES] valid-page masks
+constexpr int OFF_ALPHA = OFF_VALID + 4 * STAGES;           // [2][kMaxRep + 1] rescale factors, flag
+constexpr int OFF_WRED = OFF_ALPHA + 4 * 2 * (kMaxRep + 1) + 8;  // [NWARPS][kMaxRep] floats
+constexpr int OFF_WRED2 = OFF_WRED + 4 * NWARPS * kMaxRep;
+constexpr int OFF_MFIN = OFF_WRED2 + 4 * NWARPS * kMaxRep;  // [kMaxRep] final reference maxima
+constexpr int MISC_BYTES = OFF_MFIN + 4 * kMaxRep - OFF_MISC;
 constexpr int SMEM_USED = OFF_MISC + MISC_BYTES;
-// With the alignment slack: above a third of the SM's shared memory, so at most two CTAs (2 x 256
-// tensor-memory columns) share an SM and tcgen05.alloc never waits.
-constexpr int HY_SMEM = SMEM_USED + 1024 > 80 * 1024 ? SMEM_USED + 1024 : 80 * 1024;
-static_assert((size_t)NW * kMaxRep * D * sizeof(float) <= (size_t)STAGES * STAGE_BYTES, "combine buffer fits");
+constexpr int HY_SMEM = SMEM_USED + 1024;
+// The ring item combines its warps' results in the (idle) stage ring.
+static_assert((size_t)NWARPS * kMaxRep * D * sizeof(float) <= (size_t)STAGES * STAGE_BYTES, "combine buffer fits");
+// More than half of an SM's shared memory: one CTA per SM, so that the CTA's 512 tensor-memory
+// columns are always free when it allocates them.
+static_assert(HY_SMEM > 116 * 1024 && HY_SMEM <= 227 * 1024, "one CTA per SM");
 static_assert(OFF_STAGE % 16 == 0 && OFF_PBUF % 16 == 0 && OFF_MISC % 16 == 0, "alignment");
+static_assert(OFF_BAR_SFULL % 8 == 0 && OFF_BAR_Q % 8 == 0, "mbarrier alignment");
 
 // A key bit lands at bit position P of its e4m3 byte, which then holds base_P when the bit is 0 and
 // base_P | 1 << P when it is 1 (the e4m3 value beta0 + delta bit).  Only three positions are used:
@@ -181,6 +204,20 @@ __device__ __forceinline__ void tm_ld48(uint32_t taddr, float (&v)[48]) {
   for (int i = 0; i < 48; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tm_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Named barrier 1 over the score warps: the OR of v over their threads (ordering their shared
+// memory accesses like bar.sync).
+__device__ __forceinline__ bool score_any(bool v) {
+  uint32_t r;
+  asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 1, %2, p; selp.u32 %0, 1, 0, q; }"
+               : "=r"(r)
+               : "r"((uint32_t)v), "n"(NSW * 32)
+               : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void score_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NSW * 32) : "memory"); }
 
 // ---------------------------------------------------------------- query record
 // Per (sequence, head group), 4 warps: q_r = H (D q) / sqrt(d) of the group's heads, t = S q_r
@@ -322,8 +359,8 @@ struct Smem {
   __device__ uint32_t addr(int off) const { return base_s + (uint32_t)off; }
 };
 
-// The ring item (exact fp16 buffer): the mma.sync path of decode_tc.cu, per-warp softmax states
-// combined at the end.
+// The ring item (exact fp16 buffer): the mma.sync path of decode_tc.cu on every warp of the CTA,
+// per-warp softmax states combined at the end.
 __device__ void ring_item(const TcArgs& a, const Smem& sm, int b, int h0, int kvh, int nb, int nparts, int part) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -348,12 +385,12 @@ __device__ void ring_item(const TcArgs& a, const Smem& sm, int b, int h0, int kv
   }
   const __half* rk = a.ring_k + ((size_t)b * a.hkv + kvh) * kRing * D;
   const __half* rv = a.ring_v + ((size_t)b * a.hkv + kvh) * kRing * D;
-  for (int t0 = warp * 16; t0 < nb; t0 += NW * 16) page_ring(a, Aq, rk, rv, t0, min(16, nb - t0), st, lane);
+  for (int t0 = warp * 16; t0 < nb; t0 += NWARPS * 16) page_ring(a, Aq, rk, rv, t0, min(16, nb - t0), st, lane);
   float l = st.l;
   l += __shfl_xor_sync(kFull, l, 1);
   l += __shfl_xor_sync(kFull, l, 2);
-  float* wo = reinterpret_cast<float*>(sm.ptr(OFF_STAGE));  // [NW][kMaxRep][D]
-  float* wm = reinterpret_cast<float*>(sm.ptr(OFF_WRED));   // [NW][kMaxRep]
+  float* wo = reinterpret_cast<float*>(sm.ptr(OFF_STAGE));  // [NWARPS][kMaxRep][D]
+  float* wm = reinterpret_cast<float*>(sm.ptr(OFF_WRED));   // [NWARPS][kMaxRep]
   float* wl = reinterpret_cast<float*>(sm.ptr(OFF_WRED2));
 #pragma unroll
   for (int nt = 0; nt < 16; ++nt)
@@ -365,14 +402,14 @@ __device__ void ring_item(const TcArgs& a, const Smem& sm, int b, int h0, int kv
     wl[warp * kMaxRep + g] = l;
   }
   __syncthreads();
-  for (int i = tid; i < a.nrg * D; i += NW * 32) {
+  for (int i = tid; i < a.nrg * D; i += NTHREADS) {
     const int h = i / D, dim = i % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w2 = 0; w2 < NW; ++w2) M = fmaxf(M, wm[w2 * kMaxRep + h]);
+    for (int w2 = 0; w2 < NWARPS; ++w2) M = fmaxf(M, wm[w2 * kMaxRep + h]);
     float num = 0.f, den = 0.f;
 #pragma unroll
-    for (int w2 = 0; w2 < NW; ++w2) {
+    for (int w2 = 0; w2 < NWARPS; ++w2) {
       const float f = M == -INFINITY ? 0.f : exp2f(wm[w2 * kMaxRep + h] - M);
       num = fmaf(f, wo[((size_t)w2 * kMaxRep + h) * D + dim], num);
       den = fmaf(f, wl[w2 * kMaxRep + h], den);
@@ -435,7 +472,13 @@ __device__ __forceinline__ void page_values(const uint8_t* T, const float* pb, f
   }
 }
 
-__global__ void __launch_bounds__(NW * 32, 2) hy_decode_kernel(TcArgs a, const uint8_t* qrec) {
+// Pipeline of a compressed chunk, in tiles of 128 tokens (8 pages).  Producer: tile i's pages into
+// stage i mod STAGES.  Score warps: tile i's key bits into key-byte buffer i mod 2 of tensor memory
+// (a_full), then the epilogue of tile i - 1 (d_full): logits, the lazy reference update, p and the
+// rescale factors into p buffer (i - 1) mod 2 (p_full).  MMA lane: the 12 score MMAs of tile i into
+// accumulator buffer i mod 2 (d_full).  Value warps: page v of tile j once its p is written; they
+// release the p buffer (p_empty) and, with the score warps, the stage (s_empty).
+__global__ void __launch_bounds__(NTHREADS, 1) hy_decode_kernel(TcArgs a, const uint8_t* qrec, int batch) {
   extern __shared__ uint8_t smem_raw[];
   Smem sm;
   {
@@ -444,7 +487,14 @@ __global__ void __launch_bounds__(NW * 32, 2) hy_decode_kernel(TcArgs a, const u
     sm.base = smem_raw + (al - s0);
     sm.base_s = al;
   }
-  const int part = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
+  // One-dimensional grid: every (sequence, head group)'s chunks first, then the ring items, so the
+  // short ring CTAs take whatever SMs the chunks leave and never hold a chunk back a wave.
+  const int hgroups = a.hkv * a.groups;
+  const int nchunk_ctas = a.n_chunks * batch * hgroups;
+  const int id = blockIdx.x;
+  const int part = id < nchunk_ctas ? id % a.n_chunks : a.n_chunks;
+  const int item = id < nchunk_ctas ? id / a.n_chunks : id - nchunk_ctas;  // (sequence, head group)
+  const int hg = item % hgroups, b = item / hgroups;
   const int kvh = hg / a.groups;
   const int h0 = kvh * a.n_rep + (hg % a.groups) * a.nrg;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -471,7 +521,16 @@ __global__ void __launch_bounds__(NW * 32, 2) hy_decode_kernel(TcArgs a, const u
   const int32_t* btb = a.block_table + (size_t)b * a.max_blocks + pbeg;
   uint32_t* abort_flag = reinterpret_cast<uint32_t*>(sm.ptr(OFF_ABORT));
   uint32_t* valid = reinterpret_cast<uint32_t*>(sm.ptr(OFF_VALID));
-  const uint32_t bar_full = sm.addr(OFF_BAR_FULL), bar_mma = sm.addr(OFF_BAR_MMA), bar_q = sm.addr(OFF_BAR_Q);
+  float* alpha_s = reinterpret_cast<float*>(sm.ptr(OFF_ALPHA));  // [2][kMaxRep + 1]: factors, flag
+  float* wred = reinterpret_cast<float*>(sm.ptr(OFF_WRED));
+  float* wl = reinterpret_cast<float*>(sm.ptr(OFF_WRED2));
+  float* mfin = reinterpret_cast<float*>(sm.ptr(OFF_MFIN));
+  float* wo = reinterpret_cast<float*>(sm.ptr(OFF_WO));
+  const uint32_t bar_sfull = sm.addr(OFF_BAR_SFULL), bar_sempty = sm.addr(OFF_BAR_SEMPTY);
+  const uint32_t bar_afull = sm.addr(OFF_BAR_AFULL), bar_dfull = sm.addr(OFF_BAR_DFULL);
+  const uint32_t bar_pfull = sm.addr(OFF_BAR_PFULL), bar_pempty = sm.addr(OFF_BAR_PEMPTY);
+  const uint32_t bar_q = sm.addr(OFF_BAR_Q);
+  auto stage = [&](int st) { return sm.ptr(OFF_STAGE + st * STAGE_BYTES); };
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sm.addr(OFF_TMEM)),
@@ -479,268 +538,312 @@ __global__ void __launch_bounds__(NW * 32, 2) hy_decode_kernel(TcArgs a, const u
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // Thread 0 issues every copy: the query record, then the first STAGES tiles of pages.
-  int issued = 0;  // tiles whose copies thread 0 has issued
-  // Block ids of a tile's pages (thread 0; -1 past the chunk), requested one tile before the copies
-  // are issued so that the table read is off the path of the barrier that follows the issue.
-  auto tile_blocks = [&](int ti, int (&blk)[TILE_PAGES]) {
-    const int p0 = ti * TILE_PAGES, np = ti < ntiles ? min(TILE_PAGES, npg - p0) : 0;
-#pragma unroll
-    for (int q = 0; q < TILE_PAGES; ++q) blk[q] = q < np ? __ldg(btb + p0 + q) : -1;
-  };
-  auto issue_tile = [&](int ti, const int (&blk)[TILE_PAGES]) {
-    issued = ti + 1;
-    const int st = ti % STAGES;
-    const int p0 = ti * TILE_PAGES, np = min(TILE_PAGES, npg - p0);
-    uint32_t mask = 0, bytes = 0;
-#pragma unroll
-    for (int q = 0; q < TILE_PAGES; ++q) {
-      if (q < np) {
-        if (blk[q] >= 0 && blk[q] < a.num_blocks) {
-          mask |= 1u << q;
-          bytes += PAGE_BYTES;
-        } else {
-          flag_error(a.err, TQ_DEVERR_BLOCK_ID);
-        }
-      }
-    }
-    valid[st] = mask;
-    mbar_expect_tx(bar_full + 8 * st, bytes);
-#pragma unroll
-    for (int q = 0; q < TILE_PAGES; ++q)
-      if (mask >> q & 1)
-        bulk_g2s(sm.addr(OFF_STAGE + st * STAGE_BYTES + q * PAGE_BYTES),
-                 a.pool + ((size_t)blk[q] * a.hkv + kvh) * PAGE_BYTES, PAGE_BYTES, bar_full + 8 * st);
-  };
-  if (tid == 0) {
+  if (tid == W_PROD * 32) {
     *abort_flag = 0;
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) mbar_init(bar_full + 8 * s, 1);
-    mbar_init(bar_mma, 1);
+    for (int st = 0; st < STAGES; ++st) {
+      mbar_init(bar_sfull + 8 * st, 1);
+      mbar_init(bar_sempty + 8 * st, NSW + NVW);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar_afull + 8 * k, NSW * 32);
+      mbar_init(bar_dfull + 8 * k, 1);
+      mbar_init(bar_pfull + 8 * k, NSW * 32);
+      mbar_init(bar_pempty + 8 * k, NVW);
+    }
     mbar_init(bar_q, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     mbar_expect_tx(bar_q, QREC_BYTES);
     bulk_g2s(sm.addr(OFF_Q), qrec + ((size_t)b * a.hkv * a.groups + hg) * QREC_BYTES, QREC_BYTES, bar_q);
-    for (int ti = 0; ti < min(STAGES, ntiles); ++ti) {
-      int blk[TILE_PAGES];
-      tile_blocks(ti, blk);
-      issue_tile(ti, blk);
-    }
   }
-  int nblk[TILE_PAGES];  // thread 0: block ids of the next tile to issue
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm.ptr(OFF_TMEM));
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  bool bad = false;  // a bounded wait of this thread expired
 
-  // per-thread state: the CTA's reference maxima (identical in every thread), this token's share of
-  // the normalisers, the warp's value accumulators and group-minimum terms
-  float mref[kMaxRep], lsum[kMaxRep];
+  if (warp < NSW) {
+    // ================================================================ score warps: thread = token
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float* qs = reinterpret_cast<const float*>(sm.ptr(OFF_Q + QOP_BYTES));  // scale[2][8], off[2][8]
+    const float coef = a.qjl_coef, lscale = a.logit_scale;
+    float mref[kMaxRep], lsum[kMaxRep];
 #pragma unroll
-  for (int h = 0; h < kMaxRep; ++h) {
-    mref[h] = -INFINITY;
-    lsum[h] = 0.f;
-  }
-  float o[16][4], mnacc[4];
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) o[nt][r] = 0.f;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) mnacc[k] = 0.f;
-  const float coef = a.qjl_coef, lscale = a.logit_scale;
-  bool aborted = false;
-
-  auto values_of = [&](int ti) {
-    const int st = ti % STAGES;
-    const uint32_t mask = valid[st];
-    const float* pb = reinterpret_cast<const float*>(sm.ptr(OFF_PBUF + (ti & 1) * PBUF_BYTES));
+    for (int h = 0; h < kMaxRep; ++h) {
+      mref[h] = -INFINITY;
+      lsum[h] = 0.f;
+    }
+    bool stop = false;
 #pragma unroll 1
-    for (int q = warp; q < TILE_PAGES; q += NW)
-      if (mask >> q & 1)
-        page_values(sm.ptr(OFF_STAGE + st * STAGE_BYTES + q * PAGE_BYTES), pb + q * kPage, o, mnacc, lane);
-  };
-
-#pragma unroll 1
-  for (int ti = 0; ti < ntiles; ++ti) {
-    const int st = ti % STAGES;
-    if (tid == 0 && ti > 0) tile_blocks(ti - 1 + STAGES, nblk);  // issued at the end of this iteration
-    // ---- tile ti's pages in shared memory; key bits of token tid -> e4m3 bytes in tensor memory
-    if (!mbar_wait(bar_full + 8 * st, (uint32_t)(ti / STAGES) & 1u)) atomicOr(abort_flag, 1u);
-    {
-      const uint8_t* T = sm.ptr(OFF_STAGE + st * STAGE_BYTES + (tid >> 4) * PAGE_BYTES);
-      const int slot = tid & 15;
+    for (int i = 0; i <= ntiles; ++i) {
+      if (i < ntiles) {
+        // key bits of token tid of tile i -> e4m3 bytes in key-byte buffer i mod 2
+        const int st = i % STAGES;
+        bad |= !mbar_wait(bar_sfull + 8 * st, (uint32_t)(i / STAGES) & 1u);
+        const uint8_t* T = stage(st) + (tid >> 4) * PAGE_BYTES;
+        const int slot = tid & 15;
 #pragma unroll
-      for (int p = 0; p < 3; ++p) {
-        const uint4 row = *reinterpret_cast<const uint4*>(T + 2 * D * p + slot * 16);
-        uint32_t r[32];
+        for (int p = 0; p < 3; ++p) {
+          const uint4 row = *reinterpret_cast<const uint4*>(T + 2 * D * p + slot * 16);
+          uint32_t r[32];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const uint32_t x = word_of(row, w);
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t x = word_of(row, w);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) r[8 * w + j] = key_bytes(x, j);
+            for (int j = 0; j < 8; ++j) r[8 * w + j] = key_bytes(x, j);
+          }
+          tm_st32(tmem + lane_base + (i & 1) * TM_BUF + TM_A + 32 * p, r);
         }
-        tm_st32(tmem + lane_base + TM_A + 32 * p, r);
+        tm_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_afull + 8 * (i & 1));
       }
-      tm_wait_st();
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (*reinterpret_cast<volatile uint32_t*>(abort_flag)) {
-      aborted = true;
-      break;
-    }
-    tc_fence_after();
-    if (tid == 0) {
-      if (ti == 0 && !mbar_wait(bar_q, 0)) atomicOr(abort_flag, 2u);
-      const uint32_t qop = sm.addr(OFF_Q);
+      if (i == 0) continue;
+      // ---- epilogue of tile j = i - 1
+      const int j = i - 1, st = j % STAGES, buf = j & 1;
+      if (j == 0) bad |= !mbar_wait(bar_q, 0);
+      bad |= !mbar_wait(bar_dfull + 8 * buf, (uint32_t)(j >> 1) & 1u);
+      tc_fence_after();
+      float logit[kMaxRep];
+      {
+        float lm[kMaxRep], qj[kMaxRep];
 #pragma unroll
-      for (int s = 0; s < NSLICE; ++s)
-        mma_f8(tmem + (s < 8 ? TM_LM : TM_QJ), tmem + TM_A + 8 * s, sdesc(qop + s * SLICE_BYTES), s % 8 != 0);
-      mma_commit(bar_mma);
-    }
-    // ---- meanwhile: the value product of the previous tile
-    if (ti > 0) values_of(ti - 1);
-    // ---- score epilogue of tile ti: thread = token
-    if (ti == 0 && tid != 0 && !mbar_wait(bar_q, 0)) atomicOr(abort_flag, 2u);
-    if (!mbar_wait(bar_mma, (uint32_t)ti & 1u)) atomicOr(abort_flag, 4u);
-    tc_fence_after();
-    float logit[kMaxRep];
-    {
-      const float* qs = reinterpret_cast<const float*>(sm.ptr(OFF_Q + QOP_BYTES));  // scale[2][8], off[2][8]
-      float lm[kMaxRep], qj[kMaxRep];
+        for (int set = 0; set < 2; ++set) {
+          float v[QN];
+          tm_ld48(tmem + lane_base + buf * TM_BUF + (set ? TM_QJ : TM_LM), v);
 #pragma unroll
-      for (int set = 0; set < 2; ++set) {
-        float v[QN];
-        tm_ld48(tmem + lane_base + (set ? TM_QJ : TM_LM), v);
+          for (int h = 0; h < kMaxRep; ++h) {
+            float acc = v[NPIECE * h + NPIECE - 1];
+#pragma unroll
+            for (int pc = NPIECE - 2; pc >= 0; --pc) acc = fmaf(acc, 0.0625f, v[NPIECE * h + pc]);
+            const float r = fmaf(acc, qs[set * kMaxRep + h], qs[2 * kMaxRep + set * kMaxRep + h]);
+            if (set == 0)
+              lm[h] = r;
+            else
+              qj[h] = r;
+          }
+        }
+        const uint8_t* T = stage(st) + (tid >> 4) * PAGE_BYTES;
+        const int slot = tid & 15;
+        const float nk = __half2float(*reinterpret_cast<const __half*>(T + O_NORM + 2 * slot));
+        const float nr = __half2float(*reinterpret_cast<const __half*>(T + O_NORM + 32 + 2 * slot));
+        const bool ok = valid[st] >> (tid >> 4) & 1;
+        const float cnr = coef * nr, nks = nk * lscale;
+#pragma unroll
+        for (int h = 0; h < kMaxRep; ++h) logit[h] = (ok && h < a.nrg) ? nks * fmaf(cnr, qj[h], lm[h]) : -INFINITY;
+      }
+      // p buffer j mod 2 and its rescale factors are free once the value warps are done with tile j - 2
+      if (j >= 2) bad |= !mbar_wait(bar_pempty + 8 * buf, (uint32_t)((j >> 1) - 1) & 1u);
+      bad |= *reinterpret_cast<volatile uint32_t*>(abort_flag) != 0;
+      // lazy reference update: only when a logit passes its reference by more than 2^kLazyLog2;
+      // the same vote carries the abort decision, so the four warps always leave together
+      int exceed = 0;
+#pragma unroll
+      for (int h = 0; h < kMaxRep; ++h) exceed |= logit[h] > mref[h] + kLazyLog2;
+      float* al = alpha_s + buf * (kMaxRep + 1);
+      if (score_any(exceed || bad)) {
+        if (score_any(bad)) {
+          stop = true;
+          break;
+        }
 #pragma unroll
         for (int h = 0; h < kMaxRep; ++h) {
-          float acc = v[NPIECE * h + NPIECE - 1];
-#pragma unroll
-          for (int pc = NPIECE - 2; pc >= 0; --pc) acc = fmaf(acc, 0.0625f, v[NPIECE * h + pc]);
-          const float r = fmaf(acc, qs[set * kMaxRep + h], qs[2 * kMaxRep + set * kMaxRep + h]);
-          if (set == 0)
-            lm[h] = r;
-          else
-            qj[h] = r;
+          const float m = warp_max(logit[h]);
+          if (lane == 0) wred[warp * kMaxRep + h] = m;
         }
-      }
-      const uint8_t* T = sm.ptr(OFF_STAGE + st * STAGE_BYTES + (tid >> 4) * PAGE_BYTES);
-      const int slot = tid & 15;
-      const float nk = __half2float(*reinterpret_cast<const __half*>(T + O_NORM + 2 * slot));
-      const float nr = __half2float(*reinterpret_cast<const __half*>(T + O_NORM + 32 + 2 * slot));
-      const bool ok = valid[st] >> (tid >> 4) & 1;
-      const float cnr = coef * nr, nks = nk * lscale;
+        score_sync();
 #pragma unroll
-      for (int h = 0; h < kMaxRep; ++h) logit[h] = (ok && h < a.nrg) ? nks * fmaf(cnr, qj[h], lm[h]) : -INFINITY;
-    }
-    // lazy reference update: only when a logit passes its reference by more than 2^kLazyLog2
-    int exceed = 0;
+        for (int h = 0; h < kMaxRep; ++h) {
+          float m = mref[h];
 #pragma unroll
-    for (int h = 0; h < kMaxRep; ++h) exceed |= logit[h] > mref[h] + kLazyLog2;
-    tc_fence_before();
-    if (__syncthreads_or(exceed)) {
-      float* wred = reinterpret_cast<float*>(sm.ptr(OFF_WRED));
-#pragma unroll
-      for (int h = 0; h < kMaxRep; ++h) {
-        const float m = warp_max(logit[h]);
-        if (lane == 0) wred[warp * kMaxRep + h] = m;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int h = 0; h < kMaxRep; ++h) {
-        float m = mref[h];
-#pragma unroll
-        for (int w2 = 0; w2 < NW; ++w2) m = fmaxf(m, wred[w2 * kMaxRep + h]);
-        // 0 on a head's first update (reference -inf); 1 while the head has no valid token
-        const float alpha = m == -INFINITY ? 1.f : fast_exp2(mref[h] - m);
-        mref[h] = m;
-        lsum[h] *= alpha;
-        // this warp's value state: lane (g, t) holds head g's rows
-        if ((lane >> 2) == h) {
-#pragma unroll
-          for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) o[nt][r] *= alpha;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mnacc[k] *= alpha;
+          for (int w2 = 0; w2 < NSW; ++w2) m = fmaxf(m, wred[w2 * kMaxRep + h]);
+          // 0 on a head's first update (reference -inf); 1 while the head has no valid token
+          const float alpha = m == -INFINITY ? 1.f : fast_exp2(mref[h] - m);
+          mref[h] = m;
+          lsum[h] *= alpha;
+          if (tid == 0) al[h] = alpha;
         }
+        if (tid == 0) al[kMaxRep] = 1.f;
+      } else if (tid == 0) {
+        al[kMaxRep] = 0.f;
       }
-    }
-    {
-      float* pb = reinterpret_cast<float*>(sm.ptr(OFF_PBUF + (ti & 1) * PBUF_BYTES));
+      float* pb = reinterpret_cast<float*>(sm.ptr(OFF_PBUF + buf * PBUF_BYTES));
 #pragma unroll
       for (int h = 0; h < kMaxRep; ++h) {
         const float p = logit[h] == -INFINITY ? 0.f : fast_exp2(logit[h] - mref[h]);
         lsum[h] += p;
         pb[h * TILE_TOK + tid] = p;
       }
+      mbar_arrive(bar_pfull + 8 * buf);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_sempty + 8 * st);
     }
-    __syncthreads();  // p of tile ti visible; tile ti-1's stage and values done by every warp
-    if (*reinterpret_cast<volatile uint32_t*>(abort_flag)) {
-      aborted = true;
-      break;
+    if (stop) {
+      if (tid == 0) atomicOr(abort_flag, 1u);
+    } else {
+      // this CTA's normalisers (in their own array: another score warp may still read the maxima
+      // of the last update) and reference maxima
+#pragma unroll
+      for (int h = 0; h < kMaxRep; ++h) {
+        const float s = warp_sum(lsum[h]);
+        if (lane == 0) wl[warp * kMaxRep + h] = s;
+        if (tid == 0) mfin[h] = mref[h];
+      }
     }
-    if (tid == 0 && ti > 0 && ti - 1 + STAGES < ntiles) issue_tile(ti - 1 + STAGES, nblk);
+  } else if (warp == W_PROD) {
+    // ================================================================ producer
+    if (lane == 0) {
+      int issued = 0;
+      int blk[TILE_PAGES];  // block ids of the next tile (-1 past the chunk), read one tile ahead
+      auto tile_blocks = [&](int ti) {
+        const int p0 = ti * TILE_PAGES, np = min(TILE_PAGES, npg - p0);
+#pragma unroll
+        for (int q = 0; q < TILE_PAGES; ++q) blk[q] = q < np ? __ldg(btb + p0 + q) : -1;
+      };
+      tile_blocks(0);
+#pragma unroll 1
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % STAGES;
+        if (i >= STAGES && !mbar_wait(bar_sempty + 8 * st, (uint32_t)(i / STAGES - 1) & 1u)) {
+          bad = true;
+          break;
+        }
+        uint32_t mask = 0, bytes = 0;
+#pragma unroll
+        for (int q = 0; q < TILE_PAGES; ++q) {
+          if (blk[q] >= 0 && blk[q] < a.num_blocks) {
+            mask |= 1u << q;
+            bytes += PAGE_BYTES;
+          } else if (q < min(TILE_PAGES, npg - i * TILE_PAGES)) {
+            flag_error(a.err, TQ_DEVERR_BLOCK_ID);
+          }
+        }
+        valid[st] = mask;
+        mbar_expect_tx(bar_sfull + 8 * st, bytes);
+#pragma unroll
+        for (int q = 0; q < TILE_PAGES; ++q)
+          if (mask >> q & 1)
+            bulk_g2s(sm.addr(OFF_STAGE + st * STAGE_BYTES + q * PAGE_BYTES),
+                     a.pool + ((size_t)blk[q] * a.hkv + kvh) * PAGE_BYTES, PAGE_BYTES, bar_sfull + 8 * st);
+        issued = i + 1;
+        if (i + 1 < ntiles) tile_blocks(i + 1);
+        if (*reinterpret_cast<volatile uint32_t*>(abort_flag)) break;
+      }
+      if (bad) atomicOr(abort_flag, 1u);
+      // the copies of the last tile issued into each stage land before the CTA leaves (every earlier
+      // tile was consumed, which needed its copies)
+      for (int i = max(0, issued - STAGES); i < issued; ++i)
+        mbar_wait(bar_sfull + 8 * (i % STAGES), (uint32_t)(i / STAGES) & 1u);
+    }
+  } else if (warp == W_MMA) {
+    // ================================================================ MMA issue
+    if (lane == 0) {
+      int last = -1;
+      bad = !mbar_wait(bar_q, 0);
+      const uint32_t qop = sm.addr(OFF_Q);
+#pragma unroll 1
+      for (int i = 0; i < ntiles && !bad; ++i) {
+        const int buf = i & 1;
+        if (!mbar_wait(bar_afull + 8 * buf, (uint32_t)(i >> 1) & 1u)) {
+          bad = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + buf * TM_BUF;
+#pragma unroll
+        for (int s = 0; s < NSLICE; ++s)
+          mma_f8(d + (s < 8 ? TM_LM : TM_QJ), d + TM_A + 8 * s, sdesc(qop + s * SLICE_BYTES), s % 8 != 0);
+        mma_commit(bar_dfull + 8 * buf);
+        last = i;
+      }
+      if (bad) atomicOr(abort_flag, 1u);
+      // the tensor memory is released only after the last MMA has completed
+      if (last >= 0) mbar_wait(bar_dfull + 8 * (last & 1), (uint32_t)(last >> 1) & 1u);
+    }
+  } else {
+    // ================================================================ value warps: page v of each tile
+    const int v = warp - W_VAL0;
+    const int g = lane >> 2, t = lane & 3;
+    float o[16][4], mnacc[4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) o[nt][r] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mnacc[k] = 0.f;
+#pragma unroll 1
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j % STAGES, buf = j & 1;
+      bool ok = mbar_wait(bar_sfull + 8 * st, (uint32_t)(j / STAGES) & 1u);
+      ok = ok && mbar_wait(bar_pfull + 8 * buf, (uint32_t)(j >> 1) & 1u);
+      if (!__all_sync(kFull, ok)) {
+        bad = true;
+        break;
+      }
+      const float* al = alpha_s + buf * (kMaxRep + 1);
+      if (al[kMaxRep] != 0.f) {
+        const float f = al[g];
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) o[nt][r] *= f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mnacc[k] *= f;
+      }
+      if (valid[st] >> v & 1)
+        page_values(stage(st) + v * PAGE_BYTES, reinterpret_cast<const float*>(sm.ptr(OFF_PBUF + buf * PBUF_BYTES)) +
+                                                    v * kPage,
+                    o, mnacc, lane);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_pempty + 8 * buf);
+        mbar_arrive(bar_sempty + 8 * st);
+      }
+    }
+    if (bad && lane == 0) atomicOr(abort_flag, 1u);
+    float mn[4];
+#pragma unroll
+    for (int gg = 0; gg < 4; ++gg) {
+      mn[gg] = mnacc[gg];
+      mn[gg] += __shfl_xor_sync(kFull, mn[gg], 1);
+      mn[gg] += __shfl_xor_sync(kFull, mn[gg], 2);
+    }
+    constexpr float vscale = 4.f / kWeightScale;  // codes 1 + q/4, weights p s 2^-kLazyLog2
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        wo[((size_t)v * kMaxRep + g) * D + nt * 8 + 2 * t + e] =
+            fmaf(o[nt][2 + e], kLoUnscale, o[nt][e]) * vscale + mn[nt >> 2];
   }
-  if (!aborted && ntiles > 0) values_of(ntiles - 1);
 
-  if (aborted) {
-    if (tid == 0) {
-      flag_error(a.err, TQ_DEVERR_TIMEOUT);
-      // drain: the copies of the last tile issued into each stage complete (bounded) before the
-      // shared memory is released
-      for (int ti = max(0, issued - STAGES); ti < issued; ++ti)
-        mbar_wait(bar_full + 8 * (ti % STAGES), (uint32_t)(ti / STAGES) & 1u);
-    }
-  }
-  // the tensor memory is free once the last MMA has been waited for (or the wait gave up)
+  // every role is done: MMAs complete, copies landed, tensor memory read
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(TM_COLS) : "memory");
-  if (aborted) return;
+  if (*reinterpret_cast<volatile uint32_t*>(abort_flag)) {
+    if (tid == 0) flag_error(a.err, TQ_DEVERR_TIMEOUT);
+    return;
+  }
 
-  // ---- combine: normalisers over the CTA's tokens, value accumulators over its warps
-  float* wred = reinterpret_cast<float*>(sm.ptr(OFF_WRED));
-#pragma unroll
-  for (int h = 0; h < kMaxRep; ++h) {
-    const float s = warp_sum(lsum[h]);
-    if (lane == 0) wred[warp * kMaxRep + h] = s;
-  }
-  const int g = lane >> 2, t = lane & 3;
-  float mn[4];
-#pragma unroll
-  for (int gg = 0; gg < 4; ++gg) {
-    mn[gg] = mnacc[gg];
-    mn[gg] += __shfl_xor_sync(kFull, mn[gg], 1);
-    mn[gg] += __shfl_xor_sync(kFull, mn[gg], 2);
-  }
-  float* wo = reinterpret_cast<float*>(sm.ptr(OFF_STAGE));  // [NW][kMaxRep][D]; stages are idle
-  constexpr float vscale = 4.f / kWeightScale;             // codes 1 + q/4, weights p s 2^-kLazyLog2
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e)
-      wo[((size_t)warp * kMaxRep + g) * D + nt * 8 + 2 * t + e] =
-          fmaf(o[nt][2 + e], kLoUnscale, o[nt][e]) * vscale + mn[nt >> 2];
-  __syncthreads();
+  // ---- combine: normalisers over the score warps, value results over the value warps
   const bool direct = nparts == 1;
-  for (int i = tid; i < a.nrg * D; i += NW * 32) {
+  for (int i = tid; i < a.nrg * D; i += NTHREADS) {
     const int h = i / D, dim = i % D;
-    const float den = (wred[h] + wred[kMaxRep + h]) + (wred[2 * kMaxRep + h] + wred[3 * kMaxRep + h]);
+    const float den = (wl[h] + wl[kMaxRep + h]) + (wl[2 * kMaxRep + h] + wl[3 * kMaxRep + h]);
     float num = 0.f;
 #pragma unroll
-    for (int w2 = 0; w2 < NW; ++w2) num += wo[((size_t)w2 * kMaxRep + h) * D + dim];
+    for (int v = 0; v < NVW; ++v) num += wo[((size_t)v * kMaxRep + h) * D + dim];
     if (direct) {
       a.out[((size_t)b * a.hq + h0 + h) * D + dim] = den > 0.f ? num / den : 0.f;
     } else {
       float* dst = a.parts + (((size_t)b * a.hq + h0 + h) * a.n_parts + part) * (D + 4);
       dst[dim] = num;
       if (dim == 0) {
-        dst[D] = mref[h];
+        dst[D] = mfin[h];
         dst[D + 1] = den;
       }
     }
@@ -765,7 +868,7 @@ cudaError_t launch_decode_hy(tq_ctx* ctx, TcArgs& a, int batch, uint8_t* qrec, c
   if (e != cudaSuccess) return e;
   ctx->decode_kernel = "hy_decode_kernel";
   prof_start(ctx, kProfDecode, s);
-  hy_decode_kernel<<<dim3(a.n_parts, hgroups, batch), NW * 32, HY_SMEM, s>>>(a, qrec);
+  hy_decode_kernel<<<a.n_parts * hgroups * batch, NTHREADS, HY_SMEM, s>>>(a, qrec, batch);
   prof_stop(ctx, kProfDecode, s);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -362,20 +362,28 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
     per = (total_pages + 1215) / 1216;
     per = std::max<int64_t>(4, std::min<int64_t>(64, per));
   }
-  // The tcgen05 score path (decode_hy.cu): 3-bit keys, 2-bit values, m = d.  Its CTAs hold 256
-  // tensor-memory columns, two per SM, and walk their chunk in tiles of 8 pages; the chunks of a
-  // sequence are sized so that all chunks of a uniform batch (plus its ring items) fit in one wave
-  // of two CTAs per SM.
+  // The tcgen05 score path (decode_hy.cu): 3-bit keys, 2-bit values, m = d.  One 14-warp CTA per
+  // SM (it holds all 512 tensor-memory columns) walks its chunk in tiles of 8 pages.  The chunks
+  // per sequence and head group minimise waves x (tiles per chunk + 3), the 3 standing for the
+  // pipeline's fill and drain; ring items (short, launched after every chunk) are not counted.
   const bool hy_ok = pl.tensor_core && ctx->cfg.key_bits == 3 && ctx->cfg.value_bits == 2 && ctx->cfg.qjl_m == d;
-  // TQ_DECODE_AUTO keeps the mma.sync kernels: on GB300 they measured faster (88 against 125 us
-  // per launch at batch 8 x 32K, 28 / 4 heads).
   pl.hybrid = hy_ok && ctx->decode_path == TQ_DECODE_TCGEN05;
   if (pl.hybrid) {
     const int64_t bh = (int64_t)batch * hkv * groups;
-    const int64_t slots = 2 * (int64_t)std::max(1, ctx->sm_count);
-    const int64_t cps = std::max<int64_t>(1, (slots - bh) / std::max<int64_t>(1, bh));
-    per = (pages + cps - 1) / cps;
-    per = std::max<int64_t>(64, std::min<int64_t>(512, (per + 7) / 8 * 8));
+    const int64_t sms = std::max(1, ctx->sm_count);
+    int64_t best_cost = -1;
+    // beyond about two waves more chunks only add partials
+    const int64_t cmax = std::min<int64_t>(kMaxChunks, 2 * ((sms + bh - 1) / bh) + 2);
+    for (int64_t c = 1; c <= cmax; ++c) {
+      const int64_t per_c = ((pages + c - 1) / c + 7) / 8 * 8;
+      const int64_t chunks = (pages + per_c - 1) / per_c;
+      const int64_t cost = ((bh * chunks + sms - 1) / sms) * (per_c / 8 + 3);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        per = per_c;
+      }
+      if (per_c == 8) break;
+    }
   }
   // at most kMaxChunks chunks per sequence: the merge keeps one weight per part in shared memory
   per = std::max<int64_t>(per, (pages + kMaxChunks - 1) / kMaxChunks);
