@@ -37,11 +37,11 @@ __device__ __forceinline__ void wht_warp(float (&x)[E], int lane) {
 #pragma unroll
   for (int lb = 0; lb < 5; ++lb) {
     const int mask = lb == 0 ? 16 : (1 << (lb - 1));
-    const bool upper = lane & mask;
+    const float sgn = (lane & mask) ? -1.f : 1.f;  // upper half: p - x, lower half: x + p
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      float p = __shfl_xor_sync(kFull, x[e], mask);
-      x[e] = upper ? (p - x[e]) : (x[e] + p);
+      const float p = __shfl_xor_sync(kFull, x[e], mask);
+      x[e] = fmaf(sgn, x[e], p);
     }
   }
 #pragma unroll
@@ -81,32 +81,29 @@ struct GroupCode {
   int q;
 };
 // Minimum and maximum of each of the E groups of a warp-distributed vector (group e = element e
-// of every lane), for values exactly representable in fp16: two groups per half2 register and
-// the maximum of -v for the minimum, so the E minima and E maxima take E 5-step reductions
-// instead of 2E (exact: fp16 comparisons of fp16 values).
+// of every lane): one warp-wide float reduction each (redux.sync, exact).
 template <int E>
 __device__ __forceinline__ void group_minmax(const float (&v)[E], float (&mn)[E], float (&mx)[E]) {
-  constexpr int P = (E + 1) / 2;
-  __half2 hi[P], lo[P];
-#pragma unroll
-  for (int p = 0; p < P; ++p) {
-    const float a = v[2 * p], b = 2 * p + 1 < E ? v[2 * p + 1] : v[2 * p];
-    hi[p] = __floats2half2_rn(a, b);
-    lo[p] = __floats2half2_rn(-a, -b);
-  }
-#pragma unroll
-  for (int m = 16; m; m >>= 1)
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-      hi[p] = __hmax2(hi[p], __shfl_xor_sync(kFull, hi[p], m));
-      lo[p] = __hmax2(lo[p], __shfl_xor_sync(kFull, lo[p], m));
-    }
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    const int p = e >> 1;
-    mx[e] = (e & 1) ? __high2float(hi[p]) : __low2float(hi[p]);
-    mn[e] = -((e & 1) ? __high2float(lo[p]) : __low2float(lo[p]));
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx[e]) : "f"(v[e]));
+    asm("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(mn[e]) : "f"(v[e]));
   }
+}
+
+// rint of the IEEE quotient num / s (round half to even), with rs an approximate 1 / s: the
+// product num * rs decides, unless it lies within 2^-10 of a rounding boundary k + 1/2, where the
+// correctly rounded quotient is formed and rounded instead.  Exact for quotients below 2^12 (the
+// product's error is then far below 2^-10); the callers clamp larger ones to the top level.
+__device__ __forceinline__ float rint_quot(float num, float s, float rs) {
+  const float t = num * rs;
+  if (fabsf(t - floorf(t) - 0.5f) < 0.0009765625f) return rintf(__fdiv_rn(num, s));
+  return rintf(t);
+}
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
 }
 
 // As group_quant_lane, with the group's minimum and maximum already known.
@@ -117,7 +114,7 @@ __device__ __forceinline__ GroupCode group_quant_mm(float v, float mn, float mx,
   const float s = __half2float(g.s);
   int q = 0;
   if (s > 0.f) {
-    float t = rintf(__fdiv_rn(__fsub_rn(v, mn), s));
+    float t = rint_quot(__fsub_rn(v, mn), s, rcp_approx(s));
     t = fminf(fmaxf(t, 0.f), levels);
     q = (int)t;
   }
@@ -137,7 +134,7 @@ __device__ __forceinline__ GroupCode group_quant_signed(float v, float absmax, f
   const float mn = __half2float(g.mn);
   int q = 0;
   if (s > 0.f) {
-    float t = rintf(__fdiv_rn(__fsub_rn(v, mn), s));
+    float t = rint_quot(__fsub_rn(v, mn), s, rcp_approx(s));
     t = fminf(fmaxf(t, 0.f), levels);
     q = (int)t;
   }

@@ -88,12 +88,18 @@ __global__ void sketch_frag_enc_kernel(const float* __restrict__ s, int d, uint4
 // Main tile: key bit planes (kb - 1 Lloyd-Max index planes, high bit first, then the QJL plane;
 // turboquant vLLM guide, --key-bits 2, 3 or 4), VB-bit value codes (--value-bits 2 or 4), the
 // group scale / minimum, the two norm rows.  Staging in shared memory is sized for kb = 4.
-template <int D, int VB>
+// Tokens per CTA for long encodes: 64 at d <= 256 (about 50 KB of shared memory at d = 128, 4 CTAs
+// per SM; 128 tokens per CTA fit only 2 per SM and encoded 21% fewer tokens per second), 32 at d = 512.
+// Short encodes (a 128-token flush) use 16 tokens per CTA: 8 times the CTAs, a quarter of the
+// tokens per warp, for latency.
+template <int D>
+constexpr int main_tb_long() { return D <= 256 ? 64 : 32; }
+constexpr int kMainTbShort = 16;
+
+template <int D, int VB, int TB_ = main_tb_long<D>()>
 struct MainEnc {
   static constexpr int E = D / 32;
-  // tokens per CTA: 64 at d <= 128 (about 50 KB of shared memory, 4 CTAs per SM; 128 tokens per CTA
-  // fit only 2 per SM and encoded 21% fewer tokens per second), fewer for larger d
-  static constexpr int TB = D <= 128 ? 64 : (D == 256 ? 64 : 32);
+  static constexpr int TB = TB_;
   static constexpr int TILE = (10 + 2 * VB) * D + 64;  // largest tile (kb = 4): staging stride
   static constexpr int THREADS = 256;
   static constexpr int RS = D + 8;                     // residual row stride (halves): conflict-free fragments
@@ -120,9 +126,9 @@ __device__ void store_tiles(const EncArgs& a, const uint8_t* tiles, int stride, 
   }
 }
 
-template <int D, int VB, int KB>
+template <int D, int VB, int KB, int TB_>
 __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int ntok, int start, uint8_t* smem) {
-  using C = MainEnc<D, VB>;
+  using C = MainEnc<D, VB, TB_>;
   constexpr int E = C::E;
   constexpr int TB = C::TB;
   __half* rh = reinterpret_cast<__half*>(smem);                 // [TB][RS] residual, fp16 high part
@@ -475,12 +481,32 @@ __device__ void encode_alt_block(const EncArgs& a, int b, int h, int tok0, int n
 }
 
 // ------------------------------------------------------------------ kernels
-// VB: value bits of the main layout (2 or 4), 0 for the alternate layout.
+// VB: value bits of the main layout (2 or 4), 0 for the alternate layout; TB: tokens per CTA of
+// the main layout (the alternate layout's are fixed).
 template <int D, int VB>
+constexpr int enc_tb(bool short_run) {
+  return VB ? (short_run ? kMainTbShort : main_tb_long<D>()) : AltEnc<D>::TB;
+}
+
+template <int D, int VB, int TB>
+__device__ __forceinline__ void encode_block(const EncArgs& a, int b, int h, int tok0, int ntok, int start,
+                                             uint8_t* smem) {
+  if constexpr (VB == 0) {
+    encode_alt_block<D>(a, b, h, tok0, ntok, start, smem);
+  } else {
+    if (a.kb == 3)
+      encode_main_block<D, VB, 3, TB>(a, b, h, tok0, ntok, start, smem);
+    else if (a.kb == 2)
+      encode_main_block<D, VB, 2, TB>(a, b, h, tok0, ntok, start, smem);
+    else
+      encode_main_block<D, VB, 4, TB>(a, b, h, tok0, ntok, start, smem);
+  }
+}
+
+template <int D, int VB, int TB>
 __global__ void __launch_bounds__(256) encode_kernel(EncArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int b = blockIdx.z, h = blockIdx.y;
-  constexpr int TB = VB ? MainEnc<D, (VB ? VB : 2)>::TB : AltEnc<D>::TB;
   const int tok0 = blockIdx.x * TB;
   const int ntok = min(TB, a.n_tokens - tok0);
   const int start = a.start_pos[b];
@@ -488,14 +514,7 @@ __global__ void __launch_bounds__(256) encode_kernel(EncArgs a) {
     if (threadIdx.x == 0) flag_error(a.err, TQ_DEVERR_POSITION);
     return;
   }
-  if (!VB)
-    encode_alt_block<D>(a, b, h, tok0, ntok, start, smem);
-  else if (a.kb == 3)
-    encode_main_block<D, (VB ? VB : 2), 3>(a, b, h, tok0, ntok, start, smem);
-  else if (a.kb == 2)
-    encode_main_block<D, (VB ? VB : 2), 2>(a, b, h, tok0, ntok, start, smem);
-  else
-    encode_main_block<D, (VB ? VB : 2), 4>(a, b, h, tok0, ntok, start, smem);
+  encode_block<D, VB, TB>(a, b, h, tok0, ntok, start, smem);
 }
 
 struct AppendArgs {
@@ -507,32 +526,22 @@ struct AppendArgs {
   __half* ring_v;
 };
 
-template <int D, int VB>
+// One CTA per (KV head, sequence, TB-token slice of the ring).  When the ring is full (pos a
+// nonzero multiple of 128) each slice compresses its tokens; the new token then goes to ring
+// slot pos mod 128, written by the slice that holds that slot, after its own tokens were read.
+template <int D, int VB, int TB>
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  const int b = blockIdx.y, h = blockIdx.x;
+  const int b = blockIdx.y, h = blockIdx.x, t0 = blockIdx.z * TB;
+  static_assert(kRing % TB == 0, "ring flush is a whole number of encode batches");
   const int pos = a.pos[b];
   if (pos < 0) {
-    if (threadIdx.x == 0) flag_error(a.enc.err, TQ_DEVERR_POSITION);
+    if (threadIdx.x == 0 && blockIdx.z == 0) flag_error(a.enc.err, TQ_DEVERR_POSITION);
     return;
   }
-  if (pos > 0 && (pos % kRing) == 0) {
-    const int start = pos - kRing;
-    constexpr int TB = VB ? MainEnc<D, (VB ? VB : 2)>::TB : AltEnc<D>::TB;
-    static_assert(kRing % TB == 0, "ring flush is a whole number of encode batches");
-    for (int t0 = 0; t0 < kRing; t0 += TB) {
-      if (VB && a.enc.kb == 3)
-        encode_main_block<D, (VB ? VB : 2), 3>(a.enc, b, h, t0, TB, start, smem);
-      else if (VB && a.enc.kb == 2)
-        encode_main_block<D, (VB ? VB : 2), 2>(a.enc, b, h, t0, TB, start, smem);
-      else if (VB)
-        encode_main_block<D, (VB ? VB : 2), 4>(a.enc, b, h, t0, TB, start, smem);
-      else
-        encode_alt_block<D>(a.enc, b, h, t0, TB, start, smem);
-      __syncthreads();
-    }
-  }
   const int slot = pos % kRing;
+  if (pos > 0 && slot == 0) encode_block<D, VB, TB>(a.enc, b, h, t0, TB, pos - kRing, smem);
+  if (slot < t0 || slot >= t0 + TB) return;
   const size_t src = ((size_t)b * a.enc.hkv + h) * D;
   const size_t dst = (((size_t)b * a.enc.hkv + h) * kRing + slot) * D;
   for (int i = threadIdx.x; i < D / 8; i += blockDim.x) {
@@ -543,31 +552,44 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
 
 // Dynamic shared memory of one launch: the main layout's fixed staging, or the alternate layout's
 // for its key and value widths (the function attribute allows the largest).
-template <int D, int VB>
+template <int D, int VB, int TB>
 size_t enc_smem(const EncArgs& a) {
-  return VB ? MainEnc<D, (VB ? VB : 2)>::SMEM : AltEnc<D>::smem(a.kb, a.avb);
+  if constexpr (VB == 0) return AltEnc<D>::smem(a.kb, a.avb);
+  else return MainEnc<D, VB, TB>::SMEM;
+}
+template <int D, int VB, int TB>
+constexpr size_t enc_smem_max() {
+  if constexpr (VB == 0) return AltEnc<D>::SMEM;
+  else return MainEnc<D, VB, TB>::SMEM;
 }
 
-template <int D, int VB>
-cudaError_t launch_encode_t(const EncArgs& a, int batch, cudaStream_t s) {
-  constexpr int TB = VB ? MainEnc<D, (VB ? VB : 2)>::TB : AltEnc<D>::TB;
-  constexpr size_t SMEM_MAX = VB ? MainEnc<D, (VB ? VB : 2)>::SMEM : AltEnc<D>::SMEM;
-  auto kern = encode_kernel<D, VB>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
+template <int D, int VB, int TB>
+cudaError_t launch_encode_tb(const EncArgs& a, int batch, cudaStream_t s) {
+  auto kern = encode_kernel<D, VB, TB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)enc_smem_max<D, VB, TB>());
   if (e != cudaSuccess) return e;
   dim3 grid((a.n_tokens + TB - 1) / TB, a.hkv, batch);
-  kern<<<grid, 256, enc_smem<D, VB>(a), s>>>(a);
+  kern<<<grid, 256, enc_smem<D, VB, TB>(a), s>>>(a);
   return cudaGetLastError();
+}
+
+// Short encodes (fewer CTAs of the long size than two per SM) take the short CTAs.
+template <int D, int VB>
+cudaError_t launch_encode_t(const EncArgs& a, int batch, int sm_count, cudaStream_t s) {
+  constexpr int TL = enc_tb<D, VB>(false);
+  const int64_t ctas = (int64_t)((a.n_tokens + TL - 1) / TL) * a.hkv * batch;
+  if (VB && ctas < 2 * (int64_t)sm_count) return launch_encode_tb<D, VB, enc_tb<D, VB>(true)>(a, batch, s);
+  return launch_encode_tb<D, VB, TL>(a, batch, s);
 }
 
 template <int D, int VB>
 cudaError_t launch_append_t(const AppendArgs& a, int batch, cudaStream_t s) {
-  constexpr size_t SMEM_MAX = VB ? MainEnc<D, (VB ? VB : 2)>::SMEM : AltEnc<D>::SMEM;
-  auto kern = append_kernel<D, VB>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
+  constexpr int TB = enc_tb<D, VB>(true);
+  auto kern = append_kernel<D, VB, TB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)enc_smem_max<D, VB, TB>());
   if (e != cudaSuccess) return e;
-  dim3 grid(a.enc.hkv, batch);
-  kern<<<grid, 256, enc_smem<D, VB>(a.enc), s>>>(a);
+  dim3 grid(a.enc.hkv, batch, kRing / TB);
+  kern<<<grid, 256, enc_smem<D, VB, TB>(a.enc), s>>>(a);
   return cudaGetLastError();
 }
 
@@ -605,10 +627,10 @@ cudaError_t launch_encode(tq_ctx* ctx, const void* k, const void* v, int batch, 
   cudaError_t e = cudaErrorInvalidValue;
   prof_start(ctx, kProfEncode, s);
   switch (ctx->cfg.head_dim) {
-    case 64: e = vb == 4 ? launch_encode_t<64, 4>(a, batch, s) : vb == 2 ? launch_encode_t<64, 2>(a, batch, s) : launch_encode_t<64, 0>(a, batch, s); break;
-    case 128: e = vb == 4 ? launch_encode_t<128, 4>(a, batch, s) : vb == 2 ? launch_encode_t<128, 2>(a, batch, s) : launch_encode_t<128, 0>(a, batch, s); break;
-    case 256: e = vb == 4 ? launch_encode_t<256, 4>(a, batch, s) : vb == 2 ? launch_encode_t<256, 2>(a, batch, s) : launch_encode_t<256, 0>(a, batch, s); break;
-    case 512: e = vb == 4 ? launch_encode_t<512, 4>(a, batch, s) : vb == 2 ? launch_encode_t<512, 2>(a, batch, s) : launch_encode_t<512, 0>(a, batch, s); break;
+    case 64: e = vb == 4 ? launch_encode_t<64, 4>(a, batch, ctx->sm_count, s) : vb == 2 ? launch_encode_t<64, 2>(a, batch, ctx->sm_count, s) : launch_encode_t<64, 0>(a, batch, ctx->sm_count, s); break;
+    case 128: e = vb == 4 ? launch_encode_t<128, 4>(a, batch, ctx->sm_count, s) : vb == 2 ? launch_encode_t<128, 2>(a, batch, ctx->sm_count, s) : launch_encode_t<128, 0>(a, batch, ctx->sm_count, s); break;
+    case 256: e = vb == 4 ? launch_encode_t<256, 4>(a, batch, ctx->sm_count, s) : vb == 2 ? launch_encode_t<256, 2>(a, batch, ctx->sm_count, s) : launch_encode_t<256, 0>(a, batch, ctx->sm_count, s); break;
+    case 512: e = vb == 4 ? launch_encode_t<512, 4>(a, batch, ctx->sm_count, s) : vb == 2 ? launch_encode_t<512, 2>(a, batch, ctx->sm_count, s) : launch_encode_t<512, 0>(a, batch, ctx->sm_count, s); break;
   }
   prof_stop(ctx, kProfEncode, s);
   if (e == cudaSuccess) ctx->launches++;
