@@ -24,6 +24,7 @@
 
 namespace tq {
 
+bool alt_v2_supported(const tq_ctx* ctx);
 cudaError_t launch_decode_alt_v2(tq_ctx* ctx, const void* q, const void* pool, int num_blocks,
                                  const int32_t* block_table, int max_blocks, const int32_t* n_compressed, int max_ctx,
                                  float* parts, int chunk_tokens, int n_chunks, int n_parts, int batch, cudaStream_t s);
@@ -767,7 +768,7 @@ cudaError_t launch_decode(tq_ctx* ctx, const DecodePlan& plan, const void* q, in
   a.first_part = 0;
   dim3 grid(plan.n_parts, a.hkv * a.groups, batch);
   bool done = false;
-  if (!main) {
+  if (!main && alt_v2_supported(ctx)) {
     // compressed chunks: warp-per-page kernel; the exact buffer (if any): the part kernel below
     ctx->decode_kernel = "decode_alt_v2_kernel";
     prof_start(ctx, kProfDecode, s);

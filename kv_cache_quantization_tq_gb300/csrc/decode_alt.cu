@@ -52,6 +52,8 @@ struct AltArgs {
   int hq, hkv, n_rep, nrg, groups;
   const float* signs;
   CodeTables tab;
+  int vb;              // value bits (read by the 5- to 8-bit instance)
+  const float* vcent;  // the 2^vb value centroids (device)
   uint32_t* err;
 };
 
@@ -146,15 +148,20 @@ struct KeyEntry {
   static constexpr float kScale = kBiased ? 1.f : (float)(1 << KB);
 };
 
-template <int D, int NR, int VB, int KB>
+// VBT: the value bits (2, 3 or 4), or 0 for 5- to 8-bit values read from the arguments (one
+// instance for the four widths: the stages are sized for 8 bits, the centroid table holds 256).
+template <int D, int NR, int VBT, int KB>
 __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
   static_assert(KB == 16 || KB == 8 || KB == 5 || KB == 4 || KB == 2, "key widths");
-  using C = AltCfg<D, VB, KB>;
-  constexpr int NC = 1 << VB;  // centroids
+  using C = AltCfg<D, VBT ? VBT : 8, KB>;  // staging for the widest values of the instance
+  constexpr int NCMAX = 1 << (VBT ? VBT : 8);
+  const int VB = VBT ? VBT : a.vb;
+  const int tile = VBT ? C::TILE : alt_tile_bytes(D, KB, VB);  // bytes of a page in the pool
+  const uint32_t vmask = (1u << VB) - 1u;
   constexpr int E = C::E;
   constexpr int G = D / 32;
   extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ float lut[NC];
+  __shared__ float lut[NCMAX];
   __shared__ float wm[kWarps][NR], wl[kWarps][NR];
   __shared__ float wo[kWarps][NR][D];
   __shared__ int sblk[kWarps][C::STAGES];
@@ -172,10 +179,12 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
   const int tbeg = part * a.chunk_tokens;
   const int tend = min(nc, tbeg + a.chunk_tokens);
   if (tbeg >= tend) return;
-  if (tid < NC) {
+  if (VBT == 0) {
+    for (int i = tid; i < (1 << VB); i += blockDim.x) lut[i] = __ldg(a.vcent + i);
+  } else if (tid < NCMAX) {
     float c = a.tab.c[0];
 #pragma unroll
-    for (int j = 1; j < NC; ++j) c = tid == j ? a.tab.c[j] : c;
+    for (int j = 1; j < NCMAX; ++j) c = tid == j ? a.tab.c[j] : c;
     lut[tid] = c;
   }
 
@@ -234,9 +243,9 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
     if (k < nw) {
       if (lane == 0) sblk[warp][k % C::STAGES] = blk;
       if (blk >= 0 && blk < a.num_blocks) {
-        const uint8_t* src = a.pool + ((size_t)blk * a.hkv + kvh) * C::TILE;
+        const uint8_t* src = a.pool + ((size_t)blk * a.hkv + kvh) * tile;
         uint8_t* dst = wst + (k % C::STAGES) * C::TILE;
-        for (int c = lane; c < C::TILE / 16; c += 32) {
+        for (int c = lane; c < tile / 16; c += 32) {
           int cd = c;
           if ((KB == 8 || KB == 4 || KB == 2) && c < KB * D / 8) {  // key rows: 16 x KB D / 128 chunks
             constexpr int NCH = KB * D / 128 > 0 ? KB * D / 128 : 1;
@@ -384,21 +393,23 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
       for (int e = 0; e < E; ++e) acc[h][e] *= alpha;
       const float w = p * __half2float(vn[lane >> 1]);
       // v_rot += w_t c[idx_t] for the lane's E dimensions: VB E bits at bit VB E lane of the token's
-      // index stream, read in pieces of up to 8 indices (at most 32 bits, one funnel shift each)
+      // index stream, read in pieces of up to 8 indices of up to 4 bits or 4 wider ones (at most 32
+      // bits, one funnel shift each)
 #pragma unroll
       for (int t = 0; t < 16; ++t) {
         const float wt = __shfl_sync(kFull, w, 2 * t);
         const uint32_t* row = vi + t * (VB * D / 32);
+        constexpr int PMAX = VBT != 0 ? 8 : 4;
+        constexpr int PIECE = E < PMAX ? E : PMAX;
 #pragma unroll
-        for (int c0 = 0; c0 < E; c0 += 8) {
-          constexpr int PIECE = E < 8 ? E : 8;
+        for (int c0 = 0; c0 < E; c0 += PIECE) {
           const int bitc = VB * (E * lane + c0);
           const uint32_t lo = row[bitc >> 5];
           const uint32_t hi = ((bitc & 31) + VB * PIECE > 32) ? row[(bitc >> 5) + 1] : 0u;
           const uint32_t bits = __funnelshift_r(lo, hi, bitc & 31);
 #pragma unroll
           for (int e = 0; e < PIECE; ++e)
-            acc[h][c0 + e] = fmaf(wt, lut[(bits >> (VB * e)) & (NC - 1)], acc[h][c0 + e]);
+            acc[h][c0 + e] = fmaf(wt, lut[(bits >> (VB * e)) & vmask], acc[h][c0 + e]);
         }
       }
     }
@@ -454,15 +465,21 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
 template <int D, int NR, int VB, int KB>
 cudaError_t launch_alt_vb(const AltArgs& a, dim3 grid, cudaStream_t s) {
   auto kern = decode_alt_v2_kernel<D, NR, VB, KB>;
-  constexpr size_t SMEM = AltCfg<D, VB, KB>::SMEM;
+  constexpr size_t SMEM = AltCfg<D, VB ? VB : 8, KB>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, 128, SMEM, s>>>(a);
   return cudaGetLastError();
 }
 
+// 5- to 8-bit values (q5_0 .. q8_0) only with 8-bit or fp16 keys; other pairs take the CUDA-core
+// decoder.
 template <int D, int NR, int KB>
 cudaError_t launch_alt_kb(const AltArgs& a, int vb, dim3 grid, cudaStream_t s) {
+  if (vb > 4) {
+    if constexpr (KB == 8 || KB == 16) return launch_alt_vb<D, NR, 0, KB>(a, grid, s);
+    return cudaErrorNotSupported;
+  }
   return vb == 2 ? launch_alt_vb<D, NR, 2, KB>(a, grid, s)
        : vb == 4 ? launch_alt_vb<D, NR, 4, KB>(a, grid, s)
                  : launch_alt_vb<D, NR, 3, KB>(a, grid, s);
@@ -480,6 +497,19 @@ cudaError_t launch_alt(const AltArgs& a, int vb, int kb, dim3 grid, cudaStream_t
 }
 
 }  // namespace
+
+// Whether the warp-per-page kernel has an instance for the context: up to 4 query heads per KV-head
+// group (4 at d <= 128, 2 at d <= 256, 1 at d = 512), value bits 2..4, or 5..8 beside 8-bit or
+// fp16 keys.
+bool alt_v2_supported(const tq_ctx* ctx) {
+  const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
+  const int groups = (ctx->n_rep + kMaxRep - 1) / kMaxRep, nr = ctx->n_rep / groups;
+  const bool heads = nr == 1 ? (d == 64 || d == 128 || d == 256 || d == 512)
+                   : nr == 2 ? (d == 64 || d == 128 || d == 256)
+                   : nr <= 4 && (d == 64 || d == 128);
+  const bool widths = vb <= 4 || ((kb == 8 || kb == 16) && ctx->d_vcent);
+  return heads && widths;
+}
 
 // Compressed parts of the alternate layout with the warp-per-page kernel, when it
 // supports (d, heads per group); returns cudaErrorNotSupported otherwise.
@@ -505,10 +535,12 @@ cudaError_t launch_decode_alt_v2(tq_ctx* ctx, const void* q, const void* pool, i
   a.nrg = ctx->n_rep / a.groups;
   a.signs = ctx->d_signs;
   a.tab = ctx->tab;
+  a.vb = ctx->cfg.value_bits;
+  a.vcent = ctx->d_vcent;
   a.err = ctx->d_err;
   dim3 grid(n_chunks, a.hkv * a.groups, batch);
   const int d = ctx->cfg.head_dim, nr = a.nrg, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
-  if (vb > 4) return cudaErrorNotSupported;  // 5- to 8-bit values: the CUDA-core decoder (device codebook)
+  if (!alt_v2_supported(ctx)) return cudaErrorNotSupported;
   if (nr == 1) {
     switch (d) {
       case 64: return launch_alt<64, 1>(a, vb, kb, grid, s);

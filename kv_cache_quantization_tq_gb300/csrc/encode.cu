@@ -194,19 +194,30 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
     for (int e = 0; e < E; ++e) {
       const float y = x[e] * inv;
       // #{boundaries <= y} over the 2^(kb-1) - 1 boundaries (straight-line code per key width)
-      int idx;
+      // #{boundaries <= y}: the comparisons with the ascending boundaries form a thermometer code
+      // n_0 >= n_1 >= ..., so the index bits are XORs of comparisons (bit 1 of a 2-bit index is
+      // n_1, bit 0 the parity of all three) and the centroid is a chain of selects (a NaN y
+      // compares false everywhere: index 0, as with the count)
+      bool ib0, ib1 = false, ib2 = false;  // index bits
       float cy;
       if (KB == 3) {
-        idx = (y >= a.tab.b[0]) + (y >= a.tab.b[1]) + (y >= a.tab.b[2]);
-        cy = sel4(a.tab, idx);
+        const bool n0 = y >= a.tab.b[0], n1 = y >= a.tab.b[1], n2 = y >= a.tab.b[2];
+        ib1 = n1;
+        ib0 = n0 ^ n1 ^ n2;
+        cy = n2 ? a.tab.c[3] : n1 ? a.tab.c[2] : n0 ? a.tab.c[1] : a.tab.c[0];
       } else if (KB == 2) {
-        idx = y >= a.tab.b[0];
-        cy = idx ? a.tab.c[1] : a.tab.c[0];
+        ib0 = y >= a.tab.b[0];
+        cy = ib0 ? a.tab.c[1] : a.tab.c[0];
       } else {
-        idx = 0;
+        bool n[7];
 #pragma unroll
-        for (int j = 0; j < 7; ++j) idx += y >= a.tab.b[j];
-        cy = sel8(a.tab, idx);
+        for (int j = 0; j < 7; ++j) n[j] = y >= a.tab.b[j];
+        ib2 = n[3];
+        ib1 = n[1] ^ n[3] ^ n[5];
+        ib0 = n[0] ^ n[1] ^ n[2] ^ n[3] ^ n[4] ^ n[5] ^ n[6];
+        cy = a.tab.c[0];
+#pragma unroll
+        for (int j = 0; j < 7; ++j) cy = n[j] ? a.tab.c[j + 1] : cy;
       }
       const float r = y - cy;
       rr = fmaf(r, r, rr);
@@ -216,19 +227,19 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
       // index planes, high bit first
       uint32_t* kp0 = reinterpret_cast<uint32_t*>(tile + slot * (D / 8)) + e;
       if (KB == 3) {
-        const unsigned hi = __ballot_sync(kFull, idx >> 1);
-        const unsigned lo = __ballot_sync(kFull, idx & 1);
+        const unsigned hi = __ballot_sync(kFull, ib1);
+        const unsigned lo = __ballot_sync(kFull, ib0);
         if (lane == 0) {
           kp0[0] = hi;
           kp0[2 * D / 4] = lo;
         }
       } else if (KB == 2) {
-        const unsigned bits = __ballot_sync(kFull, idx);
+        const unsigned bits = __ballot_sync(kFull, ib0);
         if (lane == 0) kp0[0] = bits;
       } else {
-        const unsigned b2 = __ballot_sync(kFull, idx >> 2);
-        const unsigned b1 = __ballot_sync(kFull, (idx >> 1) & 1);
-        const unsigned b0 = __ballot_sync(kFull, idx & 1);
+        const unsigned b2 = __ballot_sync(kFull, ib2);
+        const unsigned b1 = __ballot_sync(kFull, ib1);
+        const unsigned b0 = __ballot_sync(kFull, ib0);
         if (lane == 0) {
           kp0[0] = b2;
           kp0[2 * D / 4] = b1;

@@ -71,23 +71,47 @@ def test_encode_parity(d, vb):
         assert fg["vidx"].max() >= 1 << (vb - 1)
 
 
-@pytest.mark.parametrize("vb", [2, 4, 5, 8])
-@pytest.mark.parametrize("d,n_rep", [(64, 1), (128, 2), (128, 4), (256, 1), (512, 1), (128, 8)])
-def test_decode_parity(d, n_rep, vb):
-    seed, hkv = 70 + d + n_rep + vb, 2
+def _decode_case(d, n_rep, vb, kb, seed, lengths=(544, 96)):
+    hkv = 2
     hq = hkv * n_rep
-    ctx, c, s, _ = make_ctx(tq, False, d, hq, hkv, seed, value_bits=vb)
-    e = build_alt_cache(seed, d, hkv, [544, 96], c, s)
-    q = synth.queries(seed, 2, hq, d)
-    out = torch.empty((2, hq, d), dtype=torch.float32, device="cuda")
-    ws = torch.empty(ctx.workspace_size(2, e["max_ctx"]), dtype=torch.uint8, device="cuda")
+    ctx, c, s, _ = make_ctx(tq, False, d, hq, hkv, seed, value_bits=vb, key_bits=kb)
+    e = build_alt_cache(seed, d, hkv, list(lengths), c, s, key_bits=kb)
+    q = synth.queries(seed, len(lengths), hq, d)
+    out = torch.empty((len(lengths), hq, d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(ctx.workspace_size(len(lengths), e["max_ctx"]), dtype=torch.uint8, device="cuda")
+    ctx.profile_begin()
     ctx.decode_attention(to_dev(q), to_dev(e["pool"]), to_dev(e["bt"]), to_dev(e["n_c"]), None, None, None,
                          e["max_ctx"], out, ws)
+    kernel = ctx.profile_end()["decode_kernel"]
     got = out.cpu().numpy()
     assert ctx.device_errors() == 0
     ref = attention.decode_alt(q, e["pool"], e["bt"], e["n_c"], None, None, None, s, c, hkv)
     ok, maxerr, nbad = allclose_report(got, ref)
     assert ok, f"max abs err {maxerr}, {nbad} bad"
+    return kernel
+
+
+@pytest.mark.parametrize("vb", [2, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("d,n_rep", [(64, 1), (128, 2), (128, 4), (256, 1), (512, 1), (128, 8)])
+def test_decode_parity(d, n_rep, vb):
+    kernel = _decode_case(d, n_rep, vb, 8, 70 + d + n_rep + vb)
+    # up to 4 query heads per KV head (8-bit keys): the warp-per-page tensor-core decoder at every width
+    assert kernel == ("decode_alt_v2_kernel" if n_rep <= 4 else "decode_alt_kernel"), kernel
+
+
+@pytest.mark.parametrize("vb", [5, 8])
+@pytest.mark.parametrize("d,n_rep", [(64, 2), (128, 1), (512, 1)])
+def test_decode_parity_wide_values_fp16_keys(d, n_rep, vb):
+    """q5_0 / q8_0 values beside fp16 keys (the V-only cache with wide values), ragged lengths with a
+    partial last chunk."""
+    kernel = _decode_case(d, n_rep, vb, 16, 170 + d + n_rep + vb, lengths=(1040, 16, 400))
+    assert kernel == "decode_alt_v2_kernel", kernel
+
+
+def test_decode_wide_values_low_bit_keys_use_the_cuda_core_decoder():
+    """5- to 8-bit values with 2-, 4- or 5-bit keys: no tensor-core instance, same results."""
+    kernel = _decode_case(128, 2, 6, 4, 311)
+    assert kernel == "decode_alt_kernel", kernel
 
 
 @pytest.mark.parametrize("vb", [2, 4, 6, 8])
