@@ -101,3 +101,25 @@ def test_decode_path_rejects_unknown_value():
     ctx, c, s, sk = make_ctx(tq, True, d, 4, 1, seed)
     with pytest.raises(tq.TQError):
         ctx.set_decode_path(7)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_consecutive_calls_on_one_context(path):
+    """Calls of different batch sizes and split-K plans back to back on one context (a one-wave
+    plan, a single sequence, a four-sequence batch, a plan sized for 128K tokens, then the first
+    call again), each checked against the oracle: no state of one call may leak into the next."""
+    d, hkv, n_rep, seed = 128, 2, 4, 61
+    hq = hkv * n_rep
+    ctx, c, s, sk = make_ctx(tq, True, d, hq, hkv, seed)
+    ctx.set_decode_path(path)
+    cases = [([2000, 700, 5], None), ([300], None), ([4096, 4096, 1200, 33], None), ([1500, 20], 1 << 17),
+             ([2000, 700, 5], None)]
+    for k, (lengths, max_ctx) in enumerate(cases):
+        e = build_main_cache(seed + k, d, hkv, lengths, c, s, sk)
+        q = synth.queries(seed + k, len(lengths), hq, d)
+        got = _decode(ctx, e, q, hq, d, max_ctx)
+        assert ctx.device_errors() == 0
+        ref = attention.decode_main(q, e["pool"], e["bt"], e["n_c"], e["ring_k"], e["ring_v"], e["n_b"], s, c, sk,
+                                    hkv)
+        ok, maxerr, nbad = allclose_report(got, ref)
+        assert ok, f"call {k} ({lengths}): max abs err {maxerr}, {nbad} bad"
