@@ -25,9 +25,13 @@
 // a logit exceeds it by more than 2^kLazyLog2); every warp's value accumulators share it, so the
 // warps' results add without reweighting.
 //
-// Work split and merge: the chunks / ring item / split-K partials of decode_tc.cu; the ring item
-// runs the mma.sync path of decode_tc.cu.  Every wait on an mbarrier is bounded (about a second):
-// on expiry the CTA flags TQ_DEVERR_TIMEOUT, drains its copies, frees its tensor memory and leaves.
+// CTA: one per SM with all 512 tensor-memory columns, its warps in roles joined by mbarriers (a
+// page-copy lane, 4 score warps, an MMA-issue lane, 8 value warps; see hy_decode_kernel).
+// Work split and merge: the chunks / ring item / split-K partials of decode_tc.cu, in a
+// one-dimensional grid with the ring items last; the ring item runs the mma.sync path of
+// decode_tc.cu on every warp.  Every wait on an mbarrier is bounded (about a second): on expiry the
+// CTA flags TQ_DEVERR_TIMEOUT, waits for its own copies and MMAs, frees its tensor memory and
+// leaves.
 #include <cuda_fp8.h>
 
 #include "tc_mma.cuh"
