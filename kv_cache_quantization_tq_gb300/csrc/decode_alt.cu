@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
   __shared__ float wo[kWarps][NR][D];
   __shared__ int sblk[kWarps][C::STAGES];
   __shared__ float qsum_s[NR * G];
+  __shared__ __align__(16) float wbuf[kWarps][16];  // this warp's token weights of the current head
 
   const int part = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int kvh = hg / a.groups;
@@ -392,12 +393,30 @@ __global__ void __launch_bounds__(128) decode_alt_v2_kernel(AltArgs a) {
 #pragma unroll
       for (int e = 0; e < E; ++e) acc[h][e] *= alpha;
       const float w = p * __half2float(vn[lane >> 1]);
+      // the 16 token weights to every lane: at d <= 128 stored once (even lanes) and read back as
+      // four broadcast 16-byte loads (measured: +3% at d = 64, no change at 128); at larger d by
+      // one shuffle per token (the staged form measured 2% slower at d = 512)
+      constexpr bool kStagedW = E <= 4;
+      float wts[16];
+      if constexpr (kStagedW) {
+        if ((lane & 1) == 0) wbuf[warp][lane >> 1] = w;
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 w4 = reinterpret_cast<const float4*>(wbuf[warp])[k];
+          wts[4 * k] = w4.x;
+          wts[4 * k + 1] = w4.y;
+          wts[4 * k + 2] = w4.z;
+          wts[4 * k + 3] = w4.w;
+        }
+        __syncwarp();  // every lane has the weights before the next head overwrites them
+      }
       // v_rot += w_t c[idx_t] for the lane's E dimensions: VB E bits at bit VB E lane of the token's
       // index stream, read in pieces of up to 8 indices of up to 4 bits or 4 wider ones (at most 32
       // bits, one funnel shift each)
 #pragma unroll
       for (int t = 0; t < 16; ++t) {
-        const float wt = __shfl_sync(kFull, w, 2 * t);
+        const float wt = kStagedW ? wts[t] : __shfl_sync(kFull, w, 2 * t);
         const uint32_t* row = vi + t * (VB * D / 32);
         constexpr int PMAX = VBT != 0 ? 8 : 4;
         constexpr int PIECE = E < PMAX ? E : PMAX;
