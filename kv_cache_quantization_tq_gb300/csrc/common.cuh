@@ -73,13 +73,6 @@ __device__ __forceinline__ float warp_min(float v) {
   return v;
 }
 
-// Asymmetric min/max quantiser of one group held as one value per lane
-// (IEEE float32 arithmetic, no contraction): s = fp16((mx - mn) / levels),
-// q = clamp(rint((v - mn) / s), 0, levels), q = 0 when s == 0.
-struct GroupCode {
-  __half s, mn;
-  int q;
-};
 // Minimum and maximum of each of the E groups of a warp-distributed vector (group e = element e
 // of every lane): one warp-wide float reduction each (redux.sync, exact).
 template <int E>
@@ -106,44 +99,49 @@ __device__ __forceinline__ float rcp_approx(float s) {
   return r;
 }
 
-// As group_quant_lane, with the group's minimum and maximum already known.
-__device__ __forceinline__ GroupCode group_quant_mm(float v, float mn, float mx, float levels) {
-  GroupCode g;
-  g.s = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), levels));
-  g.mn = __float2half_rn(mn);
-  const float s = __half2float(g.s);
+// Group quantisers of a warp-distributed vector (group e = element e of every lane), IEEE float32
+// arithmetic without contraction, the (scale, minimum) of each group stored as fp16:
+//   asymmetric min/max:      s = fp16((mx - mn) / levels),            mn = fp16(mn)
+//   signed symmetric:        s = fp16(max |x| / (levels / 2)),         mn = fp16(-(levels / 2) s)
+//   q = clamp(rint((v - mn) / s), 0, levels), q = 0 when s == 0 (v and mn are fp16 values, so the
+//   asymmetric mn is exact in either precision).
+// Each group's pair is formed once, by lane e for group e (one IEEE division per lane instead of
+// E), and one shuffle per group hands it to the warp; `mine` is lane e's own pair (lanes >= E:
+// group 0's), for the store.
+template <int E, bool SIGNED>
+__device__ __forceinline__ void group_pairs(const float (&mn)[E], const float (&mx)[E], float levels, int lane,
+                                            __half2 (&sm)[E], __half2& mine) {
+  static_assert(E <= 32, "one lane per group");
+  float lo = mn[0], hi = mx[0];
+#pragma unroll
+  for (int e = 1; e < E; ++e)
+    if (lane == e) {
+      lo = mn[e];
+      hi = mx[e];
+    }
+  __half s, m;
+  if (SIGNED) {
+    const float half = 0.5f * levels;
+    s = __float2half_rn(__fdiv_rn(fmaxf(-lo, hi), half));
+    m = __float2half_rn(__fmul_rn(-half, __half2float(s)));
+  } else {
+    s = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), levels));
+    m = __float2half_rn(lo);
+  }
+  mine = __halves2half2(s, m);
+#pragma unroll
+  for (int e = 0; e < E; ++e) sm[e] = __shfl_sync(kFull, mine, e);
+}
+// The code of v in the group with the fp16 pair (s, mn).
+__device__ __forceinline__ int group_code(float v, __half2 sm, float levels) {
+  const float s = __low2float(sm), mn = __high2float(sm);
   int q = 0;
   if (s > 0.f) {
     float t = rint_quot(__fsub_rn(v, mn), s, rcp_approx(s));
     t = fminf(fmaxf(t, 0.f), levels);
     q = (int)t;
   }
-  g.q = q;
-  return g;
-}
-
-// Signed symmetric mid-rise quantiser of a block with the given max |x| (IEEE float32, no
-// contraction): s = fp16(absmax / (levels / 2)), mn = fp16(-(levels / 2) s),
-// q = clamp(rint((v - mn) / s), 0, levels), q = 0 when s == 0: levels (q - levels/2) s.
-__device__ __forceinline__ GroupCode group_quant_signed(float v, float absmax, float levels) {
-  GroupCode g;
-  const float half = 0.5f * levels;
-  g.s = __float2half_rn(__fdiv_rn(absmax, half));
-  const float s = __half2float(g.s);
-  g.mn = __float2half_rn(__fmul_rn(-half, s));
-  const float mn = __half2float(g.mn);
-  int q = 0;
-  if (s > 0.f) {
-    float t = rint_quot(__fsub_rn(v, mn), s, rcp_approx(s));
-    t = fminf(fmaxf(t, 0.f), levels);
-    q = (int)t;
-  }
-  g.q = q;
-  return g;
-}
-
-__device__ __forceinline__ GroupCode group_quant_lane(float v, float levels) {
-  return group_quant_mm(v, warp_min(v), warp_max(v), levels);
+  return q;
 }
 
 // c[i] for a 4-entry table held in kernel parameters, without dynamic indexing.

@@ -255,6 +255,10 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
     // values: group e = coordinates 32e..32e+31, one per lane
     float vmn[E], vmx[E];
     group_minmax<E>(vv, vmn, vmx);
+    constexpr float vlevels = (float)((1 << VB) - 1);
+    __half2 vsm[E], vmine;
+    group_pairs<E, false>(vmn, vmx, vlevels, lane, vsm, vmine);
+    if (lane < E) *reinterpret_cast<__half2*>(tile + o_vsm + (slot * (D / 32) + lane) * 4) = vmine;
     // dimension-major code words: 2-bit: one word per dimension, token 2j+e at bits 16e+2j; 4-bit:
     // two words per dimension (all first words, then all second words), word w holding tokens
     // 8w+2j+e at bits 16e+4j.  Tokens of a page come from different warps: OR into the words.
@@ -262,13 +266,8 @@ __device__ void encode_main_block(const EncArgs& a, int b, int h, int tok0, int 
     const int vsh = VB == 2 ? 16 * (slot & 1) + 2 * (slot >> 1) : 16 * (slot & 1) + 4 * ((slot & 7) >> 1);
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      GroupCode g = group_quant_mm(vv[e], vmn[e], vmx[e], (float)((1 << VB) - 1));
-      if (g.q) atomicOr(vqw + coord_of(e, lane), (uint32_t)g.q << vsh);
-      if (lane == 0) {
-        __half* sm = reinterpret_cast<__half*>(tile + o_vsm + (slot * (D / 32) + e) * 4);
-        sm[0] = g.s;
-        sm[1] = g.mn;
-      }
+      const int q = group_code(vv[e], vsm[e], vlevels);
+      if (q) atomicOr(vqw + coord_of(e, lane), (uint32_t)q << vsh);
     }
   }
   __syncthreads();
@@ -424,20 +423,21 @@ __device__ void encode_alt_block_vb(const EncArgs& a, int b, int h, int tok0, in
       for (int e = 0; e < E; ++e) kh[coord_of(e, lane)] = __float2half_rn(kx[e]);
     } else {
       group_minmax<E>(kx, kmn, kmx);
+      const float klevels = (float)((1 << kb) - 1);
+      __half2 ksm[E], kmine;
+      if (a.key_signed)
+        group_pairs<E, true>(kmn, kmx, klevels, lane, ksm, kmine);
+      else
+        group_pairs<E, false>(kmn, kmx, klevels, lane, ksm, kmine);
+      if (lane < E) *reinterpret_cast<__half2*>(tile + o_ksm + (slot * (D / 32) + lane) * 4) = kmine;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int c = coord_of(e, lane);
-        GroupCode g = a.key_signed ? group_quant_signed(kx[e], fmaxf(-kmn[e], kmx[e]), (float)((1 << kb) - 1))
-                                   : group_quant_mm(kx[e], kmn[e], kmx[e], (float)((1 << kb) - 1));
+        const int q = group_code(kx[e], ksm[e], klevels);
         if (kb == 8)
-          tile[slot * D + c] = (uint8_t)g.q;
+          tile[slot * D + c] = (uint8_t)q;
         else
-          kcodes[tt * D + c] = (uint8_t)g.q;
-        if (lane == 0) {
-          __half* sm = reinterpret_cast<__half*>(tile + o_ksm + (slot * (D / 32) + e) * 4);
-          sm[0] = g.s;
-          sm[1] = g.mn;
-        }
+          kcodes[tt * D + c] = (uint8_t)q;
       }
     }
     float ss = 0.f;
