@@ -38,7 +38,7 @@ def _bench_max_ctx(lengths):
     return ((max(lengths) + 3 + 64 + 64 + 15) // 16) * 16
 
 
-def _run_main(seed, hq, hkv, lengths, oracle_seqs, shuffled=True, n_sample_pages=24):
+def _run_main(seed, hq, hkv, lengths, oracle_seqs, shuffled=True, n_sample_pages=24, paths=(None,)):
     d = 128
     bsz = len(lengths)
     ctx, c, s, sk = make_ctx(tq, True, d, hq, hkv, seed)
@@ -93,25 +93,32 @@ def _run_main(seed, hq, hkv, lengths, oracle_seqs, shuffled=True, n_sample_pages
     torch.cuda.synchronize()
     assert ctx.device_errors() == 0
     q = synth.queries(seed, bsz, hq, d)
-    out = torch.empty((bsz, hq, d), dtype=torch.float32, device="cuda")
-    ws = torch.empty(ctx.workspace_size(bsz, max_ctx), dtype=torch.uint8, device="cuda")
-    ctx.decode_attention(to_dev(q), pool, bt_d, to_dev(n_c), to_dev(ring_k), to_dev(ring_v), to_dev(n_b), max_ctx,
-                         out, ws)
-    got = out.cpu().numpy()
-    assert ctx.device_errors() == 0
-    assert np.all(np.isfinite(got))
+    refs = {}
     for b in oracle_seqs:
         p = oracle_pools.get(b, np.zeros((nblk, hkv, tile), np.uint8))
-        ref = attention.decode_main(q[b:b + 1], p, bt[b:b + 1], n_c[b:b + 1], ring_k[b:b + 1], ring_v[b:b + 1],
-                                    n_b[b:b + 1], s, c, sk, hkv)
-        ok, maxerr, nbad = allclose_report(got[b:b + 1], ref)
-        assert ok, f"sequence {b}: max abs err {maxerr}, {nbad} outside tolerance"
+        refs[b] = attention.decode_main(q[b:b + 1], p, bt[b:b + 1], n_c[b:b + 1], ring_k[b:b + 1], ring_v[b:b + 1],
+                                        n_b[b:b + 1], s, c, sk, hkv)
+    for path in paths:  # None: the default path; else a TQ_DECODE_* value
+        if path is not None:
+            ctx.set_decode_path(path)
+        out = torch.empty((bsz, hq, d), dtype=torch.float32, device="cuda")
+        ws = torch.empty(ctx.workspace_size(bsz, max_ctx), dtype=torch.uint8, device="cuda")
+        ctx.decode_attention(to_dev(q), pool, bt_d, to_dev(n_c), to_dev(ring_k), to_dev(ring_v), to_dev(n_b),
+                             max_ctx, out, ws)
+        got = out.cpu().numpy()
+        assert ctx.device_errors() == 0
+        assert np.all(np.isfinite(got))
+        for b in oracle_seqs:
+            ok, maxerr, nbad = allclose_report(got[b:b + 1], refs[b])
+            assert ok, f"path {path}, sequence {b}: max abs err {maxerr}, {nbad} outside tolerance"
     return checked_pages
 
 
 def test_qwen25_7b_b8_32k_shuffled_pages():
-    """Batch 8, 28 q / 4 KV heads, 32768 tokens each, shuffled 16-token pages."""
-    assert _run_main(0, 28, 4, [32768] * 8, oracle_seqs={0, 5}) > 0
+    """Batch 8, 28 q / 4 KV heads, 32768 tokens each, shuffled 16-token pages; the default decoder
+    and the tcgen05 score path on the same cache."""
+    assert _run_main(0, 28, 4, [32768] * 8, oracle_seqs={0, 5},
+                     paths=(None, tq.TQ_DECODE_TCGEN05)) > 0
 
 
 def test_qwen3_06b_32k_two_layers():
