@@ -144,21 +144,14 @@ __device__ __forceinline__ int group_code(float v, __half2 sm, float levels) {
   return q;
 }
 
-// c[i] for a 4-entry table held in kernel parameters, without dynamic indexing.
-__device__ __forceinline__ float sel4(const CodeTables& t, int i) {
-  float r = t.c[0];
-  r = i == 1 ? t.c[1] : r;
-  r = i == 2 ? t.c[2] : r;
-  r = i == 3 ? t.c[3] : r;
-  return r;
-}
-
-// c[i] of a codebook of up to 8 centroids without an indexed (local-memory) access.
-__device__ __forceinline__ float sel8(const CodeTables& t, int i) {
-  float r = t.c[0];
-#pragma unroll
-  for (int j = 1; j < 8; ++j) r = i == j ? t.c[j] : r;
-  return r;
+// c[idx] of a 2-, 4- or 8-entry codebook (kb - 1 = 1, 2 or 3 index bits) by a select tree on the
+// index bits i0 (high) .. i2, without an indexed (local-memory) access.
+__device__ __forceinline__ float sel_bits(const CodeTables& t, int kb, bool i0, bool i1, bool i2) {
+  if (kb == 2) return i0 ? t.c[1] : t.c[0];
+  if (kb == 3) return i0 ? (i1 ? t.c[3] : t.c[2]) : (i1 ? t.c[1] : t.c[0]);
+  const float lo = i1 ? (i2 ? t.c[3] : t.c[2]) : (i2 ? t.c[1] : t.c[0]);
+  const float hi = i1 ? (i2 ? t.c[7] : t.c[6]) : (i2 ? t.c[5] : t.c[4]);
+  return i0 ? hi : lo;
 }
 
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }

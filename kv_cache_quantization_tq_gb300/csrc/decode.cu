@@ -336,10 +336,9 @@ __global__ void __launch_bounds__(128) decode_main_kernel(DecArgs a) {
       for (int k = 0; k < D / 8; ++k) {
         const int dim = pp * (D / 8) + k;
         const int w = dim >> 5, bp = 16 * (dim & 1) + ((dim & 31) >> 1);
-        int idx = (int)((khr[w] >> bp) & 1);
-        if (kb >= 3) idx = (idx << 1) | (int)((klr[w] >> bp) & 1);
-        if (kb == 4) idx = (idx << 1) | (int)((k3r[w] >> bp) & 1);
-        const float cv = sel8(a.tab, idx);
+        const bool i0 = (khr[w] >> bp) & 1;
+        const bool i1 = kb >= 3 && ((klr[w] >> bp) & 1), i2 = kb == 4 && ((k3r[w] >> bp) & 1);
+        const float cv = sel_bits(a.tab, kb, i0, i1, i2);
         const float sv = ((ksr[w] >> bp) & 1) ? 1.f : -1.f;
 #pragma unroll
         for (int h = 0; h < NR; ++h) {

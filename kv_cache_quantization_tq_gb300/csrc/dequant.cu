@@ -226,10 +226,10 @@ __global__ void __launch_bounds__(256) dequant_main_kernel(DqArgs a) {
     float x[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      int idx = (int)((kh[e] >> bit) & 1u);
-      if (kb >= 3) idx = (idx << 1) | (int)((kl[e] >> bit) & 1u);
-      if (kb == 4) idx = (idx << 1) | (int)((k3[e] >> bit) & 1u);
-      x[e] = fmaf(a.qjl_coef * nr, corr[tt * C::CORR_STRIDE + coord_of(e, lane)], sel8(a.tab, idx));
+      // c[idx] by a select tree on the index bits as they come from the planes (high bit first)
+      const bool i0 = (kh[e] >> bit) & 1u;
+      const bool i1 = kb >= 3 && ((kl[e] >> bit) & 1u), i2 = kb == 4 && ((k3[e] >> bit) & 1u);
+      x[e] = fmaf(a.qjl_coef * nr, corr[tt * C::CORR_STRIDE + coord_of(e, lane)], sel_bits(a.tab, kb, i0, i1, i2));
     }
     wht_warp<E>(x, lane);
     const size_t row = (((size_t)b * a.hkv + h) * a.max_tokens + tok0 + tt) * D;
