@@ -50,7 +50,7 @@ constexpr int NVW = 8;                 // value warps
 constexpr int W_PROD = NSW, W_MMA = NSW + 1, W_VAL0 = NSW + 2;
 constexpr int NWARPS = W_VAL0 + NVW;
 constexpr int NTHREADS = 32 * NWARPS;
-constexpr int NW = NSW;                // warps of the ring item (the mma.sync path)
+constexpr int NW = NSW;                // warps of the query-record kernel (hy_prep_kernel)
 constexpr int TILE_PAGES = 8;          // pages per score tile: 128 tokens = M of the MMA
 static_assert(TILE_PAGES == NVW, "one value warp per page of a tile");
 constexpr int TILE_TOK = TILE_PAGES * kPage;
