@@ -123,3 +123,29 @@ def test_consecutive_calls_on_one_context(path):
                                     hkv)
         ok, maxerr, nbad = allclose_report(got, ref)
         assert ok, f"call {k} ({lengths}): max abs err {maxerr}, {nbad} bad"
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_repeated_decodes_are_bit_identical(path):
+    """Each decoder's arithmetic order is fixed (per-CTA combine order, lazy reference updates,
+    merge order), so the same inputs give the same bits on every call; a race between warp roles
+    or CTAs would show as a difference.  Twenty calls per shape, the first also against the
+    oracle."""
+    d = 128
+    for k, (hkv, n_rep, lengths) in enumerate([(2, 7, [5000, 130, 2049]), (4, 4, [777]), (1, 16, [3000, 1])]):
+        hq = hkv * n_rep
+        seed = 71 + k
+        ctx, c, s, sk = make_ctx(tq, True, d, hq, hkv, seed)
+        ctx.set_decode_path(path)
+        e = build_main_cache(seed, d, hkv, lengths, c, s, sk)
+        q = synth.queries(seed, len(lengths), hq, d)
+        first = _decode(ctx, e, q, hq, d)
+        assert ctx.device_errors() == 0
+        ref = attention.decode_main(q, e["pool"], e["bt"], e["n_c"], e["ring_k"], e["ring_v"], e["n_b"], s, c, sk,
+                                    hkv)
+        ok, maxerr, nbad = allclose_report(first, ref)
+        assert ok, f"shape {k}: max abs err {maxerr}, {nbad} bad"
+        for it in range(19):
+            again = _decode(ctx, e, q, hq, d)
+            assert np.array_equal(again, first), f"shape {k}, call {it + 2}: output differs from the first call"
+        assert ctx.device_errors() == 0
