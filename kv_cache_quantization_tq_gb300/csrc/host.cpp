@@ -366,6 +366,8 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx) {
   // SM (it holds all 512 tensor-memory columns) walks its chunk in tiles of 8 pages.  The chunks
   // per sequence and head group minimise waves x (tiles per chunk + 3), the 3 standing for the
   // pipeline's fill and drain; ring items (short, launched after every chunk) are not counted.
+  // TQ_DECODE_AUTO keeps the mma.sync kernels: on GB300 they measured faster (88 against 102 us per
+  // launch at batch 8 x 32K, 28 / 4 heads).
   const bool hy_ok = pl.tensor_core && ctx->cfg.key_bits == 3 && ctx->cfg.value_bits == 2 && ctx->cfg.qjl_m == d;
   pl.hybrid = hy_ok && ctx->decode_path == TQ_DECODE_TCGEN05;
   if (pl.hybrid) {
